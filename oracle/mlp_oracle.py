@@ -1,0 +1,241 @@
+"""Plain, slow, fp64 CPU oracle of one supervised MLP training step.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this module.  It shares no code with the CUDA path
+and must never be used as a fallback for it.
+
+What it computes, with the passage each step follows:
+
+* Linear layer y = x W^T + b, W stored [out, in] (MuNet, pypi "munet-nn",
+  section "Python training": `mu.nn.Linear(in, out)`; noeira.ai "Neural
+  networks", section "A complete example": `LinearReLU[784, 256]`).
+* Activation after every hidden Linear, none after the output Linear
+  (noeira "A complete example": two LinearReLU layers then a plain Linear).
+  ReLU is max(0, u); GELU is the tanh form 0.5 u (1 + tanh(sqrt(2/pi)(u +
+  0.044715 u^3))) (textbook definition, Hendrycks & Gimpel; the pages do not
+  define it).
+* Softmax cross-entropy with integer labels, mean over the batch (Orthon,
+  devpost "Orthon", sections "Core capabilities" and "Selected Orthon vs.
+  PyTorch results"; integer labels are the one-hot rows of noeira "A complete
+  example").
+* Backward as the composition of per-layer vector-Jacobian products, no tape
+  (noeira "The design in one page": "Forward and backward are explicit").
+* AdamW with decoupled weight decay and moments m, v kept per parameter,
+  zero before the first step (MuNet "What runs today": AdamW; noeira "The
+  design in one page": a Param is four tensors, moments allocated lazily).
+* Mixed precision: matmul inputs rounded to nearest (even), fp32-or-better
+  accumulation, fp32 master weights (MuNet "Configuration", precision="mixed";
+  Orthon "Core capabilities", Mixed precision).  Here the low-precision type
+  is bfloat16.
+
+Readings of points the pages leave open (each is also listed in the design doc):
+ReLU'(0) = 0 and the ReLU mask is taken from the stored activation h > 0;
+AdamW follows the Loshchilov-Hutter / PyTorch form (eps added to sqrt(v_hat)
+after bias correction, decay applied to the pre-step parameter, t starts at 1,
+decay on every parameter including biases); argmax returns the lowest index
+among equal maxima; a label outside [0, C) is an error.
+
+Precision modes
+  "fp64"      everything in float64 (used for the fp32 workloads, whose inputs
+              are fp32 values).
+  "bf16"      "exact" bf16 reading: only x and the bf16 weight copy
+              W16 = rne_bf16(P) are rounded; all else float64.
+  "bf16_mirror" rounds to bf16 at the points where a bf16 implementation
+              stores tensors: W16, hidden activations h (and GELU
+              pre-activations u), logits z, dz and every dY; bias, gradients,
+              master params and moments stay unrounded.  Accumulation is
+              float64 in between.
+
+All functions take and return float64 numpy arrays unless stated.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
+_SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
+_GELU_C = 0.044715
+
+
+# ---------------------------------------------------------------------------
+# bfloat16 round-to-nearest-even (definition: keep 8 significant bits; the
+# smallest quantum is 2^-133, bf16's subnormal spacing; ties go to the even
+# neighbour).  Mixed precision per MuNet "Configuration" (precision="mixed":
+# inputs rounded to nearest), with bfloat16 in place of fp16.
+# ---------------------------------------------------------------------------
+def rne_bf16(a: np.ndarray) -> np.ndarray:
+    a = np.asarray(a, dtype=np.float64)
+    out = np.zeros_like(a)
+    nz = (a != 0) & np.isfinite(a)
+    _, e = np.frexp(a[nz])                      # a = m 2^e, 0.5 <= |m| < 1
+    q = np.ldexp(1.0, np.maximum(e - 8, -133))  # value of one unit in the 8th bit
+    out[nz] = np.rint(a[nz] / q) * q            # rint: round half to even
+    out[~nz] = a[~nz]
+    bf16_max = (2.0 - 2.0 ** -7) * 2.0 ** 127
+    out[np.abs(out) > bf16_max] = np.copysign(np.inf, out[np.abs(out) > bf16_max])
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Activations and their derivatives.
+# ---------------------------------------------------------------------------
+def act_forward(u: np.ndarray, act: int) -> np.ndarray:
+    if act == ACT_NONE:
+        return u.copy()
+    if act == ACT_RELU:
+        return np.maximum(u, 0.0)
+    if act == ACT_GELU_TANH:
+        t = np.tanh(_SQRT_2_OVER_PI * (u + _GELU_C * u ** 3))
+        return 0.5 * u * (1.0 + t)
+    raise ValueError(f"unknown activation {act}")
+
+
+def gelu_tanh_grad(u: np.ndarray) -> np.ndarray:
+    """d/du of the tanh-form GELU (product and chain rule on the definition)."""
+    inner = _SQRT_2_OVER_PI * (u + _GELU_C * u ** 3)
+    t = np.tanh(inner)
+    dinner = _SQRT_2_OVER_PI * (1.0 + 3.0 * _GELU_C * u ** 2)
+    return 0.5 * (1.0 + t) + 0.5 * u * (1.0 - t * t) * dinner
+
+
+# ---------------------------------------------------------------------------
+# Steps of the path.
+# ---------------------------------------------------------------------------
+def linear(X: np.ndarray, W: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """u = X W^T + b  (W is [out, in])."""
+    return X @ W.T + b[None, :]
+
+
+def softmax_ce(z: np.ndarray, y: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-row loss l_i = logsumexp(z_i) - z_i[y_i] and dz = (softmax(z) -
+    onehot(y)) / B, the gradient of the batch-mean loss."""
+    B, C = z.shape
+    y = np.asarray(y)
+    if B and (y.min() < 0 or y.max() >= C):
+        raise ValueError("label out of range")
+    m = z.max(axis=1, keepdims=True)
+    e = np.exp(z - m)
+    s = e.sum(axis=1, keepdims=True)
+    rows = np.arange(B)
+    loss_rows = (m[:, 0] + np.log(s[:, 0])) - z[rows, y]
+    p = e / s
+    dz = p.copy()
+    dz[rows, y] -= 1.0
+    return loss_rows, dz / B
+
+
+def argmax_rows(z: np.ndarray) -> np.ndarray:
+    """Index of the row maximum, lowest index among equal maxima."""
+    return np.argmax(z, axis=1).astype(np.int32)   # numpy returns the first
+
+
+def adamw(p, g, m, v, t: int, lr, beta1, beta2, eps, wd):
+    """One AdamW update at step t (t >= 1); returns new (p, m, v).
+
+    m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+    p <- p - lr (m_hat / (sqrt(v_hat) + eps) + wd p),  m_hat = m/(1-b1^t),
+    v_hat = v/(1-b2^t), with p on the right the pre-step value."""
+    m = beta1 * m + (1.0 - beta1) * g
+    v = beta2 * v + (1.0 - beta2) * g * g
+    m_hat = m / (1.0 - beta1 ** t)
+    v_hat = v / (1.0 - beta2 ** t)
+    p = p - lr * (m_hat / (np.sqrt(v_hat) + eps) + wd * p)
+    return p, m, v
+
+
+# ---------------------------------------------------------------------------
+# Whole network.
+# ---------------------------------------------------------------------------
+def _round(a, on: bool):
+    return rne_bf16(a) if on else a
+
+
+def forward(params: Sequence[np.ndarray], x: np.ndarray, acts: Sequence[int],
+            mode: str = "fp64") -> Dict[str, list]:
+    """Forward pass.  params = [W1, b1, ..., WL, bL] (float64 master values).
+
+    Returns dict with the per-layer inputs X_l, pre-activations u_l (as stored:
+    rounded in mirror mode), and the logits z."""
+    L = len(params) // 2
+    lowp = mode in ("bf16", "bf16_mirror")
+    mirror = mode == "bf16_mirror"
+    X = _round(np.asarray(x, np.float64), lowp)
+    Xs, us, Ws = [], [], []
+    for l in range(L):
+        W = _round(params[2 * l], lowp)
+        b = params[2 * l + 1]
+        u = linear(X, W, b)
+        Xs.append(X)
+        Ws.append(W)
+        if l < L - 1:
+            act = acts[l]
+            h = _round(act_forward(u, act), mirror)
+            us.append(_round(u, mirror))
+            X = h
+        else:
+            us.append(_round(u, mirror))
+    return {"X": Xs, "u": us, "W": Ws, "z": us[-1]}
+
+
+def backward(fw: Dict[str, list], dz: np.ndarray, acts: Sequence[int],
+             mode: str = "fp64") -> List[np.ndarray]:
+    """Gradients [dW1, db1, ..., dWL, dbL] by composing the layer VJPs:
+    dW_l = dY_l^T X_l, db_l = sum_i dY_l[i], dY_{l-1} = (dY_l W_l) * act'."""
+    mirror = mode == "bf16_mirror"
+    L = len(fw["W"])
+    grads: List[Optional[np.ndarray]] = [None] * (2 * L)
+    dY = _round(dz, mirror)
+    for l in range(L - 1, -1, -1):
+        X = fw["X"][l]
+        grads[2 * l] = dY.T @ X
+        grads[2 * l + 1] = dY.sum(axis=0)
+        if l > 0:
+            dX = dY @ fw["W"][l]
+            act = acts[l - 1]
+            if act == ACT_RELU:
+                d = dX * (fw["X"][l] > 0)            # mask from the stored h
+            elif act == ACT_GELU_TANH:
+                d = dX * gelu_tanh_grad(fw["u"][l - 1])
+            else:
+                d = dX
+            dY = _round(d, mirror)
+    return grads
+
+
+def train_step(params: Sequence[np.ndarray], m: Sequence[np.ndarray],
+               v: Sequence[np.ndarray], t: int, x: np.ndarray, y: np.ndarray,
+               acts: Sequence[int], lr, beta1, beta2, eps, wd,
+               mode: str = "fp64"):
+    """One step: forward, CE loss (batch mean), backward, AdamW at step t.
+
+    Returns (loss, new_params, new_m, new_v, grads, extras)."""
+    fw = forward(params, x, acts, mode)
+    loss_rows, dz = softmax_ce(fw["z"], y)
+    loss = float(loss_rows.mean())
+    grads = backward(fw, dz, acts, mode)
+    newp, newm, newv = [], [], []
+    for p_, g_, m_, v_ in zip(params, grads, m, v):
+        a, b, c = adamw(p_, g_, m_, v_, t, lr, beta1, beta2, eps, wd)
+        newp.append(a)
+        newm.append(b)
+        newv.append(c)
+    return loss, newp, newm, newv, grads, {"fw": fw, "loss_rows": loss_rows, "dz": dz}
+
+
+def run_steps(params, acts, batches, hyper, mode="fp64", t0: int = 0):
+    """Run len(batches) consecutive steps from zero moments.  batches yields
+    (x, y) pairs.  hyper = (lr, beta1, beta2, eps, wd).  Returns (losses,
+    params, m, v, first_step_grads)."""
+    p = [np.asarray(a, np.float64) for a in params]
+    m = [np.zeros_like(a) for a in p]
+    v = [np.zeros_like(a) for a in p]
+    losses, g1 = [], None
+    for i, (x, y) in enumerate(batches):
+        loss, p, m, v, g, _ = train_step(p, m, v, t0 + i + 1, x, y, acts, *hyper, mode=mode)
+        losses.append(loss)
+        if g1 is None:
+            g1 = g
+    return losses, p, m, v, g1
