@@ -1,0 +1,147 @@
+/*
+ * mlp.h -- C ABI of a GB300-native training step for a fused-activation MLP.
+ *
+ * The step (one supervised update of an L-layer perceptron) is:
+ *   forward   u_l = X_l W_l^T + b_l, h_l = act(u_l) for hidden layers, logits
+ *             z = h_{L-1} W_L^T + b_L (Linear layers as in pypi "munet-nn",
+ *             "Python training"; the MatMul+Bias+Activation fusion of
+ *             noeira.ai "Neural networks", "The design in one page");
+ *   loss      mean over the batch of softmax cross-entropy with integer
+ *             labels (devpost "Orthon", "Core capabilities" and "Selected
+ *             Orthon vs. PyTorch results");
+ *   backward  explicit vector-Jacobian products (noeira "The design in one
+ *             page": forward and vjp per module, no tape): dW_l = dY_l^T X_l,
+ *             db_l = column sums of dY_l, dY_{l-1} = (dY_l W_l) * act';
+ *   update    AdamW with moments stored beside each parameter (noeira "The
+ *             design in one page": a Param is four tensors; MuNet "What runs
+ *             today": AdamW), decoupled decay, bias-corrected moments.
+ * The whole step is recorded once as a CUDA graph and replayed (noeira "What
+ * is in it": optional CUDA-graph capture; MuNet "What runs today": recorded
+ * command-buffer replay).
+ *
+ * Conventions
+ *   - All device pointers are plain CUDA device addresses on the model's
+ *     device; host pointers are ordinary process memory.  `stream` is a
+ *     cudaStream_t (NULL = the legacy default stream).
+ *   - Tensors are dense row-major.  x is [batch, dims[0]] in the model dtype
+ *     (float for MLP_F32, bfloat16 bits for MLP_BF16); labels are int32
+ *     [batch]; logits are [batch, C] in the model dtype.
+ *   - Parameters use a flat order: for l = 1..L, W_l [dims[l], dims[l-1]]
+ *     row-major then b_l [dims[l]].  mlp_read_params / mlp_write_params move
+ *     them densely packed in that order.
+ *   - Memory: the caller allocates ONE device buffer of mlp_arena_bytes()
+ *     bytes (e.g. with torch) and hands it to mlp_create; the library lays
+ *     out parameters, gradients, moments, the bf16 weight copy, activations,
+ *     workspace and a control block inside it and allocates no device memory
+ *     of its own.  The arena must outlive the model.
+ *   - One batch size per model (fixed at create; MuNet "Python training":
+ *     one specialization per compiled object).  Calls on one model are
+ *     serialised by a mutex; at most one step is in flight per model.
+ *   - Errors: argument / shape errors return before anything is enqueued;
+ *     CUDA errors return MLP_ERR_CUDA; conditions found on the device (a
+ *     label outside [0, C), a non-finite loss, a device wait that gave up)
+ *     are latched in the control block and returned by the next
+ *     mlp_check_errors.  mlp_last_error() gives a message for the calling
+ *     thread.  There is no CPU fallback: without a usable GPU every compute
+ *     call fails.
+ */
+#ifndef MLP_H_
+#define MLP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mlp mlp_t;
+
+typedef enum {
+  MLP_OK = 0,
+  MLP_ERR_ARG = 1,          /* bad argument (null pointer, bad enum, ...) */
+  MLP_ERR_SHAPE = 2,        /* unsupported or mismatched shape */
+  MLP_ERR_DTYPE = 3,        /* unsupported dtype */
+  MLP_ERR_CUDA = 4,         /* a CUDA call failed */
+  MLP_ERR_LABEL_RANGE = 5,  /* device: a label outside [0, C) */
+  MLP_ERR_NONFINITE = 6,    /* device: non-finite batch loss */
+  MLP_ERR_STATE = 7,        /* call not valid in the model's state */
+  MLP_ERR_TIMEOUT = 8       /* device: a bounded wait inside a kernel gave up */
+} mlp_status;
+
+enum { MLP_ACT_NONE = 0, MLP_ACT_RELU = 1, MLP_ACT_GELU_TANH = 2 };
+/* MLP_F32: fp32 everywhere, FFMA GEMMs (no TF32).
+ * MLP_BF16: bf16 x / weights copy / activations / logits / gradients of
+ * activations, fp32 accumulation, fp32 bias, fp32 master weights, gradients
+ * and Adam moments (MuNet "Configuration", precision="mixed"; Orthon
+ * "Core capabilities", FP32 master weights). */
+enum { MLP_F32 = 0, MLP_BF16 = 1 };
+/* Parameter planes, all indexed by the same flat parameter order. */
+enum { MLP_PLANE_P = 0, MLP_PLANE_G = 1, MLP_PLANE_M = 2, MLP_PLANE_V = 3 };
+
+/* Bytes of device memory a model with this shape needs.  dims has n_dims
+ * entries [in, h1, ..., C] (n_dims >= 2); acts has n_dims-2 entries (one per
+ * hidden layer) or is NULL to use `act` on every hidden layer.  Returns 0 on
+ * an invalid shape (see mlp_last_error). */
+size_t mlp_arena_bytes(const int64_t* dims, int n_dims, const int* acts, int act, int dtype, int64_t batch);
+
+/* Create a model in the caller's arena on `device`.  Weights are drawn
+ * Kaiming-normal (std = sqrt(2 / fan_in), noeira "A complete example":
+ * make[Kaiming]) from a host generator seeded by `seed`; biases, gradients
+ * and moments are zero; the step counter is 0.  For MLP_BF16 every input and
+ * hidden width must be a multiple of 8 (16-byte rows for TMA).  On success
+ * *out owns no memory except host bookkeeping. */
+mlp_status mlp_create(const int64_t* dims, int n_dims, const int* acts, int act, int dtype, uint64_t seed,
+                      int64_t batch, void* arena_dev, size_t arena_bytes, int device, mlp_t** out);
+
+/* Forward only: logits_dev ([batch, C], model dtype; nullable) and
+ * argmax_dev (int32 [batch], lowest index among equal maxima; nullable). */
+mlp_status mlp_forward(mlp_t* model, const void* x_dev, void* logits_dev, int32_t* argmax_dev, void* stream);
+
+/* One training step on (x_dev, labels_dev): forward, softmax-CE, backward,
+ * AdamW(lr, beta1, beta2, eps, wd) at step t = (step counter + 1).  The
+ * batch-mean loss is written to loss_dev (device float; nullable).  Nothing
+ * is read back; the call returns once the work is enqueued on `stream`. */
+mlp_status mlp_train_step(mlp_t* model, const void* x_dev, const int32_t* labels_dev, float lr, float beta1,
+                          float beta2, float eps, float wd, float* loss_dev, void* stream);
+
+/* n_steps consecutive training steps enqueued as ONE CUDA-graph launch;
+ * step i reads x_devs[i] / label_devs[i] (host arrays of device pointers)
+ * and writes its loss to losses_dev[i] (nullable).  The graph is built on
+ * the first call for a given n_steps and re-pointed on later calls. */
+mlp_status mlp_train_steps(mlp_t* model, int n_steps, const void* const* x_devs, const int32_t* const* label_devs,
+                           float lr, float beta1, float beta2, float eps, float wd, float* losses_dev,
+                           void* stream);
+
+/* Use a CUDA graph for mlp_train_step / mlp_train_steps (1, the default) or
+ * launch the kernels one by one (0). */
+mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
+
+/* Number of parameters (flat, densely packed) and of Linear layers. */
+int64_t mlp_num_params(const mlp_t* model);
+int mlp_num_layers(const mlp_t* model);
+
+/* Synchronous copies of a parameter plane to / from host memory (n must be
+ * mlp_num_params).  read also returns the step counter (nullable);
+ * write sets it.  Writing plane P of an MLP_BF16 model refreshes the bf16
+ * weight copy.  Both synchronise the model's device. */
+mlp_status mlp_read_params(mlp_t* model, int plane, float* host_out, size_t n, int64_t* step_out);
+mlp_status mlp_write_params(mlp_t* model, int plane, const float* host_in, size_t n, int64_t step);
+
+/* Synchronise `stream`, read and clear the device error word, and return
+ * the first latched condition (MLP_OK if none). */
+mlp_status mlp_check_errors(mlp_t* model, void* stream);
+
+/* Number of kernels one training step launches (graph nodes per step). */
+int mlp_kernels_per_step(const mlp_t* model);
+
+/* Message for the last failed call on this thread ("" if none). */
+const char* mlp_last_error(void);
+
+/* Destroy the model (the arena is the caller's and is not freed). */
+void mlp_destroy(mlp_t* model);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLP_H_ */

@@ -1,0 +1,87 @@
+/*
+ * mlp_ops.h -- the individual operations of the MLP training step, callable
+ * on caller-owned device buffers.  They run the same kernels mlp_train_step
+ * runs; they exist so that each step of the path can be checked and timed on
+ * its own at full size.
+ *
+ * Common conventions: device pointers on the current CUDA device; dense
+ * row-major layouts with explicit leading dimensions (`ld*`, in elements);
+ * dtype MLP_F32 (float) or MLP_BF16 (bfloat16 bits); `stream` is a
+ * cudaStream_t.  Every call validates its arguments and returns before
+ * enqueuing anything when they are invalid; it returns once its kernels are
+ * enqueued.  Device-side conditions (label range, wait timeouts) are OR-ed
+ * into `err_dev` (a device uint32, nullable) with the bits
+ *   1 = label outside [0, C), 2 = non-finite loss, 4 = bounded wait gave up.
+ * For MLP_BF16 the GEMM operands are read by TMA: every operand base must be
+ * 16-byte aligned and every leading dimension a multiple of 8 elements.
+ */
+#ifndef MLP_OPS_H_
+#define MLP_OPS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "mlp.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* LinearAct forward (noeira.ai "Neural networks", "The design in one page":
+ * MatMul+Bias+Activation as one kernel, bias and activation in the GEMM
+ * epilogue):  u = X W^T + b,  H = act(u),  U = u (optional, nullable).
+ *   X [M, K] (ldx), W [N, K] (ldw), b fp32 [N], H [M, N] (ldh), U [M, N] (ldu).
+ * Accumulation is fp32; H and U are rounded to the dtype. */
+mlp_status mlp_op_linear_act(int dtype, int act, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx,
+                             const void* W, int64_t ldw, const float* b, void* H, int64_t ldh, void* U, int64_t ldu,
+                             uint32_t* err_dev, void* stream);
+
+/* dgrad with the activation VJP fused (noeira "The design in one page":
+ * vjp per module):  dX = (dY W) * act'(S)
+ *   dY [M, N] (ldy), W [N, K] (ldw), S [M, K] (lds) = what the forward of the
+ *   layer below stored: h for ReLU (mask h > 0), u for GELU, unused for
+ *   MLP_ACT_NONE (nullable); dX [M, K] (ldx). */
+mlp_status mlp_op_dgrad(int dtype, int act, int64_t M, int64_t N, int64_t K, const void* dY, int64_t ldy,
+                        const void* W, int64_t ldw, const void* S, int64_t lds, void* dX, int64_t ldx,
+                        uint32_t* err_dev, void* stream);
+
+/* Workspace bytes mlp_op_wgrad needs for this shape (0 if none). */
+size_t mlp_op_wgrad_workspace_bytes(int dtype, int64_t N, int64_t K, int64_t B);
+
+/* wgrad with the bias gradient fused:  dW = dY^T X (fp32 [N, K], lddw),
+ * db = sum over rows of dY (fp32 [N], nullable).
+ *   dY [B, N] (ldy), X [B, K] (ldx).  The reduction over B may be split;
+ *   partial sums go to `workspace` (device, ws_bytes >= the size above) and
+ *   are added in a fixed order, so results are deterministic. */
+mlp_status mlp_op_wgrad(int dtype, int64_t N, int64_t K, int64_t B, const void* dY, int64_t ldy, const void* X,
+                        int64_t ldx, float* dW, int64_t lddw, float* db, void* workspace, size_t ws_bytes,
+                        uint32_t* err_dev, void* stream);
+
+/* Softmax cross-entropy, forward and backward in one pass over each row
+ * (devpost "Orthon", "Selected Orthon vs. PyTorch results": one kernel reads
+ * the logits once):  loss_rows[i] = logsumexp(z_i) - z_i[y_i] (fp32),
+ * dz_i = (softmax(z_i) - onehot(y_i)) * grad_scale (dtype; grad_scale = 1/B
+ * gives the gradient of the batch-mean loss).
+ *   z [B, C] (ldz), labels int32 [B], dz [B, C] (lddz). */
+mlp_status mlp_op_softmax_ce(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, const int32_t* labels,
+                             float grad_scale, void* dz, int64_t lddz, float* loss_rows, uint32_t* err_dev,
+                             void* stream);
+
+/* loss = mean(loss_rows[0..B)) summed in a fixed order (device float). */
+mlp_status mlp_op_loss_mean(int64_t B, const float* loss_rows, float* loss, uint32_t* err_dev, void* stream);
+
+/* AdamW at step t >= 1 over flat fp32 planes p, g, m, v of n elements
+ * (MuNet "What runs today": AdamW; noeira "The design in one page": moments
+ * co-located per parameter):  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ * p = p - lr (m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps) + wd p).  w16 (nullable)
+ * receives bf16(p) after the update.  Planes 16-byte aligned, w16 8-byte. */
+mlp_status mlp_op_adamw(int64_t n, float* p, const float* g, float* m, float* v, void* w16, int64_t t, float lr,
+                        float beta1, float beta2, float eps, float wd, void* stream);
+
+/* Row argmax of z [B, C] (ldz) into int32 out [B]; lowest index on ties. */
+mlp_status mlp_op_argmax(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, int32_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLP_OPS_H_ */

@@ -1,0 +1,291 @@
+"""Python binding of the GB300 MLP training-step library (libmlpstep.so).
+
+The functions below carry the C ABI's names (include/mlp.h, include/mlp_ops.h)
+and only marshal arguments: pointers are passed as integers (device addresses
+from torch tensors' data_ptr()), streams as cudaStream_t integers.  Every
+step of the path runs in the library's CUDA kernels; there is no CPU path.
+`Model` is a small convenience wrapper that lets torch allocate the arena.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmlpstep.so")
+
+MLP_OK = 0
+STATUS_NAMES = {0: "MLP_OK", 1: "MLP_ERR_ARG", 2: "MLP_ERR_SHAPE", 3: "MLP_ERR_DTYPE", 4: "MLP_ERR_CUDA",
+                5: "MLP_ERR_LABEL_RANGE", 6: "MLP_ERR_NONFINITE", 7: "MLP_ERR_STATE", 8: "MLP_ERR_TIMEOUT"}
+ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
+F32, BF16 = 0, 1
+PLANE_P, PLANE_G, PLANE_M, PLANE_V = 0, 1, 2, 3
+
+
+class MlpError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+_c = ctypes
+_P, _I64, _I32, _F, _SZ = _c.c_void_p, _c.c_int64, _c.c_int, _c.c_float, _c.c_size_t
+
+_SIGS = {
+    "mlp_arena_bytes": (_SZ, [_c.POINTER(_I64), _I32, _c.POINTER(_I32), _I32, _I32, _I64]),
+    "mlp_create": (_I32, [_c.POINTER(_I64), _I32, _c.POINTER(_I32), _I32, _I32, _c.c_uint64, _I64, _P, _SZ, _I32,
+                          _c.POINTER(_P)]),
+    "mlp_forward": (_I32, [_P, _P, _P, _P, _P]),
+    "mlp_train_step": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P]),
+    "mlp_train_steps": (_I32, [_P, _I32, _c.POINTER(_P), _c.POINTER(_P), _F, _F, _F, _F, _F, _P, _P]),
+    "mlp_set_graph_mode": (_I32, [_P, _I32]),
+    "mlp_num_params": (_I64, [_P]),
+    "mlp_num_layers": (_I32, [_P]),
+    "mlp_read_params": (_I32, [_P, _I32, _P, _SZ, _c.POINTER(_I64)]),
+    "mlp_write_params": (_I32, [_P, _I32, _P, _SZ, _I64]),
+    "mlp_check_errors": (_I32, [_P, _P]),
+    "mlp_kernels_per_step": (_I32, [_P]),
+    "mlp_last_error": (_c.c_char_p, []),
+    "mlp_destroy": (None, [_P]),
+    "mlp_op_linear_act": (_I32, [_I32, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _P, _P]),
+    "mlp_op_dgrad": (_I32, [_I32, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P]),
+    "mlp_op_wgrad_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64]),
+    "mlp_op_wgrad": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
+    "mlp_op_softmax_ce": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _F, _P, _I64, _P, _P, _P]),
+    "mlp_op_loss_mean": (_I32, [_I64, _P, _P, _P, _P]),
+    "mlp_op_adamw": (_I32, [_I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _P]),
+    "mlp_op_argmax": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _P]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmlpstep.so (built by neural_net_step_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with neural_net_step_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def mlp_last_error() -> str:
+    return (lib().mlp_last_error() or b"").decode()
+
+
+def _check(st: int) -> None:
+    if st != MLP_OK:
+        raise MlpError(st, mlp_last_error())
+
+
+def _i64arr(v: Sequence[int]):
+    return (_I64 * len(v))(*v)
+
+
+def _i32arr(v: Optional[Sequence[int]]):
+    return None if v is None else (_I32 * len(v))(*v)
+
+
+# ---- model ---------------------------------------------------------------
+def mlp_arena_bytes(dims, acts, act, dtype, batch) -> int:
+    n = lib().mlp_arena_bytes(_i64arr(dims), len(dims), _i32arr(acts), act, dtype, batch)
+    if n == 0:
+        raise MlpError(1, mlp_last_error())
+    return n
+
+
+def mlp_create(dims, acts, act, dtype, seed, batch, arena_ptr, arena_bytes, device) -> int:
+    h = _P()
+    _check(lib().mlp_create(_i64arr(dims), len(dims), _i32arr(acts), act, dtype, seed, batch, arena_ptr,
+                            arena_bytes, device, ctypes.byref(h)))
+    return h.value
+
+
+def mlp_forward(h, x_ptr, logits_ptr, argmax_ptr, stream) -> None:
+    _check(lib().mlp_forward(h, x_ptr, logits_ptr, argmax_ptr, stream))
+
+
+def mlp_train_step(h, x_ptr, labels_ptr, lr, beta1, beta2, eps, wd, loss_ptr, stream) -> None:
+    _check(lib().mlp_train_step(h, x_ptr, labels_ptr, lr, beta1, beta2, eps, wd, loss_ptr, stream))
+
+
+def mlp_train_steps(h, x_ptrs, label_ptrs, lr, beta1, beta2, eps, wd, losses_ptr, stream) -> None:
+    n = len(x_ptrs)
+    xs = (_P * n)(*x_ptrs)
+    ys = (_P * n)(*label_ptrs)
+    _check(lib().mlp_train_steps(h, n, xs, ys, lr, beta1, beta2, eps, wd, losses_ptr, stream))
+
+
+def mlp_set_graph_mode(h, enable: bool) -> None:
+    _check(lib().mlp_set_graph_mode(h, int(bool(enable))))
+
+
+def mlp_num_params(h) -> int:
+    return lib().mlp_num_params(h)
+
+
+def mlp_num_layers(h) -> int:
+    return lib().mlp_num_layers(h)
+
+
+def mlp_kernels_per_step(h) -> int:
+    return lib().mlp_kernels_per_step(h)
+
+
+def mlp_read_params(h, plane, host_ptr, n) -> int:
+    step = _I64(0)
+    _check(lib().mlp_read_params(h, plane, host_ptr, n, ctypes.byref(step)))
+    return step.value
+
+
+def mlp_write_params(h, plane, host_ptr, n, step) -> None:
+    _check(lib().mlp_write_params(h, plane, host_ptr, n, step))
+
+
+def mlp_check_errors(h, stream) -> None:
+    _check(lib().mlp_check_errors(h, stream))
+
+
+def mlp_destroy(h) -> None:
+    lib().mlp_destroy(h)
+
+
+# ---- individual operations -------------------------------------------------
+def mlp_op_linear_act(dtype, act, M, N, K, X, ldx, W, ldw, b, H, ldh, U, ldu, err, stream) -> None:
+    _check(lib().mlp_op_linear_act(dtype, act, M, N, K, X, ldx, W, ldw, b, H, ldh, U, ldu, err, stream))
+
+
+def mlp_op_dgrad(dtype, act, M, N, K, dY, ldy, W, ldw, S, lds, dX, ldx, err, stream) -> None:
+    _check(lib().mlp_op_dgrad(dtype, act, M, N, K, dY, ldy, W, ldw, S, lds, dX, ldx, err, stream))
+
+
+def mlp_op_wgrad_workspace_bytes(dtype, N, K, B) -> int:
+    return lib().mlp_op_wgrad_workspace_bytes(dtype, N, K, B)
+
+
+def mlp_op_wgrad(dtype, N, K, B, dY, ldy, X, ldx, dW, lddw, db, ws, ws_bytes, err, stream) -> None:
+    _check(lib().mlp_op_wgrad(dtype, N, K, B, dY, ldy, X, ldx, dW, lddw, db, ws, ws_bytes, err, stream))
+
+
+def mlp_op_softmax_ce(dtype, B, C, z, ldz, labels, grad_scale, dz, lddz, loss_rows, err, stream) -> None:
+    _check(lib().mlp_op_softmax_ce(dtype, B, C, z, ldz, labels, grad_scale, dz, lddz, loss_rows, err, stream))
+
+
+def mlp_op_loss_mean(B, loss_rows, loss, err, stream) -> None:
+    _check(lib().mlp_op_loss_mean(B, loss_rows, loss, err, stream))
+
+
+def mlp_op_adamw(n, p, g, m, v, w16, t, lr, beta1, beta2, eps, wd, stream) -> None:
+    _check(lib().mlp_op_adamw(n, p, g, m, v, w16, t, lr, beta1, beta2, eps, wd, stream))
+
+
+def mlp_op_argmax(dtype, B, C, z, ldz, out, stream) -> None:
+    _check(lib().mlp_op_argmax(dtype, B, C, z, ldz, out, stream))
+
+
+# ---- convenience wrapper ---------------------------------------------------
+class Model:
+    """An MLP whose arena is a torch uint8 CUDA tensor.  Inputs are torch CUDA
+    tensors (x in the model dtype, labels int32); outputs are torch tensors."""
+
+    def __init__(self, dims: Sequence[int], acts: Optional[Sequence[int]] = None, act: int = ACT_RELU,
+                 dtype: int = F32, seed: int = 0, batch: int = 1, device: int = 0):
+        import torch
+        self.torch = torch
+        self.dims = list(dims)
+        self.acts = None if acts is None else list(acts)
+        self.dtype = dtype
+        self.batch = batch
+        self.device = device
+        nbytes = mlp_arena_bytes(self.dims, self.acts, act, dtype, batch)
+        self.arena = torch.empty(nbytes, dtype=torch.uint8, device=f"cuda:{device}")
+        self.h = mlp_create(self.dims, self.acts, act, dtype, seed, batch, self.arena.data_ptr(), nbytes, device)
+        self.n_params = mlp_num_params(self.h)
+
+    @property
+    def tdtype(self):
+        return self.torch.float32 if self.dtype == F32 else self.torch.bfloat16
+
+    def stream(self) -> int:
+        return self.torch.cuda.current_stream(self.device).cuda_stream
+
+    def set_graph_mode(self, enable: bool) -> None:
+        mlp_set_graph_mode(self.h, enable)
+
+    def _check_x(self, x, labels=None):
+        t = self.torch
+        assert x.is_cuda and x.dtype == self.tdtype and x.is_contiguous() and tuple(x.shape) == (self.batch, self.dims[0])
+        if labels is not None:
+            assert labels.is_cuda and labels.dtype == t.int32 and labels.is_contiguous() and labels.numel() == self.batch
+
+    def train_step(self, x, labels, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0, loss=None):
+        self._check_x(x, labels)
+        if loss is None:
+            loss = self.torch.empty((), dtype=self.torch.float32, device=x.device)
+        mlp_train_step(self.h, x.data_ptr(), labels.data_ptr(), lr, beta1, beta2, eps, wd, loss.data_ptr(),
+                       self.stream())
+        return loss
+
+    def train_steps(self, xs, ys, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0, losses=None):
+        for x, y in zip(xs, ys):
+            self._check_x(x, y)
+        if losses is None:
+            losses = self.torch.empty(len(xs), dtype=self.torch.float32, device=xs[0].device)
+        mlp_train_steps(self.h, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys], lr, beta1, beta2, eps, wd,
+                        losses.data_ptr(), self.stream())
+        return losses
+
+    def forward(self, x, want_logits=True, want_argmax=True):
+        self._check_x(x)
+        t = self.torch
+        logits = t.empty((self.batch, self.dims[-1]), dtype=self.tdtype, device=x.device) if want_logits else None
+        am = t.empty(self.batch, dtype=t.int32, device=x.device) if want_argmax else None
+        mlp_forward(self.h, x.data_ptr(), logits.data_ptr() if logits is not None else None,
+                    am.data_ptr() if am is not None else None, self.stream())
+        return logits, am
+
+    def read_flat(self, plane: int = PLANE_P):
+        import numpy as np
+        out = np.empty(self.n_params, dtype=np.float32)
+        step = mlp_read_params(self.h, plane, out.ctypes.data, self.n_params)
+        return out, step
+
+    def write_flat(self, flat, plane: int = PLANE_P, step: int = 0) -> None:
+        import numpy as np
+        a = np.ascontiguousarray(flat, dtype=np.float32)
+        assert a.size == self.n_params
+        mlp_write_params(self.h, plane, a.ctypes.data, self.n_params, step)
+
+    def split(self, flat) -> List:
+        """Cut a flat parameter vector into [W1, b1, ..., WL, bL] (views)."""
+        out, pos = [], 0
+        for l in range(len(self.dims) - 1):
+            n, k = self.dims[l + 1], self.dims[l]
+            out.append(flat[pos:pos + n * k].reshape(n, k))
+            pos += n * k
+            out.append(flat[pos:pos + n])
+            pos += n
+        return out
+
+    def check_errors(self) -> None:
+        mlp_check_errors(self.h, self.stream())
+
+    def kernels_per_step(self) -> int:
+        return mlp_kernels_per_step(self.h)
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            mlp_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,69 @@
+// Device-side helpers shared by the kernels of the MLP training step.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace mlpk {
+
+enum Act : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU_TANH = 2 };
+enum DType : int { DT_F32 = 0, DT_BF16 = 1 };
+
+// Device error word bits (latched in the model's control block).
+enum : uint32_t {
+  ERRBIT_LABEL_RANGE = 1u << 0,   // a label outside [0, C)
+  ERRBIT_NONFINITE = 1u << 1,     // non-finite batch loss
+  ERRBIT_TIMEOUT = 1u << 2,       // a bounded device-side wait gave up
+  ERRBIT_BAD_LAUNCH = 1u << 3,    // a kernel saw parameters it cannot handle
+};
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// tanh-form GELU and its derivative (Hendrycks & Gimpel); tanhf from CUDA.
+__device__ __forceinline__ float gelu_tanh(float u) {
+  const float k0 = 0.7978845608028654f;   // sqrt(2/pi)
+  const float k1 = 0.044715f;
+  float t = tanhf(k0 * (u + k1 * u * u * u));
+  return 0.5f * u * (1.0f + t);
+}
+__device__ __forceinline__ float gelu_tanh_grad(float u) {
+  const float k0 = 0.7978845608028654f;
+  const float k1 = 0.044715f;
+  float t = tanhf(k0 * (u + k1 * u * u * u));
+  float dinner = k0 * (1.0f + 3.0f * k1 * u * u);
+  return 0.5f * (1.0f + t) + 0.5f * u * (1.0f - t * t) * dinner;
+}
+__device__ __forceinline__ float apply_act(float v, int act) {
+  if (act == ACT_RELU) return fmaxf(v, 0.0f);
+  if (act == ACT_GELU_TANH) return gelu_tanh(v);
+  return v;
+}
+// Derivative factor of the activation, from what the forward stored:
+// ReLU: stored h (mask h > 0); GELU: stored pre-activation u.
+__device__ __forceinline__ float act_grad_from_stored(float s, int act) {
+  if (act == ACT_RELU) return s > 0.0f ? 1.0f : 0.0f;
+  if (act == ACT_GELU_TANH) return gelu_tanh_grad(s);
+  return 1.0f;
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace mlpk

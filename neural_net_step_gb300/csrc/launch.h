@@ -1,0 +1,54 @@
+// A kernel launch described as data, so that the same step can be launched
+// eagerly on a stream or recorded as nodes of an explicitly built CUDA graph
+// (and re-pointed later by updating a node's arguments).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+namespace mlpk {
+
+constexpr unsigned kMaxArgBytes = 1024;
+
+struct LaunchRec {
+  const void* func = nullptr;
+  dim3 grid{1, 1, 1};
+  dim3 block{1, 1, 1};
+  unsigned smem = 0;
+  unsigned args_size = 0;
+  const char* name = "";
+  alignas(128) unsigned char args[kMaxArgBytes];
+
+  template <typename P>
+  void set_args(const P& p) {
+    static_assert(sizeof(P) <= kMaxArgBytes, "kernel parameter block too large");
+    static_assert(alignof(P) <= 128, "over-aligned kernel parameter block");
+    memcpy(args, &p, sizeof(P));
+    args_size = sizeof(P);
+  }
+  bool same_as(const LaunchRec& o) const {
+    return func == o.func && grid.x == o.grid.x && grid.y == o.grid.y && grid.z == o.grid.z &&
+           block.x == o.block.x && block.y == o.block.y && block.z == o.block.z &&
+           smem == o.smem && args_size == o.args_size && memcmp(args, o.args, args_size) == 0;
+  }
+};
+
+inline cudaError_t launch_rec(const LaunchRec& r, cudaStream_t s) {
+  void* argp[1] = {const_cast<unsigned char*>(r.args)};
+  return cudaLaunchKernel(r.func, r.grid, r.block, argp, r.smem, s);
+}
+
+inline cudaKernelNodeParams node_params(const LaunchRec& r, void** argp) {
+  cudaKernelNodeParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.func = const_cast<void*>(r.func);
+  kp.gridDim = r.grid;
+  kp.blockDim = r.block;
+  kp.sharedMemBytes = r.smem;
+  argp[0] = const_cast<unsigned char*>(r.args);
+  kp.kernelParams = argp;
+  kp.extra = nullptr;
+  return kp;
+}
+
+}  // namespace mlpk

@@ -1,0 +1,759 @@
+// Step runtime behind the C ABI: arena layout, parameter initialisation,
+// the per-step launch plan, CUDA-graph construction/replay, and the
+// op-level entry points.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "mlp.h"
+#include "mlp_ops.h"
+#include "ops.h"
+
+using namespace mlpk;
+
+// ---------------------------------------------------------------------------
+// Errors.
+// ---------------------------------------------------------------------------
+static thread_local char g_err[1024] = "";
+
+static mlp_status fail(mlp_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+static mlp_status fail(mlp_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+static mlp_status ok() {
+  g_err[0] = 0;
+  return MLP_OK;
+}
+#define CUDA_TRY(expr)                                                                       \
+  do {                                                                                       \
+    cudaError_t e_ = (expr);                                                                 \
+    if (e_ != cudaSuccess) return fail(MLP_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+struct DevGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DevGuard(int d) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != d) changed = cudaSetDevice(d) == cudaSuccess;
+  }
+  ~DevGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Arena layout.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  int L = 0;
+  int dtype = 0;
+  int64_t B = 0;
+  std::vector<int64_t> dims;
+  std::vector<int> acts;          // per hidden layer
+  int64_t n_params = 0;           // dense count
+  int64_t plane_n = 0;            // elements per plane (padded)
+  std::vector<int64_t> woff, boff;
+  size_t off_P = 0, off_G = 0, off_M = 0, off_V = 0, off_W16 = 0;
+  std::vector<size_t> off_h, off_u;
+  std::vector<int64_t> ld_h;
+  size_t off_z = 0, off_dz = 0;
+  int64_t ldz = 0;
+  size_t off_dy[2] = {0, 0};
+  size_t off_loss_rows = 0, off_ws = 0, ws_bytes = 0, off_ctl = 0;
+  size_t total = 0;
+};
+
+struct Ctl {   // control block at off_ctl
+  int64_t step;
+  uint32_t err;
+  uint32_t pad;
+  float loss_slot;
+};
+
+mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act, int dtype, int64_t batch,
+                       Layout* Lo) {
+  if (!dims || n_dims < 2) return fail(MLP_ERR_ARG, "need at least 2 dims");
+  if (dtype != MLP_F32 && dtype != MLP_BF16) return fail(MLP_ERR_DTYPE, "dtype must be MLP_F32 or MLP_BF16");
+  if (batch < 1 || batch > (1ll << 30)) return fail(MLP_ERR_SHAPE, "batch out of range");
+  Layout& L = *Lo;
+  L.L = n_dims - 1;
+  L.dtype = dtype;
+  L.B = batch;
+  L.dims.assign(dims, dims + n_dims);
+  for (int i = 0; i < n_dims; ++i)
+    if (dims[i] < 1 || dims[i] > (1ll << 30)) return fail(MLP_ERR_SHAPE, "dims[%d] out of range", i);
+  L.acts.resize(n_dims - 2);
+  for (int i = 0; i < n_dims - 2; ++i) {
+    int a = acts ? acts[i] : act;
+    if (a < MLP_ACT_NONE || a > MLP_ACT_GELU_TANH) return fail(MLP_ERR_ARG, "bad activation %d", a);
+    L.acts[i] = a;
+  }
+  if (dtype == MLP_BF16)
+    for (int i = 0; i < n_dims - 1; ++i)
+      if (dims[i] % 8) return fail(MLP_ERR_SHAPE, "bf16 models need input/hidden widths that are multiples of 8");
+  // parameter planes
+  int64_t off = 0;
+  for (int l = 0; l < L.L; ++l) {
+    L.woff.push_back(off);
+    off += (dims[l + 1] * dims[l] + 63) / 64 * 64;
+    L.boff.push_back(off);
+    off += (dims[l + 1] + 63) / 64 * 64;
+    L.n_params += dims[l + 1] * dims[l] + dims[l + 1];
+  }
+  L.plane_n = off;
+  const size_t es = dtype == MLP_F32 ? 4 : 2;
+  size_t cur = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = cur;
+    cur = align_up(cur + bytes);
+    return o;
+  };
+  L.off_P = take(L.plane_n * 4);
+  L.off_G = take(L.plane_n * 4);
+  L.off_M = take(L.plane_n * 4);
+  L.off_V = take(L.plane_n * 4);
+  L.off_W16 = dtype == MLP_BF16 ? take(L.plane_n * 2) : 0;
+  int64_t max_ld = 8;
+  for (int l = 0; l < L.L - 1; ++l) {
+    int64_t ld = (dims[l + 1] + 7) / 8 * 8;
+    L.ld_h.push_back(ld);
+    max_ld = ld > max_ld ? ld : max_ld;
+    L.off_h.push_back(take(batch * ld * es));
+    L.off_u.push_back(L.acts[l] == MLP_ACT_GELU_TANH ? take(batch * ld * es) : 0);
+  }
+  L.ldz = (dims[L.L] + 7) / 8 * 8;
+  L.off_z = take(batch * L.ldz * es);
+  L.off_dz = take(batch * L.ldz * es);
+  L.off_dy[0] = take(batch * max_ld * es);
+  L.off_dy[1] = take(batch * max_ld * es);
+  L.off_loss_rows = take(batch * 4);
+  size_t ws = 0;
+  for (int l = 0; l < L.L; ++l) {
+    int s = wgrad_splits(dtype, dims[l + 1], dims[l], batch);
+    size_t b = wgrad_workspace_bytes(dtype, dims[l + 1], dims[l], batch, s);
+    ws = b > ws ? b : ws;
+  }
+  L.ws_bytes = ws;
+  L.off_ws = take(ws ? ws : 4);
+  L.off_ctl = take(sizeof(Ctl));
+  L.total = cur;
+  return MLP_OK;
+}
+
+// splitmix64 + Box-Muller: host generator for the Kaiming-normal draw.
+struct HostRng {
+  uint64_t s;
+  uint64_t next() {
+    uint64_t z = (s += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+  }
+  double uniform() { return ((next() >> 11) + 0.5) * (1.0 / 9007199254740992.0); }   // (0, 1)
+  bool have = false;
+  double spare = 0;
+  double normal() {
+    if (have) { have = false; return spare; }
+    double u1 = uniform(), u2 = uniform();
+    double r = sqrt(-2.0 * log(u1)), th = 6.283185307179586 * u2;
+    spare = r * sin(th);
+    have = true;
+    return r * cos(th);
+  }
+};
+
+struct GraphCache {
+  int n_steps = 0;
+  cudaGraphExec_t exec = nullptr;
+  cudaGraph_t graph = nullptr;
+  std::vector<cudaGraphNode_t> nodes;
+  std::vector<LaunchRec> recs;
+};
+
+}  // namespace
+
+struct mlp {
+  int device = 0;
+  Layout lay;
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+  bool use_graph = true;
+  std::mutex mu;
+  std::vector<GraphCache> graphs;
+  int kernels_per_step = 0;
+
+  float* plane(int which) const {
+    size_t off = which == MLP_PLANE_P ? lay.off_P : which == MLP_PLANE_G ? lay.off_G
+               : which == MLP_PLANE_M ? lay.off_M : lay.off_V;
+    return reinterpret_cast<float*>(arena + off);
+  }
+  void* w16() const { return lay.dtype == MLP_BF16 ? (void*)(arena + lay.off_W16) : nullptr; }
+  Ctl* ctl() const { return reinterpret_cast<Ctl*>(arena + lay.off_ctl); }
+  size_t es() const { return lay.dtype == MLP_F32 ? 4 : 2; }
+  void* at(size_t off) const { return arena + off; }
+  // weight operand of layer l in the compute dtype
+  const void* weight(int l) const {
+    return lay.dtype == MLP_BF16 ? (const void*)((const uint16_t*)w16() + lay.woff[l])
+                                 : (const void*)(plane(MLP_PLANE_P) + lay.woff[l]);
+  }
+  ~mlp() {
+    for (auto& g : graphs) {
+      if (g.exec) cudaGraphExecDestroy(g.exec);
+      if (g.graph) cudaGraphDestroy(g.graph);
+    }
+  }
+};
+
+namespace {
+
+mlp_status add(std::vector<LaunchRec>& out, int n, const LaunchRec* recs) {
+  for (int i = 0; i < n; ++i) out.push_back(recs[i]);
+  return MLP_OK;
+}
+
+#define PLAN_TRY(call)                                              \
+  do {                                                              \
+    char e_[512] = "";                                              \
+    LaunchRec r_[2];                                                \
+    int n_ = (call);                                                \
+    if (n_ < 0) return fail(MLP_ERR_SHAPE, "%s", e_);               \
+    add(out, n_, r_);                                               \
+  } while (0)
+
+// Forward GEMMs of all layers (logits into the arena's z buffer).
+mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out) {
+  const Layout& L = m->lay;
+  const void* X = x;
+  int64_t ldx = L.dims[0];
+  for (int l = 0; l < L.L; ++l) {
+    GemmOp op;
+    op.dtype = L.dtype;
+    op.kind = GEMM_FWD;
+    op.M = L.B; op.N = L.dims[l + 1]; op.K = L.dims[l];
+    op.A = X; op.lda = ldx; op.a_kmajor = true;
+    op.B = m->weight(l); op.ldb = L.dims[l]; op.b_kmajor = true;
+    op.bias = m->plane(MLP_PLANE_P) + L.boff[l];
+    op.err = &m->ctl()->err;
+    if (l < L.L - 1) {
+      op.act = L.acts[l];
+      op.out = m->at(L.off_h[l]); op.ldo = L.ld_h[l];
+      if (op.act == MLP_ACT_GELU_TANH) { op.out_u = m->at(L.off_u[l]); op.ldu = L.ld_h[l]; }
+      X = op.out; ldx = L.ld_h[l];
+    } else {
+      op.act = MLP_ACT_NONE;
+      op.out = m->at(L.off_z); op.ldo = L.ldz;
+    }
+    PLAN_TRY(gemm_plan(op, r_, e_, sizeof(e_)));
+  }
+  return MLP_OK;
+}
+
+struct Hyper { float lr, b1, b2, eps, wd; };
+
+mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper& hp, float* loss,
+                     std::vector<LaunchRec>& out) {
+  const Layout& L = m->lay;
+  mlp_status st = plan_forward(m, x, out);
+  if (st != MLP_OK) return st;
+  Ctl* ctl = m->ctl();
+  {
+    CeOp ce;
+    ce.dtype = L.dtype; ce.B = L.B; ce.C = L.dims[L.L];
+    ce.z = m->at(L.off_z); ce.ldz = L.ldz;
+    ce.labels = y;
+    ce.dz = m->at(L.off_dz); ce.lddz = L.ldz;
+    ce.loss_rows = (float*)m->at(L.off_loss_rows);
+    ce.grad_scale = (float)(1.0 / (double)L.B);
+    ce.err = &ctl->err;
+    char e_[512] = "";
+    LaunchRec r;
+    if (ce_plan(ce, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    out.push_back(r);
+    LossMeanOp lm;
+    lm.B = L.B; lm.loss_rows = ce.loss_rows;
+    lm.loss = loss ? loss : &ctl->loss_slot;
+    lm.step_counter = &ctl->step;
+    lm.err = &ctl->err;
+    if (loss_mean_plan(lm, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    out.push_back(r);
+  }
+  const void* dY = m->at(L.off_dz);
+  int64_t ldy = L.ldz;
+  int buf = 0;
+  float* G = m->plane(MLP_PLANE_G);
+  for (int l = L.L - 1; l >= 0; --l) {
+    const void* Xl = l == 0 ? x : m->at(L.off_h[l - 1]);
+    const int64_t ldxl = l == 0 ? L.dims[0] : L.ld_h[l - 1];
+    GemmOp wg;
+    wg.dtype = L.dtype; wg.kind = GEMM_WGRAD;
+    wg.M = L.dims[l + 1]; wg.N = L.dims[l]; wg.K = L.B;
+    wg.A = dY; wg.lda = ldy; wg.a_kmajor = false;
+    wg.B = Xl; wg.ldb = ldxl; wg.b_kmajor = false;
+    wg.dW = G + L.woff[l]; wg.ld_dw = L.dims[l];
+    wg.db = G + L.boff[l];
+    wg.ws = (float*)m->at(L.off_ws); wg.ws_bytes = L.ws_bytes;
+    wg.err = &ctl->err;
+    PLAN_TRY(gemm_plan(wg, r_, e_, sizeof(e_)));
+    if (l > 0) {
+      GemmOp dg;
+      dg.dtype = L.dtype; dg.kind = GEMM_DGRAD;
+      dg.act = L.acts[l - 1];
+      dg.M = L.B; dg.N = L.dims[l]; dg.K = L.dims[l + 1];
+      dg.A = dY; dg.lda = ldy; dg.a_kmajor = true;
+      dg.B = m->weight(l); dg.ldb = L.dims[l]; dg.b_kmajor = false;
+      dg.aux = dg.act == MLP_ACT_GELU_TANH ? m->at(L.off_u[l - 1]) : m->at(L.off_h[l - 1]);
+      dg.ld_aux = L.ld_h[l - 1];
+      dg.out = m->at(L.off_dy[buf]); dg.ldo = L.ld_h[l - 1];
+      dg.err = &ctl->err;
+      PLAN_TRY(gemm_plan(dg, r_, e_, sizeof(e_)));
+      dY = dg.out; ldy = dg.ldo;
+      buf ^= 1;
+    }
+  }
+  AdamWOp ad;
+  ad.n = L.plane_n;
+  ad.p = m->plane(MLP_PLANE_P); ad.g = G; ad.m = m->plane(MLP_PLANE_M); ad.v = m->plane(MLP_PLANE_V);
+  ad.w16 = m->w16();
+  ad.step_counter = &ctl->step;
+  ad.lr = hp.lr; ad.beta1 = hp.b1; ad.beta2 = hp.b2; ad.eps = hp.eps; ad.wd = hp.wd;
+  char e_[512] = "";
+  LaunchRec r;
+  if (adamw_plan(ad, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_ARG, "%s", e_);
+  out.push_back(r);
+  return MLP_OK;
+}
+
+mlp_status launch_eager(const std::vector<LaunchRec>& recs, cudaStream_t s) {
+  for (const auto& r : recs) {
+    cudaError_t e = launch_rec(r, s);
+    if (e != cudaSuccess) return fail(MLP_ERR_CUDA, "launch of %s failed: %s", r.name, cudaGetErrorString(e));
+  }
+  return MLP_OK;
+}
+
+bool same_topology(const std::vector<LaunchRec>& a, const std::vector<LaunchRec>& b) {
+  if (a.size() != b.size()) return false;
+  for (size_t i = 0; i < a.size(); ++i) {
+    const LaunchRec &x = a[i], &y = b[i];
+    if (x.func != y.func || x.grid.x != y.grid.x || x.grid.y != y.grid.y || x.grid.z != y.grid.z ||
+        x.block.x != y.block.x || x.smem != y.smem)
+      return false;
+  }
+  return true;
+}
+
+mlp_status launch_graph(mlp* m, int key, std::vector<LaunchRec>& recs, cudaStream_t s) {
+  GraphCache* gc = nullptr;
+  for (auto& g : m->graphs)
+    if (g.n_steps == key) gc = &g;
+  if (gc && !same_topology(gc->recs, recs)) {
+    cudaGraphExecDestroy(gc->exec);
+    cudaGraphDestroy(gc->graph);
+    gc->exec = nullptr;
+    gc->graph = nullptr;
+    gc->nodes.clear();
+    gc->recs.clear();
+  }
+  if (!gc) {
+    m->graphs.emplace_back();
+    gc = &m->graphs.back();
+    gc->n_steps = key;
+  }
+  if (!gc->exec) {
+    CUDA_TRY(cudaGraphCreate(&gc->graph, 0));
+    cudaGraphNode_t prev = nullptr;
+    for (auto& r : recs) {
+      void* argp[1];
+      cudaKernelNodeParams kp = node_params(r, argp);
+      cudaGraphNode_t node;
+      CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, prev ? &prev : nullptr, prev ? 1 : 0, &kp));
+      gc->nodes.push_back(node);
+      prev = node;
+    }
+    CUDA_TRY(cudaGraphInstantiate(&gc->exec, gc->graph, 0));
+    gc->recs = recs;
+  } else {
+    for (size_t i = 0; i < recs.size(); ++i) {
+      if (recs[i].same_as(gc->recs[i])) continue;
+      void* argp[1];
+      cudaKernelNodeParams kp = node_params(recs[i], argp);
+      CUDA_TRY(cudaGraphExecKernelNodeSetParams(gc->exec, gc->nodes[i], &kp));
+      gc->recs[i] = recs[i];
+    }
+  }
+  CUDA_TRY(cudaGraphLaunch(gc->exec, s));
+  return MLP_OK;
+}
+
+mlp_status run(mlp* m, int key, std::vector<LaunchRec>& recs, cudaStream_t s) {
+  mlp_status st = m->use_graph ? launch_graph(m, key, recs, s) : launch_eager(recs, s);
+  if (st != MLP_OK) return st;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MLP_ERR_CUDA, "after launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// C ABI: model.
+// ---------------------------------------------------------------------------
+extern "C" {
+
+const char* mlp_last_error(void) { return g_err; }
+
+size_t mlp_arena_bytes(const int64_t* dims, int n_dims, const int* acts, int act, int dtype, int64_t batch) {
+  Layout L;
+  if (plan_layout(dims, n_dims, acts, act, dtype, batch, &L) != MLP_OK) return 0;
+  return L.total;
+}
+
+mlp_status mlp_create(const int64_t* dims, int n_dims, const int* acts, int act, int dtype, uint64_t seed,
+                      int64_t batch, void* arena_dev, size_t arena_bytes, int device, mlp_t** out) {
+  if (!out) return fail(MLP_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  Layout L;
+  mlp_status st = plan_layout(dims, n_dims, acts, act, dtype, batch, &L);
+  if (st != MLP_OK) return st;
+  if (!arena_dev) return fail(MLP_ERR_ARG, "arena is NULL");
+  if ((uintptr_t)arena_dev % kAlign) return fail(MLP_ERR_ARG, "arena must be %zu-byte aligned", kAlign);
+  if (arena_bytes < L.total) return fail(MLP_ERR_ARG, "arena too small (%zu < %zu)", arena_bytes, L.total);
+  int ndev = 0;
+  CUDA_TRY(cudaGetDeviceCount(&ndev));
+  if (device < 0 || device >= ndev) return fail(MLP_ERR_ARG, "device %d not present", device);
+  DevGuard g(device);
+  cudaPointerAttributes pa;
+  CUDA_TRY(cudaPointerGetAttributes(&pa, arena_dev));
+  if (pa.type != cudaMemoryTypeDevice || pa.device != device)
+    return fail(MLP_ERR_ARG, "arena is not device memory of device %d", device);
+  mlp* m = new mlp();
+  m->device = device;
+  m->lay = L;
+  m->arena = (uint8_t*)arena_dev;
+  m->arena_bytes = arena_bytes;
+  cudaError_t e = cudaMemset(arena_dev, 0, L.total);
+  // Kaiming-normal weights, zero biases (P plane), drawn on the host.
+  std::vector<float> host(L.plane_n, 0.f);
+  HostRng rng{seed ^ 0x6A09E667F3BCC909ull};
+  for (int l = 0; l < L.L && e == cudaSuccess; ++l) {
+    const double std_ = sqrt(2.0 / (double)L.dims[l]);
+    const int64_t n = L.dims[l + 1] * L.dims[l];
+    for (int64_t i = 0; i < n; ++i) host[L.woff[l] + i] = (float)(rng.normal() * std_);
+  }
+  if (e == cudaSuccess) e = cudaMemcpy(m->plane(MLP_PLANE_P), host.data(), L.plane_n * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && dtype == MLP_BF16) {
+    char eb[256];
+    LaunchRec r;
+    cast_bf16_plan(L.plane_n, m->plane(MLP_PLANE_P), m->w16(), &r, eb, sizeof(eb));
+    e = launch_rec(r, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  }
+  if (e != cudaSuccess) {
+    delete m;
+    return fail(MLP_ERR_CUDA, "create: %s", cudaGetErrorString(e));
+  }
+  std::vector<LaunchRec> recs;
+  Hyper hp{1e-3f, 0.9f, 0.999f, 1e-8f, 0.f};
+  st = plan_step(m, arena_dev, (const int32_t*)arena_dev, hp, nullptr, recs);
+  if (st != MLP_OK) {
+    delete m;
+    return st;
+  }
+  m->kernels_per_step = (int)recs.size();
+  *out = m;
+  return ok();
+}
+
+void mlp_destroy(mlp_t* m) {
+  if (!m) return;
+  DevGuard g(m->device);
+  delete m;
+}
+
+int64_t mlp_num_params(const mlp_t* m) { return m ? m->lay.n_params : -1; }
+int mlp_num_layers(const mlp_t* m) { return m ? m->lay.L : -1; }
+int mlp_kernels_per_step(const mlp_t* m) { return m ? m->kernels_per_step : -1; }
+
+mlp_status mlp_set_graph_mode(mlp_t* m, int enable) {
+  if (!m) return fail(MLP_ERR_ARG, "model is NULL");
+  std::lock_guard<std::mutex> lk(m->mu);
+  m->use_graph = enable != 0;
+  return ok();
+}
+
+mlp_status mlp_forward(mlp_t* m, const void* x, void* logits, int32_t* argmax_out, void* stream) {
+  if (!m || !x) return fail(MLP_ERR_ARG, "model or x is NULL");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_forward(m, x, recs);
+  if (st != MLP_OK) return st;
+  const Layout& L = m->lay;
+  char e_[512] = "";
+  LaunchRec r;
+  if (logits) {
+    CopyRowsOp c;
+    c.dtype = L.dtype; c.B = L.B; c.C = L.dims[L.L];
+    c.src = m->at(L.off_z); c.lds = L.ldz;
+    c.dst = logits; c.ldd = L.dims[L.L];
+    if (copy_rows_plan(c, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    recs.push_back(r);
+  }
+  if (argmax_out) {
+    ArgmaxOp a;
+    a.dtype = L.dtype; a.B = L.B; a.C = L.dims[L.L];
+    a.z = m->at(L.off_z); a.ldz = L.ldz; a.out = argmax_out;
+    if (argmax_plan(a, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    recs.push_back(r);
+  }
+  st = launch_eager(recs, (cudaStream_t)stream);
+  if (st != MLP_OK) return st;
+  return ok();
+}
+
+mlp_status mlp_train_step(mlp_t* m, const void* x, const int32_t* y, float lr, float b1, float b2, float eps,
+                          float wd, float* loss, void* stream) {
+  if (!m || !x || !y) return fail(MLP_ERR_ARG, "model, x or labels is NULL");
+  if (!(lr >= 0) || !(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1) || !(eps >= 0) || !(wd >= 0))
+    return fail(MLP_ERR_ARG, "bad hyper-parameters");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_step(m, x, y, Hyper{lr, b1, b2, eps, wd}, loss, recs);
+  if (st != MLP_OK) return st;
+  return run(m, 1, recs, (cudaStream_t)stream);
+}
+
+mlp_status mlp_train_steps(mlp_t* m, int n_steps, const void* const* xs, const int32_t* const* ys, float lr,
+                           float b1, float b2, float eps, float wd, float* losses, void* stream) {
+  if (!m || !xs || !ys || n_steps < 1) return fail(MLP_ERR_ARG, "bad arguments");
+  if (!(lr >= 0) || !(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1) || !(eps >= 0) || !(wd >= 0))
+    return fail(MLP_ERR_ARG, "bad hyper-parameters");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  std::vector<LaunchRec> recs;
+  for (int i = 0; i < n_steps; ++i) {
+    if (!xs[i] || !ys[i]) return fail(MLP_ERR_ARG, "null batch pointer at step %d", i);
+    mlp_status st = plan_step(m, xs[i], ys[i], Hyper{lr, b1, b2, eps, wd}, losses ? losses + i : nullptr, recs);
+    if (st != MLP_OK) return st;
+  }
+  return run(m, n_steps, recs, (cudaStream_t)stream);
+}
+
+static mlp_status copy_plane(mlp_t* m, int plane, float* host_out, const float* host_in, size_t n) {
+  if (plane < MLP_PLANE_P || plane > MLP_PLANE_V) return fail(MLP_ERR_ARG, "bad plane %d", plane);
+  if ((int64_t)n != m->lay.n_params) return fail(MLP_ERR_ARG, "n must be %lld", (long long)m->lay.n_params);
+  const Layout& L = m->lay;
+  float* base = m->plane(plane);
+  size_t pos = 0;
+  for (int l = 0; l < L.L; ++l) {
+    const size_t nw = L.dims[l + 1] * L.dims[l], nb = L.dims[l + 1];
+    if (host_out) {
+      CUDA_TRY(cudaMemcpy(host_out + pos, base + L.woff[l], nw * 4, cudaMemcpyDeviceToHost));
+      CUDA_TRY(cudaMemcpy(host_out + pos + nw, base + L.boff[l], nb * 4, cudaMemcpyDeviceToHost));
+    } else {
+      CUDA_TRY(cudaMemcpy(base + L.woff[l], host_in + pos, nw * 4, cudaMemcpyHostToDevice));
+      CUDA_TRY(cudaMemcpy(base + L.boff[l], host_in + pos + nw, nb * 4, cudaMemcpyHostToDevice));
+    }
+    pos += nw + nb;
+  }
+  return MLP_OK;
+}
+
+mlp_status mlp_read_params(mlp_t* m, int plane, float* host_out, size_t n, int64_t* step_out) {
+  if (!m || !host_out) return fail(MLP_ERR_ARG, "model or buffer is NULL");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  CUDA_TRY(cudaDeviceSynchronize());
+  mlp_status st = copy_plane(m, plane, host_out, nullptr, n);
+  if (st != MLP_OK) return st;
+  if (step_out) CUDA_TRY(cudaMemcpy(step_out, &m->ctl()->step, sizeof(int64_t), cudaMemcpyDeviceToHost));
+  return ok();
+}
+
+mlp_status mlp_write_params(mlp_t* m, int plane, const float* host_in, size_t n, int64_t step) {
+  if (!m || !host_in) return fail(MLP_ERR_ARG, "model or buffer is NULL");
+  if (step < 0) return fail(MLP_ERR_ARG, "negative step");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  CUDA_TRY(cudaDeviceSynchronize());
+  mlp_status st = copy_plane(m, plane, nullptr, host_in, n);
+  if (st != MLP_OK) return st;
+  CUDA_TRY(cudaMemcpy(&m->ctl()->step, &step, sizeof(int64_t), cudaMemcpyHostToDevice));
+  if (plane == MLP_PLANE_P && m->lay.dtype == MLP_BF16) {
+    char eb[256];
+    LaunchRec r;
+    cast_bf16_plan(m->lay.plane_n, m->plane(MLP_PLANE_P), m->w16(), &r, eb, sizeof(eb));
+    CUDA_TRY(launch_rec(r, 0));
+  }
+  CUDA_TRY(cudaDeviceSynchronize());
+  return ok();
+}
+
+static mlp_status status_from_bits(uint32_t bits) {
+  if (bits & ERRBIT_LABEL_RANGE) return fail(MLP_ERR_LABEL_RANGE, "a label was outside [0, C)");
+  if (bits & ERRBIT_NONFINITE) return fail(MLP_ERR_NONFINITE, "non-finite batch loss");
+  if (bits & ERRBIT_TIMEOUT) return fail(MLP_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (bits) return fail(MLP_ERR_STATE, "device error bits 0x%x", bits);
+  return ok();
+}
+
+mlp_status mlp_check_errors(mlp_t* m, void* stream) {
+  if (!m) return fail(MLP_ERR_ARG, "model is NULL");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+  uint32_t bits = 0;
+  CUDA_TRY(cudaMemcpy(&bits, &m->ctl()->err, 4, cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemset(&m->ctl()->err, 0, 4));
+  return status_from_bits(bits);
+}
+
+// ---------------------------------------------------------------------------
+// C ABI: individual operations.
+// ---------------------------------------------------------------------------
+static mlp_status run_ops(LaunchRec* r, int n, void* stream) {
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = launch_rec(r[i], (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(MLP_ERR_CUDA, "launch of %s failed: %s", r[i].name, cudaGetErrorString(e));
+  }
+  return ok();
+}
+
+static bool dtype_ok(int d) { return d == MLP_F32 || d == MLP_BF16; }
+static bool act_ok(int a) { return a >= MLP_ACT_NONE && a <= MLP_ACT_GELU_TANH; }
+
+mlp_status mlp_op_linear_act(int dtype, int act, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx,
+                             const void* W, int64_t ldw, const float* b, void* H, int64_t ldh, void* U, int64_t ldu,
+                             uint32_t* err_dev, void* stream) {
+  if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
+  if (!act_ok(act)) return fail(MLP_ERR_ARG, "bad activation");
+  if (!X || !W || !b || !H) return fail(MLP_ERR_ARG, "null pointer");
+  if (ldx < K || ldw < K || ldh < N || (U && ldu < N)) return fail(MLP_ERR_SHAPE, "leading dimension too small");
+  GemmOp op;
+  op.dtype = dtype; op.kind = GEMM_FWD; op.act = act;
+  op.M = M; op.N = N; op.K = K;
+  op.A = X; op.lda = ldx; op.a_kmajor = true;
+  op.B = W; op.ldb = ldw; op.b_kmajor = true;
+  op.bias = b; op.out = H; op.ldo = ldh; op.out_u = U; op.ldu = ldu;
+  op.err = err_dev;
+  LaunchRec r[2];
+  char e_[512] = "";
+  int n = gemm_plan(op, r, e_, sizeof(e_));
+  if (n < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  return run_ops(r, n, stream);
+}
+
+mlp_status mlp_op_dgrad(int dtype, int act, int64_t M, int64_t N, int64_t K, const void* dY, int64_t ldy,
+                        const void* W, int64_t ldw, const void* S, int64_t lds, void* dX, int64_t ldx,
+                        uint32_t* err_dev, void* stream) {
+  if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
+  if (!act_ok(act)) return fail(MLP_ERR_ARG, "bad activation");
+  if (!dY || !W || !dX || (act != MLP_ACT_NONE && !S)) return fail(MLP_ERR_ARG, "null pointer");
+  if (ldy < N || ldw < K || ldx < K || (S && lds < K)) return fail(MLP_ERR_SHAPE, "leading dimension too small");
+  GemmOp op;
+  op.dtype = dtype; op.kind = GEMM_DGRAD; op.act = act;
+  op.M = M; op.N = K; op.K = N;
+  op.A = dY; op.lda = ldy; op.a_kmajor = true;
+  op.B = W; op.ldb = ldw; op.b_kmajor = false;
+  op.aux = S; op.ld_aux = lds;
+  op.out = dX; op.ldo = ldx;
+  op.err = err_dev;
+  LaunchRec r[2];
+  char e_[512] = "";
+  int n = gemm_plan(op, r, e_, sizeof(e_));
+  if (n < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  return run_ops(r, n, stream);
+}
+
+size_t mlp_op_wgrad_workspace_bytes(int dtype, int64_t N, int64_t K, int64_t B) {
+  if (!dtype_ok(dtype) || N < 1 || K < 1 || B < 1) return 0;
+  int s = wgrad_splits(dtype, N, K, B);
+  return wgrad_workspace_bytes(dtype, N, K, B, s);
+}
+
+mlp_status mlp_op_wgrad(int dtype, int64_t N, int64_t K, int64_t B, const void* dY, int64_t ldy, const void* X,
+                        int64_t ldx, float* dW, int64_t lddw, float* db, void* workspace, size_t ws_bytes,
+                        uint32_t* err_dev, void* stream) {
+  if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
+  if (!dY || !X || !dW) return fail(MLP_ERR_ARG, "null pointer");
+  if (ldy < N || ldx < K || lddw < K) return fail(MLP_ERR_SHAPE, "leading dimension too small");
+  GemmOp op;
+  op.dtype = dtype; op.kind = GEMM_WGRAD;
+  op.M = N; op.N = K; op.K = B;
+  op.A = dY; op.lda = ldy; op.a_kmajor = false;
+  op.B = X; op.ldb = ldx; op.b_kmajor = false;
+  op.dW = dW; op.ld_dw = lddw; op.db = db;
+  op.ws = (float*)workspace; op.ws_bytes = ws_bytes;
+  op.err = err_dev;
+  LaunchRec r[2];
+  char e_[512] = "";
+  int n = gemm_plan(op, r, e_, sizeof(e_));
+  if (n < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  return run_ops(r, n, stream);
+}
+
+mlp_status mlp_op_softmax_ce(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, const int32_t* labels,
+                             float grad_scale, void* dz, int64_t lddz, float* loss_rows, uint32_t* err_dev,
+                             void* stream) {
+  if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
+  if (!z || !labels || !dz || !loss_rows) return fail(MLP_ERR_ARG, "null pointer");
+  CeOp op;
+  op.dtype = dtype; op.B = B; op.C = C; op.z = z; op.ldz = ldz; op.labels = labels;
+  op.dz = dz; op.lddz = lddz; op.loss_rows = loss_rows; op.grad_scale = grad_scale; op.err = err_dev;
+  LaunchRec r;
+  char e_[512] = "";
+  if (ce_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  return run_ops(&r, 1, stream);
+}
+
+mlp_status mlp_op_loss_mean(int64_t B, const float* loss_rows, float* loss, uint32_t* err_dev, void* stream) {
+  if (!loss_rows || !loss) return fail(MLP_ERR_ARG, "null pointer");
+  LossMeanOp op;
+  op.B = B; op.loss_rows = loss_rows; op.loss = loss; op.err = err_dev;
+  LaunchRec r;
+  char e_[512] = "";
+  if (loss_mean_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  return run_ops(&r, 1, stream);
+}
+
+mlp_status mlp_op_adamw(int64_t n, float* p, const float* g, float* m, float* v, void* w16, int64_t t, float lr,
+                        float beta1, float beta2, float eps, float wd, void* stream) {
+  if (!p || !g || !m || !v) return fail(MLP_ERR_ARG, "null pointer");
+  if (t < 1) return fail(MLP_ERR_ARG, "t must be >= 1");
+  AdamWOp op;
+  op.n = n; op.p = p; op.g = g; op.m = m; op.v = v; op.w16 = w16; op.t = t;
+  op.lr = lr; op.beta1 = beta1; op.beta2 = beta2; op.eps = eps; op.wd = wd;
+  LaunchRec r;
+  char e_[512] = "";
+  if (adamw_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_ARG, "%s", e_);
+  return run_ops(&r, 1, stream);
+}
+
+mlp_status mlp_op_argmax(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, int32_t* out, void* stream) {
+  if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
+  if (!z || !out) return fail(MLP_ERR_ARG, "null pointer");
+  if (ldz < C) return fail(MLP_ERR_SHAPE, "ldz < C");
+  ArgmaxOp op;
+  op.dtype = dtype; op.B = B; op.C = C; op.z = z; op.ldz = ldz; op.out = out;
+  LaunchRec r;
+  char e_[512] = "";
+  if (argmax_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  return run_ops(&r, 1, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+// Internal interface between the step runtime and the kernels.  Every op is
+// turned into one or more LaunchRec's; the runtime decides whether to launch
+// them on a stream or to record them into a CUDA graph.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace mlpk {
+
+enum GemmKind : int { GEMM_FWD = 0, GEMM_DGRAD = 1, GEMM_WGRAD = 2 };
+
+// C[m, n] = sum_k A(m, k) * B(k, n), with the epilogue chosen by `kind`.
+//   A(m, k) = A[m*lda + k] if a_kmajor else A[k*lda + m]
+//   B(k, n) = B[n*ldb + k] if b_kmajor else B[k*ldb + n]
+// GEMM_FWD   : out[m, n] = act(C + bias[n]); out_u (optional) = C + bias[n]
+// GEMM_DGRAD : out[m, n] = C * act'(aux[m, n])   (aux = stored h for ReLU,
+//              stored u for GELU)
+// GEMM_WGRAD : dW[m, n] = C (fp32);  db[m] = sum_k A(m, k) (fp32), the bias
+//              gradient fused in.  With splits > 1 the K range is cut into
+//              `splits` chunks whose fp32 partials go to `ws` and are summed
+//              in a fixed order by a second kernel (deterministic).
+struct GemmOp {
+  int dtype = 0;            // DT_F32 or DT_BF16 (A, B, out, aux)
+  int kind = GEMM_FWD;
+  int act = 0;
+  int64_t M = 0, N = 0, K = 0;
+  const void* A = nullptr; int64_t lda = 0; bool a_kmajor = true;
+  const void* B = nullptr; int64_t ldb = 0; bool b_kmajor = true;
+  const float* bias = nullptr;
+  void* out = nullptr; int64_t ldo = 0;
+  void* out_u = nullptr; int64_t ldu = 0;
+  const void* aux = nullptr; int64_t ld_aux = 0;
+  float* dW = nullptr; int64_t ld_dw = 0;
+  float* db = nullptr;
+  float* ws = nullptr; size_t ws_bytes = 0;
+  int splits = 0;           // 0 = choose
+  uint32_t* err = nullptr;  // device error word (bounded-wait timeouts)
+};
+
+// Number of K splits the wgrad of this shape uses, and the workspace bytes.
+int wgrad_splits(int dtype, int64_t M, int64_t N, int64_t K);
+size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int splits);
+
+// Plans: fill recs[0..n) and return n (<= 2), or -1 with a message in err.
+int simt_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen);
+int tc_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen);
+// The kernel used by the model: tcgen05 for bf16, SIMT FFMA for fp32.
+int gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen);
+
+// Softmax cross-entropy, forward and backward in one pass over each row.
+struct CeOp {
+  int dtype = 0;
+  int64_t B = 0, C = 0;
+  const void* z = nullptr; int64_t ldz = 0;
+  const int32_t* labels = nullptr;
+  void* dz = nullptr; int64_t lddz = 0;
+  float* loss_rows = nullptr;
+  float grad_scale = 1.0f;   // 1/B for a batch-mean loss
+  uint32_t* err = nullptr;
+};
+int ce_plan(const CeOp& op, LaunchRec* rec, char* err, size_t errlen);
+
+// loss = mean(loss_rows) in a fixed order; optionally bumps the step counter
+// and latches a non-finite loss into the error word.
+struct LossMeanOp {
+  int64_t B = 0;
+  const float* loss_rows = nullptr;
+  float* loss = nullptr;
+  int64_t* step_counter = nullptr;   // nullable
+  uint32_t* err = nullptr;           // nullable
+};
+int loss_mean_plan(const LossMeanOp& op, LaunchRec* rec, char* err, size_t errlen);
+
+// AdamW over flat fp32 planes (one launch for every parameter).
+struct AdamWOp {
+  int64_t n = 0;
+  float* p = nullptr; const float* g = nullptr; float* m = nullptr; float* v = nullptr;
+  void* w16 = nullptr;                 // bf16 copy of p written after the update (nullable)
+  const int64_t* step_counter = nullptr;   // t read from device (already incremented)...
+  int64_t t = 0;                       // ...or given explicitly when > 0
+  float lr = 0, beta1 = 0, beta2 = 0, eps = 0, wd = 0;
+};
+int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen);
+
+// Row argmax, lowest index among equal maxima.
+struct ArgmaxOp {
+  int dtype = 0;
+  int64_t B = 0, C = 0;
+  const void* z = nullptr; int64_t ldz = 0;
+  int32_t* out = nullptr;
+};
+int argmax_plan(const ArgmaxOp& op, LaunchRec* rec, char* err, size_t errlen);
+
+// Copy rows of a padded [B, ld] matrix into a dense [B, C] one.
+struct CopyRowsOp {
+  int dtype = 0;
+  int64_t B = 0, C = 0;
+  const void* src = nullptr; int64_t lds = 0;
+  void* dst = nullptr; int64_t ldd = 0;
+};
+int copy_rows_plan(const CopyRowsOp& op, LaunchRec* rec, char* err, size_t errlen);
+
+// w16[i] = bf16_rne(p[i]).
+int cast_bf16_plan(int64_t n, const float* p, void* w16, LaunchRec* rec, char* err, size_t errlen);
+
+}  // namespace mlpk

@@ -1,0 +1,437 @@
+// Bandwidth-bound kernels of the step: the one-pass softmax cross-entropy
+// (forward loss and backward dz from a single read of each logits row, the
+// fused form described on devpost "Orthon", "Selected Orthon vs. PyTorch
+// results"), the batch-mean loss, the flat multi-tensor AdamW update over
+// co-located parameter/gradient/moment planes (noeira.ai "Neural networks",
+// "The design in one page": a Param is four tensors), the row argmax, and
+// small copies.
+#include <math.h>
+#include <stdio.h>
+
+#include "common.cuh"
+#include "ops.h"
+
+namespace mlpk {
+
+// ---------------------------------------------------------------------------
+// Softmax cross-entropy.
+//   m = max_j z_j;  s = sum_j exp(z_j - m);  loss_i = m + log(s) - z[y_i];
+//   dz_j = (exp(z_j - m) / s - [j == y_i]) * grad_scale.
+// ---------------------------------------------------------------------------
+struct CeParams {
+  const void* z; int64_t ldz;
+  const int32_t* labels;
+  void* dz; int64_t lddz;
+  float* loss_rows;
+  int B, C;
+  float grad_scale;
+  uint32_t* err;
+};
+
+template <typename T>
+__device__ __forceinline__ void ce_finish_row(const CeParams& p, int row, int y, float m, float s,
+                                              bool bad_label, int lane_or_tid) {
+  if (lane_or_tid == 0) {
+    const T* zr = reinterpret_cast<const T*>(p.z) + (int64_t)row * p.ldz;
+    float zy = bad_label ? 0.f : to_f32(zr[y]);
+    p.loss_rows[row] = bad_label ? 0.f : (m + logf(s)) - zy;
+    if (bad_label && p.err) atomicOr(p.err, ERRBIT_LABEL_RANGE);
+  }
+}
+
+// One warp per row; the row lives in registers (C <= 32 * VPL).
+template <typename T, int VPL>
+__global__ void __launch_bounds__(256) ce_warp_kernel(const __grid_constant__ CeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= p.B) return;
+  const T* zr = reinterpret_cast<const T*>(p.z) + (int64_t)row * p.ldz;
+  float v[VPL];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    int j = lane + 32 * i;
+    v[i] = j < p.C ? to_f32(zr[j]) : -INFINITY;
+    m = fmaxf(m, v[i]);
+  }
+  m = warp_max(m);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    int j = lane + 32 * i;
+    v[i] = j < p.C ? expf(v[i] - m) : 0.f;
+    s += v[i];
+  }
+  s = warp_sum(s);
+  const int y = p.labels[row];
+  const bool bad = y < 0 || y >= p.C;
+  const float inv_s = 1.0f / s;
+  T* dr = reinterpret_cast<T*>(p.dz) + (int64_t)row * p.lddz;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    int j = lane + 32 * i;
+    if (j < p.C) dr[j] = from_f32<T>((v[i] * inv_s - (j == y ? 1.f : 0.f)) * p.grad_scale);
+  }
+  ce_finish_row<T>(p, row, y, m, s, bad, lane);
+}
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = is_max ? warp_max(v) : warp_sum(v);
+  __syncthreads();   // protect red from a previous use
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float r = lane < nw ? red[lane] : (is_max ? -INFINITY : 0.f);
+  r = is_max ? warp_max(r) : warp_sum(r);
+  return r;
+}
+
+// One CTA per row, the row held in registers as 16-byte vectors:
+// C % (16 / sizeof(T)) == 0 and C <= blockDim * VPT * (16 / sizeof(T)).
+template <typename T, int VPT>
+__global__ void __launch_bounds__(512) ce_block_kernel(const __grid_constant__ CeParams p) {
+  constexpr int E = 16 / sizeof(T);   // elements per vector
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  const int nvec = p.C / E;
+  const uint4* zr = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.z) + (int64_t)row * p.ldz);
+  uint4 raw[VPT];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    int vi = threadIdx.x + i * blockDim.x;
+    if (vi < nvec) {
+      raw[i] = __ldg(zr + vi);
+      const T* e = reinterpret_cast<const T*>(&raw[i]);
+#pragma unroll
+      for (int k = 0; k < E; ++k) m = fmaxf(m, to_f32(e[k]));
+    }
+  }
+  m = block_reduce(m, true, red);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    int vi = threadIdx.x + i * blockDim.x;
+    if (vi < nvec) {
+      const T* e = reinterpret_cast<const T*>(&raw[i]);
+#pragma unroll
+      for (int k = 0; k < E; ++k) s += expf(to_f32(e[k]) - m);
+    }
+  }
+  s = block_reduce(s, false, red);
+  const int y = p.labels[row];
+  const bool bad = y < 0 || y >= p.C;
+  const float inv_s = 1.0f / s;
+  uint4* dr = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.dz) + (int64_t)row * p.lddz);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    int vi = threadIdx.x + i * blockDim.x;
+    if (vi < nvec) {
+      const T* e = reinterpret_cast<const T*>(&raw[i]);
+      uint4 o;
+      T* oe = reinterpret_cast<T*>(&o);
+#pragma unroll
+      for (int k = 0; k < E; ++k) {
+        int j = vi * E + k;
+        oe[k] = from_f32<T>((expf(to_f32(e[k]) - m) * inv_s - (j == y ? 1.f : 0.f)) * p.grad_scale);
+      }
+      dr[vi] = o;
+    }
+  }
+  ce_finish_row<T>(p, row, y, m, s, bad, threadIdx.x);
+}
+
+// Any C: one CTA per row, three passes over the row (max, sum, write).
+template <typename T>
+__global__ void __launch_bounds__(256) ce_generic_kernel(const __grid_constant__ CeParams p) {
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  const T* zr = reinterpret_cast<const T*>(p.z) + (int64_t)row * p.ldz;
+  float m = -INFINITY;
+  for (int j = threadIdx.x; j < p.C; j += blockDim.x) m = fmaxf(m, to_f32(zr[j]));
+  m = block_reduce(m, true, red);
+  float s = 0.f;
+  for (int j = threadIdx.x; j < p.C; j += blockDim.x) s += expf(to_f32(zr[j]) - m);
+  s = block_reduce(s, false, red);
+  const int y = p.labels[row];
+  const bool bad = y < 0 || y >= p.C;
+  const float inv_s = 1.0f / s;
+  T* dr = reinterpret_cast<T*>(p.dz) + (int64_t)row * p.lddz;
+  for (int j = threadIdx.x; j < p.C; j += blockDim.x)
+    dr[j] = from_f32<T>((expf(to_f32(zr[j]) - m) * inv_s - (j == y ? 1.f : 0.f)) * p.grad_scale);
+  ce_finish_row<T>(p, row, y, m, s, bad, threadIdx.x);
+}
+
+template <typename T>
+static int ce_plan_t(const CeOp& op, LaunchRec* rec, const CeParams& q) {
+  constexpr int E = 16 / sizeof(T);
+  const int64_t C = op.C;
+  rec->smem = 0;
+  rec->name = "softmax_ce";
+  if (C <= 32 * 8) {
+    rec->block = dim3(256);
+    rec->grid = dim3((unsigned)ceil_div(op.B, 8));
+    if (C <= 32) rec->func = (const void*)ce_warp_kernel<T, 1>;
+    else if (C <= 64) rec->func = (const void*)ce_warp_kernel<T, 2>;
+    else if (C <= 128) rec->func = (const void*)ce_warp_kernel<T, 4>;
+    else rec->func = (const void*)ce_warp_kernel<T, 8>;
+  } else {
+    const bool vec_ok = (C % E == 0) && (op.ldz % E == 0) && (op.lddz % E == 0) &&
+                        ((uintptr_t)op.z % 16 == 0) && ((uintptr_t)op.dz % 16 == 0);
+    const int64_t nvec = C / E;
+    rec->grid = dim3((unsigned)op.B);
+    if (vec_ok && nvec <= 512 * 8) {
+      rec->block = dim3(nvec <= 128 * 8 ? 128 : nvec <= 256 * 8 ? 256 : 512);
+      rec->func = (const void*)ce_block_kernel<T, 8>;
+    } else {
+      rec->block = dim3(256);
+      rec->func = (const void*)ce_generic_kernel<T>;
+    }
+  }
+  rec->set_args(q);
+  return 1;
+}
+
+int ce_plan(const CeOp& op, LaunchRec* rec, char* err, size_t errlen) {
+  if (op.B <= 0 || op.C <= 0 || op.B > INT32_MAX || op.C > INT32_MAX || op.ldz < op.C || op.lddz < op.C) {
+    snprintf(err, errlen, "softmax_ce: bad shape B=%lld C=%lld", (long long)op.B, (long long)op.C);
+    return -1;
+  }
+  CeParams q{op.z, op.ldz, op.labels, op.dz, op.lddz, op.loss_rows, (int)op.B, (int)op.C, op.grad_scale, op.err};
+  if (op.dtype == DT_F32) return ce_plan_t<float>(op, rec, q);
+  return ce_plan_t<__nv_bfloat16>(op, rec, q);
+}
+
+// ---------------------------------------------------------------------------
+// Batch-mean loss (fixed-order, fp64 partial sums), step counter, finiteness.
+// ---------------------------------------------------------------------------
+struct LossMeanParams {
+  const float* loss_rows; int64_t B;
+  float* loss;
+  int64_t* step_counter;
+  uint32_t* err;
+};
+
+__global__ void __launch_bounds__(1024) loss_mean_kernel(const __grid_constant__ LossMeanParams p) {
+  __shared__ double red[1024];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < p.B; i += blockDim.x) s += (double)p.loss_rows[i];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    float L = (float)(red[0] / (double)p.B);
+    if (p.loss) *p.loss = L;
+    if (p.step_counter) *p.step_counter += 1;
+    if (p.err && !isfinite(L)) atomicOr(p.err, ERRBIT_NONFINITE);
+  }
+}
+
+int loss_mean_plan(const LossMeanOp& op, LaunchRec* rec, char* err, size_t errlen) {
+  if (op.B <= 0) { snprintf(err, errlen, "loss_mean: empty batch"); return -1; }
+  LossMeanParams q{op.loss_rows, op.B, op.loss, op.step_counter, op.err};
+  rec->func = (const void*)loss_mean_kernel;
+  rec->grid = dim3(1);
+  rec->block = dim3(1024);
+  rec->smem = 0;
+  rec->name = "loss_mean";
+  rec->set_args(q);
+  return 1;
+}
+
+// ---------------------------------------------------------------------------
+// AdamW over flat planes.  PyTorch / Loshchilov-Hutter form:
+//   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+//   p = p - lr * (m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps) + wd * p_old).
+// ---------------------------------------------------------------------------
+struct AdamWParams {
+  float* p; const float* g; float* m; float* v;
+  __nv_bfloat16* w16;
+  const int64_t* step_counter; int64_t t;
+  int64_t n;
+  float lr, beta1, beta2, eps, wd;
+};
+
+__device__ __forceinline__ void adamw_one(float& p, float g, float& m, float& v, float lr, float b1,
+                                          float b2, float eps, float wd, float inv_bc1, float inv_sqrt_bc2) {
+  m = b1 * m + (1.f - b1) * g;
+  v = b2 * v + (1.f - b2) * g * g;
+  float mhat = m * inv_bc1;
+  float denom = sqrtf(v) * inv_sqrt_bc2 + eps;
+  p = p - lr * (mhat / denom + wd * p);
+}
+
+__global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamWParams q) {
+  const int64_t t = q.t > 0 ? q.t : *q.step_counter;
+  const double bc1 = 1.0 - pow((double)q.beta1, (double)t);
+  const double bc2 = 1.0 - pow((double)q.beta2, (double)t);
+  const float inv_bc1 = (float)(1.0 / bc1);
+  const float inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
+  const int64_t n4 = q.n / 4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 p = reinterpret_cast<float4*>(q.p)[i];
+    float4 g = reinterpret_cast<const float4*>(q.g)[i];
+    float4 m = reinterpret_cast<float4*>(q.m)[i];
+    float4 v = reinterpret_cast<float4*>(q.v)[i];
+    adamw_one(p.x, g.x, m.x, v.x, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
+    adamw_one(p.y, g.y, m.y, v.y, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
+    adamw_one(p.z, g.z, m.z, v.z, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
+    adamw_one(p.w, g.w, m.w, v.w, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
+    reinterpret_cast<float4*>(q.p)[i] = p;
+    reinterpret_cast<float4*>(q.m)[i] = m;
+    reinterpret_cast<float4*>(q.v)[i] = v;
+    if (q.w16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(p.x, p.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(p.z, p.w);
+      uint2 o;
+      o.x = *reinterpret_cast<uint32_t*>(&lo);
+      o.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(q.w16)[i] = o;
+    }
+  }
+  // tail (n not a multiple of 4)
+  for (int64_t i = n4 * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < q.n; i += stride) {
+    float p = q.p[i], m = q.m[i], v = q.v[i];
+    adamw_one(p, q.g[i], m, v, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
+    q.p[i] = p; q.m[i] = m; q.v[i] = v;
+    if (q.w16) q.w16[i] = __float2bfloat16_rn(p);
+  }
+}
+
+int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
+  if (op.n < 0) { snprintf(err, errlen, "adamw: negative size"); return -1; }
+  if (op.t <= 0 && !op.step_counter) { snprintf(err, errlen, "adamw: no step"); return -1; }
+  auto al = [](const void* ptr, int a) { return ((uintptr_t)ptr % a) == 0; };
+  if (!al(op.p, 16) || !al(op.g, 16) || !al(op.m, 16) || !al(op.v, 16) || (op.w16 && !al(op.w16, 8))) {
+    snprintf(err, errlen, "adamw: planes must be 16-byte aligned (w16: 8)");
+    return -1;
+  }
+  AdamWParams q{op.p, op.g, op.m, op.v, (__nv_bfloat16*)op.w16, op.step_counter, op.t, op.n,
+                op.lr, op.beta1, op.beta2, op.eps, op.wd};
+  rec->func = (const void*)adamw_kernel;
+  int64_t blocks = ceil_div(op.n / 4 + 1, 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks < 1) blocks = 1;
+  rec->grid = dim3((unsigned)blocks);
+  rec->block = dim3(256);
+  rec->smem = 0;
+  rec->name = "adamw_flat";
+  rec->set_args(q);
+  return 1;
+}
+
+// ---------------------------------------------------------------------------
+// Row argmax (lowest index on ties).
+// ---------------------------------------------------------------------------
+struct ArgmaxParams {
+  const void* z; int64_t ldz; int B, C; int32_t* out;
+};
+
+__device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i) || (v != v && v2 == v2)) { v = v2; i = i2; }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) argmax_kernel(const __grid_constant__ ArgmaxParams p) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const int row = blockIdx.x;
+  const T* zr = reinterpret_cast<const T*>(p.z) + (int64_t)row * p.ldz;
+  float v = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int j = threadIdx.x; j < p.C; j += blockDim.x) argmax_merge(v, idx, to_f32(zr[j]), j);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    argmax_merge(v, idx, v2, i2);
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) { sv[wid] = v; si[wid] = idx; }
+  __syncthreads();
+  if (wid == 0) {
+    v = lane < nw ? sv[lane] : -INFINITY;
+    idx = lane < nw ? si[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+      int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+      argmax_merge(v, idx, v2, i2);
+    }
+    if (lane == 0) p.out[row] = idx == 0x7fffffff ? 0 : idx;
+  }
+}
+
+int argmax_plan(const ArgmaxOp& op, LaunchRec* rec, char* err, size_t errlen) {
+  if (op.B <= 0 || op.C <= 0 || op.B > INT32_MAX || op.C > INT32_MAX) {
+    snprintf(err, errlen, "argmax: bad shape");
+    return -1;
+  }
+  ArgmaxParams q{op.z, op.ldz, (int)op.B, (int)op.C, op.out};
+  rec->func = op.dtype == DT_F32 ? (const void*)argmax_kernel<float> : (const void*)argmax_kernel<__nv_bfloat16>;
+  rec->grid = dim3((unsigned)op.B);
+  rec->block = dim3(op.C <= 32 ? 32 : op.C <= 1024 ? 128 : 256);
+  rec->smem = 0;
+  rec->name = "argmax";
+  rec->set_args(q);
+  return 1;
+}
+
+// ---------------------------------------------------------------------------
+// Copies.
+// ---------------------------------------------------------------------------
+struct CopyRowsParams {
+  const unsigned char* src; int64_t lds_bytes;
+  unsigned char* dst; int64_t ldd_bytes;
+  int64_t B, row_bytes;
+};
+
+__global__ void copy_rows_kernel(const __grid_constant__ CopyRowsParams p) {
+  const int64_t total = p.B * p.row_bytes;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r = i / p.row_bytes, c = i % p.row_bytes;
+    p.dst[r * p.ldd_bytes + c] = p.src[r * p.lds_bytes + c];
+  }
+}
+
+int copy_rows_plan(const CopyRowsOp& op, LaunchRec* rec, char* err, size_t errlen) {
+  if (op.B <= 0 || op.C <= 0) { snprintf(err, errlen, "copy_rows: bad shape"); return -1; }
+  int64_t es = op.dtype == DT_F32 ? 4 : 2;
+  CopyRowsParams q{(const unsigned char*)op.src, op.lds * es, (unsigned char*)op.dst, op.ldd * es, op.B, op.C * es};
+  rec->func = (const void*)copy_rows_kernel;
+  int64_t blocks = ceil_div(op.B * op.C * es, 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  rec->grid = dim3((unsigned)blocks);
+  rec->block = dim3(256);
+  rec->smem = 0;
+  rec->name = "copy_rows";
+  rec->set_args(q);
+  return 1;
+}
+
+struct CastParams { const float* p; __nv_bfloat16* w16; int64_t n; };
+
+__global__ void cast_bf16_kernel(const __grid_constant__ CastParams q) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < q.n; i += (int64_t)gridDim.x * blockDim.x)
+    q.w16[i] = __float2bfloat16_rn(q.p[i]);
+}
+
+int cast_bf16_plan(int64_t n, const float* p, void* w16, LaunchRec* rec, char* err, size_t errlen) {
+  if (n <= 0) { snprintf(err, errlen, "cast: empty"); return -1; }
+  CastParams q{p, (__nv_bfloat16*)w16, n};
+  rec->func = (const void*)cast_bf16_kernel;
+  int64_t blocks = ceil_div(n, 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  rec->grid = dim3((unsigned)blocks);
+  rec->block = dim3(256);
+  rec->smem = 0;
+  rec->name = "cast_bf16";
+  rec->set_args(q);
+  return 1;
+}
+
+}  // namespace mlpk

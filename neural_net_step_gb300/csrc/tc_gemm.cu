@@ -1,0 +1,559 @@
+// bf16 GEMMs of the training step on the sm_103a tensor cores: tcgen05.mma
+// with the fp32 accumulator in tensor memory (TMEM), operands staged in
+// shared memory by TMA (cp.async.bulk.tensor, 128-byte swizzle) through an
+// mbarrier ring, and the step's epilogue fused after the TMEM read-back:
+//   forward : h = act(acc + b) (and u = acc + b for GELU), bf16 out
+//             (noeira.ai "Neural networks", "The design in one page":
+//             MatMul+Bias+Activation in one kernel, bias and activation in
+//             the GEMM epilogue);
+//   dgrad   : dY_prev = acc * act'(stored h or u), bf16 out;
+//   wgrad   : dW = acc in fp32, plus db = row sums of the A tile (dY^T) read
+//             from shared memory by the otherwise idle epilogue warps.
+// Mixed precision as in MuNet (pypi "munet-nn", "Configuration",
+// precision="mixed"): rounded low-precision inputs, fp32 accumulation.
+//
+// One 128 x BN output tile per CTA; 6 warps: warp 0 issues TMA, warp 1 owns
+// TMEM and issues the MMAs (one elected lane), warps 2..5 run the epilogue
+// (warp w reads TMEM lanes 32*(w%4) .. +31).  Every mbarrier wait is bounded
+// by a wall-clock limit; on expiry the kernel latches ERRBIT_TIMEOUT in the
+// error word, drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ops.h"
+
+namespace mlpk {
+
+int split_reduce_plan(const float* ws, int splits, int64_t M, int64_t N, float* dW, int64_t ld_dw,
+                      float* db, LaunchRec* rec);
+int simt_gemm_splits(int64_t M, int64_t N, int64_t K);
+
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                       // 64 bf16 = 128 bytes = one swizzle row
+constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
+constexpr int NUM_THREADS = 192;
+constexpr uint64_t kWaitLimitNs = 500000000ull;   // 0.5 s (a legitimate wait is microseconds)
+
+template <int BN> struct Cfg {
+  static constexpr int B_STAGE_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int STAGES = BN >= 256 ? 4 : BN >= 128 ? 6 : 8;
+  static constexpr int TMEM_COLS = BN <= 32 ? 32 : BN;   // power of two >= 32
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
+};
+
+struct Params {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  int M, N, K;
+  int kb_per_split;     // k-blocks per blockIdx.z
+  int num_kb;           // total k-blocks
+  int a_mn, b_mn;       // 1: operand is MN-major in memory
+  int kind, act;
+  uint32_t idesc;
+  const float* bias;
+  __nv_bfloat16* out; int64_t ldo;
+  __nv_bfloat16* out_u; int64_t ldu;
+  const __nv_bfloat16* aux; int64_t ld_aux;
+  float* dW; int64_t ld_dw;
+  float* db;
+  float* ws;            // split-K partials (splits > 1)
+  uint32_t* err;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: true when the phase completed, false after the time limit
+// (the error word is then marked).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      if (err) atomicOr(err, ERRBIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"((uint64_t)tm), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tm) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 32 lanes x 32 bits, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format:
+// start>>4 in [0,14), LBO>>4 in [16,30), SBO>>4 in [32,46), version 1 at
+// [46,48), layout type 2 = SWIZZLE_128B at [61,64)).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t a_base = base;
+  const uint32_t b_base = base + C::STAGES * A_STAGE_BYTES;
+  const uint32_t bar_base = b_base + C::STAGES * C::B_STAGE_BYTES;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
+  const uint32_t acc_bar = bar_base + 8u * (2 * C::STAGES);
+  const uint32_t tmem_slot = acc_bar + 8u;
+  volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int kb0 = blockIdx.z * p.kb_per_split;
+  const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+  const int nkb = max(kb1 - kb0, 0);
+  const bool do_db = p.kind == GEMM_WGRAD && blockIdx.x == 0 && p.db != nullptr;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), do_db ? 5 : 1);
+    }
+    mbar_init(acc_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_ptr;
+
+  const uint32_t b_bytes = C::B_STAGE_BYTES;
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&p.tmA);
+      prefetch_tmap(&p.tmB);
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < nkb && ok; ++i) {
+        const int s = i % C::STAGES;
+        const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
+        if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
+        mbar_expect_tx(full_bar(s), A_STAGE_BYTES + b_bytes);
+        const int k0 = (kb0 + i) * BK;
+        const uint32_t sa = a_base + s * A_STAGE_BYTES;
+        const uint32_t sb = b_base + s * C::B_STAGE_BYTES;
+        if (!p.a_mn) {
+          tma_load_2d(sa, &p.tmA, k0, m0, full_bar(s));
+        } else {
+          tma_load_2d(sa, &p.tmA, m0, k0, full_bar(s));
+          tma_load_2d(sa + 8192, &p.tmA, m0 + 64, k0, full_bar(s));
+        }
+        if (!p.b_mn) {
+          tma_load_2d(sb, &p.tmB, k0, n0, full_bar(s));
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + 8192 * c, &p.tmB, n0 + 64 * c, k0, full_bar(s));
+        }
+        ++issued;
+      }
+      // Drain: every issued copy must land before the CTA may exit.
+      for (int i = max(0, issued - C::STAGES); i < issued; ++i)
+        mbar_wait(full_bar(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u, p.err);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      // K advance per 16-deep MMA: K-major -> 32 bytes inside the swizzle
+      // row; MN-major -> 16 rows of 128 bytes.
+      const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
+      const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % C::STAGES;
+        const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
+        if (!mbar_wait(full_bar(s), ph, p.err)) break;
+        tc_fence_after();
+        const uint32_t sa = a_base + s * A_STAGE_BYTES;
+        const uint32_t sb = b_base + s * C::B_STAGE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          uint64_t ad = sdesc(sa + kk * a_kstep, a_lbo, 1024);
+          uint64_t bd = sdesc(sb + kk * b_kstep, b_lbo, 1024);
+          mma_bf16(tmem, ad, bd, p.idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(empty_bar(s));
+      }
+      // Always signal the epilogue (also after an early exit) once every
+      // issued MMA has completed.
+      mma_commit(acc_bar);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int row_in_tile = q * 32 + lane;
+    const int gm = m0 + row_in_tile;
+    bool ok = true;
+    if (do_db) {
+      // db[m] = sum over this split's K range of A(m, k) = dY[k, m]; A is
+      // MN-major: two 64(m) x 64(k) boxes, 128-byte rows, 128B swizzle.
+      float colsum = 0.f;
+      const int t = threadIdx.x - 64;       // 0..127 -> m within the tile
+      const int box = t >> 6, mi = t & 63;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % C::STAGES;
+        const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
+        ok = __all_sync(0xffffffffu, mbar_wait(full_bar(s), ph, p.err));
+        if (!ok) break;
+        const uint8_t* tile = base_ptr + (a_base - base) + s * A_STAGE_BYTES + box * 8192;
+#pragma unroll 8
+        for (int r = 0; r < BK; ++r) {
+          const int off = r * 128 + ((((mi >> 3) ^ (r & 7))) << 4) + ((mi & 7) << 1);
+          colsum += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + off));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+      }
+      const int m = m0 + t;
+      if (ok && m < p.M) {
+        if (p.ws) p.ws[(int64_t)gridDim.z * p.M * p.N + (int64_t)blockIdx.z * p.M + m] = colsum;
+        else p.db[m] = colsum;
+      }
+    }
+    ok = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0, p.err) && ok);
+    tc_fence_after();
+    if (ok && nkb > 0) {
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(trow + c0, v);
+        const int gn0 = n0 + c0;
+        if (gm >= p.M || gn0 >= p.N) continue;
+        const bool full = gn0 + 16 <= p.N;
+        if (p.kind == GEMM_WGRAD) {
+          float* dst = p.ws ? p.ws + ((int64_t)blockIdx.z * p.M + gm) * p.N + gn0
+                            : p.dW + (int64_t)gm * p.ld_dw + gn0;
+          const bool vec = full && (((uintptr_t)dst & 15) == 0);
+          if (vec) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          } else {
+            for (int j = 0; j < 16 && gn0 + j < p.N; ++j) dst[j] = v[j];
+          }
+          continue;
+        }
+        float o[16];
+        if (p.kind == GEMM_FWD) {
+          float u[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int gn = gn0 + j;
+            u[j] = v[j] + (gn < p.N ? __ldg(p.bias + gn) : 0.f);
+            o[j] = apply_act(u[j], p.act);
+          }
+          if (p.out_u) {
+            __nv_bfloat16* du = p.out_u + (int64_t)gm * p.ldu + gn0;
+            if (full && (((uintptr_t)du & 15) == 0)) {
+              __align__(16) __nv_bfloat16 tmp[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) tmp[j] = __float2bfloat16_rn(u[j]);
+              reinterpret_cast<uint4*>(du)[0] = reinterpret_cast<uint4*>(tmp)[0];
+              reinterpret_cast<uint4*>(du)[1] = reinterpret_cast<uint4*>(tmp)[1];
+            } else {
+              for (int j = 0; j < 16 && gn0 + j < p.N; ++j) du[j] = __float2bfloat16_rn(u[j]);
+            }
+          }
+        } else {  // GEMM_DGRAD
+          const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
+          if (p.act == ACT_NONE) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = v[j];
+          } else if (full && (((uintptr_t)ar & 15) == 0)) {
+            __align__(16) __nv_bfloat16 tmp[16];
+            reinterpret_cast<uint4*>(tmp)[0] = __ldg(reinterpret_cast<const uint4*>(ar));
+            reinterpret_cast<uint4*>(tmp)[1] = __ldg(reinterpret_cast<const uint4*>(ar) + 1);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = v[j] * act_grad_from_stored(__bfloat162float(tmp[j]), p.act);
+          } else {
+            for (int j = 0; j < 16; ++j)
+              o[j] = gn0 + j < p.N ? v[j] * act_grad_from_stored(__bfloat162float(ar[j]), p.act) : 0.f;
+          }
+        }
+        __nv_bfloat16* dst = p.out + (int64_t)gm * p.ldo + gn0;
+        if (full && (((uintptr_t)dst & 15) == 0)) {
+          __align__(16) __nv_bfloat16 tmp[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) tmp[j] = __float2bfloat16_rn(o[j]);
+          reinterpret_cast<uint4*>(dst)[0] = reinterpret_cast<uint4*>(tmp)[0];
+          reinterpret_cast<uint4*>(dst)[1] = reinterpret_cast<uint4*>(tmp)[1];
+        } else {
+          for (int j = 0; j < 16 && gn0 + j < p.N; ++j) dst[j] = __float2bfloat16_rn(o[j]);
+        }
+      }
+    }
+    if (ok && nkb == 0 && gm < p.M) {
+      // Empty K range (only possible for a trailing split): contribute zeros.
+      for (int gn = n0; gn < min(n0 + BN, p.N); ++gn) {
+        if (p.kind == GEMM_WGRAD) {
+          if (p.ws) p.ws[((int64_t)blockIdx.z * p.M + gm) * p.N + gn] = 0.f;
+          else p.dW[(int64_t)gm * p.ld_dw + gn] = 0.f;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map: inner extent `inner` (contiguous), outer extent
+// `outer` with row pitch `ld` elements; box {box_inner, box_outer}; 128B
+// swizzle; out-of-range elements read as zero.
+bool make_tmap(CUtensorMap* tm, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int box_inner,
+               int box_outer, char* err, size_t errlen) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) { snprintf(err, errlen, "cuTensorMapEncodeTiled unavailable"); return false; }
+  if (((uintptr_t)ptr & 15) || ((ld * 2) & 15)) {
+    snprintf(err, errlen, "TMA operand needs a 16-byte aligned base and row pitch (ld=%lld)", (long long)ld);
+    return false;
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, errlen, "cuTensorMapEncodeTiled failed (%d) inner=%lld outer=%lld ld=%lld box=%dx%d", (int)r,
+             (long long)inner, (long long)outer, (long long)ld, box_inner, box_outer);
+    return false;
+  }
+  return true;
+}
+
+template <int BN>
+const void* tc_kernel_ptr() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute((const void*)tc::tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         tc::Cfg<BN>::SMEM_BYTES);
+  });
+  return (const void*)tc::tc_gemm_kernel<BN>;
+}
+
+constexpr int kSMs = 152;
+
+int pick_bn(const GemmOp& op) {
+  if (op.kind == GEMM_WGRAD) return 128;
+  if (op.N <= 16 && !(!op.b_kmajor)) return 16;
+  if (op.N >= 4096) return 256;
+  return 128;
+}
+
+}  // namespace
+
+int tc_wgrad_splits(int64_t M, int64_t N, int64_t K) {
+  const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, 128);
+  const int64_t kbs = ceil_div(K, tc::BK);
+  int64_t s = 1;
+  while (tiles * s < kSMs && kbs / (s * 2) >= 8) s *= 2;
+  return (int)s;
+}
+
+int wgrad_splits(int dtype, int64_t M, int64_t N, int64_t K) {
+  return dtype == DT_F32 ? simt_gemm_splits(M, N, K) : tc_wgrad_splits(M, N, K);
+}
+
+size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int splits) {
+  (void)dtype; (void)K;
+  if (splits <= 1) return 0;
+  return (size_t)splits * (size_t)(M * N + M) * sizeof(float);
+}
+
+int tc_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
+  if (op.dtype != DT_BF16) { snprintf(err, errlen, "tensor-core GEMM is bf16 only"); return -1; }
+  if (op.M <= 0 || op.N <= 0 || op.K <= 0 || op.M > INT32_MAX || op.N > INT32_MAX || op.K > INT32_MAX) {
+    snprintf(err, errlen, "bad GEMM shape %lld x %lld x %lld", (long long)op.M, (long long)op.N, (long long)op.K);
+    return -1;
+  }
+  const int BN = pick_bn(op);
+  if (!op.b_kmajor && BN % 64) { snprintf(err, errlen, "MN-major B needs BN %% 64 == 0"); return -1; }
+  tc::Params p;
+  memset(&p, 0, sizeof(p));
+  // A operand: K-major [M rows, K] or MN-major [K rows, M].
+  if (op.a_kmajor) {
+    if (!make_tmap(&p.tmA, op.A, op.K, op.M, op.lda, 64, 128, err, errlen)) return -1;
+  } else {
+    if (!make_tmap(&p.tmA, op.A, op.M, op.K, op.lda, 64, 64, err, errlen)) return -1;
+  }
+  if (op.b_kmajor) {
+    if (!make_tmap(&p.tmB, op.B, op.K, op.N, op.ldb, 64, BN, err, errlen)) return -1;
+  } else {
+    if (!make_tmap(&p.tmB, op.B, op.N, op.K, op.ldb, 64, 64, err, errlen)) return -1;
+  }
+  p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
+  p.num_kb = (int)ceil_div(op.K, tc::BK);
+  p.a_mn = op.a_kmajor ? 0 : 1;
+  p.b_mn = op.b_kmajor ? 0 : 1;
+  p.kind = op.kind; p.act = op.act;
+  p.idesc = (1u << 4)                       // D: f32
+          | (1u << 7) | (1u << 10)          // A, B: bf16
+          | ((uint32_t)p.a_mn << 15) | ((uint32_t)p.b_mn << 16)
+          | ((uint32_t)(BN >> 3) << 17)
+          | ((uint32_t)(tc::BM >> 4) << 24);
+  p.bias = op.bias;
+  p.out = (__nv_bfloat16*)op.out; p.ldo = op.ldo;
+  p.out_u = (__nv_bfloat16*)op.out_u; p.ldu = op.ldu;
+  p.aux = (const __nv_bfloat16*)op.aux; p.ld_aux = op.ld_aux;
+  p.dW = op.dW; p.ld_dw = op.ld_dw;
+  p.db = op.db;
+  p.err = op.err;
+  int splits = 1;
+  if (op.kind == GEMM_WGRAD) {
+    splits = op.splits > 0 ? op.splits : tc_wgrad_splits(op.M, op.N, op.K);
+    if (splits > p.num_kb) splits = p.num_kb;
+  }
+  p.kb_per_split = (int)ceil_div(p.num_kb, splits);
+  splits = (int)ceil_div(p.num_kb, p.kb_per_split);
+  if (splits > 1) {
+    size_t need = wgrad_workspace_bytes(DT_BF16, op.M, op.N, op.K, splits);
+    if (!op.ws || op.ws_bytes < need) {
+      snprintf(err, errlen, "wgrad workspace too small (%zu < %zu)", op.ws_bytes, need);
+      return -1;
+    }
+    p.ws = op.ws;
+  }
+  LaunchRec& r = recs[0];
+  switch (BN) {
+    case 16: r.func = tc_kernel_ptr<16>(); r.smem = tc::Cfg<16>::SMEM_BYTES; break;
+    case 128: r.func = tc_kernel_ptr<128>(); r.smem = tc::Cfg<128>::SMEM_BYTES; break;
+    default: r.func = tc_kernel_ptr<256>(); r.smem = tc::Cfg<256>::SMEM_BYTES; break;
+  }
+  r.grid = dim3((unsigned)ceil_div(op.N, BN), (unsigned)ceil_div(op.M, tc::BM), (unsigned)splits);
+  r.block = dim3(tc::NUM_THREADS);
+  r.name = op.kind == GEMM_FWD ? "tc_gemm_fwd" : op.kind == GEMM_DGRAD ? "tc_gemm_dgrad" : "tc_gemm_wgrad";
+  r.set_args(p);
+  if (splits > 1) {
+    split_reduce_plan(op.ws, splits, op.M, op.N, op.dW, op.ld_dw, op.db, &recs[1]);
+    return 2;
+  }
+  return 1;
+}
+
+int gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
+  return op.dtype == DT_F32 ? simt_gemm_plan(op, recs, err, errlen) : tc_gemm_plan(op, recs, err, errlen);
+}
+
+}  // namespace mlpk

@@ -1,0 +1,73 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/*.h declares, sizes arenas, rejects
+bad shapes, and refuses to compute without a GPU (no CPU fallback)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import neural_net_step_gb300 as nn
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from neural_net_step_gb300 import build
+    build.build()
+    return nn.lib()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", f)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(mlp_\w+)\s*\(", txt))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 20
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+        assert n in nn._SIGS, f"{n} has no Python binding"
+
+
+def test_arena_bytes_for_every_workload(lib):
+    for name in synth.WORKLOAD_ORDER:
+        w = synth.WORKLOADS[name]
+        n = nn.mlp_arena_bytes(list(w.dims), list(w.acts), nn.ACT_RELU, w.dtype, w.batch)
+        es = 4 if w.dtype == synth.F32 else 2
+        # at least the four fp32 planes and the activations of the forward
+        acts = sum(w.batch * d * es for d in w.dims[1:])
+        assert n >= 16 * w.n_params() + acts
+        assert n % 256 == 0
+
+
+@pytest.mark.parametrize("dims,dtype", [([784], 0), ([100, 20, 10], 1), ([8, 0, 4], 0)])
+def test_bad_shapes_rejected(lib, dims, dtype):
+    with pytest.raises(nn.MlpError):
+        nn.mlp_arena_bytes(dims, None, nn.ACT_RELU, dtype, 4)
+
+
+def test_bad_dtype_and_activation_rejected(lib):
+    with pytest.raises(nn.MlpError):
+        nn.mlp_arena_bytes([8, 8, 4], None, nn.ACT_RELU, 7, 4)
+    with pytest.raises(nn.MlpError):
+        nn.mlp_arena_bytes([8, 8, 4], [9], nn.ACT_RELU, 0, 4)
+
+
+def test_no_gpu_means_no_compute(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    dims = (ctypes.c_int64 * 3)(8, 8, 4)
+    st = lib.mlp_create(dims, 3, None, 1, 0, 0, 4, ctypes.c_void_p(256), 1 << 20, 0, ctypes.byref(h))
+    assert st != 0 and not h.value
+    assert nn.mlp_last_error()

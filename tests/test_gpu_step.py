@@ -1,0 +1,223 @@
+"""Whole-step parity: mlp_train_step / mlp_train_steps / mlp_forward through
+the C ABI against the CPU oracle on the same seeded batches and initial
+parameters (drawn by synth, written into the model), plus closed forms and
+properties that hold at the full sizes of the five workloads."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import neural_net_step_gb300 as nn
+import synth
+from oracle import mlp_oracle as om
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+W = synth.WORKLOADS
+
+
+def make_model(w: synth.Workload, batch=None, params=None, graph=True):
+    B = w.batch if batch is None else batch
+    m = nn.Model(w.dims, w.acts, nn.ACT_RELU, w.dtype, seed=w.seed, batch=B)
+    m.set_graph_mode(graph)
+    if params is not None:
+        m.write_flat(P.flat([p.numpy() for p in params]).astype(np.float32), nn.PLANE_P, 0)
+    return m
+
+
+def gpu_run(m: nn.Model, w: synth.Workload, bl, one_graph=False):
+    xs = [x.to(DEV) for x, _ in bl]
+    ys = [y.to(DEV) for _, y in bl]
+    hyper = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, wd=w.wd)
+    if one_graph:
+        losses = m.train_steps(xs, ys, **hyper)
+    else:
+        losses = torch.empty(len(bl), dtype=torch.float32, device=DEV)
+        for i in range(len(bl)):
+            m.train_step(xs[i], ys[i], loss=losses[i], **hyper)
+    m.check_errors()
+    p, step = m.read_flat(nn.PLANE_P)
+    assert step == len(bl)
+    return losses.cpu().numpy().astype(np.float64), m.split(p.astype(np.float64))
+
+
+def check_trajectory(w: synth.Workload, n_steps: int, batch=None, one_graph=False):
+    B = w.batch if batch is None else batch
+    params0 = synth.make_params(w)
+    bl = P.batches(w, n_steps, B)
+    m = make_model(w, B, params0)
+    g_losses, g_params = gpu_run(m, w, bl, one_graph)
+    p0 = [P.to64(p) for p in params0]
+    if w.dtype == synth.F32:
+        o_losses, o_params, *_ = P.oracle_run(w, params0, bl, "fp64")
+        rel = np.abs(g_losses - o_losses) / np.abs(o_losses)
+        assert rel.max() <= 1e-4, (rel.max(), g_losses, o_losses)
+        errs = [P.f32_param_error(g, o, w.lr) for g, o in zip(g_params, o_params)]
+        assert max(errs) <= 1e-4, errs
+    else:
+        e_losses, *_ = P.oracle_run(w, params0, bl, "bf16")
+        m_losses, m_params, *_ = P.oracle_run(w, params0, bl, "bf16_mirror")
+        rel = np.abs(g_losses - np.array(e_losses)) / np.abs(e_losses)
+        assert rel.max() <= 2e-2, (rel.max(), g_losses, e_losses)
+        relm = np.abs(g_losses - np.array(m_losses)) / np.abs(m_losses)
+        assert relm.max() <= 1e-3, (relm.max(), g_losses, m_losses)
+        errs = P.bf16_param_errors(g_params, m_params, p0)
+        assert max(errs) <= 3e-2, errs
+    m.close()
+
+
+# --------------------------------------------------------------------------
+# Trajectories: element-by-element against the oracle
+# --------------------------------------------------------------------------
+def test_mnist_mlp_b64_one_step():
+    check_trajectory(W["mnist_mlp_b64"], 1)
+
+
+def test_mnist_mlp_b64_eager_matches():
+    check_trajectory(W["mnist_mlp_b64"], 3)
+
+
+@pytest.mark.slow
+def test_mnist_mlp_b4096_100_steps():
+    w = W["mnist_mlp_b4096"]
+    check_trajectory(w, w.steps)
+
+
+def test_mnist_mlp_ragged_batch():
+    check_trajectory(W["mnist_mlp_b64"], 2, batch=333)
+
+
+def test_cifar_mlp_reduced_batch():
+    check_trajectory(W["cifar_mlp_b8192"], 3, batch=320)
+
+
+def test_lm_block_reduced_batch():
+    check_trajectory(W["lm_block_t16384"], 2, batch=200)
+
+
+def test_deep_narrow_reduced_batch_one_graph():
+    check_trajectory(W["deep_narrow_b65536"], 4, batch=300, one_graph=True)
+
+
+# --------------------------------------------------------------------------
+# Full-size closed form: all-zero parameters
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
+def test_zero_params_closed_form_full_size(name):
+    """W = b = 0 => h = 0, z = 0, loss = ln C; only the last bias has a
+    gradient, db_c = 1/C - n_c/B, so after one AdamW step
+    b_c = -lr g/(|g| + eps) and every other parameter stays exactly 0.
+    This pins label indexing, CE, the fused bias-gradient and AdamW end to end
+    at the workload's full size and launch configuration."""
+    w = W[name]
+    m = make_model(w)
+    m.write_flat(np.zeros(m.n_params, np.float32), nn.PLANE_P, 0)
+    x, y = synth.make_batch(w, 0)
+    loss = m.train_step(x.to(DEV), y.to(DEV), w.lr, w.beta1, w.beta2, w.eps, w.wd)
+    m.check_errors()
+    C = w.n_classes
+    assert abs(loss.item() - math.log(C)) <= 1e-6 * math.log(C)
+    p, _ = m.read_flat(nn.PLANE_P)
+    parts = m.split(p)
+    for t in parts[:-1]:
+        assert np.all(t == 0)
+    n_c = np.bincount(y.numpy(), minlength=C)
+    g = 1.0 / C - n_c / w.batch
+    want = -w.lr * g / (np.abs(g) + w.eps)
+    np.testing.assert_allclose(parts[-1], want, rtol=1e-3, atol=1e-3 * w.lr)
+    m.close()
+
+
+# --------------------------------------------------------------------------
+# Full-size sampled forward: logits of sampled rows against the oracle
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
+def test_forward_sampled_rows_full_size(name):
+    w = W[name]
+    params0 = synth.make_params(w)
+    m = make_model(w, params=params0)
+    x, _ = synth.make_batch(w, 0)
+    logits, am = m.forward(x.to(DEV))
+    torch.cuda.synchronize()
+    rows = np.unique(np.random.default_rng(7).integers(0, w.batch, 24))
+    rows = np.concatenate([rows, [0, w.batch - 1]])
+    p64 = [P.to64(p) for p in params0]
+    mode = P.oracle_mode(w, exact=False)
+    fw = om.forward(p64, P.to64(x[rows]), w.acts, mode)
+    z_ref = fw["z"]
+    z = P.to64(logits[rows])
+    scale = np.max(np.abs(z_ref), axis=1, keepdims=True)
+    tol = 1e-4 if w.dtype == synth.F32 else 3e-2
+    assert np.all(np.abs(z - z_ref) <= tol * scale), np.max(np.abs(z - z_ref) / scale)
+    # argmax: exact wherever the oracle's top-2 gap exceeds the tolerance
+    amr = om.argmax_rows(z_ref)
+    s = np.sort(z_ref, axis=1)
+    gap = s[:, -1] - s[:, -2] if z_ref.shape[1] > 1 else np.full(len(rows), np.inf)
+    clear = gap > 2 * tol * scale[:, 0]
+    assert np.array_equal(am.cpu().numpy()[rows][clear], amr[clear])
+    # and always consistent with the GPU's own logits (lowest index on ties)
+    assert np.array_equal(am.cpu().numpy(), np.argmax(P.to64(logits), axis=1))
+    m.close()
+
+
+# --------------------------------------------------------------------------
+# Determinism, graph vs eager, error reporting
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["mnist_mlp_b4096", "cifar_mlp_b8192"])
+def test_bitwise_deterministic_and_graph_equals_eager(name):
+    w = W[name]
+    params0 = synth.make_params(w)
+    bl = P.batches(w, 2)
+    res = []
+    for graph in (True, True, False):
+        m = make_model(w, params=params0, graph=graph)
+        losses, _ = gpu_run(m, w, bl)
+        p, _ = m.read_flat(nn.PLANE_P)
+        res.append((losses, p))
+        m.close()
+    for l_, p_ in res[1:]:
+        assert np.array_equal(l_, res[0][0])
+        assert np.array_equal(p_, res[0][1])
+
+
+def test_label_out_of_range_reported():
+    w = W["mnist_mlp_b64"]
+    m = make_model(w)
+    x, y = synth.make_batch(w, 0)
+    y[5] = 10
+    m.train_step(x.to(DEV), y.to(DEV), w.lr)
+    with pytest.raises(nn.MlpError) as e:
+        m.check_errors()
+    assert e.value.status == 5
+    m.check_errors()   # cleared
+    m.close()
+
+
+def test_kaiming_init_statistics():
+    w = W["cifar_mlp_b8192"]
+    m = make_model(w)
+    p, step = m.read_flat(nn.PLANE_P)
+    assert step == 0
+    parts = m.split(p)
+    for l in range(w.n_layers):
+        Wl, bl = parts[2 * l], parts[2 * l + 1]
+        std = math.sqrt(2.0 / w.dims[l])
+        assert abs(Wl.std() / std - 1) < 0.02 + 3 / math.sqrt(Wl.size)
+        assert abs(Wl.mean()) < 5 * std / math.sqrt(Wl.size)
+        assert np.all(bl == 0)
+    m.close()
+
+
+def test_shape_mismatch_and_bad_args_fail_before_enqueue():
+    with pytest.raises(nn.MlpError):
+        nn.Model([100, 20, 10], None, nn.ACT_RELU, nn.BF16, batch=8)    # 100 % 8 != 0 in bf16
+    w = W["mnist_mlp_b64"]
+    m = make_model(w)
+    x, y = synth.make_batch(w, 0)
+    with pytest.raises(nn.MlpError):
+        nn.mlp_train_step(m.h, x.to(DEV).data_ptr(), y.to(DEV).data_ptr(), -1.0, 0.9, 0.999, 1e-8, 0.0, None,
+                          0)
+    m.close()
