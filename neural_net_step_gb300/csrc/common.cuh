@@ -20,19 +20,28 @@ enum : uint32_t {
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
-// tanh-form GELU and its derivative (Hendrycks & Gimpel); tanhf from CUDA.
-__device__ __forceinline__ float gelu_tanh(float u) {
+// tanh-form GELU (Hendrycks & Gimpel): gelu(u) = 0.5 u (1 + tanh(a)),
+// a = sqrt(2/pi) (u + 0.044715 u^3).  Evaluated through the identities
+// 1 + tanh(a) = 2 s and 1 - tanh(a)^2 = 4 s (1 - s), s = 1 / (1 + e^{-2a}),
+// 1 - s = 1 / (1 + e^{2a}), which keep fp32 relative accuracy in both tails
+// (1 + tanh(a) computed directly cancels to 0 for very negative u).
+__device__ __forceinline__ void gelu_parts(float u, float& s, float& sm, float& dinner) {
   const float k0 = 0.7978845608028654f;   // sqrt(2/pi)
   const float k1 = 0.044715f;
-  float t = tanhf(k0 * (u + k1 * u * u * u));
-  return 0.5f * u * (1.0f + t);
+  const float a = k0 * (u + k1 * u * u * u);
+  s = 1.0f / (1.0f + expf(-2.0f * a));
+  sm = 1.0f / (1.0f + expf(2.0f * a));
+  dinner = k0 * (1.0f + 3.0f * k1 * u * u);
+}
+__device__ __forceinline__ float gelu_tanh(float u) {
+  float s, sm, d;
+  gelu_parts(u, s, sm, d);
+  return u * s;
 }
 __device__ __forceinline__ float gelu_tanh_grad(float u) {
-  const float k0 = 0.7978845608028654f;
-  const float k1 = 0.044715f;
-  float t = tanhf(k0 * (u + k1 * u * u * u));
-  float dinner = k0 * (1.0f + 3.0f * k1 * u * u);
-  return 0.5f * (1.0f + t) + 0.5f * u * (1.0f - t * t) * dinner;
+  float s, sm, d;
+  gelu_parts(u, s, sm, d);
+  return s + 2.0f * u * s * sm * d;
 }
 __device__ __forceinline__ float apply_act(float v, int act) {
   if (act == ACT_RELU) return fmaxf(v, 0.0f);

@@ -109,6 +109,21 @@ def linear(X: np.ndarray, W: np.ndarray, b: np.ndarray) -> np.ndarray:
     return X @ W.T + b[None, :]
 
 
+def weight_grad(dY: np.ndarray, X: np.ndarray) -> np.ndarray:
+    """dW = dY^T X: the VJP of u = X W^T + b with respect to W."""
+    return dY.T @ X
+
+
+def input_grad(dY: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """dX = dY W: the VJP of u = X W^T + b with respect to X."""
+    return dY @ W
+
+
+def bias_grad(dY: np.ndarray) -> np.ndarray:
+    """db = sum over rows of dY: the VJP of u = X W^T + b with respect to b."""
+    return dY.sum(axis=0)
+
+
 def softmax_ce(z: np.ndarray, y: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     """Per-row loss l_i = logsumexp(z_i) - z_i[y_i] and dz = (softmax(z) -
     onehot(y)) / B, the gradient of the batch-mean loss."""
@@ -190,10 +205,10 @@ def backward(fw: Dict[str, list], dz: np.ndarray, acts: Sequence[int],
     dY = _round(dz, mirror)
     for l in range(L - 1, -1, -1):
         X = fw["X"][l]
-        grads[2 * l] = dY.T @ X
-        grads[2 * l + 1] = dY.sum(axis=0)
+        grads[2 * l] = weight_grad(dY, X)
+        grads[2 * l + 1] = bias_grad(dY)
         if l > 0:
-            dX = dY @ fw["W"][l]
+            dX = input_grad(dY, fw["W"][l])
             act = acts[l - 1]
             if act == ACT_RELU:
                 d = dX * (fw["X"][l] > 0)            # mask from the stored h
