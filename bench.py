@@ -1,0 +1,466 @@
+"""Benchmark of the GB300 MLP training step (one JSON line on rank 0).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole hot path -- LinearAct forward GEMMs,
+softmax-CE forward+backward, loss mean, wgrad (+ fused bias gradient) and
+dgrad (+ fused activation VJP) GEMMs, one flat AdamW update -- over one batch
+of synthetic data, launched as one CUDA-graph replay through the C ABI.
+Default workload: the 784-256-128-10 ReLU MLP in fp32 at batch 4096.
+
+Timing: W untimed warm-up steps, then K steps between CUDA events on the
+launching stream, bracketed by a barrier and a device synchronize; the step
+reads a fresh batch each time from a device-resident pool larger than L2
+(129 MB), so no step finds its input in L2.  Under torchrun every rank runs
+an independent replica of the step on its own GPU (the path is replicated,
+not sharded, here) and the slowest rank's time counts.
+
+Also reported: `e2e` (the same metric through the C ABI with pinned host
+buffers: every step copies its batch host->device and reads the loss back),
+`roofline` for the kernel with the largest device time (per-kernel times
+from the library's serialised profiling pass, mlp_profile_step), a
+per-kernel table, `cpu_baseline` (the CPU oracle timed on a bounded sample
+of the same workload on this host), and SM clocks sampled during the timed
+region.  `--impl reference` times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "train samples/sec per MLP step (fwd+bwd+AdamW), 1 GB300; % of step roofline"
+L2_BYTES = 129 * 1024 * 1024
+SMS, FP32_LANES, SM_MAX_GHZ = 152, 128, 2.07
+FP32_FFMA_PEAK_TFLOPS = SMS * FP32_LANES * 2 * SM_MAX_GHZ / 1e3   # 80.5 TFLOP/s, derived
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work of each kernel of the step (the order the library plans it)
+# ---------------------------------------------------------------------------
+def step_work(w):
+    """[(kind, layer, flops, bytes)] in launch order, without split-K reduces."""
+    B, es = w.batch, (4 if w.dtype == 0 else 2)
+    L, d = w.n_layers, w.dims
+    out = []
+    for l in range(L):
+        K, N = d[l], d[l + 1]
+        gelu_u = es * B * N if (l < L - 1 and w.acts[l] == 2) else 0
+        out.append(("fwd", l, 2 * B * K * N, es * (B * K + N * K + B * N) + 4 * N + gelu_u))
+    C = d[L]
+    out.append(("ce", -1, 0, 2 * es * B * C + 8 * B))
+    out.append(("loss_mean", -1, 0, 4 * B))
+    for l in range(L - 1, -1, -1):
+        K, N = d[l], d[l + 1]
+        out.append(("wgrad", l, 2 * B * K * N, es * (B * N + B * K) + 4 * (N * K + N)))
+        if l > 0:
+            out.append(("dgrad", l, 2 * B * K * N, es * (B * N + N * K + 2 * B * K)))
+    out.append(("adamw", -1, 0, w.n_params() * (28 + (2 if w.dtype == 1 else 0))))
+    return out
+
+
+def attach_work(w, prof):
+    """Pair the profiled launches with the algorithmic work list."""
+    work = step_work(w)
+    rows, wi = [], 0
+    for name, ms in prof:
+        if name == "split_reduce":
+            rows.append({"kernel": name, "layer": rows[-1]["layer"], "ms": ms, "flops": 0, "bytes": 0})
+            continue
+        kind, layer, fl, by = work[wi]
+        wi += 1
+        rows.append({"kernel": name, "kind": kind, "layer": layer, "ms": ms, "flops": fl, "bytes": by})
+    assert wi == len(work), (wi, len(work), [p[0] for p in prof])
+    return rows
+
+
+def roofline_rows(w, rows, peaks):
+    """Per kernel: bound, achieved, peak, fraction; and the step roofline."""
+    t_roof = 0.0
+    for r in rows:
+        sec = max(r["ms"], 1e-9) / 1e3
+        if r["flops"]:
+            if w.dtype == 0:
+                bound, peak, unit = "alu", FP32_FFMA_PEAK_TFLOPS, "TFLOP/s"
+            else:
+                bound, peak, unit = "tensor", peaks["bf16_tflops"], "TFLOP/s"
+            ach = r["flops"] / sec / 1e12
+            t = max(r["flops"] / (peak * 1e12), r["bytes"] / (peaks["hbm_gbs"] * 1e9))
+        else:
+            bound, peak, unit = "hbm", peaks["hbm_gbs"], "GB/s"
+            ach = r["bytes"] / sec / 1e9
+            t = r["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        r.update(bound=bound, achieved=ach, peak=peak, unit=unit, frac=ach / peak, t_roof_ms=t * 1e3)
+        t_roof += t
+    return t_roof * 1e3
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "neural_net_step_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, or None when absent or when the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("source_hash") != source_hash():
+        return None
+    return t.get("kernels", {}).get(f"{workload}:{kernel}")
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.file:
+            return None
+        try:
+            with open(self.file.name) as f:
+                lines = [l.strip().split(",") for l in f if l.strip()]
+            os.unlink(self.file.name)
+        except Exception:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in lines:
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+                for n, v in zip(names, p[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except Exception:
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample_rows(w, budget_s=1.0):
+    """Rows per oracle step so that one step costs about budget_s of CPU
+    (fp64 at an assumed ~50 GFLOP/s, refined by measurement)."""
+    flops_per_row = w.gemm_flops() / w.batch
+    return int(max(64, min(w.batch, budget_s * 50e9 / flops_per_row)))
+
+
+class OracleRunner:
+    """The CPU oracle, as it stands, stepping on a bounded row sample."""
+
+    def __init__(self, w):
+        import numpy as np
+        import synth
+        from oracle import mlp_oracle as om
+        self.np, self.om, self.w = np, om, w
+        self.rows = oracle_sample_rows(w)
+        self.params = [p.numpy().astype(np.float64) for p in synth.make_params(w)]
+        self.m = [np.zeros_like(p) for p in self.params]
+        self.v = [np.zeros_like(p) for p in self.params]
+        self.mode = "fp64" if w.dtype == 0 else "bf16_mirror"
+        self.hyper = tuple(float(np.float32(a)) for a in (w.lr, w.beta1, w.beta2, w.eps, w.wd))
+        self.batches = []
+        for s in range(4):
+            x, y = synth.make_batch(w, s)
+            self.batches.append((x[:self.rows].float().numpy().astype(np.float64),
+                                 y[:self.rows].numpy().astype(np.int64)))
+        self.t = 0
+
+    def step(self) -> float:
+        x, y = self.batches[self.t % 4]
+        t0 = time.perf_counter()
+        _, self.params, self.m, self.v, _, _ = self.om.train_step(self.params, self.m, self.v, self.t + 1, x, y,
+                                                                  self.w.acts, *self.hyper, mode=self.mode)
+        self.t += 1
+        return time.perf_counter() - t0
+
+    def sample(self) -> str:
+        return (f"oracle steps (numpy fp64, {self.mode} mode) on {self.rows} of {self.w.batch} rows of the "
+                f"{self.w.name} workload; OpenBLAS threads = host cores")
+
+
+def time_oracle(w, target_s=10.0):
+    r = OracleRunner(w)
+    el, steps = 0.0, 0
+    while el < target_s:
+        el += r.step()
+        steps += 1
+    return {"value": r.rows * steps / el, "unit": "samples/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{steps} " + r.sample()}
+
+
+# ---------------------------------------------------------------------------
+# Main
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    r = OracleRunner(w)
+    for _ in range(args.warmup):
+        r.step()
+    t_all = sum(r.step() for _ in range(args.steps))
+    value = r.rows * args.steps / t_all
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "samples/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t_all / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": {"value": round(value, 2), "unit": "samples/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": f"each step: one of {args.steps} " + r.sample()},
+            "e2e": {"value": round(value, 2), "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(w, extra=None):
+    c = {"workload": f"{w.name}: MLP {'-'.join(map(str, w.dims))}, "
+                     f"{'fp32' if w.dtype == 0 else 'bf16 + fp32 master'}, batch {w.batch}",
+         "dims": list(w.dims), "acts": [["none", "relu", "gelu_tanh"][a] for a in w.acts], "global_batch": w.batch,
+         "optimizer": f"AdamW lr={w.lr} betas=({w.beta1},{w.beta2}) eps={w.eps} wd={w.wd}",
+         "parallelism": "replicas"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mnist_mlp_b4096")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernels", action="store_true", help="include the per-kernel table")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import synth
+    w = synth.WORKLOADS[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+
+    import torch
+    import neural_net_step_gb300 as nn
+    from neural_net_step_gb300 import build as nbuild
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    if not os.path.exists(nn.LIB_PATH):
+        nbuild.build()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+        pg = dist
+
+    peaks = load_peaks()
+    model = nn.Model(w.dims, w.acts, nn.ACT_RELU, w.dtype, seed=w.seed + rank, batch=w.batch, device=local)
+    hyper = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, wd=w.wd)
+
+    # device-resident batch pool larger than L2
+    x0, y0 = synth.make_batch(w, 0)
+    per = x0.numel() * x0.element_size() + y0.numel() * 4
+    n_pool = max(4, min(64, math.ceil(1.5 * L2_BYTES / per)))
+    n_gen = min(n_pool, 8)
+    gen = [synth.make_batch(w, s + 1000 * rank) for s in range(n_gen)]
+    xs, ys = [], []
+    for i in range(n_pool):
+        x, y = gen[i % n_gen]
+        if i >= n_gen:   # distinct bytes for every pool slot: roll the rows
+            x, y = torch.roll(x, i, 0), torch.roll(y, i, 0)
+        xs.append(x.to(dev))
+        ys.append(y.to(dev))
+    stream = torch.cuda.current_stream()
+    losses = torch.empty(args.steps + args.warmup, dtype=torch.float32, device=dev)
+
+    def step(i, loss_slot):
+        model.train_step(xs[i % n_pool], ys[i % n_pool], loss=loss_slot, **hyper)
+
+    for i in range(args.warmup):
+        step(i, losses[i])
+    model.check_errors()
+    torch.cuda.synchronize()
+
+    # ---- timed region (clocks sampled from ~1 s before it, under the same
+    # continuous load, until it ends) ----
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_end = time.perf_counter() + 1.0
+        i = 0
+        while time.perf_counter() < t_end:
+            step(i, losses[i % args.warmup])
+            i += 1
+            if i % 16 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, losses[args.warmup + i])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms = ev0.elapsed_time(ev1)
+    model.check_errors()
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = w.batch * world * args.steps / (ms / 1e3)
+    kernels_per_step = model.kernels_per_step()
+    clocks = clk.summary()
+
+    # ---- end to end through the C ABI with pinned host buffers ----
+    hx = [gen[i % n_gen][0].pin_memory() for i in range(n_gen)]
+    hy = [gen[i % n_gen][1].pin_memory() for i in range(n_gen)]
+    dx = torch.empty_like(xs[0])
+    dy = torch.empty_like(ys[0])
+    hl = torch.empty(args.steps, dtype=torch.float32).pin_memory()
+    dl = torch.empty(args.steps, dtype=torch.float32, device=dev)
+    for i in range(3):
+        dx.copy_(hx[i % n_gen], non_blocking=True)
+        dy.copy_(hy[i % n_gen], non_blocking=True)
+        model.train_step(dx, dy, loss=dl[i], **hyper)
+        hl[i:i + 1].copy_(dl[i:i + 1], non_blocking=True)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        dx.copy_(hx[i % n_gen], non_blocking=True)
+        dy.copy_(hy[i % n_gen], non_blocking=True)
+        model.train_step(dx, dy, loss=dl[i], **hyper)
+        hl[i:i + 1].copy_(dl[i:i + 1], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": w.batch * world * args.steps / (e2e_ms / 1e3), "unit": "samples/s",
+           "h2d_bytes_per_step": int(dx.numel() * dx.element_size() + dy.numel() * 4), "d2h_bytes_per_step": 4}
+
+    # ---- per-kernel times (serialised profiling pass, same stream) ----
+    n_prof = 10
+    acc = None
+    for i in range(n_prof):
+        prof = nn.mlp_profile_step(model.h, xs[i % n_pool].data_ptr(), ys[i % n_pool].data_ptr(), w.lr, w.beta1,
+                                   w.beta2, w.eps, w.wd, None, stream.cuda_stream)
+        if acc is None:
+            acc = [[n, 0.0] for n, _ in prof]
+        for a, (_, t) in zip(acc, prof):
+            a[1] += t / n_prof
+    rows = attach_work(w, [(n, t) for n, t in acc])
+    t_roof_ms = roofline_rows(w, rows, peaks)
+    top = max(rows, key=lambda r: r["ms"])
+    rf = {"bound": top["bound"], "achieved": round(top["achieved"], 3), "peak": top["peak"], "unit": top["unit"],
+          "frac": round(top["frac"], 4), "traffic": ncu_traffic(top["kernel"], w.name),
+          "kernel": f"{top['kernel']} (layer {top['layer'] + 1})" if top["layer"] >= 0 else top["kernel"],
+          "launch_ms": round(top["ms"], 5),
+          "peak_source": (f"{peaks['source']} ({'derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz' if top['bound'] == 'alu' else 'MEASURED_PEAKS.json burst'})")}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "samples/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if w.dtype == 0 else "bf16",
+            "data": "synthetic",
+            "config": config_of(w, {"l2": f"fresh batch per step from a {n_pool}-batch device pool "
+                                          f"({n_pool * per / 2**20:.0f} MiB > 129 MB L2)",
+                                    "graph": "one CUDA-graph replay per step"}),
+            "roofline": rf,
+            "step_roofline": {"t_roof_ms": round(t_roof_ms, 5), "measured_ms": round(ms_per_step, 5),
+                              "frac": round(t_roof_ms / ms_per_step, 4),
+                              "kernels_serial_ms": round(sum(r["ms"] for r in rows), 5)},
+            "e2e": {k: (round(v, 1) if isinstance(v, float) else v) for k, v in e2e.items()},
+            "gpu_launches": kernels_per_step * args.steps,
+            "clocks": clocks}
+    if args.kernels:
+        line["kernels"] = [{k: (round(v, 5) if isinstance(v, float) else v) for k, v in r.items()} for r in rows]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = time_oracle(w, target_s=10.0)
+        line["cpu_baseline"] = {k: (round(v, 2) if isinstance(v, float) else v) for k, v in cb.items()}
+    if rank == 0:
+        print(json.dumps(line))
+    model.close()
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -135,6 +135,17 @@ mlp_status mlp_check_errors(mlp_t* model, void* stream);
 /* Number of kernels one training step launches (graph nodes per step). */
 int mlp_kernels_per_step(const mlp_t* model);
 
+/* One training step (same arguments and effect as mlp_train_step) with every
+ * kernel launched on its own and bracketed by CUDA events on `stream`
+ * (MuNet "Configuration": profile=True serialises kernels and records
+ * per-kernel GPU timestamps).  Writes the device time of kernel i in ms to
+ * ms_out[i] and its name (a static string) to names_out[i] (nullable) for
+ * i < min(*n_out, max_kernels); *n_out = kernels in the step.  Synchronises
+ * the stream before returning. */
+mlp_status mlp_profile_step(mlp_t* model, const void* x_dev, const int32_t* labels_dev, float lr, float beta1,
+                            float beta2, float eps, float wd, float* loss_dev, void* stream, float* ms_out,
+                            const char** names_out, int max_kernels, int* n_out);
+
 /* Message for the last failed call on this thread ("" if none). */
 const char* mlp_last_error(void);
 

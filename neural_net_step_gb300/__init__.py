@@ -47,6 +47,8 @@ _SIGS = {
     "mlp_write_params": (_I32, [_P, _I32, _P, _SZ, _I64]),
     "mlp_check_errors": (_I32, [_P, _P]),
     "mlp_kernels_per_step": (_I32, [_P]),
+    "mlp_profile_step": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P, _c.POINTER(_F), _c.POINTER(_c.c_char_p),
+                                _I32, _c.POINTER(_I32)]),
     "mlp_last_error": (_c.c_char_p, []),
     "mlp_destroy": (None, [_P]),
     "mlp_op_linear_act": (_I32, [_I32, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _P, _P]),
@@ -136,6 +138,16 @@ def mlp_num_layers(h) -> int:
 
 def mlp_kernels_per_step(h) -> int:
     return lib().mlp_kernels_per_step(h)
+
+
+def mlp_profile_step(h, x_ptr, labels_ptr, lr, beta1, beta2, eps, wd, loss_ptr, stream, max_kernels=256):
+    """Returns [(kernel name, device ms), ...] for one serialised step."""
+    ms = (_F * max_kernels)()
+    names = (_c.c_char_p * max_kernels)()
+    n = _I32(0)
+    _check(lib().mlp_profile_step(h, x_ptr, labels_ptr, lr, beta1, beta2, eps, wd, loss_ptr, stream, ms, names,
+                                  max_kernels, ctypes.byref(n)))
+    return [(names[i].decode(), ms[i]) for i in range(min(n.value, max_kernels))]
 
 
 def mlp_read_params(h, plane, host_ptr, n) -> int:

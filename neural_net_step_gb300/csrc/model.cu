@@ -554,6 +554,39 @@ mlp_status mlp_train_steps(mlp_t* m, int n_steps, const void* const* xs, const i
   return run(m, n_steps, recs, (cudaStream_t)stream);
 }
 
+mlp_status mlp_profile_step(mlp_t* m, const void* x, const int32_t* y, float lr, float b1, float b2, float eps,
+                            float wd, float* loss, void* stream, float* ms_out, const char** names_out,
+                            int max_kernels, int* n_out) {
+  if (!m || !x || !y || !n_out || (max_kernels > 0 && !ms_out)) return fail(MLP_ERR_ARG, "bad arguments");
+  if (!(lr >= 0) || !(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1) || !(eps >= 0) || !(wd >= 0))
+    return fail(MLP_ERR_ARG, "bad hyper-parameters");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_step(m, x, y, Hyper{lr, b1, b2, eps, wd}, loss, recs);
+  if (st != MLP_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int n = (int)recs.size();
+  std::vector<cudaEvent_t> ev(n + 1, nullptr);
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i <= n && e == cudaSuccess; ++i) e = cudaEventCreate(&ev[i]);
+  for (int i = 0; i < n && e == cudaSuccess; ++i) {
+    if (i == 0) e = cudaEventRecord(ev[0], s);
+    if (e == cudaSuccess) e = launch_rec(recs[i], s);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[i + 1], s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  for (int i = 0; i < n && i < max_kernels && e == cudaSuccess; ++i) {
+    e = cudaEventElapsedTime(&ms_out[i], ev[i], ev[i + 1]);
+    if (names_out) names_out[i] = recs[i].name;
+  }
+  for (auto& v : ev)
+    if (v) cudaEventDestroy(v);
+  if (e != cudaSuccess) return fail(MLP_ERR_CUDA, "profile: %s", cudaGetErrorString(e));
+  *n_out = n;
+  return ok();
+}
+
 static mlp_status copy_plane(mlp_t* m, int plane, float* host_out, const float* host_in, size_t n) {
   if (plane < MLP_PLANE_P || plane > MLP_PLANE_V) return fail(MLP_ERR_ARG, "bad plane %d", plane);
   if ((int64_t)n != m->lay.n_params) return fail(MLP_ERR_ARG, "n must be %lld", (long long)m->lay.n_params);
