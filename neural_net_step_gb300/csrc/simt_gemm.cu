@@ -43,7 +43,7 @@ simt_gemm_kernel(const __grid_constant__ SimtGemmParams p) {
   const int kbeg = blockIdx.z * p.k_chunk;
   const int kend = min(p.K, kbeg + p.k_chunk);
   const int ntiles = kend > kbeg ? (kend - kbeg + SK - 1) / SK : 0;
-  const bool do_db = (p.kind == GEMM_WGRAD) && blockIdx.x == 0;
+  const bool do_db = (p.kind == GEMM_WGRAD) && blockIdx.x == 0 && p.db != nullptr;
 
   float ra[A_PER], rb[B_PER];
   auto load = [&](int t) {
