@@ -57,6 +57,29 @@ mlp_status mlp_op_wgrad(int dtype, int64_t N, int64_t K, int64_t B, const void* 
                         int64_t ldx, float* dW, int64_t lddw, float* db, void* workspace, size_t ws_bytes,
                         uint32_t* err_dev, void* stream);
 
+/* mlp_op_wgrad without a workspace argument (the pages have no counterpart:
+ * this is a convenience of this library).  Some callers cannot call
+ * cudaMalloc: an application whose device memory belongs to another
+ * allocator (a framework's caching pool, a fixed up-front reservation) has
+ * no extra buffer to pass, and a latency-critical loop must not allocate,
+ * since cudaMalloc/cudaFree can synchronise the device and fail under memory
+ * pressure.  This entry point allocates nothing: the split-K partial sums go
+ * to a built-in device array of 16 MiB, which every GPU that loads the
+ * library holds until the process exits.
+ *   Same arguments, layouts and results as mlp_op_wgrad.  Returns
+ *   MLP_ERR_SHAPE, before enqueuing anything, when the shape needs more than
+ *   16 MiB of scratch (mlp_op_wgrad_workspace_bytes tells how much).
+ *   The first call on a device that needs scratch looks up the array's
+ *   device address (cudaGetSymbolAddress) with that device current and
+ *   caches it; make that first call before any stream capture.
+ *   Every call shares the one array per device: calls whose kernels overlap
+ *   on the GPU (other streams, other threads) race on it and must be
+ *   serialised by the caller.  Each call writes every scratch element it
+ *   later reads, so nothing is carried over from a previous call. */
+mlp_status mlp_op_wgrad_noalloc(int dtype, int64_t N, int64_t K, int64_t B, const void* dY, int64_t ldy,
+                                const void* X, int64_t ldx, float* dW, int64_t lddw, float* db, uint32_t* err_dev,
+                                void* stream);
+
 /* Softmax cross-entropy, forward and backward in one pass over each row
  * (devpost "Orthon", "Selected Orthon vs. PyTorch results": one kernel reads
  * the logits once):  loss_rows[i] = logsumexp(z_i) - z_i[y_i] (fp32),

@@ -55,6 +55,7 @@ _SIGS = {
     "mlp_op_dgrad": (_I32, [_I32, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P]),
     "mlp_op_wgrad_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64]),
     "mlp_op_wgrad": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
+    "mlp_op_wgrad_noalloc": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
     "mlp_op_softmax_ce": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _F, _P, _I64, _P, _P, _P]),
     "mlp_op_loss_mean": (_I32, [_I64, _P, _P, _P, _P]),
     "mlp_op_adamw": (_I32, [_I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _P]),
@@ -183,6 +184,12 @@ def mlp_op_wgrad_workspace_bytes(dtype, N, K, B) -> int:
 
 def mlp_op_wgrad(dtype, N, K, B, dY, ldy, X, ldx, dW, lddw, db, ws, ws_bytes, err, stream) -> None:
     _check(lib().mlp_op_wgrad(dtype, N, K, B, dY, ldy, X, ldx, dW, lddw, db, ws, ws_bytes, err, stream))
+
+
+def mlp_op_wgrad_noalloc(dtype, N, K, B, dY, ldy, X, ldx, dW, lddw, db, err, stream) -> None:
+    """mlp_op_wgrad for callers that cannot provide a workspace: the split-K
+    partial sums live in the library's built-in 16 MiB device array."""
+    _check(lib().mlp_op_wgrad_noalloc(dtype, N, K, B, dY, ldy, X, ldx, dW, lddw, db, err, stream))
 
 
 def mlp_op_softmax_ce(dtype, B, C, z, ldz, labels, grad_scale, dz, lddz, loss_rows, err, stream) -> None:

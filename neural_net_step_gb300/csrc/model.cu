@@ -33,6 +33,7 @@ static mlp_status ok() {
   g_err[0] = 0;
   return MLP_OK;
 }
+void mlpk::set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
 #define CUDA_TRY(expr)                                                                       \
   do {                                                                                       \
     cudaError_t e_ = (expr);                                                                 \

@@ -105,4 +105,7 @@ int copy_rows_plan(const CopyRowsOp& op, LaunchRec* rec, char* err, size_t errle
 // w16[i] = bf16_rne(p[i]).
 int cast_bf16_plan(int64_t n, const float* p, void* w16, LaunchRec* rec, char* err, size_t errlen);
 
+// Set the message mlp_last_error() returns on the calling thread.
+void set_last_error(const char* msg);
+
 }  // namespace mlpk
