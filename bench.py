@@ -58,39 +58,58 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 # Algorithmic work of each kernel of the step (the order the library plans it)
 # ---------------------------------------------------------------------------
-def step_work(w):
-    """[(kind, layer, flops, bytes)] in launch order, without split-K reduces."""
+def layer_work(w, kind, l):
+    """(flops, algorithmic bytes) of one kernel of the step."""
     B, es = w.batch, (4 if w.dtype == 0 else 2)
-    L, d = w.n_layers, w.dims
-    out = []
-    for l in range(L):
+    d, L = w.dims, w.n_layers
+    if kind in ("fwd", "wgrad", "dgrad"):
         K, N = d[l], d[l + 1]
-        gelu_u = es * B * N if (l < L - 1 and w.acts[l] == 2) else 0
-        out.append(("fwd", l, 2 * B * K * N, es * (B * K + N * K + B * N) + 4 * N + gelu_u))
+        if kind == "fwd":
+            gelu_u = es * B * N if (l < L - 1 and w.acts[l] == 2) else 0
+            return 2 * B * K * N, es * (B * K + N * K + B * N) + 4 * N + gelu_u
+        if kind == "wgrad":
+            return 2 * B * K * N, es * (B * N + B * K) + 4 * (N * K + N)
+        return 2 * B * K * N, es * (B * N + N * K + 2 * B * K)
     C = d[L]
-    out.append(("ce", -1, 0, 2 * es * B * C + 8 * B))
-    out.append(("loss_mean", -1, 0, 4 * B))
-    for l in range(L - 1, -1, -1):
-        K, N = d[l], d[l + 1]
-        out.append(("wgrad", l, 2 * B * K * N, es * (B * N + B * K) + 4 * (N * K + N)))
-        if l > 0:
-            out.append(("dgrad", l, 2 * B * K * N, es * (B * N + N * K + 2 * B * K)))
-    out.append(("adamw", -1, 0, w.n_params() * (28 + (2 if w.dtype == 1 else 0))))
-    return out
+    if kind == "head":   # output layer fwd + CE + dgrad + wgrad in one pass over h
+        K = d[L - 1]
+        return 3 * 2 * B * K * C, es * 3 * B * K + 4 * B + 4 * (C * K + C)
+    if kind == "ce":
+        return 0, 2 * es * B * C + 8 * B
+    if kind == "loss_mean":
+        return 0, 4 * B
+    if kind == "adamw":
+        return 0, w.n_params() * (28 + (2 if w.dtype == 1 else 0))
+    return 0, 0
 
 
 def attach_work(w, prof):
-    """Pair the profiled launches with the algorithmic work list."""
-    work = step_work(w)
-    rows, wi = [], 0
+    """Pair each profiled launch (in plan order) with its algorithmic work."""
+    rows, fwd_l, bwd_l = [], 0, w.n_layers - 1
     for name, ms in prof:
-        if name == "split_reduce":
-            rows.append({"kernel": name, "layer": rows[-1]["layer"], "ms": ms, "flops": 0, "bytes": 0})
-            continue
-        kind, layer, fl, by = work[wi]
-        wi += 1
-        rows.append({"kernel": name, "kind": kind, "layer": layer, "ms": ms, "flops": fl, "bytes": by})
-    assert wi == len(work), (wi, len(work), [p[0] for p in prof])
+        if name.endswith("_fwd"):
+            kind, l = "fwd", fwd_l
+            fwd_l += 1
+        elif name == "head_ce":
+            kind, l = "head", w.n_layers - 1
+            bwd_l = w.n_layers - 2
+        elif name == "softmax_ce":
+            kind, l = "ce", -1
+        elif name == "loss_mean":
+            kind, l = "loss_mean", -1
+        elif name.endswith("_wgrad"):
+            kind, l = "wgrad", bwd_l
+        elif name.endswith("_dgrad"):
+            kind, l = "dgrad", bwd_l
+            bwd_l -= 1
+        elif name == "split_reduce":
+            kind, l = "split_reduce", rows[-1]["layer"]
+        elif name.startswith("adamw"):
+            kind, l = "adamw", -1
+        else:
+            kind, l = name, -1
+        fl, by = layer_work(w, kind, l)
+        rows.append({"kernel": name, "kind": kind, "layer": l, "ms": ms, "flops": fl, "bytes": by})
     return rows
 
 
@@ -99,7 +118,7 @@ def roofline_rows(w, rows, peaks):
     t_roof = 0.0
     for r in rows:
         sec = max(r["ms"], 1e-9) / 1e3
-        if r["flops"]:
+        if r["flops"] and r["kind"] != "head":
             if w.dtype == 0:
                 bound, peak, unit = "alu", FP32_FFMA_PEAK_TFLOPS, "TFLOP/s"
             else:

@@ -117,6 +117,19 @@ mlp_status mlp_train_steps(mlp_t* model, int n_steps, const void* const* x_devs,
  * launch the kernels one by one (0). */
 mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
 
+/* Step options.
+ *   MLP_OPT_GRAPH      (default 1): same as mlp_set_graph_mode.
+ *   MLP_OPT_FUSE_HEAD  (default 1): where the output layer is small (at most
+ *     16 classes, at most 256 inputs, and a hidden layer below it), run it
+ *     as one kernel together with softmax-CE, its dgrad and wgrad and the
+ *     loss mean (the single logits read of devpost "Orthon", "Selected
+ *     Orthon vs. PyTorch results", extended to the whole layer); 0 keeps the
+ *     separate GEMM / CE / loss-mean kernels.  Results agree within
+ *     rounding; the arithmetic and rounding points are the same.
+ * Returns MLP_ERR_ARG for an unknown option. */
+enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1 };
+mlp_status mlp_set_option(mlp_t* model, int option, int64_t value);
+
 /* Number of parameters (flat, densely packed) and of Linear layers. */
 int64_t mlp_num_params(const mlp_t* model);
 int mlp_num_layers(const mlp_t* model);

@@ -41,6 +41,7 @@ _SIGS = {
     "mlp_train_step": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P]),
     "mlp_train_steps": (_I32, [_P, _I32, _c.POINTER(_P), _c.POINTER(_P), _F, _F, _F, _F, _F, _P, _P]),
     "mlp_set_graph_mode": (_I32, [_P, _I32]),
+    "mlp_set_option": (_I32, [_P, _I32, _I64]),
     "mlp_num_params": (_I64, [_P]),
     "mlp_num_layers": (_I32, [_P]),
     "mlp_read_params": (_I32, [_P, _I32, _P, _SZ, _c.POINTER(_I64)]),
@@ -127,6 +128,13 @@ def mlp_train_steps(h, x_ptrs, label_ptrs, lr, beta1, beta2, eps, wd, losses_ptr
 
 def mlp_set_graph_mode(h, enable: bool) -> None:
     _check(lib().mlp_set_graph_mode(h, int(bool(enable))))
+
+
+OPT_GRAPH, OPT_FUSE_HEAD = 0, 1
+
+
+def mlp_set_option(h, option: int, value: int) -> None:
+    _check(lib().mlp_set_option(h, option, value))
 
 
 def mlp_num_params(h) -> int:
@@ -236,6 +244,9 @@ class Model:
 
     def set_graph_mode(self, enable: bool) -> None:
         mlp_set_graph_mode(self.h, enable)
+
+    def set_option(self, option: int, value: int) -> None:
+        mlp_set_option(self.h, option, value)
 
     def _check_x(self, x, labels=None):
         t = self.torch

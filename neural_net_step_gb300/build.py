@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmlpstep.so")
-SOURCES = ["simt_gemm.cu", "tc_gemm.cu", "rowops.cu", "model.cu", "noalloc.cu"]
+SOURCES = ["simt_gemm.cu", "tc_gemm.cu", "rowops.cu", "model.cu", "noalloc.cu", "head.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

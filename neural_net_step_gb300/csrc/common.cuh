@@ -56,6 +56,18 @@ __device__ __forceinline__ float act_grad_from_stored(float s, int act) {
   return 1.0f;
 }
 
+// Advance the device step counter to t and store AdamW's bias corrections
+// for that step, 1/(1 - beta1^t) and 1/sqrt(1 - beta2^t), computed in fp64
+// (one thread, once per step).
+__device__ __forceinline__ void advance_step(int64_t* counter, float* bias_corr, float beta1, float beta2) {
+  const int64_t t = *counter + 1;
+  *counter = t;
+  if (bias_corr) {
+    bias_corr[0] = (float)(1.0 / (1.0 - pow((double)beta1, (double)t)));
+    bias_corr[1] = (float)(1.0 / sqrt(1.0 - pow((double)beta2, (double)t)));
+  }
+}
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 template <typename T> __device__ __forceinline__ T from_f32(float v);

@@ -81,8 +81,9 @@ struct Layout {
 struct Ctl {   // control block at off_ctl
   int64_t step;
   uint32_t err;
-  uint32_t pad;
+  uint32_t head_ticket;   // arrival counter of the fused output layer (re-armed to 0 by it)
   float loss_slot;
+  float bias_corr[2];     // AdamW 1/(1-b1^t), 1/sqrt(1-b2^t) of the current step
 };
 
 mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act, int dtype, int64_t batch,
@@ -148,6 +149,10 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     size_t b = wgrad_workspace_bytes(dtype, dims[l + 1], dims[l], batch, s);
     ws = b > ws ? b : ws;
   }
+  if (n_dims >= 3 && head_supported(dims[L.L], dims[L.L - 1])) {
+    size_t b = head_workspace_bytes(batch, dims[L.L], dims[L.L - 1]);
+    ws = b > ws ? b : ws;
+  }
   L.ws_bytes = ws;
   L.off_ws = take(ws ? ws : 4);
   L.off_ctl = take(sizeof(Ctl));
@@ -193,6 +198,7 @@ struct mlp {
   uint8_t* arena = nullptr;
   size_t arena_bytes = 0;
   bool use_graph = true;
+  bool fuse_head = true;     // fused output layer + CE where the shape allows
   std::mutex mu;
   std::vector<GraphCache> graphs;
   int kernels_per_step = 0;
@@ -236,11 +242,14 @@ mlp_status add(std::vector<LaunchRec>& out, int n, const LaunchRec* recs) {
   } while (0)
 
 // Forward GEMMs of all layers (logits into the arena's z buffer).
-mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out) {
+// Forward GEMMs of layers [0, n_layers) (all layers: logits into the arena's
+// z buffer).
+mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out, int n_layers = -1) {
   const Layout& L = m->lay;
   const void* X = x;
   int64_t ldx = L.dims[0];
-  for (int l = 0; l < L.L; ++l) {
+  if (n_layers < 0) n_layers = L.L;
+  for (int l = 0; l < n_layers; ++l) {
     GemmOp op;
     op.dtype = L.dtype;
     op.kind = GEMM_FWD;
@@ -268,10 +277,45 @@ struct Hyper { float lr, b1, b2, eps, wd; };
 mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper& hp, float* loss,
                      std::vector<LaunchRec>& out) {
   const Layout& L = m->lay;
-  mlp_status st = plan_forward(m, x, out);
+  const bool fuse = m->fuse_head && L.L >= 2 && head_supported(L.dims[L.L], L.dims[L.L - 1]);
+  mlp_status st = plan_forward(m, x, out, fuse ? L.L - 1 : L.L);
   if (st != MLP_OK) return st;
   Ctl* ctl = m->ctl();
-  {
+  const void* dY = m->at(L.off_dz);
+  int64_t ldy = L.ldz;
+  int buf = 0;
+  int top = L.L - 1;   // highest layer whose wgrad/dgrad still has to be planned
+  if (fuse) {
+    // output layer + CE + its VJPs in one kernel; dY of the last hidden layer
+    // goes to the first ping-pong buffer
+    const int l = L.L - 1;
+    HeadOp hd;
+    hd.dtype = L.dtype; hd.act = L.acts[l - 1];
+    hd.B = L.B; hd.C = L.dims[L.L]; hd.K = L.dims[l];
+    hd.h = m->at(L.off_h[l - 1]); hd.ldh = L.ld_h[l - 1];
+    hd.W = m->weight(l);
+    hd.bias = m->plane(MLP_PLANE_P) + L.boff[l];
+    hd.labels = y;
+    hd.aux = hd.act == MLP_ACT_GELU_TANH ? m->at(L.off_u[l - 1]) : m->at(L.off_h[l - 1]);
+    hd.ld_aux = L.ld_h[l - 1];
+    hd.dY = m->at(L.off_dy[0]); hd.ldy = L.ld_h[l - 1];
+    hd.dW = m->plane(MLP_PLANE_G) + L.woff[l];
+    hd.db = m->plane(MLP_PLANE_G) + L.boff[l];
+    hd.loss = loss ? loss : &ctl->loss_slot;
+    hd.step_counter = &ctl->step;
+    hd.err = &ctl->err;
+    hd.ws = (float*)m->at(L.off_ws); hd.ws_bytes = L.ws_bytes;
+    hd.ticket = &ctl->head_ticket;
+    hd.grad_scale = (float)(1.0 / (double)L.B);
+    hd.bias_corr = ctl->bias_corr; hd.beta1 = hp.b1; hd.beta2 = hp.b2;
+    char e_[512] = "";
+    LaunchRec r;
+    if (head_plan(hd, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    out.push_back(r);
+    dY = hd.dY; ldy = hd.ldy;
+    buf = 1;
+    top = L.L - 2;
+  } else {
     CeOp ce;
     ce.dtype = L.dtype; ce.B = L.B; ce.C = L.dims[L.L];
     ce.z = m->at(L.off_z); ce.ldz = L.ldz;
@@ -289,14 +333,12 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     lm.loss = loss ? loss : &ctl->loss_slot;
     lm.step_counter = &ctl->step;
     lm.err = &ctl->err;
+    lm.bias_corr = ctl->bias_corr; lm.beta1 = hp.b1; lm.beta2 = hp.b2;
     if (loss_mean_plan(lm, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
     out.push_back(r);
   }
-  const void* dY = m->at(L.off_dz);
-  int64_t ldy = L.ldz;
-  int buf = 0;
   float* G = m->plane(MLP_PLANE_G);
-  for (int l = L.L - 1; l >= 0; --l) {
+  for (int l = top; l >= 0; --l) {
     const void* Xl = l == 0 ? x : m->at(L.off_h[l - 1]);
     const int64_t ldxl = l == 0 ? L.dims[0] : L.ld_h[l - 1];
     GemmOp wg;
@@ -330,6 +372,7 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
   ad.p = m->plane(MLP_PLANE_P); ad.g = G; ad.m = m->plane(MLP_PLANE_M); ad.v = m->plane(MLP_PLANE_V);
   ad.w16 = m->w16();
   ad.step_counter = &ctl->step;
+  ad.bias_corr = ctl->bias_corr;
   ad.lr = hp.lr; ad.beta1 = hp.b1; ad.beta2 = hp.b2; ad.eps = hp.eps; ad.wd = hp.wd;
   char e_[512] = "";
   LaunchRec r;
@@ -493,6 +536,22 @@ mlp_status mlp_set_graph_mode(mlp_t* m, int enable) {
   if (!m) return fail(MLP_ERR_ARG, "model is NULL");
   std::lock_guard<std::mutex> lk(m->mu);
   m->use_graph = enable != 0;
+  return ok();
+}
+
+mlp_status mlp_set_option(mlp_t* m, int option, int64_t value) {
+  if (!m) return fail(MLP_ERR_ARG, "model is NULL");
+  std::lock_guard<std::mutex> lk(m->mu);
+  switch (option) {
+    case MLP_OPT_GRAPH: m->use_graph = value != 0; break;
+    case MLP_OPT_FUSE_HEAD: m->fuse_head = value != 0; break;
+    default: return fail(MLP_ERR_ARG, "unknown option %d", option);
+  }
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_step(m, m->arena, (const int32_t*)m->arena, Hyper{1e-3f, 0.9f, 0.999f, 1e-8f, 0.f},
+                            nullptr, recs);
+  if (st != MLP_OK) return st;
+  m->kernels_per_step = (int)recs.size();
   return ok();
 }
 

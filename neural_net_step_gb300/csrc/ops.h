@@ -70,6 +70,8 @@ struct LossMeanOp {
   float* loss = nullptr;
   int64_t* step_counter = nullptr;   // nullable
   uint32_t* err = nullptr;           // nullable
+  float* bias_corr = nullptr;        // nullable: AdamW bias corrections for the new step
+  float beta1 = 0.9f, beta2 = 0.999f;
 };
 int loss_mean_plan(const LossMeanOp& op, LaunchRec* rec, char* err, size_t errlen);
 
@@ -80,6 +82,7 @@ struct AdamWOp {
   void* w16 = nullptr;                 // bf16 copy of p written after the update (nullable)
   const int64_t* step_counter = nullptr;   // t read from device (already incremented)...
   int64_t t = 0;                       // ...or given explicitly when > 0
+  const float* bias_corr = nullptr;    // precomputed [1/(1-b1^t), 1/sqrt(1-b2^t)] (nullable)
   float lr = 0, beta1 = 0, beta2 = 0, eps = 0, wd = 0;
 };
 int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen);
@@ -104,6 +107,33 @@ int copy_rows_plan(const CopyRowsOp& op, LaunchRec* rec, char* err, size_t errle
 
 // w16[i] = bf16_rne(p[i]).
 int cast_bf16_plan(int64_t n, const float* p, void* w16, LaunchRec* rec, char* err, size_t errlen);
+
+// The output layer fused with softmax-CE for a small class count (C <= 16,
+// K <= 256): logits, loss, dz, dY = (dz W) * act'(aux), dW, db and the mean
+// loss in one kernel (deterministic last-CTA reduction of per-CTA partials).
+struct HeadOp {
+  int dtype = 0;
+  int act = 0;                          // activation of the hidden layer below (for its VJP)
+  int64_t B = 0, C = 0, K = 0;
+  const void* h = nullptr; int64_t ldh = 0;
+  const void* W = nullptr;              // [C, K], row pitch K
+  const float* bias = nullptr;
+  const int32_t* labels = nullptr;
+  const void* aux = nullptr; int64_t ld_aux = 0;
+  void* dY = nullptr; int64_t ldy = 0;
+  float* dW = nullptr; float* db = nullptr;
+  float* loss = nullptr;
+  int64_t* step_counter = nullptr;
+  uint32_t* err = nullptr;
+  float* ws = nullptr; size_t ws_bytes = 0;
+  unsigned int* ticket = nullptr;       // a zeroed device word owned by the caller
+  float grad_scale = 1.0f;
+  float* bias_corr = nullptr;           // nullable: AdamW bias corrections for the new step
+  float beta1 = 0.9f, beta2 = 0.999f;
+};
+bool head_supported(int64_t C, int64_t K);
+size_t head_workspace_bytes(int64_t B, int64_t C, int64_t K);
+int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen);
 
 // Set the message mlp_last_error() returns on the calling thread.
 void set_last_error(const char* msg);

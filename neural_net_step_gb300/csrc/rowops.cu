@@ -210,6 +210,8 @@ struct LossMeanParams {
   float* loss;
   int64_t* step_counter;
   uint32_t* err;
+  float* bias_corr;
+  float beta1, beta2;
 };
 
 __global__ void __launch_bounds__(1024) loss_mean_kernel(const __grid_constant__ LossMeanParams p) {
@@ -225,14 +227,14 @@ __global__ void __launch_bounds__(1024) loss_mean_kernel(const __grid_constant__
   if (threadIdx.x == 0) {
     float L = (float)(red[0] / (double)p.B);
     if (p.loss) *p.loss = L;
-    if (p.step_counter) *p.step_counter += 1;
+    if (p.step_counter) advance_step(p.step_counter, p.bias_corr, p.beta1, p.beta2);
     if (p.err && !isfinite(L)) atomicOr(p.err, ERRBIT_NONFINITE);
   }
 }
 
 int loss_mean_plan(const LossMeanOp& op, LaunchRec* rec, char* err, size_t errlen) {
   if (op.B <= 0) { snprintf(err, errlen, "loss_mean: empty batch"); return -1; }
-  LossMeanParams q{op.loss_rows, op.B, op.loss, op.step_counter, op.err};
+  LossMeanParams q{op.loss_rows, op.B, op.loss, op.step_counter, op.err, op.bias_corr, op.beta1, op.beta2};
   rec->func = (const void*)loss_mean_kernel;
   rec->grid = dim3(1);
   rec->block = dim3(1024);
@@ -251,6 +253,7 @@ struct AdamWParams {
   float* p; const float* g; float* m; float* v;
   __nv_bfloat16* w16;
   const int64_t* step_counter; int64_t t;
+  const float* bias_corr;
   int64_t n;
   float lr, beta1, beta2, eps, wd;
 };
@@ -265,11 +268,21 @@ __device__ __forceinline__ void adamw_one(float& p, float g, float& m, float& v,
 }
 
 __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamWParams q) {
-  const int64_t t = q.t > 0 ? q.t : *q.step_counter;
-  const double bc1 = 1.0 - pow((double)q.beta1, (double)t);
-  const double bc2 = 1.0 - pow((double)q.beta2, (double)t);
-  const float inv_bc1 = (float)(1.0 / bc1);
-  const float inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
+  // bias corrections: precomputed for the step, else 1 - beta^t in fp64 once
+  // per CTA
+  __shared__ float s_bc[2];
+  if (q.bias_corr) {
+    if (threadIdx.x == 0) { s_bc[0] = q.bias_corr[0]; s_bc[1] = q.bias_corr[1]; }
+  } else if (threadIdx.x == 0) {
+    const int64_t t = q.t > 0 ? q.t : *q.step_counter;
+    const double bc1 = 1.0 - pow((double)q.beta1, (double)t);
+    const double bc2 = 1.0 - pow((double)q.beta2, (double)t);
+    s_bc[0] = (float)(1.0 / bc1);
+    s_bc[1] = (float)(1.0 / sqrt(bc2));
+  }
+  __syncthreads();
+  const float inv_bc1 = s_bc[0];
+  const float inv_sqrt_bc2 = s_bc[1];
   const int64_t n4 = q.n / 4;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -310,7 +323,7 @@ int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
     snprintf(err, errlen, "adamw: planes must be 16-byte aligned (w16: 8)");
     return -1;
   }
-  AdamWParams q{op.p, op.g, op.m, op.v, (__nv_bfloat16*)op.w16, op.step_counter, op.t, op.n,
+  AdamWParams q{op.p, op.g, op.m, op.v, (__nv_bfloat16*)op.w16, op.step_counter, op.t, op.bias_corr, op.n,
                 op.lr, op.beta1, op.beta2, op.eps, op.wd};
   rec->func = (const void*)adamw_kernel;
   int64_t blocks = ceil_div(op.n / 4 + 1, 256);

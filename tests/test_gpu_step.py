@@ -282,3 +282,28 @@ def test_shape_mismatch_and_bad_args_fail_before_enqueue():
         nn.mlp_train_step(m.h, x.to(DEV).data_ptr(), y.to(DEV).data_ptr(), -1.0, 0.9, 0.999, 1e-8, 0.0, None,
                           0)
     m.close()
+
+
+# --------------------------------------------------------------------------
+# Fused output layer (head + CE + its VJPs) against the unfused kernels
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("name,batch", [("mnist_mlp_b4096", None), ("mnist_mlp_b64", 333)])
+def test_fused_head_matches_unfused_path(name, batch):
+    """Same step with and without the fused output layer: the arithmetic and
+    rounding points are the same, only the order of fp32 additions differs,
+    so loss and gradients agree to fp32 accumulation error."""
+    w = W[name]
+    B = w.batch if batch is None else batch
+    params0 = synth.make_params(w)
+    bl = P.batches(w, 1, B)
+    res = []
+    for fuse in (1, 0):
+        m = make_model(w, B, params0)
+        m.set_option(nn.OPT_FUSE_HEAD, fuse)
+        res.append(gpu_run(m, w, bl))
+        m.close()
+    (l1, p1, g1), (l0, p0_, g0) = res
+    assert abs(l1[0] - l0[0]) <= 1e-6 * abs(l0[0])
+    kappa = P.oracle_abs_sums(w, params0, *bl[0], "fp64")
+    for a, b, k in zip(g1, g0, kappa):
+        assert np.all(np.abs(a - b) <= P.fp32_grad_tol(k))
