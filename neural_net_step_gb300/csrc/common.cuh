@@ -25,12 +25,17 @@ __host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return ceil_
 // 1 + tanh(a) = 2 s and 1 - tanh(a)^2 = 4 s (1 - s), s = 1 / (1 + e^{-2a}),
 // 1 - s = 1 / (1 + e^{2a}), which keep fp32 relative accuracy in both tails
 // (1 + tanh(a) computed directly cancels to 0 for very negative u).
+// The GEMM epilogues evaluate this for every output, so it uses CUDA's fast
+// intrinsics (__expf, __fdividef: a few ulp in fp32, far below the bf16
+// rounding of the stored result).
 __device__ __forceinline__ void gelu_parts(float u, float& s, float& sm, float& dinner) {
   const float k0 = 0.7978845608028654f;   // sqrt(2/pi)
   const float k1 = 0.044715f;
   const float a = k0 * (u + k1 * u * u * u);
-  s = 1.0f / (1.0f + expf(-2.0f * a));
-  sm = 1.0f / (1.0f + expf(2.0f * a));
+  // clamp keeps e finite (the results saturate long before |2a| = 80)
+  const float e = __expf(fminf(fmaxf(-2.0f * a, -80.f), 80.f));   // e^{-2a}
+  s = __fdividef(1.0f, 1.0f + e);
+  sm = __fdividef(e, 1.0f + e);
   dinner = k0 * (1.0f + 3.0f * k1 * u * u);
 }
 __device__ __forceinline__ float gelu_tanh(float u) {

@@ -148,11 +148,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -393,6 +394,264 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   }
 }
 
+// ---------------------------------------------------------------------------
+// Persistent variant for the forward and dgrad GEMMs (bf16 out).
+//
+// One CTA per SM walks output tiles t = blockIdx.x, +gridDim.x, ... in
+// m-major order (concurrent CTAs share A row blocks in L2).  The TMA ring runs
+// across tile boundaries; the MMA warp accumulates tile i into TMEM buffer
+// i % 2 while the epilogue warps drain buffer (i - 1) % 2; the epilogue
+// stages each 32-row x 64-column bf16 chunk in 128B-swizzled shared memory
+// (two buffers per warp) and writes it with a TMA bulk-tensor store, which
+// also clips the ragged edges of the output.
+// ---------------------------------------------------------------------------
+constexpr int PT_STAGE_BYTES_EPI = 4 * 2 * 4096;   // 4 warps x 2 buffers x (32 rows x 128 B)
+
+template <int BN> struct PCfg {
+  static constexpr int B_STAGE_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int STAGES = BN >= 256 ? 4 : 5;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + PT_STAGE_BYTES_EPI + 1024 + 256;
+};
+
+struct PParams {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  CUtensorMap tmOut;     // bf16 [M rows, N cols], box {64, 32}, 128B swizzle
+  int M, N, K;
+  int num_kb, tiles_n, num_tiles;
+  int b_mn;
+  int kind, act;
+  uint32_t idesc;
+  const float* bias;
+  __nv_bfloat16* out_u; int64_t ldu;
+  const __nv_bfloat16* aux; int64_t ld_aux;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v, int off) {
+  uint32_t r[32];
+  // load and wait in one statement: the outputs are defined only after the wait
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr + (uint32_t)off)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"((uint64_t)tm),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_persistent_kernel(const __grid_constant__ PParams p) {
+  using C = PCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t a_base = base;
+  const uint32_t b_base = base + C::STAGES * A_STAGE_BYTES;
+  const uint32_t epi_base = b_base + C::STAGES * C::B_STAGE_BYTES;
+  const uint32_t bar_base = epi_base + PT_STAGE_BYTES_EPI;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * C::STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * C::STAGES + 2 + b); };
+  const uint32_t tmem_slot = bar_base + 8u * (2 * C::STAGES + 4);
+  volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_ptr;
+  const uint32_t stage_tx = A_STAGE_BYTES + C::B_STAGE_BYTES;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&p.tmA);
+      prefetch_tmap(&p.tmB);
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
+          mbar_expect_tx(full_bar(s), stage_tx);
+          const int k0 = kb * BK;
+          tma_load_2d(a_base + s * A_STAGE_BYTES, &p.tmA, k0, m0, full_bar(s));
+          const uint32_t sb = b_base + s * C::B_STAGE_BYTES;
+          if (!p.b_mn) {
+            tma_load_2d(sb, &p.tmB, k0, n0, full_bar(s));
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + 8192 * c, &p.tmB, n0 + 64 * c, k0, full_bar(s));
+          }
+        }
+      }
+      for (int i = max(0, it - C::STAGES); i < it; ++i)
+        mbar_wait(full_bar(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u, p.err);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
+      const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++tc) {
+        const int buf = tc & 1;
+        if (!mbar_wait(tempty_bar(buf), (((uint32_t)tc >> 1) & 1u) ^ 1u, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+          if (!mbar_wait(full_bar(s), ph, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = a_base + s * A_STAGE_BYTES;
+          const uint32_t sb = b_base + s * C::B_STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sdesc(sa + kk * 32u, 16u, 1024u);
+            const uint64_t bd = sdesc(sb + kk * b_kstep, b_lbo, 1024u);
+            mma_bf16(d, ad, bd, p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(empty_bar(s));
+        }
+        mma_commit(tfull_bar(buf));
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int q = warp & 3;
+    const uint32_t stage0 = epi_base + (uint32_t)(q * 2 * 4096);
+    uint8_t* stage0_ptr = base_ptr + (stage0 - base);
+    int tc = 0, chunk = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++tc) {
+      const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
+      const int buf = tc & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), ((uint32_t)tc >> 1) & 1u, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      const int gm = m0 + q * 32 + lane;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 64, ++chunk) {
+        float v[64];
+        tmem_ld32(trow, v, c0);
+        tmem_ld32(trow, v + 32, c0 + 32);
+        if (c0 + 64 >= BN) {
+          // this TMEM buffer is drained: hand it back to the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));
+        }
+        const int gn0 = n0 + c0;
+        const bool row_ok = gm < p.M;
+        if (p.kind == GEMM_FWD) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const int gn = gn0 + j;
+            v[j] += gn < p.N ? __ldg(p.bias + gn) : 0.f;
+          }
+          if (p.out_u && row_ok) {
+            __nv_bfloat16* du = p.out_u + (int64_t)gm * p.ldu + gn0;
+            if (gn0 + 64 <= p.N) {
+#pragma unroll
+              for (int j = 0; j < 64; j += 8) {
+                uint4 w;
+                __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+                for (int h = 0; h < 4; ++h) w2[h] = __floats2bfloat162_rn(v[j + 2 * h], v[j + 2 * h + 1]);
+                *reinterpret_cast<uint4*>(du + j) = w;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 64; ++j)
+                if (gn0 + j < p.N) du[j] = __float2bfloat16_rn(v[j]);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 64; ++j) v[j] = apply_act(v[j], p.act);
+        } else if (p.act != ACT_NONE) {   // GEMM_DGRAD
+          const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
+          if (row_ok && gn0 + 64 <= p.N) {
+#pragma unroll
+            for (int j = 0; j < 64; j += 8) {
+              uint4 w = __ldg(reinterpret_cast<const uint4*>(ar + j));
+              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&w);
+#pragma unroll
+              for (int h = 0; h < 8; ++h) v[j + h] *= act_grad_from_stored(__bfloat162float(e[h]), p.act);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              v[j] *= (row_ok && gn0 + j < p.N) ? act_grad_from_stored(__bfloat162float(ar[j]), p.act) : 0.f;
+          }
+        }
+        // stage (128B swizzle: 16-byte unit u of row r at r*128 + ((u ^ (r & 7)) * 16)) and store
+        const int sbuf = chunk & 1;
+        if (lane == 0) bulk_wait_read1();   // the store that last used this buffer has read it
+        __syncwarp();
+        uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 w;
+          __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) w2[h] = __floats2bfloat162_rn(v[8 * u + 2 * h], v[8 * u + 2 * h + 1]);
+          *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) << 4)) = w;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32);
+          bulk_commit();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 }  // namespace tc
 
 // ---------------------------------------------------------------------------
@@ -482,12 +741,71 @@ size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int spl
   return (size_t)splits * (size_t)(M * N + M) * sizeof(float);
 }
 
+namespace {
+template <int BN>
+const void* tcp_kernel_ptr() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute((const void*)tc::tc_gemm_persistent_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         tc::PCfg<BN>::SMEM_BYTES);
+  });
+  return (const void*)tc::tc_gemm_persistent_kernel<BN>;
+}
+
+int device_sms() {
+  static int n = [] {
+    int d = 0, v = kSMs;
+    if (cudaGetDevice(&d) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+      v = kSMs;
+    return v;
+  }();
+  return n;
+}
+
+// Forward / dgrad on the persistent kernel (bf16 output through TMA stores).
+int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
+  const int BN = op.N > 128 ? 256 : 128;
+  tc::PParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_tmap(&p.tmA, op.A, op.K, op.M, op.lda, 64, tc::BM, err, errlen)) return -1;
+  if (op.b_kmajor) {
+    if (!make_tmap(&p.tmB, op.B, op.K, op.N, op.ldb, 64, BN, err, errlen)) return -1;
+  } else {
+    if (!make_tmap(&p.tmB, op.B, op.N, op.K, op.ldb, 64, 64, err, errlen)) return -1;
+  }
+  if (!make_tmap(&p.tmOut, op.out, op.N, op.M, op.ldo, 64, 32, err, errlen)) return -1;
+  p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
+  p.num_kb = (int)ceil_div(op.K, tc::BK);
+  p.tiles_n = (int)ceil_div(op.N, BN);
+  p.num_tiles = (int)(ceil_div(op.M, tc::BM) * p.tiles_n);
+  p.b_mn = op.b_kmajor ? 0 : 1;
+  p.kind = op.kind; p.act = op.act;
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)p.b_mn << 16) | ((uint32_t)(BN >> 3) << 17) |
+            ((uint32_t)(tc::BM >> 4) << 24);
+  p.bias = op.bias;
+  p.out_u = (__nv_bfloat16*)op.out_u; p.ldu = op.ldu;
+  p.aux = (const __nv_bfloat16*)op.aux; p.ld_aux = op.ld_aux;
+  p.err = op.err;
+  LaunchRec& r = recs[0];
+  if (BN == 256) { r.func = tcp_kernel_ptr<256>(); r.smem = tc::PCfg<256>::SMEM_BYTES; }
+  else { r.func = tcp_kernel_ptr<128>(); r.smem = tc::PCfg<128>::SMEM_BYTES; }
+  const int sms = device_sms();
+  r.grid = dim3((unsigned)(p.num_tiles < sms ? p.num_tiles : sms));
+  r.block = dim3(tc::NUM_THREADS);
+  r.name = op.kind == GEMM_FWD ? "tc_gemm_fwd" : "tc_gemm_dgrad";
+  r.set_args(p);
+  return 1;
+}
+}  // namespace
+
 int tc_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   if (op.dtype != DT_BF16) { snprintf(err, errlen, "tensor-core GEMM is bf16 only"); return -1; }
   if (op.M <= 0 || op.N <= 0 || op.K <= 0 || op.M > INT32_MAX || op.N > INT32_MAX || op.K > INT32_MAX) {
     snprintf(err, errlen, "bad GEMM shape %lld x %lld x %lld", (long long)op.M, (long long)op.N, (long long)op.K);
     return -1;
   }
+  if ((op.kind == GEMM_FWD || op.kind == GEMM_DGRAD) && op.a_kmajor && op.N > 16)
+    return tc_persistent_plan(op, recs, err, errlen);
   const int BN = pick_bn(op);
   if (!op.b_kmajor && BN % 64) { snprintf(err, errlen, "MN-major B needs BN %% 64 == 0"); return -1; }
   tc::Params p;

@@ -165,6 +165,7 @@ def test_wgrad(dtype, N, K, B):
 CE_CASES = [
     (nn.F32, 64, 10), (nn.F32, 4096, 10), (nn.BF16, 8192, 10), (nn.BF16, 1000, 100),
     (nn.BF16, 256, 32000), (nn.F32, 33, 1003), (nn.BF16, 17, 777), (nn.F32, 5, 1),
+    (nn.F32, 40, 8000), (nn.BF16, 64, 4096),
 ]
 
 
