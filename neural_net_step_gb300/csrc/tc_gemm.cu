@@ -405,14 +405,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 // (two buffers per warp) and writes it with a TMA bulk-tensor store, which
 // also clips the ragged edges of the output.
 // ---------------------------------------------------------------------------
-constexpr int PT_STAGE_BYTES_EPI = 4 * 2 * 4096;   // 4 warps x 2 buffers x (32 rows x 128 B)
+constexpr int P_EPI_WARPS = 8;
+constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;   // producer warp, MMA warp, 8 epilogue warps
+// epilogue staging: per warp, 1 or 2 buffers of 32 rows x 128 B
 
 template <int BN> struct PCfg {
   static constexpr int B_STAGE_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-  static constexpr int STAGES = BN >= 256 ? 4 : 5;
+  static constexpr int STAGES = 4;
+  static constexpr int EPI_BUFS = BN >= 256 ? 1 : 2;   // staging buffers per epilogue warp
+  static constexpr int EPI_BYTES = P_EPI_WARPS * EPI_BUFS * 4096;
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + PT_STAGE_BYTES_EPI + 1024 + 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
 };
 
 struct PParams {
@@ -453,11 +457,12 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 template <int BN>
-__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_persistent_kernel(const __grid_constant__ PParams p) {
+__global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const __grid_constant__ PParams p) {
   using C = PCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -466,7 +471,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_persistent_kernel(cons
   const uint32_t a_base = base;
   const uint32_t b_base = base + C::STAGES * A_STAGE_BYTES;
   const uint32_t epi_base = b_base + C::STAGES * C::B_STAGE_BYTES;
-  const uint32_t bar_base = epi_base + PT_STAGE_BYTES_EPI;
+  const uint32_t bar_base = epi_base + C::EPI_BYTES;
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
   auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * C::STAGES + b); };
@@ -482,7 +487,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_persistent_kernel(cons
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
+      mbar_init(tempty_bar(b), P_EPI_WARPS);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -552,9 +557,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_persistent_kernel(cons
       }
     }
   } else {
-    // ---------------- epilogue warps 2..5 ----------------
+    // ---------------- epilogue warps 2..9 ----------------
+    // warp w reads TMEM lanes 32*(w%4)..+31 (its lane quarter) and the
+    // columns of its half of the tile: two warps share each quarter
     const int q = warp & 3;
-    const uint32_t stage0 = epi_base + (uint32_t)(q * 2 * 4096);
+    const int half = (warp - 2) >> 2;
+    const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * C::EPI_BUFS * 4096);
     uint8_t* stage0_ptr = base_ptr + (stage0 - base);
     int tc = 0, chunk = 0;
     bool ok = true;
@@ -566,28 +574,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_persistent_kernel(cons
       tc_fence_after();
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
       const int gm = m0 + q * 32 + lane;
+      const bool row_ok = gm < p.M;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 64, ++chunk) {
+      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 64, ++chunk) {
+        const int gn0 = n0 + c0;
+        const bool full = gn0 + 64 <= p.N;
+        // dgrad: start the loads of the stored activation before reading TMEM
+        uint4 aux[8];
+        const bool use_aux = p.kind == GEMM_DGRAD && p.act != ACT_NONE;
+        const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
+        if (use_aux && row_ok && full) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) aux[u] = __ldg(reinterpret_cast<const uint4*>(ar) + u);
+        }
         float v[64];
         tmem_ld32(trow, v, c0);
         tmem_ld32(trow, v + 32, c0 + 32);
-        if (c0 + 64 >= BN) {
-          // this TMEM buffer is drained: hand it back to the MMA warp
+        if (c0 + 64 >= (half + 1) * (BN / 2)) {
+          // this warp's part of the TMEM buffer is drained: hand it back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(buf));
         }
-        const int gn0 = n0 + c0;
-        const bool row_ok = gm < p.M;
         if (p.kind == GEMM_FWD) {
+          if (full) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int gn = gn0 + j;
-            v[j] += gn < p.N ? __ldg(p.bias + gn) : 0.f;
+            for (int j = 0; j < 64; j += 4) {
+              const float4 b4 = __ldg(reinterpret_cast<const float4*>(p.bias + gn0 + j));
+              v[j] += b4.x; v[j + 1] += b4.y; v[j + 2] += b4.z; v[j + 3] += b4.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) v[j] += gn0 + j < p.N ? __ldg(p.bias + gn0 + j) : 0.f;
           }
           if (p.out_u && row_ok) {
             __nv_bfloat16* du = p.out_u + (int64_t)gm * p.ldu + gn0;
-            if (gn0 + 64 <= p.N) {
+            if (full) {
 #pragma unroll
               for (int j = 0; j < 64; j += 8) {
                 uint4 w;
@@ -604,15 +626,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_persistent_kernel(cons
           }
 #pragma unroll
           for (int j = 0; j < 64; ++j) v[j] = apply_act(v[j], p.act);
-        } else if (p.act != ACT_NONE) {   // GEMM_DGRAD
-          const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
-          if (row_ok && gn0 + 64 <= p.N) {
+        } else if (use_aux) {   // GEMM_DGRAD
+          if (row_ok && full) {
 #pragma unroll
-            for (int j = 0; j < 64; j += 8) {
-              uint4 w = __ldg(reinterpret_cast<const uint4*>(ar + j));
-              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&w);
+            for (int u = 0; u < 8; ++u) {
+              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&aux[u]);
 #pragma unroll
-              for (int h = 0; h < 8; ++h) v[j + h] *= act_grad_from_stored(__bfloat162float(e[h]), p.act);
+              for (int h = 0; h < 8; ++h) v[8 * u + h] *= act_grad_from_stored(__bfloat162float(e[h]), p.act);
             }
           } else {
 #pragma unroll
@@ -621,8 +641,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_persistent_kernel(cons
           }
         }
         // stage (128B swizzle: 16-byte unit u of row r at r*128 + ((u ^ (r & 7)) * 16)) and store
-        const int sbuf = chunk & 1;
-        if (lane == 0) bulk_wait_read1();   // the store that last used this buffer has read it
+        const int sbuf = chunk % C::EPI_BUFS;
+        if (lane == 0) {   // the store that last used this buffer has read it
+          if (C::EPI_BUFS == 1) bulk_wait_read0();
+          else bulk_wait_read1();
+        }
         __syncwarp();
         uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
 #pragma unroll
@@ -649,6 +672,221 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_persistent_kernel(cons
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Persistent split-K weight gradient: dW[m, n] = sum_k A(m, k) B(k, n), with
+// A = dY^T and B = X both MN-major in memory, fp32 out.  The bias gradient
+// db[m] = sum_k A(m, k) comes from the tensor cores too: for units of the
+// first column tile a second MMA multiplies the same A tile by a constant
+// 16 x 64 tile of ones (N = 16) into spare TMEM columns.
+//
+// Work units are (tile, K split) pairs, tile index fastest, so CTAs running
+// at the same time share K ranges in L2.  Each unit's fp32 result goes out
+// through TMA stores to the gradient plane (one split) or to a split-K
+// workspace that a fixed-order reduce kernel sums (several splits).
+// ---------------------------------------------------------------------------
+constexpr int W_BN = 128;
+constexpr int W_STAGES = 4;
+constexpr int W_STAGE_BYTES = A_STAGE_BYTES + W_BN * BK * 2;   // 32 KB
+constexpr int W_EPI_BUFS = 2;
+constexpr int W_EPI_BYTES = P_EPI_WARPS * W_EPI_BUFS * 4096;
+constexpr int W_ONES_BYTES = 16 * 128;                          // 16 rows x 64 bf16
+constexpr int W_TMEM_COLS = 512;                                // 2 x (128 dW + 32 db), stride 256
+constexpr int W_SMEM_BYTES = W_STAGES * W_STAGE_BYTES + W_EPI_BYTES + W_ONES_BYTES + 1024 + 256;
+
+struct WParams {
+  CUtensorMap tmA;       // A^T storage: inner M, outer K; box {64, 64}
+  CUtensorMap tmB;       // inner N, outer K; box {64, 64}
+  CUtensorMap tmOut;     // fp32 3-D {N, M, splits}; box {32, 32, 1}; 128B swizzle
+  int M, N, K;
+  int num_kb, kb_per_split, splits;
+  int tiles_n, num_tiles, num_units;
+  uint32_t idesc, idesc_db;
+  float* db_out;         // [splits][M] (nullable: no bias gradient)
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"((uint64_t)tm),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r)
+      : "r"(taddr)
+      : "memory");
+  return __uint_as_float(r);
+}
+
+__global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const __grid_constant__ WParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t a_base = base;
+  const uint32_t b_base = base + W_STAGES * A_STAGE_BYTES;
+  const uint32_t epi_base = b_base + W_STAGES * (W_BN * BK * 2);
+  const uint32_t ones_base = epi_base + W_EPI_BYTES;
+  const uint32_t bar_base = ones_base + W_ONES_BYTES;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (W_STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * W_STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * W_STAGES + 2 + b); };
+  const uint32_t tmem_slot = bar_base + 8u * (2 * W_STAGES + 4);
+  volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {   // the constant ones tile (bf16 1.0 = 0x3F80)
+    uint32_t* ones = reinterpret_cast<uint32_t*>(base_ptr + (ones_base - base));
+    for (int i = threadIdx.x; i < W_ONES_BYTES / 4; i += blockDim.x) ones[i] = 0x3F803F80u;
+    fence_async_smem();   // visible to the tensor cores (async proxy)
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < W_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), P_EPI_WARPS);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, W_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_ptr;
+  auto unit_coords = [&](int u, int& m0, int& n0, int& split, int& kb0, int& kb1) {
+    const int tile = u % p.num_tiles;
+    split = u / p.num_tiles;
+    m0 = (tile / p.tiles_n) * BM;
+    n0 = (tile % p.tiles_n) * W_BN;
+    kb0 = split * p.kb_per_split;
+    kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&p.tmA);
+      prefetch_tmap(&p.tmB);
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        int m0, n0, split, kb0, kb1;
+        unit_coords(u, m0, n0, split, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % W_STAGES;
+          const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
+          mbar_expect_tx(full_bar(s), W_STAGE_BYTES);
+          const int k0 = kb * BK;
+          const uint32_t sa = a_base + s * A_STAGE_BYTES;
+          const uint32_t sb = b_base + s * (W_BN * BK * 2);
+          tma_load_2d(sa, &p.tmA, m0, k0, full_bar(s));
+          tma_load_2d(sa + 8192, &p.tmA, m0 + 64, k0, full_bar(s));
+          tma_load_2d(sb, &p.tmB, n0, k0, full_bar(s));
+          tma_load_2d(sb + 8192, &p.tmB, n0 + 64, k0, full_bar(s));
+        }
+      }
+      for (int i = max(0, it - W_STAGES); i < it; ++i)
+        mbar_wait(full_bar(i % W_STAGES), (uint32_t)(i / W_STAGES) & 1u, p.err);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++tc) {
+        int m0, n0, split, kb0, kb1;
+        unit_coords(u, m0, n0, split, kb0, kb1);
+        const bool do_db = p.db_out != nullptr && n0 == 0;
+        const int buf = tc & 1;
+        if (!mbar_wait(tempty_bar(buf), (((uint32_t)tc >> 1) & 1u) ^ 1u, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * 256);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % W_STAGES;
+          const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
+          if (!mbar_wait(full_bar(s), ph, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = a_base + s * A_STAGE_BYTES;
+          const uint32_t sb = b_base + s * (W_BN * BK * 2);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sdesc(sa + kk * 2048u, 8192u, 1024u);
+            const uint64_t bd = sdesc(sb + kk * 2048u, 8192u, 1024u);
+            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+            mma_bf16(d, ad, bd, p.idesc, acc);
+            if (do_db) mma_bf16(d + 128u, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db, acc);
+          }
+          mma_commit(empty_bar(s));
+        }
+        mma_commit(tfull_bar(buf));
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..9 ----------------
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * W_EPI_BUFS * 4096);
+    uint8_t* stage0_ptr = base_ptr + (stage0 - base);
+    int tc = 0, chunk = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++tc) {
+      int m0, n0, split, kb0, kb1;
+      unit_coords(u, m0, n0, split, kb0, kb1);
+      const bool do_db = p.db_out != nullptr && n0 == 0;
+      const int buf = tc & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), ((uint32_t)tc >> 1) & 1u, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
+      const int gm = m0 + q * 32 + lane;
+      float dbv = 0.f;
+      if (do_db && half == 0) dbv = tmem_ld1(trow + 128u);
+      float v[64];
+      tmem_ld32(trow, v, half * 64);
+      tmem_ld32(trow, v + 32, half * 64 + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(buf));   // this warp's part of TMEM is read
+      if (do_db && half == 0 && gm < p.M) p.db_out[(int64_t)split * p.M + gm] = dbv;
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub, ++chunk) {
+        const int sbuf = chunk % W_EPI_BUFS;
+        if (lane == 0) bulk_wait_read1();
+        __syncwarp();
+        uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
+#pragma unroll
+        for (int w4 = 0; w4 < 8; ++w4) {
+          const float4 f = make_float4(v[sub * 32 + 4 * w4], v[sub * 32 + 4 * w4 + 1], v[sub * 32 + 4 * w4 + 2],
+                                       v[sub * 32 + 4 * w4 + 3]);
+          *reinterpret_cast<float4*>(srow + ((w4 ^ (lane & 7)) << 4)) = f;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&p.tmOut, stage0 + sbuf * 4096, n0 + half * 64 + sub * 32, m0 + q * 32, split);
+          bulk_commit();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, W_TMEM_COLS);
   }
 }
 
@@ -727,7 +965,7 @@ int tc_wgrad_splits(int64_t M, int64_t N, int64_t K) {
   const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, 128);
   const int64_t kbs = ceil_div(K, tc::BK);
   int64_t s = 1;
-  while (tiles * s < kSMs && kbs / (s * 2) >= 8) s *= 2;
+  while (tiles * s < 2 * kSMs && kbs / (s * 2) >= 8) s *= 2;   // >= 2 work units per SM
   return (int)s;
 }
 
@@ -762,6 +1000,87 @@ int device_sms() {
   return n;
 }
 
+// 3-D fp32 tensor map {inner, rows, planes} with row pitch `ld` elements and
+// plane pitch `plane` elements; box {32, 32, 1}; 128B swizzle.
+bool make_tmap_f32_3d(CUtensorMap* tm, const void* ptr, int64_t inner, int64_t rows, int64_t planes, int64_t ld,
+                      int64_t plane, char* err, size_t errlen) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) { snprintf(err, errlen, "cuTensorMapEncodeTiled unavailable"); return false; }
+  if (((uintptr_t)ptr & 15) || ((ld * 4) & 15) || ((plane * 4) & 15)) {
+    snprintf(err, errlen, "fp32 TMA output needs 16-byte aligned base and pitches");
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * 4), (cuuint64_t)(plane * 4)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, errlen, "cuTensorMapEncodeTiled (fp32 3-D) failed (%d)", (int)r);
+    return false;
+  }
+  return true;
+}
+
+const void* tcw_kernel_ptr() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute((const void*)tc::tc_wgrad_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         tc::W_SMEM_BYTES);
+  });
+  return (const void*)tc::tc_wgrad_persistent_kernel;
+}
+
+// Weight gradient on the persistent split-K kernel (+ the fixed-order reduce).
+int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
+  tc::WParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_tmap(&p.tmA, op.A, op.M, op.K, op.lda, 64, 64, err, errlen)) return -1;
+  if (!make_tmap(&p.tmB, op.B, op.N, op.K, op.ldb, 64, 64, err, errlen)) return -1;
+  p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
+  p.num_kb = (int)ceil_div(op.K, tc::BK);
+  int splits = op.splits > 0 ? op.splits : tc_wgrad_splits(op.M, op.N, op.K);
+  if (splits > p.num_kb) splits = p.num_kb;
+  p.kb_per_split = (int)ceil_div(p.num_kb, splits);
+  splits = (int)ceil_div(p.num_kb, p.kb_per_split);
+  p.splits = splits;
+  p.tiles_n = (int)ceil_div(op.N, tc::W_BN);
+  p.num_tiles = (int)(ceil_div(op.M, tc::BM) * p.tiles_n);
+  p.num_units = p.num_tiles * splits;
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(tc::W_BN >> 3) << 17) |
+            ((uint32_t)(tc::BM >> 4) << 24);
+  p.idesc_db = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(16 >> 3) << 17) |
+               ((uint32_t)(tc::BM >> 4) << 24);
+  p.err = op.err;
+  if (splits > 1) {
+    const size_t need = wgrad_workspace_bytes(DT_BF16, op.M, op.N, op.K, splits);
+    if (!op.ws || op.ws_bytes < need) {
+      snprintf(err, errlen, "wgrad workspace too small (%zu < %zu)", op.ws_bytes, need);
+      return -1;
+    }
+    if (!make_tmap_f32_3d(&p.tmOut, op.ws, op.N, op.M, splits, op.N, op.M * op.N, err, errlen)) return -1;
+    p.db_out = op.db ? op.ws + (int64_t)splits * op.M * op.N : nullptr;
+  } else {
+    if (!make_tmap_f32_3d(&p.tmOut, op.dW, op.N, op.M, 1, op.ld_dw, op.M * op.ld_dw, err, errlen)) return -1;
+    p.db_out = op.db;
+  }
+  LaunchRec& r = recs[0];
+  r.func = tcw_kernel_ptr();
+  r.smem = tc::W_SMEM_BYTES;
+  const int sms = device_sms();
+  r.grid = dim3((unsigned)(p.num_units < sms ? p.num_units : sms));
+  r.block = dim3(tc::P_THREADS);
+  r.name = "tc_gemm_wgrad";
+  r.set_args(p);
+  if (splits > 1) {
+    split_reduce_plan(op.ws, splits, op.M, op.N, op.dW, op.ld_dw, op.db, &recs[1]);
+    return 2;
+  }
+  return 1;
+}
+
 // Forward / dgrad on the persistent kernel (bf16 output through TMA stores).
 int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   const int BN = op.N > 128 ? 256 : 128;
@@ -791,7 +1110,7 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   else { r.func = tcp_kernel_ptr<128>(); r.smem = tc::PCfg<128>::SMEM_BYTES; }
   const int sms = device_sms();
   r.grid = dim3((unsigned)(p.num_tiles < sms ? p.num_tiles : sms));
-  r.block = dim3(tc::NUM_THREADS);
+  r.block = dim3(tc::P_THREADS);
   r.name = op.kind == GEMM_FWD ? "tc_gemm_fwd" : "tc_gemm_dgrad";
   r.set_args(p);
   return 1;
@@ -806,6 +1125,7 @@ int tc_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   }
   if ((op.kind == GEMM_FWD || op.kind == GEMM_DGRAD) && op.a_kmajor && op.N > 16)
     return tc_persistent_plan(op, recs, err, errlen);
+  if (op.kind == GEMM_WGRAD && !op.a_kmajor && !op.b_kmajor) return tc_wgrad_plan(op, recs, err, errlen);
   const int BN = pick_bn(op);
   if (!op.b_kmajor && BN % 64) { snprintf(err, errlen, "MN-major B needs BN %% 64 == 0"); return -1; }
   tc::Params p;
