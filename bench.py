@@ -80,7 +80,24 @@ def layer_work(w, kind, l):
         return 0, 4 * B
     if kind == "adamw":
         return 0, w.n_params() * (28 + (2 if w.dtype == 1 else 0))
+    if kind == "split3":   # fp32 input -> three bf16 planes (read 4 B, write 6 B per element)
+        return 0, 10 * B * d[0]
     return 0, 0
+
+
+# fp32 GEMMs on the tensor cores run six bf16 plane products per fp32
+# product: their ceiling is the bf16 peak / 6.
+X3_PRODUCTS = 6
+
+
+def peak_source(peaks, top, w):
+    if top["bound"] == "alu":
+        how = "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"
+    elif top["bound"] == "tensor" and w.dtype == 0:
+        how = "MEASURED_PEAKS.json bf16 burst / 6: fp32 operands as three bf16 planes, six products"
+    else:
+        how = "MEASURED_PEAKS.json burst"
+    return f"{peaks['source']} ({how})"
 
 
 def attach_work(w, prof):
@@ -119,7 +136,9 @@ def roofline_rows(w, rows, peaks):
     for r in rows:
         sec = max(r["ms"], 1e-9) / 1e3
         if r["flops"] and r["kind"] != "head":
-            if w.dtype == 0:
+            if w.dtype == 0 and r["kernel"].startswith("tc_"):
+                bound, peak, unit = "tensor", peaks["bf16_tflops"] / X3_PRODUCTS, "TFLOP/s"
+            elif w.dtype == 0:
                 bound, peak, unit = "alu", FP32_FFMA_PEAK_TFLOPS, "TFLOP/s"
             else:
                 bound, peak, unit = "tensor", peaks["bf16_tflops"], "TFLOP/s"
@@ -316,6 +335,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels", action="store_true", help="include the per-kernel table")
+    ap.add_argument("--f32-ffma", action="store_true",
+                    help="fp32 models: GEMMs on the FFMA pipes instead of the tensor cores")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -342,6 +363,10 @@ def main():
 
     peaks = load_peaks()
     model = nn.Model(w.dims, w.acts, nn.ACT_RELU, w.dtype, seed=w.seed + rank, batch=w.batch, device=local)
+    if w.dtype == 0:
+        model.set_option(nn.OPT_F32_TENSOR_CORES, 0 if args.f32_ffma else 1)
+    gemm_mode = None if w.dtype != 0 else (
+        "FFMA" if args.f32_ffma else "tensor cores, fp32 operands as three bf16 planes (6 products, fp32 accumulate)")
     hyper = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, wd=w.wd)
 
     # device-resident batch pool larger than L2
@@ -452,7 +477,7 @@ def main():
           "frac": round(top["frac"], 4), "traffic": ncu_traffic(top["kernel"], w.name),
           "kernel": f"{top['kernel']} (layer {top['layer'] + 1})" if top["layer"] >= 0 else top["kernel"],
           "launch_ms": round(top["ms"], 5),
-          "peak_source": (f"{peaks['source']} ({'derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz' if top['bound'] == 'alu' else 'MEASURED_PEAKS.json burst'})")}
+          "peak_source": peak_source(peaks, top, w)}
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "samples/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
@@ -460,7 +485,8 @@ def main():
             "data": "synthetic",
             "config": config_of(w, {"l2": f"fresh batch per step from a {n_pool}-batch device pool "
                                           f"({n_pool * per / 2**20:.0f} MiB > 129 MB L2)",
-                                    "graph": "one CUDA-graph replay per step"}),
+                                    "graph": "one CUDA-graph replay per step",
+                                    **({"f32_gemm": gemm_mode} if gemm_mode else {})}),
             "roofline": rf,
             "step_roofline": {"t_roof_ms": round(t_roof_ms, 5), "measured_ms": round(ms_per_step, 5),
                               "frac": round(t_roof_ms / ms_per_step, 4),

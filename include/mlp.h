@@ -70,12 +70,19 @@ typedef enum {
 } mlp_status;
 
 enum { MLP_ACT_NONE = 0, MLP_ACT_RELU = 1, MLP_ACT_GELU_TANH = 2 };
-/* MLP_F32: fp32 everywhere, FFMA GEMMs (no TF32).
+/* MLP_F32: fp32 everywhere (no TF32).  The GEMMs of the training step run
+ *   on the tensor cores with each fp32 operand held as three bf16 planes
+ *   (see MLP_OPT_F32_TENSOR_CORES), or on the FFMA pipes.
  * MLP_BF16: bf16 x / weights copy / activations / logits / gradients of
  * activations, fp32 accumulation, fp32 bias, fp32 master weights, gradients
  * and Adam moments (MuNet "Configuration", precision="mixed"; Orthon
  * "Core capabilities", FP32 master weights). */
 enum { MLP_F32 = 0, MLP_BF16 = 1 };
+/* Operand encoding of the op-level GEMM entry points only (mlp_ops.h): fp32
+ * values as three bf16 planes hi, mid, lo stored one after another, each
+ * plane [rows, ld]:  hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi -
+ * mid), so hi + mid + lo = x exactly for fp32 x in the normal range. */
+enum { MLP_F32X3 = 2 };
 /* Parameter planes, all indexed by the same flat parameter order. */
 enum { MLP_PLANE_P = 0, MLP_PLANE_G = 1, MLP_PLANE_M = 2, MLP_PLANE_V = 3 };
 
@@ -127,7 +134,16 @@ mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
  *     separate GEMM / CE / loss-mean kernels.  Results agree within
  *     rounding; the arithmetic and rounding points are the same.
  * Returns MLP_ERR_ARG for an unknown option. */
-enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1 };
+/*   MLP_OPT_F32_TENSOR_CORES (default 1; MLP_F32 models): run the training
+ *     step's GEMMs on the tensor cores with fp32 operands as three bf16
+ *     planes (MLP_F32X3): the six plane products above 2^-24 relative
+ *     (hi*hi, mid*hi, hi*mid, lo*hi, mid*mid, hi*lo) are accumulated in
+ *     fp32, so each product carries fp32-level error and no TF32 rounding.
+ *     Used where the model allows it: ReLU / no activation, the fused output
+ *     layer (MLP_OPT_FUSE_HEAD on and supported), and input / hidden widths
+ *     below the output layer that are multiples of 8.  Otherwise, or with 0,
+ *     the GEMMs run on the FFMA pipes.  mlp_forward always uses FFMA. */
+enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2 };
 mlp_status mlp_set_option(mlp_t* model, int option, int64_t value);
 
 /* Number of parameters (flat, densely packed) and of Linear layers. */

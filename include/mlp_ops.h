@@ -14,6 +14,11 @@
  *   1 = label outside [0, C), 2 = non-finite loss, 4 = bounded wait gave up.
  * For MLP_BF16 the GEMM operands are read by TMA: every operand base must be
  * 16-byte aligned and every leading dimension a multiple of 8 elements.
+ * The GEMM entry points (linear_act, dgrad, wgrad) also take MLP_F32X3:
+ * every matrix argument that is fp32 under MLP_F32 (X, W, H, dY, dX) is then
+ * three bf16 planes [3][rows][ld] (mlp.h), produced by mlp_op_split3; the
+ * bias, dW and db stay fp32; S is read from its first (hi) plane only, so
+ * only ReLU / no activation are accepted; the TMA rules of MLP_BF16 apply.
  */
 #ifndef MLP_OPS_H_
 #define MLP_OPS_H_
@@ -44,6 +49,12 @@ mlp_status mlp_op_linear_act(int dtype, int act, int64_t M, int64_t N, int64_t K
 mlp_status mlp_op_dgrad(int dtype, int act, int64_t M, int64_t N, int64_t K, const void* dY, int64_t ldy,
                         const void* W, int64_t ldw, const void* S, int64_t lds, void* dX, int64_t ldx,
                         uint32_t* err_dev, void* stream);
+
+/* The three bf16 planes of an fp32 matrix X [rows, cols] (ldx):
+ * P [3][rows][ldp] with P[0] = bf16(X), P[1] = bf16(X - P[0]),
+ * P[2] = bf16(X - P[0] - P[1]) (the MLP_F32X3 encoding, mlp.h). */
+mlp_status mlp_op_split3(int64_t rows, int64_t cols, const float* X, int64_t ldx, void* P, int64_t ldp,
+                         void* stream);
 
 /* Workspace bytes mlp_op_wgrad needs for this shape (0 if none). */
 size_t mlp_op_wgrad_workspace_bytes(int dtype, int64_t N, int64_t K, int64_t B);

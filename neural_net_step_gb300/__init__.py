@@ -20,6 +20,7 @@ STATUS_NAMES = {0: "MLP_OK", 1: "MLP_ERR_ARG", 2: "MLP_ERR_SHAPE", 3: "MLP_ERR_D
                 5: "MLP_ERR_LABEL_RANGE", 6: "MLP_ERR_NONFINITE", 7: "MLP_ERR_STATE", 8: "MLP_ERR_TIMEOUT"}
 ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
 F32, BF16 = 0, 1
+F32X3 = 2   # op-level GEMM operands: fp32 as three bf16 planes [3][rows][ld]
 PLANE_P, PLANE_G, PLANE_M, PLANE_V = 0, 1, 2, 3
 
 
@@ -57,6 +58,7 @@ _SIGS = {
     "mlp_op_wgrad_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I64]),
     "mlp_op_wgrad": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "mlp_op_wgrad_noalloc": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
+    "mlp_op_split3": (_I32, [_I64, _I64, _P, _I64, _P, _I64, _P]),
     "mlp_op_softmax_ce": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _F, _P, _I64, _P, _P, _P]),
     "mlp_op_loss_mean": (_I32, [_I64, _P, _P, _P, _P]),
     "mlp_op_adamw": (_I32, [_I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _P]),
@@ -130,7 +132,7 @@ def mlp_set_graph_mode(h, enable: bool) -> None:
     _check(lib().mlp_set_graph_mode(h, int(bool(enable))))
 
 
-OPT_GRAPH, OPT_FUSE_HEAD = 0, 1
+OPT_GRAPH, OPT_FUSE_HEAD, OPT_F32_TENSOR_CORES = 0, 1, 2
 
 
 def mlp_set_option(h, option: int, value: int) -> None:
@@ -198,6 +200,10 @@ def mlp_op_wgrad_noalloc(dtype, N, K, B, dY, ldy, X, ldx, dW, lddw, db, err, str
     """mlp_op_wgrad for callers that cannot provide a workspace: the split-K
     partial sums live in the library's built-in 16 MiB device array."""
     _check(lib().mlp_op_wgrad_noalloc(dtype, N, K, B, dY, ldy, X, ldx, dW, lddw, db, err, stream))
+
+
+def mlp_op_split3(rows, cols, X, ldx, P, ldp, stream) -> None:
+    _check(lib().mlp_op_split3(rows, cols, X, ldx, P, ldp, stream))
 
 
 def mlp_op_softmax_ce(dtype, B, C, z, ldz, labels, grad_scale, dz, lddz, loss_rows, err, stream) -> None:

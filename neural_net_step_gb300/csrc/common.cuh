@@ -7,7 +7,9 @@
 namespace mlpk {
 
 enum Act : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU_TANH = 2 };
-enum DType : int { DT_F32 = 0, DT_BF16 = 1 };
+// DT_F32X3: fp32 values held as three bf16 planes for the tensor cores
+// (internal to the fp32 model's step; never a model dtype).
+enum DType : int { DT_F32 = 0, DT_BF16 = 1, DT_F32X3 = 2 };
 
 // Device error word bits (latched in the model's control block).
 enum : uint32_t {

@@ -55,6 +55,7 @@ struct HeadParams {
   float grad_scale;
   float* bias_corr;
   float beta1, beta2;
+  int64_t h_plane, dy_plane;           // fp32 h / dY held as three bf16 planes (X3 variant)
 };
 
 struct HeadSmem {
@@ -66,7 +67,30 @@ struct HeadSmem {
   double loss;              // this CTA's loss partial
 };
 
-template <typename T>
+// X3: h and dY are fp32 values held as bf16 planes hi + mid + lo (the sum is
+// the fp32 value exactly); the arithmetic is the fp32 kernel's.
+template <bool X3>
+__device__ __forceinline__ float load_h(const HeadParams& p, int64_t i) {
+  if (!X3) return reinterpret_cast<const float*>(p.h)[i];
+  const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(p.h);
+  return (__bfloat162float(b[i]) + __bfloat162float(b[i + p.h_plane])) + __bfloat162float(b[i + 2 * p.h_plane]);
+}
+template <bool X3>
+__device__ __forceinline__ void store_dy(const HeadParams& p, int64_t i, float v) {
+  if (!X3) {
+    reinterpret_cast<float*>(p.dY)[i] = v;
+    return;
+  }
+  __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(p.dY);
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const float r = v - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r);
+  b[i] = hi;
+  b[i + p.dy_plane] = mid;
+  b[i + 2 * p.dy_plane] = __float2bfloat16_rn(r - __bfloat162float(mid));
+}
+
+template <typename T, bool X3 = false>
 __global__ void __cluster_dims__(kHCluster, 1, 1) __launch_bounds__(kHT)
 head_kernel(const __grid_constant__ HeadParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -93,7 +117,8 @@ head_kernel(const __grid_constant__ HeadParams p) {
     for (int j = 0; j < kHR * kHK / kHT; ++j) {
       const int i = tid + j * kHT;
       const int r = i / kHK, k = i % kHK;
-      s.h[r][k] = r < nr ? to_f32(reinterpret_cast<const T*>(p.h)[(int64_t)(r0 + r) * p.ldh + k]) : 0.f;
+      if (X3) s.h[r][k] = r < nr ? load_h<true>(p, (int64_t)(r0 + r) * p.ldh + k) : 0.f;
+      else s.h[r][k] = r < nr ? to_f32(reinterpret_cast<const T*>(p.h)[(int64_t)(r0 + r) * p.ldh + k]) : 0.f;
     }
     __syncthreads();
     // logits rounded to the model dtype (the value a stored logits tensor holds)
@@ -156,7 +181,8 @@ head_kernel(const __grid_constant__ HeadParams p) {
         if (p.act == ACT_RELU) g = s.h[r][kcol] > 0.f ? 1.f : 0.f;   // this tile's h is the stored h
         else if (p.act == ACT_GELU_TANH)
           g = gelu_tanh_grad(to_f32(reinterpret_cast<const T*>(p.aux)[(int64_t)(r0 + r) * p.ld_aux + kcol]));
-        reinterpret_cast<T*>(p.dY)[(int64_t)(r0 + r) * p.ldy + kcol] = from_f32<T>(a * g);
+        if (X3) store_dy<true>(p, (int64_t)(r0 + r) * p.ldy + kcol, a * g);
+        else reinterpret_cast<T*>(p.dY)[(int64_t)(r0 + r) * p.ldy + kcol] = from_f32<T>(a * g);
       }
     }
     // dW += dz^T h, db += sum dz over the tile's rows (zero rows add 0)
@@ -258,6 +284,11 @@ int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen) {
     snprintf(err, errlen, "fused output layer: unsupported C=%lld K=%lld", (long long)op.C, (long long)op.K);
     return -1;
   }
+  const bool x3 = op.dtype == DT_F32X3;
+  if (x3 && (op.act == ACT_GELU_TANH || op.h_plane < op.B * op.ldh || op.dy_plane < op.B * op.ldy)) {
+    snprintf(err, errlen, "fused output layer: planes need ReLU/none below and full plane pitches");
+    return -1;
+  }
   if (op.ws_bytes < head_workspace_bytes(op.B, op.C, op.K)) {
     snprintf(err, errlen, "fused output layer: workspace too small");
     return -1;
@@ -270,13 +301,15 @@ int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen) {
   q.B = (int)op.B; q.act = op.act;
   q.grad_scale = op.grad_scale;
   q.bias_corr = op.bias_corr; q.beta1 = op.beta1; q.beta2 = op.beta2;
-  const void* fns[2] = {(const void*)head_kernel<float>, (const void*)head_kernel<__nv_bfloat16>};
+  q.h_plane = op.h_plane; q.dy_plane = op.dy_plane;
+  const void* fns[3] = {(const void*)head_kernel<float>, (const void*)head_kernel<__nv_bfloat16>,
+                        (const void*)head_kernel<float, true>};
   static std::once_flag once;
   std::call_once(once, [&] {
     for (const void* f : fns)
       cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(HeadSmem));
   });
-  rec->func = fns[op.dtype == DT_F32 ? 0 : 1];
+  rec->func = fns[x3 ? 2 : op.dtype == DT_F32 ? 0 : 1];
   rec->grid = dim3(head_grid(op.B));
   rec->block = dim3(kHT);
   rec->smem = (unsigned)sizeof(HeadSmem);

@@ -69,6 +69,13 @@ struct Layout {
   int64_t plane_n = 0;            // elements per plane (padded)
   std::vector<int64_t> woff, boff;
   size_t off_P = 0, off_G = 0, off_M = 0, off_V = 0, off_W16 = 0;
+  // fp32 models whose GEMMs can run on the tensor cores with operands as
+  // three bf16 planes: W16 holds the weight planes, xs the input's planes,
+  // h / dY buffers hold planes (6 bytes per element, room for fp32 too)
+  bool x3_ok = false;
+  size_t off_xs = 0;
+  int64_t ld_x = 0;               // row pitch of the input planes
+  int64_t max_ld = 8;             // row pitch bound of the dY ping-pong buffers
   std::vector<size_t> off_h, off_u;
   std::vector<int64_t> ld_h;
   size_t off_z = 0, off_dz = 0;
@@ -117,7 +124,12 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     L.n_params += dims[l + 1] * dims[l] + dims[l + 1];
   }
   L.plane_n = off;
-  const size_t es = dtype == MLP_F32 ? 4 : 2;
+  // tensor cores for an fp32 model: ReLU / none below a fused output layer,
+  // 16-byte TMA rows for every GEMM operand
+  L.x3_ok = dtype == MLP_F32 && L.L >= 2 && head_supported(dims[L.L], dims[L.L - 1]);
+  for (int i = 0; i < n_dims - 2 && L.x3_ok; ++i) L.x3_ok = L.acts[i] != MLP_ACT_GELU_TANH;
+  for (int i = 0; i < L.L - 1 && L.x3_ok; ++i) L.x3_ok = dims[i] % 8 == 0;
+  const size_t es = dtype == MLP_F32 ? (L.x3_ok ? 6 : 4) : 2;   // activation buffers
   size_t cur = 0;
   auto take = [&](size_t bytes) {
     size_t o = cur;
@@ -128,7 +140,9 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
   L.off_G = take(L.plane_n * 4);
   L.off_M = take(L.plane_n * 4);
   L.off_V = take(L.plane_n * 4);
-  L.off_W16 = dtype == MLP_BF16 ? take(L.plane_n * 2) : 0;
+  L.off_W16 = dtype == MLP_BF16 ? take(L.plane_n * 2) : L.x3_ok ? take(L.plane_n * 6) : 0;
+  L.ld_x = (dims[0] + 7) / 8 * 8;
+  L.off_xs = L.x3_ok ? take(batch * L.ld_x * 6) : 0;
   int64_t max_ld = 8;
   for (int l = 0; l < L.L - 1; ++l) {
     int64_t ld = (dims[l + 1] + 7) / 8 * 8;
@@ -140,6 +154,7 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
   L.ldz = (dims[L.L] + 7) / 8 * 8;
   L.off_z = take(batch * L.ldz * es);
   L.off_dz = take(batch * L.ldz * es);
+  L.max_ld = max_ld;
   L.off_dy[0] = take(batch * max_ld * es);
   L.off_dy[1] = take(batch * max_ld * es);
   L.off_loss_rows = take(batch * 4);
@@ -148,6 +163,11 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     int s = wgrad_splits(dtype, dims[l + 1], dims[l], batch);
     size_t b = wgrad_workspace_bytes(dtype, dims[l + 1], dims[l], batch, s);
     ws = b > ws ? b : ws;
+    if (L.x3_ok) {
+      s = wgrad_splits(DT_F32X3, dims[l + 1], dims[l], batch);
+      b = wgrad_workspace_bytes(DT_F32X3, dims[l + 1], dims[l], batch, s);
+      ws = b > ws ? b : ws;
+    }
   }
   if (n_dims >= 3 && head_supported(dims[L.L], dims[L.L - 1])) {
     size_t b = head_workspace_bytes(batch, dims[L.L], dims[L.L - 1]);
@@ -199,6 +219,7 @@ struct mlp {
   size_t arena_bytes = 0;
   bool use_graph = true;
   bool fuse_head = true;     // fused output layer + CE where the shape allows
+  bool f32_tc = true;        // fp32 GEMMs on the tensor cores (three bf16 planes) where the model allows
   std::mutex mu;
   std::vector<GraphCache> graphs;
   int kernels_per_step = 0;
@@ -208,7 +229,9 @@ struct mlp {
                : which == MLP_PLANE_M ? lay.off_M : lay.off_V;
     return reinterpret_cast<float*>(arena + off);
   }
-  void* w16() const { return lay.dtype == MLP_BF16 ? (void*)(arena + lay.off_W16) : nullptr; }
+  void* w16() const { return lay.dtype == MLP_BF16 || lay.x3_ok ? (void*)(arena + lay.off_W16) : nullptr; }
+  // the training step's GEMMs take fp32 operands as bf16 planes
+  bool x3() const { return lay.x3_ok && f32_tc && fuse_head; }
   Ctl* ctl() const { return reinterpret_cast<Ctl*>(arena + lay.off_ctl); }
   size_t es() const { return lay.dtype == MLP_F32 ? 4 : 2; }
   void* at(size_t off) const { return arena + off; }
@@ -217,6 +240,8 @@ struct mlp {
     return lay.dtype == MLP_BF16 ? (const void*)((const uint16_t*)w16() + lay.woff[l])
                                  : (const void*)(plane(MLP_PLANE_P) + lay.woff[l]);
   }
+  // weight of layer l as three bf16 planes (plane pitch lay.plane_n)
+  const void* weight_planes(int l) const { return (const void*)((const uint16_t*)w16() + lay.woff[l]); }
   ~mlp() {
     for (auto& g : graphs) {
       if (g.exec) cudaGraphExecDestroy(g.exec);
@@ -241,28 +266,39 @@ mlp_status add(std::vector<LaunchRec>& out, int n, const LaunchRec* recs) {
     add(out, n_, r_);                                               \
   } while (0)
 
-// Forward GEMMs of all layers (logits into the arena's z buffer).
 // Forward GEMMs of layers [0, n_layers) (all layers: logits into the arena's
-// z buffer).
-mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out, int n_layers = -1) {
+// z buffer).  x3: fp32 model with operands as bf16 planes (the input is
+// split into the arena's xs planes first; hidden outputs are planes).
+mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out, int n_layers = -1,
+                        bool x3 = false) {
   const Layout& L = m->lay;
   const void* X = x;
-  int64_t ldx = L.dims[0];
+  int64_t ldx = L.dims[0], xplane = 0;
   if (n_layers < 0) n_layers = L.L;
+  if (x3) {
+    char e_[512] = "";
+    LaunchRec r;
+    if (split3_plan(L.B, L.dims[0], (const float*)x, L.dims[0], m->at(L.off_xs), L.ld_x, L.B * L.ld_x, &r, e_,
+                    sizeof(e_)) < 0)
+      return fail(MLP_ERR_SHAPE, "%s", e_);
+    out.push_back(r);
+    X = m->at(L.off_xs); ldx = L.ld_x; xplane = L.B * L.ld_x;
+  }
   for (int l = 0; l < n_layers; ++l) {
     GemmOp op;
-    op.dtype = L.dtype;
+    op.dtype = x3 ? DT_F32X3 : L.dtype;
     op.kind = GEMM_FWD;
     op.M = L.B; op.N = L.dims[l + 1]; op.K = L.dims[l];
-    op.A = X; op.lda = ldx; op.a_kmajor = true;
-    op.B = m->weight(l); op.ldb = L.dims[l]; op.b_kmajor = true;
+    op.A = X; op.lda = ldx; op.a_kmajor = true; op.a_plane = xplane;
+    op.B = x3 ? m->weight_planes(l) : m->weight(l); op.ldb = L.dims[l]; op.b_kmajor = true;
+    op.b_plane = L.plane_n;
     op.bias = m->plane(MLP_PLANE_P) + L.boff[l];
     op.err = &m->ctl()->err;
     if (l < L.L - 1) {
       op.act = L.acts[l];
-      op.out = m->at(L.off_h[l]); op.ldo = L.ld_h[l];
+      op.out = m->at(L.off_h[l]); op.ldo = L.ld_h[l]; op.out_plane = L.B * L.ld_h[l];
       if (op.act == MLP_ACT_GELU_TANH) { op.out_u = m->at(L.off_u[l]); op.ldu = L.ld_h[l]; }
-      X = op.out; ldx = L.ld_h[l];
+      X = op.out; ldx = L.ld_h[l]; xplane = op.out_plane;
     } else {
       op.act = MLP_ACT_NONE;
       op.out = m->at(L.off_z); op.ldo = L.ldz;
@@ -278,7 +314,9 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
                      std::vector<LaunchRec>& out) {
   const Layout& L = m->lay;
   const bool fuse = m->fuse_head && L.L >= 2 && head_supported(L.dims[L.L], L.dims[L.L - 1]);
-  mlp_status st = plan_forward(m, x, out, fuse ? L.L - 1 : L.L);
+  const bool x3 = m->x3();   // implies fuse
+  const int64_t dy_plane = L.B * L.max_ld;
+  mlp_status st = plan_forward(m, x, out, fuse ? L.L - 1 : L.L, x3);
   if (st != MLP_OK) return st;
   Ctl* ctl = m->ctl();
   const void* dY = m->at(L.off_dz);
@@ -290,10 +328,11 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     // goes to the first ping-pong buffer
     const int l = L.L - 1;
     HeadOp hd;
-    hd.dtype = L.dtype; hd.act = L.acts[l - 1];
+    hd.dtype = x3 ? DT_F32X3 : L.dtype; hd.act = L.acts[l - 1];
     hd.B = L.B; hd.C = L.dims[L.L]; hd.K = L.dims[l];
     hd.h = m->at(L.off_h[l - 1]); hd.ldh = L.ld_h[l - 1];
-    hd.W = m->weight(l);
+    hd.h_plane = L.B * L.ld_h[l - 1]; hd.dy_plane = dy_plane;
+    hd.W = m->weight(l);   // fp32 master weights for an fp32 model
     hd.bias = m->plane(MLP_PLANE_P) + L.boff[l];
     hd.labels = y;
     hd.aux = hd.act == MLP_ACT_GELU_TANH ? m->at(L.off_u[l - 1]) : m->at(L.off_h[l - 1]);
@@ -339,13 +378,13 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
   }
   float* G = m->plane(MLP_PLANE_G);
   for (int l = top; l >= 0; --l) {
-    const void* Xl = l == 0 ? x : m->at(L.off_h[l - 1]);
-    const int64_t ldxl = l == 0 ? L.dims[0] : L.ld_h[l - 1];
+    const void* Xl = l == 0 ? (x3 ? m->at(L.off_xs) : x) : m->at(L.off_h[l - 1]);
+    const int64_t ldxl = l == 0 ? (x3 ? L.ld_x : L.dims[0]) : L.ld_h[l - 1];
     GemmOp wg;
-    wg.dtype = L.dtype; wg.kind = GEMM_WGRAD;
+    wg.dtype = x3 ? DT_F32X3 : L.dtype; wg.kind = GEMM_WGRAD;
     wg.M = L.dims[l + 1]; wg.N = L.dims[l]; wg.K = L.B;
-    wg.A = dY; wg.lda = ldy; wg.a_kmajor = false;
-    wg.B = Xl; wg.ldb = ldxl; wg.b_kmajor = false;
+    wg.A = dY; wg.lda = ldy; wg.a_kmajor = false; wg.a_plane = dy_plane;
+    wg.B = Xl; wg.ldb = ldxl; wg.b_kmajor = false; wg.b_plane = L.B * ldxl;
     wg.dW = G + L.woff[l]; wg.ld_dw = L.dims[l];
     wg.db = G + L.boff[l];
     wg.ws = (float*)m->at(L.off_ws); wg.ws_bytes = L.ws_bytes;
@@ -353,11 +392,12 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     PLAN_TRY(gemm_plan(wg, r_, e_, sizeof(e_)));
     if (l > 0) {
       GemmOp dg;
-      dg.dtype = L.dtype; dg.kind = GEMM_DGRAD;
+      dg.dtype = x3 ? DT_F32X3 : L.dtype; dg.kind = GEMM_DGRAD;
       dg.act = L.acts[l - 1];
       dg.M = L.B; dg.N = L.dims[l]; dg.K = L.dims[l + 1];
-      dg.A = dY; dg.lda = ldy; dg.a_kmajor = true;
-      dg.B = m->weight(l); dg.ldb = L.dims[l]; dg.b_kmajor = false;
+      dg.A = dY; dg.lda = ldy; dg.a_kmajor = true; dg.a_plane = dy_plane;
+      dg.B = x3 ? m->weight_planes(l) : m->weight(l); dg.ldb = L.dims[l]; dg.b_kmajor = false;
+      dg.b_plane = L.plane_n; dg.out_plane = dy_plane;
       dg.aux = dg.act == MLP_ACT_GELU_TANH ? m->at(L.off_u[l - 1]) : m->at(L.off_h[l - 1]);
       dg.ld_aux = L.ld_h[l - 1];
       dg.out = m->at(L.off_dy[buf]); dg.ldo = L.ld_h[l - 1];
@@ -370,7 +410,8 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
   AdamWOp ad;
   ad.n = L.plane_n;
   ad.p = m->plane(MLP_PLANE_P); ad.g = G; ad.m = m->plane(MLP_PLANE_M); ad.v = m->plane(MLP_PLANE_V);
-  ad.w16 = m->w16();
+  ad.w16 = L.dtype == MLP_BF16 || x3 ? m->w16() : nullptr;
+  ad.w16_plane = x3 ? L.plane_n : 0;
   ad.step_counter = &ctl->step;
   ad.bias_corr = ctl->bias_corr;
   ad.lr = hp.lr; ad.beta1 = hp.b1; ad.beta2 = hp.b2; ad.eps = hp.eps; ad.wd = hp.wd;
@@ -451,6 +492,24 @@ mlp_status run(mlp* m, int key, std::vector<LaunchRec>& recs, cudaStream_t s) {
   return ok();
 }
 
+// The bf16 copy of the P plane the GEMMs read: one plane for a bf16 model,
+// three (hi, mid, lo) for an fp32 model that can run on the tensor cores.
+// Synchronous (create, write_params, option changes).
+cudaError_t refresh_w16(mlp* m) {
+  const Layout& L = m->lay;
+  if (L.dtype != MLP_BF16 && !L.x3_ok) return cudaSuccess;
+  char eb[256];
+  LaunchRec r;
+  int n = L.dtype == MLP_BF16
+              ? cast_bf16_plan(L.plane_n, m->plane(MLP_PLANE_P), m->w16(), &r, eb, sizeof(eb))
+              : split3_plan(1, L.plane_n, m->plane(MLP_PLANE_P), L.plane_n, m->w16(), L.plane_n, L.plane_n, &r, eb,
+                            sizeof(eb));
+  if (n < 0) return cudaErrorInvalidValue;
+  cudaError_t e = launch_rec(r, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return e;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -499,13 +558,7 @@ mlp_status mlp_create(const int64_t* dims, int n_dims, const int* acts, int act,
     for (int64_t i = 0; i < n; ++i) host[L.woff[l] + i] = (float)(rng.normal() * std_);
   }
   if (e == cudaSuccess) e = cudaMemcpy(m->plane(MLP_PLANE_P), host.data(), L.plane_n * 4, cudaMemcpyHostToDevice);
-  if (e == cudaSuccess && dtype == MLP_BF16) {
-    char eb[256];
-    LaunchRec r;
-    cast_bf16_plan(L.plane_n, m->plane(MLP_PLANE_P), m->w16(), &r, eb, sizeof(eb));
-    e = launch_rec(r, 0);
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  }
+  if (e == cudaSuccess) e = refresh_w16(m);
   if (e != cudaSuccess) {
     delete m;
     return fail(MLP_ERR_CUDA, "create: %s", cudaGetErrorString(e));
@@ -545,7 +598,13 @@ mlp_status mlp_set_option(mlp_t* m, int option, int64_t value) {
   switch (option) {
     case MLP_OPT_GRAPH: m->use_graph = value != 0; break;
     case MLP_OPT_FUSE_HEAD: m->fuse_head = value != 0; break;
+    case MLP_OPT_F32_TENSOR_CORES: m->f32_tc = value != 0; break;
     default: return fail(MLP_ERR_ARG, "unknown option %d", option);
+  }
+  if (option != MLP_OPT_GRAPH) {   // the weight planes are only kept current while in use
+    DevGuard g(m->device);
+    cudaError_t e = refresh_w16(m);
+    if (e != cudaSuccess) return fail(MLP_ERR_CUDA, "refreshing weight planes: %s", cudaGetErrorString(e));
   }
   std::vector<LaunchRec> recs;
   mlp_status st = plan_step(m, m->arena, (const int32_t*)m->arena, Hyper{1e-3f, 0.9f, 0.999f, 1e-8f, 0.f},
@@ -687,12 +746,7 @@ mlp_status mlp_write_params(mlp_t* m, int plane, const float* host_in, size_t n,
   mlp_status st = copy_plane(m, plane, nullptr, host_in, n);
   if (st != MLP_OK) return st;
   CUDA_TRY(cudaMemcpy(&m->ctl()->step, &step, sizeof(int64_t), cudaMemcpyHostToDevice));
-  if (plane == MLP_PLANE_P && m->lay.dtype == MLP_BF16) {
-    char eb[256];
-    LaunchRec r;
-    cast_bf16_plan(m->lay.plane_n, m->plane(MLP_PLANE_P), m->w16(), &r, eb, sizeof(eb));
-    CUDA_TRY(launch_rec(r, 0));
-  }
+  if (plane == MLP_PLANE_P) CUDA_TRY(refresh_w16(m));
   CUDA_TRY(cudaDeviceSynchronize());
   return ok();
 }
@@ -728,17 +782,19 @@ static mlp_status run_ops(LaunchRec* r, int n, void* stream) {
 }
 
 static bool dtype_ok(int d) { return d == MLP_F32 || d == MLP_BF16; }
+static bool gemm_dtype_ok(int d) { return d == MLP_F32 || d == MLP_BF16 || d == MLP_F32X3; }
 static bool act_ok(int a) { return a >= MLP_ACT_NONE && a <= MLP_ACT_GELU_TANH; }
 
 mlp_status mlp_op_linear_act(int dtype, int act, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx,
                              const void* W, int64_t ldw, const float* b, void* H, int64_t ldh, void* U, int64_t ldu,
                              uint32_t* err_dev, void* stream) {
-  if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
+  if (!gemm_dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
   if (!act_ok(act)) return fail(MLP_ERR_ARG, "bad activation");
   if (!X || !W || !b || !H) return fail(MLP_ERR_ARG, "null pointer");
   if (ldx < K || ldw < K || ldh < N || (U && ldu < N)) return fail(MLP_ERR_SHAPE, "leading dimension too small");
   GemmOp op;
   op.dtype = dtype; op.kind = GEMM_FWD; op.act = act;
+  op.a_plane = M * ldx; op.b_plane = N * ldw; op.out_plane = M * ldh;
   op.M = M; op.N = N; op.K = K;
   op.A = X; op.lda = ldx; op.a_kmajor = true;
   op.B = W; op.ldb = ldw; op.b_kmajor = true;
@@ -754,12 +810,13 @@ mlp_status mlp_op_linear_act(int dtype, int act, int64_t M, int64_t N, int64_t K
 mlp_status mlp_op_dgrad(int dtype, int act, int64_t M, int64_t N, int64_t K, const void* dY, int64_t ldy,
                         const void* W, int64_t ldw, const void* S, int64_t lds, void* dX, int64_t ldx,
                         uint32_t* err_dev, void* stream) {
-  if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
+  if (!gemm_dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
   if (!act_ok(act)) return fail(MLP_ERR_ARG, "bad activation");
   if (!dY || !W || !dX || (act != MLP_ACT_NONE && !S)) return fail(MLP_ERR_ARG, "null pointer");
   if (ldy < N || ldw < K || ldx < K || (S && lds < K)) return fail(MLP_ERR_SHAPE, "leading dimension too small");
   GemmOp op;
   op.dtype = dtype; op.kind = GEMM_DGRAD; op.act = act;
+  op.a_plane = M * ldy; op.b_plane = N * ldw; op.out_plane = M * ldx;
   op.M = M; op.N = K; op.K = N;
   op.A = dY; op.lda = ldy; op.a_kmajor = true;
   op.B = W; op.ldb = ldw; op.b_kmajor = false;
@@ -774,7 +831,7 @@ mlp_status mlp_op_dgrad(int dtype, int act, int64_t M, int64_t N, int64_t K, con
 }
 
 size_t mlp_op_wgrad_workspace_bytes(int dtype, int64_t N, int64_t K, int64_t B) {
-  if (!dtype_ok(dtype) || N < 1 || K < 1 || B < 1) return 0;
+  if (!gemm_dtype_ok(dtype) || N < 1 || K < 1 || B < 1) return 0;
   int s = wgrad_splits(dtype, N, K, B);
   return wgrad_workspace_bytes(dtype, N, K, B, s);
 }
@@ -782,11 +839,12 @@ size_t mlp_op_wgrad_workspace_bytes(int dtype, int64_t N, int64_t K, int64_t B) 
 mlp_status mlp_op_wgrad(int dtype, int64_t N, int64_t K, int64_t B, const void* dY, int64_t ldy, const void* X,
                         int64_t ldx, float* dW, int64_t lddw, float* db, void* workspace, size_t ws_bytes,
                         uint32_t* err_dev, void* stream) {
-  if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
+  if (!gemm_dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
   if (!dY || !X || !dW) return fail(MLP_ERR_ARG, "null pointer");
   if (ldy < N || ldx < K || lddw < K) return fail(MLP_ERR_SHAPE, "leading dimension too small");
   GemmOp op;
   op.dtype = dtype; op.kind = GEMM_WGRAD;
+  op.a_plane = B * ldy; op.b_plane = B * ldx;
   op.M = N; op.N = K; op.K = B;
   op.A = dY; op.lda = ldy; op.a_kmajor = false;
   op.B = X; op.ldb = ldx; op.b_kmajor = false;
@@ -798,6 +856,17 @@ mlp_status mlp_op_wgrad(int dtype, int64_t N, int64_t K, int64_t B, const void* 
   int n = gemm_plan(op, r, e_, sizeof(e_));
   if (n < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
   return run_ops(r, n, stream);
+}
+
+mlp_status mlp_op_split3(int64_t rows, int64_t cols, const float* X, int64_t ldx, void* P, int64_t ldp,
+                         void* stream) {
+  if (!X || !P) return fail(MLP_ERR_ARG, "null pointer");
+  if (ldx < cols || ldp < cols) return fail(MLP_ERR_SHAPE, "leading dimension too small");
+  LaunchRec r;
+  char e_[512] = "";
+  if (split3_plan(rows, cols, X, ldx, P, ldp, rows * ldp, &r, e_, sizeof(e_)) < 0)
+    return fail(MLP_ERR_SHAPE, "%s", e_);
+  return run_ops(&r, 1, stream);
 }
 
 mlp_status mlp_op_softmax_ce(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, const int32_t* labels,

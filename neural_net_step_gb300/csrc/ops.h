@@ -21,8 +21,14 @@ enum GemmKind : int { GEMM_FWD = 0, GEMM_DGRAD = 1, GEMM_WGRAD = 2 };
 //              gradient fused in.  With splits > 1 the K range is cut into
 //              `splits` chunks whose fp32 partials go to `ws` and are summed
 //              in a fixed order by a second kernel (deterministic).
+//
+// With dtype DT_F32X3 every fp32 operand and fp32 result is held as three
+// bf16 planes (hi, mid, lo; hi + mid + lo = the fp32 value) `a_plane`,
+// `b_plane`, `out_plane` elements apart, and the tensor cores accumulate the
+// six significant plane products in fp32.  aux is then the hi plane of the
+// stored activation (ReLU mask only).
 struct GemmOp {
-  int dtype = 0;            // DT_F32 or DT_BF16 (A, B, out, aux)
+  int dtype = 0;            // DT_F32, DT_BF16 or DT_F32X3 (A, B, out, aux)
   int kind = GEMM_FWD;
   int act = 0;
   int64_t M = 0, N = 0, K = 0;
@@ -37,6 +43,7 @@ struct GemmOp {
   float* ws = nullptr; size_t ws_bytes = 0;
   int splits = 0;           // 0 = choose
   uint32_t* err = nullptr;  // device error word (bounded-wait timeouts)
+  int64_t a_plane = 0, b_plane = 0, out_plane = 0;   // DT_F32X3 plane pitches (elements)
 };
 
 // Number of K splits the wgrad of this shape uses, and the workspace bytes.
@@ -80,6 +87,7 @@ struct AdamWOp {
   int64_t n = 0;
   float* p = nullptr; const float* g = nullptr; float* m = nullptr; float* v = nullptr;
   void* w16 = nullptr;                 // bf16 copy of p written after the update (nullable)
+  int64_t w16_plane = 0;               // > 0: write the three bf16 planes of p, this many apart
   const int64_t* step_counter = nullptr;   // t read from device (already incremented)...
   int64_t t = 0;                       // ...or given explicitly when > 0
   const float* bias_corr = nullptr;    // precomputed [1/(1-b1^t), 1/sqrt(1-b2^t)] (nullable)
@@ -108,6 +116,12 @@ int copy_rows_plan(const CopyRowsOp& op, LaunchRec* rec, char* err, size_t errle
 // w16[i] = bf16_rne(p[i]).
 int cast_bf16_plan(int64_t n, const float* p, void* w16, LaunchRec* rec, char* err, size_t errlen);
 
+// The three bf16 planes of an fp32 [rows, cols] matrix (row pitch lds):
+// dst[pl * plane + r * ldd + c] for pl = 0 (hi), 1 (mid), 2 (lo), with
+// hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid).
+int split3_plan(int64_t rows, int64_t cols, const float* src, int64_t lds, void* dst, int64_t ldd, int64_t plane,
+                LaunchRec* rec, char* err, size_t errlen);
+
 // The output layer fused with softmax-CE for a small class count (C <= 16,
 // K <= 256): logits, loss, dz, dY = (dz W) * act'(aux), dW, db and the mean
 // loss in one kernel (deterministic last-CTA reduction of per-CTA partials).
@@ -130,6 +144,7 @@ struct HeadOp {
   float grad_scale = 1.0f;
   float* bias_corr = nullptr;           // nullable: AdamW bias corrections for the new step
   float beta1 = 0.9f, beta2 = 0.999f;
+  int64_t h_plane = 0, dy_plane = 0;    // DT_F32X3: h and dY as bf16 planes this far apart; W fp32
 };
 bool head_supported(int64_t C, int64_t K);
 size_t head_workspace_bytes(int64_t B, int64_t C, int64_t K);

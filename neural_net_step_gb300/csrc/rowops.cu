@@ -323,7 +323,7 @@ int loss_mean_plan(const LossMeanOp& op, LaunchRec* rec, char* err, size_t errle
 // ---------------------------------------------------------------------------
 struct AdamWParams {
   float* p; const float* g; float* m; float* v;
-  __nv_bfloat16* w16;
+  __nv_bfloat16* w16; int64_t w16_plane;   // w16_plane > 0: three planes (hi, mid, lo)
   const int64_t* step_counter; int64_t t;
   const float* bias_corr;
   int64_t n;
@@ -337,6 +337,26 @@ __device__ __forceinline__ void adamw_one(float& p, float g, float& m, float& v,
   float mhat = m * inv_bc1;
   float denom = sqrtf(v) * inv_sqrt_bc2 + eps;
   p = p - lr * (mhat / denom + wd * p);
+}
+
+// bf16 planes of x: hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid)
+// (hi + mid + lo = x for fp32 x in the normal range; each difference is
+// exact in fp32).
+__device__ __forceinline__ void split3(float x, __nv_bfloat16& hi, __nv_bfloat16& mid, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(x);
+  const float r = x - __bfloat162float(hi);
+  mid = __float2bfloat16_rn(r);
+  lo = __float2bfloat16_rn(r - __bfloat162float(mid));
+}
+__device__ __forceinline__ void store_planes4(__nv_bfloat16* dst, int64_t plane, float4 v) {
+  __nv_bfloat16 h[4], m[4], l[4];
+  split3(v.x, h[0], m[0], l[0]);
+  split3(v.y, h[1], m[1], l[1]);
+  split3(v.z, h[2], m[2], l[2]);
+  split3(v.w, h[3], m[3], l[3]);
+  *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(h);
+  *reinterpret_cast<uint2*>(dst + plane) = *reinterpret_cast<const uint2*>(m);
+  *reinterpret_cast<uint2*>(dst + 2 * plane) = *reinterpret_cast<const uint2*>(l);
 }
 
 __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamWParams q) {
@@ -369,7 +389,9 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
     reinterpret_cast<float4*>(q.p)[i] = p;
     reinterpret_cast<float4*>(q.m)[i] = m;
     reinterpret_cast<float4*>(q.v)[i] = v;
-    if (q.w16) {
+    if (q.w16 && q.w16_plane > 0) {
+      store_planes4(q.w16 + 4 * i, q.w16_plane, p);
+    } else if (q.w16) {
       __nv_bfloat162 lo = __floats2bfloat162_rn(p.x, p.y);
       __nv_bfloat162 hi = __floats2bfloat162_rn(p.z, p.w);
       uint2 o;
@@ -383,7 +405,8 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
     float p = q.p[i], m = q.m[i], v = q.v[i];
     adamw_one(p, q.g[i], m, v, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
     q.p[i] = p; q.m[i] = m; q.v[i] = v;
-    if (q.w16) q.w16[i] = __float2bfloat16_rn(p);
+    if (q.w16 && q.w16_plane > 0) split3(p, q.w16[i], q.w16[i + q.w16_plane], q.w16[i + 2 * q.w16_plane]);
+    else if (q.w16) q.w16[i] = __float2bfloat16_rn(p);
   }
 }
 
@@ -391,12 +414,13 @@ int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
   if (op.n < 0) { snprintf(err, errlen, "adamw: negative size"); return -1; }
   if (op.t <= 0 && !op.step_counter) { snprintf(err, errlen, "adamw: no step"); return -1; }
   auto al = [](const void* ptr, int a) { return ((uintptr_t)ptr % a) == 0; };
-  if (!al(op.p, 16) || !al(op.g, 16) || !al(op.m, 16) || !al(op.v, 16) || (op.w16 && !al(op.w16, 8))) {
-    snprintf(err, errlen, "adamw: planes must be 16-byte aligned (w16: 8)");
+  if (!al(op.p, 16) || !al(op.g, 16) || !al(op.m, 16) || !al(op.v, 16) || (op.w16 && !al(op.w16, 8)) ||
+      op.w16_plane % 4 || (op.w16_plane > 0 && op.w16_plane < op.n)) {
+    snprintf(err, errlen, "adamw: planes must be 16-byte aligned (w16: 8, plane pitch >= n, multiple of 4)");
     return -1;
   }
-  AdamWParams q{op.p, op.g, op.m, op.v, (__nv_bfloat16*)op.w16, op.step_counter, op.t, op.bias_corr, op.n,
-                op.lr, op.beta1, op.beta2, op.eps, op.wd};
+  AdamWParams q{op.p, op.g, op.m, op.v, (__nv_bfloat16*)op.w16, op.w16_plane, op.step_counter, op.t, op.bias_corr,
+                op.n, op.lr, op.beta1, op.beta2, op.eps, op.wd};
   rec->func = (const void*)adamw_kernel;
   int64_t blocks = ceil_div(op.n / 4 + 1, 256);
   if (blocks > 152 * 8) blocks = 152 * 8;
@@ -515,6 +539,58 @@ int cast_bf16_plan(int64_t n, const float* p, void* w16, LaunchRec* rec, char* e
   rec->block = dim3(256);
   rec->smem = 0;
   rec->name = "cast_bf16";
+  rec->set_args(q);
+  return 1;
+}
+
+// ---------------------------------------------------------------------------
+// fp32 matrix -> its three bf16 planes (the fp32 model's operands for the
+// tensor cores).  Streaming: one read of x, three bf16 writes.
+// ---------------------------------------------------------------------------
+struct Split3Params {
+  const float* src; int64_t lds;
+  __nv_bfloat16* dst; int64_t ldd, plane;
+  int64_t rows, cols;
+  int vec;   // 1: 4-wide loads/stores are aligned
+};
+
+__global__ void __launch_bounds__(256) split3_kernel(const __grid_constant__ Split3Params q) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if (q.vec) {
+    const int64_t c4 = q.cols / 4;
+    const int64_t n = q.rows * c4;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+      const int64_t r = i / c4, c = (i - r * c4) * 4;
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(q.src + r * q.lds + c));
+      store_planes4(q.dst + r * q.ldd + c, q.plane, v);
+    }
+  } else {
+    const int64_t n = q.rows * q.cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+      const int64_t r = i / q.cols, c = i - r * q.cols;
+      __nv_bfloat16* d = q.dst + r * q.ldd + c;
+      split3(q.src[r * q.lds + c], d[0], d[q.plane], d[2 * q.plane]);
+    }
+  }
+}
+
+int split3_plan(int64_t rows, int64_t cols, const float* src, int64_t lds, void* dst, int64_t ldd, int64_t plane,
+                LaunchRec* rec, char* err, size_t errlen) {
+  if (rows <= 0 || cols <= 0 || lds < cols || ldd < cols || plane < rows * ldd || !src || !dst) {
+    snprintf(err, errlen, "split3: bad shape");
+    return -1;
+  }
+  Split3Params q{src, lds, (__nv_bfloat16*)dst, ldd, plane, rows, cols, 0};
+  q.vec = cols % 4 == 0 && lds % 4 == 0 && ldd % 4 == 0 && plane % 4 == 0 && (uintptr_t)src % 16 == 0 &&
+          (uintptr_t)dst % 8 == 0;
+  const int64_t work = q.vec ? rows * (cols / 4) : rows * cols;
+  int64_t blocks = ceil_div(work, 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  rec->func = (const void*)split3_kernel;
+  rec->grid = dim3((unsigned)blocks);
+  rec->block = dim3(256);
+  rec->smem = 0;
+  rec->name = "split3";
   rec->set_args(q);
   return 1;
 }

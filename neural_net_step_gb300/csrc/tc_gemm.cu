@@ -419,10 +419,31 @@ template <int BN> struct PCfg {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
 };
 
+// fp32 operands on the tensor cores: an fp32 value x is stored as three bf16
+// planes hi + mid + lo (= x to 24 bits); an fp32 GEMM accumulates the six
+// significant plane products in fp32.  Every bf16 x bf16 product is exact in
+// fp32, so the result carries fp32-level error.  Phase f of the K loop uses
+// planes (pa, pb) below, smallest products first: the accumulator is still
+// small while the small phases are added, so its rounding at each step costs
+// them nothing, and the hi x hi phase accumulates like a plain GEMM.
+__device__ __forceinline__ void prod6_planes(int f, int& pa, int& pb) {
+  // (1,1) (2,0) (0,2) (1,0) (0,1) (0,0)
+  pa = (0x001021 >> (4 * f)) & 0xF;
+  pb = (0x010201 >> (4 * f)) & 0xF;
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(dst),
+      "l"((uint64_t)tm), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
 struct PParams {
   CUtensorMap tmA;
   CUtensorMap tmB;
-  CUtensorMap tmOut;     // bf16 [M rows, N cols], box {64, 32}, 128B swizzle
+  CUtensorMap tmOut;     // bf16 [M rows, N cols] (2-D, or 3-D with 3 planes), box {64, 32}, 128B swizzle
   int M, N, K;
   int num_kb, tiles_n, num_tiles;
   int b_mn;
@@ -450,6 +471,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v, int off) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"((uint64_t)tm),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+// The value whose bf16 rounding is plane `pl` of x (x = hi + mid + lo):
+// pl 0 -> x, pl 1 -> x - hi, pl 2 -> x - hi - mid.  The differences are exact
+// in fp32.
+__device__ __forceinline__ float split_plane(float x, int pl) {
+  if (pl == 0) return x;
+  const float r = x - __bfloat162float(__float2bfloat16_rn(x));
+  if (pl == 1) return r;
+  return r - __bfloat162float(__float2bfloat16_rn(r));
+}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"((uint64_t)tm),
                "r"(src), "r"(c0), "r"(c1)
@@ -461,9 +496,13 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-template <int BN>
+// X3: fp32 operands as three bf16 planes (3-D maps, six K-loop phases) and
+// an fp32 result written as its three planes.
+template <int BN, bool X3>
 __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const __grid_constant__ PParams p) {
   using C = PCfg<BN>;
+  constexpr int NPH = X3 ? 6 : 1;
+  constexpr int OUT_PLANES = X3 ? 3 : 1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -505,21 +544,35 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
       prefetch_tmap(&p.tmB);
       int it = 0;
       bool ok = true;
+      const int kb_total = p.num_kb * NPH;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int kbt = 0; kbt < kb_total; ++kbt, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
           mbar_expect_tx(full_bar(s), stage_tx);
-          const int k0 = kb * BK;
-          tma_load_2d(a_base + s * A_STAGE_BYTES, &p.tmA, k0, m0, full_bar(s));
+          const int k0 = (kbt % p.num_kb) * BK;
+          const uint32_t sa = a_base + s * A_STAGE_BYTES;
           const uint32_t sb = b_base + s * C::B_STAGE_BYTES;
-          if (!p.b_mn) {
-            tma_load_2d(sb, &p.tmB, k0, n0, full_bar(s));
-          } else {
+          if (!X3) {
+            tma_load_2d(sa, &p.tmA, k0, m0, full_bar(s));
+            if (!p.b_mn) {
+              tma_load_2d(sb, &p.tmB, k0, n0, full_bar(s));
+            } else {
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + 8192 * c, &p.tmB, n0 + 64 * c, k0, full_bar(s));
+              for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + 8192 * c, &p.tmB, n0 + 64 * c, k0, full_bar(s));
+            }
+          } else {
+            int pa, pb;
+            prod6_planes(kbt / p.num_kb, pa, pb);
+            tma_load_3d(sa, &p.tmA, k0, m0, pa, full_bar(s));
+            if (!p.b_mn) {
+              tma_load_3d(sb, &p.tmB, k0, n0, pb, full_bar(s));
+            } else {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + 8192 * c, &p.tmB, n0 + 64 * c, k0, pb, full_bar(s));
+            }
           }
         }
       }
@@ -538,7 +591,8 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
         if (!mbar_wait(tempty_bar(buf), (((uint32_t)tc >> 1) & 1u) ^ 1u, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * BN);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const int kb_total = p.num_kb * NPH;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(full_bar(s), ph, p.err)) { ok = false; break; }
@@ -576,7 +630,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
       const int gm = m0 + q * 32 + lane;
       const bool row_ok = gm < p.M;
 #pragma unroll 1
-      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 64, ++chunk) {
+      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 64) {
         const int gn0 = n0 + c0;
         const bool full = gn0 + 64 <= p.N;
         // dgrad: start the loads of the stored activation before reading TMEM
@@ -640,27 +694,33 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
               v[j] *= (row_ok && gn0 + j < p.N) ? act_grad_from_stored(__bfloat162float(ar[j]), p.act) : 0.f;
           }
         }
-        // stage (128B swizzle: 16-byte unit u of row r at r*128 + ((u ^ (r & 7)) * 16)) and store
-        const int sbuf = chunk % C::EPI_BUFS;
-        if (lane == 0) {   // the store that last used this buffer has read it
-          if (C::EPI_BUFS == 1) bulk_wait_read0();
-          else bulk_wait_read1();
-        }
-        __syncwarp();
-        uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
+        // stage (128B swizzle: 16-byte unit u of row r at r*128 + ((u ^ (r & 7)) * 16)) and store;
+        // an fp32 result goes out as its three bf16 planes
+#pragma unroll 1
+        for (int pl = 0; pl < OUT_PLANES; ++pl, ++chunk) {
+          const int sbuf = chunk % C::EPI_BUFS;
+          if (lane == 0) {   // the store that last used this buffer has read it
+            if (C::EPI_BUFS == 1) bulk_wait_read0();
+            else bulk_wait_read1();
+          }
+          __syncwarp();
+          uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint4 w;
-          __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&w);
+          for (int u = 0; u < 8; ++u) {
+            uint4 w;
+            __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&w);
 #pragma unroll
-          for (int h = 0; h < 4; ++h) w2[h] = __floats2bfloat162_rn(v[8 * u + 2 * h], v[8 * u + 2 * h + 1]);
-          *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) << 4)) = w;
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32);
-          bulk_commit();
+            for (int h = 0; h < 4; ++h)
+              w2[h] = __floats2bfloat162_rn(split_plane(v[8 * u + 2 * h], pl), split_plane(v[8 * u + 2 * h + 1], pl));
+            *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) << 4)) = w;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (!X3) tma_store_2d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32);
+            else tma_store_3d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32, pl);
+            bulk_commit();
+          }
         }
       }
     }
@@ -701,18 +761,14 @@ struct WParams {
   CUtensorMap tmB;       // inner N, outer K; box {64, 64}
   CUtensorMap tmOut;     // fp32 3-D {N, M, splits}; box {32, 32, 1}; 128B swizzle
   int M, N, K;
-  int num_kb, kb_per_split, splits;
+  int num_kb, kb_per_split, splits;   // num_kb per phase; splits cut the nph * num_kb sequence
+  int nph;                            // 1: bf16 operands; 6: fp32 operands as three bf16 planes
   int tiles_n, num_tiles, num_units;
   uint32_t idesc, idesc_db;
   float* db_out;         // [splits][M] (nullable: no bias gradient)
   uint32_t* err;
 };
 
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"((uint64_t)tm),
-               "r"(src), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
 __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
   uint32_t r;
   asm volatile(
@@ -722,6 +778,18 @@ __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
       : "r"(taddr)
       : "memory");
   return __uint_as_float(r);
+}
+
+// Whether the K range [kb0, kb1) of a unit holds a k-block that adds to the
+// bias gradient (with planes: one of the phases pairing A with B's plane 0).
+__device__ __forceinline__ bool db_in_range(const WParams& p, int kb0, int kb1) {
+  if (p.nph == 1) return kb1 > kb0;
+  for (int f = 0; f < p.nph; ++f) {
+    int pa, pb;
+    prod6_planes(f, pa, pb);
+    if (pb == 0 && max(kb0, f * p.num_kb) < min(kb1, (f + 1) * p.num_kb)) return true;
+  }
+  return false;
 }
 
 __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const __grid_constant__ WParams p) {
@@ -769,7 +837,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
     m0 = (tile / p.tiles_n) * BM;
     n0 = (tile % p.tiles_n) * W_BN;
     kb0 = split * p.kb_per_split;
-    kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+    kb1 = min(p.num_kb * p.nph, kb0 + p.kb_per_split);
   };
 
   if (warp == 0) {
@@ -787,13 +855,22 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
           const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
           mbar_expect_tx(full_bar(s), W_STAGE_BYTES);
-          const int k0 = kb * BK;
+          const int k0 = (kb % p.num_kb) * BK;
           const uint32_t sa = a_base + s * A_STAGE_BYTES;
           const uint32_t sb = b_base + s * (W_BN * BK * 2);
-          tma_load_2d(sa, &p.tmA, m0, k0, full_bar(s));
-          tma_load_2d(sa + 8192, &p.tmA, m0 + 64, k0, full_bar(s));
-          tma_load_2d(sb, &p.tmB, n0, k0, full_bar(s));
-          tma_load_2d(sb + 8192, &p.tmB, n0 + 64, k0, full_bar(s));
+          if (p.nph == 1) {
+            tma_load_2d(sa, &p.tmA, m0, k0, full_bar(s));
+            tma_load_2d(sa + 8192, &p.tmA, m0 + 64, k0, full_bar(s));
+            tma_load_2d(sb, &p.tmB, n0, k0, full_bar(s));
+            tma_load_2d(sb + 8192, &p.tmB, n0 + 64, k0, full_bar(s));
+          } else {
+            int pa, pb;
+            prod6_planes(kb / p.num_kb, pa, pb);
+            tma_load_3d(sa, &p.tmA, m0, k0, pa, full_bar(s));
+            tma_load_3d(sa + 8192, &p.tmA, m0 + 64, k0, pa, full_bar(s));
+            tma_load_3d(sb, &p.tmB, n0, k0, pb, full_bar(s));
+            tma_load_3d(sb + 8192, &p.tmB, n0 + 64, k0, pb, full_bar(s));
+          }
         }
       }
       for (int i = max(0, it - W_STAGES); i < it; ++i)
@@ -812,6 +889,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
         if (!mbar_wait(tempty_bar(buf), (((uint32_t)tc >> 1) & 1u) ^ 1u, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * 256);
+        bool db_started = false;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % W_STAGES;
           const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
@@ -819,13 +897,19 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
           tc_fence_after();
           const uint32_t sa = a_base + s * A_STAGE_BYTES;
           const uint32_t sb = b_base + s * (W_BN * BK * 2);
+          // the bias gradient sums A's planes once: only in phases that pair
+          // them with B's first plane (all phases when there is one plane)
+          int pa = 0, pb = 0;
+          if (p.nph != 1) prod6_planes(kb / p.num_kb, pa, pb);
+          const bool db_here = do_db && pb == 0;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = sdesc(sa + kk * 2048u, 8192u, 1024u);
             const uint64_t bd = sdesc(sb + kk * 2048u, 8192u, 1024u);
             const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
             mma_bf16(d, ad, bd, p.idesc, acc);
-            if (do_db) mma_bf16(d + 128u, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db, acc);
+            if (db_here) mma_bf16(d + 128u, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db, db_started ? 1u : 0u);
+            if (db_here) db_started = true;
           }
           mma_commit(empty_bar(s));
         }
@@ -851,7 +935,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
       const int gm = m0 + q * 32 + lane;
       float dbv = 0.f;
-      if (do_db && half == 0) dbv = tmem_ld1(trow + 128u);
+      if (do_db && half == 0 && db_in_range(p, kb0, kb1)) dbv = tmem_ld1(trow + 128u);
       float v[64];
       tmem_ld32(trow, v, half * 64);
       tmem_ld32(trow, v + 32, half * 64 + 32);
@@ -940,6 +1024,38 @@ bool make_tmap(CUtensorMap* tm, const void* ptr, int64_t inner, int64_t outer, i
   return true;
 }
 
+// make_tmap over three planes `plane` elements apart (fp32 operands held as
+// bf16 hi/mid/lo planes): dims {inner, outer, 3}.
+bool make_tmap_x3(CUtensorMap* tm, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int64_t plane,
+                  int box_inner, int box_outer, char* err, size_t errlen) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) { snprintf(err, errlen, "cuTensorMapEncodeTiled unavailable"); return false; }
+  if (((uintptr_t)ptr & 15) || ((ld * 2) & 15) || ((plane * 2) & 15) || plane < ld * outer) {
+    snprintf(err, errlen, "plane operand needs a 16-byte aligned base and pitches (ld=%lld plane=%lld)",
+             (long long)ld, (long long)plane);
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, 3};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(plane * 2)};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, errlen, "cuTensorMapEncodeTiled (planes) failed (%d) inner=%lld outer=%lld", (int)r,
+             (long long)inner, (long long)outer);
+    return false;
+  }
+  return true;
+}
+// A 2-D map for bf16 operands, a 3-plane map for DT_F32X3 ones.
+bool make_tmap_op(CUtensorMap* tm, bool x3, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int64_t plane,
+                  int box_inner, int box_outer, char* err, size_t errlen) {
+  return x3 ? make_tmap_x3(tm, ptr, inner, outer, ld, plane, box_inner, box_outer, err, errlen)
+            : make_tmap(tm, ptr, inner, outer, ld, box_inner, box_outer, err, errlen);
+}
+
 template <int BN>
 const void* tc_kernel_ptr() {
   static std::once_flag once;
@@ -961,16 +1077,17 @@ int pick_bn(const GemmOp& op) {
 
 }  // namespace
 
-int tc_wgrad_splits(int64_t M, int64_t N, int64_t K) {
+// nph: K-loop phases per k-block (6 for fp32 operands held as planes).
+int tc_wgrad_splits(int64_t M, int64_t N, int64_t K, int nph = 1) {
   const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, 128);
-  const int64_t kbs = ceil_div(K, tc::BK);
+  const int64_t kbs = ceil_div(K, tc::BK) * nph;
   int64_t s = 1;
   while (tiles * s < 2 * kSMs && kbs / (s * 2) >= 8) s *= 2;   // >= 2 work units per SM
   return (int)s;
 }
 
 int wgrad_splits(int dtype, int64_t M, int64_t N, int64_t K) {
-  return dtype == DT_F32 ? simt_gemm_splits(M, N, K) : tc_wgrad_splits(M, N, K);
+  return dtype == DT_F32 ? simt_gemm_splits(M, N, K) : tc_wgrad_splits(M, N, K, dtype == DT_F32X3 ? 6 : 1);
 }
 
 size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int splits) {
@@ -980,14 +1097,14 @@ size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int spl
 }
 
 namespace {
-template <int BN>
+template <int BN, bool X3>
 const void* tcp_kernel_ptr() {
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute((const void*)tc::tc_gemm_persistent_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         tc::PCfg<BN>::SMEM_BYTES);
+    cudaFuncSetAttribute((const void*)tc::tc_gemm_persistent_kernel<BN, X3>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, tc::PCfg<BN>::SMEM_BYTES);
   });
-  return (const void*)tc::tc_gemm_persistent_kernel<BN>;
+  return (const void*)tc::tc_gemm_persistent_kernel<BN, X3>;
 }
 
 int device_sms() {
@@ -1037,14 +1154,17 @@ const void* tcw_kernel_ptr() {
 int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   tc::WParams p;
   memset(&p, 0, sizeof(p));
-  if (!make_tmap(&p.tmA, op.A, op.M, op.K, op.lda, 64, 64, err, errlen)) return -1;
-  if (!make_tmap(&p.tmB, op.B, op.N, op.K, op.ldb, 64, 64, err, errlen)) return -1;
+  const bool x3 = op.dtype == DT_F32X3;
+  if (!make_tmap_op(&p.tmA, x3, op.A, op.M, op.K, op.lda, op.a_plane, 64, 64, err, errlen)) return -1;
+  if (!make_tmap_op(&p.tmB, x3, op.B, op.N, op.K, op.ldb, op.b_plane, 64, 64, err, errlen)) return -1;
   p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
   p.num_kb = (int)ceil_div(op.K, tc::BK);
-  int splits = op.splits > 0 ? op.splits : tc_wgrad_splits(op.M, op.N, op.K);
-  if (splits > p.num_kb) splits = p.num_kb;
-  p.kb_per_split = (int)ceil_div(p.num_kb, splits);
-  splits = (int)ceil_div(p.num_kb, p.kb_per_split);
+  p.nph = x3 ? 6 : 1;
+  const int kb_total = p.num_kb * p.nph;
+  int splits = op.splits > 0 ? op.splits : tc_wgrad_splits(op.M, op.N, op.K, p.nph);
+  if (splits > kb_total) splits = kb_total;
+  p.kb_per_split = (int)ceil_div(kb_total, splits);
+  splits = (int)ceil_div(kb_total, p.kb_per_split);
   p.splits = splits;
   p.tiles_n = (int)ceil_div(op.N, tc::W_BN);
   p.num_tiles = (int)(ceil_div(op.M, tc::BM) * p.tiles_n);
@@ -1055,7 +1175,7 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
                ((uint32_t)(tc::BM >> 4) << 24);
   p.err = op.err;
   if (splits > 1) {
-    const size_t need = wgrad_workspace_bytes(DT_BF16, op.M, op.N, op.K, splits);
+    const size_t need = wgrad_workspace_bytes(op.dtype, op.M, op.N, op.K, splits);
     if (!op.ws || op.ws_bytes < need) {
       snprintf(err, errlen, "wgrad workspace too small (%zu < %zu)", op.ws_bytes, need);
       return -1;
@@ -1083,16 +1203,19 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
 
 // Forward / dgrad on the persistent kernel (bf16 output through TMA stores).
 int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
-  const int BN = op.N > 128 ? 256 : 128;
+  // 256-wide tiles where they still give every SM a tile
+  const int sms = device_sms();
+  const int BN = op.N > 128 && ceil_div(op.M, tc::BM) * ceil_div(op.N, 256) >= sms ? 256 : 128;
   tc::PParams p;
   memset(&p, 0, sizeof(p));
-  if (!make_tmap(&p.tmA, op.A, op.K, op.M, op.lda, 64, tc::BM, err, errlen)) return -1;
+  const bool x3 = op.dtype == DT_F32X3;
+  if (!make_tmap_op(&p.tmA, x3, op.A, op.K, op.M, op.lda, op.a_plane, 64, tc::BM, err, errlen)) return -1;
   if (op.b_kmajor) {
-    if (!make_tmap(&p.tmB, op.B, op.K, op.N, op.ldb, 64, BN, err, errlen)) return -1;
+    if (!make_tmap_op(&p.tmB, x3, op.B, op.K, op.N, op.ldb, op.b_plane, 64, BN, err, errlen)) return -1;
   } else {
-    if (!make_tmap(&p.tmB, op.B, op.N, op.K, op.ldb, 64, 64, err, errlen)) return -1;
+    if (!make_tmap_op(&p.tmB, x3, op.B, op.N, op.K, op.ldb, op.b_plane, 64, 64, err, errlen)) return -1;
   }
-  if (!make_tmap(&p.tmOut, op.out, op.N, op.M, op.ldo, 64, 32, err, errlen)) return -1;
+  if (!make_tmap_op(&p.tmOut, x3, op.out, op.N, op.M, op.ldo, op.out_plane, 64, 32, err, errlen)) return -1;
   p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
   p.num_kb = (int)ceil_div(op.K, tc::BK);
   p.tiles_n = (int)ceil_div(op.N, BN);
@@ -1106,9 +1229,13 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   p.aux = (const __nv_bfloat16*)op.aux; p.ld_aux = op.ld_aux;
   p.err = op.err;
   LaunchRec& r = recs[0];
-  if (BN == 256) { r.func = tcp_kernel_ptr<256>(); r.smem = tc::PCfg<256>::SMEM_BYTES; }
-  else { r.func = tcp_kernel_ptr<128>(); r.smem = tc::PCfg<128>::SMEM_BYTES; }
-  const int sms = device_sms();
+  if (BN == 256) {
+    r.func = x3 ? tcp_kernel_ptr<256, true>() : tcp_kernel_ptr<256, false>();
+    r.smem = tc::PCfg<256>::SMEM_BYTES;
+  } else {
+    r.func = x3 ? tcp_kernel_ptr<128, true>() : tcp_kernel_ptr<128, false>();
+    r.smem = tc::PCfg<128>::SMEM_BYTES;
+  }
   r.grid = dim3((unsigned)(p.num_tiles < sms ? p.num_tiles : sms));
   r.block = dim3(tc::P_THREADS);
   r.name = op.kind == GEMM_FWD ? "tc_gemm_fwd" : "tc_gemm_dgrad";
@@ -1118,14 +1245,26 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
 }  // namespace
 
 int tc_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
-  if (op.dtype != DT_BF16) { snprintf(err, errlen, "tensor-core GEMM is bf16 only"); return -1; }
+  if (op.dtype != DT_BF16 && op.dtype != DT_F32X3) {
+    snprintf(err, errlen, "tensor-core GEMM takes bf16 or fp32-as-planes operands");
+    return -1;
+  }
   if (op.M <= 0 || op.N <= 0 || op.K <= 0 || op.M > INT32_MAX || op.N > INT32_MAX || op.K > INT32_MAX) {
     snprintf(err, errlen, "bad GEMM shape %lld x %lld x %lld", (long long)op.M, (long long)op.N, (long long)op.K);
     return -1;
   }
-  if ((op.kind == GEMM_FWD || op.kind == GEMM_DGRAD) && op.a_kmajor && op.N > 16)
+  if ((op.kind == GEMM_FWD || op.kind == GEMM_DGRAD) && op.a_kmajor && op.N > 16) {
+    if (op.dtype == DT_F32X3 && (op.out_u || (op.kind == GEMM_DGRAD && op.act == ACT_GELU_TANH))) {
+      snprintf(err, errlen, "fp32 planes: no GELU (its VJP needs the fp32 pre-activation)");
+      return -1;
+    }
     return tc_persistent_plan(op, recs, err, errlen);
+  }
   if (op.kind == GEMM_WGRAD && !op.a_kmajor && !op.b_kmajor) return tc_wgrad_plan(op, recs, err, errlen);
+  if (op.dtype == DT_F32X3) {
+    snprintf(err, errlen, "fp32 planes: no tensor-core kernel for this GEMM form (N=%lld)", (long long)op.N);
+    return -1;
+  }
   const int BN = pick_bn(op);
   if (!op.b_kmajor && BN % 64) { snprintf(err, errlen, "MN-major B needs BN %% 64 == 0"); return -1; }
   tc::Params p;
@@ -1191,6 +1330,7 @@ int tc_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
 }
 
 int gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
+  // fp32 on the FFMA pipes; bf16 and fp32-as-planes on the tensor cores
   return op.dtype == DT_F32 ? simt_gemm_plan(op, recs, err, errlen) : tc_gemm_plan(op, recs, err, errlen);
 }
 

@@ -19,10 +19,12 @@ DEV = "cuda:0"
 W = synth.WORKLOADS
 
 
-def make_model(w: synth.Workload, batch=None, params=None, graph=True):
+def make_model(w: synth.Workload, batch=None, params=None, graph=True, f32_tc=None):
     B = w.batch if batch is None else batch
     m = nn.Model(w.dims, w.acts, nn.ACT_RELU, w.dtype, seed=w.seed, batch=B)
     m.set_graph_mode(graph)
+    if f32_tc is not None:
+        m.set_option(nn.OPT_F32_TENSOR_CORES, f32_tc)
     if params is not None:
         m.write_flat(P.flat([p.numpy() for p in params]).astype(np.float32), nn.PLANE_P, 0)
     return m
@@ -46,14 +48,14 @@ def gpu_run(m: nn.Model, w: synth.Workload, bl, one_graph=False):
             m.split(g.astype(np.float64)))
 
 
-def fp32_one_step(w: synth.Workload, batch=None):
+def fp32_one_step(w: synth.Workload, batch=None, f32_tc=None):
     """One fp32 step from a shared state: loss, every gradient element and
     every parameter element against the oracle with the arithmetic-derived
     bounds of tests/parity.py."""
     B = w.batch if batch is None else batch
     params0 = synth.make_params(w)
     bl = P.batches(w, 1, B)
-    m = make_model(w, B, params0)
+    m = make_model(w, B, params0, f32_tc=f32_tc)
     g_losses, g_params, g_grads = gpu_run(m, w, bl)
     m.close()
     o_losses, o_params, _, _, o_grads = P.oracle_run(w, params0, bl, "fp64")
@@ -70,12 +72,12 @@ def fp32_one_step(w: synth.Workload, batch=None):
         assert n_cond <= 1e-3 * p.size + 2, (i, n_cond)
 
 
-def trajectory_ensemble(w: synth.Workload, n_steps: int, batch=None, one_graph=False):
+def trajectory_ensemble(w: synth.Workload, n_steps: int, batch=None, one_graph=False, f32_tc=None):
     """Free-running trajectory against the oracle and its perturbed ensemble."""
     B = w.batch if batch is None else batch
     params0 = synth.make_params(w)
     bl = P.batches(w, n_steps, B)
-    m = make_model(w, B, params0)
+    m = make_model(w, B, params0, f32_tc=f32_tc)
     g_losses, g_params, g_grads = gpu_run(m, w, bl, one_graph)
     m.close()
     p0 = [P.to64(p) for p in params0]
@@ -104,23 +106,50 @@ def trajectory_ensemble(w: synth.Workload, n_steps: int, batch=None, one_graph=F
 # --------------------------------------------------------------------------
 # fp32: one step, element by element
 # --------------------------------------------------------------------------
-def test_mnist_mlp_b64_one_step():
-    fp32_one_step(W["mnist_mlp_b64"])
+# f32_tc = 1: GEMMs on the tensor cores with fp32 operands as three bf16
+# planes (the default); 0: FFMA.
+F32_MODES = [pytest.param(1, id="tc3planes"), pytest.param(0, id="ffma")]
 
 
-def test_mnist_mlp_b4096_one_step_full_size():
-    fp32_one_step(W["mnist_mlp_b4096"])
+@pytest.mark.parametrize("f32_tc", F32_MODES)
+def test_mnist_mlp_b64_one_step(f32_tc):
+    fp32_one_step(W["mnist_mlp_b64"], f32_tc=f32_tc)
 
 
-def test_mnist_mlp_ragged_batch_one_step():
-    fp32_one_step(W["mnist_mlp_b64"], batch=333)
+@pytest.mark.parametrize("f32_tc", F32_MODES)
+def test_mnist_mlp_b4096_one_step_full_size(f32_tc):
+    fp32_one_step(W["mnist_mlp_b4096"], f32_tc=f32_tc)
+
+
+@pytest.mark.parametrize("f32_tc", F32_MODES)
+def test_mnist_mlp_ragged_batch_one_step(f32_tc):
+    fp32_one_step(W["mnist_mlp_b64"], batch=333, f32_tc=f32_tc)
+
+
+def test_f32_tensor_core_mode_runs_tensor_core_kernels():
+    """The fp32 step's GEMMs run on the tcgen05 kernels in the default mode
+    and on the FFMA kernels with the option off."""
+    w = W["mnist_mlp_b4096"]
+    x, y = P.batches(w, 1)[0]
+    names = {}
+    for tc in (1, 0):
+        m = make_model(w, f32_tc=tc)
+        xd, yd = x.to(DEV), y.to(DEV)
+        prof = nn.mlp_profile_step(m.h, xd.data_ptr(), yd.data_ptr(), w.lr, w.beta1, w.beta2, w.eps, w.wd, None,
+                                   m.stream())
+        names[tc] = [n for n, _ in prof]
+        m.close()
+    assert "split3" in names[1] and "tc_gemm_fwd" in names[1] and "tc_gemm_wgrad" in names[1]
+    assert not any(n.startswith("simt") for n in names[1])
+    assert "simt_gemm_fwd" in names[0] and "split3" not in names[0]
 
 
 # --------------------------------------------------------------------------
 # Trajectories against the oracle ensemble
 # --------------------------------------------------------------------------
-def test_mnist_mlp_b64_three_steps():
-    trajectory_ensemble(W["mnist_mlp_b64"], 3)
+@pytest.mark.parametrize("f32_tc", F32_MODES)
+def test_mnist_mlp_b64_three_steps(f32_tc):
+    trajectory_ensemble(W["mnist_mlp_b64"], 3, f32_tc=f32_tc)
 
 
 @pytest.mark.slow
@@ -289,16 +318,17 @@ def test_shape_mismatch_and_bad_args_fail_before_enqueue():
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("name,batch", [("mnist_mlp_b4096", None), ("mnist_mlp_b64", 333)])
 def test_fused_head_matches_unfused_path(name, batch):
-    """Same step with and without the fused output layer: the arithmetic and
-    rounding points are the same, only the order of fp32 additions differs,
-    so loss and gradients agree to fp32 accumulation error."""
+    """Same step with and without the fused output layer (GEMMs on the FFMA
+    pipes in both): the arithmetic and rounding points are the same, only the
+    order of fp32 additions differs, so loss and gradients agree to fp32
+    accumulation error."""
     w = W[name]
     B = w.batch if batch is None else batch
     params0 = synth.make_params(w)
     bl = P.batches(w, 1, B)
     res = []
     for fuse in (1, 0):
-        m = make_model(w, B, params0)
+        m = make_model(w, B, params0, f32_tc=0)
         m.set_option(nn.OPT_FUSE_HEAD, fuse)
         res.append(gpu_run(m, w, bl))
         m.close()
