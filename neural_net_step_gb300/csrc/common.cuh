@@ -63,15 +63,22 @@ __device__ __forceinline__ float act_grad_from_stored(float s, int act) {
   return 1.0f;
 }
 
+// 1 - beta^t in fp32 without cancellation: -expm1(t log1p(beta - 1)) (beta - 1
+// is exact for beta in [0.5, 1]); a few ulp.  GB300's fp64 pipe is slow, so
+// the step's scalars stay in fp32.
+__device__ __forceinline__ float one_minus_pow(float beta, int64_t t) {
+  return -expm1f((float)t * log1pf(beta - 1.0f));
+}
+
 // Advance the device step counter to t and store AdamW's bias corrections
-// for that step, 1/(1 - beta1^t) and 1/sqrt(1 - beta2^t), computed in fp64
-// (one thread, once per step).
+// for that step, 1/(1 - beta1^t) and 1/sqrt(1 - beta2^t) (one thread, once
+// per step).
 __device__ __forceinline__ void advance_step(int64_t* counter, float* bias_corr, float beta1, float beta2) {
   const int64_t t = *counter + 1;
   *counter = t;
   if (bias_corr) {
-    bias_corr[0] = (float)(1.0 / (1.0 - pow((double)beta1, (double)t)));
-    bias_corr[1] = (float)(1.0 / sqrt(1.0 - pow((double)beta2, (double)t)));
+    bias_corr[0] = 1.0f / one_minus_pow(beta1, t);
+    bias_corr[1] = 1.0f / sqrtf(one_minus_pow(beta2, t));
   }
 }
 

@@ -1,24 +1,24 @@
 // The output layer of the step fused into one kernel for the 10-class,
 // 128-input layer of the MNIST-shaped MLP: logits z = h W^T + b, softmax
 // cross-entropy (loss and dz), the dgrad of the layer with the hidden
-// activation's VJP (dY = (dz W) * act'), and the layer's weight and bias
-// gradients (dW = dz^T h, db = sum dz) with the batch-mean loss.  Each row of
-// h is read once; W lives in shared memory.  This is the single-read
-// cross-entropy of devpost "Orthon" ("Selected Orthon vs. PyTorch results")
-// extended to the whole output layer, with the layer's VJPs written out as in
-// noeira.ai "Neural networks" ("The design in one page": forward and vjp per
-// module).
+// activation's VJP (dY = (dz W) * act'), and the partial sums of the layer's
+// weight and bias gradients (dW = dz^T h, db = sum dz) and of the batch loss.
+// Each row of h is read once; W lives in shared memory.  This is the
+// single-read cross-entropy of devpost "Orthon" ("Selected Orthon vs.
+// PyTorch results") extended to the whole output layer, with the layer's
+// VJPs written out as in noeira.ai "Neural networks" ("The design in one
+// page": forward and vjp per module).
 //
-// Each CTA takes 32-row tiles: the h tile is staged in shared memory, then
-// logits (one thread per row and class), softmax and dz (one thread per row),
-// dY (one thread per input column, looping over the tile's rows) and the
-// dW / db partial sums (one thread per weight) come from shared memory.
-// CTAs run in clusters of 8: after a cluster barrier, rank 0 adds its
-// cluster's partials through distributed shared memory in rank order, and
-// the last cluster leader to finish (an atomic ticket) adds the cluster
-// partials in cluster order -- deterministic -- writes dW, db and the mean
-// loss, advances the step counter and re-arms the ticket.  No CTA spins on
-// another.
+// Each CTA takes 32-row tiles: the h tile is staged in shared memory (16-byte
+// loads), then logits (one thread per row and class), softmax and dz (one
+// thread per row), dY (one thread per 4 columns x 4 rows, 8- or 16-byte
+// stores) and the dW / db partial sums (one thread per weight) come from
+// shared memory.  CTAs run in clusters of 8: after a cluster barrier, CTA
+// rank q adds slice q of the cluster's dW / db partials through distributed
+// shared memory in rank order and writes it to the workspace; the optimizer
+// adds the cluster partials (and the loss partials) in cluster order, so the
+// result is deterministic and no CTA waits for another.  Block 0 advances
+// the step counter and stores AdamW's bias corrections on entry.
 #include <cooperative_groups.h>
 #include <stdio.h>
 
@@ -37,6 +37,7 @@ constexpr int kHT = 256;                  // threads
 constexpr int kHCluster = 8;
 constexpr int kHKP = kHK + 4;             // padded smem pitch (keeps 16-byte rows)
 constexpr int kHPart = kHC * kHK + kHC;   // dW + db partial length
+constexpr int kHPartPitch = 1292;         // kHPart rounded up to 16 bytes
 
 struct HeadParams {
   const void* h; int64_t ldh;          // [B, 128] model dtype (input of the output layer)
@@ -45,12 +46,9 @@ struct HeadParams {
   const int32_t* labels;               // [B]
   const void* aux; int64_t ld_aux;     // stored u of the layer below (GELU only)
   void* dY; int64_t ldy;               // [B, 128] model dtype
-  float* dW; float* db;                // [10, 128], [10] fp32 (gradient plane)
-  float* loss;
   int64_t* step_counter;
   uint32_t* err;
-  float* ws;                           // [clusters][kHPart] fp32, then [clusters] fp64 loss partials
-  unsigned int* ticket;                // zero before the first launch; re-armed by the last leader
+  float* ws;                           // [clusters][kHPartPitch] fp32, then [clusters] fp32 loss partials
   int B, act;
   float grad_scale;
   float* bias_corr;
@@ -63,31 +61,73 @@ struct HeadSmem {
   float h[kHR][kHKP];
   float z[kHR][kHC];        // logits, then dz
   float part[kHPart];       // this CTA's dW / db partial
-  double loss_rows[kHR];
-  double loss;              // this CTA's loss partial
+  float loss_rows[kHR];
+  float loss;               // this CTA's loss partial
 };
 
-// X3: h and dY are fp32 values held as bf16 planes hi + mid + lo (the sum is
-// the fp32 value exactly); the arithmetic is the fp32 kernel's.
-template <bool X3>
-__device__ __forceinline__ float load_h(const HeadParams& p, int64_t i) {
-  if (!X3) return reinterpret_cast<const float*>(p.h)[i];
-  const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(p.h);
-  return (__bfloat162float(b[i]) + __bfloat162float(b[i + p.h_plane])) + __bfloat162float(b[i + 2 * p.h_plane]);
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f[i] = __bfloat162float(e[i]);
 }
-template <bool X3>
-__device__ __forceinline__ void store_dy(const HeadParams& p, int64_t i, float v) {
-  if (!X3) {
-    reinterpret_cast<float*>(p.dY)[i] = v;
-    return;
+
+// 16 consecutive elements of h at element index i (16-byte aligned) as fp32.
+// X3: h is held as bf16 planes hi + mid + lo whose fp32 sum is h exactly.
+template <typename T, bool X3>
+__device__ __forceinline__ void load_h16(const HeadParams& p, int64_t i, float* f) {
+  if (X3) {
+    const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(p.h) + i;
+    uint4 u[6];
+#pragma unroll
+    for (int pl = 0; pl < 3; ++pl) {
+      u[2 * pl] = __ldg(reinterpret_cast<const uint4*>(b + pl * p.h_plane));
+      u[2 * pl + 1] = __ldg(reinterpret_cast<const uint4*>(b + pl * p.h_plane) + 1);
+    }
+    float hi[16], mid[16], lo[16];
+    bf16x8_to_f32(u[0], hi); bf16x8_to_f32(u[1], hi + 8);
+    bf16x8_to_f32(u[2], mid); bf16x8_to_f32(u[3], mid + 8);
+    bf16x8_to_f32(u[4], lo); bf16x8_to_f32(u[5], lo + 8);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) f[j] = (hi[j] + mid[j]) + lo[j];
+  } else if (sizeof(T) == 4) {
+    const float4* q = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.h) + i);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 v = __ldg(q + j);
+      f[4 * j] = v.x; f[4 * j + 1] = v.y; f[4 * j + 2] = v.z; f[4 * j + 3] = v.w;
+    }
+  } else {
+    const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.h) + i);
+    bf16x8_to_f32(__ldg(q), f);
+    bf16x8_to_f32(__ldg(q + 1), f + 8);
   }
-  __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(p.dY);
-  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-  const float r = v - __bfloat162float(hi);
-  const __nv_bfloat16 mid = __float2bfloat16_rn(r);
-  b[i] = hi;
-  b[i + p.dy_plane] = mid;
-  b[i + 2 * p.dy_plane] = __float2bfloat16_rn(r - __bfloat162float(mid));
+}
+
+// 4 consecutive dY elements at element index i (aligned to 4 elements).
+template <typename T, bool X3>
+__device__ __forceinline__ void store_dy4(const HeadParams& p, int64_t i, const float* v) {
+  if (X3) {
+    __nv_bfloat16 hi[4], mid[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      hi[j] = __float2bfloat16_rn(v[j]);
+      const float r = v[j] - __bfloat162float(hi[j]);
+      mid[j] = __float2bfloat16_rn(r);
+      lo[j] = __float2bfloat16_rn(r - __bfloat162float(mid[j]));
+    }
+    __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(p.dY) + i;
+    *reinterpret_cast<uint2*>(b) = *reinterpret_cast<const uint2*>(hi);
+    *reinterpret_cast<uint2*>(b + p.dy_plane) = *reinterpret_cast<const uint2*>(mid);
+    *reinterpret_cast<uint2*>(b + 2 * p.dy_plane) = *reinterpret_cast<const uint2*>(lo);
+  } else if (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.dY) + i) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&a);
+    o.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.dY) + i) = o;
+  }
 }
 
 template <typename T, bool X3 = false>
@@ -95,15 +135,19 @@ __global__ void __cluster_dims__(kHCluster, 1, 1) __launch_bounds__(kHT)
 head_kernel(const __grid_constant__ HeadParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   HeadSmem& s = *reinterpret_cast<HeadSmem*>(smem_raw);
-  __shared__ bool is_last;
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x;
+  // nothing else in the step reads the counter before the optimizer
+  if (blockIdx.x == 0 && tid == 0 && p.step_counter)
+    advance_step(p.step_counter, p.bias_corr, p.beta1, p.beta2);
   for (int i = tid; i < kHC * kHK; i += kHT) s.W[i / kHK][i % kHK] = to_f32(reinterpret_cast<const T*>(p.W)[i]);
-  if (tid < kHR) s.loss_rows[tid] = 0.0;
+  if (tid < kHR) s.loss_rows[tid] = 0.f;
 
-  // this thread's fixed column for dY and its five dW elements
-  const int kcol = tid % kHK;           // dY: column kcol, rows tid/128, +2, +4, ...
-  const int rsub = tid / kHK;           // 0 or 1
+  // dY: this thread's 4 columns kq..kq+3 and rows rq, rq + 8, rq + 16, rq + 24
+  const int kq = 4 * (tid & 31);
+  const int rq = tid >> 5;
+  // h tile staging: row hr, columns hc..hc+15
+  const int hr = tid >> 3, hc = 16 * (tid & 7);
   float acc[kHPart / kHT + 1];
 #pragma unroll
   for (int j = 0; j < kHPart / kHT + 1; ++j) acc[j] = 0.f;
@@ -112,14 +156,17 @@ head_kernel(const __grid_constant__ HeadParams p) {
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int r0 = tile * kHR;
     const int nr = min(kHR, p.B - r0);
+    float hv[16];
+    if (hr < nr) {
+      load_h16<T, X3>(p, (int64_t)(r0 + hr) * p.ldh + hc, hv);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) hv[j] = 0.f;
+    }
     __syncthreads();   // W loaded / previous tile finished with h and z
 #pragma unroll
-    for (int j = 0; j < kHR * kHK / kHT; ++j) {
-      const int i = tid + j * kHT;
-      const int r = i / kHK, k = i % kHK;
-      if (X3) s.h[r][k] = r < nr ? load_h<true>(p, (int64_t)(r0 + r) * p.ldh + k) : 0.f;
-      else s.h[r][k] = r < nr ? to_f32(reinterpret_cast<const T*>(p.h)[(int64_t)(r0 + r) * p.ldh + k]) : 0.f;
-    }
+    for (int j = 0; j < 16; j += 4)
+      *reinterpret_cast<float4*>(&s.h[hr][hc + j]) = make_float4(hv[j], hv[j + 1], hv[j + 2], hv[j + 3]);
     __syncthreads();
     // logits rounded to the model dtype (the value a stored logits tensor holds)
     for (int t = tid; t < kHR * kHC; t += kHT) {
@@ -127,10 +174,10 @@ head_kernel(const __grid_constant__ HeadParams p) {
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 8
       for (int k = 0; k < kHK; k += 4) {
-        const float4 hv = *reinterpret_cast<const float4*>(&s.h[r][k]);
-        const float4 wv = *reinterpret_cast<const float4*>(&s.W[c][k]);
-        a0 = fmaf(hv.x, wv.x, a0); a1 = fmaf(hv.y, wv.y, a1);
-        a2 = fmaf(hv.z, wv.z, a2); a3 = fmaf(hv.w, wv.w, a3);
+        const float4 h4 = *reinterpret_cast<const float4*>(&s.h[r][k]);
+        const float4 w4 = *reinterpret_cast<const float4*>(&s.W[c][k]);
+        a0 = fmaf(h4.x, w4.x, a0); a1 = fmaf(h4.y, w4.y, a1);
+        a2 = fmaf(h4.z, w4.z, a2); a3 = fmaf(h4.w, w4.w, a3);
       }
       s.z[r][c] = to_f32(from_f32<T>((a0 + a1) + (a2 + a3) + p.bias[c]));
     }
@@ -160,7 +207,7 @@ head_kernel(const __grid_constant__ HeadParams p) {
         if (bad) {
           if (p.err) atomicOr(p.err, ERRBIT_LABEL_RANGE);
         } else {
-          s.loss_rows[r] += (double)((m + logf(se)) - zy);
+          s.loss_rows[r] += (m + logf(se)) - zy;
         }
       } else {
 #pragma unroll
@@ -168,21 +215,32 @@ head_kernel(const __grid_constant__ HeadParams p) {
       }
     }
     __syncthreads();
-    // dY = (dz W) * act': column kcol, rows rsub, rsub + 2, ...
+    // dY = (dz W) * act'
     {
-      float wcol[kHC];
+      float4 wq[kHC];
 #pragma unroll
-      for (int c = 0; c < kHC; ++c) wcol[c] = s.W[c][kcol];
-      for (int r = rsub; r < nr; r += kHT / kHK) {
-        float a = 0.f;
+      for (int c = 0; c < kHC; ++c) wq[c] = *reinterpret_cast<const float4*>(&s.W[c][kq]);
 #pragma unroll
-        for (int c = 0; c < kHC; ++c) a = fmaf(s.z[r][c], wcol[c], a);
-        float g = 1.f;
-        if (p.act == ACT_RELU) g = s.h[r][kcol] > 0.f ? 1.f : 0.f;   // this tile's h is the stored h
-        else if (p.act == ACT_GELU_TANH)
-          g = gelu_tanh_grad(to_f32(reinterpret_cast<const T*>(p.aux)[(int64_t)(r0 + r) * p.ld_aux + kcol]));
-        if (X3) store_dy<true>(p, (int64_t)(r0 + r) * p.ldy + kcol, a * g);
-        else reinterpret_cast<T*>(p.dY)[(int64_t)(r0 + r) * p.ldy + kcol] = from_f32<T>(a * g);
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = rq + 8 * rr;
+        if (r < nr) {
+          float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < kHC; ++c) {
+            const float d = s.z[r][c];
+            a[0] = fmaf(d, wq[c].x, a[0]); a[1] = fmaf(d, wq[c].y, a[1]);
+            a[2] = fmaf(d, wq[c].z, a[2]); a[3] = fmaf(d, wq[c].w, a[3]);
+          }
+          if (p.act == ACT_RELU) {   // this tile's h is the stored h
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a[j] *= s.h[r][kq + j] > 0.f ? 1.f : 0.f;
+          } else if (p.act == ACT_GELU_TANH) {
+            const T* u = reinterpret_cast<const T*>(p.aux) + (int64_t)(r0 + r) * p.ld_aux + kq;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a[j] *= gelu_tanh_grad(to_f32(u[j]));
+          }
+          store_dy4<T, X3>(p, (int64_t)(r0 + r) * p.ldy + kq, a);
+        }
       }
     }
     // dW += dz^T h, db += sum dz over the tile's rows (zero rows add 0)
@@ -211,55 +269,31 @@ head_kernel(const __grid_constant__ HeadParams p) {
     if (e < kHPart) s.part[e] = acc[j];
   }
   __syncthreads();
-  if (tid == 0) {
-    double a = 0.0;
-    for (int r = 0; r < kHR; ++r) a += s.loss_rows[r];
-    s.loss = a;
+  if (tid < 32) {   // this CTA's loss partial: a fixed-order tree over the 32 row slots
+    static_assert(kHR == 32, "one loss slot per lane");
+    const float a = warp_sum(s.loss_rows[tid]);
+    if (tid == 0) s.loss = a;
   }
-  // ---- cluster: rank 0 adds the cluster's partials in rank order ----
+  // ---- cluster: CTA rank q adds slice q of the partial vector over the
+  //      cluster's CTAs (in rank order) through distributed shared memory ----
   cluster.sync();
   const unsigned rank = cluster.block_rank();
   const int nclusters = gridDim.x / kHCluster;
   const int cid = blockIdx.x / kHCluster;
-  double* lws = reinterpret_cast<double*>(p.ws + round_up((int64_t)nclusters * kHPart, 2));
-  if (rank == 0) {
-    for (int e = tid; e < kHPart; e += kHT) {
-      float a = 0.f;
-#pragma unroll
-      for (int q = 0; q < kHCluster; ++q) a += cluster.map_shared_rank(&s, q)->part[e];
-      p.ws[(int64_t)cid * kHPart + e] = a;
-    }
-    if (tid == 0) {
-      double a = 0.0;
-      for (int q = 0; q < kHCluster; ++q) a += cluster.map_shared_rank(&s, q)->loss;
-      lws[cid] = a;
-    }
-  }
-  cluster.sync();   // the other CTAs keep their shared memory until rank 0 has read it
-  if (rank != 0) return;
-  // ---- the last cluster leader adds the cluster partials in order ----
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) is_last = atomicAdd(p.ticket, 1u) == (unsigned)nclusters - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  for (int e = tid; e < kHPart; e += kHT) {
+  constexpr int kSlice = (kHPart + kHCluster - 1) / kHCluster;
+  const int e_end = min(kHPart, (int)(rank + 1) * kSlice);
+  for (int e = (int)rank * kSlice + tid; e < e_end; e += kHT) {
     float a = 0.f;
-#pragma unroll 4
-    for (int b = 0; b < nclusters; ++b) a += __ldcg(p.ws + (int64_t)b * kHPart + e);
-    if (e < kHC * kHK) p.dW[e] = a;
-    else p.db[e - kHC * kHK] = a;
+#pragma unroll
+    for (int q = 0; q < kHCluster; ++q) a += cluster.map_shared_rank(&s, q)->part[e];
+    p.ws[(int64_t)cid * kHPartPitch + e] = a;
   }
-  if (tid == 0) {
-    double a = 0.0;
-    for (int b = 0; b < nclusters; ++b) a += __ldcg(lws + b);
-    const float L = (float)(a / (double)p.B);
-    if (p.loss) *p.loss = L;
-    if (p.step_counter) advance_step(p.step_counter, p.bias_corr, p.beta1, p.beta2);
-    if (p.err && !isfinite(L)) atomicOr(p.err, ERRBIT_NONFINITE);
-    *p.ticket = 0u;
+  if (rank == 0 && tid == 0) {
+    float a = 0.f;
+    for (int q = 0; q < kHCluster; ++q) a += cluster.map_shared_rank(&s, q)->loss;
+    p.ws[(int64_t)nclusters * kHPartPitch + cid] = a;
   }
+  cluster.sync();   // every CTA keeps its shared memory until the cluster has read it
 }
 
 namespace {
@@ -271,10 +305,15 @@ int head_grid(int64_t B) {
 }
 }  // namespace
 
-size_t head_workspace_bytes(int64_t B, int64_t C, int64_t K) {
+HeadPartials head_partials(int64_t B, int64_t C, int64_t K) {
   (void)C; (void)K;
   const int nc = head_grid(B) / kHCluster;
-  return (size_t)round_up((int64_t)nc * kHPart, 2) * 4 + (size_t)nc * 8;
+  return HeadPartials{nc, kHPartPitch, (int64_t)nc * kHPartPitch};
+}
+
+size_t head_workspace_bytes(int64_t B, int64_t C, int64_t K) {
+  const HeadPartials hp = head_partials(B, C, K);
+  return (size_t)(hp.loss_off + hp.n) * 4;
 }
 
 bool head_supported(int64_t C, int64_t K) { return C == kHC && K == kHK; }
@@ -289,6 +328,12 @@ int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen) {
     snprintf(err, errlen, "fused output layer: planes need ReLU/none below and full plane pitches");
     return -1;
   }
+  const int64_t al = x3 || op.dtype == DT_BF16 ? 8 : 4;   // 16-byte h rows, 8/16-byte dY stores
+  if (op.ldh % al || op.ldy % al || ((uintptr_t)op.h & 15) || ((uintptr_t)op.dY & 15) ||
+      (x3 && (op.h_plane % 8 || op.dy_plane % 8))) {
+    snprintf(err, errlen, "fused output layer: h / dY need 16-byte aligned rows");
+    return -1;
+  }
   if (op.ws_bytes < head_workspace_bytes(op.B, op.C, op.K)) {
     snprintf(err, errlen, "fused output layer: workspace too small");
     return -1;
@@ -296,8 +341,8 @@ int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen) {
   HeadParams q;
   q.h = op.h; q.ldh = op.ldh; q.W = op.W; q.bias = op.bias; q.labels = op.labels;
   q.aux = op.aux; q.ld_aux = op.ld_aux; q.dY = op.dY; q.ldy = op.ldy;
-  q.dW = op.dW; q.db = op.db; q.loss = op.loss; q.step_counter = op.step_counter; q.err = op.err;
-  q.ws = op.ws; q.ticket = op.ticket;
+  q.step_counter = op.step_counter; q.err = op.err;
+  q.ws = op.ws;
   q.B = (int)op.B; q.act = op.act;
   q.grad_scale = op.grad_scale;
   q.bias_corr = op.bias_corr; q.beta1 = op.beta1; q.beta2 = op.beta2;

@@ -82,13 +82,13 @@ struct Layout {
   int64_t ldz = 0;
   size_t off_dy[2] = {0, 0};
   size_t off_loss_rows = 0, off_ws = 0, ws_bytes = 0, off_ctl = 0;
+  size_t off_hws = 0, hws_bytes = 0;   // the fused output layer's partials (read by the optimizer)
   size_t total = 0;
 };
 
 struct Ctl {   // control block at off_ctl
   int64_t step;
   uint32_t err;
-  uint32_t head_ticket;   // arrival counter of the fused output layer (re-armed to 0 by it)
   float loss_slot;
   float bias_corr[2];     // AdamW 1/(1-b1^t), 1/sqrt(1-b2^t) of the current step
 };
@@ -169,12 +169,12 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
       ws = b > ws ? b : ws;
     }
   }
-  if (n_dims >= 3 && head_supported(dims[L.L], dims[L.L - 1])) {
-    size_t b = head_workspace_bytes(batch, dims[L.L], dims[L.L - 1]);
-    ws = b > ws ? b : ws;
-  }
   L.ws_bytes = ws;
   L.off_ws = take(ws ? ws : 4);
+  if (n_dims >= 3 && head_supported(dims[L.L], dims[L.L - 1])) {
+    L.hws_bytes = head_workspace_bytes(batch, dims[L.L], dims[L.L - 1]);
+    L.off_hws = take(L.hws_bytes);
+  }
   L.off_ctl = take(sizeof(Ctl));
   L.total = cur;
   return MLP_OK;
@@ -338,13 +338,9 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     hd.aux = hd.act == MLP_ACT_GELU_TANH ? m->at(L.off_u[l - 1]) : m->at(L.off_h[l - 1]);
     hd.ld_aux = L.ld_h[l - 1];
     hd.dY = m->at(L.off_dy[0]); hd.ldy = L.ld_h[l - 1];
-    hd.dW = m->plane(MLP_PLANE_G) + L.woff[l];
-    hd.db = m->plane(MLP_PLANE_G) + L.boff[l];
-    hd.loss = loss ? loss : &ctl->loss_slot;
     hd.step_counter = &ctl->step;
     hd.err = &ctl->err;
-    hd.ws = (float*)m->at(L.off_ws); hd.ws_bytes = L.ws_bytes;
-    hd.ticket = &ctl->head_ticket;
+    hd.ws = (float*)m->at(L.off_hws); hd.ws_bytes = L.hws_bytes;
     hd.grad_scale = (float)(1.0 / (double)L.B);
     hd.bias_corr = ctl->bias_corr; hd.beta1 = hp.b1; hd.beta2 = hp.b2;
     char e_[512] = "";
@@ -415,6 +411,16 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
   ad.step_counter = &ctl->step;
   ad.bias_corr = ctl->bias_corr;
   ad.lr = hp.lr; ad.beta1 = hp.b1; ad.beta2 = hp.b2; ad.eps = hp.eps; ad.wd = hp.wd;
+  if (fuse) {   // the output layer's gradient and the loss arrive as partial sums
+    const int l = L.L - 1;
+    const HeadPartials hpart = head_partials(L.B, L.dims[L.L], L.dims[l]);
+    const float* hws = (const float*)m->at(L.off_hws);
+    ad.gpart = hws; ad.gpart_n = hpart.n; ad.gpart_stride = hpart.stride;
+    ad.woff = L.woff[l]; ad.nw = L.dims[L.L] * L.dims[l]; ad.boff = L.boff[l]; ad.nb = L.dims[L.L];
+    ad.loss_parts = hws + hpart.loss_off; ad.loss_n = hpart.n; ad.loss_scale = 1.0f / (float)L.B;
+    ad.loss = loss ? loss : &ctl->loss_slot;
+    ad.err = &ctl->err;
+  }
   char e_[512] = "";
   LaunchRec r;
   if (adamw_plan(ad, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_ARG, "%s", e_);
@@ -898,7 +904,7 @@ mlp_status mlp_op_adamw(int64_t n, float* p, const float* g, float* m, float* v,
   if (!p || !g || !m || !v) return fail(MLP_ERR_ARG, "null pointer");
   if (t < 1) return fail(MLP_ERR_ARG, "t must be >= 1");
   AdamWOp op;
-  op.n = n; op.p = p; op.g = g; op.m = m; op.v = v; op.w16 = w16; op.t = t;
+  op.n = n; op.p = p; op.g = const_cast<float*>(g); op.m = m; op.v = v; op.w16 = w16; op.t = t;
   op.lr = lr; op.beta1 = beta1; op.beta2 = beta2; op.eps = eps; op.wd = wd;
   LaunchRec r;
   char e_[512] = "";

@@ -85,13 +85,23 @@ int loss_mean_plan(const LossMeanOp& op, LaunchRec* rec, char* err, size_t errle
 // AdamW over flat fp32 planes (one launch for every parameter).
 struct AdamWOp {
   int64_t n = 0;
-  float* p = nullptr; const float* g = nullptr; float* m = nullptr; float* v = nullptr;
+  float* p = nullptr; float* g = nullptr; float* m = nullptr; float* v = nullptr;
   void* w16 = nullptr;                 // bf16 copy of p written after the update (nullable)
   int64_t w16_plane = 0;               // > 0: write the three bf16 planes of p, this many apart
   const int64_t* step_counter = nullptr;   // t read from device (already incremented)...
   int64_t t = 0;                       // ...or given explicitly when > 0
   const float* bias_corr = nullptr;    // precomputed [1/(1-b1^t), 1/sqrt(1-b2^t)] (nullable)
   float lr = 0, beta1 = 0, beta2 = 0, eps = 0, wd = 0;
+  // Optional: one layer's gradient left as gpart_n partial sums
+  // [gpart_n][gpart_stride] (element e < nw belongs to g[woff + e], the rest
+  // to g[boff + e - nw]); they are added in a fixed order, written to g and
+  // used.  woff and nw must be multiples of 4.
+  const float* gpart = nullptr; int gpart_n = 0; int64_t gpart_stride = 0;
+  int64_t woff = 0, nw = 0, boff = 0, nb = 0;
+  // Optional: loss = sum(loss_parts[0 .. loss_n)) * loss_scale (one thread;
+  // a non-finite loss sets the error bit in err).
+  const float* loss_parts = nullptr; int loss_n = 0; float loss_scale = 1.f;
+  float* loss = nullptr; uint32_t* err = nullptr;
 };
 int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen);
 
@@ -122,9 +132,10 @@ int cast_bf16_plan(int64_t n, const float* p, void* w16, LaunchRec* rec, char* e
 int split3_plan(int64_t rows, int64_t cols, const float* src, int64_t lds, void* dst, int64_t ldd, int64_t plane,
                 LaunchRec* rec, char* err, size_t errlen);
 
-// The output layer fused with softmax-CE for a small class count (C <= 16,
-// K <= 256): logits, loss, dz, dY = (dz W) * act'(aux), dW, db and the mean
-// loss in one kernel (deterministic last-CTA reduction of per-CTA partials).
+// The output layer fused with softmax-CE for the 10-class, 128-input head:
+// logits, per-row loss, dz, dY = (dz W) * act'(aux), and per-cluster partial
+// sums of dW, db and the loss in the workspace (head_partials), which the
+// optimizer adds in a fixed order.  Block 0 advances the step counter.
 struct HeadOp {
   int dtype = 0;
   int act = 0;                          // activation of the hidden layer below (for its VJP)
@@ -135,12 +146,9 @@ struct HeadOp {
   const int32_t* labels = nullptr;
   const void* aux = nullptr; int64_t ld_aux = 0;
   void* dY = nullptr; int64_t ldy = 0;
-  float* dW = nullptr; float* db = nullptr;
-  float* loss = nullptr;
   int64_t* step_counter = nullptr;
   uint32_t* err = nullptr;
   float* ws = nullptr; size_t ws_bytes = 0;
-  unsigned int* ticket = nullptr;       // a zeroed device word owned by the caller
   float grad_scale = 1.0f;
   float* bias_corr = nullptr;           // nullable: AdamW bias corrections for the new step
   float beta1 = 0.9f, beta2 = 0.999f;
@@ -148,6 +156,11 @@ struct HeadOp {
 };
 bool head_supported(int64_t C, int64_t K);
 size_t head_workspace_bytes(int64_t B, int64_t C, int64_t K);
+// What the fused output layer leaves in its workspace for the optimizer:
+// n partial sums of [dW (C*K, row-major), db (C)] with row pitch `stride`
+// floats, then n loss partials starting at float offset `loss_off`.
+struct HeadPartials { int n; int64_t stride; int64_t loss_off; };
+HeadPartials head_partials(int64_t B, int64_t C, int64_t K);
 int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen);
 
 // Set the message mlp_last_error() returns on the calling thread.

@@ -322,13 +322,33 @@ int loss_mean_plan(const LossMeanOp& op, LaunchRec* rec, char* err, size_t errle
 //   p = p - lr * (m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps) + wd * p_old).
 // ---------------------------------------------------------------------------
 struct AdamWParams {
-  float* p; const float* g; float* m; float* v;
+  float* p; float* g; float* m; float* v;
   __nv_bfloat16* w16; int64_t w16_plane;   // w16_plane > 0: three planes (hi, mid, lo)
   const int64_t* step_counter; int64_t t;
   const float* bias_corr;
   int64_t n;
   float lr, beta1, beta2, eps, wd;
+  // one layer's gradient as partial sums (added here in a fixed order and
+  // written to g): [gpart_n][gpart_stride], element e < nw -> g[woff + e],
+  // else g[boff + e - nw]
+  const float* gpart; int gpart_n; int64_t gpart_stride, woff, nw, boff, nb;
+  // batch loss = sum(loss_parts) * loss_scale, by one thread (nullable)
+  const float* loss_parts; int loss_n; float loss_scale; float* loss; uint32_t* err;
 };
+
+// Gradient element f: from the partial sums when f lies in the partial
+// layer's weight or bias range, else from the gradient plane.
+__device__ __forceinline__ float grad_elem(const AdamWParams& q, int64_t f, bool& from_parts) {
+  int64_t e = -1;
+  if (f >= q.woff && f < q.woff + q.nw) e = f - q.woff;
+  else if (f >= q.boff && f < q.boff + q.nb) e = q.nw + f - q.boff;
+  from_parts = e >= 0;
+  if (e < 0) return q.g[f];
+  float a = 0.f;
+#pragma unroll 8
+  for (int b = 0; b < q.gpart_n; ++b) a += __ldcg(q.gpart + (int64_t)b * q.gpart_stride + e);
+  return a;
+}
 
 __device__ __forceinline__ void adamw_one(float& p, float g, float& m, float& v, float lr, float b1,
                                           float b2, float eps, float wd, float inv_bc1, float inv_sqrt_bc2) {
@@ -360,17 +380,21 @@ __device__ __forceinline__ void store_planes4(__nv_bfloat16* dst, int64_t plane,
 }
 
 __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamWParams q) {
-  // bias corrections: precomputed for the step, else 1 - beta^t in fp64 once
-  // per CTA
+  // bias corrections: precomputed for the step, else computed once per CTA
   __shared__ float s_bc[2];
   if (q.bias_corr) {
     if (threadIdx.x == 0) { s_bc[0] = q.bias_corr[0]; s_bc[1] = q.bias_corr[1]; }
   } else if (threadIdx.x == 0) {
     const int64_t t = q.t > 0 ? q.t : *q.step_counter;
-    const double bc1 = 1.0 - pow((double)q.beta1, (double)t);
-    const double bc2 = 1.0 - pow((double)q.beta2, (double)t);
-    s_bc[0] = (float)(1.0 / bc1);
-    s_bc[1] = (float)(1.0 / sqrt(bc2));
+    s_bc[0] = 1.0f / one_minus_pow(q.beta1, t);
+    s_bc[1] = 1.0f / sqrtf(one_minus_pow(q.beta2, t));
+  }
+  if (q.loss_parts && blockIdx.x == 0 && threadIdx.x == 0) {
+    float a = 0.f;
+    for (int c = 0; c < q.loss_n; ++c) a += __ldcg(q.loss_parts + c);
+    const float L = a * q.loss_scale;   // loss_scale = 1/B: the batch mean
+    if (q.loss) *q.loss = L;
+    if (q.err && !isfinite(L)) atomicOr(q.err, ERRBIT_NONFINITE);
   }
   __syncthreads();
   const float inv_bc1 = s_bc[0];
@@ -379,7 +403,15 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
     float4 p = reinterpret_cast<float4*>(q.p)[i];
-    float4 g = reinterpret_cast<const float4*>(q.g)[i];
+    float4 g;
+    const int64_t f = 4 * i;
+    if (q.gpart && ((f + 3 >= q.woff && f < q.woff + q.nw) || (f + 3 >= q.boff && f < q.boff + q.nb))) {
+      bool a, b, c, d;
+      g = make_float4(grad_elem(q, f, a), grad_elem(q, f + 1, b), grad_elem(q, f + 2, c), grad_elem(q, f + 3, d));
+      reinterpret_cast<float4*>(q.g)[i] = g;   // the gradient plane holds the summed gradient
+    } else {
+      g = reinterpret_cast<const float4*>(q.g)[i];
+    }
     float4 m = reinterpret_cast<float4*>(q.m)[i];
     float4 v = reinterpret_cast<float4*>(q.v)[i];
     adamw_one(p.x, g.x, m.x, v.x, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
@@ -403,7 +435,10 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
   // tail (n not a multiple of 4)
   for (int64_t i = n4 * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < q.n; i += stride) {
     float p = q.p[i], m = q.m[i], v = q.v[i];
-    adamw_one(p, q.g[i], m, v, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
+    bool fp = false;
+    const float g = q.gpart ? grad_elem(q, i, fp) : q.g[i];
+    if (fp) q.g[i] = g;
+    adamw_one(p, g, m, v, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
     q.p[i] = p; q.m[i] = m; q.v[i] = v;
     if (q.w16 && q.w16_plane > 0) split3(p, q.w16[i], q.w16[i + q.w16_plane], q.w16[i + 2 * q.w16_plane]);
     else if (q.w16) q.w16[i] = __float2bfloat16_rn(p);
@@ -419,8 +454,15 @@ int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
     snprintf(err, errlen, "adamw: planes must be 16-byte aligned (w16: 8, plane pitch >= n, multiple of 4)");
     return -1;
   }
+  if (op.gpart && (op.gpart_n < 1 || op.gpart_stride < op.nw + op.nb || op.woff % 4 || op.nw % 4 ||
+                   op.woff + op.nw > op.n || op.boff + op.nb > op.n)) {
+    snprintf(err, errlen, "adamw: bad gradient partials");
+    return -1;
+  }
   AdamWParams q{op.p, op.g, op.m, op.v, (__nv_bfloat16*)op.w16, op.w16_plane, op.step_counter, op.t, op.bias_corr,
-                op.n, op.lr, op.beta1, op.beta2, op.eps, op.wd};
+                op.n, op.lr, op.beta1, op.beta2, op.eps, op.wd,
+                op.gpart, op.gpart_n, op.gpart_stride, op.woff, op.nw, op.boff, op.nb,
+                op.loss_parts, op.loss_n, op.loss_scale, op.loss, op.err};
   rec->func = (const void*)adamw_kernel;
   int64_t blocks = ceil_div(op.n / 4 + 1, 256);
   if (blocks > 152 * 8) blocks = 152 * 8;

@@ -408,15 +408,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 constexpr int P_EPI_WARPS = 8;
 constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;   // producer warp, MMA warp, 8 epilogue warps
 // epilogue staging: per warp, 1 or 2 buffers of 32 rows x 128 B
+//
+// A k-block's loads take about a microsecond to land (L2 across the two
+// dies), so a stage must buy enough MMA time: bf16 stages are 32-48 KB, four
+// or five deep; with fp32 operands as planes (X3) a stage holds all three
+// planes of A and of B (96 KB, two deep) and feeds six MMA groups.  X3 keeps
+// two accumulators per TMEM buffer: hi x hi, and the five smaller products.
 
-template <int BN> struct PCfg {
-  static constexpr int B_STAGE_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-  static constexpr int STAGES = 4;
-  static constexpr int EPI_BUFS = BN >= 256 ? 1 : 2;   // staging buffers per epilogue warp
+template <int BN, bool X3 = false> struct PCfg {
+  static constexpr int NPL = X3 ? 3 : 1;                 // operand planes per stage
+  static constexpr int A_BYTES = NPL * A_STAGE_BYTES;
+  static constexpr int B_PLANE_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = NPL * B_PLANE_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = X3 ? 2 : (BN >= 256 ? 4 : 5);
+  static constexpr int EPI_BUFS = (X3 || BN >= 256) ? 1 : 2;   // staging buffers per epilogue warp
   static constexpr int EPI_BYTES = P_EPI_WARPS * EPI_BUFS * 4096;
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int ACC_COLS = X3 ? 2 * BN : BN;      // TMEM columns per accumulator buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
+  static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 // fp32 operands on the tensor cores: an fp32 value x is stored as three bf16
@@ -471,6 +483,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v, int off) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 64 consecutive TMEM columns of this warp's 32 lanes: two x32 loads and one
+// wait in a single statement (the outputs are defined only after the wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + 32u)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"((uint64_t)tm),
                "r"(src), "r"(c0), "r"(c1), "r"(c2)
@@ -500,16 +535,15 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 // an fp32 result written as its three planes.
 template <int BN, bool X3>
 __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const __grid_constant__ PParams p) {
-  using C = PCfg<BN>;
-  constexpr int NPH = X3 ? 6 : 1;
+  using C = PCfg<BN, X3>;
   constexpr int OUT_PLANES = X3 ? 3 : 1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
   const uint32_t a_base = base;
-  const uint32_t b_base = base + C::STAGES * A_STAGE_BYTES;
-  const uint32_t epi_base = b_base + C::STAGES * C::B_STAGE_BYTES;
+  const uint32_t b_base = base + C::STAGES * C::A_BYTES;
+  const uint32_t epi_base = b_base + C::STAGES * C::B_BYTES;
   const uint32_t bar_base = epi_base + C::EPI_BYTES;
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
@@ -535,7 +569,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
-  const uint32_t stage_tx = A_STAGE_BYTES + C::B_STAGE_BYTES;
+  const uint32_t stage_tx = C::STAGE_BYTES;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -544,17 +578,16 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
       prefetch_tmap(&p.tmB);
       int it = 0;
       bool ok = true;
-      const int kb_total = p.num_kb * NPH;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
-        for (int kbt = 0; kbt < kb_total; ++kbt, ++it) {
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
           mbar_expect_tx(full_bar(s), stage_tx);
-          const int k0 = (kbt % p.num_kb) * BK;
-          const uint32_t sa = a_base + s * A_STAGE_BYTES;
-          const uint32_t sb = b_base + s * C::B_STAGE_BYTES;
+          const int k0 = kb * BK;
+          const uint32_t sa = a_base + s * C::A_BYTES;
+          const uint32_t sb = b_base + s * C::B_BYTES;
           if (!X3) {
             tma_load_2d(sa, &p.tmA, k0, m0, full_bar(s));
             if (!p.b_mn) {
@@ -564,14 +597,16 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
               for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + 8192 * c, &p.tmB, n0 + 64 * c, k0, full_bar(s));
             }
           } else {
-            int pa, pb;
-            prod6_planes(kbt / p.num_kb, pa, pb);
-            tma_load_3d(sa, &p.tmA, k0, m0, pa, full_bar(s));
-            if (!p.b_mn) {
-              tma_load_3d(sb, &p.tmB, k0, n0, pb, full_bar(s));
-            } else {
 #pragma unroll
-              for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + 8192 * c, &p.tmB, n0 + 64 * c, k0, pb, full_bar(s));
+            for (int pl = 0; pl < 3; ++pl) {   // every plane of A and B once
+              tma_load_3d(sa + pl * A_STAGE_BYTES, &p.tmA, k0, m0, pl, full_bar(s));
+              const uint32_t sbp = sb + pl * C::B_PLANE_BYTES;
+              if (!p.b_mn) {
+                tma_load_3d(sbp, &p.tmB, k0, n0, pl, full_bar(s));
+              } else {
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c) tma_load_3d(sbp + 8192 * c, &p.tmB, n0 + 64 * c, k0, pl, full_bar(s));
+              }
             }
           }
         }
@@ -590,20 +625,38 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
         const int buf = tc & 1;
         if (!mbar_wait(tempty_bar(buf), (((uint32_t)tc >> 1) & 1u) ^ 1u, p.err)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * BN);
-        const int kb_total = p.num_kb * NPH;
-        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+        const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(full_bar(s), ph, p.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = a_base + s * A_STAGE_BYTES;
-          const uint32_t sb = b_base + s * C::B_STAGE_BYTES;
+          const uint32_t sa = a_base + s * C::A_BYTES;
+          const uint32_t sb = b_base + s * C::B_BYTES;
+          if (!X3) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sdesc(sa + kk * 32u, 16u, 1024u);
-            const uint64_t bd = sdesc(sb + kk * b_kstep, b_lbo, 1024u);
-            mma_bf16(d, ad, bd, p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = sdesc(sa + kk * 32u, 16u, 1024u);
+              const uint64_t bd = sdesc(sb + kk * b_kstep, b_lbo, 1024u);
+              mma_bf16(d, ad, bd, p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
+            // five small products into the second accumulator (smallest
+            // first), then hi x hi into the first
+#pragma unroll
+            for (int f = 0; f < 6; ++f) {
+              int pa, pb;
+              prod6_planes(f, pa, pb);
+              const uint32_t dd = f < 5 ? d + BN : d;
+              const uint32_t spa = sa + pa * A_STAGE_BYTES, spb = sb + pb * C::B_PLANE_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                const uint64_t ad = sdesc(spa + kk * 32u, 16u, 1024u);
+                const uint64_t bd = sdesc(spb + kk * b_kstep, b_lbo, 1024u);
+                const bool first = kb == 0 && kk == 0 && (f == 0 || f == 5);
+                mma_bf16(dd, ad, bd, p.idesc, first ? 0u : 1u);
+              }
+            }
           }
           mma_commit(empty_bar(s));
         }
@@ -626,24 +679,56 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), ((uint32_t)tc >> 1) & 1u, p.err));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::ACC_COLS);
       const int gm = m0 + q * 32 + lane;
       const bool row_ok = gm < p.M;
+      // 64-column chunks of this warp's half of the tile: read from TMEM once,
+      // finished in registers, then each output plane is staged in
+      // 128B-swizzled shared memory (16-byte unit u of row r at
+      // r*128 + ((u ^ (r & 7)) * 16)) and written by a TMA store.
 #pragma unroll 1
       for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 64) {
         const int gn0 = n0 + c0;
-        const bool full = gn0 + 64 <= p.N;
-        // dgrad: start the loads of the stored activation before reading TMEM
-        uint4 aux[8];
-        const bool use_aux = p.kind == GEMM_DGRAD && p.act != ACT_NONE;
-        const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
-        if (use_aux && row_ok && full) {
+        // the chunk's bias (lane j: columns j and 32 + j) or ReLU mask of the
+        // stored activation, loaded before the TMEM read
+        float bias0 = 0.f, bias1 = 0.f;
+        uint32_t mask0 = 0u, mask1 = 0u;
+        if (p.kind == GEMM_FWD) {
+          if (gn0 + lane < p.N) bias0 = __ldg(p.bias + gn0 + lane);
+          if (gn0 + 32 + lane < p.N) bias1 = __ldg(p.bias + gn0 + 32 + lane);
+        } else if (p.act == ACT_RELU && row_ok) {
+          const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
+          if (gn0 + 64 <= p.N) {
+            uint4 a[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) aux[u] = __ldg(reinterpret_cast<const uint4*>(ar) + u);
+            for (int u = 0; u < 8; ++u) a[u] = __ldg(reinterpret_cast<const uint4*>(ar) + u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&a[u]);
+              uint32_t bits = 0u;
+#pragma unroll
+              for (int h = 0; h < 8; ++h) bits |= (__bfloat162float(e[h]) > 0.f ? 1u : 0u) << h;
+              if (u < 4) mask0 |= bits << (8 * u);
+              else mask1 |= bits << (8 * (u - 4));
+            }
+          } else {
+            for (int j = 0; j < 32; ++j) {
+              if (gn0 + j < p.N && __bfloat162float(ar[j]) > 0.f) mask0 |= 1u << j;
+              if (gn0 + 32 + j < p.N && __bfloat162float(ar[32 + j]) > 0.f) mask1 |= 1u << j;
+            }
+          }
         }
         float v[64];
-        tmem_ld32(trow, v, c0);
-        tmem_ld32(trow, v + 32, c0 + 32);
+        tmem_ld64(trow + (uint32_t)c0, v);
+        if (X3) {   // hi x hi + the five smaller products
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            float w[32];
+            tmem_ld32(trow + (uint32_t)(BN + c0 + 32 * hh), w, 0);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[32 * hh + j] += w[j];
+          }
+        }
         if (c0 + 64 >= (half + 1) * (BN / 2)) {
           // this warp's part of the TMEM buffer is drained: hand it back
           tc_fence_before();
@@ -651,19 +736,14 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
           if (lane == 0) mbar_arrive(tempty_bar(buf));
         }
         if (p.kind == GEMM_FWD) {
-          if (full) {
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              const float4 b4 = __ldg(reinterpret_cast<const float4*>(p.bias + gn0 + j));
-              v[j] += b4.x; v[j + 1] += b4.y; v[j + 2] += b4.z; v[j + 3] += b4.w;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) v[j] += gn0 + j < p.N ? __ldg(p.bias + gn0 + j) : 0.f;
+          for (int j = 0; j < 32; ++j) {
+            v[j] += __shfl_sync(0xffffffffu, bias0, j);
+            v[32 + j] += __shfl_sync(0xffffffffu, bias1, j);
           }
           if (p.out_u && row_ok) {
             __nv_bfloat16* du = p.out_u + (int64_t)gm * p.ldu + gn0;
-            if (full) {
+            if (gn0 + 64 <= p.N) {
 #pragma unroll
               for (int j = 0; j < 64; j += 8) {
                 uint4 w;
@@ -680,22 +760,28 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
           }
 #pragma unroll
           for (int j = 0; j < 64; ++j) v[j] = apply_act(v[j], p.act);
-        } else if (use_aux) {   // GEMM_DGRAD
-          if (row_ok && full) {
+        } else if (p.act == ACT_RELU) {   // dgrad: dX * 1[h > 0]
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] *= (float)((mask0 >> j) & 1u);
+            v[32 + j] *= (float)((mask1 >> j) & 1u);
+          }
+        } else if (p.act == ACT_GELU_TANH) {   // dgrad: dX * gelu'(u) (bf16 only)
+          const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
+          if (row_ok && gn0 + 64 <= p.N) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&aux[u]);
+              const uint4 a = __ldg(reinterpret_cast<const uint4*>(ar) + u);
+              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&a);
 #pragma unroll
-              for (int h = 0; h < 8; ++h) v[8 * u + h] *= act_grad_from_stored(__bfloat162float(e[h]), p.act);
+              for (int h = 0; h < 8; ++h) v[8 * u + h] *= gelu_tanh_grad(__bfloat162float(e[h]));
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 64; ++j)
-              v[j] *= (row_ok && gn0 + j < p.N) ? act_grad_from_stored(__bfloat162float(ar[j]), p.act) : 0.f;
+              v[j] *= (row_ok && gn0 + j < p.N) ? gelu_tanh_grad(__bfloat162float(ar[j])) : 0.f;
           }
         }
-        // stage (128B swizzle: 16-byte unit u of row r at r*128 + ((u ^ (r & 7)) * 16)) and store;
-        // an fp32 result goes out as its three bf16 planes
 #pragma unroll 1
         for (int pl = 0; pl < OUT_PLANES; ++pl, ++chunk) {
           const int sbuf = chunk % C::EPI_BUFS;
@@ -1102,7 +1188,7 @@ const void* tcp_kernel_ptr() {
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute((const void*)tc::tc_gemm_persistent_kernel<BN, X3>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, tc::PCfg<BN>::SMEM_BYTES);
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, tc::PCfg<BN, X3>::SMEM_BYTES);
   });
   return (const void*)tc::tc_gemm_persistent_kernel<BN, X3>;
 }
@@ -1205,10 +1291,10 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
 int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   // 256-wide tiles where they still give every SM a tile
   const int sms = device_sms();
-  const int BN = op.N > 128 && ceil_div(op.M, tc::BM) * ceil_div(op.N, 256) >= sms ? 256 : 128;
+  const bool x3 = op.dtype == DT_F32X3;   // 128-wide tiles only (three planes per stage)
+  const int BN = !x3 && op.N > 128 && ceil_div(op.M, tc::BM) * ceil_div(op.N, 256) >= sms ? 256 : 128;
   tc::PParams p;
   memset(&p, 0, sizeof(p));
-  const bool x3 = op.dtype == DT_F32X3;
   if (!make_tmap_op(&p.tmA, x3, op.A, op.K, op.M, op.lda, op.a_plane, 64, tc::BM, err, errlen)) return -1;
   if (op.b_kmajor) {
     if (!make_tmap_op(&p.tmB, x3, op.B, op.K, op.N, op.ldb, op.b_plane, 64, BN, err, errlen)) return -1;
@@ -1229,11 +1315,14 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   p.aux = (const __nv_bfloat16*)op.aux; p.ld_aux = op.ld_aux;
   p.err = op.err;
   LaunchRec& r = recs[0];
-  if (BN == 256) {
-    r.func = x3 ? tcp_kernel_ptr<256, true>() : tcp_kernel_ptr<256, false>();
+  if (x3) {
+    r.func = tcp_kernel_ptr<128, true>();
+    r.smem = tc::PCfg<128, true>::SMEM_BYTES;
+  } else if (BN == 256) {
+    r.func = tcp_kernel_ptr<256, false>();
     r.smem = tc::PCfg<256>::SMEM_BYTES;
   } else {
-    r.func = x3 ? tcp_kernel_ptr<128, true>() : tcp_kernel_ptr<128, false>();
+    r.func = tcp_kernel_ptr<128, false>();
     r.smem = tc::PCfg<128>::SMEM_BYTES;
   }
   r.grid = dim3((unsigned)(p.num_tiles < sms ? p.num_tiles : sms));
