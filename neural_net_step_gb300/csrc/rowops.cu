@@ -405,10 +405,29 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
     float4 p = reinterpret_cast<float4*>(q.p)[i];
     float4 g;
     const int64_t f = 4 * i;
-    if (q.gpart && ((f + 3 >= q.woff && f < q.woff + q.nw) || (f + 3 >= q.boff && f < q.boff + q.nb))) {
+    if (q.gpart && f >= q.woff && f + 3 < q.woff + q.nw) {
+      // four weights from the partial sums: 16-byte loads, all in flight
+      // (woff, nw and the partial pitch are multiples of 4)
+      const float* src = q.gpart + (f - q.woff);
+      float4 part[16];
+#pragma unroll
+      for (int b = 0; b < 16; ++b)
+        part[b] = b < q.gpart_n ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)b * q.gpart_stride))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      g = part[0];
+#pragma unroll
+      for (int b = 1; b < 16; ++b) {
+        g.x += part[b].x; g.y += part[b].y; g.z += part[b].z; g.w += part[b].w;
+      }
+      for (int b = 16; b < q.gpart_n; ++b) {
+        const float4 t = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)b * q.gpart_stride));
+        g.x += t.x; g.y += t.y; g.z += t.z; g.w += t.w;
+      }
+      reinterpret_cast<float4*>(q.g)[i] = g;   // the gradient plane holds the summed gradient
+    } else if (q.gpart && f + 3 >= q.boff && f < q.boff + q.nb) {
       bool a, b, c, d;
       g = make_float4(grad_elem(q, f, a), grad_elem(q, f + 1, b), grad_elem(q, f + 2, c), grad_elem(q, f + 3, d));
-      reinterpret_cast<float4*>(q.g)[i] = g;   // the gradient plane holds the summed gradient
+      reinterpret_cast<float4*>(q.g)[i] = g;
     } else {
       g = reinterpret_cast<const float4*>(q.g)[i];
     }
@@ -454,7 +473,8 @@ int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
     snprintf(err, errlen, "adamw: planes must be 16-byte aligned (w16: 8, plane pitch >= n, multiple of 4)");
     return -1;
   }
-  if (op.gpart && (op.gpart_n < 1 || op.gpart_stride < op.nw + op.nb || op.woff % 4 || op.nw % 4 ||
+  if (op.gpart && (op.gpart_n < 1 || op.gpart_stride < op.nw + op.nb || op.gpart_stride % 4 || op.woff % 4 ||
+                   op.nw % 4 || (uintptr_t)op.gpart % 16 ||
                    op.woff + op.nw > op.n || op.boff + op.nb > op.n)) {
     snprintf(err, errlen, "adamw: bad gradient partials");
     return -1;

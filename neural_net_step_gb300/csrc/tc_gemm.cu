@@ -834,21 +834,33 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
 // workspace that a fixed-order reduce kernel sums (several splits).
 // ---------------------------------------------------------------------------
 constexpr int W_BN = 128;
-constexpr int W_STAGES = 4;
-constexpr int W_STAGE_BYTES = A_STAGE_BYTES + W_BN * BK * 2;   // 32 KB
 constexpr int W_EPI_BUFS = 2;
 constexpr int W_EPI_BYTES = P_EPI_WARPS * W_EPI_BUFS * 4096;
 constexpr int W_ONES_BYTES = 16 * 128;                          // 16 rows x 64 bf16
 constexpr int W_TMEM_COLS = 512;                                // 2 x (128 dW + 32 db), stride 256
-constexpr int W_SMEM_BYTES = W_STAGES * W_STAGE_BYTES + W_EPI_BYTES + W_ONES_BYTES + 1024 + 256;
+// X3 (fp32 operands as three bf16 planes): a stage holds every plane of a
+// 32-row K slice of A and B (48 KB, three deep) and feeds the six products,
+// smallest first, into one accumulator per work unit.
+template <bool X3> struct WCfg {
+  static constexpr int NPL = X3 ? 3 : 1;
+  static constexpr int BKW = X3 ? 32 : 64;                 // K rows per stage
+  static constexpr int CHUNK_BYTES = 64 * BKW * 2;         // one 64-wide MN chunk of a plane
+  static constexpr int A_PLANE_BYTES = (BM / 64) * CHUNK_BYTES;
+  static constexpr int B_PLANE_BYTES = (W_BN / 64) * CHUNK_BYTES;
+  static constexpr int A_BYTES = NPL * A_PLANE_BYTES;
+  static constexpr int B_BYTES = NPL * B_PLANE_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = X3 ? 3 : 4;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + W_EPI_BYTES + W_ONES_BYTES + 1024 + 256;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
 
 struct WParams {
   CUtensorMap tmA;       // A^T storage: inner M, outer K; box {64, 64}
   CUtensorMap tmB;       // inner N, outer K; box {64, 64}
   CUtensorMap tmOut;     // fp32 3-D {N, M, splits}; box {32, 32, 1}; 128B swizzle
   int M, N, K;
-  int num_kb, kb_per_split, splits;   // num_kb per phase; splits cut the nph * num_kb sequence
-  int nph;                            // 1: bf16 operands; 6: fp32 operands as three bf16 planes
+  int num_kb, kb_per_split, splits;   // K stages (32 or 64 rows each), split into units
   int tiles_n, num_tiles, num_units;
   uint32_t idesc, idesc_db;
   float* db_out;         // [splits][M] (nullable: no bias gradient)
@@ -866,26 +878,17 @@ __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
   return __uint_as_float(r);
 }
 
-// Whether the K range [kb0, kb1) of a unit holds a k-block that adds to the
-// bias gradient (with planes: one of the phases pairing A with B's plane 0).
-__device__ __forceinline__ bool db_in_range(const WParams& p, int kb0, int kb1) {
-  if (p.nph == 1) return kb1 > kb0;
-  for (int f = 0; f < p.nph; ++f) {
-    int pa, pb;
-    prod6_planes(f, pa, pb);
-    if (pb == 0 && max(kb0, f * p.num_kb) < min(kb1, (f + 1) * p.num_kb)) return true;
-  }
-  return false;
-}
-
+template <bool X3>
 __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const __grid_constant__ WParams p) {
+  using C = WCfg<X3>;
+  constexpr int W_STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
   const uint32_t a_base = base;
-  const uint32_t b_base = base + W_STAGES * A_STAGE_BYTES;
-  const uint32_t epi_base = b_base + W_STAGES * (W_BN * BK * 2);
+  const uint32_t b_base = base + W_STAGES * C::A_BYTES;
+  const uint32_t epi_base = b_base + W_STAGES * C::B_BYTES;
   const uint32_t ones_base = epi_base + W_EPI_BYTES;
   const uint32_t bar_base = ones_base + W_ONES_BYTES;
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
@@ -923,7 +926,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
     m0 = (tile / p.tiles_n) * BM;
     n0 = (tile % p.tiles_n) * W_BN;
     kb0 = split * p.kb_per_split;
-    kb1 = min(p.num_kb * p.nph, kb0 + p.kb_per_split);
+    kb1 = min(p.num_kb, kb0 + p.kb_per_split);
   };
 
   if (warp == 0) {
@@ -940,22 +943,24 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
           const int s = it % W_STAGES;
           const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
-          mbar_expect_tx(full_bar(s), W_STAGE_BYTES);
-          const int k0 = (kb % p.num_kb) * BK;
-          const uint32_t sa = a_base + s * A_STAGE_BYTES;
-          const uint32_t sb = b_base + s * (W_BN * BK * 2);
-          if (p.nph == 1) {
+          mbar_expect_tx(full_bar(s), C::STAGE_BYTES);
+          const int k0 = kb * C::BKW;
+          const uint32_t sa = a_base + s * C::A_BYTES;
+          const uint32_t sb = b_base + s * C::B_BYTES;
+          if (!X3) {
             tma_load_2d(sa, &p.tmA, m0, k0, full_bar(s));
-            tma_load_2d(sa + 8192, &p.tmA, m0 + 64, k0, full_bar(s));
+            tma_load_2d(sa + C::CHUNK_BYTES, &p.tmA, m0 + 64, k0, full_bar(s));
             tma_load_2d(sb, &p.tmB, n0, k0, full_bar(s));
-            tma_load_2d(sb + 8192, &p.tmB, n0 + 64, k0, full_bar(s));
+            tma_load_2d(sb + C::CHUNK_BYTES, &p.tmB, n0 + 64, k0, full_bar(s));
           } else {
-            int pa, pb;
-            prod6_planes(kb / p.num_kb, pa, pb);
-            tma_load_3d(sa, &p.tmA, m0, k0, pa, full_bar(s));
-            tma_load_3d(sa + 8192, &p.tmA, m0 + 64, k0, pa, full_bar(s));
-            tma_load_3d(sb, &p.tmB, n0, k0, pb, full_bar(s));
-            tma_load_3d(sb + 8192, &p.tmB, n0 + 64, k0, pb, full_bar(s));
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl) {   // every plane of A and B once
+              const uint32_t spa = sa + pl * C::A_PLANE_BYTES, spb = sb + pl * C::B_PLANE_BYTES;
+              tma_load_3d(spa, &p.tmA, m0, k0, pl, full_bar(s));
+              tma_load_3d(spa + C::CHUNK_BYTES, &p.tmA, m0 + 64, k0, pl, full_bar(s));
+              tma_load_3d(spb, &p.tmB, n0, k0, pl, full_bar(s));
+              tma_load_3d(spb + C::CHUNK_BYTES, &p.tmB, n0 + 64, k0, pl, full_bar(s));
+            }
           }
         }
       }
@@ -981,21 +986,28 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
           const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
           if (!mbar_wait(full_bar(s), ph, p.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = a_base + s * A_STAGE_BYTES;
-          const uint32_t sb = b_base + s * (W_BN * BK * 2);
-          // the bias gradient sums A's planes once: only in phases that pair
-          // them with B's first plane (all phases when there is one plane)
-          int pa = 0, pb = 0;
-          if (p.nph != 1) prod6_planes(kb / p.num_kb, pa, pb);
-          const bool db_here = do_db && pb == 0;
+          const uint32_t sa = a_base + s * C::A_BYTES;
+          const uint32_t sb = b_base + s * C::B_BYTES;
+          // products (pa, pb) of the planes, smallest first; the bias
+          // gradient sums each plane of A once, in the products that pair it
+          // with B's first plane
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sdesc(sa + kk * 2048u, 8192u, 1024u);
-            const uint64_t bd = sdesc(sb + kk * 2048u, 8192u, 1024u);
-            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-            mma_bf16(d, ad, bd, p.idesc, acc);
-            if (db_here) mma_bf16(d + 128u, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db, db_started ? 1u : 0u);
-            if (db_here) db_started = true;
+          for (int f = 0; f < (X3 ? 6 : 1); ++f) {
+            int pa = 0, pb = 0;
+            if (X3) prod6_planes(f, pa, pb);
+            const bool db_here = do_db && pb == 0;
+            const uint32_t spa = sa + pa * C::A_PLANE_BYTES, spb = sb + pb * C::B_PLANE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < C::BKW / 16; ++kk) {
+              const uint64_t ad = sdesc(spa + kk * 2048u, (uint32_t)C::CHUNK_BYTES, 1024u);
+              const uint64_t bd = sdesc(spb + kk * 2048u, (uint32_t)C::CHUNK_BYTES, 1024u);
+              const uint32_t acc = (kb > kb0 || f > 0 || kk > 0) ? 1u : 0u;
+              mma_bf16(d, ad, bd, p.idesc, acc);
+              if (db_here) {
+                mma_bf16(d + 128u, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db, db_started ? 1u : 0u);
+                db_started = true;
+              }
+            }
           }
           mma_commit(empty_bar(s));
         }
@@ -1021,7 +1033,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
       const int gm = m0 + q * 32 + lane;
       float dbv = 0.f;
-      if (do_db && half == 0 && db_in_range(p, kb0, kb1)) dbv = tmem_ld1(trow + 128u);
+      if (do_db && half == 0 && kb1 > kb0) dbv = tmem_ld1(trow + 128u);
       float v[64];
       tmem_ld32(trow, v, half * 64);
       tmem_ld32(trow, v + 32, half * 64 + 32);
@@ -1163,17 +1175,18 @@ int pick_bn(const GemmOp& op) {
 
 }  // namespace
 
-// nph: K-loop phases per k-block (6 for fp32 operands held as planes).
-int tc_wgrad_splits(int64_t M, int64_t N, int64_t K, int nph = 1) {
+// bk: K rows per pipeline stage (32 for fp32 operands held as planes).
+int tc_wgrad_splits(int64_t M, int64_t N, int64_t K, int bk = tc::BK) {
   const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, 128);
-  const int64_t kbs = ceil_div(K, tc::BK) * nph;
+  const int64_t kbs = ceil_div(K, bk);
   int64_t s = 1;
   while (tiles * s < 2 * kSMs && kbs / (s * 2) >= 8) s *= 2;   // >= 2 work units per SM
   return (int)s;
 }
 
 int wgrad_splits(int dtype, int64_t M, int64_t N, int64_t K) {
-  return dtype == DT_F32 ? simt_gemm_splits(M, N, K) : tc_wgrad_splits(M, N, K, dtype == DT_F32X3 ? 6 : 1);
+  return dtype == DT_F32 ? simt_gemm_splits(M, N, K)
+                         : tc_wgrad_splits(M, N, K, dtype == DT_F32X3 ? tc::WCfg<true>::BKW : tc::BK);
 }
 
 size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int splits) {
@@ -1227,13 +1240,14 @@ bool make_tmap_f32_3d(CUtensorMap* tm, const void* ptr, int64_t inner, int64_t r
   return true;
 }
 
+template <bool X3>
 const void* tcw_kernel_ptr() {
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute((const void*)tc::tc_wgrad_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         tc::W_SMEM_BYTES);
+    cudaFuncSetAttribute((const void*)tc::tc_wgrad_persistent_kernel<X3>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, tc::WCfg<X3>::SMEM_BYTES);
   });
-  return (const void*)tc::tc_wgrad_persistent_kernel;
+  return (const void*)tc::tc_wgrad_persistent_kernel<X3>;
 }
 
 // Weight gradient on the persistent split-K kernel (+ the fixed-order reduce).
@@ -1241,16 +1255,15 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   tc::WParams p;
   memset(&p, 0, sizeof(p));
   const bool x3 = op.dtype == DT_F32X3;
-  if (!make_tmap_op(&p.tmA, x3, op.A, op.M, op.K, op.lda, op.a_plane, 64, 64, err, errlen)) return -1;
-  if (!make_tmap_op(&p.tmB, x3, op.B, op.N, op.K, op.ldb, op.b_plane, 64, 64, err, errlen)) return -1;
+  const int bkw = x3 ? tc::WCfg<true>::BKW : tc::WCfg<false>::BKW;
+  if (!make_tmap_op(&p.tmA, x3, op.A, op.M, op.K, op.lda, op.a_plane, 64, bkw, err, errlen)) return -1;
+  if (!make_tmap_op(&p.tmB, x3, op.B, op.N, op.K, op.ldb, op.b_plane, 64, bkw, err, errlen)) return -1;
   p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
-  p.num_kb = (int)ceil_div(op.K, tc::BK);
-  p.nph = x3 ? 6 : 1;
-  const int kb_total = p.num_kb * p.nph;
-  int splits = op.splits > 0 ? op.splits : tc_wgrad_splits(op.M, op.N, op.K, p.nph);
-  if (splits > kb_total) splits = kb_total;
-  p.kb_per_split = (int)ceil_div(kb_total, splits);
-  splits = (int)ceil_div(kb_total, p.kb_per_split);
+  p.num_kb = (int)ceil_div(op.K, bkw);
+  int splits = op.splits > 0 ? op.splits : wgrad_splits(op.dtype, op.M, op.N, op.K);
+  if (splits > p.num_kb) splits = p.num_kb;
+  p.kb_per_split = (int)ceil_div(p.num_kb, splits);
+  splits = (int)ceil_div(p.num_kb, p.kb_per_split);
   p.splits = splits;
   p.tiles_n = (int)ceil_div(op.N, tc::W_BN);
   p.num_tiles = (int)(ceil_div(op.M, tc::BM) * p.tiles_n);
@@ -1273,8 +1286,8 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
     p.db_out = op.db;
   }
   LaunchRec& r = recs[0];
-  r.func = tcw_kernel_ptr();
-  r.smem = tc::W_SMEM_BYTES;
+  r.func = x3 ? tcw_kernel_ptr<true>() : tcw_kernel_ptr<false>();
+  r.smem = x3 ? tc::WCfg<true>::SMEM_BYTES : tc::WCfg<false>::SMEM_BYTES;
   const int sms = device_sms();
   r.grid = dim3((unsigned)(p.num_units < sms ? p.num_units : sms));
   r.block = dim3(tc::P_THREADS);
