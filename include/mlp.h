@@ -143,7 +143,13 @@ mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
  *     layer (MLP_OPT_FUSE_HEAD on and supported), and input / hidden widths
  *     below the output layer that are multiples of 8.  Otherwise, or with 0,
  *     the GEMMs run on the FFMA pipes.  mlp_forward always uses FFMA. */
-enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2 };
+/*   MLP_OPT_PDL (default 1): in the step's CUDA graph, let each kernel be
+ *     scheduled as soon as every block of the kernel before it has started
+ *     (programmatic dependent launch); it runs its prologue (barriers, tensor
+ *     memory) and then waits for that kernel to complete before touching
+ *     global memory.  0 chains the kernels with full dependencies.  Results
+ *     are identical either way. */
+enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2, MLP_OPT_PDL = 3 };
 mlp_status mlp_set_option(mlp_t* model, int option, int64_t value);
 
 /* Number of parameters (flat, densely packed) and of Linear layers. */

@@ -132,7 +132,7 @@ def mlp_set_graph_mode(h, enable: bool) -> None:
     _check(lib().mlp_set_graph_mode(h, int(bool(enable))))
 
 
-OPT_GRAPH, OPT_FUSE_HEAD, OPT_F32_TENSOR_CORES = 0, 1, 2
+OPT_GRAPH, OPT_FUSE_HEAD, OPT_F32_TENSOR_CORES, OPT_PDL = 0, 1, 2, 3
 
 
 def mlp_set_option(h, option: int, value: int) -> None:

@@ -20,6 +20,17 @@ enum : uint32_t {
 };
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Programmatic dependent launch: inside the step's CUDA graph each kernel may
+// be launched before its predecessor has finished.  Every kernel calls this
+// before its first global memory access: it waits until the predecessor grid
+// has completed and its writes are visible, then lets the next kernel be
+// scheduled (its blocks run their own prologue and wait here in turn).
+// Without a programmatic dependency both instructions return at once.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // tanh-form GELU (Hendrycks & Gimpel): gelu(u) = 0.5 u (1 + tanh(a)),

@@ -10,10 +10,10 @@
 // page": forward and vjp per module).
 //
 // Each CTA takes 32-row tiles: the h tile is staged in shared memory (16-byte
-// loads), then logits (one thread per row and class), softmax and dz (one
-// thread per row), dY (one thread per 4 columns x 4 rows, 8- or 16-byte
-// stores) and the dW / db partial sums (one thread per weight) come from
-// shared memory.  CTAs run in clusters of 8: after a cluster barrier, CTA
+// loads, the next tile's in flight during the current one), then logits and
+// softmax / dz (8 threads per row), dY (one thread per 4 columns x 4 rows,
+// 8- or 16-byte stores) and the dW / db partial sums (one thread per column
+// and 5 classes) come from shared memory.  CTAs run in clusters of 8: after a cluster barrier, CTA
 // rank q adds slice q of the cluster's dW / db partials through distributed
 // shared memory in rank order and writes it to the workspace; the optimizer
 // adds the cluster partials (and the loss partials) in cluster order, so the
@@ -137,81 +137,131 @@ head_kernel(const __grid_constant__ HeadParams p) {
   HeadSmem& s = *reinterpret_cast<HeadSmem*>(smem_raw);
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x;
+  pdl_enter();
   // nothing else in the step reads the counter before the optimizer
   if (blockIdx.x == 0 && tid == 0 && p.step_counter)
     advance_step(p.step_counter, p.bias_corr, p.beta1, p.beta2);
-  for (int i = tid; i < kHC * kHK; i += kHT) s.W[i / kHK][i % kHK] = to_f32(reinterpret_cast<const T*>(p.W)[i]);
-  if (tid < kHR) s.loss_rows[tid] = 0.f;
-
-  // dY: this thread's 4 columns kq..kq+3 and rows rq, rq + 8, rq + 16, rq + 24
-  const int kq = 4 * (tid & 31);
-  const int rq = tid >> 5;
   // h tile staging: row hr, columns hc..hc+15
   const int hr = tid >> 3, hc = 16 * (tid & 7);
-  float acc[kHPart / kHT + 1];
-#pragma unroll
-  for (int j = 0; j < kHPart / kHT + 1; ++j) acc[j] = 0.f;
-
   const int ntiles = (p.B + kHR - 1) / kHR;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+  float hv[16];
+  int label = 0;   // the label of row tid / 8 of the tile (logits / softmax mapping below)
+  auto load_tile = [&](int tile) {   // this thread's 16 elements of the tile (zeros past the last row)
     const int r0 = tile * kHR;
-    const int nr = min(kHR, p.B - r0);
-    float hv[16];
-    if (hr < nr) {
+    if (tile < ntiles && r0 + hr < p.B) {
       load_h16<T, X3>(p, (int64_t)(r0 + hr) * p.ldh + hc, hv);
+      label = __ldg(p.labels + r0 + hr);
     } else {
 #pragma unroll
       for (int j = 0; j < 16; ++j) hv[j] = 0.f;
     }
+  };
+  load_tile(blockIdx.x);   // in flight while W is staged
+  {   // W: 4 consecutive elements per load (rows of 128 are 4-aligned)
+    float wv[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int i = 4 * (tid + j * kHT);
+      if (i < kHC * kHK) {
+        if (sizeof(T) == 4) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.W) + i));
+          wv[j][0] = v.x; wv[j][1] = v.y; wv[j][2] = v.z; wv[j][3] = v.w;
+        } else {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.W) + i));
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) wv[j][k] = __bfloat162float(e[k]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int i = 4 * (tid + j * kHT);
+      if (i < kHC * kHK)
+        *reinterpret_cast<float4*>(&s.W[i / kHK][i % kHK]) = make_float4(wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
+    }
+  }
+  if (tid < kHR) s.loss_rows[tid] = 0.f;
+  float bias[kHC];   // every thread needs all ten
+#pragma unroll
+  for (int c = 0; c < kHC; ++c) bias[c] = __ldg(p.bias + c);
+
+  // dY: this thread's 4 columns kq..kq+3 and rows rq, rq + 8, rq + 16, rq + 24
+  const int kq = 4 * (tid & 31);
+  const int rq = tid >> 5;
+  // logits: 8 threads per row (lr = tid / 8); thread `sub` takes the float4
+  // columns sub, sub + 8, sub + 16, sub + 24 (conflict-free in shared memory)
+  const int lr = tid >> 3, sub = tid & 7;
+  // dW: this thread's column kw and classes 2 j + cw (j < 5); db: tid < 10
+  const int kw = tid & (kHK - 1), cw = tid >> 7;
+  float acc[5], accb = 0.f;
+#pragma unroll
+  for (int j = 0; j < 5; ++j) acc[j] = 0.f;
+
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int r0 = tile * kHR;
+    const int nr = min(kHR, p.B - r0);
     __syncthreads();   // W loaded / previous tile finished with h and z
 #pragma unroll
     for (int j = 0; j < 16; j += 4)
       *reinterpret_cast<float4*>(&s.h[hr][hc + j]) = make_float4(hv[j], hv[j + 1], hv[j + 2], hv[j + 3]);
+    const int y = label;   // row lr == hr of this tile
     __syncthreads();
-    // logits rounded to the model dtype (the value a stored logits tensor holds)
-    for (int t = tid; t < kHR * kHC; t += kHT) {
-      const int r = t / kHC, c = t % kHC;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < kHK; k += 4) {
-        const float4 h4 = *reinterpret_cast<const float4*>(&s.h[r][k]);
-        const float4 w4 = *reinterpret_cast<const float4*>(&s.W[c][k]);
-        a0 = fmaf(h4.x, w4.x, a0); a1 = fmaf(h4.y, w4.y, a1);
-        a2 = fmaf(h4.z, w4.z, a2); a3 = fmaf(h4.w, w4.w, a3);
+    load_tile(tile + gridDim.x);   // the next tile's h, in flight during this one
+    // logits (partial dot products over this thread's 16 columns, then a
+    // fixed xor tree over the row's 8 threads), rounded to the model dtype
+    // (the value a stored logits tensor holds); then softmax cross-entropy:
+    // dz replaces z, thread sub writes classes sub and sub + 8
+    {
+      float zc[kHC];
+#pragma unroll
+      for (int c = 0; c < kHC; ++c) zc[c] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = 4 * (sub + 8 * i);
+        const float4 h4 = *reinterpret_cast<const float4*>(&s.h[lr][k]);
+#pragma unroll
+        for (int c = 0; c < kHC; ++c) {
+          const float4 w4 = *reinterpret_cast<const float4*>(&s.W[c][k]);
+          zc[c] = fmaf(h4.x, w4.x, zc[c]);
+          zc[c] = fmaf(h4.y, w4.y, zc[c]);
+          zc[c] = fmaf(h4.z, w4.z, zc[c]);
+          zc[c] = fmaf(h4.w, w4.w, zc[c]);
+        }
       }
-      s.z[r][c] = to_f32(from_f32<T>((a0 + a1) + (a2 + a3) + p.bias[c]));
-    }
-    __syncthreads();
-    // softmax cross-entropy per row: loss and dz (dz replaces z)
-    if (tid < kHR) {
-      const int r = tid;
-      if (r < nr) {
-        const int y = p.labels[r0 + r];
-        const bool bad = y < 0 || y >= kHC;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+        for (int c = 0; c < kHC; ++c) zc[c] += __shfl_xor_sync(0xffffffffu, zc[c], o);
+      if (lr < nr) {
         float m = -INFINITY, zy = 0.f;
 #pragma unroll
         for (int c = 0; c < kHC; ++c) {
-          m = fmaxf(m, s.z[r][c]);
-          if (c == y) zy = s.z[r][c];
+          zc[c] = to_f32(from_f32<T>(zc[c] + bias[c]));
+          m = fmaxf(m, zc[c]);
+          if (c == y) zy = zc[c];
         }
-        float e[kHC], se = 0.f;
+        float se = 0.f;
 #pragma unroll
         for (int c = 0; c < kHC; ++c) {
-          e[c] = expf(s.z[r][c] - m);
-          se += e[c];
+          zc[c] = expf(zc[c] - m);
+          se += zc[c];
         }
         const float inv = 1.0f / se;
 #pragma unroll
         for (int c = 0; c < kHC; ++c)
-          s.z[r][c] = to_f32(from_f32<T>((e[c] * inv - (c == y ? 1.f : 0.f)) * p.grad_scale));
-        if (bad) {
-          if (p.err) atomicOr(p.err, ERRBIT_LABEL_RANGE);
-        } else {
-          s.loss_rows[r] += (m + logf(se)) - zy;
+          if (c == sub || c == sub + 8)
+            s.z[lr][c] = to_f32(from_f32<T>((zc[c] * inv - (c == y ? 1.f : 0.f)) * p.grad_scale));
+        if (sub == 0) {
+          if (y < 0 || y >= kHC) {
+            if (p.err) atomicOr(p.err, ERRBIT_LABEL_RANGE);
+          } else {
+            s.loss_rows[lr] += (m + logf(se)) - zy;
+          }
         }
       } else {
-#pragma unroll
-        for (int c = 0; c < kHC; ++c) s.z[r][c] = 0.f;
+        if (sub < kHC) s.z[lr][sub] = 0.f;
+        if (sub + 8 < kHC) s.z[lr][sub + 8] = 0.f;
       }
     }
     __syncthreads();
@@ -243,31 +293,23 @@ head_kernel(const __grid_constant__ HeadParams p) {
         }
       }
     }
-    // dW += dz^T h, db += sum dz over the tile's rows (zero rows add 0)
+    // dW += dz^T h, db += sum dz over the tile's rows (zero rows add 0):
+    // one h load and one dz row per row serve all five classes
+#pragma unroll 4
+    for (int r = 0; r < kHR; ++r) {
+      const float hk = s.h[r][kw];
+      float zr[kHC];
 #pragma unroll
-    for (int j = 0; j < kHPart / kHT + 1; ++j) {
-      const int e = tid + j * kHT;
-      if (e < kHC * kHK) {
-        const int c = e / kHK, k = e % kHK;
-        float a = acc[j];
-#pragma unroll 8
-        for (int r = 0; r < kHR; ++r) a = fmaf(s.z[r][c], s.h[r][k], a);
-        acc[j] = a;
-      } else if (e < kHPart) {
-        const int c = e - kHC * kHK;
-        float a = acc[j];
-#pragma unroll 8
-        for (int r = 0; r < kHR; ++r) a += s.z[r][c];
-        acc[j] = a;
-      }
+      for (int c = 0; c < kHC; ++c) zr[c] = s.z[r][c];
+#pragma unroll
+      for (int j = 0; j < 5; ++j) acc[j] = fmaf(cw ? zr[2 * j + 1] : zr[2 * j], hk, acc[j]);
+      if (tid < kHC) accb += s.z[r][tid];
     }
   }
   // ---- this CTA's partial into its shared memory ----
 #pragma unroll
-  for (int j = 0; j < kHPart / kHT + 1; ++j) {
-    const int e = tid + j * kHT;
-    if (e < kHPart) s.part[e] = acc[j];
-  }
+  for (int j = 0; j < 5; ++j) s.part[(2 * j + cw) * kHK + kw] = acc[j];
+  if (tid < kHC) s.part[kHC * kHK + tid] = accb;
   __syncthreads();
   if (tid < 32) {   // this CTA's loss partial: a fixed-order tree over the 32 row slots
     static_assert(kHR == 32, "one loss slot per lane");

@@ -204,6 +204,7 @@ struct HostRng {
 
 struct GraphCache {
   int n_steps = 0;
+  bool pdl = false;   // built with programmatic (early-launch) edges
   cudaGraphExec_t exec = nullptr;
   cudaGraph_t graph = nullptr;
   std::vector<cudaGraphNode_t> nodes;
@@ -220,6 +221,7 @@ struct mlp {
   bool use_graph = true;
   bool fuse_head = true;     // fused output layer + CE where the shape allows
   bool f32_tc = true;        // fp32 GEMMs on the tensor cores (three bf16 planes) where the model allows
+  bool pdl = true;           // graph edges let each kernel launch before its predecessor ends
   std::mutex mu;
   std::vector<GraphCache> graphs;
   int kernels_per_step = 0;
@@ -451,7 +453,7 @@ mlp_status launch_graph(mlp* m, int key, std::vector<LaunchRec>& recs, cudaStrea
   GraphCache* gc = nullptr;
   for (auto& g : m->graphs)
     if (g.n_steps == key) gc = &g;
-  if (gc && !same_topology(gc->recs, recs)) {
+  if (gc && (!same_topology(gc->recs, recs) || gc->pdl != m->pdl)) {
     cudaGraphExecDestroy(gc->exec);
     cudaGraphDestroy(gc->graph);
     gc->exec = nullptr;
@@ -467,14 +469,27 @@ mlp_status launch_graph(mlp* m, int key, std::vector<LaunchRec>& recs, cudaStrea
   if (!gc->exec) {
     CUDA_TRY(cudaGraphCreate(&gc->graph, 0));
     cudaGraphNode_t prev = nullptr;
+    // a chain; with pdl each edge is programmatic: a kernel may be scheduled
+    // once every block of its predecessor has started, and waits inside
+    // (griddepcontrol.wait) for the predecessor to complete
+    cudaGraphEdgeData ed;
+    memset(&ed, 0, sizeof(ed));
+    ed.from_port = cudaGraphKernelNodePortProgrammatic;
+    ed.type = cudaGraphDependencyTypeProgrammatic;
     for (auto& r : recs) {
       void* argp[1];
       cudaKernelNodeParams kp = node_params(r, argp);
       cudaGraphNode_t node;
-      CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, prev ? &prev : nullptr, prev ? 1 : 0, &kp));
+      if (prev && m->pdl) {
+        CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, nullptr, 0, &kp));
+        CUDA_TRY(cudaGraphAddDependencies(gc->graph, &prev, &node, &ed, 1));
+      } else {
+        CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, prev ? &prev : nullptr, prev ? 1 : 0, &kp));
+      }
       gc->nodes.push_back(node);
       prev = node;
     }
+    gc->pdl = m->pdl;
     CUDA_TRY(cudaGraphInstantiate(&gc->exec, gc->graph, 0));
     gc->recs = recs;
   } else {
@@ -605,9 +620,10 @@ mlp_status mlp_set_option(mlp_t* m, int option, int64_t value) {
     case MLP_OPT_GRAPH: m->use_graph = value != 0; break;
     case MLP_OPT_FUSE_HEAD: m->fuse_head = value != 0; break;
     case MLP_OPT_F32_TENSOR_CORES: m->f32_tc = value != 0; break;
+    case MLP_OPT_PDL: m->pdl = value != 0; break;
     default: return fail(MLP_ERR_ARG, "unknown option %d", option);
   }
-  if (option != MLP_OPT_GRAPH) {   // the weight planes are only kept current while in use
+  if (option == MLP_OPT_FUSE_HEAD || option == MLP_OPT_F32_TENSOR_CORES) {   // planes kept current only while used
     DevGuard g(m->device);
     cudaError_t e = refresh_w16(m);
     if (e != cudaSuccess) return fail(MLP_ERR_CUDA, "refreshing weight planes: %s", cudaGetErrorString(e));

@@ -42,6 +42,7 @@ __device__ __forceinline__ void ce_finish_row(const CeParams& p, int row, int y,
 // One warp per row; the row lives in registers (C <= 32 * VPL).
 template <typename T, int VPL>
 __global__ void __launch_bounds__(256) ce_warp_kernel(const __grid_constant__ CeParams p) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (row >= p.B) return;
@@ -90,6 +91,7 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
 // C % (16 / sizeof(T)) == 0 and C <= blockDim * VPT * (16 / sizeof(T)).
 template <typename T, int VPT>
 __global__ void __launch_bounds__(512) ce_block_kernel(const __grid_constant__ CeParams p) {
+  pdl_enter();
   constexpr int E = 16 / sizeof(T);   // elements per vector
   __shared__ float red[32];
   const int row = blockIdx.x;
@@ -157,6 +159,7 @@ __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s
 
 template <typename T>
 __global__ void __launch_bounds__(256) ce_row2_kernel(const __grid_constant__ CeParams p) {
+  pdl_enter();
   constexpr int E = 16 / sizeof(T);
   __shared__ float red_m[8], red_s[8];
   const int row = blockIdx.x;
@@ -210,6 +213,7 @@ __global__ void __launch_bounds__(256) ce_row2_kernel(const __grid_constant__ Ce
 // Any C: one CTA per row, three passes over the row (max, sum, write).
 template <typename T>
 __global__ void __launch_bounds__(256) ce_generic_kernel(const __grid_constant__ CeParams p) {
+  pdl_enter();
   __shared__ float red[32];
   const int row = blockIdx.x;
   const T* zr = reinterpret_cast<const T*>(p.z) + (int64_t)row * p.ldz;
@@ -287,6 +291,7 @@ struct LossMeanParams {
 // error ~ (B/1024 + 10) ulp of the sum, far below the loss tolerance, and
 // no fp64 (slow on this part) in the step.
 __global__ void __launch_bounds__(1024) loss_mean_kernel(const __grid_constant__ LossMeanParams p) {
+  pdl_enter();
   __shared__ float red[1024];
   float s = 0.f;
   for (int64_t i = threadIdx.x; i < p.B; i += blockDim.x) s += p.loss_rows[i];
@@ -380,35 +385,31 @@ __device__ __forceinline__ void store_planes4(__nv_bfloat16* dst, int64_t plane,
 }
 
 __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamWParams q) {
-  // bias corrections: precomputed for the step, else computed once per CTA
-  __shared__ float s_bc[2];
+  pdl_enter();
+  // bias corrections: precomputed for the step (read by every thread, in
+  // flight with its first parameter loads), else computed here
+  float inv_bc1, inv_sqrt_bc2;
   if (q.bias_corr) {
-    if (threadIdx.x == 0) { s_bc[0] = q.bias_corr[0]; s_bc[1] = q.bias_corr[1]; }
-  } else if (threadIdx.x == 0) {
+    inv_bc1 = __ldg(q.bias_corr);
+    inv_sqrt_bc2 = __ldg(q.bias_corr + 1);
+  } else {
     const int64_t t = q.t > 0 ? q.t : *q.step_counter;
-    s_bc[0] = 1.0f / one_minus_pow(q.beta1, t);
-    s_bc[1] = 1.0f / sqrtf(one_minus_pow(q.beta2, t));
+    inv_bc1 = 1.0f / one_minus_pow(q.beta1, t);
+    inv_sqrt_bc2 = 1.0f / sqrtf(one_minus_pow(q.beta2, t));
   }
-  if (q.loss_parts && blockIdx.x == 0 && threadIdx.x == 0) {
-    float a = 0.f;
-    for (int c = 0; c < q.loss_n; ++c) a += __ldcg(q.loss_parts + c);
-    const float L = a * q.loss_scale;   // loss_scale = 1/B: the batch mean
-    if (q.loss) *q.loss = L;
-    if (q.err && !isfinite(L)) atomicOr(q.err, ERRBIT_NONFINITE);
-  }
-  __syncthreads();
-  const float inv_bc1 = s_bc[0];
-  const float inv_sqrt_bc2 = s_bc[1];
   const int64_t n4 = q.n / 4;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
     float4 p = reinterpret_cast<float4*>(q.p)[i];
     float4 g;
     const int64_t f = 4 * i;
-    if (q.gpart && f >= q.woff && f + 3 < q.woff + q.nw) {
-      // four weights from the partial sums: 16-byte loads, all in flight
-      // (woff, nw and the partial pitch are multiples of 4)
-      const float* src = q.gpart + (f - q.woff);
+    const bool in_w = f >= q.woff && f < q.woff + q.nw;
+    if (q.gpart && (in_w || (f >= q.boff && f < q.boff + q.nb))) {
+      // four gradient elements from the partial sums: 16-byte loads, all in
+      // flight (woff, boff, nw and the partial pitch are multiples of 4; a
+      // group that starts among the biases may end in the plane's padding,
+      // which keeps its own value)
+      const float* src = q.gpart + (in_w ? f - q.woff : q.nw + f - q.boff);
       float4 part[16];
 #pragma unroll
       for (int b = 0; b < 16; ++b)
@@ -423,11 +424,13 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
         const float4 t = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)b * q.gpart_stride));
         g.x += t.x; g.y += t.y; g.z += t.z; g.w += t.w;
       }
+      if (!in_w && f + 4 > q.boff + q.nb) {   // padding after the biases
+        const float4 own = reinterpret_cast<const float4*>(q.g)[i];
+        if (f + 1 >= q.boff + q.nb) g.y = own.y;
+        if (f + 2 >= q.boff + q.nb) g.z = own.z;
+        if (f + 3 >= q.boff + q.nb) g.w = own.w;
+      }
       reinterpret_cast<float4*>(q.g)[i] = g;   // the gradient plane holds the summed gradient
-    } else if (q.gpart && f + 3 >= q.boff && f < q.boff + q.nb) {
-      bool a, b, c, d;
-      g = make_float4(grad_elem(q, f, a), grad_elem(q, f + 1, b), grad_elem(q, f + 2, c), grad_elem(q, f + 3, d));
-      reinterpret_cast<float4*>(q.g)[i] = g;
     } else {
       g = reinterpret_cast<const float4*>(q.g)[i];
     }
@@ -462,6 +465,17 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
     if (q.w16 && q.w16_plane > 0) split3(p, q.w16[i], q.w16[i + q.w16_plane], q.w16[i + 2 * q.w16_plane]);
     else if (q.w16) q.w16[i] = __float2bfloat16_rn(p);
   }
+  if (q.loss_parts && blockIdx.x == 0 && threadIdx.x < 32) {
+    // the batch loss: lane c adds partials c, c + 32, ...; then a fixed-order warp tree
+    float a = 0.f;
+    for (int c = threadIdx.x; c < q.loss_n; c += 32) a += __ldcg(q.loss_parts + c);
+    a = warp_sum(a);
+    const float L = a * q.loss_scale;   // loss_scale = 1/B: the batch mean
+    if (threadIdx.x == 0) {
+      if (q.loss) *q.loss = L;
+      if (q.err && !isfinite(L)) atomicOr(q.err, ERRBIT_NONFINITE);
+    }
+  }
 }
 
 int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
@@ -473,8 +487,8 @@ int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
     snprintf(err, errlen, "adamw: planes must be 16-byte aligned (w16: 8, plane pitch >= n, multiple of 4)");
     return -1;
   }
-  if (op.gpart && (op.gpart_n < 1 || op.gpart_stride < op.nw + op.nb || op.gpart_stride % 4 || op.woff % 4 ||
-                   op.nw % 4 || (uintptr_t)op.gpart % 16 ||
+  if (op.gpart && (op.gpart_n < 1 || op.gpart_stride < op.nw + (op.nb + 3) / 4 * 4 || op.gpart_stride % 4 ||
+                   op.woff % 4 || op.boff % 4 || op.nw % 4 || (uintptr_t)op.gpart % 16 ||
                    op.woff + op.nw > op.n || op.boff + op.nb > op.n)) {
     snprintf(err, errlen, "adamw: bad gradient partials");
     return -1;
@@ -508,6 +522,7 @@ __device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2)
 
 template <typename T>
 __global__ void __launch_bounds__(256) argmax_kernel(const __grid_constant__ ArgmaxParams p) {
+  pdl_enter();
   __shared__ float sv[32];
   __shared__ int si[32];
   const int row = blockIdx.x;
@@ -562,6 +577,7 @@ struct CopyRowsParams {
 };
 
 __global__ void copy_rows_kernel(const __grid_constant__ CopyRowsParams p) {
+  pdl_enter();
   const int64_t total = p.B * p.row_bytes;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     int64_t r = i / p.row_bytes, c = i % p.row_bytes;
@@ -587,6 +603,7 @@ int copy_rows_plan(const CopyRowsOp& op, LaunchRec* rec, char* err, size_t errle
 struct CastParams { const float* p; __nv_bfloat16* w16; int64_t n; };
 
 __global__ void cast_bf16_kernel(const __grid_constant__ CastParams q) {
+  pdl_enter();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < q.n; i += (int64_t)gridDim.x * blockDim.x)
     q.w16[i] = __float2bfloat16_rn(q.p[i]);
 }
@@ -617,14 +634,21 @@ struct Split3Params {
 };
 
 __global__ void __launch_bounds__(256) split3_kernel(const __grid_constant__ Split3Params q) {
+  pdl_enter();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if (q.vec) {
     const int64_t c4 = q.cols / 4;
     const int64_t n = q.rows * c4;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+    // two 16-byte loads in flight per thread and iteration
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += 2 * stride) {
+      const int64_t i2 = i + stride;
       const int64_t r = i / c4, c = (i - r * c4) * 4;
+      const int64_t r2 = i2 / c4, c2 = (i2 - r2 * c4) * 4;
       const float4 v = __ldcs(reinterpret_cast<const float4*>(q.src + r * q.lds + c));
+      float4 v2 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i2 < n) v2 = __ldcs(reinterpret_cast<const float4*>(q.src + r2 * q.lds + c2));
       store_planes4(q.dst + r * q.ldd + c, q.plane, v);
+      if (i2 < n) store_planes4(q.dst + r2 * q.ldd + c2, q.plane, v2);
     }
   } else {
     const int64_t n = q.rows * q.cols;

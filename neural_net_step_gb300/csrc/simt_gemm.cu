@@ -30,6 +30,7 @@ constexpr int SK = 16;   // K slice
 template <int BM, int BN, bool AK, bool BKM>
 __global__ void __launch_bounds__((BM / 8) * (BN / 8))
 simt_gemm_kernel(const __grid_constant__ SimtGemmParams p) {
+  pdl_enter();
   constexpr int NT = (BM / 8) * (BN / 8);
   constexpr int A_PER = BM * SK / NT;
   constexpr int B_PER = BN * SK / NT;
@@ -163,6 +164,7 @@ struct SplitReduceParams {
 };
 
 __global__ void split_reduce_kernel(const __grid_constant__ SplitReduceParams p) {
+  pdl_enter();
   const int64_t MN = (int64_t)p.M * p.N;
   const int64_t total = MN + p.M;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;

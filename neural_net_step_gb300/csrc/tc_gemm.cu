@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
+  pdl_enter();   // shared memory and TMEM are set up: now wait for the inputs
 
   const uint32_t b_bytes = C::B_STAGE_BYTES;
   if (warp == 0) {
@@ -569,6 +570,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
+  pdl_enter();   // shared memory and TMEM are set up: now wait for the inputs
   const uint32_t stage_tx = C::STAGE_BYTES;
 
   if (warp == 0) {
@@ -920,6 +922,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
+  pdl_enter();   // shared memory and TMEM are set up: now wait for the inputs
   auto unit_coords = [&](int u, int& m0, int& n0, int& split, int& kb0, int& kb1) {
     const int tile = u % p.num_tiles;
     split = u / p.num_tiles;

@@ -262,8 +262,10 @@ def test_bitwise_deterministic_and_graph_equals_eager(name):
     params0 = synth.make_params(w)
     bl = P.batches(w, 2)
     res = []
-    for graph in (True, True, False):
+    # graph with early-launch edges (twice), graph with plain edges, eager
+    for graph, pdl in ((True, 1), (True, 1), (True, 0), (False, 1)):
         m = make_model(w, params=params0, graph=graph)
+        m.set_option(nn.OPT_PDL, pdl)
         losses, _, _ = gpu_run(m, w, bl)
         p, _ = m.read_flat(nn.PLANE_P)
         res.append((losses, p))
