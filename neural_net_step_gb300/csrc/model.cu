@@ -81,7 +81,13 @@ struct Layout {
   size_t off_z = 0, off_dz = 0;
   int64_t ldz = 0;
   size_t off_dy[2] = {0, 0};
-  size_t off_loss_rows = 0, off_ws = 0, ws_bytes = 0, off_ctl = 0;
+  size_t off_loss_rows = 0, off_ctl = 0;
+  // Split-K partial sums of the weight gradients.  Small ones (defer_l) are
+  // left for the optimizer to add, in a region per layer since all are read
+  // at the end; the others share one region and are reduced right after
+  // their GEMM.
+  std::vector<size_t> off_wws, wws_bytes;
+  std::vector<char> defer_l;
   size_t off_hws = 0, hws_bytes = 0;   // the fused output layer's partials (read by the optimizer)
   size_t total = 0;
 };
@@ -158,19 +164,34 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
   L.off_dy[0] = take(batch * max_ld * es);
   L.off_dy[1] = take(batch * max_ld * es);
   L.off_loss_rows = take(batch * 4);
-  size_t ws = 0;
+  size_t shared_ws = 0, deferred = 0;
+  std::vector<size_t> need(L.L);
   for (int l = 0; l < L.L; ++l) {
     int s = wgrad_splits(dtype, dims[l + 1], dims[l], batch);
     size_t b = wgrad_workspace_bytes(dtype, dims[l + 1], dims[l], batch, s);
-    ws = b > ws ? b : ws;
     if (L.x3_ok) {
       s = wgrad_splits(DT_F32X3, dims[l + 1], dims[l], batch);
-      b = wgrad_workspace_bytes(DT_F32X3, dims[l + 1], dims[l], batch, s);
-      ws = b > ws ? b : ws;
+      const size_t b3 = wgrad_workspace_bytes(DT_F32X3, dims[l + 1], dims[l], batch, s);
+      b = b3 > b ? b3 : b;
+    }
+    need[l] = b;
+    const int64_t M = dims[l + 1], MN = dims[l + 1] * dims[l];
+    // deferred while the partials stay small enough to live in L2 until the optimizer runs
+    const bool d = b > 0 && MN % 4 == 0 && M % 4 == 0 && b <= (16u << 20) && deferred + b <= (48u << 20);
+    if (d) deferred += b;
+    L.defer_l.push_back(d);
+    if (!d) shared_ws = b > shared_ws ? b : shared_ws;
+  }
+  const size_t shared_off = shared_ws ? take(shared_ws) : 0;
+  for (int l = 0; l < L.L; ++l) {
+    if (L.defer_l[l]) {   // 16 bytes of slack: the optimizer reads partial rows 4 floats at a time
+      L.wws_bytes.push_back(need[l] + 16);
+      L.off_wws.push_back(take(need[l] + 16));
+    } else {
+      L.wws_bytes.push_back(need[l] ? shared_ws : 0);
+      L.off_wws.push_back(shared_off);
     }
   }
-  L.ws_bytes = ws;
-  L.off_ws = take(ws ? ws : 4);
   if (n_dims >= 3 && head_supported(dims[L.L], dims[L.L - 1])) {
     L.hws_bytes = head_workspace_bytes(batch, dims[L.L], dims[L.L - 1]);
     L.off_hws = take(L.hws_bytes);
@@ -375,6 +396,8 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     out.push_back(r);
   }
   float* G = m->plane(MLP_PLANE_G);
+  AdamWOp::Seg seg[AdamWOp::kMaxSegs];   // gradients the optimizer adds from partial sums
+  int nseg = 0;
   for (int l = top; l >= 0; --l) {
     const void* Xl = l == 0 ? (x3 ? m->at(L.off_xs) : x) : m->at(L.off_h[l - 1]);
     const int64_t ldxl = l == 0 ? (x3 ? L.ld_x : L.dims[0]) : L.ld_h[l - 1];
@@ -385,9 +408,24 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     wg.B = Xl; wg.ldb = ldxl; wg.b_kmajor = false; wg.b_plane = L.B * ldxl;
     wg.dW = G + L.woff[l]; wg.ld_dw = L.dims[l];
     wg.db = G + L.boff[l];
-    wg.ws = (float*)m->at(L.off_ws); wg.ws_bytes = L.ws_bytes;
+    wg.ws = L.wws_bytes[l] ? (float*)m->at(L.off_wws[l]) : nullptr; wg.ws_bytes = L.wws_bytes[l];
     wg.err = &ctl->err;
-    PLAN_TRY(gemm_plan(wg, r_, e_, sizeof(e_)));
+    // split-K partials go to the optimizer (it reads them 4 at a time)
+    const int64_t MN = wg.M * wg.N;
+    int used = 0;
+    wg.defer_reduce = L.defer_l[l] && nseg + 2 <= AdamWOp::kMaxSegs;
+    wg.splits_out = &used;
+    {
+      char e_[512] = "";
+      LaunchRec r_[2];
+      const int n_ = gemm_plan(wg, r_, e_, sizeof(e_));
+      if (n_ < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+      add(out, n_, r_);
+      if (n_ == 1 && used > 1) {
+        seg[nseg++] = AdamWOp::Seg{L.woff[l], MN, wg.ws, used, MN};
+        seg[nseg++] = AdamWOp::Seg{L.boff[l], wg.M, wg.ws + (int64_t)used * MN, used, wg.M};
+      }
+    }
     if (l > 0) {
       GemmOp dg;
       dg.dtype = x3 ? DT_F32X3 : L.dtype; dg.kind = GEMM_DGRAD;
@@ -413,12 +451,14 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
   ad.step_counter = &ctl->step;
   ad.bias_corr = ctl->bias_corr;
   ad.lr = hp.lr; ad.beta1 = hp.b1; ad.beta2 = hp.b2; ad.eps = hp.eps; ad.wd = hp.wd;
+  for (int k = 0; k < nseg; ++k) ad.seg[ad.nseg++] = seg[k];
   if (fuse) {   // the output layer's gradient and the loss arrive as partial sums
     const int l = L.L - 1;
     const HeadPartials hpart = head_partials(L.B, L.dims[L.L], L.dims[l]);
     const float* hws = (const float*)m->at(L.off_hws);
-    ad.gpart = hws; ad.gpart_n = hpart.n; ad.gpart_stride = hpart.stride;
-    ad.woff = L.woff[l]; ad.nw = L.dims[L.L] * L.dims[l]; ad.boff = L.boff[l]; ad.nb = L.dims[L.L];
+    const int64_t nw = L.dims[L.L] * L.dims[l];
+    ad.seg[ad.nseg++] = AdamWOp::Seg{L.woff[l], nw, hws, hpart.n, hpart.stride};
+    ad.seg[ad.nseg++] = AdamWOp::Seg{L.boff[l], L.dims[L.L], hws + nw, hpart.n, hpart.stride};
     ad.loss_parts = hws + hpart.loss_off; ad.loss_n = hpart.n; ad.loss_scale = 1.0f / (float)L.B;
     ad.loss = loss ? loss : &ctl->loss_slot;
     ad.err = &ctl->err;

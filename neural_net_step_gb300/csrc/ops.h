@@ -44,6 +44,11 @@ struct GemmOp {
   int splits = 0;           // 0 = choose
   uint32_t* err = nullptr;  // device error word (bounded-wait timeouts)
   int64_t a_plane = 0, b_plane = 0, out_plane = 0;   // DT_F32X3 plane pitches (elements)
+  // GEMM_WGRAD with splits > 1: leave the partial sums in ws ([splits][M*N],
+  // then [splits][M] for db) for the optimizer to add instead of planning the
+  // reduce kernel; the number of splits used goes to *splits_out.
+  bool defer_reduce = false;
+  int* splits_out = nullptr;
 };
 
 // Number of K splits the wgrad of this shape uses, and the workspace bytes.
@@ -92,12 +97,15 @@ struct AdamWOp {
   int64_t t = 0;                       // ...or given explicitly when > 0
   const float* bias_corr = nullptr;    // precomputed [1/(1-b1^t), 1/sqrt(1-b2^t)] (nullable)
   float lr = 0, beta1 = 0, beta2 = 0, eps = 0, wd = 0;
-  // Optional: one layer's gradient left as gpart_n partial sums
-  // [gpart_n][gpart_stride] (element e < nw belongs to g[woff + e], the rest
-  // to g[boff + e - nw]); they are added in a fixed order, written to g and
-  // used.  woff and nw must be multiples of 4.
-  const float* gpart = nullptr; int gpart_n = 0; int64_t gpart_stride = 0;
-  int64_t woff = 0, nw = 0, boff = 0, nb = 0;
+  // Optional: gradient segments left as partial sums: g[off + e] for
+  // e < len is parts[0][e] + parts[1][e] + ... + parts[n-1][e] (rows `stride`
+  // floats apart), added in that order, written to g and used.  off and
+  // stride must be multiples of 4, parts 16-byte aligned, and each partial
+  // row readable up to the next multiple of 4 past len.
+  static constexpr int kMaxSegs = 16;
+  struct Seg { int64_t off, len; const float* parts; int n; int64_t stride; };
+  Seg seg[kMaxSegs];
+  int nseg = 0;
   // Optional: loss = sum(loss_parts[0 .. loss_n)) * loss_scale (one thread;
   // a non-finite loss sets the error bit in err).
   const float* loss_parts = nullptr; int loss_n = 0; float loss_scale = 1.f;

@@ -333,26 +333,26 @@ struct AdamWParams {
   const float* bias_corr;
   int64_t n;
   float lr, beta1, beta2, eps, wd;
-  // one layer's gradient as partial sums (added here in a fixed order and
-  // written to g): [gpart_n][gpart_stride], element e < nw -> g[woff + e],
-  // else g[boff + e - nw]
-  const float* gpart; int gpart_n; int64_t gpart_stride, woff, nw, boff, nb;
-  // batch loss = sum(loss_parts) * loss_scale, by one thread (nullable)
+  // gradient segments as partial sums (added here in a fixed order, written to g)
+  AdamWOp::Seg seg[AdamWOp::kMaxSegs];
+  int nseg;
+  // batch loss = sum(loss_parts) * loss_scale, by one warp (nullable)
   const float* loss_parts; int loss_n; float loss_scale; float* loss; uint32_t* err;
 };
 
-// Gradient element f: from the partial sums when f lies in the partial
-// layer's weight or bias range, else from the gradient plane.
+// The gradient element g[f]: from its segment's partial sums, else the plane.
 __device__ __forceinline__ float grad_elem(const AdamWParams& q, int64_t f, bool& from_parts) {
-  int64_t e = -1;
-  if (f >= q.woff && f < q.woff + q.nw) e = f - q.woff;
-  else if (f >= q.boff && f < q.boff + q.nb) e = q.nw + f - q.boff;
-  from_parts = e >= 0;
-  if (e < 0) return q.g[f];
-  float a = 0.f;
-#pragma unroll 8
-  for (int b = 0; b < q.gpart_n; ++b) a += __ldcg(q.gpart + (int64_t)b * q.gpart_stride + e);
-  return a;
+  from_parts = false;
+  for (int k = 0; k < q.nseg; ++k) {
+    const AdamWOp::Seg& sg = q.seg[k];
+    if (f >= sg.off && f < sg.off + sg.len) {
+      from_parts = true;
+      float a = 0.f;
+      for (int b = 0; b < sg.n; ++b) a += __ldcg(sg.parts + (int64_t)b * sg.stride + (f - sg.off));
+      return a;
+    }
+  }
+  return q.g[f];
 }
 
 __device__ __forceinline__ void adamw_one(float& p, float g, float& m, float& v, float lr, float b1,
@@ -403,32 +403,41 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
     float4 p = reinterpret_cast<float4*>(q.p)[i];
     float4 g;
     const int64_t f = 4 * i;
-    const bool in_w = f >= q.woff && f < q.woff + q.nw;
-    if (q.gpart && (in_w || (f >= q.boff && f < q.boff + q.nb))) {
-      // four gradient elements from the partial sums: 16-byte loads, all in
-      // flight (woff, boff, nw and the partial pitch are multiples of 4; a
-      // group that starts among the biases may end in the plane's padding,
-      // which keeps its own value)
-      const float* src = q.gpart + (in_w ? f - q.woff : q.nw + f - q.boff);
+    int si = -1;
+    for (int k = 0; k < q.nseg; ++k)
+      if (f >= q.seg[k].off && f < q.seg[k].off + q.seg[k].len) si = k;
+    if (si >= 0) {
+      // four gradient elements from the segment's partial sums: 16-byte
+      // loads, up to 16 in flight; lanes past the segment keep the plane's
+      // own value (padding)
+      const AdamWOp::Seg& sg = q.seg[si];
+      const float* src = sg.parts + (f - sg.off);
       float4 part[16];
 #pragma unroll
       for (int b = 0; b < 16; ++b)
-        part[b] = b < q.gpart_n ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)b * q.gpart_stride))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        part[b] = b < sg.n ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)b * sg.stride))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
       g = part[0];
 #pragma unroll
       for (int b = 1; b < 16; ++b) {
         g.x += part[b].x; g.y += part[b].y; g.z += part[b].z; g.w += part[b].w;
       }
-      for (int b = 16; b < q.gpart_n; ++b) {
-        const float4 t = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)b * q.gpart_stride));
-        g.x += t.x; g.y += t.y; g.z += t.z; g.w += t.w;
+      for (int b0 = 16; b0 < sg.n; b0 += 16) {
+#pragma unroll
+        for (int b = 0; b < 16; ++b)
+          part[b] = b0 + b < sg.n ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)(b0 + b) * sg.stride))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+          g.x += part[b].x; g.y += part[b].y; g.z += part[b].z; g.w += part[b].w;
+        }
       }
-      if (!in_w && f + 4 > q.boff + q.nb) {   // padding after the biases
+      const int64_t end = sg.off + sg.len;
+      if (f + 4 > end) {
         const float4 own = reinterpret_cast<const float4*>(q.g)[i];
-        if (f + 1 >= q.boff + q.nb) g.y = own.y;
-        if (f + 2 >= q.boff + q.nb) g.z = own.z;
-        if (f + 3 >= q.boff + q.nb) g.w = own.w;
+        if (f + 1 >= end) g.y = own.y;
+        if (f + 2 >= end) g.z = own.z;
+        if (f + 3 >= end) g.w = own.w;
       }
       reinterpret_cast<float4*>(q.g)[i] = g;   // the gradient plane holds the summed gradient
     } else {
@@ -458,7 +467,7 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
   for (int64_t i = n4 * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < q.n; i += stride) {
     float p = q.p[i], m = q.m[i], v = q.v[i];
     bool fp = false;
-    const float g = q.gpart ? grad_elem(q, i, fp) : q.g[i];
+    const float g = q.nseg ? grad_elem(q, i, fp) : q.g[i];
     if (fp) q.g[i] = g;
     adamw_one(p, g, m, v, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
     q.p[i] = p; q.m[i] = m; q.v[i] = v;
@@ -487,16 +496,26 @@ int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
     snprintf(err, errlen, "adamw: planes must be 16-byte aligned (w16: 8, plane pitch >= n, multiple of 4)");
     return -1;
   }
-  if (op.gpart && (op.gpart_n < 1 || op.gpart_stride < op.nw + (op.nb + 3) / 4 * 4 || op.gpart_stride % 4 ||
-                   op.woff % 4 || op.boff % 4 || op.nw % 4 || (uintptr_t)op.gpart % 16 ||
-                   op.woff + op.nw > op.n || op.boff + op.nb > op.n)) {
-    snprintf(err, errlen, "adamw: bad gradient partials");
+  if (op.nseg < 0 || op.nseg > AdamWOp::kMaxSegs) {
+    snprintf(err, errlen, "adamw: too many gradient segments");
     return -1;
   }
-  AdamWParams q{op.p, op.g, op.m, op.v, (__nv_bfloat16*)op.w16, op.w16_plane, op.step_counter, op.t, op.bias_corr,
-                op.n, op.lr, op.beta1, op.beta2, op.eps, op.wd,
-                op.gpart, op.gpart_n, op.gpart_stride, op.woff, op.nw, op.boff, op.nb,
-                op.loss_parts, op.loss_n, op.loss_scale, op.loss, op.err};
+  for (int k = 0; k < op.nseg; ++k) {
+    const AdamWOp::Seg& sg = op.seg[k];
+    if (sg.n < 1 || sg.len < 1 || sg.off % 4 || sg.stride % 4 || sg.stride < sg.len || (uintptr_t)sg.parts % 16 ||
+        sg.off + sg.len > op.n) {
+      snprintf(err, errlen, "adamw: bad gradient segment %d", k);
+      return -1;
+    }
+  }
+  AdamWParams q{};
+  q.p = op.p; q.g = op.g; q.m = op.m; q.v = op.v;
+  q.w16 = (__nv_bfloat16*)op.w16; q.w16_plane = op.w16_plane;
+  q.step_counter = op.step_counter; q.t = op.t; q.bias_corr = op.bias_corr;
+  q.n = op.n; q.lr = op.lr; q.beta1 = op.beta1; q.beta2 = op.beta2; q.eps = op.eps; q.wd = op.wd;
+  for (int k = 0; k < op.nseg; ++k) q.seg[k] = op.seg[k];
+  q.nseg = op.nseg;
+  q.loss_parts = op.loss_parts; q.loss_n = op.loss_n; q.loss_scale = op.loss_scale; q.loss = op.loss; q.err = op.err;
   rec->func = (const void*)adamw_kernel;
   int64_t blocks = ceil_div(op.n / 4 + 1, 256);
   if (blocks > 152 * 8) blocks = 152 * 8;

@@ -256,7 +256,8 @@ int simt_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) 
   recs[0].smem = 0;
   recs[0].name = op.kind == GEMM_FWD ? "simt_gemm_fwd" : op.kind == GEMM_DGRAD ? "simt_gemm_dgrad" : "simt_gemm_wgrad";
   recs[0].set_args(p);
-  if (op.kind == GEMM_WGRAD && splits > 1) {
+  if (op.splits_out) *op.splits_out = splits;
+  if (op.kind == GEMM_WGRAD && splits > 1 && !op.defer_reduce) {
     split_reduce_plan(op.ws, splits, op.M, op.N, op.dW, op.ld_dw, op.db, &recs[1]);
     return 2;
   }

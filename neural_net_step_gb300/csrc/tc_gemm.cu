@@ -1182,8 +1182,13 @@ int pick_bn(const GemmOp& op) {
 int tc_wgrad_splits(int64_t M, int64_t N, int64_t K, int bk = tc::BK) {
   const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, 128);
   const int64_t kbs = ceil_div(K, bk);
+  // >= 2 work units per SM, each at least 8 stages long (4 with planes: a
+  // stage then carries six products)
+  const int64_t min_kb = bk >= tc::BK ? 8 : 4;
+  // with planes the partial sums are also capped at 4 M floats (16 MB)
+  const int64_t max_parts = bk >= tc::BK ? INT64_MAX : (int64_t)4 << 20;
   int64_t s = 1;
-  while (tiles * s < 2 * kSMs && kbs / (s * 2) >= 8) s *= 2;   // >= 2 work units per SM
+  while (tiles * s < 2 * kSMs && kbs / (s * 2) >= min_kb && s * 2 * M * N <= max_parts) s *= 2;
   return (int)s;
 }
 
@@ -1296,7 +1301,8 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   r.block = dim3(tc::P_THREADS);
   r.name = "tc_gemm_wgrad";
   r.set_args(p);
-  if (splits > 1) {
+  if (op.splits_out) *op.splits_out = splits;
+  if (splits > 1 && !op.defer_reduce) {
     split_reduce_plan(op.ws, splits, op.M, op.N, op.dW, op.ld_dw, op.db, &recs[1]);
     return 2;
   }
