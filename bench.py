@@ -163,8 +163,9 @@ def source_hash():
 
 
 def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
-    summary, or None when absent or when the kernels changed since."""
+    """DRAM bytes per launch of `kernel` (name and layer, e.g.
+    "tc_gemm_fwd:L1") on `workload` from the committed ncu summary, or None
+    when absent or when the kernels changed since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -474,7 +475,8 @@ def main():
     t_roof_ms = roofline_rows(w, rows, peaks)
     top = max(rows, key=lambda r: r["ms"])
     rf = {"bound": top["bound"], "achieved": round(top["achieved"], 3), "peak": top["peak"], "unit": top["unit"],
-          "frac": round(top["frac"], 4), "traffic": ncu_traffic(top["kernel"], w.name),
+          "frac": round(top["frac"], 4),
+          "traffic": ncu_traffic(f"{top['kernel']}:L{top['layer'] + 1}" if top["layer"] >= 0 else top["kernel"], w.name),
           "kernel": f"{top['kernel']} (layer {top['layer'] + 1})" if top["layer"] >= 0 else top["kernel"],
           "launch_ms": round(top["ms"], 5),
           "peak_source": peak_source(peaks, top, w)}
