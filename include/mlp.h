@@ -112,6 +112,18 @@ mlp_status mlp_forward(mlp_t* model, const void* x_dev, void* logits_dev, int32_
 mlp_status mlp_train_step(mlp_t* model, const void* x_dev, const int32_t* labels_dev, float lr, float beta1,
                           float beta2, float eps, float wd, float* loss_dev, void* stream);
 
+/* One training step on a batch in HOST memory (page-locked, so the copies are
+ * asynchronous): x_host [batch, dims[0]] in the model dtype, labels_host
+ * int32 [batch].  The library copies them on its own copy stream into one of
+ * two device input slots in the arena, so the copies for the next call
+ * overlap the kernels of this one; the step waits for its own copies.  The
+ * host buffers must stay valid and unchanged until their copy has completed
+ * (at the latest when the step completes).  loss_host (nullable, pinned)
+ * receives the step's batch-mean loss when the step completes.  Returns once
+ * the copies and the step are enqueued on `stream`. */
+mlp_status mlp_train_step_host(mlp_t* model, const void* x_host, const int32_t* labels_host, float lr, float beta1,
+                               float beta2, float eps, float wd, float* loss_host, void* stream);
+
 /* n_steps consecutive training steps enqueued as ONE CUDA-graph launch;
  * step i reads x_devs[i] / label_devs[i] (host arrays of device pointers)
  * and writes its loss to losses_dev[i] (nullable).  The graph is built on

@@ -40,6 +40,7 @@ _SIGS = {
                           _c.POINTER(_P)]),
     "mlp_forward": (_I32, [_P, _P, _P, _P, _P]),
     "mlp_train_step": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P]),
+    "mlp_train_step_host": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P]),
     "mlp_train_steps": (_I32, [_P, _I32, _c.POINTER(_P), _c.POINTER(_P), _F, _F, _F, _F, _F, _P, _P]),
     "mlp_set_graph_mode": (_I32, [_P, _I32]),
     "mlp_set_option": (_I32, [_P, _I32, _I64]),
@@ -119,6 +120,10 @@ def mlp_forward(h, x_ptr, logits_ptr, argmax_ptr, stream) -> None:
 
 def mlp_train_step(h, x_ptr, labels_ptr, lr, beta1, beta2, eps, wd, loss_ptr, stream) -> None:
     _check(lib().mlp_train_step(h, x_ptr, labels_ptr, lr, beta1, beta2, eps, wd, loss_ptr, stream))
+
+
+def mlp_train_step_host(h, x_host_ptr, labels_host_ptr, lr, beta1, beta2, eps, wd, loss_host_ptr, stream) -> None:
+    _check(lib().mlp_train_step_host(h, x_host_ptr, labels_host_ptr, lr, beta1, beta2, eps, wd, loss_host_ptr, stream))
 
 
 def mlp_train_steps(h, x_ptrs, label_ptrs, lr, beta1, beta2, eps, wd, losses_ptr, stream) -> None:
@@ -267,6 +272,15 @@ class Model:
         mlp_train_step(self.h, x.data_ptr(), labels.data_ptr(), lr, beta1, beta2, eps, wd, loss.data_ptr(),
                        self.stream())
         return loss
+
+    def train_step_host(self, x, labels, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0, loss=None):
+        """One step on pinned host tensors (copies overlap the previous step);
+        `loss` (optional) is a pinned float32 host tensor of one element."""
+        t = self.torch
+        assert not x.is_cuda and x.dtype == self.tdtype and x.is_contiguous() and tuple(x.shape) == (self.batch, self.dims[0])
+        assert not labels.is_cuda and labels.dtype == t.int32 and labels.is_contiguous() and labels.numel() == self.batch
+        mlp_train_step_host(self.h, x.data_ptr(), labels.data_ptr(), lr, beta1, beta2, eps, wd,
+                            loss.data_ptr() if loss is not None else None, self.stream())
 
     def train_steps(self, xs, ys, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0, losses=None):
         for x, y in zip(xs, ys):

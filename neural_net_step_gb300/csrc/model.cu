@@ -89,6 +89,7 @@ struct Layout {
   std::vector<size_t> off_wws, wws_bytes;
   std::vector<char> defer_l;
   size_t off_hws = 0, hws_bytes = 0;   // the fused output layer's partials (read by the optimizer)
+  size_t off_xin[2] = {0, 0}, off_yin[2] = {0, 0};   // device inputs of mlp_train_step_host (two slots)
   size_t total = 0;
 };
 
@@ -196,6 +197,10 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     L.hws_bytes = head_workspace_bytes(batch, dims[L.L], dims[L.L - 1]);
     L.off_hws = take(L.hws_bytes);
   }
+  for (int k = 0; k < 2; ++k) {
+    L.off_xin[k] = take(batch * dims[0] * (dtype == MLP_F32 ? 4 : 2));
+    L.off_yin[k] = take(batch * 4);
+  }
   L.off_ctl = take(sizeof(Ctl));
   L.total = cur;
   return MLP_OK;
@@ -246,6 +251,11 @@ struct mlp {
   std::mutex mu;
   std::vector<GraphCache> graphs;
   int kernels_per_step = 0;
+  // mlp_train_step_host: a copy stream and two input slots, so the copies of
+  // step i+1 run while step i computes
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t copied[2] = {nullptr, nullptr}, consumed[2] = {nullptr, nullptr};
+  int host_calls = 0;
 
   float* plane(int which) const {
     size_t off = which == MLP_PLANE_P ? lay.off_P : which == MLP_PLANE_G ? lay.off_G
@@ -266,6 +276,11 @@ struct mlp {
   // weight of layer l as three bf16 planes (plane pitch lay.plane_n)
   const void* weight_planes(int l) const { return (const void*)((const uint16_t*)w16() + lay.woff[l]); }
   ~mlp() {
+    for (int k = 0; k < 2; ++k) {
+      if (copied[k]) cudaEventDestroy(copied[k]);
+      if (consumed[k]) cudaEventDestroy(consumed[k]);
+    }
+    if (copy_stream) cudaStreamDestroy(copy_stream);
     for (auto& g : graphs) {
       if (g.exec) cudaGraphExecDestroy(g.exec);
       if (g.graph) cudaGraphDestroy(g.graph);
@@ -717,6 +732,45 @@ mlp_status mlp_train_step(mlp_t* m, const void* x, const int32_t* y, float lr, f
   mlp_status st = plan_step(m, x, y, Hyper{lr, b1, b2, eps, wd}, loss, recs);
   if (st != MLP_OK) return st;
   return run(m, 1, recs, (cudaStream_t)stream);
+}
+
+mlp_status mlp_train_step_host(mlp_t* m, const void* x_host, const int32_t* y_host, float lr, float b1, float b2,
+                               float eps, float wd, float* loss_host, void* stream) {
+  if (!m || !x_host || !y_host) return fail(MLP_ERR_ARG, "model, x or labels is NULL");
+  if (!(lr >= 0) || !(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1) || !(eps >= 0) || !(wd >= 0))
+    return fail(MLP_ERR_ARG, "bad hyper-parameters");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  const Layout& L = m->lay;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!m->copy_stream) {
+    CUDA_TRY(cudaStreamCreateWithFlags(&m->copy_stream, cudaStreamNonBlocking));
+    for (int k = 0; k < 2; ++k) {
+      CUDA_TRY(cudaEventCreateWithFlags(&m->copied[k], cudaEventDisableTiming));
+      CUDA_TRY(cudaEventCreateWithFlags(&m->consumed[k], cudaEventDisableTiming));
+      CUDA_TRY(cudaEventRecord(m->consumed[k], s));
+    }
+  }
+  const int k = m->host_calls & 1;
+  void* xd = m->at(L.off_xin[k]);
+  int32_t* yd = (int32_t*)m->at(L.off_yin[k]);
+  const size_t xbytes = (size_t)L.B * L.dims[0] * (L.dtype == MLP_F32 ? 4 : 2);
+  // slot k is free once the step that last read it has finished
+  CUDA_TRY(cudaStreamWaitEvent(m->copy_stream, m->consumed[k], 0));
+  CUDA_TRY(cudaMemcpyAsync(xd, x_host, xbytes, cudaMemcpyHostToDevice, m->copy_stream));
+  CUDA_TRY(cudaMemcpyAsync(yd, y_host, (size_t)L.B * 4, cudaMemcpyHostToDevice, m->copy_stream));
+  CUDA_TRY(cudaEventRecord(m->copied[k], m->copy_stream));
+  CUDA_TRY(cudaStreamWaitEvent(s, m->copied[k], 0));
+  std::vector<LaunchRec> recs;
+  float* loss_dev = &m->ctl()->loss_slot;
+  mlp_status st = plan_step(m, xd, yd, Hyper{lr, b1, b2, eps, wd}, loss_dev, recs);
+  if (st != MLP_OK) return st;
+  st = run(m, 1, recs, s);
+  if (st != MLP_OK) return st;
+  CUDA_TRY(cudaEventRecord(m->consumed[k], s));
+  if (loss_host) CUDA_TRY(cudaMemcpyAsync(loss_host, loss_dev, 4, cudaMemcpyDeviceToHost, s));
+  ++m->host_calls;
+  return ok();
 }
 
 mlp_status mlp_train_steps(mlp_t* m, int n_steps, const void* const* xs, const int32_t* const* ys, float lr,

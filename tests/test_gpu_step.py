@@ -339,3 +339,34 @@ def test_fused_head_matches_unfused_path(name, batch):
     kappa = P.oracle_abs_sums(w, params0, *bl[0], "fp64")
     for a, b, k in zip(g1, g0, kappa):
         assert np.all(np.abs(a - b) <= P.fp32_grad_tol(k))
+
+
+# --------------------------------------------------------------------------
+# Host-input steps (copies on the library's copy stream, two input slots)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("name,batch", [("mnist_mlp_b4096", None), ("cifar_mlp_b8192", 512)])
+def test_train_step_host_matches_device_inputs(name, batch):
+    """mlp_train_step_host on pinned host batches gives bit-identical losses and
+    parameters to mlp_train_step on the same batches already on the device,
+    over more steps than input slots (the slots are reused)."""
+    w = W[name]
+    B = w.batch if batch is None else batch
+    params0 = synth.make_params(w)
+    bl = P.batches(w, 5, B)
+    m = make_model(w, B, params0)
+    d_losses, d_params, _ = gpu_run(m, w, bl)
+    m.close()
+    m = make_model(w, B, params0)
+    hyper = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, wd=w.wd)
+    hl = torch.zeros(len(bl), dtype=torch.float32).pin_memory()
+    hx = [x.contiguous().pin_memory() for x, _ in bl]
+    hy = [y.contiguous().pin_memory() for _, y in bl]
+    for i in range(len(bl)):
+        m.train_step_host(hx[i], hy[i], loss=hl[i:i + 1], **hyper)
+    torch.cuda.synchronize()
+    m.check_errors()
+    p, step = m.read_flat(nn.PLANE_P)
+    m.close()
+    assert step == len(bl)
+    assert np.array_equal(hl.numpy().astype(np.float64), d_losses)
+    assert np.array_equal(P.flat(m.split(p.astype(np.float64))), P.flat(d_params))
