@@ -251,10 +251,11 @@ struct mlp {
   std::mutex mu;
   std::vector<GraphCache> graphs;
   int kernels_per_step = 0;
-  // mlp_train_step_host: a copy stream and two input slots, so the copies of
+  // mlp_train_step_host: copy streams and two input slots, so the copies of
   // step i+1 run while step i computes
-  cudaStream_t copy_stream = nullptr;
-  cudaEvent_t copied[2] = {nullptr, nullptr}, consumed[2] = {nullptr, nullptr};
+  static constexpr int kCopyStreams = 4;   // x is copied in this many pieces, one per stream (copy engine)
+  cudaStream_t copy_stream[kCopyStreams] = {};
+  cudaEvent_t copied[2][kCopyStreams] = {}, consumed[2] = {nullptr, nullptr};
   int host_calls = 0;
 
   float* plane(int which) const {
@@ -277,10 +278,12 @@ struct mlp {
   const void* weight_planes(int l) const { return (const void*)((const uint16_t*)w16() + lay.woff[l]); }
   ~mlp() {
     for (int k = 0; k < 2; ++k) {
-      if (copied[k]) cudaEventDestroy(copied[k]);
+      for (int c = 0; c < kCopyStreams; ++c)
+        if (copied[k][c]) cudaEventDestroy(copied[k][c]);
       if (consumed[k]) cudaEventDestroy(consumed[k]);
     }
-    if (copy_stream) cudaStreamDestroy(copy_stream);
+    for (int c = 0; c < kCopyStreams; ++c)
+      if (copy_stream[c]) cudaStreamDestroy(copy_stream[c]);
     for (auto& g : graphs) {
       if (g.exec) cudaGraphExecDestroy(g.exec);
       if (g.graph) cudaGraphDestroy(g.graph);
@@ -743,24 +746,34 @@ mlp_status mlp_train_step_host(mlp_t* m, const void* x_host, const int32_t* y_ho
   DevGuard g(m->device);
   const Layout& L = m->lay;
   cudaStream_t s = (cudaStream_t)stream;
-  if (!m->copy_stream) {
-    CUDA_TRY(cudaStreamCreateWithFlags(&m->copy_stream, cudaStreamNonBlocking));
+  constexpr int NC = mlp::kCopyStreams;
+  if (!m->copy_stream[0]) {
+    for (int c = 0; c < NC; ++c) CUDA_TRY(cudaStreamCreateWithFlags(&m->copy_stream[c], cudaStreamNonBlocking));
     for (int k = 0; k < 2; ++k) {
-      CUDA_TRY(cudaEventCreateWithFlags(&m->copied[k], cudaEventDisableTiming));
+      for (int c = 0; c < NC; ++c) CUDA_TRY(cudaEventCreateWithFlags(&m->copied[k][c], cudaEventDisableTiming));
       CUDA_TRY(cudaEventCreateWithFlags(&m->consumed[k], cudaEventDisableTiming));
       CUDA_TRY(cudaEventRecord(m->consumed[k], s));
     }
   }
   const int k = m->host_calls & 1;
-  void* xd = m->at(L.off_xin[k]);
+  uint8_t* xd = (uint8_t*)m->at(L.off_xin[k]);
   int32_t* yd = (int32_t*)m->at(L.off_yin[k]);
   const size_t xbytes = (size_t)L.B * L.dims[0] * (L.dtype == MLP_F32 ? 4 : 2);
-  // slot k is free once the step that last read it has finished
-  CUDA_TRY(cudaStreamWaitEvent(m->copy_stream, m->consumed[k], 0));
-  CUDA_TRY(cudaMemcpyAsync(xd, x_host, xbytes, cudaMemcpyHostToDevice, m->copy_stream));
-  CUDA_TRY(cudaMemcpyAsync(yd, y_host, (size_t)L.B * 4, cudaMemcpyHostToDevice, m->copy_stream));
-  CUDA_TRY(cudaEventRecord(m->copied[k], m->copy_stream));
-  CUDA_TRY(cudaStreamWaitEvent(s, m->copied[k], 0));
+  // slot k is free once the step that last read it has finished; x goes in
+  // NC pieces on NC streams (several copy engines), the labels with the last
+  const size_t piece = (xbytes / NC + 255) / 256 * 256;
+  for (int c = 0; c < NC; ++c) {
+    CUDA_TRY(cudaStreamWaitEvent(m->copy_stream[c], m->consumed[k], 0));
+    const size_t o = (size_t)c * piece;
+    if (o < xbytes) {
+      const size_t n = o + piece <= xbytes ? piece : xbytes - o;
+      CUDA_TRY(cudaMemcpyAsync(xd + o, (const uint8_t*)x_host + o, n, cudaMemcpyHostToDevice, m->copy_stream[c]));
+    }
+    if (c == NC - 1)
+      CUDA_TRY(cudaMemcpyAsync(yd, y_host, (size_t)L.B * 4, cudaMemcpyHostToDevice, m->copy_stream[c]));
+    CUDA_TRY(cudaEventRecord(m->copied[k][c], m->copy_stream[c]));
+    CUDA_TRY(cudaStreamWaitEvent(s, m->copied[k][c], 0));
+  }
   std::vector<LaunchRec> recs;
   float* loss_dev = &m->ctl()->loss_slot;
   mlp_status st = plan_step(m, xd, yd, Hyper{lr, b1, b2, eps, wd}, loss_dev, recs);
