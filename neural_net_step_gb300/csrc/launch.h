@@ -17,7 +17,25 @@ struct LaunchRec {
   unsigned smem = 0;
   unsigned args_size = 0;
   const char* name = "";
+  // Graph dependencies: indices of earlier records in the same plan that this
+  // launch must follow; ndeps < 0 means "the record just before it".  Eager
+  // launches run the records in order and ignore this.
+  static constexpr int kMaxDeps = 4;
+  int deps[kMaxDeps] = {0, 0, 0, 0};
+  int ndeps = -1;
   alignas(128) unsigned char args[kMaxArgBytes];
+
+  void depend_on(const int* d, int n) {
+    ndeps = 0;
+    for (int i = 0; i < n; ++i)
+      if (d[i] >= 0 && ndeps < kMaxDeps) deps[ndeps++] = d[i];
+  }
+  bool same_deps(const LaunchRec& o) const {
+    if (ndeps != o.ndeps) return false;
+    for (int i = 0; i < ndeps; ++i)
+      if (deps[i] != o.deps[i]) return false;
+    return true;
+  }
 
   template <typename P>
   void set_args(const P& p) {

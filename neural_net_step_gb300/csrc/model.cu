@@ -416,7 +416,13 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
   float* G = m->plane(MLP_PLANE_G);
   AdamWOp::Seg seg[AdamWOp::kMaxSegs];   // gradients the optimizer adds from partial sums
   int nseg = 0;
+  // In the graph the weight gradients form a side chain: wgrad(l) runs beside
+  // dgrad(l) (both only read dY_l).  dgrad(l) also waits for wgrad(l+1), the
+  // last reader of the ping-pong buffer it overwrites; the optimizer joins both.
+  int main_tail = (int)out.size() - 1, side_tail = -1;
   for (int l = top; l >= 0; --l) {
+    const int side_prev = side_tail;
+    const int wg_first = (int)out.size();
     const void* Xl = l == 0 ? (x3 ? m->at(L.off_xs) : x) : m->at(L.off_h[l - 1]);
     const int64_t ldxl = l == 0 ? (x3 ? L.ld_x : L.dims[0]) : L.ld_h[l - 1];
     GemmOp wg;
@@ -439,6 +445,9 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
       const int n_ = gemm_plan(wg, r_, e_, sizeof(e_));
       if (n_ < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
       add(out, n_, r_);
+      const int d[2] = {main_tail, side_tail};
+      out[wg_first].depend_on(d, 2);   // a split-K reduce after it follows it
+      side_tail = (int)out.size() - 1;
       if (n_ == 1 && used > 1) {
         seg[nseg++] = AdamWOp::Seg{L.woff[l], MN, wg.ws, used, MN};
         seg[nseg++] = AdamWOp::Seg{L.boff[l], wg.M, wg.ws + (int64_t)used * MN, used, wg.M};
@@ -457,6 +466,9 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
       dg.out = m->at(L.off_dy[buf]); dg.ldo = L.ld_h[l - 1];
       dg.err = &ctl->err;
       PLAN_TRY(gemm_plan(dg, r_, e_, sizeof(e_)));
+      const int d[2] = {main_tail, side_prev};
+      out.back().depend_on(d, 2);
+      main_tail = (int)out.size() - 1;
       dY = dg.out; ldy = dg.ldo;
       buf ^= 1;
     }
@@ -484,6 +496,8 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
   char e_[512] = "";
   LaunchRec r;
   if (adamw_plan(ad, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_ARG, "%s", e_);
+  const int d[2] = {main_tail, side_tail};
+  r.depend_on(d, 2);
   out.push_back(r);
   return MLP_OK;
 }
@@ -501,7 +515,7 @@ bool same_topology(const std::vector<LaunchRec>& a, const std::vector<LaunchRec>
   for (size_t i = 0; i < a.size(); ++i) {
     const LaunchRec &x = a[i], &y = b[i];
     if (x.func != y.func || x.grid.x != y.grid.x || x.grid.y != y.grid.y || x.grid.z != y.grid.z ||
-        x.block.x != y.block.x || x.smem != y.smem)
+        x.block.x != y.block.x || x.smem != y.smem || !x.same_deps(y))
       return false;
   }
   return true;
@@ -526,26 +540,37 @@ mlp_status launch_graph(mlp* m, int key, std::vector<LaunchRec>& recs, cudaStrea
   }
   if (!gc->exec) {
     CUDA_TRY(cudaGraphCreate(&gc->graph, 0));
-    cudaGraphNode_t prev = nullptr;
-    // a chain; with pdl each edge is programmatic: a kernel may be scheduled
-    // once every block of its predecessor has started, and waits inside
-    // (griddepcontrol.wait) for the predecessor to complete
+    // Each record depends on the one before it unless it names its own
+    // dependencies (the side chain of weight gradients).  With pdl a
+    // single-dependency edge is programmatic: the kernel may be scheduled once
+    // every block of its predecessor has started, and waits inside
+    // (griddepcontrol.wait) for the predecessor to complete.
     cudaGraphEdgeData ed;
     memset(&ed, 0, sizeof(ed));
     ed.from_port = cudaGraphKernelNodePortProgrammatic;
     ed.type = cudaGraphDependencyTypeProgrammatic;
-    for (auto& r : recs) {
+    for (size_t i = 0; i < recs.size(); ++i) {
+      const LaunchRec& r = recs[i];
+      cudaGraphNode_t dn[LaunchRec::kMaxDeps];
+      int nd = 0;
+      if (r.ndeps < 0) {
+        if (i > 0) dn[nd++] = gc->nodes[i - 1];
+      } else {
+        for (int k = 0; k < r.ndeps; ++k) {
+          if (r.deps[k] < 0 || r.deps[k] >= (int)i) return fail(MLP_ERR_STATE, "bad plan dependency");
+          dn[nd++] = gc->nodes[r.deps[k]];
+        }
+      }
       void* argp[1];
       cudaKernelNodeParams kp = node_params(r, argp);
       cudaGraphNode_t node;
-      if (prev && m->pdl) {
+      if (nd == 1 && m->pdl) {
         CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, nullptr, 0, &kp));
-        CUDA_TRY(cudaGraphAddDependencies(gc->graph, &prev, &node, &ed, 1));
+        CUDA_TRY(cudaGraphAddDependencies(gc->graph, dn, &node, &ed, 1));
       } else {
-        CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, prev ? &prev : nullptr, prev ? 1 : 0, &kp));
+        CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, nd ? dn : nullptr, nd, &kp));
       }
       gc->nodes.push_back(node);
-      prev = node;
     }
     gc->pdl = m->pdl;
     CUDA_TRY(cudaGraphInstantiate(&gc->exec, gc->graph, 0));
