@@ -843,16 +843,22 @@ constexpr int W_TMEM_COLS = 512;                                // 2 x (128 dW +
 // X3 (fp32 operands as three bf16 planes): a stage holds every plane of a
 // 32-row K slice of A and B (48 KB, three deep) and feeds the six products,
 // smallest first, into one accumulator per work unit.
-template <bool X3> struct WCfg {
+// WBN = 256 (bf16, long K per work unit): 128x256 tiles halve the operand
+// bytes per MMA; the accumulator then fills TMEM with the bias gradient
+// beside it, so it is single-buffered (the epilogue does not overlap the next
+// unit, which long units amortise).
+template <bool X3, int WBN = W_BN> struct WCfg {
   static constexpr int NPL = X3 ? 3 : 1;
   static constexpr int BKW = X3 ? 32 : 64;                 // K rows per stage
   static constexpr int CHUNK_BYTES = 64 * BKW * 2;         // one 64-wide MN chunk of a plane
   static constexpr int A_PLANE_BYTES = (BM / 64) * CHUNK_BYTES;
-  static constexpr int B_PLANE_BYTES = (W_BN / 64) * CHUNK_BYTES;
+  static constexpr int B_PLANE_BYTES = (WBN / 64) * CHUNK_BYTES;
   static constexpr int A_BYTES = NPL * A_PLANE_BYTES;
   static constexpr int B_BYTES = NPL * B_PLANE_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = X3 ? 3 : 4;
+  static constexpr int STAGES = X3 ? 3 : (WBN >= 256 ? 3 : 4);
+  static constexpr int NBUF = WBN >= 256 ? 1 : 2;          // TMEM accumulator buffers (stride 256 columns)
+  static_assert(!(X3 && WBN >= 256), "planes use 128-wide tiles");
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + W_EPI_BYTES + W_ONES_BYTES + 1024 + 256;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
@@ -880,9 +886,9 @@ __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
   return __uint_as_float(r);
 }
 
-template <bool X3>
+template <bool X3, int WBN>
 __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const __grid_constant__ WParams p) {
-  using C = WCfg<X3>;
+  using C = WCfg<X3, WBN>;
   constexpr int W_STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -927,7 +933,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
     const int tile = u % p.num_tiles;
     split = u / p.num_tiles;
     m0 = (tile / p.tiles_n) * BM;
-    n0 = (tile % p.tiles_n) * W_BN;
+    n0 = (tile % p.tiles_n) * WBN;
     kb0 = split * p.kb_per_split;
     kb1 = min(p.num_kb, kb0 + p.kb_per_split);
   };
@@ -953,8 +959,8 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
           if (!X3) {
             tma_load_2d(sa, &p.tmA, m0, k0, full_bar(s));
             tma_load_2d(sa + C::CHUNK_BYTES, &p.tmA, m0 + 64, k0, full_bar(s));
-            tma_load_2d(sb, &p.tmB, n0, k0, full_bar(s));
-            tma_load_2d(sb + C::CHUNK_BYTES, &p.tmB, n0 + 64, k0, full_bar(s));
+#pragma unroll
+            for (int c = 0; c < WBN / 64; ++c) tma_load_2d(sb + c * C::CHUNK_BYTES, &p.tmB, n0 + 64 * c, k0, full_bar(s));
           } else {
 #pragma unroll
             for (int pl = 0; pl < 3; ++pl) {   // every plane of A and B once
@@ -979,8 +985,9 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
         const bool do_db = p.db_out != nullptr && n0 == 0;
-        const int buf = tc & 1;
-        if (!mbar_wait(tempty_bar(buf), (((uint32_t)tc >> 1) & 1u) ^ 1u, p.err)) break;
+        const int buf = C::NBUF == 2 ? (tc & 1) : 0;
+        const uint32_t tph = C::NBUF == 2 ? (((uint32_t)tc >> 1) & 1u) : ((uint32_t)tc & 1u);
+        if (!mbar_wait(tempty_bar(buf), tph ^ 1u, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * 256);
         bool db_started = false;
@@ -1007,7 +1014,8 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
               const uint32_t acc = (kb > kb0 || f > 0 || kk > 0) ? 1u : 0u;
               mma_bf16(d, ad, bd, p.idesc, acc);
               if (db_here) {
-                mma_bf16(d + 128u, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db, db_started ? 1u : 0u);
+                mma_bf16(d + (uint32_t)WBN, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db,
+                         db_started ? 1u : 0u);
                 db_started = true;
               }
             }
@@ -1029,38 +1037,45 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       int m0, n0, split, kb0, kb1;
       unit_coords(u, m0, n0, split, kb0, kb1);
       const bool do_db = p.db_out != nullptr && n0 == 0;
-      const int buf = tc & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), ((uint32_t)tc >> 1) & 1u, p.err));
+      const int buf = C::NBUF == 2 ? (tc & 1) : 0;
+      const uint32_t tph = C::NBUF == 2 ? (((uint32_t)tc >> 1) & 1u) : ((uint32_t)tc & 1u);
+      ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), tph, p.err));
       if (!ok) break;
       tc_fence_after();
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
       const int gm = m0 + q * 32 + lane;
       float dbv = 0.f;
-      if (do_db && half == 0 && kb1 > kb0) dbv = tmem_ld1(trow + 128u);
-      float v[64];
-      tmem_ld32(trow, v, half * 64);
-      tmem_ld32(trow, v + 32, half * 64 + 32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));   // this warp's part of TMEM is read
+      if (do_db && half == 0 && kb1 > kb0) dbv = tmem_ld1(trow + (uint32_t)WBN);
       if (do_db && half == 0 && gm < p.M) p.db_out[(int64_t)split * p.M + gm] = dbv;
-#pragma unroll
-      for (int sub = 0; sub < 2; ++sub, ++chunk) {
-        const int sbuf = chunk % W_EPI_BUFS;
-        if (lane == 0) bulk_wait_read1();
-        __syncwarp();
-        uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
-#pragma unroll
-        for (int w4 = 0; w4 < 8; ++w4) {
-          const float4 f = make_float4(v[sub * 32 + 4 * w4], v[sub * 32 + 4 * w4 + 1], v[sub * 32 + 4 * w4 + 2],
-                                       v[sub * 32 + 4 * w4 + 3]);
-          *reinterpret_cast<float4*>(srow + ((w4 ^ (lane & 7)) << 4)) = f;
+      // this warp's WBN/2 columns, 64 at a time, each as two 32x32 fp32 stores
+#pragma unroll 1
+      for (int c0 = half * (WBN / 2); c0 < (half + 1) * (WBN / 2); c0 += 64) {
+        float v[64];
+        tmem_ld32(trow, v, c0);
+        tmem_ld32(trow, v + 32, c0 + 32);
+        if (c0 + 64 >= (half + 1) * (WBN / 2)) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));   // this warp's part of TMEM is read
         }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&p.tmOut, stage0 + sbuf * 4096, n0 + half * 64 + sub * 32, m0 + q * 32, split);
-          bulk_commit();
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub, ++chunk) {
+          const int sbuf = chunk % W_EPI_BUFS;
+          if (lane == 0) bulk_wait_read1();
+          __syncwarp();
+          uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
+#pragma unroll
+          for (int w4 = 0; w4 < 8; ++w4) {
+            const float4 f = make_float4(v[sub * 32 + 4 * w4], v[sub * 32 + 4 * w4 + 1], v[sub * 32 + 4 * w4 + 2],
+                                         v[sub * 32 + 4 * w4 + 3]);
+            *reinterpret_cast<float4*>(srow + ((w4 ^ (lane & 7)) << 4)) = f;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&p.tmOut, stage0 + sbuf * 4096, n0 + c0 + sub * 32, m0 + q * 32, split);
+            bulk_commit();
+          }
         }
       }
     }
@@ -1178,9 +1193,10 @@ int pick_bn(const GemmOp& op) {
 
 }  // namespace
 
-// bk: K rows per pipeline stage (32 for fp32 operands held as planes).
-int tc_wgrad_splits(int64_t M, int64_t N, int64_t K, int bk = tc::BK) {
-  const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, 128);
+// bk: K rows per pipeline stage (32 for fp32 operands held as planes); bn:
+// the tile width.
+int tc_wgrad_splits(int64_t M, int64_t N, int64_t K, int bk = tc::BK, int bn = tc::W_BN) {
+  const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, bn);
   const int64_t kbs = ceil_div(K, bk);
   // >= 2 work units per SM, each at least 8 stages long (4 with planes: a
   // stage then carries six products)
@@ -1192,9 +1208,37 @@ int tc_wgrad_splits(int64_t M, int64_t N, int64_t K, int bk = tc::BK) {
   return (int)s;
 }
 
+// Tile width and K splits of a tensor-core weight gradient.  bf16 with at
+// least 256 columns: 256-wide tiles, with the split count that minimises
+// waves x (stages per unit + 6), the 6 standing for the epilogue that a
+// single-buffered accumulator does not overlap; else 128-wide tiles.
+static void tc_wgrad_choice(int dtype, int64_t M, int64_t N, int64_t K, int* bn, int* splits) {
+  if (dtype == DT_F32X3) {
+    *bn = tc::W_BN;
+    *splits = tc_wgrad_splits(M, N, K, tc::WCfg<true>::BKW);
+    return;
+  }
+  if (N < 256) {
+    *bn = tc::W_BN;
+    *splits = tc_wgrad_splits(M, N, K);
+    return;
+  }
+  const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, 256);
+  const int64_t kbs = ceil_div(K, tc::BK);
+  int64_t best_s = 1, best_cost = INT64_MAX;
+  for (int64_t s = 1; s <= 256 && (s == 1 || kbs / s >= 8); s *= 2) {
+    const int64_t cost = ceil_div(tiles * s, kSMs) * (ceil_div(kbs, s) + 6);
+    if (cost < best_cost) { best_cost = cost; best_s = s; }
+  }
+  *bn = 256;
+  *splits = (int)best_s;
+}
+
 int wgrad_splits(int dtype, int64_t M, int64_t N, int64_t K) {
-  return dtype == DT_F32 ? simt_gemm_splits(M, N, K)
-                         : tc_wgrad_splits(M, N, K, dtype == DT_F32X3 ? tc::WCfg<true>::BKW : tc::BK);
+  if (dtype == DT_F32) return simt_gemm_splits(M, N, K);
+  int bn, s;
+  tc_wgrad_choice(dtype, M, N, K, &bn, &s);
+  return s;
 }
 
 size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int splits) {
@@ -1248,14 +1292,14 @@ bool make_tmap_f32_3d(CUtensorMap* tm, const void* ptr, int64_t inner, int64_t r
   return true;
 }
 
-template <bool X3>
+template <bool X3, int WBN>
 const void* tcw_kernel_ptr() {
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute((const void*)tc::tc_wgrad_persistent_kernel<X3>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, tc::WCfg<X3>::SMEM_BYTES);
+    cudaFuncSetAttribute((const void*)tc::tc_wgrad_persistent_kernel<X3, WBN>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, tc::WCfg<X3, WBN>::SMEM_BYTES);
   });
-  return (const void*)tc::tc_wgrad_persistent_kernel<X3>;
+  return (const void*)tc::tc_wgrad_persistent_kernel<X3, WBN>;
 }
 
 // Weight gradient on the persistent split-K kernel (+ the fixed-order reduce).
@@ -1268,15 +1312,17 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   if (!make_tmap_op(&p.tmB, x3, op.B, op.N, op.K, op.ldb, op.b_plane, 64, bkw, err, errlen)) return -1;
   p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
   p.num_kb = (int)ceil_div(op.K, bkw);
-  int splits = op.splits > 0 ? op.splits : wgrad_splits(op.dtype, op.M, op.N, op.K);
+  int wbn, splits;
+  tc_wgrad_choice(op.dtype, op.M, op.N, op.K, &wbn, &splits);
+  if (op.splits > 0) splits = op.splits;
   if (splits > p.num_kb) splits = p.num_kb;
   p.kb_per_split = (int)ceil_div(p.num_kb, splits);
   splits = (int)ceil_div(p.num_kb, p.kb_per_split);
   p.splits = splits;
-  p.tiles_n = (int)ceil_div(op.N, tc::W_BN);
+  p.tiles_n = (int)ceil_div(op.N, wbn);
   p.num_tiles = (int)(ceil_div(op.M, tc::BM) * p.tiles_n);
   p.num_units = p.num_tiles * splits;
-  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(tc::W_BN >> 3) << 17) |
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(wbn >> 3) << 17) |
             ((uint32_t)(tc::BM >> 4) << 24);
   p.idesc_db = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(16 >> 3) << 17) |
                ((uint32_t)(tc::BM >> 4) << 24);
@@ -1294,8 +1340,9 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
     p.db_out = op.db;
   }
   LaunchRec& r = recs[0];
-  r.func = x3 ? tcw_kernel_ptr<true>() : tcw_kernel_ptr<false>();
-  r.smem = x3 ? tc::WCfg<true>::SMEM_BYTES : tc::WCfg<false>::SMEM_BYTES;
+  r.func = x3 ? tcw_kernel_ptr<true, 128>() : wbn == 256 ? tcw_kernel_ptr<false, 256>() : tcw_kernel_ptr<false, 128>();
+  r.smem = x3 ? tc::WCfg<true>::SMEM_BYTES
+              : wbn == 256 ? tc::WCfg<false, 256>::SMEM_BYTES : tc::WCfg<false, 128>::SMEM_BYTES;
   const int sms = device_sms();
   r.grid = dim3((unsigned)(p.num_units < sms ? p.num_units : sms));
   r.block = dim3(tc::P_THREADS);

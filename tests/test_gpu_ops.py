@@ -131,6 +131,7 @@ WGRAD_CASES = [
     (nn.BF16, 100, 512, 1000),                    # ragged batch
     (nn.BF16, 512, 512, 4096),                    # split-K
     (nn.BF16, 4096, 1024, 256),
+    (nn.BF16, 2000, 1000, 16384),                 # 256-wide tiles (long K per unit), ragged M and N
 ]
 
 
