@@ -521,6 +521,27 @@ __device__ __forceinline__ float split_plane(float x, int pl) {
   if (pl == 1) return r;
   return r - __bfloat162float(__float2bfloat16_rn(r));
 }
+// Thread-block cluster helpers (the CTA pair of tc_gemm_pair_kernel).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA in the cluster: release this thread's prior
+// writes (including to other CTAs' shared memory) and wait for all threads.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The shared::cluster address of this CTA's shared::cta address `a` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_cluster(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t a, float x, float y, float z, float w) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w)
+               : "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"((uint64_t)tm),
                "r"(src), "r"(c0), "r"(c1)
@@ -534,8 +555,13 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 
 // X3: fp32 operands as three bf16 planes (3-D maps, six K-loop phases) and
 // an fp32 result written as its three planes.
-template <int BN, bool X3>
-__global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const __grid_constant__ PParams p) {
+// PAIR: the CTAs of a 2-CTA cluster share one output tile, each taking half of
+// the K stages; after both main loops each CTA hands the accumulator rows the
+// other finishes (64 of the 128) to it through distributed shared memory and
+// finishes its own 64 rows.  Used when there are at most half as many tiles
+// as SMs, so every CTA has one tile and its pipeline memory is free at the end.
+template <int BN, bool X3, bool PAIR>
+__device__ __forceinline__ void persistent_body(const PParams& p) {
   using C = PCfg<BN, X3>;
   constexpr int OUT_PLANES = X3 ? 3 : 1;
   extern __shared__ uint8_t smem_raw[];
@@ -572,6 +598,16 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
   const uint32_t tmem = *tmem_slot_ptr;
   pdl_enter();   // shared memory and TMEM are set up: now wait for the inputs
   const uint32_t stage_tx = C::STAGE_BYTES;
+  // tiles walked by this CTA (a pair walks them together) and its K stages
+  const int pr = PAIR ? (int)cluster_ctarank() : 0;
+  // a pair handles exactly one tile; a launch with more tiles than pairs does nothing
+  const bool bad_pair = PAIR && p.num_tiles > (int)(gridDim.x >> 1);
+  if (bad_pair && threadIdx.x == 0 && blockIdx.x == 0 && p.err) atomicOr(p.err, ERRBIT_BAD_LAUNCH);
+  const int t0 = bad_pair ? p.num_tiles : PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int tstep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int kh = PAIR ? (p.num_kb + 1) / 2 : p.num_kb;
+  const int kb_lo = PAIR ? pr * kh : 0;
+  const int kb_hi = PAIR ? min(p.num_kb, kb_lo + kh) : p.num_kb;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -580,9 +616,9 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
       prefetch_tmap(&p.tmB);
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = t0; t < p.num_tiles && ok; t += tstep) {
         const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
@@ -623,12 +659,12 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
       const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
       int it = 0, tc = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++tc) {
+      for (int t = t0; t < p.num_tiles && ok; t += tstep, ++tc) {
         const int buf = tc & 1;
         if (!mbar_wait(tempty_bar(buf), (((uint32_t)tc >> 1) & 1u) ^ 1u, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(full_bar(s), ph, p.err)) { ok = false; break; }
@@ -640,7 +676,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t ad = sdesc(sa + kk * 32u, 16u, 1024u);
               const uint64_t bd = sdesc(sb + kk * b_kstep, b_lbo, 1024u);
-              mma_bf16(d, ad, bd, p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              mma_bf16(d, ad, bd, p.idesc, (kb > kb_lo || kk > 0) ? 1u : 0u);
             }
           } else {
             // five small products into the second accumulator (smallest
@@ -655,7 +691,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
               for (int kk = 0; kk < BK / 16; ++kk) {
                 const uint64_t ad = sdesc(spa + kk * 32u, 16u, 1024u);
                 const uint64_t bd = sdesc(spb + kk * b_kstep, b_lbo, 1024u);
-                const bool first = kb == 0 && kk == 0 && (f == 0 || f == 5);
+                const bool first = kb == kb_lo && kk == 0 && (f == 0 || f == 5);
                 mma_bf16(dd, ad, bd, p.idesc, first ? 0u : 1u);
               }
             }
@@ -665,7 +701,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
         mma_commit(tfull_bar(buf));
       }
     }
-  } else {
+  } else if (!PAIR) {
     // ---------------- epilogue warps 2..9 ----------------
     // warp w reads TMEM lanes 32*(w%4)..+31 (its lane quarter) and the
     // columns of its half of the tile: two warps share each quarter
@@ -675,7 +711,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
     uint8_t* stage0_ptr = base_ptr + (stage0 - base);
     int tc = 0, chunk = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++tc) {
+    for (int t = t0; t < p.num_tiles && ok; t += tstep, ++tc) {
       const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
       const int buf = tc & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), ((uint32_t)tc >> 1) & 1u, p.err));
@@ -815,12 +851,160 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
+  if (PAIR) {
+    // ---------------- the pair's epilogue (every thread of both CTAs) ----------------
+    // CTA rank r finishes rows 64 r .. 64 r + 63 (TMEM lane quarters 2r, 2r+1)
+    // and sends the other 64 rows (big + small accumulators added) to its
+    // peer's pipeline memory, padded rows of kRP floats.
+    constexpr int kRP = BN + 4;
+    const bool have = t0 < p.num_tiles;   // the same for both CTAs of the pair
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const bool mine = warp >= 2 && (q >> 1) == pr;
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    bool ok = true;
+    if (warp >= 2 && have) {
+      ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(0), 0u, p.err));
+      tc_fence_after();
+    }
+    cluster_sync_all();   // both CTAs' MMAs are done: their pipeline memory is free
+    const uint32_t recv = a_base;   // [64][kRP] fp32
+    if (warp >= 2 && !mine && have && ok) {
+      const uint32_t peer = mapa_cluster(recv, (uint32_t)(pr ^ 1)) +
+                            (uint32_t)((((q & 1) * 32 + lane) * kRP + half * (BN / 2)) * 4);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN / 2; c0 += 64) {
+        float v[64];
+        tmem_ld64(trow + (uint32_t)(half * (BN / 2) + c0), v);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float w[32];
+          tmem_ld32(trow + (uint32_t)(BN + half * (BN / 2) + c0 + 32 * hh), w, 0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[32 * hh + j] += w[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) st_cluster_v4(peer + (uint32_t)((c0 + j) * 4), v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
+    }
+    cluster_sync_all();   // the peer's rows have landed
+    if (mine && have && ok) {
+      const int t = t0;
+      const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
+      const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * C::EPI_BUFS * 4096);
+      uint8_t* stage0_ptr = base_ptr + (stage0 - base);
+      const float* rrow = reinterpret_cast<const float*>(base_ptr + (recv - base)) + ((q & 1) * 32 + lane) * kRP;
+      const int gm = m0 + q * 32 + lane;
+      const bool row_ok = gm < p.M;
+      int chunk = 0;
+#pragma unroll 1
+      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 64) {
+        const int gn0 = n0 + c0;
+        float bias0 = 0.f, bias1 = 0.f;
+        uint32_t mask0 = 0u, mask1 = 0u;
+        if (p.kind == GEMM_FWD) {
+          if (gn0 + lane < p.N) bias0 = __ldg(p.bias + gn0 + lane);
+          if (gn0 + 32 + lane < p.N) bias1 = __ldg(p.bias + gn0 + 32 + lane);
+        } else if (p.act == ACT_RELU && row_ok) {
+          const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
+          if (gn0 + 64 <= p.N) {
+            uint4 a[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] = __ldg(reinterpret_cast<const uint4*>(ar) + u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&a[u]);
+              uint32_t bits = 0u;
+#pragma unroll
+              for (int h = 0; h < 8; ++h) bits |= (__bfloat162float(e[h]) > 0.f ? 1u : 0u) << h;
+              if (u < 4) mask0 |= bits << (8 * u);
+              else mask1 |= bits << (8 * (u - 4));
+            }
+          } else {
+            for (int j = 0; j < 32; ++j) {
+              if (gn0 + j < p.N && __bfloat162float(ar[j]) > 0.f) mask0 |= 1u << j;
+              if (gn0 + 32 + j < p.N && __bfloat162float(ar[32 + j]) > 0.f) mask1 |= 1u << j;
+            }
+          }
+        }
+        float v[64];
+        tmem_ld64(trow + (uint32_t)c0, v);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float w[32];
+          tmem_ld32(trow + (uint32_t)(BN + c0 + 32 * hh), w, 0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[32 * hh + j] += w[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {   // + the peer's partial sums of these rows
+          const float4 r4 = *reinterpret_cast<const float4*>(rrow + c0 + j);
+          v[j] += r4.x; v[j + 1] += r4.y; v[j + 2] += r4.z; v[j + 3] += r4.w;
+        }
+        if (p.kind == GEMM_FWD) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] += __shfl_sync(0xffffffffu, bias0, j);
+            v[32 + j] += __shfl_sync(0xffffffffu, bias1, j);
+          }
+#pragma unroll
+          for (int j = 0; j < 64; ++j) v[j] = apply_act(v[j], p.act);
+        } else if (p.act == ACT_RELU) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] *= (float)((mask0 >> j) & 1u);
+            v[32 + j] *= (float)((mask1 >> j) & 1u);
+          }
+        }
+#pragma unroll 1
+        for (int pl = 0; pl < OUT_PLANES; ++pl, ++chunk) {
+          const int sbuf = chunk % C::EPI_BUFS;
+          if (lane == 0) {
+            if (C::EPI_BUFS == 1) bulk_wait_read0();
+            else bulk_wait_read1();
+          }
+          __syncwarp();
+          uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint4 w;
+            __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+              w2[h] = __floats2bfloat162_rn(split_plane(v[8 * u + 2 * h], pl), split_plane(v[8 * u + 2 * h + 1], pl));
+            *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) << 4)) = w;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (!X3) tma_store_2d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32);
+            else tma_store_3d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32, pl);
+            bulk_commit();
+          }
+        }
+      }
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+template <int BN, bool X3>
+__global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const __grid_constant__ PParams p) {
+  persistent_body<BN, X3, false>(p);
+}
+
+// fp32-as-planes forward / dgrad with each 128x128 tile shared by a CTA pair
+// (split K, exchange through distributed shared memory).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
+tc_gemm_pair_kernel(const __grid_constant__ PParams p) {
+  persistent_body<128, true, true>(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -1248,6 +1432,15 @@ size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int spl
 }
 
 namespace {
+const void* tcpair_kernel_ptr() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute((const void*)tc::tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         tc::PCfg<128, true>::SMEM_BYTES);
+  });
+  return (const void*)tc::tc_gemm_pair_kernel;
+}
+
 template <int BN, bool X3>
 const void* tcp_kernel_ptr() {
   static std::once_flag once;
@@ -1384,7 +1577,12 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   p.aux = (const __nv_bfloat16*)op.aux; p.ld_aux = op.ld_aux;
   p.err = op.err;
   LaunchRec& r = recs[0];
-  if (x3) {
+  // fp32 planes with few tiles: a CTA pair per tile, each half of K
+  const bool pair = x3 && 2 * p.num_tiles <= sms && p.num_kb >= 2;
+  if (pair) {
+    r.func = tcpair_kernel_ptr();
+    r.smem = tc::PCfg<128, true>::SMEM_BYTES;
+  } else if (x3) {
     r.func = tcp_kernel_ptr<128, true>();
     r.smem = tc::PCfg<128, true>::SMEM_BYTES;
   } else if (BN == 256) {
@@ -1394,7 +1592,7 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
     r.func = tcp_kernel_ptr<128, false>();
     r.smem = tc::PCfg<128>::SMEM_BYTES;
   }
-  r.grid = dim3((unsigned)(p.num_tiles < sms ? p.num_tiles : sms));
+  r.grid = dim3(pair ? (unsigned)(2 * p.num_tiles) : (unsigned)(p.num_tiles < sms ? p.num_tiles : sms));
   r.block = dim3(tc::P_THREADS);
   r.name = op.kind == GEMM_FWD ? "tc_gemm_fwd" : "tc_gemm_dgrad";
   r.set_args(p);
