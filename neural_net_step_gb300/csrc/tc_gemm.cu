@@ -1398,8 +1398,17 @@ int tc_wgrad_splits(int64_t M, int64_t N, int64_t K, int bk = tc::BK, int bn = t
 // single-buffered accumulator does not overlap; else 128-wide tiles.
 static void tc_wgrad_choice(int dtype, int64_t M, int64_t N, int64_t K, int* bn, int* splits) {
   if (dtype == DT_F32X3) {
+    // double-buffered accumulators hide most of the epilogue (cost 2); at
+    // least 4 stages per unit and at most 4 M floats of partial sums
+    const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, tc::W_BN);
+    const int64_t kbs = ceil_div(K, tc::WCfg<true>::BKW);
+    int64_t best_s = 1, best_cost = INT64_MAX;
+    for (int64_t s = 1; s <= 256 && (s == 1 || (kbs / s >= 4 && s * M * N <= ((int64_t)4 << 20))); s *= 2) {
+      const int64_t cost = ceil_div(tiles * s, kSMs) * (ceil_div(kbs, s) + 2);
+      if (cost < best_cost) { best_cost = cost; best_s = s; }
+    }
     *bn = tc::W_BN;
-    *splits = tc_wgrad_splits(M, N, K, tc::WCfg<true>::BKW);
+    *splits = (int)best_s;
     return;
   }
   if (N < 256) {
