@@ -497,8 +497,10 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
   char e_[512] = "";
   LaunchRec r;
   if (adamw_plan(ad, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_ARG, "%s", e_);
-  const int d[2] = {main_tail, side_tail};
-  r.depend_on(d, 2);
+  // the last weight gradient already follows the last dgrad (a single edge
+  // can be an early-launch one)
+  const int d[1] = {side_tail >= 0 ? side_tail : main_tail};
+  r.depend_on(d, 1);
   out.push_back(r);
   return MLP_OK;
 }
