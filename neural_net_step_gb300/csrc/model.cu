@@ -567,7 +567,7 @@ mlp_status launch_graph(mlp* m, int key, std::vector<LaunchRec>& recs, cudaStrea
       void* argp[1];
       cudaKernelNodeParams kp = node_params(r, argp);
       cudaGraphNode_t node;
-      if (nd == 1 && m->pdl) {
+      if (nd == 1 && m->pdl && r.early) {
         CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, nullptr, 0, &kp));
         CUDA_TRY(cudaGraphAddDependencies(gc->graph, dn, &node, &ed, 1));
       } else {

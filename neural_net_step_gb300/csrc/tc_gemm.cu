@@ -1548,6 +1548,7 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   const int sms = device_sms();
   r.grid = dim3((unsigned)(p.num_units < sms ? p.num_units : sms));
   r.block = dim3(tc::P_THREADS);
+  r.early = true;
   r.name = "tc_gemm_wgrad";
   r.set_args(p);
   if (op.splits_out) *op.splits_out = splits;
@@ -1603,6 +1604,7 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   }
   r.grid = dim3(pair ? (unsigned)(2 * p.num_tiles) : (unsigned)(p.num_tiles < sms ? p.num_tiles : sms));
   r.block = dim3(tc::P_THREADS);
+  r.early = true;
   r.name = op.kind == GEMM_FWD ? "tc_gemm_fwd" : "tc_gemm_dgrad";
   r.set_args(p);
   return 1;
