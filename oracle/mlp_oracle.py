@@ -161,6 +161,64 @@ def adamw(p, g, m, v, t: int, lr, beta1, beta2, eps, wd):
     return p, m, v
 
 
+def adam_l2(p, g, m, v, t: int, lr, beta1, beta2, eps, wd):
+    """One Adam update with L2 regularisation folded into the gradient
+    (noeira "Neural networks", section "What is in it", optimizers: Adam next
+    to AdamW; Orthon "Core capabilities", training stack: SGD and Adam).
+    Reading (the pages give no formula): the PyTorch Adam form, decay coupled
+    into the gradient, g' = g + wd p, then the AdamW moments and step without
+    the decoupled term, p <- p - lr m_hat / (sqrt(v_hat) + eps).  Returns new
+    (p, m, v)."""
+    g = g + wd * p
+    m = beta1 * m + (1.0 - beta1) * g
+    v = beta2 * v + (1.0 - beta2) * g * g
+    m_hat = m / (1.0 - beta1 ** t)
+    v_hat = v / (1.0 - beta2 ** t)
+    return p - lr * m_hat / (np.sqrt(v_hat) + eps), m, v
+
+
+def sgd(p, g, buf, lr, momentum, wd):
+    """One SGD update (MuNet "What runs today" lists SGD and its "Python
+    training" example steps `mu.optim.SGD(params, lr=0.03)`; noeira "What is in
+    it"; Orthon "Core capabilities").  Reading: the PyTorch SGD form with
+    heavy-ball momentum, no dampening and coupled L2: g' = g + wd p,
+    buf <- momentum buf + g' (buf zero before the first step), p <- p - lr buf.
+    momentum = 0 and wd = 0 give the plain p <- p - lr g of the example.
+    Returns (p, buf)."""
+    g = g + wd * p
+    buf = momentum * buf + g
+    return p - lr * buf, buf
+
+
+def clip_coef(grads, max_norm) -> float:
+    """Global gradient-norm clipping (MuNet "What runs today" and noeira "What
+    is in it" list gradient clipping; neither gives the rule).  Reading: the
+    PyTorch clip_grad_norm_ form, the factor min(1, max_norm / (||G||_2 +
+    1e-6)) applied to every gradient, ||G|| the 2-norm over every element of
+    every gradient; 1 when max_norm <= 0 (off)."""
+    if not max_norm or max_norm <= 0:
+        return 1.0
+    total = math.sqrt(sum(float(np.sum(np.asarray(g, np.float64) ** 2)) for g in grads))
+    return min(1.0, float(max_norm) / (total + 1e-6))
+
+
+OPTIMIZERS = ("adamw", "adam", "sgd")
+
+
+def update(optim: str, p, g, m, v, t: int, lr, beta1, beta2, eps, wd):
+    """The parameter update of the step: AdamW (default), Adam with L2, or
+    SGD whose momentum coefficient is beta1 (its buffer kept in m; v
+    unchanged)."""
+    if optim == "adamw":
+        return adamw(p, g, m, v, t, lr, beta1, beta2, eps, wd)
+    if optim == "adam":
+        return adam_l2(p, g, m, v, t, lr, beta1, beta2, eps, wd)
+    if optim == "sgd":
+        pn, buf = sgd(p, g, m, lr, beta1, wd)
+        return pn, buf, v
+    raise ValueError(f"unknown optimizer {optim}")
+
+
 # ---------------------------------------------------------------------------
 # Whole network.
 # ---------------------------------------------------------------------------
@@ -223,24 +281,28 @@ def backward(fw: Dict[str, list], dz: np.ndarray, acts: Sequence[int],
 def train_step(params: Sequence[np.ndarray], m: Sequence[np.ndarray],
                v: Sequence[np.ndarray], t: int, x: np.ndarray, y: np.ndarray,
                acts: Sequence[int], lr, beta1, beta2, eps, wd,
-               mode: str = "fp64"):
-    """One step: forward, CE loss (batch mean), backward, AdamW at step t.
+               mode: str = "fp64", optim: str = "adamw", max_norm: float = 0.0):
+    """One step: forward, CE loss (batch mean), backward, the update at step
+    t (AdamW by default) of the gradient scaled by the clipping factor.
 
-    Returns (loss, new_params, new_m, new_v, grads, extras)."""
+    Returns (loss, new_params, new_m, new_v, grads, extras); grads are the
+    unclipped gradients."""
     fw = forward(params, x, acts, mode)
     loss_rows, dz = softmax_ce(fw["z"], y)
     loss = float(loss_rows.mean())
     grads = backward(fw, dz, acts, mode)
+    c = clip_coef(grads, max_norm)
     newp, newm, newv = [], [], []
     for p_, g_, m_, v_ in zip(params, grads, m, v):
-        a, b, c = adamw(p_, g_, m_, v_, t, lr, beta1, beta2, eps, wd)
+        a, b, c_ = update(optim, p_, g_ * c, m_, v_, t, lr, beta1, beta2, eps, wd)
         newp.append(a)
         newm.append(b)
-        newv.append(c)
-    return loss, newp, newm, newv, grads, {"fw": fw, "loss_rows": loss_rows, "dz": dz}
+        newv.append(c_)
+    return loss, newp, newm, newv, grads, {"fw": fw, "loss_rows": loss_rows, "dz": dz, "clip": c}
 
 
-def run_steps(params, acts, batches, hyper, mode="fp64", t0: int = 0):
+def run_steps(params, acts, batches, hyper, mode="fp64", t0: int = 0, optim: str = "adamw",
+              max_norm: float = 0.0):
     """Run len(batches) consecutive steps from zero moments.  batches yields
     (x, y) pairs.  hyper = (lr, beta1, beta2, eps, wd).  Returns (losses,
     params, m, v, first_step_grads)."""
@@ -249,7 +311,8 @@ def run_steps(params, acts, batches, hyper, mode="fp64", t0: int = 0):
     v = [np.zeros_like(a) for a in p]
     losses, g1 = [], None
     for i, (x, y) in enumerate(batches):
-        loss, p, m, v, g, _ = train_step(p, m, v, t0 + i + 1, x, y, acts, *hyper, mode=mode)
+        loss, p, m, v, g, _ = train_step(p, m, v, t0 + i + 1, x, y, acts, *hyper, mode=mode, optim=optim,
+                                         max_norm=max_norm)
         losses.append(loss)
         if g1 is None:
             g1 = g

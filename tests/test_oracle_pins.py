@@ -260,6 +260,120 @@ def test_adamw_matches_torch_optim_adamw_100_steps():
 
 
 # --------------------------------------------------------------------------
+# Adam with L2, SGD with momentum, global-norm clipping: closed forms and the
+# torch.optim / torch.nn.utils routines of the same definitions (float64)
+# --------------------------------------------------------------------------
+def test_adam_l2_first_step_closed_form():
+    p0, g = _rand(1000, 91), _rand(1000, 92, 1e-3)
+    lr, b1, b2, eps, wd = 1e-3, 0.9, 0.999, 1e-8, 0.01
+    p1, m1, v1 = om.adam_l2(p0, g, 0 * p0, 0 * p0, 1, lr, b1, b2, eps, wd)
+    gp = g + wd * p0          # the decay enters the moments, not the step
+    assert np.allclose(p1, p0 - lr * gp / (np.abs(gp) + eps), rtol=0, atol=1e-15)
+    assert np.allclose(m1, 0.1 * gp, rtol=1e-15) and np.allclose(v1, 0.001 * gp * gp, rtol=1e-15)
+
+
+def test_adam_l2_matches_torch_optim_adam_100_steps():
+    rng = np.random.default_rng(93)
+    p0 = rng.standard_normal(500)
+    lr, b1, b2, eps, wd = 1e-3, 0.9, 0.999, 1e-8, 0.1
+    tp = torch.tensor(p0, requires_grad=True)
+    opt = torch.optim.Adam([tp], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd)
+    p, m, v = p0.copy(), np.zeros(500), np.zeros(500)
+    for t in range(1, 101):
+        g = rng.standard_normal(500) * 10 ** rng.uniform(-6, 0)
+        tp.grad = torch.tensor(g)
+        opt.step()
+        p, m, v = om.adam_l2(p, g, m, v, t, lr, b1, b2, eps, wd)
+    assert np.allclose(p, tp.detach().numpy(), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("momentum,wd", [(0.0, 0.0), (0.9, 0.0), (0.9, 0.01), (0.5, 0.1)])
+def test_sgd_matches_torch_optim_sgd_50_steps(momentum, wd):
+    rng = np.random.default_rng(94)
+    p0 = rng.standard_normal(300)
+    lr = 0.03
+    tp = torch.tensor(p0, requires_grad=True)
+    opt = torch.optim.SGD([tp], lr=lr, momentum=momentum, weight_decay=wd)
+    p, buf = p0.copy(), np.zeros(300)
+    for _ in range(50):
+        g = rng.standard_normal(300) * 10 ** rng.uniform(-3, 0)
+        tp.grad = torch.tensor(g)
+        opt.step()
+        p, buf = om.sgd(p, g, buf, lr, momentum, wd)
+    assert np.allclose(p, tp.detach().numpy(), rtol=0, atol=1e-13)
+
+
+def test_sgd_constant_gradient_closed_form():
+    # buf_t = g (1 - mu^t) / (1 - mu), so p_T = p_0 - lr g sum_t (1 - mu^t) / (1 - mu)
+    p0, g = _rand(64, 95), _rand(64, 96)
+    lr, mu, T = 0.01, 0.9, 7
+    p, buf = p0, 0 * p0
+    for _ in range(T):
+        p, buf = om.sgd(p, g, buf, lr, mu, 0.0)
+    s = sum((1 - mu ** t) / (1 - mu) for t in range(1, T + 1))
+    assert np.allclose(p, p0 - lr * g * s, rtol=0, atol=1e-14)
+    assert np.allclose(buf, g * (1 - mu ** T) / (1 - mu), rtol=1e-14)
+
+
+def test_clip_coef_closed_form():
+    grads = [np.array([[3.0, 0.0]]), np.array([4.0])]           # ||G|| = 5
+    assert om.clip_coef(grads, 1.0) == 1.0 / (5.0 + 1e-6)
+    assert om.clip_coef(grads, 2.5) == 2.5 / (5.0 + 1e-6)
+    assert om.clip_coef(grads, 10.0) == 1.0                        # below the threshold: unchanged
+    assert om.clip_coef(grads, 0.0) == 1.0                         # off
+    assert om.clip_coef([np.zeros(3)], 1.0) == 1.0                 # zero gradient: 1 / 1e-6 clamps to 1
+
+
+def test_clip_matches_torch_clip_grad_norm():
+    rng = np.random.default_rng(97)
+    shapes = [(7, 5), (7,), (3, 7), (3,)]
+    grads = [rng.standard_normal(s) * 0.3 for s in shapes]
+    for max_norm in (0.1, 1.0, 100.0):
+        ts = [torch.zeros(s, dtype=torch.float64, requires_grad=True) for s in shapes]
+        for t_, g in zip(ts, grads):
+            t_.grad = torch.tensor(g)
+        total = torch.nn.utils.clip_grad_norm_(ts, max_norm)
+        c = om.clip_coef(grads, max_norm)
+        assert abs(float(total) - math.sqrt(sum(float((g ** 2).sum()) for g in grads))) < 1e-14
+        for t_, g in zip(ts, grads):
+            assert np.allclose(t_.grad.numpy(), g * c, rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("optim", ["adamw", "adam", "sgd"])
+@pytest.mark.parametrize("max_norm", [0.0, 0.05])
+def test_whole_step_matches_torch_modules_and_optimizers(optim, max_norm):
+    """One whole step of the oracle against torch (float64): nn.Linear + ReLU
+    layers, F.cross_entropy (mean), backward, clip_grad_norm_, the optimizer."""
+    dims = [9, 7, 6, 5]
+    acts = (RELU, RELU)
+    B = 11
+    ps = _tiny_net(dims, 98)
+    x = _rand((B, dims[0]), 99)
+    y = np.random.default_rng(100).integers(0, dims[-1], B)
+    lr, b1, b2, eps, wd = 1e-2, 0.9, 0.999, 1e-8, 0.05
+    loss, newp, _, _, grads, ex = om.train_step(ps, [0 * p for p in ps], [0 * p for p in ps], 1, x, y, acts,
+                                                lr, b1, b2, eps, wd, optim=optim, max_norm=max_norm)
+    tps = [torch.tensor(p, requires_grad=True) for p in ps]
+    h = torch.tensor(x)
+    for l in range(3):
+        h = h @ tps[2 * l].T + tps[2 * l + 1]
+        if l < 2:
+            h = torch.relu(h)
+    tl = F.cross_entropy(h, torch.tensor(y))
+    tl.backward()
+    if max_norm:
+        torch.nn.utils.clip_grad_norm_(tps, max_norm)
+        assert ex["clip"] < 1.0            # the threshold is below this gradient's norm
+    opt = {"adamw": lambda: torch.optim.AdamW(tps, lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd),
+           "adam": lambda: torch.optim.Adam(tps, lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd),
+           "sgd": lambda: torch.optim.SGD(tps, lr=lr, momentum=b1, weight_decay=wd)}[optim]()
+    opt.step()
+    assert abs(loss - tl.item()) < 1e-13
+    for a, b in zip(newp, tps):
+        assert np.allclose(a, b.detach().numpy(), rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
 # Whole step: all-zero parameters have a closed form
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("mode", ["fp64", "bf16", "bf16_mirror"])
@@ -343,3 +457,36 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(om, "backward", backward_transposed)
     with pytest.raises((AssertionError, ValueError)):
         test_backward_matches_torch_autograd()
+    monkeypatch.setattr(om, "backward", orig_backward)
+
+    # (5) Adam with the decay decoupled (an AdamW step) -> the L2 pins fail
+    orig_adam = om.adam_l2
+    monkeypatch.setattr(om, "adam_l2", om.adamw)
+    with pytest.raises(AssertionError):
+        test_adam_l2_first_step_closed_form()
+    with pytest.raises(AssertionError):
+        test_adam_l2_matches_torch_optim_adam_100_steps()
+    monkeypatch.setattr(om, "adam_l2", orig_adam)
+
+    # (6) SGD with dampening (buf = mu buf + (1 - mu) g) -> closed form fails
+    orig_sgd = om.sgd
+
+    def sgd_damped(p, g, buf, lr, mu, wd):
+        g = g + wd * p
+        buf = mu * buf + (1 - mu) * g
+        return p - lr * buf, buf
+
+    monkeypatch.setattr(om, "sgd", sgd_damped)
+    with pytest.raises(AssertionError):
+        test_sgd_constant_gradient_closed_form()
+    monkeypatch.setattr(om, "sgd", orig_sgd)
+
+    # (7) clipping by the squared norm, or per tensor -> closed form / torch fail
+    orig_clip = om.clip_coef
+    monkeypatch.setattr(om, "clip_coef", lambda g, c: orig_clip(g, c) ** 2 if c else 1.0)
+    with pytest.raises(AssertionError):
+        test_clip_coef_closed_form()
+    monkeypatch.setattr(om, "clip_coef", lambda g, c: min(orig_clip([x], c) for x in g))
+    with pytest.raises(AssertionError):
+        test_clip_matches_torch_clip_grad_norm()
+    monkeypatch.setattr(om, "clip_coef", orig_clip)
