@@ -58,8 +58,9 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 # Algorithmic work of each kernel of the step (the order the library plans it)
 # ---------------------------------------------------------------------------
-def layer_work(w, kind, l):
-    """(flops, algorithmic bytes) of one kernel of the step."""
+def layer_work(w, kind, l, x3=False):
+    """(flops, algorithmic bytes) of one kernel of the step.  x3: the fp32
+    model keeps its weights as three bf16 planes, which the update writes."""
     B, es = w.batch, (4 if w.dtype == 0 else 2)
     d, L = w.dims, w.n_layers
     if kind in ("fwd", "wgrad", "dgrad"):
@@ -78,8 +79,13 @@ def layer_work(w, kind, l):
         return 0, 2 * es * B * C + 8 * B
     if kind == "loss_mean":
         return 0, 4 * B
-    if kind == "adamw":
-        return 0, w.n_params() * (28 + (2 if w.dtype == 1 else 0))
+    w16 = 2 if w.dtype == 1 else (6 if x3 else 0)   # bf16 weight copy (planes) written by the update
+    if kind in ("adamw", "adam_l2"):   # read p, g, m, v; write p, m, v
+        return 0, w.n_params() * (28 + w16)
+    if kind == "sgd":                  # read p, g, m; write p, m
+        return 0, w.n_params() * (20 + w16)
+    if kind == "grad_norm":            # read g
+        return 0, w.n_params() * 4
     if kind == "split3":   # fp32 input -> three bf16 planes (read 4 B, write 6 B per element)
         return 0, 10 * B * d[0]
     return 0, 0
@@ -103,6 +109,7 @@ def peak_source(peaks, top, w):
 def attach_work(w, prof):
     """Pair each profiled launch (in plan order) with its algorithmic work."""
     rows, fwd_l, bwd_l = [], 0, w.n_layers - 1
+    x3 = any(name == "split3" for name, _ in prof)
     for name, ms in prof:
         if name.endswith("_fwd"):
             kind, l = "fwd", fwd_l
@@ -121,11 +128,11 @@ def attach_work(w, prof):
             bwd_l -= 1
         elif name == "split_reduce":
             kind, l = "split_reduce", rows[-1]["layer"]
-        elif name.startswith("adamw"):
-            kind, l = "adamw", -1
+        elif name.endswith("_flat"):   # adamw_flat, adam_l2_flat, sgd_flat
+            kind, l = name[:-len("_flat")], -1
         else:
             kind, l = name, -1
-        fl, by = layer_work(w, kind, l)
+        fl, by = layer_work(w, kind, l, x3)
         rows.append({"kernel": name, "kind": kind, "layer": l, "ms": ms, "flops": fl, "bytes": by})
     return rows
 
@@ -246,7 +253,7 @@ def oracle_sample_rows(w, budget_s=1.0):
 class OracleRunner:
     """The CPU oracle, as it stands, stepping on a bounded row sample."""
 
-    def __init__(self, w):
+    def __init__(self, w, optim="adamw", max_norm=0.0):
         import numpy as np
         import synth
         from oracle import mlp_oracle as om
@@ -257,6 +264,7 @@ class OracleRunner:
         self.v = [np.zeros_like(p) for p in self.params]
         self.mode = "fp64" if w.dtype == 0 else "bf16_mirror"
         self.hyper = tuple(float(np.float32(a)) for a in (w.lr, w.beta1, w.beta2, w.eps, w.wd))
+        self.optim, self.max_norm = optim, float(np.float32(max_norm))
         self.batches = []
         for s in range(4):
             x, y = synth.make_batch(w, s)
@@ -268,7 +276,8 @@ class OracleRunner:
         x, y = self.batches[self.t % 4]
         t0 = time.perf_counter()
         _, self.params, self.m, self.v, _, _ = self.om.train_step(self.params, self.m, self.v, self.t + 1, x, y,
-                                                                  self.w.acts, *self.hyper, mode=self.mode)
+                                                                  self.w.acts, *self.hyper, mode=self.mode,
+                                                                  optim=self.optim, max_norm=self.max_norm)
         self.t += 1
         return time.perf_counter() - t0
 
@@ -277,8 +286,8 @@ class OracleRunner:
                 f"{self.w.name} workload; OpenBLAS threads = host cores")
 
 
-def time_oracle(w, target_s=10.0):
-    r = OracleRunner(w)
+def time_oracle(w, target_s=10.0, optim="adamw", max_norm=0.0):
+    r = OracleRunner(w, optim, max_norm)
     el, steps = 0.0, 0
     while el < target_s:
         el += r.step()
@@ -300,7 +309,7 @@ def dist_setup():
 def run_reference(args, w, world, rank):
     if rank != 0:
         return 0
-    r = OracleRunner(w)
+    r = OracleRunner(w, args.optim, args.max_grad_norm)
     for _ in range(args.warmup):
         r.step()
     t_all = sum(r.step() for _ in range(args.steps))
@@ -308,7 +317,7 @@ def run_reference(args, w, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "samples/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * t_all / args.steps, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(w),
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(w, None, args),
             "cpu_baseline": {"value": round(value, 2), "unit": "samples/s", "cores": os.cpu_count(),
                              "kind": "oracle", "sample": f"each step: one of {args.steps} " + r.sample()},
             "e2e": {"value": round(value, 2), "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -316,11 +325,19 @@ def run_reference(args, w, world, rank):
     return 0
 
 
-def config_of(w, extra=None):
+OPTIM_NAMES = {"adamw": "AdamW", "adam": "Adam (L2 in the gradient)", "sgd": "SGD (momentum = beta1, L2)"}
+
+
+def config_of(w, extra=None, args=None):
+    optim = args.optim if args else "adamw"
+    opt = (f"{OPTIM_NAMES[optim]} lr={w.lr} momentum={w.beta1} wd={w.wd}" if optim == "sgd" else
+           f"{OPTIM_NAMES[optim]} lr={w.lr} betas=({w.beta1},{w.beta2}) eps={w.eps} wd={w.wd}")
+    if args and args.max_grad_norm > 0:
+        opt += f", global grad-norm clipping at {args.max_grad_norm}"
     c = {"workload": f"{w.name}: MLP {'-'.join(map(str, w.dims))}, "
                      f"{'fp32' if w.dtype == 0 else 'bf16 + fp32 master'}, batch {w.batch}",
          "dims": list(w.dims), "acts": [["none", "relu", "gelu_tanh"][a] for a in w.acts], "global_batch": w.batch,
-         "optimizer": f"AdamW lr={w.lr} betas=({w.beta1},{w.beta2}) eps={w.eps} wd={w.wd}",
+         "optimizer": opt,
          "parallelism": "replicas"}
     if extra:
         c.update(extra)
@@ -338,6 +355,9 @@ def main():
     ap.add_argument("--kernels", action="store_true", help="include the per-kernel table")
     ap.add_argument("--f32-ffma", action="store_true",
                     help="fp32 models: GEMMs on the FFMA pipes instead of the tensor cores")
+    ap.add_argument("--optim", default="adamw", choices=["adamw", "adam", "sgd"],
+                    help="update rule (default AdamW)")
+    ap.add_argument("--max-grad-norm", type=float, default=0.0, help="> 0: global gradient-norm clipping")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -366,6 +386,8 @@ def main():
     model = nn.Model(w.dims, w.acts, nn.ACT_RELU, w.dtype, seed=w.seed + rank, batch=w.batch, device=local)
     if w.dtype == 0:
         model.set_option(nn.OPT_F32_TENSOR_CORES, 0 if args.f32_ffma else 1)
+    model.set_optimizer({"adamw": nn.OPTIM_ADAMW, "adam": nn.OPTIM_ADAM, "sgd": nn.OPTIM_SGD}[args.optim],
+                        args.max_grad_norm)
     gemm_mode = None if w.dtype != 0 else (
         "FFMA" if args.f32_ffma else "tensor cores, fp32 operands as three bf16 planes (6 products, fp32 accumulate)")
     hyper = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, wd=w.wd)
@@ -483,7 +505,7 @@ def main():
             "config": config_of(w, {"l2": f"fresh batch per step from a {n_pool}-batch device pool "
                                           f"({n_pool * per / 2**20:.0f} MiB > 129 MB L2)",
                                     "graph": "one CUDA-graph replay per step",
-                                    **({"f32_gemm": gemm_mode} if gemm_mode else {})}),
+                                    **({"f32_gemm": gemm_mode} if gemm_mode else {})}, args),
             "roofline": rf,
             "step_roofline": {"t_roof_ms": round(t_roof_ms, 5), "measured_ms": round(ms_per_step, 5),
                               "frac": round(t_roof_ms / ms_per_step, 4),
@@ -494,7 +516,7 @@ def main():
     if args.kernels:
         line["kernels"] = [{k: (round(v, 5) if isinstance(v, float) else v) for k, v in r.items()} for r in rows]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = time_oracle(w, target_s=10.0)
+        cb = time_oracle(w, target_s=10.0, optim=args.optim, max_norm=args.max_grad_norm)
         line["cpu_baseline"] = {k: (round(v, 2) if isinstance(v, float) else v) for k, v in cb.items()}
     if rank == 0:
         print(json.dumps(line))

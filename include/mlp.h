@@ -164,6 +164,31 @@ mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
 enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2, MLP_OPT_PDL = 3 };
 mlp_status mlp_set_option(mlp_t* model, int option, int64_t value);
 
+/* The update rule of the training step (default MLP_OPTIM_ADAMW) and global
+ * gradient-norm clipping (MuNet "What runs today": SGD, AdamW, gradient
+ * clipping; noeira "What is in it": SGD, Adam, AdamW, gradient clipping).
+ * The hyper-parameters of mlp_train_step* keep their places:
+ *   MLP_OPTIM_ADAMW  the AdamW step described at the top.
+ *   MLP_OPTIM_ADAM   Adam with the decay as L2 in the gradient: g' = g + wd p,
+ *                    the AdamW moments of g', p -= lr m_hat / (sqrt(v_hat) +
+ *                    eps).
+ *   MLP_OPTIM_SGD    SGD with heavy-ball momentum beta1 and L2 wd: buf =
+ *                    beta1 buf + (g + wd p), p -= lr buf (no dampening; buf
+ *                    is plane M, zero after create; beta2, eps and plane V
+ *                    are not used).
+ * max_grad_norm > 0 scales the whole gradient by min(1, max_grad_norm /
+ * (||g||_2 + 1e-6)) before the update, ||g|| over every gradient element;
+ * the G plane keeps the unscaled gradient and mlp_read_grad_norm returns
+ * ||g|| of the last step.  0 turns clipping off.  The moments are not reset:
+ * switching rules mid-run carries planes M and V over as they are.  Returns
+ * MLP_ERR_ARG for an unknown kind or a negative or non-finite threshold. */
+enum { MLP_OPTIM_ADAMW = 0, MLP_OPTIM_ADAM = 1, MLP_OPTIM_SGD = 2 };
+mlp_status mlp_set_optimizer(mlp_t* model, int kind, float max_grad_norm);
+
+/* ||g||_2 computed by the last training step that clipped (0 before any);
+ * synchronises the model's device. */
+mlp_status mlp_read_grad_norm(mlp_t* model, float* out);
+
 /* Number of parameters (flat, densely packed) and of Linear layers. */
 int64_t mlp_num_params(const mlp_t* model);
 int mlp_num_layers(const mlp_t* model);

@@ -112,6 +112,20 @@ mlp_status mlp_op_loss_mean(int64_t B, const float* loss_rows, float* loss, uint
 mlp_status mlp_op_adamw(int64_t n, float* p, const float* g, float* m, float* v, void* w16, int64_t t, float lr,
                         float beta1, float beta2, float eps, float wd, void* stream);
 
+/* One update of rule `kind` (MLP_OPTIM_ADAMW / _ADAM / _SGD of mlp.h, same
+ * formulas) over flat fp32 planes of n elements, with global-norm clipping
+ * when max_norm > 0: g is scaled by min(1, max_norm / (||g||_2 + 1e-6))
+ * before the update (g itself is not changed) and ||g|| goes to norm_dev
+ * (device float, nullable).  ws_dev (device, 16-byte aligned, at least
+ * MLP_OPTIM_WS_FLOATS floats) holds per-block partial sums of squares; it is
+ * needed only when clipping.  t >= 1 for the Adam rules (bias correction);
+ * SGD ignores t, beta2, eps and v.  w16 (nullable) receives bf16(p).
+ * Clipping launches two kernels (norm, then update), otherwise one. */
+enum { MLP_OPTIM_WS_FLOATS = 1216 };
+mlp_status mlp_op_optim(int kind, int64_t n, float* p, float* g, float* m, float* v, void* w16, int64_t t, float lr,
+                        float beta1, float beta2, float eps, float wd, float max_norm, float* ws_dev,
+                        float* norm_dev, void* stream);
+
 /* Row argmax of z [B, C] (ldz) into int32 out [B]; lowest index on ties. */
 mlp_status mlp_op_argmax(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, int32_t* out, void* stream);
 

@@ -22,6 +22,8 @@ ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
 F32, BF16 = 0, 1
 F32X3 = 2   # op-level GEMM operands: fp32 as three bf16 planes [3][rows][ld]
 PLANE_P, PLANE_G, PLANE_M, PLANE_V = 0, 1, 2, 3
+OPTIM_ADAMW, OPTIM_ADAM, OPTIM_SGD = 0, 1, 2
+OPTIM_WS_FLOATS = 1216   # op-level clipping workspace (floats)
 
 
 class MlpError(RuntimeError):
@@ -44,6 +46,8 @@ _SIGS = {
     "mlp_train_steps": (_I32, [_P, _I32, _c.POINTER(_P), _c.POINTER(_P), _F, _F, _F, _F, _F, _P, _P]),
     "mlp_set_graph_mode": (_I32, [_P, _I32]),
     "mlp_set_option": (_I32, [_P, _I32, _I64]),
+    "mlp_set_optimizer": (_I32, [_P, _I32, _F]),
+    "mlp_read_grad_norm": (_I32, [_P, _c.POINTER(_F)]),
     "mlp_num_params": (_I64, [_P]),
     "mlp_num_layers": (_I32, [_P]),
     "mlp_read_params": (_I32, [_P, _I32, _P, _SZ, _c.POINTER(_I64)]),
@@ -63,6 +67,7 @@ _SIGS = {
     "mlp_op_softmax_ce": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _F, _P, _I64, _P, _P, _P]),
     "mlp_op_loss_mean": (_I32, [_I64, _P, _P, _P, _P]),
     "mlp_op_adamw": (_I32, [_I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _P]),
+    "mlp_op_optim": (_I32, [_I32, _I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _F, _P, _P, _P]),
     "mlp_op_argmax": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _P]),
 }
 
@@ -144,6 +149,16 @@ def mlp_set_option(h, option: int, value: int) -> None:
     _check(lib().mlp_set_option(h, option, value))
 
 
+def mlp_set_optimizer(h, kind: int, max_grad_norm: float = 0.0) -> None:
+    _check(lib().mlp_set_optimizer(h, kind, max_grad_norm))
+
+
+def mlp_read_grad_norm(h) -> float:
+    out = _F(0.0)
+    _check(lib().mlp_read_grad_norm(h, ctypes.byref(out)))
+    return out.value
+
+
 def mlp_num_params(h) -> int:
     return lib().mlp_num_params(h)
 
@@ -223,6 +238,10 @@ def mlp_op_adamw(n, p, g, m, v, w16, t, lr, beta1, beta2, eps, wd, stream) -> No
     _check(lib().mlp_op_adamw(n, p, g, m, v, w16, t, lr, beta1, beta2, eps, wd, stream))
 
 
+def mlp_op_optim(kind, n, p, g, m, v, w16, t, lr, beta1, beta2, eps, wd, max_norm, ws, norm, stream) -> None:
+    _check(lib().mlp_op_optim(kind, n, p, g, m, v, w16, t, lr, beta1, beta2, eps, wd, max_norm, ws, norm, stream))
+
+
 def mlp_op_argmax(dtype, B, C, z, ldz, out, stream) -> None:
     _check(lib().mlp_op_argmax(dtype, B, C, z, ldz, out, stream))
 
@@ -258,6 +277,12 @@ class Model:
 
     def set_option(self, option: int, value: int) -> None:
         mlp_set_option(self.h, option, value)
+
+    def set_optimizer(self, kind: int, max_grad_norm: float = 0.0) -> None:
+        mlp_set_optimizer(self.h, kind, max_grad_norm)
+
+    def grad_norm(self) -> float:
+        return mlp_read_grad_norm(self.h)
 
     def _check_x(self, x, labels=None):
         t = self.torch

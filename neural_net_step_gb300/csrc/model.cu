@@ -91,6 +91,7 @@ struct Layout {
   std::vector<char> defer_l;
   size_t off_hws = 0, hws_bytes = 0;   // the fused output layer's partials (read by the optimizer)
   size_t off_xin[2] = {0, 0}, off_yin[2] = {0, 0};   // device inputs of mlp_train_step_host (two slots)
+  size_t off_norm = 0;   // per-block sums of squares of the gradient (clipping)
   size_t total = 0;
 };
 
@@ -99,6 +100,7 @@ struct Ctl {   // control block at off_ctl
   uint32_t err;
   float loss_slot;
   float bias_corr[2];     // AdamW 1/(1-b1^t), 1/sqrt(1-b2^t) of the current step
+  float grad_norm;        // ||g||_2 of the last step that clipped
 };
 
 mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act, int dtype, int64_t batch,
@@ -202,6 +204,7 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     L.off_xin[k] = take(batch * dims[0] * (dtype == MLP_F32 ? 4 : 2));
     L.off_yin[k] = take(batch * 4);
   }
+  L.off_norm = take(AdamWOp::kNormParts * sizeof(float));
   L.off_ctl = take(sizeof(Ctl));
   L.total = cur;
   return MLP_OK;
@@ -249,6 +252,8 @@ struct mlp {
   bool fuse_head = true;     // fused output layer + CE where the shape allows
   bool f32_tc = true;        // fp32 GEMMs on the tensor cores (three bf16 planes) where the model allows
   bool pdl = true;           // graph edges let each kernel launch before its predecessor ends
+  int optim = MLP_OPTIM_ADAMW;
+  float max_grad_norm = 0.f; // > 0: global-norm clipping of the gradient before the update
   std::mutex mu;
   std::vector<GraphCache> graphs;
   int kernels_per_step = 0;
@@ -482,6 +487,10 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
   ad.step_counter = &ctl->step;
   ad.bias_corr = ctl->bias_corr;
   ad.lr = hp.lr; ad.beta1 = hp.b1; ad.beta2 = hp.b2; ad.eps = hp.eps; ad.wd = hp.wd;
+  ad.kind = m->optim;
+  ad.max_norm = m->max_grad_norm;
+  ad.norm_ws = (float*)m->at(L.off_norm);
+  ad.norm_out = &ctl->grad_norm;
   for (int k = 0; k < nseg; ++k) ad.seg[ad.nseg++] = seg[k];
   if (fuse) {   // the output layer's gradient and the loss arrive as partial sums
     const int l = L.L - 1;
@@ -495,13 +504,14 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     ad.err = &ctl->err;
   }
   char e_[512] = "";
-  LaunchRec r;
-  if (adamw_plan(ad, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_ARG, "%s", e_);
+  LaunchRec r[2];
+  const int nr = adamw_plan(ad, r, e_, sizeof(e_));
+  if (nr < 0) return fail(MLP_ERR_ARG, "%s", e_);
   // the last weight gradient already follows the last dgrad (a single edge
-  // can be an early-launch one)
+  // can be an early-launch one); with clipping the update follows the norm
   const int d[1] = {side_tail >= 0 ? side_tail : main_tail};
-  r.depend_on(d, 1);
-  out.push_back(r);
+  r[0].depend_on(d, 1);
+  add(out, nr, r);
   return MLP_OK;
 }
 
@@ -691,6 +701,31 @@ void mlp_destroy(mlp_t* m) {
 int64_t mlp_num_params(const mlp_t* m) { return m ? m->lay.n_params : -1; }
 int mlp_num_layers(const mlp_t* m) { return m ? m->lay.L : -1; }
 int mlp_kernels_per_step(const mlp_t* m) { return m ? m->kernels_per_step : -1; }
+
+mlp_status mlp_set_optimizer(mlp_t* m, int kind, float max_grad_norm) {
+  if (!m) return fail(MLP_ERR_ARG, "model is NULL");
+  if (kind < MLP_OPTIM_ADAMW || kind > MLP_OPTIM_SGD) return fail(MLP_ERR_ARG, "unknown optimizer %d", kind);
+  if (!(max_grad_norm >= 0.f) || !(max_grad_norm < INFINITY))
+    return fail(MLP_ERR_ARG, "max_grad_norm must be finite and >= 0");
+  std::lock_guard<std::mutex> lk(m->mu);
+  m->optim = kind;
+  m->max_grad_norm = max_grad_norm;
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_step(m, m->arena, (const int32_t*)m->arena, Hyper{1e-3f, 0.9f, 0.999f, 1e-8f, 0.f},
+                            nullptr, recs);
+  if (st != MLP_OK) return st;
+  m->kernels_per_step = (int)recs.size();
+  return ok();
+}
+
+mlp_status mlp_read_grad_norm(mlp_t* m, float* out) {
+  if (!m || !out) return fail(MLP_ERR_ARG, "model or out is NULL");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  CUDA_TRY(cudaDeviceSynchronize());
+  CUDA_TRY(cudaMemcpy(out, &m->ctl()->grad_norm, sizeof(float), cudaMemcpyDeviceToHost));
+  return ok();
+}
 
 mlp_status mlp_set_graph_mode(mlp_t* m, int enable) {
   if (!m) return fail(MLP_ERR_ARG, "model is NULL");
@@ -1057,10 +1092,32 @@ mlp_status mlp_op_adamw(int64_t n, float* p, const float* g, float* m, float* v,
   AdamWOp op;
   op.n = n; op.p = p; op.g = const_cast<float*>(g); op.m = m; op.v = v; op.w16 = w16; op.t = t;
   op.lr = lr; op.beta1 = beta1; op.beta2 = beta2; op.eps = eps; op.wd = wd;
-  LaunchRec r;
+  LaunchRec r[2];
   char e_[512] = "";
-  if (adamw_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_ARG, "%s", e_);
-  return run_ops(&r, 1, stream);
+  const int nr = adamw_plan(op, r, e_, sizeof(e_));
+  if (nr < 0) return fail(MLP_ERR_ARG, "%s", e_);
+  return run_ops(r, nr, stream);
+}
+
+static_assert(AdamWOp::kNormParts == MLP_OPTIM_WS_FLOATS, "norm workspace size of the C ABI");
+
+mlp_status mlp_op_optim(int kind, int64_t n, float* p, float* g, float* m, float* v, void* w16, int64_t t, float lr,
+                        float beta1, float beta2, float eps, float wd, float max_norm, float* ws_dev,
+                        float* norm_dev, void* stream) {
+  if (!p || !g || !m || !v) return fail(MLP_ERR_ARG, "null pointer");
+  if (kind < MLP_OPTIM_ADAMW || kind > MLP_OPTIM_SGD) return fail(MLP_ERR_ARG, "unknown optimizer %d", kind);
+  if (kind != MLP_OPTIM_SGD && t < 1) return fail(MLP_ERR_ARG, "t must be >= 1");
+  if (max_norm > 0 && !ws_dev) return fail(MLP_ERR_ARG, "clipping needs ws_dev");
+  AdamWOp op;
+  op.kind = kind;
+  op.n = n; op.p = p; op.g = g; op.m = m; op.v = v; op.w16 = w16; op.t = kind == MLP_OPTIM_SGD ? 1 : t;
+  op.lr = lr; op.beta1 = beta1; op.beta2 = beta2; op.eps = eps; op.wd = wd;
+  op.max_norm = max_norm; op.norm_ws = ws_dev; op.norm_out = norm_dev;
+  LaunchRec r[2];
+  char e_[512] = "";
+  const int nr = adamw_plan(op, r, e_, sizeof(e_));
+  if (nr < 0) return fail(MLP_ERR_ARG, "%s", e_);
+  return run_ops(r, nr, stream);
 }
 
 mlp_status mlp_op_argmax(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, int32_t* out, void* stream) {

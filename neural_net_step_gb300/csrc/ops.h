@@ -110,7 +110,20 @@ struct AdamWOp {
   // a non-finite loss sets the error bit in err).
   const float* loss_parts = nullptr; int loss_n = 0; float loss_scale = 1.f;
   float* loss = nullptr; uint32_t* err = nullptr;
+  // The update rule (OPTIM_*): AdamW; Adam with the decay as L2 added to the
+  // gradient; SGD with momentum beta1 (buffer in m, v untouched), L2 wd.
+  int kind = 0;
+  // Global-norm clipping when max_norm > 0: a first kernel adds the segments,
+  // writes g and leaves one partial sum of squares per block in norm_ws
+  // (kNormParts floats); the update scales g by min(1, max_norm / (||g|| +
+  // 1e-6)) and block 0 writes ||g|| to norm_out (nullable).
+  float max_norm = 0.f;
+  float* norm_ws = nullptr;
+  float* norm_out = nullptr;
+  static constexpr int kNormParts = 152 * 8;
 };
+enum { OPTIM_ADAMW = 0, OPTIM_ADAM = 1, OPTIM_SGD = 2 };
+// One or two records (clipping: norm, then update) into rec[0..1].
 int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen);
 
 // Row argmax, lowest index among equal maxima.

@@ -322,9 +322,16 @@ int loss_mean_plan(const LossMeanOp& op, LaunchRec* rec, char* err, size_t errle
 }
 
 // ---------------------------------------------------------------------------
-// AdamW over flat planes.  PyTorch / Loshchilov-Hutter form:
-//   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
-//   p = p - lr * (m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps) + wd * p_old).
+// Optimizer update over flat planes (p, g, m, v at one index).
+//   AdamW (PyTorch / Loshchilov-Hutter form):
+//     m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+//     p = p - lr * (m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps) + wd * p_old).
+//   Adam, decay as L2: g' = g + wd p, then the same moments and
+//     p = p - lr * m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps).
+//   SGD, momentum b1, L2 wd: buf = b1 buf + (g + wd p) (buf in m, zero
+//     before the first step), p = p - lr buf.
+// With global-norm clipping every g above is c g, c = min(1, max_norm /
+// (||g||_2 + 1e-6)) over the whole flat gradient.
 // ---------------------------------------------------------------------------
 struct AdamWParams {
   float* p; float* g; float* m; float* v;
@@ -338,6 +345,9 @@ struct AdamWParams {
   int nseg;
   // batch loss = sum(loss_parts) * loss_scale, by one warp (nullable)
   const float* loss_parts; int loss_n; float loss_scale; float* loss; uint32_t* err;
+  // clipping: per-block sums of squares (written by the norm kernel, read by
+  // the update), their count, the threshold and the norm's destination
+  float* norm_ws; int norm_n; float max_norm; float* norm_out;
 };
 
 // The gradient element g[f]: from its segment's partial sums, else the plane.
@@ -355,13 +365,70 @@ __device__ __forceinline__ float grad_elem(const AdamWParams& q, int64_t f, bool
   return q.g[f];
 }
 
-__device__ __forceinline__ void adamw_one(float& p, float g, float& m, float& v, float lr, float b1,
-                                          float b2, float eps, float wd, float inv_bc1, float inv_sqrt_bc2) {
-  m = b1 * m + (1.f - b1) * g;
-  v = b2 * v + (1.f - b2) * g * g;
-  float mhat = m * inv_bc1;
-  float denom = sqrtf(v) * inv_sqrt_bc2 + eps;
-  p = p - lr * (mhat / denom + wd * p);
+// Gradient elements 4i .. 4i+3: from the plane, or summed from their
+// segment's partials (16-byte loads, up to 16 in flight, added in partial
+// order) and then written to the plane.  Lanes past the segment keep the
+// plane's own value (padding).
+__device__ __forceinline__ float4 load_grad4(const AdamWParams& q, int64_t i) {
+  const int64_t f = 4 * i;
+  int si = -1;
+  for (int k = 0; k < q.nseg; ++k)
+    if (f >= q.seg[k].off && f < q.seg[k].off + q.seg[k].len) si = k;
+  if (si < 0) return reinterpret_cast<const float4*>(q.g)[i];
+  const AdamWOp::Seg& sg = q.seg[si];
+  const float* src = sg.parts + (f - sg.off);
+  float4 part[16];
+#pragma unroll
+  for (int b = 0; b < 16; ++b)
+    part[b] = b < sg.n ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)b * sg.stride))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 g = part[0];
+#pragma unroll
+  for (int b = 1; b < 16; ++b) {
+    g.x += part[b].x; g.y += part[b].y; g.z += part[b].z; g.w += part[b].w;
+  }
+  for (int b0 = 16; b0 < sg.n; b0 += 16) {
+#pragma unroll
+    for (int b = 0; b < 16; ++b)
+      part[b] = b0 + b < sg.n ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)(b0 + b) * sg.stride))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      g.x += part[b].x; g.y += part[b].y; g.z += part[b].z; g.w += part[b].w;
+    }
+  }
+  const int64_t end = sg.off + sg.len;
+  if (f + 4 > end) {
+    const float4 own = reinterpret_cast<const float4*>(q.g)[i];
+    if (f + 1 >= end) g.y = own.y;
+    if (f + 2 >= end) g.z = own.z;
+    if (f + 3 >= end) g.w = own.w;
+  }
+  reinterpret_cast<float4*>(q.g)[i] = g;   // the gradient plane holds the summed gradient
+  return g;
+}
+
+template <int KIND>
+__device__ __forceinline__ void update_one(float& p, float g, float& m, float& v, const AdamWParams& q,
+                                           float inv_bc1, float inv_sqrt_bc2) {
+  if (KIND == OPTIM_ADAMW) {
+    m = q.beta1 * m + (1.f - q.beta1) * g;
+    v = q.beta2 * v + (1.f - q.beta2) * g * g;
+    const float mhat = m * inv_bc1;
+    const float denom = sqrtf(v) * inv_sqrt_bc2 + q.eps;
+    p = p - q.lr * (mhat / denom + q.wd * p);
+  } else if (KIND == OPTIM_ADAM) {
+    g = g + q.wd * p;
+    m = q.beta1 * m + (1.f - q.beta1) * g;
+    v = q.beta2 * v + (1.f - q.beta2) * g * g;
+    const float mhat = m * inv_bc1;
+    const float denom = sqrtf(v) * inv_sqrt_bc2 + q.eps;
+    p = p - q.lr * (mhat / denom);
+  } else {
+    g = g + q.wd * p;
+    m = q.beta1 * m + g;
+    p = p - q.lr * m;
+  }
 }
 
 // bf16 planes of x: hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid)
@@ -384,74 +451,81 @@ __device__ __forceinline__ void store_planes4(__nv_bfloat16* dst, int64_t plane,
   *reinterpret_cast<uint2*>(dst + 2 * plane) = *reinterpret_cast<const uint2*>(l);
 }
 
+// Sum over a 256-thread block in a fixed order (warp trees, then a tree over
+// the eight warp sums); every thread gets the result.
+__device__ __forceinline__ float block_sum256(float a, float* red) {
+  a = warp_sum(a);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  float b = (threadIdx.x & 31) < 8 ? red[threadIdx.x & 31] : 0.f;
+  b = warp_sum(b);
+  __syncthreads();   // red may be reused after this
+  return b;
+}
+
+// Clipping, first pass: finish the gradient (segments added and written to
+// g) and leave this block's sum of squares in norm_ws[blockIdx.x].
+__global__ void __launch_bounds__(256) grad_norm_kernel(const __grid_constant__ AdamWParams q) {
+  __shared__ float red[8];
+  pdl_enter();
+  const int64_t n4 = q.n / 4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  float a = 0.f;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 g = load_grad4(q, i);
+    a += g.x * g.x + g.y * g.y + g.z * g.z + g.w * g.w;
+  }
+  for (int64_t i = n4 * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < q.n; i += stride) {
+    bool fp = false;
+    const float g = q.nseg ? grad_elem(q, i, fp) : q.g[i];
+    if (fp) q.g[i] = g;
+    a += g * g;
+  }
+  a = block_sum256(a, red);
+  if (threadIdx.x == 0) q.norm_ws[blockIdx.x] = a;
+}
+
+template <int KIND, bool CLIP>
 __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamWParams q) {
   pdl_enter();
   // bias corrections: precomputed for the step (read by every thread, in
   // flight with its first parameter loads), else computed here
-  float inv_bc1, inv_sqrt_bc2;
-  if (q.bias_corr) {
-    inv_bc1 = __ldg(q.bias_corr);
-    inv_sqrt_bc2 = __ldg(q.bias_corr + 1);
-  } else {
-    const int64_t t = q.t > 0 ? q.t : *q.step_counter;
-    inv_bc1 = 1.0f / one_minus_pow(q.beta1, t);
-    inv_sqrt_bc2 = 1.0f / sqrtf(one_minus_pow(q.beta2, t));
+  float inv_bc1 = 1.f, inv_sqrt_bc2 = 1.f;
+  if (KIND != OPTIM_SGD) {
+    if (q.bias_corr) {
+      inv_bc1 = __ldg(q.bias_corr);
+      inv_sqrt_bc2 = __ldg(q.bias_corr + 1);
+    } else {
+      const int64_t t = q.t > 0 ? q.t : *q.step_counter;
+      inv_bc1 = 1.0f / one_minus_pow(q.beta1, t);
+      inv_sqrt_bc2 = 1.0f / sqrtf(one_minus_pow(q.beta2, t));
+    }
+  }
+  float clip = 1.f;
+  if (CLIP) {
+    // every block adds the same partials in the same order: the same factor
+    __shared__ float red[8];
+    float a = 0.f;
+    for (int c = threadIdx.x; c < q.norm_n; c += blockDim.x) a += __ldcg(q.norm_ws + c);
+    const float norm = sqrtf(block_sum256(a, red));
+    clip = fminf(1.f, q.max_norm / (norm + 1e-6f));
+    if (blockIdx.x == 0 && threadIdx.x == 0 && q.norm_out) *q.norm_out = norm;
   }
   const int64_t n4 = q.n / 4;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
     float4 p = reinterpret_cast<float4*>(q.p)[i];
-    float4 g;
-    const int64_t f = 4 * i;
-    int si = -1;
-    for (int k = 0; k < q.nseg; ++k)
-      if (f >= q.seg[k].off && f < q.seg[k].off + q.seg[k].len) si = k;
-    if (si >= 0) {
-      // four gradient elements from the segment's partial sums: 16-byte
-      // loads, up to 16 in flight; lanes past the segment keep the plane's
-      // own value (padding)
-      const AdamWOp::Seg& sg = q.seg[si];
-      const float* src = sg.parts + (f - sg.off);
-      float4 part[16];
-#pragma unroll
-      for (int b = 0; b < 16; ++b)
-        part[b] = b < sg.n ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)b * sg.stride))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-      g = part[0];
-#pragma unroll
-      for (int b = 1; b < 16; ++b) {
-        g.x += part[b].x; g.y += part[b].y; g.z += part[b].z; g.w += part[b].w;
-      }
-      for (int b0 = 16; b0 < sg.n; b0 += 16) {
-#pragma unroll
-        for (int b = 0; b < 16; ++b)
-          part[b] = b0 + b < sg.n ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)(b0 + b) * sg.stride))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int b = 0; b < 16; ++b) {
-          g.x += part[b].x; g.y += part[b].y; g.z += part[b].z; g.w += part[b].w;
-        }
-      }
-      const int64_t end = sg.off + sg.len;
-      if (f + 4 > end) {
-        const float4 own = reinterpret_cast<const float4*>(q.g)[i];
-        if (f + 1 >= end) g.y = own.y;
-        if (f + 2 >= end) g.z = own.z;
-        if (f + 3 >= end) g.w = own.w;
-      }
-      reinterpret_cast<float4*>(q.g)[i] = g;   // the gradient plane holds the summed gradient
-    } else {
-      g = reinterpret_cast<const float4*>(q.g)[i];
-    }
+    float4 g = load_grad4(q, i);
+    if (CLIP) { g.x *= clip; g.y *= clip; g.z *= clip; g.w *= clip; }
     float4 m = reinterpret_cast<float4*>(q.m)[i];
-    float4 v = reinterpret_cast<float4*>(q.v)[i];
-    adamw_one(p.x, g.x, m.x, v.x, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
-    adamw_one(p.y, g.y, m.y, v.y, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
-    adamw_one(p.z, g.z, m.z, v.z, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
-    adamw_one(p.w, g.w, m.w, v.w, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
+    float4 v = KIND == OPTIM_SGD ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<float4*>(q.v)[i];
+    update_one<KIND>(p.x, g.x, m.x, v.x, q, inv_bc1, inv_sqrt_bc2);
+    update_one<KIND>(p.y, g.y, m.y, v.y, q, inv_bc1, inv_sqrt_bc2);
+    update_one<KIND>(p.z, g.z, m.z, v.z, q, inv_bc1, inv_sqrt_bc2);
+    update_one<KIND>(p.w, g.w, m.w, v.w, q, inv_bc1, inv_sqrt_bc2);
     reinterpret_cast<float4*>(q.p)[i] = p;
     reinterpret_cast<float4*>(q.m)[i] = m;
-    reinterpret_cast<float4*>(q.v)[i] = v;
+    if (KIND != OPTIM_SGD) reinterpret_cast<float4*>(q.v)[i] = v;
     if (q.w16 && q.w16_plane > 0) {
       store_planes4(q.w16 + 4 * i, q.w16_plane, p);
     } else if (q.w16) {
@@ -465,12 +539,14 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
   }
   // tail (n not a multiple of 4)
   for (int64_t i = n4 * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < q.n; i += stride) {
-    float p = q.p[i], m = q.m[i], v = q.v[i];
+    float p = q.p[i], m = q.m[i], v = KIND == OPTIM_SGD ? 0.f : q.v[i];
     bool fp = false;
-    const float g = q.nseg ? grad_elem(q, i, fp) : q.g[i];
+    float g = q.nseg ? grad_elem(q, i, fp) : q.g[i];
     if (fp) q.g[i] = g;
-    adamw_one(p, g, m, v, q.lr, q.beta1, q.beta2, q.eps, q.wd, inv_bc1, inv_sqrt_bc2);
-    q.p[i] = p; q.m[i] = m; q.v[i] = v;
+    if (CLIP) g *= clip;
+    update_one<KIND>(p, g, m, v, q, inv_bc1, inv_sqrt_bc2);
+    q.p[i] = p; q.m[i] = m;
+    if (KIND != OPTIM_SGD) q.v[i] = v;
     if (q.w16 && q.w16_plane > 0) split3(p, q.w16[i], q.w16[i + q.w16_plane], q.w16[i + 2 * q.w16_plane]);
     else if (q.w16) q.w16[i] = __float2bfloat16_rn(p);
   }
@@ -487,9 +563,17 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
   }
 }
 
+template <bool CLIP>
+const void* update_kernel(int kind) {
+  return kind == OPTIM_ADAM ? (const void*)adamw_kernel<OPTIM_ADAM, CLIP>
+         : kind == OPTIM_SGD ? (const void*)adamw_kernel<OPTIM_SGD, CLIP>
+                             : (const void*)adamw_kernel<OPTIM_ADAMW, CLIP>;
+}
+
 int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
   if (op.n < 0) { snprintf(err, errlen, "adamw: negative size"); return -1; }
-  if (op.t <= 0 && !op.step_counter) { snprintf(err, errlen, "adamw: no step"); return -1; }
+  if (op.kind < OPTIM_ADAMW || op.kind > OPTIM_SGD) { snprintf(err, errlen, "adamw: unknown optimizer"); return -1; }
+  if (op.kind != OPTIM_SGD && op.t <= 0 && !op.step_counter) { snprintf(err, errlen, "adamw: no step"); return -1; }
   auto al = [](const void* ptr, int a) { return ((uintptr_t)ptr % a) == 0; };
   if (!al(op.p, 16) || !al(op.g, 16) || !al(op.m, 16) || !al(op.v, 16) || (op.w16 && !al(op.w16, 8)) ||
       op.w16_plane % 4 || (op.w16_plane > 0 && op.w16_plane < op.n)) {
@@ -508,6 +592,12 @@ int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
       return -1;
     }
   }
+  const bool clip = op.max_norm > 0.f;
+  if (clip && !op.norm_ws) { snprintf(err, errlen, "adamw: clipping needs a norm workspace"); return -1; }
+  if (!(op.max_norm >= 0.f) || !(op.max_norm < INFINITY)) {
+    snprintf(err, errlen, "adamw: max_norm must be finite and >= 0");
+    return -1;
+  }
   AdamWParams q{};
   q.p = op.p; q.g = op.g; q.m = op.m; q.v = op.v;
   q.w16 = (__nv_bfloat16*)op.w16; q.w16_plane = op.w16_plane;
@@ -516,16 +606,33 @@ int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
   for (int k = 0; k < op.nseg; ++k) q.seg[k] = op.seg[k];
   q.nseg = op.nseg;
   q.loss_parts = op.loss_parts; q.loss_n = op.loss_n; q.loss_scale = op.loss_scale; q.loss = op.loss; q.err = op.err;
-  rec->func = (const void*)adamw_kernel;
   int64_t blocks = ceil_div(op.n / 4 + 1, 256);
-  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks > AdamWOp::kNormParts) blocks = AdamWOp::kNormParts;
   if (blocks < 1) blocks = 1;
-  rec->grid = dim3((unsigned)blocks);
-  rec->block = dim3(256);
-  rec->smem = 0;
-  rec->name = "adamw_flat";
-  rec->set_args(q);
-  return 1;
+  int nrec = 0;
+  if (clip) {
+    // first pass: the finished gradient and its per-block sums of squares
+    AdamWParams qn = q;
+    qn.loss_parts = nullptr;
+    qn.norm_ws = op.norm_ws;
+    LaunchRec& r = rec[nrec++];
+    r.func = (const void*)grad_norm_kernel;
+    r.grid = dim3((unsigned)blocks);
+    r.block = dim3(256);
+    r.smem = 0;
+    r.name = "grad_norm";
+    r.set_args(qn);
+    q.nseg = 0;   // the update reads the gradient the first pass wrote
+    q.norm_ws = op.norm_ws; q.norm_n = (int)blocks; q.max_norm = op.max_norm; q.norm_out = op.norm_out;
+  }
+  LaunchRec& r = rec[nrec++];
+  r.func = clip ? update_kernel<true>(op.kind) : update_kernel<false>(op.kind);
+  r.grid = dim3((unsigned)blocks);
+  r.block = dim3(256);
+  r.smem = 0;
+  r.name = op.kind == OPTIM_ADAM ? "adam_l2_flat" : op.kind == OPTIM_SGD ? "sgd_flat" : "adamw_flat";
+  r.set_args(q);
+  return nrec;
 }
 
 // ---------------------------------------------------------------------------

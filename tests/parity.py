@@ -107,7 +107,7 @@ def perturbed_products(seed: int):
     input_grad, bias_grad) is multiplied elementwise by (1 + eta r),
     r ~ U(-1, 1), eta = sqrt(K) 2^-24 for a reduction over K terms."""
     rng = np.random.default_rng(seed)
-    orig = (om.linear, om.weight_grad, om.input_grad, om.bias_grad, om.softmax_ce, om.adamw)
+    orig = (om.linear, om.weight_grad, om.input_grad, om.bias_grad, om.softmax_ce, om.update, om.clip_coef)
 
     def rel(a, e):
         return a * (1.0 + e * rng.uniform(-1.0, 1.0, np.shape(a)))
@@ -117,13 +117,19 @@ def perturbed_products(seed: int):
         lr_, dz_ = orig[4](z, y)
         return rel(lr_, 2.0 ** -22), rel(dz_, 2.0 ** -22)
 
-    def adamw(p, g, m, v, t, *hyper):
+    def update(optim, p, g, m, v, t, *hyper):
         # fp32 arithmetic and fp32 storage of p, m, v after every step
-        p2, m2, v2 = orig[5](p, g, m, v, t, *hyper)
+        p2, m2, v2 = orig[5](optim, p, g, m, v, t, *hyper)
         return rel(p2, 2.0 ** -23), rel(m2, 2.0 ** -22), rel(v2, 2.0 ** -22)
 
+    def clip_coef(grads, max_norm):
+        # an fp32 sum of squares over every gradient element
+        c = orig[6](grads, max_norm)
+        return c if c == 1.0 else rel(c, 2.0 ** -20)
+
     om.softmax_ce = ce
-    om.adamw = adamw
+    om.update = update
+    om.clip_coef = clip_coef
 
     def noisy(a, absum, K):
         # fp32 accumulation error scales with the sum of |terms|, not with
@@ -138,18 +144,20 @@ def perturbed_products(seed: int):
     try:
         yield
     finally:
-        om.linear, om.weight_grad, om.input_grad, om.bias_grad, om.softmax_ce, om.adamw = orig
+        om.linear, om.weight_grad, om.input_grad, om.bias_grad, om.softmax_ce, om.update, om.clip_coef = orig
 
 
-def oracle_run(w: synth.Workload, params0, bl, mode: str, perturb_seed: int = 0):
+def oracle_run(w: synth.Workload, params0, bl, mode: str, perturb_seed: int = 0, optim: str = "adamw",
+               max_norm: float = 0.0):
     """(losses, params, m, v, first-step grads) of len(bl) steps from params0."""
     hyper = hyper32(w)
     xs = [(to64(x), y.numpy().astype(np.int64)) for x, y in bl]
     p0 = [to64(p) for p in params0]
+    kw = dict(mode=mode, optim=optim, max_norm=float(np.float32(max_norm)))
     if perturb_seed:
         with perturbed_products(perturb_seed):
-            return om.run_steps(p0, w.acts, xs, hyper, mode=mode)
-    return om.run_steps(p0, w.acts, xs, hyper, mode=mode)
+            return om.run_steps(p0, w.acts, xs, hyper, **kw)
+    return om.run_steps(p0, w.acts, xs, hyper, **kw)
 
 
 def oracle_abs_sums(w: synth.Workload, params0, x, y, mode: str) -> List[np.ndarray]:
