@@ -18,11 +18,16 @@ What it computes, with the passage each step follows:
   devpost "Orthon", sections "Core capabilities" and "Selected Orthon vs.
   PyTorch results"; integer labels are the one-hot rows of noeira "A complete
   example").
+* Mean squared error against real targets, mean over all elements (MuNet
+  "Python training": mse_loss in the example step; "Training swarm").
 * Backward as the composition of per-layer vector-Jacobian products, no tape
   (noeira "The design in one page": "Forward and backward are explicit").
 * AdamW with decoupled weight decay and moments m, v kept per parameter,
   zero before the first step (MuNet "What runs today": AdamW; noeira "The
   design in one page": a Param is four tensors, moments allocated lazily).
+* Adam with L2 in the gradient, SGD with momentum, and global gradient-norm
+  clipping (MuNet "What runs today"; noeira "What is in it"; Orthon "Core
+  capabilities"), each in its PyTorch form.
 * Mixed precision: matmul inputs rounded to nearest (even), fp32-or-better
   accumulation, fp32 master weights (MuNet "Configuration", precision="mixed";
   Orthon "Core capabilities", Mixed precision).  Here the low-precision type
@@ -140,6 +145,20 @@ def softmax_ce(z: np.ndarray, y: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     dz = p.copy()
     dz[rows, y] -= 1.0
     return loss_rows, dz / B
+
+
+def mse(z: np.ndarray, t: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Mean squared error against real targets t [B, C] (MuNet "Python
+    training": the example step calls mse_loss(model(x), target); "Training
+    swarm": the current loss is MSE).  Reading: the PyTorch mse_loss default,
+    the mean over all B C elements.  Returns the per-row sums of squares
+    r_i = sum_j (z_ij - t_ij)^2 (loss = sum_i r_i / (B C)) and dz = 2 (z - t)
+    / (B C), the gradient of that mean."""
+    t = np.asarray(t, np.float64)
+    if t.shape != z.shape:
+        raise ValueError("targets must have the shape of the outputs")
+    d = z - t
+    return (d * d).sum(axis=1), 2.0 * d / max(d.size, 1)
 
 
 def argmax_rows(z: np.ndarray) -> np.ndarray:
@@ -281,15 +300,23 @@ def backward(fw: Dict[str, list], dz: np.ndarray, acts: Sequence[int],
 def train_step(params: Sequence[np.ndarray], m: Sequence[np.ndarray],
                v: Sequence[np.ndarray], t: int, x: np.ndarray, y: np.ndarray,
                acts: Sequence[int], lr, beta1, beta2, eps, wd,
-               mode: str = "fp64", optim: str = "adamw", max_norm: float = 0.0):
-    """One step: forward, CE loss (batch mean), backward, the update at step
-    t (AdamW by default) of the gradient scaled by the clipping factor.
+               mode: str = "fp64", optim: str = "adamw", max_norm: float = 0.0, loss: str = "ce"):
+    """One step: forward, the loss (softmax CE with integer labels y, batch
+    mean; or MSE with real targets y [B, C], element mean), backward, the
+    update at step t (AdamW by default) of the gradient scaled by the
+    clipping factor.
 
     Returns (loss, new_params, new_m, new_v, grads, extras); grads are the
     unclipped gradients."""
     fw = forward(params, x, acts, mode)
-    loss_rows, dz = softmax_ce(fw["z"], y)
-    loss = float(loss_rows.mean())
+    if loss == "ce":
+        loss_rows, dz = softmax_ce(fw["z"], y)
+        loss = float(loss_rows.mean())
+    elif loss == "mse":
+        loss_rows, dz = mse(fw["z"], y)
+        loss = float(loss_rows.sum() / max(dz.size, 1))
+    else:
+        raise ValueError(f"unknown loss {loss}")
     grads = backward(fw, dz, acts, mode)
     c = clip_coef(grads, max_norm)
     newp, newm, newv = [], [], []
@@ -302,18 +329,18 @@ def train_step(params: Sequence[np.ndarray], m: Sequence[np.ndarray],
 
 
 def run_steps(params, acts, batches, hyper, mode="fp64", t0: int = 0, optim: str = "adamw",
-              max_norm: float = 0.0):
+              max_norm: float = 0.0, loss: str = "ce"):
     """Run len(batches) consecutive steps from zero moments.  batches yields
-    (x, y) pairs.  hyper = (lr, beta1, beta2, eps, wd).  Returns (losses,
-    params, m, v, first_step_grads)."""
+    (x, y) pairs (y: labels, or targets for loss="mse").  hyper = (lr, beta1,
+    beta2, eps, wd).  Returns (losses, params, m, v, first_step_grads)."""
     p = [np.asarray(a, np.float64) for a in params]
     m = [np.zeros_like(a) for a in p]
     v = [np.zeros_like(a) for a in p]
     losses, g1 = [], None
     for i, (x, y) in enumerate(batches):
-        loss, p, m, v, g, _ = train_step(p, m, v, t0 + i + 1, x, y, acts, *hyper, mode=mode, optim=optim,
-                                         max_norm=max_norm)
-        losses.append(loss)
+        L, p, m, v, g, _ = train_step(p, m, v, t0 + i + 1, x, y, acts, *hyper, mode=mode, optim=optim,
+                                      max_norm=max_norm, loss=loss)
+        losses.append(L)
         if g1 is None:
             g1 = g
     return losses, p, m, v, g1

@@ -341,25 +341,31 @@ def test_clip_matches_torch_clip_grad_norm():
 
 @pytest.mark.parametrize("optim", ["adamw", "adam", "sgd"])
 @pytest.mark.parametrize("max_norm", [0.0, 0.05])
-def test_whole_step_matches_torch_modules_and_optimizers(optim, max_norm):
+@pytest.mark.parametrize("loss_kind", ["ce", "mse"])
+def test_whole_step_matches_torch_modules_and_optimizers(optim, max_norm, loss_kind):
     """One whole step of the oracle against torch (float64): nn.Linear + ReLU
-    layers, F.cross_entropy (mean), backward, clip_grad_norm_, the optimizer."""
+    layers, F.cross_entropy or F.mse_loss (means), backward, clip_grad_norm_,
+    the optimizer."""
     dims = [9, 7, 6, 5]
     acts = (RELU, RELU)
     B = 11
     ps = _tiny_net(dims, 98)
     x = _rand((B, dims[0]), 99)
-    y = np.random.default_rng(100).integers(0, dims[-1], B)
+    if loss_kind == "ce":
+        y = np.random.default_rng(100).integers(0, dims[-1], B)
+    else:
+        y = _rand((B, dims[-1]), 100)
     lr, b1, b2, eps, wd = 1e-2, 0.9, 0.999, 1e-8, 0.05
     loss, newp, _, _, grads, ex = om.train_step(ps, [0 * p for p in ps], [0 * p for p in ps], 1, x, y, acts,
-                                                lr, b1, b2, eps, wd, optim=optim, max_norm=max_norm)
+                                                lr, b1, b2, eps, wd, optim=optim, max_norm=max_norm,
+                                                loss=loss_kind)
     tps = [torch.tensor(p, requires_grad=True) for p in ps]
     h = torch.tensor(x)
     for l in range(3):
         h = h @ tps[2 * l].T + tps[2 * l + 1]
         if l < 2:
             h = torch.relu(h)
-    tl = F.cross_entropy(h, torch.tensor(y))
+    tl = F.cross_entropy(h, torch.tensor(y)) if loss_kind == "ce" else F.mse_loss(h, torch.tensor(y))
     tl.backward()
     if max_norm:
         torch.nn.utils.clip_grad_norm_(tps, max_norm)
@@ -371,6 +377,45 @@ def test_whole_step_matches_torch_modules_and_optimizers(optim, max_norm):
     assert abs(loss - tl.item()) < 1e-13
     for a, b in zip(newp, tps):
         assert np.allclose(a, b.detach().numpy(), rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# MSE: brute force, torch mse_loss and its autograd (float64), closed forms
+# --------------------------------------------------------------------------
+def test_mse_bruteforce_and_torch():
+    z, t = _rand((5, 3), 101), _rand((5, 3), 102)
+    rows, dz = om.mse(z, t)
+    for i in range(5):
+        assert abs(rows[i] - sum((z[i, j] - t[i, j]) ** 2 for j in range(3))) < 1e-14
+    tz = torch.tensor(z, requires_grad=True)
+    tl = F.mse_loss(tz, torch.tensor(t))
+    tl.backward()
+    assert abs(rows.sum() / z.size - tl.item()) < 1e-15
+    assert np.allclose(dz, tz.grad.numpy(), rtol=1e-15, atol=0)
+
+
+def test_mse_closed_forms():
+    z = _rand((4, 6), 103)
+    rows, dz = om.mse(z, z)
+    assert np.all(rows == 0) and np.all(dz == 0)              # perfect fit
+    rows, dz = om.mse(z, z - 0.5)                             # constant offset a: loss a^2, dz 2a / (B C)
+    assert np.allclose(rows, 6 * 0.25, rtol=1e-15) and np.allclose(dz, 1.0 / 24, rtol=1e-14)
+    with pytest.raises(ValueError):
+        om.mse(z, z[:, :5])
+
+
+def test_mse_one_layer_net_is_least_squares():
+    # one Linear layer under MSE: the gradient is (2 / (B C)) (XW^T + b - T)^T X,
+    # the normal-equation residual of least squares
+    B, K, C = 9, 4, 3
+    W, b = _rand((C, K), 104), _rand(C, 105)
+    x, t = _rand((B, K), 106), _rand((B, C), 107)
+    loss, _, _, _, grads, _ = om.train_step([W, b], [0 * W, 0 * b], [0 * W, 0 * b], 1, x, t, (), 1e-3, 0.9, 0.999,
+                                            1e-8, 0.0, loss="mse")
+    r = x @ W.T + b - t
+    assert abs(loss - np.mean(r ** 2)) < 1e-14
+    assert np.allclose(grads[0], 2.0 / (B * C) * r.T @ x, rtol=1e-13, atol=1e-15)
+    assert np.allclose(grads[1], 2.0 / (B * C) * r.sum(axis=0), rtol=1e-13, atol=1e-15)
 
 
 # --------------------------------------------------------------------------
@@ -490,3 +535,13 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_clip_matches_torch_clip_grad_norm()
     monkeypatch.setattr(om, "clip_coef", orig_clip)
+
+    # (8) MSE gradient scaled by 1/B instead of 1/(B C), or missing the 2
+    orig_mse = om.mse
+    monkeypatch.setattr(om, "mse", lambda z, t: (orig_mse(z, t)[0], orig_mse(z, t)[1] * z.shape[1]))
+    with pytest.raises(AssertionError):
+        test_mse_bruteforce_and_torch()
+    monkeypatch.setattr(om, "mse", lambda z, t: (orig_mse(z, t)[0], orig_mse(z, t)[1] / 2))
+    with pytest.raises(AssertionError):
+        test_mse_closed_forms()
+    monkeypatch.setattr(om, "mse", orig_mse)
