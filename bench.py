@@ -77,6 +77,8 @@ def layer_work(w, kind, l, x3=False):
         return 3 * 2 * B * K * C, es * 3 * B * K + 4 * B + 4 * (C * K + C)
     if kind == "ce":
         return 0, 2 * es * B * C + 8 * B
+    if kind == "mse":   # read z and fp32 targets, write dz and the row sums
+        return 0, 2 * es * B * C + 4 * B * C + 4 * B
     if kind == "loss_mean":
         return 0, 4 * B
     w16 = 2 if w.dtype == 1 else (6 if x3 else 0)   # bf16 weight copy (planes) written by the update
@@ -119,6 +121,8 @@ def attach_work(w, prof):
             bwd_l = w.n_layers - 2
         elif name == "softmax_ce":
             kind, l = "ce", -1
+        elif name == "mse":
+            kind, l = "mse", -1
         elif name == "loss_mean":
             kind, l = "loss_mean", -1
         elif name.endswith("_wgrad"):
@@ -253,7 +257,7 @@ def oracle_sample_rows(w, budget_s=1.0):
 class OracleRunner:
     """The CPU oracle, as it stands, stepping on a bounded row sample."""
 
-    def __init__(self, w, optim="adamw", max_norm=0.0):
+    def __init__(self, w, optim="adamw", max_norm=0.0, loss="ce"):
         import numpy as np
         import synth
         from oracle import mlp_oracle as om
@@ -264,12 +268,13 @@ class OracleRunner:
         self.v = [np.zeros_like(p) for p in self.params]
         self.mode = "fp64" if w.dtype == 0 else "bf16_mirror"
         self.hyper = tuple(float(np.float32(a)) for a in (w.lr, w.beta1, w.beta2, w.eps, w.wd))
-        self.optim, self.max_norm = optim, float(np.float32(max_norm))
+        self.optim, self.max_norm, self.loss = optim, float(np.float32(max_norm)), loss
         self.batches = []
         for s in range(4):
             x, y = synth.make_batch(w, s)
-            self.batches.append((x[:self.rows].float().numpy().astype(np.float64),
-                                 y[:self.rows].numpy().astype(np.int64)))
+            y = (synth.make_targets(w, s)[:self.rows].numpy().astype(np.float64) if loss == "mse"
+                 else y[:self.rows].numpy().astype(np.int64))
+            self.batches.append((x[:self.rows].float().numpy().astype(np.float64), y))
         self.t = 0
 
     def step(self) -> float:
@@ -277,7 +282,8 @@ class OracleRunner:
         t0 = time.perf_counter()
         _, self.params, self.m, self.v, _, _ = self.om.train_step(self.params, self.m, self.v, self.t + 1, x, y,
                                                                   self.w.acts, *self.hyper, mode=self.mode,
-                                                                  optim=self.optim, max_norm=self.max_norm)
+                                                                  optim=self.optim, max_norm=self.max_norm,
+                                                                  loss=self.loss)
         self.t += 1
         return time.perf_counter() - t0
 
@@ -286,8 +292,8 @@ class OracleRunner:
                 f"{self.w.name} workload; OpenBLAS threads = host cores")
 
 
-def time_oracle(w, target_s=10.0, optim="adamw", max_norm=0.0):
-    r = OracleRunner(w, optim, max_norm)
+def time_oracle(w, target_s=10.0, optim="adamw", max_norm=0.0, loss="ce"):
+    r = OracleRunner(w, optim, max_norm, loss)
     el, steps = 0.0, 0
     while el < target_s:
         el += r.step()
@@ -309,7 +315,7 @@ def dist_setup():
 def run_reference(args, w, world, rank):
     if rank != 0:
         return 0
-    r = OracleRunner(w, args.optim, args.max_grad_norm)
+    r = OracleRunner(w, args.optim, args.max_grad_norm, args.loss)
     for _ in range(args.warmup):
         r.step()
     t_all = sum(r.step() for _ in range(args.steps))
@@ -334,9 +340,12 @@ def config_of(w, extra=None, args=None):
            f"{OPTIM_NAMES[optim]} lr={w.lr} betas=({w.beta1},{w.beta2}) eps={w.eps} wd={w.wd}")
     if args and args.max_grad_norm > 0:
         opt += f", global grad-norm clipping at {args.max_grad_norm}"
+    mse = bool(args and args.loss == "mse")
     c = {"workload": f"{w.name}: MLP {'-'.join(map(str, w.dims))}, "
-                     f"{'fp32' if w.dtype == 0 else 'bf16 + fp32 master'}, batch {w.batch}",
+                     f"{'fp32' if w.dtype == 0 else 'bf16 + fp32 master'}, batch {w.batch}"
+                     + (", MSE loss on fp32 targets" if mse else ""),
          "dims": list(w.dims), "acts": [["none", "relu", "gelu_tanh"][a] for a in w.acts], "global_batch": w.batch,
+         "loss": "MSE (element mean, fp32 N(0,1) targets)" if mse else "softmax CE (batch mean)",
          "optimizer": opt,
          "parallelism": "replicas"}
     if extra:
@@ -358,6 +367,7 @@ def main():
     ap.add_argument("--optim", default="adamw", choices=["adamw", "adam", "sgd"],
                     help="update rule (default AdamW)")
     ap.add_argument("--max-grad-norm", type=float, default=0.0, help="> 0: global gradient-norm clipping")
+    ap.add_argument("--loss", default="ce", choices=["ce", "mse"], help="softmax CE (default) or MSE")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -388,16 +398,22 @@ def main():
         model.set_option(nn.OPT_F32_TENSOR_CORES, 0 if args.f32_ffma else 1)
     model.set_optimizer({"adamw": nn.OPTIM_ADAMW, "adam": nn.OPTIM_ADAM, "sgd": nn.OPTIM_SGD}[args.optim],
                         args.max_grad_norm)
+    mse = args.loss == "mse"
+    if mse:
+        model.set_loss(nn.LOSS_MSE)
     gemm_mode = None if w.dtype != 0 else (
-        "FFMA" if args.f32_ffma else "tensor cores, fp32 operands as three bf16 planes (6 products, fp32 accumulate)")
+        "FFMA" if args.f32_ffma or mse else
+        "tensor cores, fp32 operands as three bf16 planes (6 products, fp32 accumulate)")
     hyper = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, wd=w.wd)
 
     # device-resident batch pool larger than L2
     x0, y0 = synth.make_batch(w, 0)
-    per = x0.numel() * x0.element_size() + y0.numel() * 4
+    per = x0.numel() * x0.element_size() + (w.batch * w.n_classes if args.loss == "mse" else y0.numel()) * 4
     n_pool = max(4, min(64, math.ceil(1.5 * L2_BYTES / per)))
     n_gen = min(n_pool, 8)
     gen = [synth.make_batch(w, s + 1000 * rank) for s in range(n_gen)]
+    if mse:   # regression targets in place of the labels
+        gen = [(x, synth.make_targets(w, s + 1000 * rank)) for s, (x, _) in enumerate(gen)]
     xs, ys = [], []
     for i in range(n_pool):
         x, y = gen[i % n_gen]
@@ -476,7 +492,7 @@ def main():
         e2e_ms = float(t.item())
     x_bytes = hx[0].numel() * hx[0].element_size()
     e2e = {"value": w.batch * world * args.steps / (e2e_ms / 1e3), "unit": "samples/s",
-           "h2d_bytes_per_step": int(x_bytes + hy[0].numel() * 4), "d2h_bytes_per_step": 4}
+           "h2d_bytes_per_step": int(x_bytes + hy[0].numel() * hy[0].element_size()), "d2h_bytes_per_step": 4}
 
     # ---- per-kernel times (serialised profiling pass, same stream) ----
     n_prof = 10
@@ -516,7 +532,7 @@ def main():
     if args.kernels:
         line["kernels"] = [{k: (round(v, 5) if isinstance(v, float) else v) for k, v in r.items()} for r in rows]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = time_oracle(w, target_s=10.0, optim=args.optim, max_norm=args.max_grad_norm)
+        cb = time_oracle(w, target_s=10.0, optim=args.optim, max_norm=args.max_grad_norm, loss=args.loss)
         line["cpu_baseline"] = {k: (round(v, 2) if isinstance(v, float) else v) for k, v in cb.items()}
     if rank == 0:
         print(json.dumps(line))

@@ -8,7 +8,8 @@
  *             noeira.ai "Neural networks", "The design in one page");
  *   loss      mean over the batch of softmax cross-entropy with integer
  *             labels (devpost "Orthon", "Core capabilities" and "Selected
- *             Orthon vs. PyTorch results");
+ *             Orthon vs. PyTorch results"), or mean squared error against
+ *             real targets (mlp_set_loss);
  *   backward  explicit vector-Jacobian products (noeira "The design in one
  *             page": forward and vjp per module, no tape): dW_l = dY_l^T X_l,
  *             db_l = column sums of dY_l, dY_{l-1} = (dY_l W_l) * act';
@@ -24,8 +25,10 @@
  *     device; host pointers are ordinary process memory.  `stream` is a
  *     cudaStream_t (NULL = the legacy default stream).
  *   - Tensors are dense row-major.  x is [batch, dims[0]] in the model dtype
- *     (float for MLP_F32, bfloat16 bits for MLP_BF16); labels are int32
- *     [batch]; logits are [batch, C] in the model dtype.
+ *     (float for MLP_F32, bfloat16 bits for MLP_BF16); the training targets
+ *     y are int32 labels [batch] (softmax CE, the default loss) or float
+ *     targets [batch, C] (MLP_LOSS_MSE, see mlp_set_loss); logits are
+ *     [batch, C] in the model dtype.
  *   - Parameters use a flat order: for l = 1..L, W_l [dims[l], dims[l-1]]
  *     row-major then b_l [dims[l]].  mlp_read_params / mlp_write_params move
  *     them densely packed in that order.
@@ -105,30 +108,34 @@ mlp_status mlp_create(const int64_t* dims, int n_dims, const int* acts, int act,
  * argmax_dev (int32 [batch], lowest index among equal maxima; nullable). */
 mlp_status mlp_forward(mlp_t* model, const void* x_dev, void* logits_dev, int32_t* argmax_dev, void* stream);
 
-/* One training step on (x_dev, labels_dev): forward, softmax-CE, backward,
- * AdamW(lr, beta1, beta2, eps, wd) at step t = (step counter + 1).  The
- * batch-mean loss is written to loss_dev (device float; nullable).  Nothing
- * is read back; the call returns once the work is enqueued on `stream`. */
-mlp_status mlp_train_step(mlp_t* model, const void* x_dev, const int32_t* labels_dev, float lr, float beta1,
+/* One training step on (x_dev, y_dev): forward, the loss (softmax-CE of
+ * int32 labels, or MSE of float targets), backward, AdamW(lr, beta1, beta2,
+ * eps, wd) (or the rule of mlp_set_optimizer) at step t = (step counter + 1).
+ * The loss (batch mean; element mean for MSE) is written to loss_dev (device
+ * float; nullable).  Nothing is read back; the call returns once the work is
+ * enqueued on `stream`. */
+mlp_status mlp_train_step(mlp_t* model, const void* x_dev, const void* y_dev, float lr, float beta1,
                           float beta2, float eps, float wd, float* loss_dev, void* stream);
 
 /* One training step on a batch in HOST memory (page-locked, so the copies are
- * asynchronous): x_host [batch, dims[0]] in the model dtype, labels_host
- * int32 [batch].  The library copies them on its own copy stream into one of
+ * asynchronous): x_host [batch, dims[0]] in the model dtype, y_host the
+ * labels or MSE targets (MSE targets from host memory need batch * C * 4 <=
+ * 64 MiB, else MLP_ERR_SHAPE).  The library copies them on its own copy
+ * stream into one of
  * two device input slots in the arena, so the copies for the next call
  * overlap the kernels of this one; the step waits for its own copies.  The
  * host buffers must stay valid and unchanged until their copy has completed
  * (at the latest when the step completes).  loss_host (nullable, pinned)
  * receives the step's batch-mean loss when the step completes.  Returns once
  * the copies and the step are enqueued on `stream`. */
-mlp_status mlp_train_step_host(mlp_t* model, const void* x_host, const int32_t* labels_host, float lr, float beta1,
+mlp_status mlp_train_step_host(mlp_t* model, const void* x_host, const void* y_host, float lr, float beta1,
                                float beta2, float eps, float wd, float* loss_host, void* stream);
 
 /* n_steps consecutive training steps enqueued as ONE CUDA-graph launch;
- * step i reads x_devs[i] / label_devs[i] (host arrays of device pointers)
+ * step i reads x_devs[i] / y_devs[i] (host arrays of device pointers)
  * and writes its loss to losses_dev[i] (nullable).  The graph is built on
  * the first call for a given n_steps and re-pointed on later calls. */
-mlp_status mlp_train_steps(mlp_t* model, int n_steps, const void* const* x_devs, const int32_t* const* label_devs,
+mlp_status mlp_train_steps(mlp_t* model, int n_steps, const void* const* x_devs, const void* const* y_devs,
                            float lr, float beta1, float beta2, float eps, float wd, float* losses_dev,
                            void* stream);
 
@@ -185,6 +192,21 @@ mlp_status mlp_set_option(mlp_t* model, int option, int64_t value);
 enum { MLP_OPTIM_ADAMW = 0, MLP_OPTIM_ADAM = 1, MLP_OPTIM_SGD = 2 };
 mlp_status mlp_set_optimizer(mlp_t* model, int kind, float max_grad_norm);
 
+/* The loss of the training step (default MLP_LOSS_CE):
+ *   MLP_LOSS_CE   softmax cross-entropy of int32 labels [batch], mean over
+ *                 the batch (the step described at the top).
+ *   MLP_LOSS_MSE  mean squared error against float targets [batch, C], mean
+ *                 over all batch * C elements (the PyTorch mse_loss
+ *                 default): dz = 2 (z - t) / (batch C) (MuNet "Python
+ *                 training": the example step trains with mse_loss; "Training
+ *                 swarm": the loss is MSE).  The step takes the same kernels
+ *                 as with CE (the fused output layer where MLP_OPT_FUSE_HEAD
+ *                 applies, the fp32 tensor-core planes), the loss part
+ *                 replaced.
+ * The targets are passed where the step entry points take y. */
+enum { MLP_LOSS_CE = 0, MLP_LOSS_MSE = 1 };
+mlp_status mlp_set_loss(mlp_t* model, int loss);
+
 /* ||g||_2 computed by the last training step that clipped (0 before any);
  * synchronises the model's device. */
 mlp_status mlp_read_grad_norm(mlp_t* model, float* out);
@@ -214,7 +236,7 @@ int mlp_kernels_per_step(const mlp_t* model);
  * ms_out[i] and its name (a static string) to names_out[i] (nullable) for
  * i < min(*n_out, max_kernels); *n_out = kernels in the step.  Synchronises
  * the stream before returning. */
-mlp_status mlp_profile_step(mlp_t* model, const void* x_dev, const int32_t* labels_dev, float lr, float beta1,
+mlp_status mlp_profile_step(mlp_t* model, const void* x_dev, const void* y_dev, float lr, float beta1,
                             float beta2, float eps, float wd, float* loss_dev, void* stream, float* ms_out,
                             const char** names_out, int max_kernels, int* n_out);
 

@@ -101,6 +101,14 @@ mlp_status mlp_op_softmax_ce(int dtype, int64_t B, int64_t C, const void* z, int
                              float grad_scale, void* dz, int64_t lddz, float* loss_rows, uint32_t* err_dev,
                              void* stream);
 
+/* Squared error of outputs z [B, C] (ldz, dtype) against fp32 targets t
+ * [B, C] (ldt), the MSE loss (pypi "munet-nn", "Python training":
+ * mse_loss):  loss_rows[i] = sum_j (z_ij - t_ij)^2 (fp32), dz_ij = (z_ij -
+ * t_ij) * grad_scale (dtype; grad_scale = 2 / (B C) gives the gradient of
+ * the mean over all elements, the loss being sum(loss_rows) / (B C)). */
+mlp_status mlp_op_mse(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, const float* t, int64_t ldt,
+                      float grad_scale, void* dz, int64_t lddz, float* loss_rows, void* stream);
+
 /* loss = mean(loss_rows[0..B)) summed in a fixed order (device float). */
 mlp_status mlp_op_loss_mean(int64_t B, const float* loss_rows, float* loss, uint32_t* err_dev, void* stream);
 

@@ -24,6 +24,7 @@ F32X3 = 2   # op-level GEMM operands: fp32 as three bf16 planes [3][rows][ld]
 PLANE_P, PLANE_G, PLANE_M, PLANE_V = 0, 1, 2, 3
 OPTIM_ADAMW, OPTIM_ADAM, OPTIM_SGD = 0, 1, 2
 OPTIM_WS_FLOATS = 1216   # op-level clipping workspace (floats)
+LOSS_CE, LOSS_MSE = 0, 1
 
 
 class MlpError(RuntimeError):
@@ -48,6 +49,7 @@ _SIGS = {
     "mlp_set_option": (_I32, [_P, _I32, _I64]),
     "mlp_set_optimizer": (_I32, [_P, _I32, _F]),
     "mlp_read_grad_norm": (_I32, [_P, _c.POINTER(_F)]),
+    "mlp_set_loss": (_I32, [_P, _I32]),
     "mlp_num_params": (_I64, [_P]),
     "mlp_num_layers": (_I32, [_P]),
     "mlp_read_params": (_I32, [_P, _I32, _P, _SZ, _c.POINTER(_I64)]),
@@ -65,6 +67,7 @@ _SIGS = {
     "mlp_op_wgrad_noalloc": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
     "mlp_op_split3": (_I32, [_I64, _I64, _P, _I64, _P, _I64, _P]),
     "mlp_op_softmax_ce": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _F, _P, _I64, _P, _P, _P]),
+    "mlp_op_mse": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _I64, _F, _P, _I64, _P, _P]),
     "mlp_op_loss_mean": (_I32, [_I64, _P, _P, _P, _P]),
     "mlp_op_adamw": (_I32, [_I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _P]),
     "mlp_op_optim": (_I32, [_I32, _I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _F, _P, _P, _P]),
@@ -153,6 +156,10 @@ def mlp_set_optimizer(h, kind: int, max_grad_norm: float = 0.0) -> None:
     _check(lib().mlp_set_optimizer(h, kind, max_grad_norm))
 
 
+def mlp_set_loss(h, loss: int) -> None:
+    _check(lib().mlp_set_loss(h, loss))
+
+
 def mlp_read_grad_norm(h) -> float:
     out = _F(0.0)
     _check(lib().mlp_read_grad_norm(h, ctypes.byref(out)))
@@ -230,6 +237,10 @@ def mlp_op_softmax_ce(dtype, B, C, z, ldz, labels, grad_scale, dz, lddz, loss_ro
     _check(lib().mlp_op_softmax_ce(dtype, B, C, z, ldz, labels, grad_scale, dz, lddz, loss_rows, err, stream))
 
 
+def mlp_op_mse(dtype, B, C, z, ldz, t, ldt, grad_scale, dz, lddz, loss_rows, stream) -> None:
+    _check(lib().mlp_op_mse(dtype, B, C, z, ldz, t, ldt, grad_scale, dz, lddz, loss_rows, stream))
+
+
 def mlp_op_loss_mean(B, loss_rows, loss, err, stream) -> None:
     _check(lib().mlp_op_loss_mean(B, loss_rows, loss, err, stream))
 
@@ -264,6 +275,7 @@ class Model:
         self.arena = torch.empty(nbytes, dtype=torch.uint8, device=f"cuda:{device}")
         self.h = mlp_create(self.dims, self.acts, act, dtype, seed, batch, self.arena.data_ptr(), nbytes, device)
         self.n_params = mlp_num_params(self.h)
+        self.loss_kind = LOSS_CE
 
     @property
     def tdtype(self):
@@ -284,11 +296,23 @@ class Model:
     def grad_norm(self) -> float:
         return mlp_read_grad_norm(self.h)
 
+    def set_loss(self, loss: int) -> None:
+        mlp_set_loss(self.h, loss)
+        self.loss_kind = loss
+
+    def _check_y(self, y, on_device: bool) -> None:
+        t = self.torch
+        assert y.is_cuda == on_device and y.is_contiguous()
+        if self.loss_kind == LOSS_MSE:
+            assert y.dtype == t.float32 and tuple(y.shape) == (self.batch, self.dims[-1])
+        else:
+            assert y.dtype == t.int32 and y.numel() == self.batch
+
     def _check_x(self, x, labels=None):
         t = self.torch
         assert x.is_cuda and x.dtype == self.tdtype and x.is_contiguous() and tuple(x.shape) == (self.batch, self.dims[0])
         if labels is not None:
-            assert labels.is_cuda and labels.dtype == t.int32 and labels.is_contiguous() and labels.numel() == self.batch
+            self._check_y(labels, True)
 
     def train_step(self, x, labels, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0, loss=None):
         self._check_x(x, labels)
@@ -303,7 +327,7 @@ class Model:
         `loss` (optional) is a pinned float32 host tensor of one element."""
         t = self.torch
         assert not x.is_cuda and x.dtype == self.tdtype and x.is_contiguous() and tuple(x.shape) == (self.batch, self.dims[0])
-        assert not labels.is_cuda and labels.dtype == t.int32 and labels.is_contiguous() and labels.numel() == self.batch
+        self._check_y(labels, False)
         mlp_train_step_host(self.h, x.data_ptr(), labels.data_ptr(), lr, beta1, beta2, eps, wd,
                             loss.data_ptr() if loss is not None else None, self.stream())
 

@@ -1,6 +1,7 @@
 // The output layer of the step fused into one kernel for the 10-class,
 // 128-input layer of the MNIST-shaped MLP: logits z = h W^T + b, softmax
-// cross-entropy (loss and dz), the dgrad of the layer with the hidden
+// cross-entropy (loss and dz; or the squared error against real targets,
+// the MSE of pypi "munet-nn", "Python training"), the dgrad of the layer with the hidden
 // activation's VJP (dY = (dz W) * act'), and the partial sums of the layer's
 // weight and bias gradients (dW = dz^T h, db = sum dz) and of the batch loss.
 // Each row of h is read once; W lives in shared memory.  This is the
@@ -43,7 +44,8 @@ struct HeadParams {
   const void* h; int64_t ldh;          // [B, 128] model dtype (input of the output layer)
   const void* W;                       // [10, 128] model dtype
   const float* bias;                   // [10]
-  const int32_t* labels;               // [B]
+  const int32_t* labels;               // [B] (softmax CE)
+  const float* targets; int64_t ldt;   // [B, 10] fp32 (MSE)
   const void* aux; int64_t ld_aux;     // stored u of the layer below (GELU only)
   void* dY; int64_t ldy;               // [B, 128] model dtype
   int64_t* step_counter;
@@ -130,7 +132,7 @@ __device__ __forceinline__ void store_dy4(const HeadParams& p, int64_t i, const 
   }
 }
 
-template <typename T, bool X3 = false>
+template <typename T, bool X3 = false, bool MSE = false>
 __global__ void __cluster_dims__(kHCluster, 1, 1) __launch_bounds__(kHT)
 head_kernel(const __grid_constant__ HeadParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -146,11 +148,19 @@ head_kernel(const __grid_constant__ HeadParams p) {
   const int ntiles = (p.B + kHR - 1) / kHR;
   float hv[16];
   int label = 0;   // the label of row tid / 8 of the tile (logits / softmax mapping below)
+  float tq[2] = {0.f, 0.f};   // MSE: targets of classes tid % 8 and tid % 8 + 8 of that row
   auto load_tile = [&](int tile) {   // this thread's 16 elements of the tile (zeros past the last row)
     const int r0 = tile * kHR;
     if (tile < ntiles && r0 + hr < p.B) {
       load_h16<T, X3>(p, (int64_t)(r0 + hr) * p.ldh + hc, hv);
-      label = __ldg(p.labels + r0 + hr);
+      if (MSE) {
+        const float* tr = p.targets + (int64_t)(r0 + hr) * p.ldt;
+        const int c0 = tid & 7;
+        tq[0] = __ldg(tr + c0);
+        tq[1] = c0 + 8 < kHC ? __ldg(tr + c0 + 8) : 0.f;
+      } else {
+        label = __ldg(p.labels + r0 + hr);
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 16; ++j) hv[j] = 0.f;
@@ -206,6 +216,7 @@ head_kernel(const __grid_constant__ HeadParams p) {
     for (int j = 0; j < 16; j += 4)
       *reinterpret_cast<float4*>(&s.h[hr][hc + j]) = make_float4(hv[j], hv[j + 1], hv[j + 2], hv[j + 3]);
     const int y = label;   // row lr == hr of this tile
+    const float t0 = tq[0], t1 = tq[1];
     __syncthreads();
     load_tile(tile + gridDim.x);   // the next tile's h, in flight during this one
     // logits (partial dot products over this thread's 16 columns, then a
@@ -233,7 +244,27 @@ head_kernel(const __grid_constant__ HeadParams p) {
       for (int o = 1; o < 8; o <<= 1)
 #pragma unroll
         for (int c = 0; c < kHC; ++c) zc[c] += __shfl_xor_sync(0xffffffffu, zc[c], o);
-      if (lr < nr) {
+      if (MSE) {
+        // d = z - t for classes sub and sub + 8; the row's squared error by
+        // a fixed xor tree over its 8 threads
+        float sq = 0.f;
+        if (lr < nr) {
+#pragma unroll
+          for (int c = 0; c < kHC; ++c) {
+            if (c == sub || c == sub + 8) {
+              const float d = to_f32(from_f32<T>(zc[c] + bias[c])) - (c == sub ? t0 : t1);
+              sq = fmaf(d, d, sq);
+              s.z[lr][c] = to_f32(from_f32<T>(d * p.grad_scale));
+            }
+          }
+        } else {
+          if (sub < kHC) s.z[lr][sub] = 0.f;
+          if (sub + 8 < kHC) s.z[lr][sub + 8] = 0.f;
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if (lr < nr && sub == 0) s.loss_rows[lr] += sq;
+      } else if (lr < nr) {
         float m = -INFINITY, zy = 0.f;
 #pragma unroll
         for (int c = 0; c < kHC; ++c) {
@@ -380,8 +411,14 @@ int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen) {
     snprintf(err, errlen, "fused output layer: workspace too small");
     return -1;
   }
+  const bool mse = op.targets != nullptr;
+  if (mse && op.ldt < op.C) {
+    snprintf(err, errlen, "fused output layer: target pitch below C");
+    return -1;
+  }
   HeadParams q;
   q.h = op.h; q.ldh = op.ldh; q.W = op.W; q.bias = op.bias; q.labels = op.labels;
+  q.targets = op.targets; q.ldt = op.ldt;
   q.aux = op.aux; q.ld_aux = op.ld_aux; q.dY = op.dY; q.ldy = op.ldy;
   q.step_counter = op.step_counter; q.err = op.err;
   q.ws = op.ws;
@@ -389,18 +426,20 @@ int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen) {
   q.grad_scale = op.grad_scale;
   q.bias_corr = op.bias_corr; q.beta1 = op.beta1; q.beta2 = op.beta2;
   q.h_plane = op.h_plane; q.dy_plane = op.dy_plane;
-  const void* fns[3] = {(const void*)head_kernel<float>, (const void*)head_kernel<__nv_bfloat16>,
-                        (const void*)head_kernel<float, true>};
+  const void* fns[6] = {(const void*)head_kernel<float>, (const void*)head_kernel<__nv_bfloat16>,
+                        (const void*)head_kernel<float, true>, (const void*)head_kernel<float, false, true>,
+                        (const void*)head_kernel<__nv_bfloat16, false, true>,
+                        (const void*)head_kernel<float, true, true>};
   static std::once_flag once;
   std::call_once(once, [&] {
     for (const void* f : fns)
       cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(HeadSmem));
   });
-  rec->func = fns[x3 ? 2 : op.dtype == DT_F32 ? 0 : 1];
+  rec->func = fns[(mse ? 3 : 0) + (x3 ? 2 : op.dtype == DT_F32 ? 0 : 1)];
   rec->grid = dim3(head_grid(op.B));
   rec->block = dim3(kHT);
   rec->smem = (unsigned)sizeof(HeadSmem);
-  rec->name = "head_ce";
+  rec->name = mse ? "head_mse" : "head_ce";
   rec->set_args(q);
   return 1;
 }

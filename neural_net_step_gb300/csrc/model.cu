@@ -91,6 +91,7 @@ struct Layout {
   std::vector<char> defer_l;
   size_t off_hws = 0, hws_bytes = 0;   // the fused output layer's partials (read by the optimizer)
   size_t off_xin[2] = {0, 0}, off_yin[2] = {0, 0};   // device inputs of mlp_train_step_host (two slots)
+  size_t yin_bytes = 0;   // labels, or MSE targets where B * C * 4 <= 64 MiB
   size_t off_norm = 0;   // per-block sums of squares of the gradient (clipping)
   size_t total = 0;
 };
@@ -200,9 +201,11 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     L.hws_bytes = head_workspace_bytes(batch, dims[L.L], dims[L.L - 1]);
     L.off_hws = take(L.hws_bytes);
   }
+  L.yin_bytes = batch * 4;
+  if (batch * dims[L.L] * 4 <= (64ll << 20)) L.yin_bytes = batch * dims[L.L] * 4;
   for (int k = 0; k < 2; ++k) {
     L.off_xin[k] = take(batch * dims[0] * (dtype == MLP_F32 ? 4 : 2));
-    L.off_yin[k] = take(batch * 4);
+    L.off_yin[k] = take(L.yin_bytes);
   }
   L.off_norm = take(AdamWOp::kNormParts * sizeof(float));
   L.off_ctl = take(sizeof(Ctl));
@@ -253,6 +256,7 @@ struct mlp {
   bool f32_tc = true;        // fp32 GEMMs on the tensor cores (three bf16 planes) where the model allows
   bool pdl = true;           // graph edges let each kernel launch before its predecessor ends
   int optim = MLP_OPTIM_ADAMW;
+  int loss = MLP_LOSS_CE;
   float max_grad_norm = 0.f; // > 0: global-norm clipping of the gradient before the update
   std::mutex mu;
   std::vector<GraphCache> graphs;
@@ -357,9 +361,10 @@ mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out
 
 struct Hyper { float lr, b1, b2, eps, wd; };
 
-mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper& hp, float* loss,
+mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp, float* loss,
                      std::vector<LaunchRec>& out) {
   const Layout& L = m->lay;
+  const bool mse = m->loss == MLP_LOSS_MSE;
   const bool fuse = m->fuse_head && L.L >= 2 && head_supported(L.dims[L.L], L.dims[L.L - 1]);
   const bool x3 = m->x3();   // implies fuse
   const int64_t dy_plane = L.B * L.max_ld;
@@ -381,14 +386,18 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     hd.h_plane = L.B * L.ld_h[l - 1]; hd.dy_plane = dy_plane;
     hd.W = m->weight(l);   // fp32 master weights for an fp32 model
     hd.bias = m->plane(MLP_PLANE_P) + L.boff[l];
-    hd.labels = y;
+    if (mse) {
+      hd.targets = (const float*)y; hd.ldt = L.dims[L.L];
+    } else {
+      hd.labels = (const int32_t*)y;
+    }
     hd.aux = hd.act == MLP_ACT_GELU_TANH ? m->at(L.off_u[l - 1]) : m->at(L.off_h[l - 1]);
     hd.ld_aux = L.ld_h[l - 1];
     hd.dY = m->at(L.off_dy[0]); hd.ldy = L.ld_h[l - 1];
     hd.step_counter = &ctl->step;
     hd.err = &ctl->err;
     hd.ws = (float*)m->at(L.off_hws); hd.ws_bytes = L.hws_bytes;
-    hd.grad_scale = (float)(1.0 / (double)L.B);
+    hd.grad_scale = (float)((mse ? 2.0 / (double)L.dims[L.L] : 1.0) / (double)L.B);
     hd.bias_corr = ctl->bias_corr; hd.beta1 = hp.b1; hd.beta2 = hp.b2;
     char e_[512] = "";
     LaunchRec r;
@@ -398,20 +407,33 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     buf = 1;
     top = L.L - 2;
   } else {
-    CeOp ce;
-    ce.dtype = L.dtype; ce.B = L.B; ce.C = L.dims[L.L];
-    ce.z = m->at(L.off_z); ce.ldz = L.ldz;
-    ce.labels = y;
-    ce.dz = m->at(L.off_dz); ce.lddz = L.ldz;
-    ce.loss_rows = (float*)m->at(L.off_loss_rows);
-    ce.grad_scale = (float)(1.0 / (double)L.B);
-    ce.err = &ctl->err;
     char e_[512] = "";
     LaunchRec r;
-    if (ce_plan(ce, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    float* loss_rows = (float*)m->at(L.off_loss_rows);
+    if (mse) {
+      MseOp op;
+      op.dtype = L.dtype; op.B = L.B; op.C = L.dims[L.L];
+      op.z = m->at(L.off_z); op.ldz = L.ldz;
+      op.t = (const float*)y; op.ldt = L.dims[L.L];
+      op.dz = m->at(L.off_dz); op.lddz = L.ldz;
+      op.loss_rows = loss_rows;
+      op.grad_scale = (float)(2.0 / ((double)L.B * (double)L.dims[L.L]));
+      if (mse_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    } else {
+      CeOp ce;
+      ce.dtype = L.dtype; ce.B = L.B; ce.C = L.dims[L.L];
+      ce.z = m->at(L.off_z); ce.ldz = L.ldz;
+      ce.labels = (const int32_t*)y;
+      ce.dz = m->at(L.off_dz); ce.lddz = L.ldz;
+      ce.loss_rows = loss_rows;
+      ce.grad_scale = (float)(1.0 / (double)L.B);
+      ce.err = &ctl->err;
+      if (ce_plan(ce, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    }
     out.push_back(r);
     LossMeanOp lm;
-    lm.B = L.B; lm.loss_rows = ce.loss_rows;
+    lm.B = L.B; lm.loss_rows = loss_rows;
+    lm.count = mse ? (double)L.B * (double)L.dims[L.L] : (double)L.B;
     lm.loss = loss ? loss : &ctl->loss_slot;
     lm.step_counter = &ctl->step;
     lm.err = &ctl->err;
@@ -499,7 +521,8 @@ mlp_status plan_step(const mlp* m, const void* x, const int32_t* y, const Hyper&
     const int64_t nw = L.dims[L.L] * L.dims[l];
     ad.seg[ad.nseg++] = AdamWOp::Seg{L.woff[l], nw, hws, hpart.n, hpart.stride};
     ad.seg[ad.nseg++] = AdamWOp::Seg{L.boff[l], L.dims[L.L], hws + nw, hpart.n, hpart.stride};
-    ad.loss_parts = hws + hpart.loss_off; ad.loss_n = hpart.n; ad.loss_scale = 1.0f / (float)L.B;
+    ad.loss_parts = hws + hpart.loss_off; ad.loss_n = hpart.n;
+    ad.loss_scale = (float)(1.0 / ((double)L.B * (mse ? (double)L.dims[L.L] : 1.0)));
     ad.loss = loss ? loss : &ctl->loss_slot;
     ad.err = &ctl->err;
   }
@@ -718,6 +741,18 @@ mlp_status mlp_set_optimizer(mlp_t* m, int kind, float max_grad_norm) {
   return ok();
 }
 
+mlp_status mlp_set_loss(mlp_t* m, int loss) {
+  if (!m) return fail(MLP_ERR_ARG, "model is NULL");
+  if (loss != MLP_LOSS_CE && loss != MLP_LOSS_MSE) return fail(MLP_ERR_ARG, "unknown loss %d", loss);
+  std::lock_guard<std::mutex> lk(m->mu);
+  m->loss = loss;
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_step(m, m->arena, m->arena, Hyper{1e-3f, 0.9f, 0.999f, 1e-8f, 0.f}, nullptr, recs);
+  if (st != MLP_OK) return st;
+  m->kernels_per_step = (int)recs.size();
+  return ok();
+}
+
 mlp_status mlp_read_grad_norm(mlp_t* m, float* out) {
   if (!m || !out) return fail(MLP_ERR_ARG, "model or out is NULL");
   std::lock_guard<std::mutex> lk(m->mu);
@@ -787,7 +822,7 @@ mlp_status mlp_forward(mlp_t* m, const void* x, void* logits, int32_t* argmax_ou
   return ok();
 }
 
-mlp_status mlp_train_step(mlp_t* m, const void* x, const int32_t* y, float lr, float b1, float b2, float eps,
+mlp_status mlp_train_step(mlp_t* m, const void* x, const void* y, float lr, float b1, float b2, float eps,
                           float wd, float* loss, void* stream) {
   if (!m || !x || !y) return fail(MLP_ERR_ARG, "model, x or labels is NULL");
   if (!(lr >= 0) || !(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1) || !(eps >= 0) || !(wd >= 0))
@@ -800,7 +835,7 @@ mlp_status mlp_train_step(mlp_t* m, const void* x, const int32_t* y, float lr, f
   return run(m, 1, recs, (cudaStream_t)stream);
 }
 
-mlp_status mlp_train_step_host(mlp_t* m, const void* x_host, const int32_t* y_host, float lr, float b1, float b2,
+mlp_status mlp_train_step_host(mlp_t* m, const void* x_host, const void* y_host, float lr, float b1, float b2,
                                float eps, float wd, float* loss_host, void* stream) {
   if (!m || !x_host || !y_host) return fail(MLP_ERR_ARG, "model, x or labels is NULL");
   if (!(lr >= 0) || !(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1) || !(eps >= 0) || !(wd >= 0))
@@ -820,7 +855,11 @@ mlp_status mlp_train_step_host(mlp_t* m, const void* x_host, const int32_t* y_ho
   }
   const int k = m->host_calls & 1;
   uint8_t* xd = (uint8_t*)m->at(L.off_xin[k]);
-  int32_t* yd = (int32_t*)m->at(L.off_yin[k]);
+  void* yd = m->at(L.off_yin[k]);
+  const size_t ybytes = m->loss == MLP_LOSS_MSE ? (size_t)L.B * L.dims[L.L] * 4 : (size_t)L.B * 4;
+  if (ybytes > L.yin_bytes)
+    return fail(MLP_ERR_SHAPE, "MSE targets of %zu bytes do not fit the host-step input slot (%zu)", ybytes,
+                L.yin_bytes);
   const size_t xbytes = (size_t)L.B * L.dims[0] * (L.dtype == MLP_F32 ? 4 : 2);
   // slot k is free once the step that last read it has finished; x goes in
   // NC pieces on NC streams (several copy engines), the labels with the last
@@ -833,7 +872,7 @@ mlp_status mlp_train_step_host(mlp_t* m, const void* x_host, const int32_t* y_ho
       CUDA_TRY(cudaMemcpyAsync(xd + o, (const uint8_t*)x_host + o, n, cudaMemcpyHostToDevice, m->copy_stream[c]));
     }
     if (c == NC - 1)
-      CUDA_TRY(cudaMemcpyAsync(yd, y_host, (size_t)L.B * 4, cudaMemcpyHostToDevice, m->copy_stream[c]));
+      CUDA_TRY(cudaMemcpyAsync(yd, y_host, ybytes, cudaMemcpyHostToDevice, m->copy_stream[c]));
     CUDA_TRY(cudaEventRecord(m->copied[k][c], m->copy_stream[c]));
     CUDA_TRY(cudaStreamWaitEvent(s, m->copied[k][c], 0));
   }
@@ -849,7 +888,7 @@ mlp_status mlp_train_step_host(mlp_t* m, const void* x_host, const int32_t* y_ho
   return ok();
 }
 
-mlp_status mlp_train_steps(mlp_t* m, int n_steps, const void* const* xs, const int32_t* const* ys, float lr,
+mlp_status mlp_train_steps(mlp_t* m, int n_steps, const void* const* xs, const void* const* ys, float lr,
                            float b1, float b2, float eps, float wd, float* losses, void* stream) {
   if (!m || !xs || !ys || n_steps < 1) return fail(MLP_ERR_ARG, "bad arguments");
   if (!(lr >= 0) || !(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1) || !(eps >= 0) || !(wd >= 0))
@@ -865,7 +904,7 @@ mlp_status mlp_train_steps(mlp_t* m, int n_steps, const void* const* xs, const i
   return run(m, n_steps, recs, (cudaStream_t)stream);
 }
 
-mlp_status mlp_profile_step(mlp_t* m, const void* x, const int32_t* y, float lr, float b1, float b2, float eps,
+mlp_status mlp_profile_step(mlp_t* m, const void* x, const void* y, float lr, float b1, float b2, float eps,
                             float wd, float* loss, void* stream, float* ms_out, const char** names_out,
                             int max_kernels, int* n_out) {
   if (!m || !x || !y || !n_out || (max_kernels > 0 && !ms_out)) return fail(MLP_ERR_ARG, "bad arguments");
@@ -1072,6 +1111,19 @@ mlp_status mlp_op_softmax_ce(int dtype, int64_t B, int64_t C, const void* z, int
   LaunchRec r;
   char e_[512] = "";
   if (ce_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  return run_ops(&r, 1, stream);
+}
+
+mlp_status mlp_op_mse(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, const float* t, int64_t ldt,
+                      float grad_scale, void* dz, int64_t lddz, float* loss_rows, void* stream) {
+  if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
+  if (!z || !t || !dz || !loss_rows) return fail(MLP_ERR_ARG, "null pointer");
+  MseOp op;
+  op.dtype = dtype; op.B = B; op.C = C; op.z = z; op.ldz = ldz; op.t = t; op.ldt = ldt;
+  op.dz = dz; op.lddz = lddz; op.loss_rows = loss_rows; op.grad_scale = grad_scale;
+  LaunchRec r;
+  char e_[512] = "";
+  if (mse_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
   return run_ops(&r, 1, stream);
 }
 

@@ -74,10 +74,26 @@ struct CeOp {
 };
 int ce_plan(const CeOp& op, LaunchRec* rec, char* err, size_t errlen);
 
-// loss = mean(loss_rows) in a fixed order; optionally bumps the step counter
-// and latches a non-finite loss into the error word.
+// Squared error against fp32 targets t [B, C] (ldt):  loss_rows[i] =
+// sum_j (z_ij - t_ij)^2 (fp32), dz_ij = (z_ij - t_ij) * grad_scale (dtype;
+// grad_scale = 2 / (B C) gives the gradient of the element-mean loss).
+struct MseOp {
+  int dtype = 0;
+  int64_t B = 0, C = 0;
+  const void* z = nullptr; int64_t ldz = 0;
+  const float* t = nullptr; int64_t ldt = 0;
+  void* dz = nullptr; int64_t lddz = 0;
+  float* loss_rows = nullptr;
+  float grad_scale = 0.f;
+};
+int mse_plan(const MseOp& op, LaunchRec* rec, char* err, size_t errlen);
+
+// loss = sum(loss_rows) / count in a fixed order (count = B when 0);
+// optionally bumps the step counter and latches a non-finite loss into the
+// error word.
 struct LossMeanOp {
   int64_t B = 0;
+  double count = 0;
   const float* loss_rows = nullptr;
   float* loss = nullptr;
   int64_t* step_counter = nullptr;   // nullable
@@ -165,6 +181,9 @@ struct HeadOp {
   const void* W = nullptr;              // [C, K], row pitch K
   const float* bias = nullptr;
   const int32_t* labels = nullptr;
+  // MSE instead of softmax CE when set: fp32 targets [B, C] (row pitch ldt);
+  // dz = (z - t) * grad_scale, loss partials are sums of (z - t)^2
+  const float* targets = nullptr; int64_t ldt = 0;
   const void* aux = nullptr; int64_t ld_aux = 0;
   void* dY = nullptr; int64_t ldy = 0;
   int64_t* step_counter = nullptr;

@@ -276,10 +276,108 @@ int ce_plan(const CeOp& op, LaunchRec* rec, char* err, size_t errlen) {
 }
 
 // ---------------------------------------------------------------------------
-// Batch-mean loss (fixed-order, fp64 partial sums), step counter, finiteness.
+// Squared error against real targets (the MSE loss):
+//   d = z - t;  loss_rows[i] = sum_j d_ij^2;  dz = d * grad_scale.
+// One warp per row: lanes stride over the row (4 elements a lane when rows
+// are 16-byte aligned), the row sum by a warp tree.
+// ---------------------------------------------------------------------------
+struct MseParams {
+  const void* z; int64_t ldz;
+  const float* t; int64_t ldt;
+  void* dz; int64_t lddz;
+  float* loss_rows;
+  int B, C;
+  float grad_scale;
+};
+
+template <typename T>
+__device__ __forceinline__ void load4(const T* src, float* v) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  } else {
+    const uint2 a = *reinterpret_cast<const uint2*>(src);
+    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&a.x);
+    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&a.y);
+    v[0] = __low2float(lo); v[1] = __high2float(lo); v[2] = __low2float(hi); v[3] = __high2float(hi);
+  }
+}
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, const float* v) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&lo);
+    o.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = o;
+  }
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256) mse_kernel(const __grid_constant__ MseParams p) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= p.B) return;
+  const T* zr = reinterpret_cast<const T*>(p.z) + (int64_t)row * p.ldz;
+  const float* tr = p.t + (int64_t)row * p.ldt;
+  T* dr = reinterpret_cast<T*>(p.dz) + (int64_t)row * p.lddz;
+  float s = 0.f;
+  if (VEC) {
+    for (int j = 4 * lane; j < p.C; j += 128) {
+      float zv[4], d[4];
+      load4<T>(zr + j, zv);
+      const float4 tv = __ldcs(reinterpret_cast<const float4*>(tr + j));
+      d[0] = zv[0] - tv.x; d[1] = zv[1] - tv.y; d[2] = zv[2] - tv.z; d[3] = zv[3] - tv.w;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        s += d[k] * d[k];
+        d[k] *= p.grad_scale;
+      }
+      store4<T>(dr + j, d);
+    }
+  } else {
+    for (int j = lane; j < p.C; j += 32) {
+      const float d = to_f32(zr[j]) - tr[j];
+      s += d * d;
+      dr[j] = from_f32<T>(d * p.grad_scale);
+    }
+  }
+  s = warp_sum(s);
+  if (lane == 0) p.loss_rows[row] = s;
+}
+
+int mse_plan(const MseOp& op, LaunchRec* rec, char* err, size_t errlen) {
+  if (op.B <= 0 || op.C <= 0 || op.B > INT32_MAX || op.C > INT32_MAX || op.ldz < op.C || op.ldt < op.C ||
+      op.lddz < op.C) {
+    snprintf(err, errlen, "mse: bad shape B=%lld C=%lld", (long long)op.B, (long long)op.C);
+    return -1;
+  }
+  if (!op.z || !op.t || !op.dz || !op.loss_rows) { snprintf(err, errlen, "mse: null pointer"); return -1; }
+  MseParams q{op.z, op.ldz, op.t, op.ldt, op.dz, op.lddz, op.loss_rows, (int)op.B, (int)op.C, op.grad_scale};
+  const size_t es = op.dtype == DT_F32 ? 4 : 2;
+  const bool vec = op.C % 4 == 0 && op.ldz % 4 == 0 && op.ldt % 4 == 0 && op.lddz % 4 == 0 &&
+                   (uintptr_t)op.t % 16 == 0 && (uintptr_t)op.z % (4 * es) == 0 && (uintptr_t)op.dz % (4 * es) == 0;
+  if (op.dtype == DT_F32)
+    rec->func = vec ? (const void*)mse_kernel<float, true> : (const void*)mse_kernel<float, false>;
+  else
+    rec->func = vec ? (const void*)mse_kernel<__nv_bfloat16, true> : (const void*)mse_kernel<__nv_bfloat16, false>;
+  rec->grid = dim3((unsigned)ceil_div(op.B, 8));
+  rec->block = dim3(256);
+  rec->smem = 0;
+  rec->name = "mse";
+  rec->set_args(q);
+  return 1;
+}
+
+// ---------------------------------------------------------------------------
+// Mean of the row losses (fixed-order fp32 sums), step counter, finiteness.
 // ---------------------------------------------------------------------------
 struct LossMeanParams {
-  const float* loss_rows; int64_t B;
+  const float* loss_rows; int64_t B; float count;
   float* loss;
   int64_t* step_counter;
   uint32_t* err;
@@ -302,7 +400,7 @@ __global__ void __launch_bounds__(1024) loss_mean_kernel(const __grid_constant__
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    float L = red[0] / (float)p.B;
+    float L = red[0] / p.count;
     if (p.loss) *p.loss = L;
     if (p.step_counter) advance_step(p.step_counter, p.bias_corr, p.beta1, p.beta2);
     if (p.err && !isfinite(L)) atomicOr(p.err, ERRBIT_NONFINITE);
@@ -311,7 +409,8 @@ __global__ void __launch_bounds__(1024) loss_mean_kernel(const __grid_constant__
 
 int loss_mean_plan(const LossMeanOp& op, LaunchRec* rec, char* err, size_t errlen) {
   if (op.B <= 0) { snprintf(err, errlen, "loss_mean: empty batch"); return -1; }
-  LossMeanParams q{op.loss_rows, op.B, op.loss, op.step_counter, op.err, op.bias_corr, op.beta1, op.beta2};
+  LossMeanParams q{op.loss_rows, op.B, (float)(op.count > 0 ? op.count : (double)op.B), op.loss,
+                   op.step_counter, op.err, op.bias_corr, op.beta1, op.beta2};
   rec->func = (const void*)loss_mean_kernel;
   rec->grid = dim3(1);
   rec->block = dim3(1024);

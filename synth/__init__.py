@@ -157,3 +157,11 @@ def make_normal(shape: Sequence[int], std: float, *key: int,
 
 def make_labels(n: int, C: int, *key: int) -> torch.Tensor:
     return torch.from_numpy(_rng(*key).integers(0, C, size=(n,), dtype=np.int32))
+
+
+def make_targets(w: Workload, step: int, batch: Optional[int] = None) -> torch.Tensor:
+    """Regression targets of batch `step` for an MSE step: float32 [B, C],
+    standard normal (the real-valued outputs MuNet's "Python training"
+    example fits with mse_loss; the pages fix no distribution)."""
+    B = w.batch if batch is None else batch
+    return torch.from_numpy(_rng(w.seed, 3, step).standard_normal((B, w.n_classes), dtype=np.float32))

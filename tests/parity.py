@@ -107,7 +107,7 @@ def perturbed_products(seed: int):
     input_grad, bias_grad) is multiplied elementwise by (1 + eta r),
     r ~ U(-1, 1), eta = sqrt(K) 2^-24 for a reduction over K terms."""
     rng = np.random.default_rng(seed)
-    orig = (om.linear, om.weight_grad, om.input_grad, om.bias_grad, om.softmax_ce, om.update, om.clip_coef)
+    orig = (om.linear, om.weight_grad, om.input_grad, om.bias_grad, om.softmax_ce, om.update, om.clip_coef, om.mse)
 
     def rel(a, e):
         return a * (1.0 + e * rng.uniform(-1.0, 1.0, np.shape(a)))
@@ -127,9 +127,15 @@ def perturbed_products(seed: int):
         c = orig[6](grads, max_norm)
         return c if c == 1.0 else rel(c, 2.0 ** -20)
 
+    def mse(z, t):
+        # fp32 difference, square and row sum; dz scaled in fp32
+        r_, dz_ = orig[7](z, t)
+        return rel(r_, 2.0 ** -22), rel(dz_, 2.0 ** -22)
+
     om.softmax_ce = ce
     om.update = update
     om.clip_coef = clip_coef
+    om.mse = mse
 
     def noisy(a, absum, K):
         # fp32 accumulation error scales with the sum of |terms|, not with
@@ -144,23 +150,25 @@ def perturbed_products(seed: int):
     try:
         yield
     finally:
-        om.linear, om.weight_grad, om.input_grad, om.bias_grad, om.softmax_ce, om.update, om.clip_coef = orig
+        (om.linear, om.weight_grad, om.input_grad, om.bias_grad, om.softmax_ce, om.update, om.clip_coef,
+         om.mse) = orig
 
 
 def oracle_run(w: synth.Workload, params0, bl, mode: str, perturb_seed: int = 0, optim: str = "adamw",
-               max_norm: float = 0.0):
-    """(losses, params, m, v, first-step grads) of len(bl) steps from params0."""
+               max_norm: float = 0.0, loss: str = "ce"):
+    """(losses, params, m, v, first-step grads) of len(bl) steps from params0.
+    bl holds (x, labels) pairs, or (x, fp32 targets) for loss="mse"."""
     hyper = hyper32(w)
-    xs = [(to64(x), y.numpy().astype(np.int64)) for x, y in bl]
+    xs = [(to64(x), to64(y) if loss == "mse" else y.numpy().astype(np.int64)) for x, y in bl]
     p0 = [to64(p) for p in params0]
-    kw = dict(mode=mode, optim=optim, max_norm=float(np.float32(max_norm)))
+    kw = dict(mode=mode, optim=optim, max_norm=float(np.float32(max_norm)), loss=loss)
     if perturb_seed:
         with perturbed_products(perturb_seed):
             return om.run_steps(p0, w.acts, xs, hyper, **kw)
     return om.run_steps(p0, w.acts, xs, hyper, **kw)
 
 
-def oracle_abs_sums(w: synth.Workload, params0, x, y, mode: str) -> List[np.ndarray]:
+def oracle_abs_sums(w: synth.Workload, params0, x, y, mode: str, loss: str = "ce") -> List[np.ndarray]:
     """kappa for every first-step gradient element (a running error bound).
 
     Forward on absolute values, F_0 = |x|, F_l = (F_{l-1} |W_l|^T + |b_l|) *
@@ -170,10 +178,15 @@ def oracle_abs_sums(w: synth.Workload, params0, x, y, mode: str) -> List[np.ndar
     2 p_ij u max_k F_L[i, k] in p_ij.  Backward on absolute values,
     A_L = |dz| + 2 p max_k F_L / B, A_{l-1} = (A_l |W_l|) * |act'|.  Then
     kappa_W = A_l^T F_{l-1} and kappa_b = sum_rows A_l bound every product
-    that feeds the gradient, including those that cancel inside dY or X."""
+    that feeds the gradient, including those that cancel inside dY or X.
+    For MSE, dz = 2 (z - t) / (B C) moves by 2 u F_L / (B C) under the same
+    logit error, so A_L = |dz| + 2 F_L / (B C)."""
     p0 = [to64(p) for p in params0]
     fw = om.forward(p0, to64(x), w.acts, mode)
-    _, dz = om.softmax_ce(fw["z"], y.numpy().astype(np.int64))
+    if loss == "mse":
+        _, dz = om.mse(fw["z"], to64(y))
+    else:
+        _, dz = om.softmax_ce(fw["z"], y.numpy().astype(np.int64))
     L = w.n_layers
 
     def dact(l):   # |act'| of hidden layer l's pre-activation
@@ -189,10 +202,13 @@ def oracle_abs_sums(w: synth.Workload, params0, x, y, mode: str) -> List[np.ndar
         Fl = F[-1] @ np.abs(fw["W"][l]).T + np.abs(p0[2 * l + 1])
         F.append(Fl * dact(l) if l < L - 1 else Fl)
     B = dz.shape[0]
-    pz = dz * B                                   # softmax probabilities p
-    pz[np.arange(B), y.numpy().astype(np.int64)] += 1.0
     out = [None] * (2 * L)
-    A = np.abs(dz) + 2.0 * pz * F[L].max(axis=1, keepdims=True) / B
+    if loss == "mse":
+        A = np.abs(dz) + 2.0 * F[L] / dz.size
+    else:
+        pz = dz * B                                   # softmax probabilities p
+        pz[np.arange(B), y.numpy().astype(np.int64)] += 1.0
+        A = np.abs(dz) + 2.0 * pz * F[L].max(axis=1, keepdims=True) / B
     for l in range(L - 1, -1, -1):
         X = F[l]
         out[2 * l] = A.T @ X
