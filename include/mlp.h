@@ -168,7 +168,21 @@ mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
  *     memory) and then waits for that kernel to complete before touching
  *     global memory.  0 chains the kernels with full dependencies.  Results
  *     are identical either way. */
-enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2, MLP_OPT_PDL = 3 };
+/*   MLP_OPT_CE_GEMM (default 0; MLP_BF16 models with at least 1024 classes):
+ *     softmax-CE inside the output layer's GEMMs.  The forward GEMM's
+ *     epilogue leaves each row's (max, sum of exponentials) over every
+ *     128-column group of the stored logits and the label's logit; a row
+ *     kernel combines them into the row's (max, 1 / sum) and loss; the
+ *     layer's dgrad and wgrad read the logits and form dz = (softmax -
+ *     onehot) / B in shared memory on the way into the tensor cores, so dz
+ *     is never stored (the single logits read of devpost "Orthon", "Selected
+ *     Orthon vs. PyTorch results", taken into the GEMMs).  0 runs the
+ *     separate softmax-CE pass (the default: on GB300 the in-GEMM dz costs
+ *     more than the pass, since every logit feeds several output tiles of
+ *     the dgrad and of the wgrad and its exponential is recomputed for each).
+ *     Same rounding points either way (logits and dz rounded to bf16); the
+ *     sums differ in order only. */
+enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2, MLP_OPT_PDL = 3, MLP_OPT_CE_GEMM = 4 };
 mlp_status mlp_set_option(mlp_t* model, int option, int64_t value);
 
 /* The update rule of the training step (default MLP_OPTIM_ADAMW) and global

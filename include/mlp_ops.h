@@ -109,6 +109,26 @@ mlp_status mlp_op_softmax_ce(int dtype, int64_t B, int64_t C, const void* z, int
 mlp_status mlp_op_mse(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, const float* t, int64_t ldt,
                       float grad_scale, void* dz, int64_t lddz, float* loss_rows, void* stream);
 
+/* A bf16 output layer fused with softmax cross-entropy, its VJPs included
+ * (the softmax-CE-in-GEMM path of MLP_OPT_CE_GEMM): for h [B, K] (ldh, bf16),
+ * W [C, K] (bf16, row pitch K), bias [C] (fp32) and labels int32 [B]:
+ *   z = h W^T + bias, stored bf16 in z [B, C] (ldz);
+ *   loss_rows[i] = logsumexp(z_i) - z_i[y_i] (fp32, from the stored logits);
+ *   dX = (dz W) * act'(aux) [B, K] (ldx, bf16; act of the layer below: aux is
+ *     its stored h for ReLU, u for GELU; MLP_ACT_NONE: aux unused), and
+ *   dW = dz^T h (fp32 [C, K], lddw), db = sum_rows dz (fp32 [C]),
+ * with dz = (softmax(z) - onehot(y)) / B formed on the fly from the stored
+ * logits and never written.  C > 128; K and the pitches multiples of 8; ws
+ * (device, 16-byte aligned) of mlp_op_linear_ce_workspace_bytes(B, C, K)
+ * bytes.  Launches the forward GEMM, the statistics combine, the dgrad and
+ * the wgrad (+ its split-K reduce).  A label outside [0, C) sets the error
+ * bit in err_dev (its loss row is 0). */
+size_t mlp_op_linear_ce_workspace_bytes(int64_t B, int64_t C, int64_t K);
+mlp_status mlp_op_linear_ce(int64_t B, int64_t C, int64_t K, const void* h, int64_t ldh, const void* W,
+                            const float* bias, const int32_t* labels, int act, const void* aux, int64_t ld_aux,
+                            void* z, int64_t ldz, float* loss_rows, void* dX, int64_t ldx, float* dW, int64_t lddw,
+                            float* db, void* ws, size_t ws_bytes, uint32_t* err_dev, void* stream);
+
 /* loss = mean(loss_rows[0..B)) summed in a fixed order (device float). */
 mlp_status mlp_op_loss_mean(int64_t B, const float* loss_rows, float* loss, uint32_t* err_dev, void* stream);
 

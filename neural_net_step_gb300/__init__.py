@@ -67,6 +67,9 @@ _SIGS = {
     "mlp_op_wgrad_noalloc": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
     "mlp_op_split3": (_I32, [_I64, _I64, _P, _I64, _P, _I64, _P]),
     "mlp_op_softmax_ce": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _F, _P, _I64, _P, _P, _P]),
+    "mlp_op_linear_ce_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "mlp_op_linear_ce": (_I32, [_I64, _I64, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I64, _P, _I64, _P, _P, _I64, _P,
+                                _I64, _P, _P, _SZ, _P, _P]),
     "mlp_op_mse": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _I64, _F, _P, _I64, _P, _P]),
     "mlp_op_loss_mean": (_I32, [_I64, _P, _P, _P, _P]),
     "mlp_op_adamw": (_I32, [_I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _P]),
@@ -145,7 +148,7 @@ def mlp_set_graph_mode(h, enable: bool) -> None:
     _check(lib().mlp_set_graph_mode(h, int(bool(enable))))
 
 
-OPT_GRAPH, OPT_FUSE_HEAD, OPT_F32_TENSOR_CORES, OPT_PDL = 0, 1, 2, 3
+OPT_GRAPH, OPT_FUSE_HEAD, OPT_F32_TENSOR_CORES, OPT_PDL, OPT_CE_GEMM = 0, 1, 2, 3, 4
 
 
 def mlp_set_option(h, option: int, value: int) -> None:
@@ -235,6 +238,16 @@ def mlp_op_split3(rows, cols, X, ldx, P, ldp, stream) -> None:
 
 def mlp_op_softmax_ce(dtype, B, C, z, ldz, labels, grad_scale, dz, lddz, loss_rows, err, stream) -> None:
     _check(lib().mlp_op_softmax_ce(dtype, B, C, z, ldz, labels, grad_scale, dz, lddz, loss_rows, err, stream))
+
+
+def mlp_op_linear_ce_workspace_bytes(B, C, K) -> int:
+    return lib().mlp_op_linear_ce_workspace_bytes(B, C, K)
+
+
+def mlp_op_linear_ce(B, C, K, h, ldh, W, bias, labels, act, aux, ld_aux, z, ldz, loss_rows, dX, ldx, dW, lddw, db,
+                     ws, ws_bytes, err, stream) -> None:
+    _check(lib().mlp_op_linear_ce(B, C, K, h, ldh, W, bias, labels, act, aux, ld_aux, z, ldz, loss_rows, dX, ldx,
+                                  dW, lddw, db, ws, ws_bytes, err, stream))
 
 
 def mlp_op_mse(dtype, B, C, z, ldz, t, ldt, grad_scale, dz, lddz, loss_rows, stream) -> None:

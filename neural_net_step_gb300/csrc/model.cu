@@ -93,8 +93,15 @@ struct Layout {
   size_t off_xin[2] = {0, 0}, off_yin[2] = {0, 0};   // device inputs of mlp_train_step_host (two slots)
   size_t yin_bytes = 0;   // labels, or MSE targets where B * C * 4 <= 64 MiB
   size_t off_norm = 0;   // per-block sums of squares of the gradient (clipping)
+  // softmax-CE fused around a wide bf16 output layer: per-row, per-128-column
+  // (max, sum) partials, the label logits, and the rows' (max, 1 / sum)
+  size_t off_cest = 0, off_cezy = 0, off_cerow = 0;
   size_t total = 0;
 };
+
+// Output layers at least this wide (bf16) take softmax-CE inside their GEMMs
+// instead of a separate pass over the logits.
+constexpr int64_t kCeGemmMinClasses = 1024;
 
 struct Ctl {   // control block at off_ctl
   int64_t step;
@@ -208,6 +215,11 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     L.off_yin[k] = take(L.yin_bytes);
   }
   L.off_norm = take(AdamWOp::kNormParts * sizeof(float));
+  if (dtype == MLP_BF16 && dims[L.L] >= kCeGemmMinClasses) {
+    L.off_cest = take(batch * ce_groups(dims[L.L]) * 8);
+    L.off_cezy = take(batch * 4);
+    L.off_cerow = take(batch * 8);
+  }
   L.off_ctl = take(sizeof(Ctl));
   L.total = cur;
   return MLP_OK;
@@ -257,6 +269,7 @@ struct mlp {
   bool pdl = true;           // graph edges let each kernel launch before its predecessor ends
   int optim = MLP_OPTIM_ADAMW;
   int loss = MLP_LOSS_CE;
+  bool ce_gemm = false;      // softmax-CE inside the GEMMs of a wide bf16 output layer (slower on this part)
   float max_grad_norm = 0.f; // > 0: global-norm clipping of the gradient before the update
   std::mutex mu;
   std::vector<GraphCache> graphs;
@@ -321,7 +334,7 @@ mlp_status add(std::vector<LaunchRec>& out, int n, const LaunchRec* recs) {
 // z buffer).  x3: fp32 model with operands as bf16 planes (the input is
 // split into the arena's xs planes first; hidden outputs are planes).
 mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out, int n_layers = -1,
-                        bool x3 = false) {
+                        bool x3 = false, const int32_t* ce_labels = nullptr) {
   const Layout& L = m->lay;
   const void* X = x;
   int64_t ldx = L.dims[0], xplane = 0;
@@ -353,6 +366,9 @@ mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out
     } else {
       op.act = MLP_ACT_NONE;
       op.out = m->at(L.off_z); op.ldo = L.ldz;
+      if (ce_labels) {   // softmax-CE statistics from the logits' epilogue
+        op.ce_stats = (float2*)m->at(L.off_cest); op.ce_zy = (float*)m->at(L.off_cezy); op.ce_labels = ce_labels;
+      }
     }
     PLAN_TRY(gemm_plan(op, r_, e_, sizeof(e_)));
   }
@@ -367,8 +383,11 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
   const bool mse = m->loss == MLP_LOSS_MSE;
   const bool fuse = m->fuse_head && L.L >= 2 && head_supported(L.dims[L.L], L.dims[L.L - 1]);
   const bool x3 = m->x3();   // implies fuse
+  // a wide bf16 output layer: softmax-CE inside its GEMMs (statistics from the
+  // forward's epilogue, dz formed from the stored logits by dgrad and wgrad)
+  const bool ce_gemm = !mse && !fuse && m->ce_gemm && L.dtype == MLP_BF16 && L.dims[L.L] >= kCeGemmMinClasses;
   const int64_t dy_plane = L.B * L.max_ld;
-  mlp_status st = plan_forward(m, x, out, fuse ? L.L - 1 : L.L, x3);
+  mlp_status st = plan_forward(m, x, out, fuse ? L.L - 1 : L.L, x3, ce_gemm ? (const int32_t*)y : nullptr);
   if (st != MLP_OK) return st;
   Ctl* ctl = m->ctl();
   const void* dY = m->at(L.off_dz);
@@ -410,7 +429,15 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     char e_[512] = "";
     LaunchRec r;
     float* loss_rows = (float*)m->at(L.off_loss_rows);
-    if (mse) {
+    if (ce_gemm) {
+      CeCombineOp cc;
+      cc.B = L.B; cc.C = L.dims[L.L];
+      cc.stats = (const float2*)m->at(L.off_cest); cc.zy = (const float*)m->at(L.off_cezy);
+      cc.labels = (const int32_t*)y;
+      cc.rowstat = (float2*)m->at(L.off_cerow); cc.loss_rows = loss_rows; cc.err = &ctl->err;
+      if (ce_combine_plan(cc, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+      dY = m->at(L.off_z);   // the top layer's VJPs read the logits and form dz themselves
+    } else if (mse) {
       MseOp op;
       op.dtype = L.dtype; op.B = L.B; op.C = L.dims[L.L];
       op.z = m->at(L.off_z); op.ldz = L.ldz;
@@ -462,6 +489,11 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     wg.db = G + L.boff[l];
     wg.ws = L.wws_bytes[l] ? (float*)m->at(L.off_wws[l]) : nullptr; wg.ws_bytes = L.wws_bytes[l];
     wg.err = &ctl->err;
+    const bool ce_top = ce_gemm && l == L.L - 1;
+    if (ce_top) {
+      wg.ce_rowstat = (const float2*)m->at(L.off_cerow); wg.ce_labels = (const int32_t*)y;
+      wg.ce_scale = (float)(1.0 / (double)L.B);
+    }
     // split-K partials go to the optimizer (it reads them 4 at a time)
     const int64_t MN = wg.M * wg.N;
     int used = 0;
@@ -493,6 +525,9 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
       dg.ld_aux = L.ld_h[l - 1];
       dg.out = m->at(L.off_dy[buf]); dg.ldo = L.ld_h[l - 1];
       dg.err = &ctl->err;
+      if (ce_top) {
+        dg.ce_rowstat = wg.ce_rowstat; dg.ce_labels = wg.ce_labels; dg.ce_scale = wg.ce_scale;
+      }
       PLAN_TRY(gemm_plan(dg, r_, e_, sizeof(e_)));
       const int d[2] = {main_tail, side_prev};
       out.back().depend_on(d, 2);
@@ -777,6 +812,7 @@ mlp_status mlp_set_option(mlp_t* m, int option, int64_t value) {
     case MLP_OPT_FUSE_HEAD: m->fuse_head = value != 0; break;
     case MLP_OPT_F32_TENSOR_CORES: m->f32_tc = value != 0; break;
     case MLP_OPT_PDL: m->pdl = value != 0; break;
+    case MLP_OPT_CE_GEMM: m->ce_gemm = value != 0; break;
     default: return fail(MLP_ERR_ARG, "unknown option %d", option);
   }
   if (option == MLP_OPT_FUSE_HEAD || option == MLP_OPT_F32_TENSOR_CORES) {   // planes kept current only while used
@@ -1125,6 +1161,83 @@ mlp_status mlp_op_mse(int dtype, int64_t B, int64_t C, const void* z, int64_t ld
   char e_[512] = "";
   if (mse_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
   return run_ops(&r, 1, stream);
+}
+
+static size_t ce_ws_layout(int64_t B, int64_t C, int64_t K, size_t* off_zy, size_t* off_row, size_t* off_split) {
+  auto al = [](size_t v) { return (v + 255) / 256 * 256; };
+  size_t o = al((size_t)B * ce_groups(C) * 8);
+  *off_zy = o;
+  o = al(o + (size_t)B * 4);
+  *off_row = o;
+  o = al(o + (size_t)B * 8);
+  *off_split = o;
+  return o + wgrad_workspace_bytes(DT_BF16, C, K, B, wgrad_splits(DT_BF16, C, K, B));
+}
+
+size_t mlp_op_linear_ce_workspace_bytes(int64_t B, int64_t C, int64_t K) {
+  if (B < 1 || C < 1 || K < 1) return 0;
+  size_t a, b, c;
+  return ce_ws_layout(B, C, K, &a, &b, &c);
+}
+
+mlp_status mlp_op_linear_ce(int64_t B, int64_t C, int64_t K, const void* h, int64_t ldh, const void* W,
+                            const float* bias, const int32_t* labels, int act, const void* aux, int64_t ld_aux,
+                            void* z, int64_t ldz, float* loss_rows, void* dX, int64_t ldx, float* dW, int64_t lddw,
+                            float* db, void* ws, size_t ws_bytes, uint32_t* err_dev, void* stream) {
+  if (!h || !W || !bias || !labels || !z || !loss_rows || !dX || !dW || !db || !ws)
+    return fail(MLP_ERR_ARG, "null pointer");
+  if (!act_ok(act) || (act != MLP_ACT_NONE && !aux)) return fail(MLP_ERR_ARG, "bad activation or aux");
+  if (B < 1 || C <= 128 || K < 1 || ldh < K || ldz < C || ldx < K || lddw < K || (act != MLP_ACT_NONE && ld_aux < K))
+    return fail(MLP_ERR_SHAPE, "bad shape (C must exceed 128)");
+  size_t off_zy, off_row, off_split;
+  const size_t need = ce_ws_layout(B, C, K, &off_zy, &off_row, &off_split);
+  if (ws_bytes < need || (uintptr_t)ws % 16) return fail(MLP_ERR_ARG, "workspace too small or misaligned");
+  uint8_t* w8 = (uint8_t*)ws;
+  float2* stats = (float2*)w8;
+  float* zy = (float*)(w8 + off_zy);
+  float2* rowstat = (float2*)(w8 + off_row);
+  LaunchRec r[8];
+  int n = 0;
+  char e_[512] = "";
+  GemmOp f;
+  f.dtype = DT_BF16; f.kind = GEMM_FWD; f.act = MLP_ACT_NONE;
+  f.M = B; f.N = C; f.K = K;
+  f.A = h; f.lda = ldh; f.a_kmajor = true;
+  f.B = W; f.ldb = K; f.b_kmajor = true;
+  f.bias = bias; f.out = z; f.ldo = ldz; f.err = err_dev;
+  f.ce_stats = stats; f.ce_zy = zy; f.ce_labels = labels;
+  int k = gemm_plan(f, r + n, e_, sizeof(e_));
+  if (k < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  n += k;
+  CeCombineOp cc;
+  cc.B = B; cc.C = C; cc.stats = stats; cc.zy = zy; cc.labels = labels; cc.rowstat = rowstat;
+  cc.loss_rows = loss_rows; cc.err = err_dev;
+  if (ce_combine_plan(cc, r + n, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  ++n;
+  GemmOp d;
+  d.dtype = DT_BF16; d.kind = GEMM_DGRAD; d.act = act;
+  d.M = B; d.N = K; d.K = C;
+  d.A = z; d.lda = ldz; d.a_kmajor = true;
+  d.B = W; d.ldb = K; d.b_kmajor = false;
+  d.aux = aux; d.ld_aux = ld_aux;
+  d.out = dX; d.ldo = ldx; d.err = err_dev;
+  d.ce_rowstat = rowstat; d.ce_labels = labels; d.ce_scale = (float)(1.0 / (double)B);
+  k = gemm_plan(d, r + n, e_, sizeof(e_));
+  if (k < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  n += k;
+  GemmOp g;
+  g.dtype = DT_BF16; g.kind = GEMM_WGRAD;
+  g.M = C; g.N = K; g.K = B;
+  g.A = z; g.lda = ldz; g.a_kmajor = false;
+  g.B = h; g.ldb = ldh; g.b_kmajor = false;
+  g.dW = dW; g.ld_dw = lddw; g.db = db;
+  g.ws = (float*)(w8 + off_split); g.ws_bytes = ws_bytes - off_split;
+  g.err = err_dev;
+  g.ce_rowstat = rowstat; g.ce_labels = labels; g.ce_scale = d.ce_scale;
+  k = gemm_plan(g, r + n, e_, sizeof(e_));
+  if (k < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+  n += k;
+  return run_ops(r, n, stream);
 }
 
 mlp_status mlp_op_loss_mean(int64_t B, const float* loss_rows, float* loss, uint32_t* err_dev, void* stream) {

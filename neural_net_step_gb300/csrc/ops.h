@@ -49,6 +49,19 @@ struct GemmOp {
   // reduce kernel; the number of splits used goes to *splits_out.
   bool defer_reduce = false;
   int* splits_out = nullptr;
+  // Softmax-CE around a bf16 output layer (tensor cores):
+  //   GEMM_FWD with ce_stats: besides the logits (stored bf16), each row's
+  //     (max, sum exp(z - max)) over every 128-column group of the stored
+  //     logits goes to ce_stats [M][ceil(N / 128)] (float2), and the logit at
+  //     ce_labels[row] to ce_zy [M].
+  //   GEMM_DGRAD (A = z, K-major) / GEMM_WGRAD (A = z as [K rows, M]) with
+  //     ce_rowstat: the operand is dz = (exp(z - M_r) invS_r - [c == y_r])
+  //     ce_scale, formed from the stored logits in shared memory;
+  //     (M_r, invS_r) = ce_rowstat[r] for batch row r.
+  float2* ce_stats = nullptr; float* ce_zy = nullptr;
+  const float2* ce_rowstat = nullptr;
+  const int32_t* ce_labels = nullptr;
+  float ce_scale = 0.f;
 };
 
 // Number of K splits the wgrad of this shape uses, and the workspace bytes.
@@ -87,6 +100,18 @@ struct MseOp {
   float grad_scale = 0.f;
 };
 int mse_plan(const MseOp& op, LaunchRec* rec, char* err, size_t errlen);
+
+// Softmax-CE row statistics from the per-group partials of the forward
+// GEMM: M_r = max_g m_rg, S_r = sum_g s_rg exp(m_rg - M_r) (fixed order);
+// rowstat[r] = (M_r, 1 / S_r), loss_rows[r] = M_r + log S_r - zy[r]; a label
+// outside [0, C) sets the error bit (loss 0).
+struct CeCombineOp {
+  int64_t B = 0, C = 0;
+  const float2* stats = nullptr; const float* zy = nullptr; const int32_t* labels = nullptr;
+  float2* rowstat = nullptr; float* loss_rows = nullptr; uint32_t* err = nullptr;
+};
+int ce_combine_plan(const CeCombineOp& op, LaunchRec* rec, char* err, size_t errlen);
+inline int64_t ce_groups(int64_t C) { return (C + 127) / 128; }
 
 // loss = sum(loss_rows) / count in a fixed order (count = B when 0);
 // optionally bumps the step counter and latches a non-finite loss into the

@@ -165,17 +165,27 @@ __global__ void __launch_bounds__(256) ce_row2_kernel(const __grid_constant__ Ce
   const int row = blockIdx.x;
   const int nvec = p.C / E;
   const uint4* zr = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.z) + (int64_t)row * p.ldz);
+  // four 16-byte loads in flight per thread (one is not enough to cover HBM
+  // latency at this occupancy), consumed in index order
+  constexpr int U = 4;
   float m = -INFINITY, s = 0.f;
-  for (int vi = threadIdx.x; vi < nvec; vi += 256) {
-    const uint4 raw = zr[vi];   // kept in L2 for the second pass
-    const T* e = reinterpret_cast<const T*>(&raw);
-    float vmax = -INFINITY;
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += 256 * U) {
+    uint4 raw[U];
 #pragma unroll
-    for (int k = 0; k < E; ++k) vmax = fmaxf(vmax, to_f32(e[k]));
-    float vs = 0.f;
+    for (int u = 0; u < U; ++u)
+      if (v0 + 256 * u < nvec) raw[u] = zr[v0 + 256 * u];   // kept in L2 for the second pass
 #pragma unroll
-    for (int k = 0; k < E; ++k) vs += __expf(to_f32(e[k]) - vmax);
-    ms_combine<T>(m, s, vmax, vs);
+    for (int u = 0; u < U; ++u) {
+      if (v0 + 256 * u >= nvec) break;
+      const T* e = reinterpret_cast<const T*>(&raw[u]);
+      float vmax = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < E; ++k) vmax = fmaxf(vmax, to_f32(e[k]));
+      float vs = 0.f;
+#pragma unroll
+      for (int k = 0; k < E; ++k) vs += __expf(to_f32(e[k]) - vmax);
+      ms_combine<T>(m, s, vmax, vs);
+    }
   }
   // combine (max, sum) across the CTA in a fixed order
 #pragma unroll
@@ -195,17 +205,25 @@ __global__ void __launch_bounds__(256) ce_row2_kernel(const __grid_constant__ Ce
   const bool bad = y < 0 || y >= p.C;
   const float inv_s = 1.0f / s;
   uint4* dr = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.dz) + (int64_t)row * p.lddz);
-  for (int vi = threadIdx.x; vi < nvec; vi += 256) {
-    const uint4 raw = __ldcs(zr + vi);
-    const T* e = reinterpret_cast<const T*>(&raw);
-    uint4 o;
-    T* oe = reinterpret_cast<T*>(&o);
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += 256 * U) {
+    uint4 raw[U];
 #pragma unroll
-    for (int k = 0; k < E; ++k) {
-      const int j = vi * E + k;
-      oe[k] = from_f32<T>((__expf(to_f32(e[k]) - m) * inv_s - (j == y ? 1.f : 0.f)) * p.grad_scale);
+    for (int u = 0; u < U; ++u)
+      if (v0 + 256 * u < nvec) raw[u] = __ldcs(zr + v0 + 256 * u);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = v0 + 256 * u;
+      if (vi >= nvec) break;
+      const T* e = reinterpret_cast<const T*>(&raw[u]);
+      uint4 o;
+      T* oe = reinterpret_cast<T*>(&o);
+#pragma unroll
+      for (int k = 0; k < E; ++k) {
+        const int j = vi * E + k;
+        oe[k] = from_f32<T>((__expf(to_f32(e[k]) - m) * inv_s - (j == y ? 1.f : 0.f)) * p.grad_scale);
+      }
+      __stcs(dr + vi, o);
     }
-    __stcs(dr + vi, o);
   }
   ce_finish_row<T>(p, row, y, m, s, bad, threadIdx.x);
 }
@@ -374,6 +392,57 @@ int mse_plan(const MseOp& op, LaunchRec* rec, char* err, size_t errlen) {
 }
 
 // ---------------------------------------------------------------------------
+// Softmax-CE row statistics from the forward GEMM's per-group partials (one
+// warp per row; lanes stride over the groups, then fixed warp trees).
+// ---------------------------------------------------------------------------
+struct CeCombineParams {
+  const float2* stats; const float* zy; const int32_t* labels;
+  float2* rowstat; float* loss_rows; uint32_t* err;
+  int B, C, G;
+};
+
+__global__ void __launch_bounds__(256) ce_combine_kernel(const __grid_constant__ CeCombineParams p) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= p.B) return;
+  const float2* st = p.stats + (int64_t)row * p.G;
+  float m = -INFINITY;
+  for (int g = lane; g < p.G; g += 32) m = fmaxf(m, st[g].x);
+  m = warp_max(m);
+  float s = 0.f;
+  for (int g = lane; g < p.G; g += 32) {
+    const float2 v = st[g];
+    s += v.y * __expf(v.x - m);
+  }
+  s = warp_sum(s);
+  if (lane == 0) {
+    const int y = p.labels[row];
+    const bool bad = y < 0 || y >= p.C;
+    p.rowstat[row] = make_float2(m, 1.0f / s);
+    p.loss_rows[row] = bad ? 0.f : (m + logf(s)) - p.zy[row];
+    if (bad && p.err) atomicOr(p.err, ERRBIT_LABEL_RANGE);
+  }
+}
+
+int ce_combine_plan(const CeCombineOp& op, LaunchRec* rec, char* err, size_t errlen) {
+  if (op.B <= 0 || op.C <= 0 || op.B > INT32_MAX || op.C > INT32_MAX || !op.stats || !op.zy || !op.labels ||
+      !op.rowstat || !op.loss_rows) {
+    snprintf(err, errlen, "ce_combine: bad arguments");
+    return -1;
+  }
+  CeCombineParams q{op.stats, op.zy, op.labels, op.rowstat, op.loss_rows, op.err, (int)op.B, (int)op.C,
+                    (int)ce_groups(op.C)};
+  rec->func = (const void*)ce_combine_kernel;
+  rec->grid = dim3((unsigned)ceil_div(op.B, 8));
+  rec->block = dim3(256);
+  rec->smem = 0;
+  rec->name = "ce_combine";
+  rec->set_args(q);
+  return 1;
+}
+
+// ---------------------------------------------------------------------------
 // Mean of the row losses (fixed-order fp32 sums), step counter, finiteness.
 // ---------------------------------------------------------------------------
 struct LossMeanParams {
@@ -392,6 +461,7 @@ __global__ void __launch_bounds__(1024) loss_mean_kernel(const __grid_constant__
   pdl_enter();
   __shared__ float red[1024];
   float s = 0.f;
+#pragma unroll 8   // loads in flight; the additions keep their order
   for (int64_t i = threadIdx.x; i < p.B; i += blockDim.x) s += p.loss_rows[i];
   red[threadIdx.x] = s;
   __syncthreads();

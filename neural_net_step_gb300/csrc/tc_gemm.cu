@@ -466,7 +466,36 @@ struct PParams {
   __nv_bfloat16* out_u; int64_t ldu;
   const __nv_bfloat16* aux; int64_t ld_aux;
   uint32_t* err;
+  // softmax-CE around the output layer (bf16, 256-wide tiles):
+  //   forward: each row's (max, sum exp(z - max)) over every 128-column group
+  //   of the stored logits -> ce_stats [M][ce_groups], z[row, label] -> ce_zy;
+  //   dgrad: A holds the logits z; dz = (exp(z - M_r) invS_r - [c == y_r])
+  //   ce_scale is formed in shared memory before the MMA reads the stage.
+  float2* ce_stats; float* ce_zy; int ce_groups;
+  const float2* ce_rowstat; const int32_t* ce_labels; float ce_scale;
 };
+
+// dz of softmax-CE from a stored logit: (exp(z - M) invS - onehot) scale, or 0
+// outside the batch rows / classes.
+__device__ __forceinline__ float ce_dz(float z, float M, float inv_s, bool hot, float scale, bool valid) {
+  return valid ? (__expf(z - M) * inv_s - (hot ? 1.f : 0.f)) * scale : 0.f;
+}
+
+// Eight bf16 logits of one 16-byte unit (classes c0 .. c0 + 7) turned into dz
+// in place.
+__device__ __forceinline__ void ce_unit(uint8_t* unit, int c0, int C, int y, float M, float inv_s, float scale,
+                                        bool row_ok) {
+  uint4 w = *reinterpret_cast<const uint4*>(unit);
+  __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const float2 z = __bfloat1622float2(w2[h]);
+    const int c = c0 + 2 * h;
+    w2[h] = __floats2bfloat162_rn(ce_dz(z.x, M, inv_s, c == y, scale, row_ok && c < C),
+                                  ce_dz(z.y, M, inv_s, c + 1 == y, scale, row_ok && c + 1 < C));
+  }
+  *reinterpret_cast<uint4*>(unit) = w;
+}
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v, int off) {
   uint32_t r[32];
@@ -576,14 +605,19 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
   auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * C::STAGES + b); };
   auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * C::STAGES + 2 + b); };
-  const uint32_t tmem_slot = bar_base + 8u * (2 * C::STAGES + 4);
+  // softmax-CE dgrad: stage s formed into dz by the epilogue warps
+  auto formed_bar = [&](int s) { return bar_base + 8u * (2 * C::STAGES + 4 + s); };
+  const uint32_t tmem_slot = bar_base + 8u * (3 * C::STAGES + 4);
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+  // the logits of a softmax-CE dgrad are turned into dz between TMA and MMA
+  const bool ce_a = !X3 && !PAIR && p.ce_rowstat != nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(formed_bar(s), P_EPI_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -667,7 +701,7 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
         for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-          if (!mbar_wait(full_bar(s), ph, p.err)) { ok = false; break; }
+          if (!mbar_wait(ce_a ? formed_bar(s) : full_bar(s), ph, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = a_base + s * C::A_BYTES;
           const uint32_t sb = b_base + s * C::B_BYTES;
@@ -709,17 +743,56 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
     const int half = (warp - 2) >> 2;
     const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * C::EPI_BUFS * 4096);
     uint8_t* stage0_ptr = base_ptr + (stage0 - base);
-    int tc = 0, chunk = 0;
+    int tc = 0, chunk = 0, it = 0;
     bool ok = true;
     for (int t = t0; t < p.num_tiles && ok; t += tstep, ++tc) {
       const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
       const int buf = tc & 1;
+      if (ce_a) {
+        // softmax-CE dgrad: every landed A stage (128 rows x 64 logits,
+        // 128B-swizzled) becomes dz in place before the MMA reads it; thread
+        // e takes row e / 2 and its 16-byte units 4 (e % 2) .. 4 (e % 2) + 3
+        const int e = threadIdx.x - 64;
+        const int r = e >> 1, hb = e & 1;
+        const int gr = m0 + r;
+        const bool rok = gr < p.M;
+        float2 st = make_float2(0.f, 0.f);
+        int y = -1;
+        if (rok) {
+          st = __ldg(p.ce_rowstat + gr);
+          y = __ldg(p.ce_labels + gr);
+        }
+        for (int kb = kb_lo; kb < kb_hi && ok; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          ok = __all_sync(0xffffffffu, mbar_wait(full_bar(s), (uint32_t)(it / C::STAGES) & 1u, p.err));
+          if (!ok) break;
+          uint8_t* row = base_ptr + (a_base - base) + s * C::A_BYTES + r * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            // logical unit j (columns 8 j .. 8 j + 7) sits at physical unit
+            // j ^ (r & 7): the eight lanes of a shared-memory phase hit eight
+            // different bank groups
+            const int j = 4 * hb + i;
+            ce_unit(row + 16 * (j ^ (r & 7)), kb * BK + 8 * j, p.K, y, st.x, st.y, p.ce_scale, rok);
+          }
+          fence_async_smem();   // the generic-proxy writes, visible to the tensor cores
+          __syncwarp();
+          if (lane == 0) mbar_arrive(formed_bar(s));
+        }
+        if (!ok) break;
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), ((uint32_t)tc >> 1) & 1u, p.err));
       if (!ok) break;
       tc_fence_after();
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::ACC_COLS);
       const int gm = m0 + q * 32 + lane;
       const bool row_ok = gm < p.M;
+      // softmax-CE forward: this row's label, and the running (max, sum) of
+      // its 128-column group (this warp's half of the 256-wide tile)
+      const bool ce_f = !X3 && !PAIR && p.ce_stats != nullptr;
+      int ce_y = -1;
+      if (ce_f && row_ok) ce_y = __ldg(p.ce_labels + gm);
+      float ce_m = -INFINITY, ce_s = 0.f;
       // 64-column chunks of this warp's half of the tile: read from TMEM once,
       // finished in registers, then each output plane is staged in
       // 128B-swizzled shared memory (16-byte unit u of row r at
@@ -798,6 +871,30 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
           }
 #pragma unroll
           for (int j = 0; j < 64; ++j) v[j] = apply_act(v[j], p.act);
+          if (ce_f) {
+            // the logits as stored (bf16): the chunk maximum folded into the
+            // group's running maximum, then the exponentials added; the
+            // label's logit is kept when it falls in this chunk
+            // (rounding v in place: the store below rounds it to the same value)
+            float mc = -INFINITY, zy = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+              if (gn0 + j < p.N) mc = fmaxf(mc, v[j]);
+              if (gn0 + j == ce_y) zy = v[j];
+            }
+            if (mc > ce_m) {
+              ce_s *= __expf(ce_m - mc);
+              ce_m = mc;
+            }
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if (gn0 + j < p.N) ce_s += __expf(v[j] - ce_m);
+            if (row_ok && ce_y >= gn0 && ce_y < gn0 + 64 && ce_y < p.N) p.ce_zy[gm] = zy;
+            const int gc0 = n0 + half * (BN / 2);   // first column of this warp's group (BN = 256)
+            if (c0 + 64 >= (half + 1) * (BN / 2) && row_ok && gc0 < p.N)
+              p.ce_stats[(int64_t)gm * p.ce_groups + gc0 / 128] = make_float2(ce_m, ce_s);
+          }
         } else if (p.act == ACT_RELU) {   // dgrad: dX * 1[h > 0]
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -1057,6 +1154,10 @@ struct WParams {
   uint32_t idesc, idesc_db;
   float* db_out;         // [splits][M] (nullable: no bias gradient)
   uint32_t* err;
+  // softmax-CE weight gradient (bf16): A^T holds the logits z [K rows
+  // (batch), M (classes)]; each stage is formed into dz in shared memory
+  // (dz = (exp(z - M_k) invS_k - [m == y_k]) ce_scale) before the MMA
+  const float2* ce_rowstat; const int32_t* ce_labels; float ce_scale;
 };
 
 __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
@@ -1087,8 +1188,10 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
   auto empty_bar = [&](int s) { return bar_base + 8u * (W_STAGES + s); };
   auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * W_STAGES + b); };
   auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * W_STAGES + 2 + b); };
-  const uint32_t tmem_slot = bar_base + 8u * (2 * W_STAGES + 4);
+  auto formed_bar = [&](int s) { return bar_base + 8u * (2 * W_STAGES + 4 + s); };
+  const uint32_t tmem_slot = bar_base + 8u * (3 * W_STAGES + 4);
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+  const bool ce_a = !X3 && p.ce_rowstat != nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   {   // the constant ones tile (bf16 1.0 = 0x3F80)
@@ -1100,6 +1203,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
     for (int s = 0; s < W_STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(formed_bar(s), P_EPI_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -1178,7 +1282,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % W_STAGES;
           const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
-          if (!mbar_wait(full_bar(s), ph, p.err)) { ok = false; break; }
+          if (!mbar_wait(ce_a ? formed_bar(s) : full_bar(s), ph, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = a_base + s * C::A_BYTES;
           const uint32_t sb = b_base + s * C::B_BYTES;
@@ -1215,11 +1319,42 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
     const int half = (warp - 2) >> 2;
     const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * W_EPI_BUFS * 4096);
     uint8_t* stage0_ptr = base_ptr + (stage0 - base);
-    int tc = 0, chunk = 0;
+    int tc = 0, chunk = 0, it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++tc) {
       int m0, n0, split, kb0, kb1;
       unit_coords(u, m0, n0, split, kb0, kb1);
+      if (ce_a) {
+        // softmax-CE: every landed A stage (two 64-class chunks of 64 batch
+        // rows, each row 128 bytes, 128B-swizzled) becomes dz in place;
+        // thread e takes chunk e / 128, row (e / 2) % 64 and the 16-byte
+        // units 4 (e % 2) .. 4 (e % 2) + 3 of it
+        const int e = threadIdx.x - 64;
+        const int ch = e >> 7, kr = (e >> 1) & 63, hb = e & 1;
+        for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
+          const int s = it % W_STAGES;
+          const int b = kb * C::BKW + kr;   // batch row
+          const bool rok = b < p.K;
+          float2 st = make_float2(0.f, 0.f);
+          int y = -1;
+          if (rok) {   // in flight while the stage lands
+            st = __ldg(p.ce_rowstat + b);
+            y = __ldg(p.ce_labels + b);
+          }
+          ok = __all_sync(0xffffffffu, mbar_wait(full_bar(s), (uint32_t)(it / W_STAGES) & 1u, p.err));
+          if (!ok) break;
+          uint8_t* row = base_ptr + (a_base - base) + s * C::A_BYTES + ch * C::CHUNK_BYTES + kr * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = 4 * hb + i;   // logical unit j at physical unit j ^ (kr & 7)
+            ce_unit(row + 16 * (j ^ (kr & 7)), m0 + 64 * ch + 8 * j, p.M, y, st.x, st.y, p.ce_scale, rok);
+          }
+          fence_async_smem();   // the generic-proxy writes, visible to the tensor cores
+          __syncwarp();
+          if (lane == 0) mbar_arrive(formed_bar(s));
+        }
+        if (!ok) break;
+      }
       const bool do_db = p.db_out != nullptr && n0 == 0;
       const int buf = C::NBUF == 2 ? (tc & 1) : 0;
       const uint32_t tph = C::NBUF == 2 ? (((uint32_t)tc >> 1) & 1u) : ((uint32_t)tc & 1u);
@@ -1514,6 +1649,10 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   if (!make_tmap_op(&p.tmB, x3, op.B, op.N, op.K, op.ldb, op.b_plane, 64, bkw, err, errlen)) return -1;
   p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
   p.num_kb = (int)ceil_div(op.K, bkw);
+  if (op.ce_rowstat) {
+    if (x3 || !op.ce_labels) { snprintf(err, errlen, "softmax-CE wgrad: bf16 with labels only"); return -1; }
+    p.ce_rowstat = op.ce_rowstat; p.ce_labels = op.ce_labels; p.ce_scale = op.ce_scale;
+  }
   int wbn, splits;
   tc_wgrad_choice(op.dtype, op.M, op.N, op.K, &wbn, &splits);
   if (op.splits > 0) splits = op.splits;
@@ -1564,7 +1703,14 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   // 256-wide tiles where they still give every SM a tile
   const int sms = device_sms();
   const bool x3 = op.dtype == DT_F32X3;   // 128-wide tiles only (three planes per stage)
-  const int BN = !x3 && op.N > 128 && ceil_div(op.M, tc::BM) * ceil_div(op.N, 256) >= sms ? 256 : 128;
+  // the softmax-CE forward groups columns by 128: one warp's half of a 256-wide tile
+  const bool ce_f = op.kind == GEMM_FWD && op.ce_stats;
+  const bool ce_a = op.kind == GEMM_DGRAD && op.ce_rowstat;
+  if ((ce_f || ce_a) && (x3 || !op.ce_labels || (ce_f && (op.N <= 128 || !op.ce_zy)))) {
+    snprintf(err, errlen, "softmax-CE GEMM: bf16, labels, and (forward) more than 128 columns");
+    return -1;
+  }
+  const int BN = !x3 && op.N > 128 && (ce_f || ceil_div(op.M, tc::BM) * ceil_div(op.N, 256) >= sms) ? 256 : 128;
   tc::PParams p;
   memset(&p, 0, sizeof(p));
   if (!make_tmap_op(&p.tmA, x3, op.A, op.K, op.M, op.lda, op.a_plane, 64, tc::BM, err, errlen)) return -1;
@@ -1586,6 +1732,12 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   p.out_u = (__nv_bfloat16*)op.out_u; p.ldu = op.ldu;
   p.aux = (const __nv_bfloat16*)op.aux; p.ld_aux = op.ld_aux;
   p.err = op.err;
+  if (ce_f) {
+    p.ce_stats = op.ce_stats; p.ce_zy = op.ce_zy; p.ce_groups = (int)ce_groups(op.N); p.ce_labels = op.ce_labels;
+  }
+  if (ce_a) {
+    p.ce_rowstat = op.ce_rowstat; p.ce_labels = op.ce_labels; p.ce_scale = op.ce_scale;
+  }
   LaunchRec& r = recs[0];
   // fp32 planes with few tiles: a CTA pair per tile, each half of K
   const bool pair = x3 && 2 * p.num_tiles <= sms && p.num_kb >= 2;
