@@ -368,11 +368,16 @@ def main():
                     help="update rule (default AdamW)")
     ap.add_argument("--max-grad-norm", type=float, default=0.0, help="> 0: global gradient-norm clipping")
     ap.add_argument("--loss", default="ce", choices=["ce", "mse"], help="softmax CE (default) or MSE")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (small cases for profiling; not a bench line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     import synth
     w = synth.WORKLOADS[args.workload]
+    if args.batch > 0:
+        import dataclasses
+        w = dataclasses.replace(w, batch=args.batch)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
