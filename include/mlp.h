@@ -125,9 +125,11 @@ mlp_status mlp_train_step(mlp_t* model, const void* x_dev, const void* y_dev, fl
  * two device input slots in the arena, so the copies for the next call
  * overlap the kernels of this one; the step waits for its own copies.  The
  * host buffers must stay valid and unchanged until their copy has completed
- * (at the latest when the step completes).  loss_host (nullable, pinned)
- * receives the step's batch-mean loss when the step completes.  Returns once
- * the copies and the step are enqueued on `stream`. */
+ * (at the latest when the step completes).  loss_host (nullable) receives
+ * the step's loss when the step completes: page-locked memory the device can
+ * address is written by the step's last kernel directly, other memory by a
+ * copy after the step.  Returns once the copies and the step are enqueued on
+ * `stream`. */
 mlp_status mlp_train_step_host(mlp_t* model, const void* x_host, const void* y_host, float lr, float beta1,
                                float beta2, float eps, float wd, float* loss_host, void* stream);
 

@@ -276,7 +276,7 @@ struct mlp {
   int kernels_per_step = 0;
   // mlp_train_step_host: copy streams and two input slots, so the copies of
   // step i+1 run while step i computes
-  static constexpr int kCopyStreams = 4;   // x is copied in this many pieces, one per stream (copy engine)
+  static constexpr int kCopyStreams = 2;   // x is copied in this many pieces, one per stream (copy engine)
   cudaStream_t copy_stream[kCopyStreams] = {};
   cudaEvent_t copied[2][kCopyStreams] = {}, consumed[2] = {nullptr, nullptr};
   int host_calls = 0;
@@ -913,13 +913,26 @@ mlp_status mlp_train_step_host(mlp_t* m, const void* x_host, const void* y_host,
     CUDA_TRY(cudaStreamWaitEvent(s, m->copied[k][c], 0));
   }
   std::vector<LaunchRec> recs;
+  // The loss goes straight from the kernel that forms it into page-locked
+  // host memory the device can address (a copy node after the step would
+  // add its own latency to every step); other host memory gets a copy.
   float* loss_dev = &m->ctl()->loss_slot;
+  bool copy_loss = loss_host != nullptr;
+  if (loss_host) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, loss_host) == cudaSuccess && pa.type == cudaMemoryTypeHost && pa.devicePointer) {
+      loss_dev = (float*)pa.devicePointer;
+      copy_loss = false;
+    } else {
+      cudaGetLastError();   // not registered memory: clear the query's error, copy instead
+    }
+  }
   mlp_status st = plan_step(m, xd, yd, Hyper{lr, b1, b2, eps, wd}, loss_dev, recs);
   if (st != MLP_OK) return st;
   st = run(m, 1, recs, s);
   if (st != MLP_OK) return st;
   CUDA_TRY(cudaEventRecord(m->consumed[k], s));
-  if (loss_host) CUDA_TRY(cudaMemcpyAsync(loss_host, loss_dev, 4, cudaMemcpyDeviceToHost, s));
+  if (copy_loss) CUDA_TRY(cudaMemcpyAsync(loss_host, &m->ctl()->loss_slot, 4, cudaMemcpyDeviceToHost, s));
   ++m->host_calls;
   return ok();
 }
