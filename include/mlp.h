@@ -184,7 +184,13 @@ mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
  *     the dgrad and of the wgrad and its exponential is recomputed for each).
  *     Same rounding points either way (logits and dz rounded to bf16); the
  *     sums differ in order only. */
-enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2, MLP_OPT_PDL = 3, MLP_OPT_CE_GEMM = 4 };
+/*   MLP_OPT_RELU_BITS (default 1; MLP_BF16 models): the forward GEMM of a
+ *     ReLU layer also writes its mask (stored h > 0) as one bit per element,
+ *     and the dgrad below reads the bits instead of the stored activation
+ *     (16x fewer bytes).  0 reads the stored activation.  Results are
+ *     identical either way. */
+enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2, MLP_OPT_PDL = 3, MLP_OPT_CE_GEMM = 4,
+       MLP_OPT_RELU_BITS = 5 };
 mlp_status mlp_set_option(mlp_t* model, int option, int64_t value);
 
 /* The update rule of the training step (default MLP_OPTIM_ADAMW) and global

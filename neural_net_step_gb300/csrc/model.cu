@@ -77,6 +77,8 @@ struct Layout {
   int64_t ld_x = 0;               // row pitch of the input planes
   int64_t max_ld = 8;             // row pitch bound of the dY ping-pong buffers
   std::vector<size_t> off_h, off_u;
+  std::vector<size_t> off_bits;   // bf16 ReLU layers: the activation's mask as bits, [N / 64][B] words
+  std::vector<int64_t> ld_bits;
   std::vector<int64_t> ld_h;
   size_t off_z = 0, off_dz = 0;
   int64_t ldz = 0;
@@ -168,6 +170,9 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     max_ld = ld > max_ld ? ld : max_ld;
     L.off_h.push_back(take(batch * ld * es));
     L.off_u.push_back(L.acts[l] == MLP_ACT_GELU_TANH ? take(batch * ld * es) : 0);
+    const bool bits = dtype == MLP_BF16 && L.acts[l] == MLP_ACT_RELU;
+    L.ld_bits.push_back(bits ? batch : 0);
+    L.off_bits.push_back(bits ? take((dims[l + 1] + 63) / 64 * batch * 8) : 0);
   }
   L.ldz = (dims[L.L] + 7) / 8 * 8;
   L.off_z = take(batch * L.ldz * es);
@@ -270,6 +275,7 @@ struct mlp {
   int optim = MLP_OPTIM_ADAMW;
   int loss = MLP_LOSS_CE;
   bool ce_gemm = false;      // softmax-CE inside the GEMMs of a wide bf16 output layer (slower on this part)
+  bool relu_bits = true;     // bf16 ReLU masks as bits between the forward and the dgrad
   float max_grad_norm = 0.f; // > 0: global-norm clipping of the gradient before the update
   std::mutex mu;
   std::vector<GraphCache> graphs;
@@ -362,6 +368,9 @@ mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out
       op.act = L.acts[l];
       op.out = m->at(L.off_h[l]); op.ldo = L.ld_h[l]; op.out_plane = L.B * L.ld_h[l];
       if (op.act == MLP_ACT_GELU_TANH) { op.out_u = m->at(L.off_u[l]); op.ldu = L.ld_h[l]; }
+      if (m->relu_bits && L.ld_bits[l] && !x3) {
+        op.relu_bits = (uint64_t*)m->at(L.off_bits[l]); op.ld_bits = L.ld_bits[l];
+      }
       X = op.out; ldx = L.ld_h[l]; xplane = op.out_plane;
     } else {
       op.act = MLP_ACT_NONE;
@@ -523,6 +532,9 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
       dg.b_plane = L.plane_n; dg.out_plane = dy_plane;
       dg.aux = dg.act == MLP_ACT_GELU_TANH ? m->at(L.off_u[l - 1]) : m->at(L.off_h[l - 1]);
       dg.ld_aux = L.ld_h[l - 1];
+      if (m->relu_bits && L.ld_bits[l - 1] && !x3) {
+        dg.relu_bits = (uint64_t*)m->at(L.off_bits[l - 1]); dg.ld_bits = L.ld_bits[l - 1];
+      }
       dg.out = m->at(L.off_dy[buf]); dg.ldo = L.ld_h[l - 1];
       dg.err = &ctl->err;
       if (ce_top) {
@@ -813,6 +825,7 @@ mlp_status mlp_set_option(mlp_t* m, int option, int64_t value) {
     case MLP_OPT_F32_TENSOR_CORES: m->f32_tc = value != 0; break;
     case MLP_OPT_PDL: m->pdl = value != 0; break;
     case MLP_OPT_CE_GEMM: m->ce_gemm = value != 0; break;
+    case MLP_OPT_RELU_BITS: m->relu_bits = value != 0; break;
     default: return fail(MLP_ERR_ARG, "unknown option %d", option);
   }
   if (option == MLP_OPT_FUSE_HEAD || option == MLP_OPT_F32_TENSOR_CORES) {   // planes kept current only while used

@@ -58,6 +58,13 @@ struct GemmOp {
   //     ce_rowstat: the operand is dz = (exp(z - M_r) invS_r - [c == y_r])
   //     ce_scale, formed from the stored logits in shared memory;
   //     (M_r, invS_r) = ce_rowstat[r] for batch row r.
+  // ReLU as one bit per element (bf16, tensor cores, one CTA per tile):
+  // GEMM_FWD with ACT_RELU also writes bits, GEMM_DGRAD with ACT_RELU reads
+  // its mask from them instead of the stored h (aux).  Layout: 64-column
+  // groups, each [rows] of 64-bit words (pitch ld_bits >= M words), so a
+  // warp's rows are contiguous: bit n % 64 of word (n / 64) * ld_bits + m is
+  // "stored h[m, n] > 0".
+  uint64_t* relu_bits = nullptr; int64_t ld_bits = 0;
   float2* ce_stats = nullptr; float* ce_zy = nullptr;
   const float2* ce_rowstat = nullptr;
   const int32_t* ce_labels = nullptr;

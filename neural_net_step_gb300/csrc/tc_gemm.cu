@@ -473,6 +473,9 @@ struct PParams {
   //   ce_scale is formed in shared memory before the MMA reads the stage.
   float2* ce_stats; float* ce_zy; int ce_groups;
   const float2* ce_rowstat; const int32_t* ce_labels; float ce_scale;
+  // ReLU mask as bits (bf16, one CTA per tile): written by the forward,
+  // read by the dgrad in place of the stored activation
+  uint64_t* relu_bits; int64_t ld_bits;
 };
 
 // dz of softmax-CE from a stored logit: (exp(z - M) invS - onehot) scale, or 0
@@ -807,6 +810,11 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
         if (p.kind == GEMM_FWD) {
           if (gn0 + lane < p.N) bias0 = __ldg(p.bias + gn0 + lane);
           if (gn0 + 32 + lane < p.N) bias1 = __ldg(p.bias + gn0 + 32 + lane);
+        } else if (p.act == ACT_RELU && row_ok && !X3 && !PAIR && p.relu_bits) {
+          // the forward's bits of these 64 columns: 8 bytes instead of 128
+          const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.relu_bits + (int64_t)(gn0 / 64) * p.ld_bits + gm));
+          mask0 = w.x;
+          mask1 = w.y;
         } else if (p.act == ACT_RELU && row_ok) {
           const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
           if (gn0 + 64 <= p.N) {
@@ -871,6 +879,17 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
           }
 #pragma unroll
           for (int j = 0; j < 64; ++j) v[j] = apply_act(v[j], p.act);
+          if (!X3 && !PAIR && p.relu_bits && row_ok) {
+            // bit j: the stored (bf16) activation is positive
+            uint32_t b0 = 0u, b1 = 0u;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              b0 |= (gn0 + j < p.N && __bfloat162float(__float2bfloat16_rn(v[j])) > 0.f ? 1u : 0u) << j;
+              b1 |= (gn0 + 32 + j < p.N && __bfloat162float(__float2bfloat16_rn(v[32 + j])) > 0.f ? 1u : 0u) << j;
+            }
+            // a warp's 32 rows are 32 consecutive words: one coalesced store
+            *reinterpret_cast<uint2*>(p.relu_bits + (int64_t)(gn0 / 64) * p.ld_bits + gm) = make_uint2(b0, b1);
+          }
           if (ce_f) {
             // the logits as stored (bf16): the chunk maximum folded into the
             // group's running maximum, then the exponentials added; the
@@ -1738,9 +1757,16 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   if (ce_a) {
     p.ce_rowstat = op.ce_rowstat; p.ce_labels = op.ce_labels; p.ce_scale = op.ce_scale;
   }
-  LaunchRec& r = recs[0];
   // fp32 planes with few tiles: a CTA pair per tile, each half of K
   const bool pair = x3 && 2 * p.num_tiles <= sms && p.num_kb >= 2;
+  if (op.relu_bits && op.act == ACT_RELU) {
+    if (x3 || pair || op.ld_bits < op.M || ((uintptr_t)op.relu_bits & 7)) {
+      snprintf(err, errlen, "ReLU bits: bf16 only, ld_bits >= M, 8-byte aligned");
+      return -1;
+    }
+    p.relu_bits = op.relu_bits; p.ld_bits = op.ld_bits;
+  }
+  LaunchRec& r = recs[0];
   if (pair) {
     r.func = tcpair_kernel_ptr();
     r.smem = tc::PCfg<128, true>::SMEM_BYTES;

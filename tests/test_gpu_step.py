@@ -370,3 +370,27 @@ def test_train_step_host_matches_device_inputs(name, batch):
     assert step == len(bl)
     assert np.array_equal(hl.numpy().astype(np.float64), d_losses)
     assert np.array_equal(P.flat(m.split(p.astype(np.float64))), P.flat(d_params))
+
+
+# --------------------------------------------------------------------------
+# ReLU masks as bits (bf16): identical to reading the stored activation
+# --------------------------------------------------------------------------
+RAGGED_BF16 = synth.Workload("bits_ragged", (64, 200, 72, 10), (om.ACT_RELU, om.ACT_RELU), synth.BF16, 300, 2,
+                             1e-3, 0.9, 0.999, 1e-8, 0.01, "normal", 11)
+
+
+@pytest.mark.parametrize("w,batch", [(W["cifar_mlp_b8192"], None), (W["deep_narrow_b65536"], 3000),
+                                     (RAGGED_BF16, None)], ids=["cifar_full", "deep_narrow_3000", "ragged"])
+def test_relu_bits_equal_stored_activation_mask(w, batch):
+    B = w.batch if batch is None else batch
+    params0 = synth.make_params(w)
+    bl = P.batches(w, 2, B)
+    res = []
+    for bits in (1, 0):
+        m = make_model(w, B, params0)
+        m.set_option(nn.OPT_RELU_BITS, bits)
+        losses, p, g = gpu_run(m, w, bl)
+        m.close()
+        res.append((losses, P.flat(p), P.flat(g)))
+    for a, b in zip(res[0], res[1]):
+        assert np.array_equal(a, b)
