@@ -1757,8 +1757,9 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   if (ce_a) {
     p.ce_rowstat = op.ce_rowstat; p.ce_labels = op.ce_labels; p.ce_scale = op.ce_scale;
   }
-  // fp32 planes with few tiles: a CTA pair per tile, each half of K
-  const bool pair = x3 && 2 * p.num_tiles <= sms && p.num_kb >= 2;
+  // fp32 planes with few tiles: a CTA pair per tile, each half of K (with
+  // fewer than three K stages the exchange costs more than the halved loop)
+  const bool pair = x3 && 2 * p.num_tiles <= sms && p.num_kb >= 3;
   if (op.relu_bits && op.act == ACT_RELU) {
     if (x3 || pair || op.ld_bits < op.M || ((uintptr_t)op.relu_bits & 7)) {
       snprintf(err, errlen, "ReLU bits: bf16 only, ld_bits >= M, 8-byte aligned");

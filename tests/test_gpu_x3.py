@@ -100,7 +100,8 @@ def test_x3_linear_act(act, M, N, K):
 
 DGRAD = [
     (nn.ACT_RELU, 64, 128, 256),
-    (nn.ACT_RELU, 4096, 128, 256),
+    (nn.ACT_RELU, 4096, 128, 256),      # CTA pairs (four K stages)
+    (nn.ACT_RELU, 4096, 256, 128),      # two K stages: one CTA per tile
     (nn.ACT_RELU, 300, 40, 136),
     (nn.ACT_NONE, 130, 256, 784),
 ]
