@@ -43,7 +43,7 @@ FWD_CASES = [
     (nn.BF16, nn.ACT_NONE, 300, 10, 1024),        # 10 outputs (16-wide tile)
     (nn.BF16, nn.ACT_NONE, 260, 100, 512),
     (nn.BF16, nn.ACT_NONE, 130, 1000, 64),
-    (nn.BF16, nn.ACT_RELU, 4864, 1000, 320),      # 256-wide tiles in multicast CTA pairs, ragged N
+    (nn.BF16, nn.ACT_RELU, 4864, 1000, 320),      # 256-wide tiles (152 and more), ragged N
 ]
 
 
@@ -85,7 +85,7 @@ DGRAD_CASES = [
     (nn.BF16, nn.ACT_GELU_TANH, 200, 1024, 4096),
     (nn.BF16, nn.ACT_NONE, 130, 32000, 1024),
     (nn.BF16, nn.ACT_RELU, 250, 100, 512),
-    (nn.BF16, nn.ACT_RELU, 4864, 200, 1000),      # multicast CTA pairs (MN-major W), K tail
+    (nn.BF16, nn.ACT_RELU, 4864, 200, 1000),      # MN-major W, ragged N, K tail
 ]
 
 
