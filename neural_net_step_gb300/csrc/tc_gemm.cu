@@ -1557,7 +1557,10 @@ static void tc_wgrad_choice(int dtype, int64_t M, int64_t N, int64_t K, int* bn,
     const int64_t tiles = ceil_div(M, tc::BM) * ceil_div(N, tc::W_BN);
     const int64_t kbs = ceil_div(K, tc::WCfg<true>::BKW);
     int64_t best_s = 1, best_cost = INT64_MAX;
-    for (int64_t s = 1; s <= 256 && (s == 1 || (kbs / s >= 4 && s * M * N <= ((int64_t)4 << 20))); s *= 2) {
+    // at most 16 splits: the optimizer adds the partials of an element in
+    // one batch of 16 loads (a second batch costs it more than the longer
+    // work units cost this kernel)
+    for (int64_t s = 1; s <= 16 && (s == 1 || (kbs / s >= 4 && s * M * N <= ((int64_t)4 << 20))); s *= 2) {
       const int64_t cost = ceil_div(tiles * s, kSMs) * (ceil_div(kbs, s) + 2);
       if (cost < best_cost) { best_cost = cost; best_s = s; }
     }
