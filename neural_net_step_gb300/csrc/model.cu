@@ -84,8 +84,8 @@ struct Layout {
   int64_t ldz = 0;
   size_t off_dy[2] = {0, 0};
   size_t off_loss_rows = 0, off_ctl = 0;
-  // Split-K partial sums of the weight gradients.  Small ones (defer_l: at
-  // most 24 MB per layer, 64 MB in all, so they stay in L2) are
+  // Split-K partial sums of the weight gradients.  In fp32 models small ones
+  // (defer_l: at most 24 MB per layer, 64 MB in all, so they stay in L2) are
   // left for the optimizer to add, in a region per layer since all are read
   // at the end; the others share one region and are reduced right after
   // their GEMM.
@@ -193,8 +193,12 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     }
     need[l] = b;
     const int64_t M = dims[l + 1], MN = dims[l + 1] * dims[l];
-    // deferred while the partials stay small enough to live in L2 until the optimizer runs
-    const bool d = b > 0 && MN % 4 == 0 && M % 4 == 0 && b <= (24u << 20) && deferred + b <= (64u << 20);
+    // deferred while the partials stay small enough to live in L2 until the
+    // optimizer runs -- for fp32 models, whose short, latency-bound step
+    // gains from one kernel less per layer; in bf16 steps the reduce kernel
+    // overlaps the next dgrad and deferring measured slower
+    const bool d = dtype == MLP_F32 && b > 0 && MN % 4 == 0 && M % 4 == 0 && b <= (24u << 20) &&
+                   deferred + b <= (64u << 20);
     if (d) deferred += b;
     L.defer_l.push_back(d);
     if (!d) shared_ws = b > shared_ws ? b : shared_ws;
