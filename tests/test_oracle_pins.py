@@ -545,3 +545,31 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_mse_closed_forms()
     monkeypatch.setattr(om, "mse", orig_mse)
+
+
+# --------------------------------------------------------------------------
+# Frozen worked examples (the oracle's own output; a regression guard)
+# --------------------------------------------------------------------------
+def test_oracle_matches_frozen_worked_examples():
+    """tests/golden/tiny_step.json holds whole steps (CE / MSE; AdamW, Adam,
+    SGD; clipping off and on) computed by this oracle when it was pinned; a
+    change of its arithmetic must show here and be justified."""
+    import json
+    import os
+    import sys
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    sys.path.insert(0, here)
+    try:
+        import make_golden
+    finally:
+        sys.path.remove(here)
+    with open(os.path.join(here, "tiny_step.json")) as f:
+        frozen = json.load(f)
+    now = make_golden.compute()
+    assert frozen["dims"] == now["dims"] and frozen["batch"] == now["batch"]
+    for name, case in frozen["cases"].items():
+        got = now["cases"][name]
+        assert abs(got["loss"] - case["loss"]) <= 1e-14 * abs(case["loss"]), name
+        assert abs(got["clip"] - case["clip"]) <= 1e-14, name
+        for a, b in zip(got["grads"] + got["params"], case["grads"] + case["params"]):
+            np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-16)
