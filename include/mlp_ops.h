@@ -154,6 +154,14 @@ mlp_status mlp_op_optim(int kind, int64_t n, float* p, float* g, float* m, float
                         float beta1, float beta2, float eps, float wd, float max_norm, float* ws_dev,
                         float* norm_dev, void* stream);
 
+/* The error path of the device waits, exercised without a fault: one thread
+ * waits, through the same bounded wait every tensor-core kernel uses for its
+ * pipeline barriers, for an mbarrier phase that nothing completes; after
+ * limit_ns (at most 1 s) it gives up, sets the timeout bit (1 << 2, the bit
+ * behind MLP_ERR_TIMEOUT) in err_dev and the kernel returns normally, so the
+ * context stays usable. */
+mlp_status mlp_op_wait_timeout_check(uint64_t limit_ns, uint32_t* err_dev, void* stream);
+
 /* Row argmax of z [B, C] (ldz) into int32 out [B]; lowest index on ties. */
 mlp_status mlp_op_argmax(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, int32_t* out, void* stream);
 

@@ -75,6 +75,7 @@ _SIGS = {
     "mlp_op_adamw": (_I32, [_I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _P]),
     "mlp_op_optim": (_I32, [_I32, _I64, _P, _P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _F, _P, _P, _P]),
     "mlp_op_argmax": (_I32, [_I32, _I64, _I64, _P, _I64, _P, _P]),
+    "mlp_op_wait_timeout_check": (_I32, [_c.c_uint64, _P, _P]),
 }
 
 
@@ -264,6 +265,10 @@ def mlp_op_adamw(n, p, g, m, v, w16, t, lr, beta1, beta2, eps, wd, stream) -> No
 
 def mlp_op_optim(kind, n, p, g, m, v, w16, t, lr, beta1, beta2, eps, wd, max_norm, ws, norm, stream) -> None:
     _check(lib().mlp_op_optim(kind, n, p, g, m, v, w16, t, lr, beta1, beta2, eps, wd, max_norm, ws, norm, stream))
+
+
+def mlp_op_wait_timeout_check(limit_ns, err, stream) -> None:
+    _check(lib().mlp_op_wait_timeout_check(limit_ns, err, stream))
 
 
 def mlp_op_argmax(dtype, B, C, z, ldz, out, stream) -> None:

@@ -1315,6 +1315,14 @@ mlp_status mlp_op_optim(int kind, int64_t n, float* p, float* g, float* m, float
   return run_ops(r, nr, stream);
 }
 
+mlp_status mlp_op_wait_timeout_check(uint64_t limit_ns, uint32_t* err_dev, void* stream) {
+  if (!err_dev) return fail(MLP_ERR_ARG, "err_dev is NULL");
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return fail(MLP_ERR_ARG, "limit_ns must be in (0, 1 s]");
+  LaunchRec r;
+  wait_timeout_check_plan(err_dev, limit_ns, &r);
+  return run_ops(&r, 1, stream);
+}
+
 mlp_status mlp_op_argmax(int dtype, int64_t B, int64_t C, const void* z, int64_t ldz, int32_t* out, void* stream) {
   if (!dtype_ok(dtype)) return fail(MLP_ERR_DTYPE, "bad dtype");
   if (!z || !out) return fail(MLP_ERR_ARG, "null pointer");

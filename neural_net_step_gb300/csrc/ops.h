@@ -235,6 +235,11 @@ struct HeadPartials { int n; int64_t stride; int64_t loss_off; };
 HeadPartials head_partials(int64_t B, int64_t C, int64_t K);
 int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen);
 
+// One thread waits, through the bounded wait every tcgen05 kernel uses, for
+// an mbarrier phase that nothing completes: after limit_ns it marks
+// ERRBIT_TIMEOUT in err_dev and returns (the error path, exercised).
+int wait_timeout_check_plan(uint32_t* err_dev, uint64_t limit_ns, LaunchRec* rec);
+
 // Set the message mlp_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 

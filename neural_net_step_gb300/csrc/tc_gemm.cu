@@ -97,19 +97,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: true when the phase completed, false after the time limit
-// (the error word is then marked).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+// Bounded wait: true when the phase completed, false after limit_ns (the
+// error word is then marked).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint32_t* err, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       if (err) atomicOr(err, ERRBIT_TIMEOUT);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+  return mbar_wait_for(bar, parity, err, kWaitLimitNs);
+}
+
+// The error path of every device wait, exercised on purpose: one thread
+// waits, through the same bounded wait, for the phase of an mbarrier that
+// nothing arrives on; it gives up after limit_ns, marks the error word and
+// the kernel returns normally.
+// (One parameter block, like every kernel here: launches pass a single
+// argument pointer.)
+struct WaitCheckParams { uint32_t* err; uint64_t limit_ns; };
+__global__ void wait_timeout_check_kernel(const __grid_constant__ WaitCheckParams q) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  mbar_wait_for(b, 0u, q.err, q.limit_ns);
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar) {
   asm volatile(
@@ -1792,6 +1810,17 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   return 1;
 }
 }  // namespace
+
+int wait_timeout_check_plan(uint32_t* err_dev, uint64_t limit_ns, LaunchRec* rec) {
+  const tc::WaitCheckParams q{err_dev, limit_ns};
+  rec->func = (const void*)tc::wait_timeout_check_kernel;
+  rec->grid = dim3(1);
+  rec->block = dim3(1);
+  rec->smem = 0;
+  rec->name = "wait_timeout_check";
+  rec->set_args(q);
+  return 1;
+}
 
 int tc_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   if (op.dtype != DT_BF16 && op.dtype != DT_F32X3) {

@@ -71,3 +71,21 @@ def test_no_gpu_means_no_compute(lib):
     st = lib.mlp_create(dims, 3, None, 1, 0, 0, 4, ctypes.c_void_p(256), 1 << 20, 0, ctypes.byref(h))
     assert st != 0 and not h.value
     assert nn.mlp_last_error()
+
+
+def test_every_kernel_takes_one_parameter_block():
+    """Launches pass one argument pointer (a kernel's parameter block), so a
+    kernel with any other parameter list would read past it: every
+    __global__ function takes exactly one `const __grid_constant__` struct."""
+    csrc = os.path.join(ROOT, "neural_net_step_gb300", "csrc")
+    n = 0
+    for f in sorted(os.listdir(csrc)):
+        if not f.endswith(".cu"):
+            continue
+        txt = re.sub(r"//[^\n]*", "", open(os.path.join(csrc, f)).read())
+        for m in re.finditer(r"__global__", txt):
+            seg = txt[m.end():txt.index("{", m.end())]
+            params = seg[seg.rindex("(") + 1:seg.rindex(")")].strip()
+            assert re.fullmatch(r"const __grid_constant__ \w+ \w+", params), (f, params)
+            n += 1
+    assert n >= 15

@@ -290,3 +290,21 @@ def test_argmax_bit_exact_with_ties(dtype, B, C):
     nn.mlp_op_argmax(dtype, B, C, zd.data_ptr(), C, out.data_ptr(), _stream())
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), om.argmax_rows(to64(z)))
+
+
+# ---------------------------------------------------------------------------
+# The error path of the bounded device waits (no fault: the wait gives up)
+# ---------------------------------------------------------------------------
+def test_bounded_wait_gives_up_and_context_stays_usable():
+    import time
+    err = _err()
+    t0 = time.perf_counter()
+    nn.mlp_op_wait_timeout_check(50_000_000, err.data_ptr(), _stream())   # 50 ms
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert err.item() == 4                 # the timeout bit, nothing else
+    assert 0.05 <= dt < 5.0
+    # the context still runs kernels correctly afterwards
+    test_linear_act_forward(nn.BF16, nn.ACT_RELU, 256, 256, 256)
+    with pytest.raises(nn.MlpError):
+        nn.mlp_op_wait_timeout_check(2_000_000_000, err.data_ptr(), _stream())   # over the 1 s cap
