@@ -157,6 +157,16 @@ __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s
   m = mm;
 }
 
+// 2^t by the hardware's base-2 exponential (PTX ex2.approx, subnormal
+// results flushed to zero); exp(x) = 2^(x log2 e), so the wide-row kernel
+// forms exp(z - m) as one FFMA (z log2e - m log2e) and one ex2.
+__device__ __forceinline__ float pow2_approx(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
 template <typename T>
 __global__ void __launch_bounds__(256) ce_row2_kernel(const __grid_constant__ CeParams p) {
   pdl_enter();
@@ -181,9 +191,10 @@ __global__ void __launch_bounds__(256) ce_row2_kernel(const __grid_constant__ Ce
       float vmax = -INFINITY;
 #pragma unroll
       for (int k = 0; k < E; ++k) vmax = fmaxf(vmax, to_f32(e[k]));
+      const float vml = vmax * kLog2e;
       float vs = 0.f;
 #pragma unroll
-      for (int k = 0; k < E; ++k) vs += __expf(to_f32(e[k]) - vmax);
+      for (int k = 0; k < E; ++k) vs += pow2_approx(fmaf(to_f32(e[k]), kLog2e, -vml));
       ms_combine<T>(m, s, vmax, vs);
     }
   }
@@ -203,7 +214,10 @@ __global__ void __launch_bounds__(256) ce_row2_kernel(const __grid_constant__ Ce
   for (int w = 1; w < 8; ++w) ms_combine<T>(m, s, red_m[w], red_s[w]);
   const int y = p.labels[row];
   const bool bad = y < 0 || y >= p.C;
-  const float inv_s = 1.0f / s;
+  // dz = exp(z - m) (1/s) grad_scale, minus grad_scale at the label (one
+  // element of the row, fixed up in the vector that holds it)
+  const float a = (1.0f / s) * p.grad_scale, ml = m * kLog2e;
+  const int yv = y / E, yk = y - yv * E;
   uint4* dr = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.dz) + (int64_t)row * p.lddz);
   for (int v0 = threadIdx.x; v0 < nvec; v0 += 256 * U) {
     uint4 raw[U];
@@ -215,13 +229,18 @@ __global__ void __launch_bounds__(256) ce_row2_kernel(const __grid_constant__ Ce
       const int vi = v0 + 256 * u;
       if (vi >= nvec) break;
       const T* e = reinterpret_cast<const T*>(&raw[u]);
+      float d[E];
+#pragma unroll
+      for (int k = 0; k < E; ++k) d[k] = pow2_approx(fmaf(to_f32(e[k]), kLog2e, -ml)) * a;
+      if (vi == yv) {
+#pragma unroll
+        for (int k = 0; k < E; ++k)
+          if (k == yk) d[k] -= p.grad_scale;
+      }
       uint4 o;
       T* oe = reinterpret_cast<T*>(&o);
 #pragma unroll
-      for (int k = 0; k < E; ++k) {
-        const int j = vi * E + k;
-        oe[k] = from_f32<T>((__expf(to_f32(e[k]) - m) * inv_s - (j == y ? 1.f : 0.f)) * p.grad_scale);
-      }
+      for (int k = 0; k < E; ++k) oe[k] = from_f32<T>(d[k]);
       __stcs(dr + vi, o);
     }
   }
