@@ -39,6 +39,33 @@ __device__ __forceinline__ void ce_finish_row(const CeParams& p, int row, int y,
   }
 }
 
+// Four consecutive elements as fp32 (16-byte fp32 / 8-byte bf16 accesses).
+template <typename T>
+__device__ __forceinline__ void load4(const T* src, float* v) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  } else {
+    const uint2 a = *reinterpret_cast<const uint2*>(src);
+    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&a.x);
+    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&a.y);
+    v[0] = __low2float(lo); v[1] = __high2float(lo); v[2] = __low2float(hi); v[3] = __high2float(hi);
+  }
+}
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, const float* v) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&lo);
+    o.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = o;
+  }
+}
+
 // One warp per row; the row lives in registers (C <= 32 * VPL).
 template <typename T, int VPL>
 __global__ void __launch_bounds__(256) ce_warp_kernel(const __grid_constant__ CeParams p) {
@@ -72,6 +99,60 @@ __global__ void __launch_bounds__(256) ce_warp_kernel(const __grid_constant__ Ce
   for (int i = 0; i < VPL; ++i) {
     int j = lane + 32 * i;
     if (j < p.C) dr[j] = from_f32<T>((v[i] * inv_s - (j == y ? 1.f : 0.f)) * p.grad_scale);
+  }
+  ce_finish_row<T>(p, row, y, m, s, bad, lane);
+}
+
+// One warp per row with 4 consecutive elements a lane (C % 4 == 0, rows
+// 8- / 16-byte aligned; C <= 128 * SLOTS): one vector load and store per
+// lane and slot; exp(z - m) = 2^(z log2e - m log2e) (one FFMA, one ex2).
+__device__ __forceinline__ float pow2_approx(float t);
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename T, int SLOTS>
+__global__ void __launch_bounds__(256) ce_warp4_kernel(const __grid_constant__ CeParams p) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= p.B) return;
+  const T* zr = reinterpret_cast<const T*>(p.z) + (int64_t)row * p.ldz;
+  float v[SLOTS][4];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    const int j = 4 * lane + 128 * i;
+    if (j < p.C) {
+      load4<T>(zr + j, v[i]);
+    } else {
+      v[i][0] = v[i][1] = v[i][2] = v[i][3] = -INFINITY;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = fmaxf(m, v[i][k]);
+  }
+  const int y = p.labels[row];
+  m = warp_max(m);
+  const float ml = m * kLog2e;
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[i][k] = 4 * lane + 128 * i < p.C ? pow2_approx(fmaf(v[i][k], kLog2e, -ml)) : 0.f;
+      s += v[i][k];
+    }
+  s = warp_sum(s);
+  const bool bad = y < 0 || y >= p.C;
+  const float a = (1.0f / s) * p.grad_scale;
+  T* dr = reinterpret_cast<T*>(p.dz) + (int64_t)row * p.lddz;
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    const int j = 4 * lane + 128 * i;
+    if (j < p.C) {
+      float d[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) d[k] = v[i][k] * a - (j + k == y ? p.grad_scale : 0.f);
+      store4<T>(dr + j, d);
+    }
   }
   ce_finish_row<T>(p, row, y, m, s, bad, lane);
 }
@@ -165,7 +246,6 @@ __device__ __forceinline__ float pow2_approx(float t) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
   return r;
 }
-constexpr float kLog2e = 1.4426950408889634f;
 
 template <typename T>
 __global__ void __launch_bounds__(256) ce_row2_kernel(const __grid_constant__ CeParams p) {
@@ -275,7 +355,13 @@ static int ce_plan_t(const CeOp& op, LaunchRec* rec, const CeParams& q) {
   const int64_t C = op.C;
   rec->smem = 0;
   rec->name = "softmax_ce";
-  if (C <= 32 * 8) {
+  const bool vec4 = C % 4 == 0 && op.ldz % 4 == 0 && op.lddz % 4 == 0 && (uintptr_t)op.z % (4 * sizeof(T)) == 0 &&
+                    (uintptr_t)op.dz % (4 * sizeof(T)) == 0;
+  if (C <= 32 * 8 && vec4) {
+    rec->block = dim3(256);
+    rec->grid = dim3((unsigned)ceil_div(op.B, 8));
+    rec->func = C <= 128 ? (const void*)ce_warp4_kernel<T, 1> : (const void*)ce_warp4_kernel<T, 2>;
+  } else if (C <= 32 * 8) {
     rec->block = dim3(256);
     rec->grid = dim3((unsigned)ceil_div(op.B, 8));
     if (C <= 32) rec->func = (const void*)ce_warp_kernel<T, 1>;
@@ -326,32 +412,6 @@ struct MseParams {
   int B, C;
   float grad_scale;
 };
-
-template <typename T>
-__device__ __forceinline__ void load4(const T* src, float* v) {
-  if constexpr (sizeof(T) == 4) {
-    const float4 a = *reinterpret_cast<const float4*>(src);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  } else {
-    const uint2 a = *reinterpret_cast<const uint2*>(src);
-    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&a.x);
-    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&a.y);
-    v[0] = __low2float(lo); v[1] = __high2float(lo); v[2] = __low2float(hi); v[3] = __high2float(hi);
-  }
-}
-template <typename T>
-__device__ __forceinline__ void store4(T* dst, const float* v) {
-  if constexpr (sizeof(T) == 4) {
-    *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-  } else {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
-    uint2 o;
-    o.x = *reinterpret_cast<const uint32_t*>(&lo);
-    o.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dst) = o;
-  }
-}
 
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(256) mse_kernel(const __grid_constant__ MseParams p) {

@@ -169,6 +169,8 @@ CE_CASES = [
     (nn.F32, 64, 10), (nn.F32, 4096, 10), (nn.BF16, 8192, 10), (nn.BF16, 1000, 100),
     (nn.BF16, 256, 32000), (nn.F32, 33, 1003), (nn.BF16, 17, 777), (nn.F32, 5, 1),
     (nn.F32, 40, 8000), (nn.BF16, 64, 4096),
+    # four elements a lane (C % 4 == 0): one and two 128-wide slots, ragged
+    (nn.F32, 77, 12), (nn.F32, 300, 200), (nn.BF16, 129, 256), (nn.BF16, 65536, 100),
 ]
 
 
@@ -231,10 +233,11 @@ def test_softmax_ce_zero_logits_closed_form_and_label_gather():
     np.testing.assert_allclose(to64(rows2), want, rtol=0, atol=2e-5)
 
 
-def test_softmax_ce_label_out_of_range_sets_error_bit():
-    B, C = 8, 10
+@pytest.mark.parametrize("C", [10, 12])
+def test_softmax_ce_label_out_of_range_sets_error_bit(C):
+    B = 8
     z = torch.zeros((B, C), dtype=torch.float32, device=DEV)
-    y = torch.tensor([0, 1, 2, 10, 4, -1, 6, 7], dtype=torch.int32, device=DEV)
+    y = torch.tensor([0, 1, 2, C, 4, -1, 6, 7], dtype=torch.int32, device=DEV)
     dz = torch.empty_like(z)
     rows = torch.empty(B, dtype=torch.float32, device=DEV)
     err = _err()
@@ -242,6 +245,8 @@ def test_softmax_ce_label_out_of_range_sets_error_bit():
                          err.data_ptr(), _stream())
     torch.cuda.synchronize()
     assert err.item() & 1
+    r = rows.cpu().numpy()
+    assert r[3] == 0.0 and r[5] == 0.0 and abs(r[0] - math.log(C)) < 1e-6
 
 
 # ---------------------------------------------------------------------------
