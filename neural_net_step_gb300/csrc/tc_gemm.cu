@@ -562,14 +562,26 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src
                "r"(src), "r"(c0), "r"(c1), "r"(c2)
                : "memory");
 }
-// The value whose bf16 rounding is plane `pl` of x (x = hi + mid + lo):
-// pl 0 -> x, pl 1 -> x - hi, pl 2 -> x - hi - mid.  The differences are exact
-// in fp32.
-__device__ __forceinline__ float split_plane(float x, int pl) {
-  if (pl == 0) return x;
-  const float r = x - __bfloat162float(__float2bfloat16_rn(x));
-  if (pl == 1) return r;
-  return r - __bfloat162float(__float2bfloat16_rn(r));
+// One output plane of a warp's 32 rows x 64 columns into 128B-swizzled
+// shared memory (16-byte unit u of row r at r*128 + ((u ^ (r & 7)) * 16)):
+// the bf16 rounding of v; with `rest`, v then keeps the remainder v - plane,
+// so that successive calls write hi, mid and lo (x = hi + mid + lo; each
+// difference is exact in fp32).  One packed conversion per pair of values.
+__device__ __forceinline__ void stage_plane(uint8_t* srow, int lane, float (&v)[64], bool rest) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    uint32_t w[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * u + 2 * h], v[8 * u + 2 * h + 1]);
+      w[h] = *reinterpret_cast<const uint32_t*>(&b2);
+      if (rest) {
+        v[8 * u + 2 * h] -= __uint_as_float(w[h] << 16);
+        v[8 * u + 2 * h + 1] -= __uint_as_float(w[h] & 0xFFFF0000u);
+      }
+    }
+    *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 // Thread-block cluster helpers (the CTA pair of tc_gemm_pair_kernel).
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -614,6 +626,10 @@ template <int BN, bool X3, bool PAIR>
 __device__ __forceinline__ void persistent_body(const PParams& p) {
   using C = PCfg<BN, X3>;
   constexpr int OUT_PLANES = X3 ? 3 : 1;
+  // X3 epilogue of a CTA's last tile: 4 KB buffers per epilogue warp (one
+  // per plane of each of its 64-column chunks), taken from pipeline memory
+  constexpr int kX3LastBufs = (BN / 128) * OUT_PLANES;
+  static_assert(!X3 || P_EPI_WARPS * kX3LastBufs * 4096 <= C::STAGES * C::STAGE_BYTES, "X3 staging");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -669,6 +685,7 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
     if (lane == 0) {
       prefetch_tmap(&p.tmA);
       prefetch_tmap(&p.tmB);
+      prefetch_tmap(&p.tmOut);   // the epilogue's first TMA store need not fetch it
       int it = 0;
       bool ok = true;
       for (int t = t0; t < p.num_tiles && ok; t += tstep) {
@@ -763,12 +780,12 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * C::EPI_BUFS * 4096);
-    uint8_t* stage0_ptr = base_ptr + (stage0 - base);
     int tc = 0, chunk = 0, it = 0;
     bool ok = true;
     for (int t = t0; t < p.num_tiles && ok; t += tstep, ++tc) {
       const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
       const int buf = tc & 1;
+      const bool last_tile = t + tstep >= p.num_tiles;
       if (ce_a) {
         // softmax-CE dgrad: every landed A stage (128 rows x 64 logits,
         // 128B-swizzled) becomes dz in place before the MMA reads it; thread
@@ -802,9 +819,6 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
         }
         if (!ok) break;
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), ((uint32_t)tc >> 1) & 1u, p.err));
-      if (!ok) break;
-      tc_fence_after();
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::ACC_COLS);
       const int gm = m0 + q * 32 + lane;
       const bool row_ok = gm < p.M;
@@ -817,7 +831,10 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
       // 64-column chunks of this warp's half of the tile: read from TMEM once,
       // finished in registers, then each output plane is staged in
       // 128B-swizzled shared memory (16-byte unit u of row r at
-      // r*128 + ((u ^ (r & 7)) * 16)) and written by a TMA store.
+      // r*128 + ((u ^ (r & 7)) * 16)) and written by a TMA store.  The
+      // accumulator wait comes after the first chunk's bias / mask loads, so
+      // their latency overlaps the MMAs.
+      bool acc_ready = false;
 #pragma unroll 1
       for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 64) {
         const int gn0 = n0 + c0;
@@ -854,6 +871,12 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
               if (gn0 + 32 + j < p.N && __bfloat162float(ar[32 + j]) > 0.f) mask1 |= 1u << j;
             }
           }
+        }
+        if (!acc_ready) {
+          ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), ((uint32_t)tc >> 1) & 1u, p.err));
+          if (!ok) break;
+          tc_fence_after();
+          acc_ready = true;
         }
         float v[64];
         tmem_ld64(trow + (uint32_t)c0, v);
@@ -956,27 +979,29 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
         }
 #pragma unroll 1
         for (int pl = 0; pl < OUT_PLANES; ++pl, ++chunk) {
-          const int sbuf = chunk % C::EPI_BUFS;
-          if (lane == 0) {   // the store that last used this buffer has read it
-            if (C::EPI_BUFS == 1) bulk_wait_read0();
-            else bulk_wait_read1();
+          // X3, last tile of this CTA: its MMAs are done and no load follows,
+          // so the pipeline memory holds every plane of every chunk of this
+          // warp at once and the stores go out back to back; otherwise the
+          // warp's staging buffers are reused once a store has read them
+          uint32_t sbuf_addr;
+          if (X3 && last_tile) {
+            sbuf_addr = a_base + (uint32_t)((((warp - 2) * kX3LastBufs) + (c0 - half * (BN / 2)) / 64 * OUT_PLANES + pl) * 4096);
+          } else {
+            const int sbuf = chunk % C::EPI_BUFS;
+            if (lane == 0) {   // the store that last used this buffer has read it
+              if (C::EPI_BUFS == 1) bulk_wait_read0();
+              else bulk_wait_read1();
+            }
+            sbuf_addr = stage0 + (uint32_t)(sbuf * 4096);
           }
           __syncwarp();
-          uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint4 w;
-            __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&w);
-#pragma unroll
-            for (int h = 0; h < 4; ++h)
-              w2[h] = __floats2bfloat162_rn(split_plane(v[8 * u + 2 * h], pl), split_plane(v[8 * u + 2 * h + 1], pl));
-            *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) << 4)) = w;
-          }
+          uint8_t* srow = base_ptr + (sbuf_addr - base) + lane * 128;
+          stage_plane(srow, lane, v, pl + 1 < OUT_PLANES);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (!X3) tma_store_2d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32);
-            else tma_store_3d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32, pl);
+            if (!X3) tma_store_2d(&p.tmOut, sbuf_addr, gn0, m0 + q * 32);
+            else tma_store_3d(&p.tmOut, sbuf_addr, gn0, m0 + q * 32, pl);
             bulk_commit();
           }
         }
@@ -1025,8 +1050,11 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
     if (mine && have && ok) {
       const int t = t0;
       const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
-      const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * C::EPI_BUFS * 4096);
-      uint8_t* stage0_ptr = base_ptr + (stage0 - base);
+      // staging: every plane of this warp's chunks at once, in the B half of
+      // the (now idle) pipeline memory; the peer's rows sit in the A half
+      static_assert(!PAIR || P_EPI_WARPS * kX3LastBufs * 4096 <= C::STAGES * C::B_BYTES, "pair staging");
+      static_assert(!PAIR || 64 * kRP * 4 <= C::STAGES * C::A_BYTES, "pair exchange");
+      const uint32_t stage0 = b_base + (uint32_t)((warp - 2) * kX3LastBufs * 4096);
       const float* rrow = reinterpret_cast<const float*>(base_ptr + (recv - base)) + ((q & 1) * 32 + lane) * kRP;
       const int gm = m0 + q * 32 + lane;
       const bool row_ok = gm < p.M;
@@ -1092,27 +1120,14 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
         }
 #pragma unroll 1
         for (int pl = 0; pl < OUT_PLANES; ++pl, ++chunk) {
-          const int sbuf = chunk % C::EPI_BUFS;
-          if (lane == 0) {
-            if (C::EPI_BUFS == 1) bulk_wait_read0();
-            else bulk_wait_read1();
-          }
-          __syncwarp();
-          uint8_t* srow = stage0_ptr + sbuf * 4096 + lane * 128;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint4 w;
-            __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&w);
-#pragma unroll
-            for (int h = 0; h < 4; ++h)
-              w2[h] = __floats2bfloat162_rn(split_plane(v[8 * u + 2 * h], pl), split_plane(v[8 * u + 2 * h + 1], pl));
-            *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) << 4)) = w;
-          }
+          const uint32_t sbuf_addr = stage0 + (uint32_t)(chunk * 4096);
+          uint8_t* srow = base_ptr + (sbuf_addr - base) + lane * 128;
+          stage_plane(srow, lane, v, pl + 1 < OUT_PLANES);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (!X3) tma_store_2d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32);
-            else tma_store_3d(&p.tmOut, stage0 + sbuf * 4096, gn0, m0 + q * 32, pl);
+            if (!X3) tma_store_2d(&p.tmOut, sbuf_addr, gn0, m0 + q * 32);
+            else tma_store_3d(&p.tmOut, sbuf_addr, gn0, m0 + q * 32, pl);
             bulk_commit();
           }
         }
@@ -1268,6 +1283,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
     if (lane == 0) {
       prefetch_tmap(&p.tmA);
       prefetch_tmap(&p.tmB);
+      prefetch_tmap(&p.tmOut);   // the epilogue's first TMA store need not fetch it
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
