@@ -440,6 +440,9 @@ int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen) {
   rec->block = dim3(kHT);
   rec->smem = (unsigned)sizeof(HeadSmem);
   rec->name = mse ? "head_mse" : "head_ce";
+  // at most one wave of CTAs: scheduled early, they wait beside the
+  // predecessor at a few CTAs per SM
+  rec->early = true;
   rec->set_args(q);
   return 1;
 }

@@ -23,10 +23,11 @@ struct LaunchRec {
   static constexpr int kMaxDeps = 4;
   int deps[kMaxDeps] = {0, 0, 0, 0};
   int ndeps = -1;
-  // May be scheduled before its predecessor ends (programmatic edge): worth it
-  // for kernels with a real prologue (barriers, TMEM) and one CTA per SM.
-  // Kernels of many small CTAs would crowd onto the SMs the predecessor
-  // leaves idle and then run there, so they keep full edges.
+  // May be scheduled before its predecessor ends (programmatic edge from the
+  // first dependency): worth it for kernels with a real prologue (barriers,
+  // TMEM) and at most one wave of CTAs.  Kernels of many small CTAs would
+  // crowd onto the SMs the predecessor leaves idle and then run there, so
+  // they keep full edges.
   bool early = false;
   alignas(128) unsigned char args[kMaxArgBytes];
 

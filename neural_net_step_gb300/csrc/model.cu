@@ -628,10 +628,12 @@ mlp_status launch_graph(mlp* m, int key, std::vector<LaunchRec>& recs, cudaStrea
   if (!gc->exec) {
     CUDA_TRY(cudaGraphCreate(&gc->graph, 0));
     // Each record depends on the one before it unless it names its own
-    // dependencies (the side chain of weight gradients).  With pdl a
-    // single-dependency edge is programmatic: the kernel may be scheduled once
-    // every block of its predecessor has started, and waits inside
-    // (griddepcontrol.wait) for the predecessor to complete.
+    // dependencies (the side chain of weight gradients).  With pdl the edge
+    // from an early-launch record's first dependency (its predecessor on the
+    // main chain) is programmatic: the kernel may be scheduled once every
+    // block of that predecessor has started, and waits inside
+    // (griddepcontrol.wait) for it to complete.  Its other dependencies stay
+    // full edges (complete before the launch).
     cudaGraphEdgeData ed;
     memset(&ed, 0, sizeof(ed));
     ed.from_port = cudaGraphKernelNodePortProgrammatic;
@@ -651,9 +653,10 @@ mlp_status launch_graph(mlp* m, int key, std::vector<LaunchRec>& recs, cudaStrea
       void* argp[1];
       cudaKernelNodeParams kp = node_params(r, argp);
       cudaGraphNode_t node;
-      if (nd == 1 && m->pdl && r.early) {
+      if (nd >= 1 && m->pdl && r.early) {
         CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, nullptr, 0, &kp));
         CUDA_TRY(cudaGraphAddDependencies(gc->graph, dn, &node, &ed, 1));
+        for (int k = 1; k < nd; ++k) CUDA_TRY(cudaGraphAddDependencies(gc->graph, dn + k, &node, nullptr, 1));
       } else {
         CUDA_TRY(cudaGraphAddKernelNode(&node, gc->graph, nd ? dn : nullptr, nd, &kp));
       }

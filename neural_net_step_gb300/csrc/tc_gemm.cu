@@ -1014,13 +1014,51 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
     // ---------------- the pair's epilogue (every thread of both CTAs) ----------------
     // CTA rank r finishes rows 64 r .. 64 r + 63 (TMEM lane quarters 2r, 2r+1)
     // and sends the other 64 rows (big + small accumulators added) to its
-    // peer's pipeline memory, padded rows of kRP floats.
+    // peer's pipeline memory, padded rows of kRP floats.  Each epilogue warp
+    // holds one 32-row x 64-column chunk; the finishing warps load their bias
+    // / mask before the accumulator is ready and read their own TMEM while
+    // the peer's rows are in flight.
+    static_assert(!PAIR || BN == 128, "one 64-column chunk per epilogue warp");
     constexpr int kRP = BN + 4;
     const bool have = t0 < p.num_tiles;   // the same for both CTAs of the pair
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const bool mine = warp >= 2 && (q >> 1) == pr;
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    const int m0 = have ? (t0 / p.tiles_n) * BM : 0, n0 = have ? (t0 % p.tiles_n) * BN : 0;
+    const int c0 = half * (BN / 2);
+    const int gn0 = n0 + c0;
+    const int gm = m0 + q * 32 + lane;
+    const bool row_ok = gm < p.M;
+    float bias0 = 0.f, bias1 = 0.f;
+    uint32_t mask0 = 0u, mask1 = 0u;
+    if (mine && have) {
+      if (p.kind == GEMM_FWD) {
+        if (gn0 + lane < p.N) bias0 = __ldg(p.bias + gn0 + lane);
+        if (gn0 + 32 + lane < p.N) bias1 = __ldg(p.bias + gn0 + 32 + lane);
+      } else if (p.act == ACT_RELU && row_ok) {
+        const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
+        if (gn0 + 64 <= p.N) {
+          uint4 a[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) a[u] = __ldg(reinterpret_cast<const uint4*>(ar) + u);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&a[u]);
+            uint32_t bits = 0u;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) bits |= (__bfloat162float(e[h]) > 0.f ? 1u : 0u) << h;
+            if (u < 4) mask0 |= bits << (8 * u);
+            else mask1 |= bits << (8 * (u - 4));
+          }
+        } else {
+          for (int j = 0; j < 32; ++j) {
+            if (gn0 + j < p.N && __bfloat162float(ar[j]) > 0.f) mask0 |= 1u << j;
+            if (gn0 + 32 + j < p.N && __bfloat162float(ar[32 + j]) > 0.f) mask1 |= 1u << j;
+          }
+        }
+      }
+    }
     bool ok = true;
     if (warp >= 2 && have) {
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(0), 0u, p.err));
@@ -1028,108 +1066,62 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
     }
     cluster_sync_all();   // both CTAs' MMAs are done: their pipeline memory is free
     const uint32_t recv = a_base;   // [64][kRP] fp32
-    if (warp >= 2 && !mine && have && ok) {
-      const uint32_t peer = mapa_cluster(recv, (uint32_t)(pr ^ 1)) +
-                            (uint32_t)((((q & 1) * 32 + lane) * kRP + half * (BN / 2)) * 4);
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN / 2; c0 += 64) {
-        float v[64];
-        tmem_ld64(trow + (uint32_t)(half * (BN / 2) + c0), v);
+    float v[64];
+    if (warp >= 2 && have && ok) {   // this warp's chunk: hi x hi + the five smaller products
+      tmem_ld64(trow + (uint32_t)c0, v);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float w[32];
-          tmem_ld32(trow + (uint32_t)(BN + half * (BN / 2) + c0 + 32 * hh), w, 0);
+      for (int hh = 0; hh < 2; ++hh) {
+        float w[32];
+        tmem_ld32(trow + (uint32_t)(BN + c0 + 32 * hh), w, 0);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[32 * hh + j] += w[j];
-        }
+        for (int j = 0; j < 32; ++j) v[32 * hh + j] += w[j];
+      }
+      if (!mine) {   // the peer finishes these rows
+        const uint32_t peer =
+            mapa_cluster(recv, (uint32_t)(pr ^ 1)) + (uint32_t)((((q & 1) * 32 + lane) * kRP + c0) * 4);
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) st_cluster_v4(peer + (uint32_t)((c0 + j) * 4), v[j], v[j + 1], v[j + 2], v[j + 3]);
+        for (int j = 0; j < 64; j += 4) st_cluster_v4(peer + (uint32_t)(j * 4), v[j], v[j + 1], v[j + 2], v[j + 3]);
       }
     }
     cluster_sync_all();   // the peer's rows have landed
     if (mine && have && ok) {
-      const int t = t0;
-      const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
-      // staging: every plane of this warp's chunks at once, in the B half of
+      // staging: every plane of this warp's chunk at once, in the B half of
       // the (now idle) pipeline memory; the peer's rows sit in the A half
       static_assert(!PAIR || P_EPI_WARPS * kX3LastBufs * 4096 <= C::STAGES * C::B_BYTES, "pair staging");
       static_assert(!PAIR || 64 * kRP * 4 <= C::STAGES * C::A_BYTES, "pair exchange");
       const uint32_t stage0 = b_base + (uint32_t)((warp - 2) * kX3LastBufs * 4096);
       const float* rrow = reinterpret_cast<const float*>(base_ptr + (recv - base)) + ((q & 1) * 32 + lane) * kRP;
-      const int gm = m0 + q * 32 + lane;
-      const bool row_ok = gm < p.M;
-      int chunk = 0;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {   // + the peer's partial sums of these rows
+        const float4 r4 = *reinterpret_cast<const float4*>(rrow + c0 + j);
+        v[j] += r4.x; v[j + 1] += r4.y; v[j + 2] += r4.z; v[j + 3] += r4.w;
+      }
+      if (p.kind == GEMM_FWD) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          v[j] += __shfl_sync(0xffffffffu, bias0, j);
+          v[32 + j] += __shfl_sync(0xffffffffu, bias1, j);
+        }
+#pragma unroll
+        for (int j = 0; j < 64; ++j) v[j] = apply_act(v[j], p.act);
+      } else if (p.act == ACT_RELU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          v[j] *= (float)((mask0 >> j) & 1u);
+          v[32 + j] *= (float)((mask1 >> j) & 1u);
+        }
+      }
 #pragma unroll 1
-      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 64) {
-        const int gn0 = n0 + c0;
-        float bias0 = 0.f, bias1 = 0.f;
-        uint32_t mask0 = 0u, mask1 = 0u;
-        if (p.kind == GEMM_FWD) {
-          if (gn0 + lane < p.N) bias0 = __ldg(p.bias + gn0 + lane);
-          if (gn0 + 32 + lane < p.N) bias1 = __ldg(p.bias + gn0 + 32 + lane);
-        } else if (p.act == ACT_RELU && row_ok) {
-          const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
-          if (gn0 + 64 <= p.N) {
-            uint4 a[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) a[u] = __ldg(reinterpret_cast<const uint4*>(ar) + u);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&a[u]);
-              uint32_t bits = 0u;
-#pragma unroll
-              for (int h = 0; h < 8; ++h) bits |= (__bfloat162float(e[h]) > 0.f ? 1u : 0u) << h;
-              if (u < 4) mask0 |= bits << (8 * u);
-              else mask1 |= bits << (8 * (u - 4));
-            }
-          } else {
-            for (int j = 0; j < 32; ++j) {
-              if (gn0 + j < p.N && __bfloat162float(ar[j]) > 0.f) mask0 |= 1u << j;
-              if (gn0 + 32 + j < p.N && __bfloat162float(ar[32 + j]) > 0.f) mask1 |= 1u << j;
-            }
-          }
-        }
-        float v[64];
-        tmem_ld64(trow + (uint32_t)c0, v);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float w[32];
-          tmem_ld32(trow + (uint32_t)(BN + c0 + 32 * hh), w, 0);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[32 * hh + j] += w[j];
-        }
-#pragma unroll
-        for (int j = 0; j < 64; j += 4) {   // + the peer's partial sums of these rows
-          const float4 r4 = *reinterpret_cast<const float4*>(rrow + c0 + j);
-          v[j] += r4.x; v[j + 1] += r4.y; v[j + 2] += r4.z; v[j + 3] += r4.w;
-        }
-        if (p.kind == GEMM_FWD) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] += __shfl_sync(0xffffffffu, bias0, j);
-            v[32 + j] += __shfl_sync(0xffffffffu, bias1, j);
-          }
-#pragma unroll
-          for (int j = 0; j < 64; ++j) v[j] = apply_act(v[j], p.act);
-        } else if (p.act == ACT_RELU) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] *= (float)((mask0 >> j) & 1u);
-            v[32 + j] *= (float)((mask1 >> j) & 1u);
-          }
-        }
-#pragma unroll 1
-        for (int pl = 0; pl < OUT_PLANES; ++pl, ++chunk) {
-          const uint32_t sbuf_addr = stage0 + (uint32_t)(chunk * 4096);
-          uint8_t* srow = base_ptr + (sbuf_addr - base) + lane * 128;
-          stage_plane(srow, lane, v, pl + 1 < OUT_PLANES);
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if (!X3) tma_store_2d(&p.tmOut, sbuf_addr, gn0, m0 + q * 32);
-            else tma_store_3d(&p.tmOut, sbuf_addr, gn0, m0 + q * 32, pl);
-            bulk_commit();
-          }
+      for (int pl = 0; pl < OUT_PLANES; ++pl) {
+        const uint32_t sbuf_addr = stage0 + (uint32_t)(pl * 4096);
+        uint8_t* srow = base_ptr + (sbuf_addr - base) + lane * 128;
+        stage_plane(srow, lane, v, pl + 1 < OUT_PLANES);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (!X3) tma_store_2d(&p.tmOut, sbuf_addr, gn0, m0 + q * 32);
+          else tma_store_3d(&p.tmOut, sbuf_addr, gn0, m0 + q * 32, pl);
+          bulk_commit();
         }
       }
       if (lane == 0) bulk_wait_all();
