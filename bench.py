@@ -72,6 +72,9 @@ def layer_work(w, kind, l, x3=False):
             return 2 * B * K * N, es * (B * N + B * K) + 4 * (N * K + N)
         return 2 * B * K * N, es * (B * N + N * K + 2 * B * K)
     C = d[L]
+    if kind == "fwd_head":   # the forward GEMM (writing dY in place of h) + the output layer's FFMA work
+        K, N, C = d[l], d[l + 1], d[L]
+        return 2 * B * K * N + 3 * 2 * B * N * C, es * (B * K + N * K + B * N) + 4 * N + 4 * (C * N + C)
     if kind == "head":   # output layer fwd + CE + dgrad + wgrad in one pass over h
         K = d[L - 1]
         return 3 * 2 * B * K * C, es * 3 * B * K + 4 * B + 4 * (C * K + C)
@@ -116,6 +119,10 @@ def attach_work(w, prof):
         if name.endswith("_fwd"):
             kind, l = "fwd", fwd_l
             fwd_l += 1
+        elif name.endswith("_fwd_head"):   # last hidden layer's forward with the output layer in its epilogue
+            kind, l = "fwd_head", fwd_l
+            fwd_l += 1
+            bwd_l = w.n_layers - 2
         elif name == "head_ce":
             kind, l = "head", w.n_layers - 1
             bwd_l = w.n_layers - 2

@@ -189,8 +189,19 @@ mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
  *     and the dgrad below reads the bits instead of the stored activation
  *     (16x fewer bytes).  0 reads the stored activation.  Results are
  *     identical either way. */
+/*   MLP_OPT_HEAD_IN_GEMM (default 1; MLP_F32 models on the tensor cores
+ *     with the fused output layer): fold that output layer (10 classes, 128
+ *     inputs) into the epilogue of the forward GEMM below it, where each
+ *     row's fp32 h is at hand (noeira.ai "Neural networks", "The design in
+ *     one page": the epilogue as the place for fused work): logits, softmax
+ *     CE, dY of the hidden layer and per-CTA partials of the output layer's
+ *     weight / bias gradients and loss, without storing h.  Applies where
+ *     that forward runs on CTA pairs (at most 76 row tiles of 128 and a
+ *     reduction of at least 192); 0, or otherwise, keeps the separate fused
+ *     output-layer kernel.  Same arithmetic in fp32; the sums differ in
+ *     order only. */
 enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2, MLP_OPT_PDL = 3, MLP_OPT_CE_GEMM = 4,
-       MLP_OPT_RELU_BITS = 5 };
+       MLP_OPT_RELU_BITS = 5, MLP_OPT_HEAD_IN_GEMM = 6 };
 mlp_status mlp_set_option(mlp_t* model, int option, int64_t value);
 
 /* The update rule of the training step (default MLP_OPTIM_ADAMW) and global

@@ -149,7 +149,7 @@ def mlp_set_graph_mode(h, enable: bool) -> None:
     _check(lib().mlp_set_graph_mode(h, int(bool(enable))))
 
 
-OPT_GRAPH, OPT_FUSE_HEAD, OPT_F32_TENSOR_CORES, OPT_PDL, OPT_CE_GEMM, OPT_RELU_BITS = 0, 1, 2, 3, 4, 5
+OPT_GRAPH, OPT_FUSE_HEAD, OPT_F32_TENSOR_CORES, OPT_PDL, OPT_CE_GEMM, OPT_RELU_BITS, OPT_HEAD_IN_GEMM = 0, 1, 2, 3, 4, 5, 6
 
 
 def mlp_set_option(h, option: int, value: int) -> None:

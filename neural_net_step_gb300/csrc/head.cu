@@ -385,8 +385,11 @@ HeadPartials head_partials(int64_t B, int64_t C, int64_t K) {
 }
 
 size_t head_workspace_bytes(int64_t B, int64_t C, int64_t K) {
-  const HeadPartials hp = head_partials(B, C, K);
-  return (size_t)(hp.loss_off + hp.n) * 4;
+  // room for this kernel's cluster partials or for those of the same layer
+  // folded into the forward GEMM below it (tc_fused_head_partials)
+  const HeadPartials hp = head_partials(B, C, K), fp = tc_fused_head_partials(B);
+  const int64_t a = hp.loss_off + hp.n, b = fp.loss_off + fp.n;
+  return (size_t)(a > b ? a : b) * 4;
 }
 
 bool head_supported(int64_t C, int64_t K) { return C == kHC && K == kHK; }

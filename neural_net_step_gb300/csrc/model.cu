@@ -280,6 +280,7 @@ struct mlp {
   int loss = MLP_LOSS_CE;
   bool ce_gemm = false;      // softmax-CE inside the GEMMs of a wide bf16 output layer (slower on this part)
   bool relu_bits = true;     // bf16 ReLU masks as bits between the forward and the dgrad
+  bool head_in_gemm = true;  // fp32 planes: the fused output layer inside the forward GEMM below it
   float max_grad_norm = 0.f; // > 0: global-norm clipping of the gradient before the update
   std::mutex mu;
   std::vector<GraphCache> graphs;
@@ -344,7 +345,7 @@ mlp_status add(std::vector<LaunchRec>& out, int n, const LaunchRec* recs) {
 // z buffer).  x3: fp32 model with operands as bf16 planes (the input is
 // split into the arena's xs planes first; hidden outputs are planes).
 mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out, int n_layers = -1,
-                        bool x3 = false, const int32_t* ce_labels = nullptr) {
+                        bool x3 = false, const int32_t* ce_labels = nullptr, const GemmOp* head_fold = nullptr) {
   const Layout& L = m->lay;
   const void* X = x;
   int64_t ldx = L.dims[0], xplane = 0;
@@ -376,6 +377,13 @@ mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out
         op.relu_bits = (uint64_t*)m->at(L.off_bits[l]); op.ld_bits = L.ld_bits[l];
       }
       X = op.out; ldx = L.ld_h[l]; xplane = op.out_plane;
+      if (head_fold && l == n_layers - 1) {   // the output layer in this epilogue: it writes dY, not h
+        op.head_W = head_fold->head_W; op.head_bias = head_fold->head_bias; op.head_labels = head_fold->head_labels;
+        op.head_ws = head_fold->head_ws; op.head_scale = head_fold->head_scale;
+        op.step_counter = head_fold->step_counter; op.bias_corr = head_fold->bias_corr;
+        op.beta1 = head_fold->beta1; op.beta2 = head_fold->beta2;
+        op.out = head_fold->out; op.ldo = head_fold->ldo; op.out_plane = head_fold->out_plane;
+      }
     } else {
       op.act = MLP_ACT_NONE;
       op.out = m->at(L.off_z); op.ldo = L.ldz;
@@ -400,14 +408,35 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
   // forward's epilogue, dz formed from the stored logits by dgrad and wgrad)
   const bool ce_gemm = !mse && !fuse && m->ce_gemm && L.dtype == MLP_BF16 && L.dims[L.L] >= kCeGemmMinClasses;
   const int64_t dy_plane = L.B * L.max_ld;
-  mlp_status st = plan_forward(m, x, out, fuse ? L.L - 1 : L.L, x3, ce_gemm ? (const int32_t*)y : nullptr);
-  if (st != MLP_OK) return st;
   Ctl* ctl = m->ctl();
+  // fp32 planes: the fused output layer inside the epilogue of the forward
+  // below it, where that forward runs on CTA pairs
+  const bool head_gemm = fuse && x3 && !mse && m->head_in_gemm &&
+                         tc_fused_head_ok(L.B, L.dims[L.L - 1], L.dims[L.L - 2], L.dims[L.L]);
+  GemmOp hf;
+  if (head_gemm) {
+    const int l = L.L - 1;
+    hf.head_W = (const float*)m->weight(l);   // fp32 master weights (an fp32 model)
+    hf.head_bias = m->plane(MLP_PLANE_P) + L.boff[l];
+    hf.head_labels = (const int32_t*)y;
+    hf.head_ws = (float*)m->at(L.off_hws);
+    hf.head_scale = (float)(1.0 / (double)L.B);
+    hf.step_counter = &ctl->step;
+    hf.bias_corr = ctl->bias_corr; hf.beta1 = hp.b1; hf.beta2 = hp.b2;
+    hf.out = m->at(L.off_dy[0]); hf.ldo = L.ld_h[l - 1]; hf.out_plane = dy_plane;
+  }
+  mlp_status st = plan_forward(m, x, out, fuse ? L.L - 1 : L.L, x3, ce_gemm ? (const int32_t*)y : nullptr,
+                               head_gemm ? &hf : nullptr);
+  if (st != MLP_OK) return st;
   const void* dY = m->at(L.off_dz);
   int64_t ldy = L.ldz;
   int buf = 0;
   int top = L.L - 1;   // highest layer whose wgrad/dgrad still has to be planned
-  if (fuse) {
+  if (head_gemm) {
+    dY = hf.out; ldy = hf.ldo;
+    buf = 1;
+    top = L.L - 2;
+  } else if (fuse) {
     // output layer + CE + its VJPs in one kernel; dY of the last hidden layer
     // goes to the first ping-pong buffer
     const int l = L.L - 1;
@@ -567,7 +596,8 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
   for (int k = 0; k < nseg; ++k) ad.seg[ad.nseg++] = seg[k];
   if (fuse) {   // the output layer's gradient and the loss arrive as partial sums
     const int l = L.L - 1;
-    const HeadPartials hpart = head_partials(L.B, L.dims[L.L], L.dims[l]);
+    const HeadPartials hpart =
+        head_gemm ? tc_fused_head_partials(L.B) : head_partials(L.B, L.dims[L.L], L.dims[l]);
     const float* hws = (const float*)m->at(L.off_hws);
     const int64_t nw = L.dims[L.L] * L.dims[l];
     ad.seg[ad.nseg++] = AdamWOp::Seg{L.woff[l], nw, hws, hpart.n, hpart.stride};
@@ -833,6 +863,7 @@ mlp_status mlp_set_option(mlp_t* m, int option, int64_t value) {
     case MLP_OPT_PDL: m->pdl = value != 0; break;
     case MLP_OPT_CE_GEMM: m->ce_gemm = value != 0; break;
     case MLP_OPT_RELU_BITS: m->relu_bits = value != 0; break;
+    case MLP_OPT_HEAD_IN_GEMM: m->head_in_gemm = value != 0; break;
     default: return fail(MLP_ERR_ARG, "unknown option %d", option);
   }
   if (option == MLP_OPT_FUSE_HEAD || option == MLP_OPT_F32_TENSOR_CORES) {   // planes kept current only while used

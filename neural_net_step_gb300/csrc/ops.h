@@ -69,6 +69,22 @@ struct GemmOp {
   const float2* ce_rowstat = nullptr;
   const int32_t* ce_labels = nullptr;
   float ce_scale = 0.f;
+  // The 10-class, 128-input softmax-CE output layer folded into the forward
+  // of the last hidden layer (fp32 planes, CTA pairs, N = 128; head_W != 0):
+  // from each row's fp32 h (never stored) the epilogue forms the logits
+  // z = h W_out^T + b_out, the loss, dz = (softmax(z) - onehot(y)) head_scale
+  // and writes dY = (dz W_out) * act'(h) to `out` (planes) in place of h; the
+  // partial sums over each CTA's rows of dW_out = dz^T h, db_out = sum dz
+  // and the loss go to head_ws (tc_fused_head_partials layout), and block 0
+  // advances the step counter (AdamW's bias corrections to bias_corr).
+  const float* head_W = nullptr;       // fp32 [10, 128]
+  const float* head_bias = nullptr;    // fp32 [10]
+  const int32_t* head_labels = nullptr;
+  float* head_ws = nullptr;
+  float head_scale = 0.f;
+  int64_t* step_counter = nullptr;
+  float* bias_corr = nullptr;
+  float beta1 = 0.9f, beta2 = 0.999f;
 };
 
 // Number of K splits the wgrad of this shape uses, and the workspace bytes.
@@ -233,6 +249,11 @@ size_t head_workspace_bytes(int64_t B, int64_t C, int64_t K);
 // floats, then n loss partials starting at float offset `loss_off`.
 struct HeadPartials { int n; int64_t stride; int64_t loss_off; };
 HeadPartials head_partials(int64_t B, int64_t C, int64_t K);
+// The same output layer folded into the forward GEMM of the layer below
+// (GemmOp::head_W): possible for an M x N x K fp32-as-planes forward that
+// runs on CTA pairs with N = 128 and C = 10; one partial per 128-row tile.
+bool tc_fused_head_ok(int64_t M, int64_t N, int64_t K, int64_t C);
+HeadPartials tc_fused_head_partials(int64_t M);
 int head_plan(const HeadOp& op, LaunchRec* rec, char* err, size_t errlen);
 
 // One thread waits, through the bounded wait every tcgen05 kernel uses, for

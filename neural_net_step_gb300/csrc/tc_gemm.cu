@@ -494,7 +494,19 @@ struct PParams {
   // ReLU mask as bits (bf16, one CTA per tile): written by the forward,
   // read by the dgrad in place of the stored activation
   uint64_t* relu_bits; int64_t ld_bits;
+  // The 10-class output layer folded into this forward (CTA pairs, X3,
+  // N = 128): `out` receives dY of this layer; per-CTA partials of dW_out
+  // (row-major [10][128]) and db_out at head_ws + tile * kFhPitch, the
+  // tile's loss sum at head_ws + head_loss_off + tile (tile = the pair's row tile)
+  const float* head_W; const float* head_bias; const int32_t* head_labels;
+  float* head_ws; int64_t head_loss_off; float head_scale;
+  int64_t* step_counter; float* bias_corr; float beta1, beta2;
 };
+
+constexpr int kFhC = 10, kFhK = 128;   // classes, inputs of the folded output layer
+constexpr int kFhPart = kFhC * kFhK + kFhC;   // dW_out + db_out partial length
+constexpr int kFhPitch = 1292;                 // partial pitch, rounded up to 16 bytes
+constexpr int kFhZ = 11;                // padded pitch of a row's 10 logits / dz in shared memory
 
 // dz of softmax-CE from a stored logit: (exp(z - M) invS - onehot) scale, or 0
 // outside the batch rows / classes.
@@ -604,6 +616,9 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t a, float x, float y, floa
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w)
                : "memory");
 }
+__device__ __forceinline__ void st_cluster_f32(uint32_t a, float x) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(x) : "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"((uint64_t)tm),
                "r"(src), "r"(c0), "r"(c1)
@@ -614,6 +629,10 @@ __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Named barrier `id` over `n` threads (whole warps) of this CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 // X3: fp32 operands as three bf16 planes (3-D maps, six K-loop phases) and
 // an fp32 result written as its three planes.
@@ -668,6 +687,10 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
   pdl_enter();   // shared memory and TMEM are set up: now wait for the inputs
+  // the folded output layer takes over the step counter (nothing before the
+  // optimizer reads it)
+  if (PAIR && p.step_counter && blockIdx.x == 0 && threadIdx.x == 0)
+    advance_step(p.step_counter, p.bias_corr, p.beta1, p.beta2);
   const uint32_t stage_tx = C::STAGE_BYTES;
   // tiles walked by this CTA (a pair walks them together) and its K stages
   const int pr = PAIR ? (int)cluster_ctarank() : 0;
@@ -1059,11 +1082,36 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
         }
       }
     }
+    // the folded output layer: its weights into shared memory (the epilogue
+    // staging area, which the pair does not use), its bias and this row's
+    // label, all before the accumulator is ready
+    const bool fh = PAIR && p.head_W != nullptr;
+    // its partial sums: this CTA's (sP) and, in rank 0, rank 1's (sP2)
+    const uint32_t fh_p_addr = epi_base + (uint32_t)((kFhC * kFhK + 2 * 64 * kFhZ + 64) * 4);
+    const uint32_t fh_p2_addr = fh_p_addr + (uint32_t)(kFhPitch * 4);
+    float hbias[kFhC];
+#pragma unroll
+    for (int c = 0; c < kFhC; ++c) hbias[c] = 0.f;
+    int hy = 0;
+    if (fh && have && warp >= 2) {
+      const int e = (int)threadIdx.x - 64;   // 0 .. 255 over the epilogue warps
+      float* sW = reinterpret_cast<float*>(base_ptr + (epi_base - base));
+      for (int i = e; i < kFhC * kFhK / 4; i += 256)
+        reinterpret_cast<float4*>(sW)[i] = __ldg(reinterpret_cast<const float4*>(p.head_W) + i);
+      if (e < 64) {   // the softmax of row e (below): its bias and label
+#pragma unroll
+        for (int c = 0; c < kFhC; ++c) hbias[c] = __ldg(p.head_bias + c);
+        if (m0 + 64 * pr + e < p.M) hy = __ldg(p.head_labels + m0 + 64 * pr + e);
+      }
+    }
     bool ok = true;
     if (warp >= 2 && have) {
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(0), 0u, p.err));
       tc_fence_after();
     }
+    // one verdict for the whole CTA: the finishing warps below meet at named
+    // barriers, so either all of them run or none
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
     cluster_sync_all();   // both CTAs' MMAs are done: their pipeline memory is free
     const uint32_t recv = a_base;   // [64][kRP] fp32
     float v[64];
@@ -1084,13 +1132,14 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
       }
     }
     cluster_sync_all();   // the peer's rows have landed
+    // staging: every plane of a finishing warp's chunk at once, in the B half
+    // of the (now idle) pipeline memory; the peer's rows sit in the A half
+    static_assert(!PAIR || P_EPI_WARPS * kX3LastBufs * 4096 <= C::STAGES * C::B_BYTES, "pair staging");
+    static_assert(!PAIR || 64 * kRP * 4 <= C::STAGES * C::A_BYTES, "pair exchange");
+    const uint32_t stage0 = b_base + (uint32_t)((warp - 2) * kX3LastBufs * 4096);
+    float* sD = reinterpret_cast<float*>(base_ptr + (recv - base));   // [64][kRP]: the peer's rows, then dY
     if (mine && have && ok) {
-      // staging: every plane of this warp's chunk at once, in the B half of
-      // the (now idle) pipeline memory; the peer's rows sit in the A half
-      static_assert(!PAIR || P_EPI_WARPS * kX3LastBufs * 4096 <= C::STAGES * C::B_BYTES, "pair staging");
-      static_assert(!PAIR || 64 * kRP * 4 <= C::STAGES * C::A_BYTES, "pair exchange");
-      const uint32_t stage0 = b_base + (uint32_t)((warp - 2) * kX3LastBufs * 4096);
-      const float* rrow = reinterpret_cast<const float*>(base_ptr + (recv - base)) + ((q & 1) * 32 + lane) * kRP;
+      const float* rrow = sD + ((q & 1) * 32 + lane) * kRP;
 #pragma unroll
       for (int j = 0; j < 64; j += 4) {   // + the peer's partial sums of these rows
         const float4 r4 = *reinterpret_cast<const float4*>(rrow + c0 + j);
@@ -1111,6 +1160,149 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
           v[32 + j] *= (float)((mask1 >> j) & 1u);
         }
       }
+    }
+    if (fh && have && ok && warp >= 2) {
+      // the folded output layer over this CTA's 64 rows (row r = 32 (q % 2) +
+      // lane of a finishing warp; batch row m0 + 64 rank + r), shared by all
+      // eight epilogue warps (thread e).  It runs once per CTA: short rolled
+      // loops over rows held in shared memory (h in sH; dY into sD, whose
+      // peer rows have been added).
+      static_assert(!PAIR || (kFhC * kFhK + 2 * 64 * kFhZ + 64 + 2 * kFhPitch) * 4 <= C::EPI_BYTES, "head smem");
+      static_assert(!PAIR || 2 * 64 * kRP * 4 <= C::STAGES * C::A_BYTES, "head rows");
+      const float* sW = reinterpret_cast<const float*>(base_ptr + (epi_base - base));   // [10][128]
+      float* sZ = reinterpret_cast<float*>(base_ptr + (epi_base - base)) + kFhC * kFhK;  // [64][kFhZ]: logits
+      float* sDz = sZ + 64 * kFhZ;                                                      // [64][kFhZ]: dz
+      float* sL = sDz + 64 * kFhZ;                                                      // [64]: row losses
+      float* sH = sD + 64 * kRP;                                                        // [64][kRP]: h
+      const int e = (int)threadIdx.x - 64;
+      if (mine) {
+        float* hrow = sH + ((q & 1) * 32 + lane) * kRP + c0;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(hrow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
+      named_bar_sync(1, 256);   // h and the weights are in shared memory
+      {   // logits of row e % 64, classes e / 64, + 4, + 8
+        const int r = e & 63, g = e >> 6;
+        const bool g3 = g + 8 < kFhC;
+        const float* hr = sH + r * kRP;
+        const float* w0 = sW + g * kFhK;
+        const float* w1 = sW + (g + 4) * kFhK;
+        const float* w2 = sW + (g3 ? g + 8 : g) * kFhK;
+        float z0 = 0.f, z1 = 0.f, z2 = 0.f;
+#pragma unroll 2
+        for (int k = 0; k < kFhK; k += 4) {
+          const float4 h4 = *reinterpret_cast<const float4*>(hr + k);
+          const float4 a = *reinterpret_cast<const float4*>(w0 + k);
+          const float4 b = *reinterpret_cast<const float4*>(w1 + k);
+          const float4 c = *reinterpret_cast<const float4*>(w2 + k);
+          z0 = fmaf(h4.x, a.x, z0); z0 = fmaf(h4.y, a.y, z0); z0 = fmaf(h4.z, a.z, z0); z0 = fmaf(h4.w, a.w, z0);
+          z1 = fmaf(h4.x, b.x, z1); z1 = fmaf(h4.y, b.y, z1); z1 = fmaf(h4.z, b.z, z1); z1 = fmaf(h4.w, b.w, z1);
+          z2 = fmaf(h4.x, c.x, z2); z2 = fmaf(h4.y, c.y, z2); z2 = fmaf(h4.z, c.z, z2); z2 = fmaf(h4.w, c.w, z2);
+        }
+        sZ[r * kFhZ + g] = z0;
+        sZ[r * kFhZ + g + 4] = z1;
+        if (g3) sZ[r * kFhZ + g + 8] = z2;
+      }
+      named_bar_sync(1, 256);
+      if (e < 64) {   // softmax cross-entropy of row e: dz (0 past the batch) and its loss
+        const bool rok = m0 + 64 * pr + e < p.M;
+        float z[kFhC];
+#pragma unroll
+        for (int c = 0; c < kFhC; ++c) z[c] = sZ[e * kFhZ + c] + hbias[c];
+        float mx = z[0], zy = 0.f;
+#pragma unroll
+        for (int c = 0; c < kFhC; ++c) {
+          mx = fmaxf(mx, z[c]);
+          if (c == hy) zy = z[c];
+        }
+        float se = 0.f;
+#pragma unroll
+        for (int c = 0; c < kFhC; ++c) {
+          z[c] = expf(z[c] - mx);
+          se += z[c];
+        }
+        const float inv = 1.0f / se;
+#pragma unroll
+        for (int c = 0; c < kFhC; ++c)
+          sDz[e * kFhZ + c] = rok ? (z[c] * inv - (c == hy ? 1.f : 0.f)) * p.head_scale : 0.f;
+        float lr = 0.f;
+        if (rok) {
+          if (hy < 0 || hy >= kFhC) {
+            if (p.err) atomicOr(p.err, ERRBIT_LABEL_RANGE);
+          } else {
+            lr = (mx + logf(se)) - zy;
+          }
+        }
+        sL[e] = lr;
+      }
+      named_bar_sync(1, 256);   // dz and the losses are in shared memory
+      {   // dY = (dz W) * act'(h) of row e % 64, columns 32 (e / 64) .. + 31, into sD
+          // (a warp reads the same weights: broadcast)
+        const int r = e & 63, cq = (e >> 6) * 32;
+        float dz[kFhC];
+#pragma unroll
+        for (int c = 0; c < kFhC; ++c) dz[c] = sDz[r * kFhZ + c];
+        const float* hr = sH + r * kRP + cq;
+        float* dr = sD + r * kRP + cq;
+#pragma unroll 1
+        for (int j = 0; j < 32; j += 4) {
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < kFhC; ++c) {
+            const float4 w = *reinterpret_cast<const float4*>(sW + c * kFhK + cq + j);
+            a.x = fmaf(dz[c], w.x, a.x);
+            a.y = fmaf(dz[c], w.y, a.y);
+            a.z = fmaf(dz[c], w.z, a.z);
+            a.w = fmaf(dz[c], w.w, a.w);
+          }
+          if (p.act == ACT_RELU) {
+            const float4 h4 = *reinterpret_cast<const float4*>(hr + j);
+            a.x = h4.x > 0.f ? a.x : 0.f;
+            a.y = h4.y > 0.f ? a.y : 0.f;
+            a.z = h4.z > 0.f ? a.z : 0.f;
+            a.w = h4.w > 0.f ? a.w : 0.f;
+          }
+          *reinterpret_cast<float4*>(dr + j) = a;
+        }
+      }
+      {   // this CTA's partial sums over its 64 rows: dW_out at column e % 128
+          // for classes 5 (e / 128) .. + 4; db_out (e < 10) and the loss
+          // (e = 10).  Rank 0 keeps its partial (sP), rank 1 writes its own
+          // into rank 0's sP2; rank 0 adds the two below.
+        const int col = e & 127, ch = e >> 7;
+        float acc[5];
+#pragma unroll
+        for (int k = 0; k < 5; ++k) acc[k] = 0.f;
+#pragma unroll 2
+        for (int r = 0; r < 64; ++r) {
+          const float h = sH[r * kRP + col];
+#pragma unroll
+          for (int k = 0; k < 5; ++k) acc[k] = fmaf(sDz[r * kFhZ + 5 * ch + k], h, acc[k]);
+        }
+        const uint32_t dst = pr == 0 ? fh_p_addr : mapa_cluster(fh_p2_addr, 0u);
+#pragma unroll
+        for (int k = 0; k < 5; ++k) st_cluster_f32(dst + 4u * (uint32_t)((5 * ch + k) * kFhK + col), acc[k]);
+        if (e < kFhC) {
+          float a = 0.f;
+          for (int r = 0; r < 64; ++r) a += sDz[r * kFhZ + e];
+          st_cluster_f32(dst + 4u * (uint32_t)(kFhC * kFhK + e), a);
+        } else if (e == kFhC) {
+          float a = 0.f;
+          for (int r = 0; r < 64; ++r) a += sL[r];
+          st_cluster_f32(dst + 4u * (uint32_t)kFhPart, a);
+        }
+      }
+      named_bar_sync(1, 256);   // every dY row is in sD
+      if (mine) {   // this warp's dY chunk back into v for the planes
+        const float* drow = sD + ((q & 1) * 32 + lane) * kRP + c0;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(drow + j);
+          v[j] = a.x; v[j + 1] = a.y; v[j + 2] = a.z; v[j + 3] = a.w;
+        }
+      }
+    }
+    if (mine && have && ok) {
 #pragma unroll 1
       for (int pl = 0; pl < OUT_PLANES; ++pl) {
         const uint32_t sbuf_addr = stage0 + (uint32_t)(pl * 4096);
@@ -1126,6 +1318,22 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
       }
       if (lane == 0) bulk_wait_all();
       __syncwarp();
+    }
+    if (fh && have) {
+      // the pair's partial sums: rank 1's have landed in rank 0's sP2 (the
+      // barrier orders them); rank 0 adds them to its own and writes the
+      // tile's partial (row-major dW_out, then db_out) and loss sum
+      cluster_sync_all();
+      if (pr == 0) {
+        const float* sP = reinterpret_cast<const float*>(base_ptr + (fh_p_addr - base));
+        const float* sP2 = reinterpret_cast<const float*>(base_ptr + (fh_p2_addr - base));
+        const int tile = (int)(blockIdx.x >> 1);
+        for (int i = threadIdx.x; i <= kFhPart; i += blockDim.x) {
+          const float a = sP[i] + sP2[i];
+          if (i < kFhPart) p.head_ws[(int64_t)tile * kFhPitch + i] = a;
+          else p.head_ws[p.head_loss_off + tile] = a;
+        }
+      }
     }
   }
   tc_fence_before();
@@ -1796,6 +2004,17 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
     }
     p.relu_bits = op.relu_bits; p.ld_bits = op.ld_bits;
   }
+  if (op.head_W) {   // the output layer folded into this forward
+    if (!pair || op.kind != GEMM_FWD || op.N != tc::kFhK || BN != 128 || !op.head_bias || !op.head_labels ||
+        !op.head_ws || (op.act != ACT_RELU && op.act != ACT_NONE) || ((uintptr_t)op.head_W & 15)) {
+      snprintf(err, errlen, "folded output layer: fp32-plane forward on CTA pairs, N = 128, ReLU or none, "
+                            "16-byte aligned weights");
+      return -1;
+    }
+    p.head_W = op.head_W; p.head_bias = op.head_bias; p.head_labels = op.head_labels;
+    p.head_ws = op.head_ws; p.head_loss_off = tc_fused_head_partials(op.M).loss_off; p.head_scale = op.head_scale;
+    p.step_counter = op.step_counter; p.bias_corr = op.bias_corr; p.beta1 = op.beta1; p.beta2 = op.beta2;
+  }
   LaunchRec& r = recs[0];
   if (pair) {
     r.func = tcpair_kernel_ptr();
@@ -1813,11 +2032,23 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   r.grid = dim3(pair ? (unsigned)(2 * p.num_tiles) : (unsigned)(p.num_tiles < sms ? p.num_tiles : sms));
   r.block = dim3(tc::P_THREADS);
   r.early = true;
-  r.name = op.kind == GEMM_FWD ? "tc_gemm_fwd" : "tc_gemm_dgrad";
+  r.name = op.head_W ? "tc_gemm_fwd_head" : op.kind == GEMM_FWD ? "tc_gemm_fwd" : "tc_gemm_dgrad";
   r.set_args(p);
   return 1;
 }
 }  // namespace
+
+bool tc_fused_head_ok(int64_t M, int64_t N, int64_t K, int64_t C) {
+  // the CTA-pair condition of tc_persistent_plan for fp32 planes (N = 128:
+  // one column tile, so a pair holds whole rows)
+  return C == tc::kFhC && N == tc::kFhK && M >= 1 && M <= INT32_MAX && K >= 1 &&
+         2 * ceil_div(M, tc::BM) <= device_sms() && ceil_div(K, tc::BK) >= 3;
+}
+
+HeadPartials tc_fused_head_partials(int64_t M) {
+  const int n = (int)ceil_div(M, tc::BM);   // one per row tile (CTA pair)
+  return HeadPartials{n, tc::kFhPitch, (int64_t)n * tc::kFhPitch};
+}
 
 int wait_timeout_check_plan(uint32_t* err_dev, uint64_t limit_ns, LaunchRec* rec) {
   const tc::WaitCheckParams q{err_dev, limit_ns};

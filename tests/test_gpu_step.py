@@ -19,12 +19,14 @@ DEV = "cuda:0"
 W = synth.WORKLOADS
 
 
-def make_model(w: synth.Workload, batch=None, params=None, graph=True, f32_tc=None):
+def make_model(w: synth.Workload, batch=None, params=None, graph=True, f32_tc=None, head_gemm=None):
     B = w.batch if batch is None else batch
     m = nn.Model(w.dims, w.acts, nn.ACT_RELU, w.dtype, seed=w.seed, batch=B)
     m.set_graph_mode(graph)
     if f32_tc is not None:
         m.set_option(nn.OPT_F32_TENSOR_CORES, f32_tc)
+    if head_gemm is not None:
+        m.set_option(nn.OPT_HEAD_IN_GEMM, head_gemm)
     if params is not None:
         m.write_flat(P.flat([p.numpy() for p in params]).astype(np.float32), nn.PLANE_P, 0)
     return m
@@ -48,14 +50,14 @@ def gpu_run(m: nn.Model, w: synth.Workload, bl, one_graph=False):
             m.split(g.astype(np.float64)))
 
 
-def fp32_one_step(w: synth.Workload, batch=None, f32_tc=None):
+def fp32_one_step(w: synth.Workload, batch=None, f32_tc=None, head_gemm=None):
     """One fp32 step from a shared state: loss, every gradient element and
     every parameter element against the oracle with the arithmetic-derived
     bounds of tests/parity.py."""
     B = w.batch if batch is None else batch
     params0 = synth.make_params(w)
     bl = P.batches(w, 1, B)
-    m = make_model(w, B, params0, f32_tc=f32_tc)
+    m = make_model(w, B, params0, f32_tc=f32_tc, head_gemm=head_gemm)
     g_losses, g_params, g_grads = gpu_run(m, w, bl)
     m.close()
     o_losses, o_params, _, _, o_grads = P.oracle_run(w, params0, bl, "fp64")
@@ -124,6 +126,32 @@ def test_mnist_mlp_b4096_one_step_full_size(f32_tc):
 @pytest.mark.parametrize("f32_tc", F32_MODES)
 def test_mnist_mlp_ragged_batch_one_step(f32_tc):
     fp32_one_step(W["mnist_mlp_b64"], batch=333, f32_tc=f32_tc)
+
+
+@pytest.mark.parametrize("batch", [4096, 333, 64])
+def test_mnist_mlp_separate_output_layer_kernel_one_step(batch):
+    """With the output layer kept out of the forward GEMM's epilogue
+    (MLP_OPT_HEAD_IN_GEMM 0) the step runs the separate fused output-layer
+    kernel; element by element within the same fp32 bounds."""
+    fp32_one_step(W["mnist_mlp_b4096"], batch=batch, f32_tc=1, head_gemm=0)
+
+
+def test_mnist_mlp_output_layer_placement():
+    """By default the fp32-plane step folds the output layer into the layer-2
+    forward (one kernel fewer); the option restores the separate kernel."""
+    w = W["mnist_mlp_b4096"]
+    x, y = P.batches(w, 1)[0]
+    names = {}
+    for hg in (1, 0):
+        m = make_model(w, f32_tc=1, head_gemm=hg)
+        xd, yd = x.to(DEV), y.to(DEV)
+        prof = nn.mlp_profile_step(m.h, xd.data_ptr(), yd.data_ptr(), w.lr, w.beta1, w.beta2, w.eps, w.wd, None,
+                                   m.stream())
+        names[hg] = [n for n, _ in prof]
+        m.close()
+    assert "tc_gemm_fwd_head" in names[1] and "head_ce" not in names[1]
+    assert "head_ce" in names[0] and "tc_gemm_fwd_head" not in names[0]
+    assert len(names[1]) == len(names[0]) - 1
 
 
 def test_f32_tensor_core_mode_runs_tensor_core_kernels():
