@@ -1793,8 +1793,11 @@ static void tc_wgrad_choice(int dtype, int64_t M, int64_t N, int64_t K, int* bn,
     int64_t best_s = 1, best_cost = INT64_MAX;
     // at most 16 splits: the optimizer adds the partials of an element in
     // one batch of 16 loads (a second batch costs it more than the longer
-    // work units cost this kernel)
-    for (int64_t s = 1; s <= 16 && (s == 1 || (kbs / s >= 4 && s * M * N <= ((int64_t)4 << 20))); s *= 2) {
+    // work units cost this kernel); any count whose K chunks come out even
+    // (kb_per_split = ceil(kbs / s) gives s chunks), so a layer can fill one
+    // wave of SMs
+    for (int64_t s = 1; s <= 16 && (s == 1 || (kbs / s >= 4 && s * M * N <= ((int64_t)4 << 20))); ++s) {
+      if (ceil_div(kbs, ceil_div(kbs, s)) != s) continue;
       const int64_t cost = ceil_div(tiles * s, kSMs) * (ceil_div(kbs, s) + 2);
       if (cost < best_cost) { best_cost = cost; best_s = s; }
     }
