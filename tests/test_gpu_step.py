@@ -128,6 +128,22 @@ def test_mnist_mlp_ragged_batch_one_step(f32_tc):
     fp32_one_step(W["mnist_mlp_b64"], batch=333, f32_tc=f32_tc)
 
 
+def test_mnist_mlp_large_batch_one_step():
+    """Batch 6000: 47 row tiles, too many for CTA pairs in the layer-1 forward
+    (94 tiles of 128 x 128) but not in the layer-2 forward, so that forward
+    runs one CTA per tile while the output layer is still folded into the
+    layer-2 forward; element by element within the fp32 bounds."""
+    w = W["mnist_mlp_b4096"]
+    m = make_model(w, 6000, f32_tc=1)
+    x, y = P.batches(w, 1, 6000)[0]
+    prof = nn.mlp_profile_step(m.h, x.to(DEV).data_ptr(), y.to(DEV).data_ptr(), w.lr, w.beta1, w.beta2, w.eps,
+                               w.wd, None, m.stream())
+    m.close()
+    names = [n for n, _ in prof]
+    assert "tc_gemm_fwd_head" in names and "head_ce" not in names
+    fp32_one_step(w, batch=6000, f32_tc=1)
+
+
 @pytest.mark.parametrize("batch", [4096, 333, 64])
 def test_mnist_mlp_separate_output_layer_kernel_one_step(batch):
     """With the output layer kept out of the forward GEMM's epilogue
