@@ -319,11 +319,14 @@ def test_bitwise_deterministic_and_graph_equals_eager(name):
         assert np.array_equal(p_, res[0][1])
 
 
-def test_label_out_of_range_reported():
+@pytest.mark.parametrize("head_gemm,bad", [(1, 10), (1, -1), (0, 10), (0, -3)])
+def test_label_out_of_range_reported(head_gemm, bad):
+    """A label outside [0, C) latches MLP_ERR_LABEL_RANGE, with the output
+    layer folded into the layer-2 forward (default) and in its own kernel."""
     w = W["mnist_mlp_b64"]
-    m = make_model(w)
+    m = make_model(w, head_gemm=head_gemm)
     x, y = synth.make_batch(w, 0)
-    y[5] = 10
+    y[5] = bad
     m.train_step(x.to(DEV), y.to(DEV), w.lr)
     with pytest.raises(nn.MlpError) as e:
         m.check_errors()
