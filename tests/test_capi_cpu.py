@@ -89,3 +89,22 @@ def test_every_kernel_takes_one_parameter_block():
             assert re.fullmatch(r"const __grid_constant__ \w+ \w+", params), (f, params)
             n += 1
     assert n >= 15
+
+
+def test_binding_constants_match_the_headers():
+    """Every enumerator the headers declare (activations, dtypes, planes,
+    options, update rules, losses, status codes, workspace sizes) has the
+    same value in the Python binding."""
+    found = {}
+    for f in ("mlp.h", "mlp_ops.h"):
+        txt = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", f)).read(), flags=re.S)
+        for body in re.findall(r"enum\s*\{(.*?)\}", txt, flags=re.S):
+            for name, val in re.findall(r"\b(MLP_\w+)\s*=\s*(-?\d+)", body):
+                found[name] = int(val)
+    assert len(found) >= 30
+    for name, val in found.items():
+        if name.startswith("MLP_ERR_") or name == "MLP_OK":
+            assert nn.STATUS_NAMES[val] == name, name
+            continue
+        py = name[len("MLP_"):]
+        assert getattr(nn, py) == val, (name, val, getattr(nn, py, None))
