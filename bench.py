@@ -30,6 +30,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -176,14 +177,22 @@ def roofline_rows(w, rows, peaks):
 HOST_ONLY_SOURCES = ("model.cu", "noalloc.cu")
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and whitespace: what a kernel is
+    made of (a comment edit leaves the counters taken on it valid)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return re.sub(r"\s+", "", text)
+
+
 def source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "neural_net_step_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f in HOST_ONLY_SOURCES:
             continue
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update((f + _code_only(fh.read())).encode())
     return h.hexdigest()[:16]
 
 

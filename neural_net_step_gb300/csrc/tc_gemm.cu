@@ -495,9 +495,10 @@ struct PParams {
   // read by the dgrad in place of the stored activation
   uint64_t* relu_bits; int64_t ld_bits;
   // The 10-class output layer folded into this forward (CTA pairs, X3,
-  // N = 128): `out` receives dY of this layer; per-CTA partials of dW_out
-  // (row-major [10][128]) and db_out at head_ws + tile * kFhPitch, the
-  // tile's loss sum at head_ws + head_loss_off + tile (tile = the pair's row tile)
+  // N = 128): `out` receives dY of this layer; the sums over each 128-row
+  // tile (a pair) of dW_out (row-major [10][128]) and db_out go to
+  // head_ws + tile * kFhPitch, the tile's loss sum to head_ws +
+  // head_loss_off + tile
   const float* head_W; const float* head_bias; const int32_t* head_labels;
   float* head_ws; int64_t head_loss_off; float head_scale;
   int64_t* step_counter; float* bias_corr; float beta1, beta2;
