@@ -108,3 +108,21 @@ def test_binding_constants_match_the_headers():
             continue
         py = name[len("MLP_"):]
         assert getattr(nn, py) == val, (name, val, getattr(nn, py, None))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 784, 4096), (128, 256, 4096), (10, 128, 4096), (256, 784, 333),
+                                   (1024, 3072, 8192), (512, 512, 65536), (100, 512, 1000)])
+def test_plane_wgrad_split_policy(lib, M, N, K):
+    """The K splits of a plane-mode (fp32 as bf16 planes) weight gradient,
+    read back from the workspace it asks for: at most 16 (the optimizer adds
+    16 partials per batch of loads), chunks of 32-row stages that come out
+    even, and for layer 1 of the 4096-row MNIST-shaped step ten splits (140
+    work units: one wave of 152 SMs)."""
+    ws = nn.mlp_op_wgrad_workspace_bytes(nn.F32X3, M, N, K)
+    s = 1 if ws == 0 else ws // ((M * N + M) * 4)
+    assert ws in (0, s * (M * N + M) * 4)
+    kbs = -(-K // 32)
+    assert 1 <= s <= 16
+    assert -(-kbs // -(-kbs // s)) == s
+    if (M, N, K) == (256, 784, 4096):
+        assert s == 10
