@@ -6,7 +6,10 @@ A step is one pass of the whole hot path -- LinearAct forward GEMMs,
 softmax-CE forward+backward, loss mean, wgrad (+ fused bias gradient) and
 dgrad (+ fused activation VJP) GEMMs, one flat AdamW update -- over one batch
 of synthetic data, launched as one CUDA-graph replay through the C ABI.
-Default workload: the 784-256-128-10 ReLU MLP in fp32 at batch 4096.
+Default workload: the token-level LM block (1024 -> 4096 GELU-tanh -> 1024 ->
+32000-way softmax-CE head, bf16 with fp32 master weights, 16384 tokens), the
+largest of the five workloads.  `--graph-steps G` launches G consecutive
+steps as one CUDA graph (the deep narrow net's configuration captures 50).
 
 Timing: W untimed warm-up steps, then K steps between CUDA events on the
 launching stream, bracketed by a barrier and a device synchronize; the step
@@ -381,7 +384,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mnist_mlp_b4096")
+    ap.add_argument("--workload", default="lm_block_t16384")
+    ap.add_argument("--graph-steps", type=int, default=0,
+                    help="steps per CUDA-graph launch (default: the workload's own, 50 for deep_narrow_b65536)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels", action="store_true", help="include the per-kernel table")
@@ -452,11 +457,30 @@ def main():
     stream = torch.cuda.current_stream()
     losses = torch.empty(args.steps + args.warmup, dtype=torch.float32, device=dev)
 
+    G = args.graph_steps if args.graph_steps > 0 else w.graph_steps
+
     def step(i, loss_slot):
         model.train_step(xs[i % n_pool], ys[i % n_pool], loss=loss_slot, **hyper)
 
+    def steps(i0, n, loss_slots):
+        """Steps i0 .. i0+n-1: one graph launch of n steps (G > 1), else n
+        single-step launches."""
+        if G > 1:
+            model.train_steps([xs[(i0 + j) % n_pool] for j in range(n)], [ys[(i0 + j) % n_pool] for j in range(n)],
+                              losses=loss_slots, **hyper)
+        else:
+            for j in range(n):
+                step(i0 + j, loss_slots[j])
+
+    def chunks(n):
+        return [G] * (n // G) + ([n % G] if n % G else []) if G > 1 else [n]
+
+    warm_losses = torch.empty(max(G, args.warmup), dtype=torch.float32, device=dev)
+    if G > 1:   # every graph shape the timed region launches is built and run at least once
+        for c in sorted(set(chunks(args.steps)) | {G}):
+            steps(0, c, warm_losses[:c])
     for i in range(args.warmup):
-        step(i, losses[i])
+        step(i, warm_losses[i])
     model.check_errors()
     torch.cuda.synchronize()
 
@@ -470,16 +494,18 @@ def main():
         t_end = time.perf_counter() + 1.0
         i = 0
         while time.perf_counter() < t_end:
-            step(i, losses[i % args.warmup])
-            i += 1
-            if i % 16 == 0:
+            steps(i, G, warm_losses[:G])
+            i += G
+            if i % (16 * G) == 0:
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
         ev0.record(stream)
-        for i in range(args.steps):
-            step(args.warmup + i, losses[args.warmup + i])
+        i = 0
+        for c in chunks(args.steps):
+            steps(args.warmup + i, c, losses[args.warmup + i:args.warmup + i + c])
+            i += c
         ev1.record(stream)
         torch.cuda.synchronize()
     if pg:
@@ -548,7 +574,8 @@ def main():
             "data": "synthetic",
             "config": config_of(w, {"l2": f"fresh batch per step from a {n_pool}-batch device pool "
                                           f"({n_pool * per / 2**20:.0f} MiB > 129 MB L2)",
-                                    "graph": "one CUDA-graph replay per step",
+                                    "graph": (f"{G} steps per CUDA-graph launch" if G > 1 else
+                                              "one CUDA-graph replay per step"),
                                     **({"f32_gemm": gemm_mode} if gemm_mode else {})}, args),
             "roofline": rf,
             "step_roofline": {"t_roof_ms": round(t_roof_ms, 5), "measured_ms": round(ms_per_step, 5),

@@ -77,12 +77,14 @@ mlp_status mlp_op_wgrad(int dtype, int64_t N, int64_t K, int64_t B, const void* 
  * pressure.  This entry point allocates nothing: the split-K partial sums go
  * to a built-in device array of 16 MiB, which every GPU that loads the
  * library holds until the process exits.
- *   Same arguments, layouts and results as mlp_op_wgrad.  Returns
- *   MLP_ERR_SHAPE, before enqueuing anything, when the shape needs more than
- *   16 MiB of scratch (mlp_op_wgrad_workspace_bytes tells how much).
- *   The first call on a device that needs scratch looks up the array's
- *   device address (cudaGetSymbolAddress) with that device current and
- *   caches it; make that first call before any stream capture.
+ *   Same arguments, layouts and results as mlp_op_wgrad, for every dtype it
+ *   takes (MLP_F32, MLP_BF16, MLP_F32X3).  Returns MLP_ERR_SHAPE, before
+ *   enqueuing anything, when the shape needs more than 16 MiB of scratch
+ *   (mlp_op_wgrad_workspace_bytes tells how much).
+ *   The array's device address is looked up (cudaGetSymbolAddress, with the
+ *   device current) by the first call on a device, which should come before
+ *   any stream capture; later calls look it up again unless their stream is
+ *   capturing, so a cudaDeviceReset between calls leaves no stale address.
  *   Every call shares the one array per device: calls whose kernels overlap
  *   on the GPU (other streams, other threads) race on it and must be
  *   serialised by the caller.  Each call writes every scratch element it

@@ -33,18 +33,26 @@ mlp_status noalloc_fail(mlp_status st, const char* msg) {
 }
 
 // In host code `g_wgrad_scratch` names a host-side stand-in, not a device
-// address; the device address is looked up once per device (with that
-// device current) and cached.
+// address.  The device address is looked up with the device current: on the
+// first call on each device (which should come before any stream capture),
+// and again on every later call whose stream is not capturing, so that the
+// address stays right after cudaDeviceReset tears the context down and a new
+// one loads the module elsewhere.  A call on a capturing stream makes no
+// lookup and reuses the address the last lookup on that device found.
 std::mutex g_mu;
 std::map<int, void*> g_addr;
 
-cudaError_t scratch_address(void** out) {
+cudaError_t scratch_address(cudaStream_t stream, void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_addr.find(dev);
-  if (it != g_addr.end()) {
+  if (cs != cudaStreamCaptureStatusNone) {
+    if (it == g_addr.end()) return cudaErrorStreamCaptureUnsupported;   // no set-up call before the capture
     *out = it->second;
     return cudaSuccess;
   }
@@ -63,7 +71,7 @@ extern "C" {
 mlp_status mlp_op_wgrad_noalloc(int dtype, int64_t N, int64_t K, int64_t B, const void* dY, int64_t ldy,
                                 const void* X, int64_t ldx, float* dW, int64_t lddw, float* db, uint32_t* err_dev,
                                 void* stream) {
-  if (dtype != MLP_F32 && dtype != MLP_BF16) return noalloc_fail(MLP_ERR_DTYPE, "bad dtype");
+  if (dtype != MLP_F32 && dtype != MLP_BF16 && dtype != MLP_F32X3) return noalloc_fail(MLP_ERR_DTYPE, "bad dtype");
   if (!dY || !X || !dW) return noalloc_fail(MLP_ERR_ARG, "null pointer");
   if (N < 1 || K < 1 || B < 1 || ldy < N || ldx < K || lddw < K)
     return noalloc_fail(MLP_ERR_SHAPE, "bad shape or leading dimension");
@@ -78,14 +86,16 @@ mlp_status mlp_op_wgrad_noalloc(int dtype, int64_t N, int64_t K, int64_t B, cons
   }
   void* scratch = nullptr;
   if (need > 0) {
-    cudaError_t e = scratch_address(&scratch);
+    cudaError_t e = scratch_address((cudaStream_t)stream, &scratch);
     if (e != cudaSuccess) {
-      snprintf(msg, sizeof(msg), "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      snprintf(msg, sizeof(msg), "scratch address lookup: %s%s", cudaGetErrorString(e),
+               e == cudaErrorStreamCaptureUnsupported ? " (make one call on this device before capturing)" : "");
       return noalloc_fail(MLP_ERR_CUDA, msg);
     }
   }
   GemmOp op;
   op.dtype = dtype; op.kind = GEMM_WGRAD;
+  op.a_plane = B * ldy; op.b_plane = B * ldx;   // MLP_F32X3: the three planes of each operand
   op.M = N; op.N = K; op.K = B;
   op.A = dY; op.lda = ldy; op.a_kmajor = false;
   op.B = X; op.ldb = ldx; op.b_kmajor = false;

@@ -33,7 +33,7 @@ What it computes, with the passage each step follows:
   Orthon "Core capabilities", Mixed precision).  Here the low-precision type
   is bfloat16.
 
-Readings of points the pages leave open (each is also listed in the design doc):
+Readings of points the pages leave open (each stated here in full):
 ReLU'(0) = 0 and the ReLU mask is taken from the stored activation h > 0;
 AdamW follows the Loshchilov-Hutter / PyTorch form (eps added to sqrt(v_hat)
 after bias correction, decay applied to the pre-step parameter, t starts at 1,

@@ -1,6 +1,6 @@
 """Shared helpers for GPU-vs-oracle parity tests.
 
-Tolerances (derived from the arithmetic; each is also stated in the design doc):
+Tolerances (each derived from the arithmetic it bounds):
 
 Single GEMM-shaped results (op tests):
     |c - c*| <= 8 sqrt(K) 2^-24 sum_k |a_k b_k|    (fp32 accumulation; 8x the

@@ -71,6 +71,47 @@ def test_noalloc_matches_wgrad_on_two_calls(dtype, N, K, B):
         assert_close_gemm(to64(dW), dy64.T @ x64, absum, B, False, f"dW vs definition, call {call}")
 
 
+def _planes(x: torch.Tensor, ld: int) -> torch.Tensor:
+    """[3, rows, ld] bf16 planes hi, mid, lo of an fp32 CPU matrix (the
+    MLP_F32X3 operand encoding), columns beyond the matrix zero."""
+    rows, cols = x.shape
+    hi = x.to(torch.bfloat16)
+    r = x - hi.float()
+    mid = r.to(torch.bfloat16)
+    out = torch.zeros((3, rows, ld), dtype=torch.bfloat16)
+    out[0, :, :cols], out[1, :, :cols], out[2, :, :cols] = hi, mid, (r - mid.float()).to(torch.bfloat16)
+    return out
+
+
+def test_noalloc_fp32_planes_match_wgrad_on_two_calls():
+    """fp32 operands given as three bf16 planes (MLP_F32X3), split over the
+    batch: the same dW and db as mlp_op_wgrad on two calls in a row."""
+    N, K, B = 256, 784, 4096
+    ldy = N
+    stream = torch.cuda.current_stream().cuda_stream
+    assert nn.mlp_op_wgrad_workspace_bytes(nn.F32X3, N, K, B) > 0
+    for call in range(2):
+        dY = synth.make_normal((B, N), 1e-3, 93, call)
+        X = torch.relu(synth.make_normal((B, K), 1.0, 94, call))
+        dYp, Xp = _planes(dY, ldy).to(DEV), _planes(X, K).to(DEV)
+        want_dW, want_db = _reference(nn.F32X3, N, K, B, dYp, ldy, Xp)
+        dW = torch.full((N, K), float("nan"), dtype=torch.float32, device=DEV)
+        db = torch.full((N,), float("nan"), dtype=torch.float32, device=DEV)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        nn.mlp_op_wgrad_noalloc(nn.F32X3, N, K, B, dYp.data_ptr(), ldy, Xp.data_ptr(), K, dW.data_ptr(), K,
+                                db.data_ptr(), err.data_ptr(), stream)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        dy64, x64 = to64(dY), to64(X)
+        absum = np.abs(dy64).T @ np.abs(x64)
+        # same kernels, same split policy: the results agree within the GEMM bound
+        assert_close_gemm(to64(dW), to64(want_dW), absum, B, False, f"dW call {call}")
+        assert_close_gemm(to64(db), to64(want_db), np.abs(dy64).sum(0), B, False, f"db call {call}")
+        # against dY^T X, allowing the three plane products the kernels leave out
+        assert_close_gemm(to64(dW), dy64.T @ x64, absum, B, False, f"dW vs definition, call {call}",
+                          2.0 ** -22 * absum)
+
+
 def test_noalloc_refuses_shapes_beyond_its_scratch():
     # 1024 x 2048 over 65536 rows splits the batch in two: 16.8 MB > 16 MiB
     N, K, B = 1024, 2048, 65536
