@@ -273,6 +273,51 @@ mlp_status mlp_profile_step(mlp_t* model, const void* x_dev, const void* y_dev, 
                             float beta2, float eps, float wd, float* loss_dev, void* stream, float* ms_out,
                             const char** names_out, int max_kernels, int* n_out);
 
+/* Traced step: one training step (same arguments and effect as
+ * mlp_train_step) whose kernels run one after another on `stream`, each
+ * followed by device-to-device copies of the tensors it wrote into the
+ * caller's trace buffer, so that every intermediate result of the step can be
+ * read back (noeira.ai "Neural networks", "The design in one page": forward
+ * and backward are explicit, every layer's output and vector-Jacobian
+ * product is a tensor of its own; MuNet "Configuration": profile=True runs
+ * the kernels one by one).  The kernels, their launch configurations and
+ * their buffers are those of mlp_train_step; only their order is serial.
+ *   trace_dev (device, caller-owned, trace_bytes long) receives the tensors
+ *   back to back, each 256-byte aligned, exactly as stored (row pitch,
+ *   padding columns and planes included).  entries[i] (host,
+ *   max_entries long, nullable) describes tensor i; *n_entries (nullable)
+ *   and *bytes_needed (nullable) receive the count and the trace size.
+ *   trace_dev NULL: nothing runs; only the count and the size are returned.
+ *   Tensors kept only inside a fused kernel (the fused output layer's logits
+ *   and dz, softmax-CE inside the GEMMs) have no entry.
+ *   Errors: MLP_ERR_ARG for a trace buffer smaller than *bytes_needed or
+ *   fewer entries than tensors (before anything runs); the rest as
+ *   mlp_train_step.  Synchronises the stream before returning. */
+enum {
+  MLP_TRACE_H = 0,          /* hidden activation h_l = act(u_l), the input of layer l + 1 */
+  MLP_TRACE_U = 1,          /* GELU pre-activation u_l as stored for the dgrad */
+  MLP_TRACE_Z = 2,          /* logits z (layer L - 1) */
+  MLP_TRACE_DZ = 3,         /* loss gradient dz = dY_{L-1} */
+  MLP_TRACE_LOSS_ROWS = 4,  /* per-row loss, fp32 [B] */
+  MLP_TRACE_DY = 5          /* dY_l, gradient w.r.t. u_l, written by the dgrad of layer l + 1 */
+};
+typedef struct {
+  int32_t kind;            /* MLP_TRACE_* */
+  int32_t layer;           /* 0-based layer l */
+  int32_t launch;          /* index of the kernel that wrote it (mlp_profile_step order) */
+  int32_t planes;          /* 1, or 3: an fp32 tensor as three bf16 planes */
+  int64_t rows, cols, ld;  /* [rows, cols], row pitch ld elements */
+  int64_t plane_stride;    /* elements from one plane to the next */
+  int32_t elem_bytes;      /* bytes of one element of one plane: 2 (bf16) or 4 (fp32) */
+  int32_t reserved;
+  uint64_t offset;         /* byte offset of the tensor in trace_dev */
+  uint64_t bytes;          /* bytes copied */
+} mlp_trace_entry;
+mlp_status mlp_trace_step(mlp_t* model, const void* x_dev, const void* y_dev, float lr, float beta1, float beta2,
+                          float eps, float wd, float* loss_dev, void* trace_dev, size_t trace_bytes,
+                          mlp_trace_entry* entries, int max_entries, int* n_entries, size_t* bytes_needed,
+                          void* stream);
+
 /* Message for the last failed call on this thread ("" if none). */
 const char* mlp_last_error(void);
 

@@ -58,6 +58,8 @@ _SIGS = {
     "mlp_kernels_per_step": (_I32, [_P]),
     "mlp_profile_step": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P, _c.POINTER(_F), _c.POINTER(_c.c_char_p),
                                 _I32, _c.POINTER(_I32)]),
+    "mlp_trace_step": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P, _SZ, _P, _I32, _c.POINTER(_I32),
+                              _c.POINTER(_SZ), _P]),
     "mlp_last_error": (_c.c_char_p, []),
     "mlp_destroy": (None, [_P]),
     "mlp_op_linear_act": (_I32, [_I32, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _P, _P]),
@@ -190,6 +192,28 @@ def mlp_profile_step(h, x_ptr, labels_ptr, lr, beta1, beta2, eps, wd, loss_ptr, 
     _check(lib().mlp_profile_step(h, x_ptr, labels_ptr, lr, beta1, beta2, eps, wd, loss_ptr, stream, ms, names,
                                   max_kernels, ctypes.byref(n)))
     return [(names[i].decode(), ms[i]) for i in range(min(n.value, max_kernels))]
+
+
+TRACE_H, TRACE_U, TRACE_Z, TRACE_DZ, TRACE_LOSS_ROWS, TRACE_DY = 0, 1, 2, 3, 4, 5
+
+
+class TraceEntry(ctypes.Structure):
+    """mlp_trace_entry (include/mlp.h)."""
+    _fields_ = [("kind", _c.c_int32), ("layer", _c.c_int32), ("launch", _c.c_int32), ("planes", _c.c_int32),
+                ("rows", _c.c_int64), ("cols", _c.c_int64), ("ld", _c.c_int64), ("plane_stride", _c.c_int64),
+                ("elem_bytes", _c.c_int32), ("reserved", _c.c_int32), ("offset", _c.c_uint64),
+                ("bytes", _c.c_uint64)]
+
+
+def mlp_trace_step(h, x_ptr, y_ptr, lr, beta1, beta2, eps, wd, loss_ptr, trace_ptr, trace_bytes, stream,
+                   max_entries=512):
+    """Returns ([TraceEntry, ...], bytes needed); with trace_ptr None nothing runs."""
+    ents = (TraceEntry * max_entries)()
+    n = _I32(0)
+    need = _SZ(0)
+    _check(lib().mlp_trace_step(h, x_ptr, y_ptr, lr, beta1, beta2, eps, wd, loss_ptr, trace_ptr, trace_bytes, ents,
+                                max_entries, ctypes.byref(n), ctypes.byref(need), stream))
+    return [ents[i] for i in range(n.value)], need.value
 
 
 def mlp_read_params(h, plane, host_ptr, n) -> int:
@@ -366,6 +390,29 @@ class Model:
         mlp_forward(self.h, x.data_ptr(), logits.data_ptr() if logits is not None else None,
                     am.data_ptr() if am is not None else None, self.stream())
         return logits, am
+
+    def trace_step(self, x, labels, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0, loss=None):
+        """One traced training step (mlp_trace_step).  Returns (loss, [(entry,
+        tensor)]): each tensor a CPU torch tensor [planes, rows, ld] of the
+        stored dtype (bf16, or fp32 for 4-byte elements), exactly as stored."""
+        t = self.torch
+        self._check_x(x, labels)
+        if loss is None:
+            loss = t.empty((), dtype=t.float32, device=x.device)
+        args = (self.h, x.data_ptr(), labels.data_ptr(), lr, beta1, beta2, eps, wd, loss.data_ptr())
+        _, need = mlp_trace_step(*args, None, 0, self.stream())
+        buf = t.empty(max(need, 256), dtype=t.uint8, device=x.device)
+        ents, _ = mlp_trace_step(*args, buf.data_ptr(), buf.numel(), self.stream())
+        out = []
+        for e in ents:
+            raw = buf[e.offset:e.offset + e.bytes].cpu()
+            td = t.bfloat16 if e.elem_bytes == 2 else t.float32
+            v = raw.view(td)
+            full = e.rows * e.ld
+            planes = [v[k * e.plane_stride:k * e.plane_stride + full].view(e.rows, e.ld) for k in range(e.planes)]
+            out.append((e, t.stack(planes)))
+        del buf
+        return loss, out
 
     def read_flat(self, plane: int = PLANE_P):
         import numpy as np

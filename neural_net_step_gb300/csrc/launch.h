@@ -29,7 +29,27 @@ struct LaunchRec {
   // crowd onto the SMs the predecessor leaves idle and then run there, so
   // they keep full edges.
   bool early = false;
+  // Tensors this launch writes that a traced step copies aside (the step's
+  // intermediate results; the graph and eager paths ignore them).
+  struct Out {
+    int kind = 0, layer = 0;        // MLP_TRACE_* and the layer it belongs to
+    const void* ptr = nullptr;
+    int64_t rows = 0, cols = 0, ld = 0, plane_stride = 0;
+    int planes = 1, elem_bytes = 0;
+  };
+  static constexpr int kMaxOuts = 2;
+  Out outs[kMaxOuts];
+  int nouts = 0;
   alignas(128) unsigned char args[kMaxArgBytes];
+
+  void add_out(int kind, int layer, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int elem_bytes,
+               int planes = 1, int64_t plane_stride = 0) {
+    if (nouts >= kMaxOuts) return;
+    Out& o = outs[nouts++];
+    o.kind = kind; o.layer = layer; o.ptr = ptr;
+    o.rows = rows; o.cols = cols; o.ld = ld; o.elem_bytes = elem_bytes;
+    o.planes = planes; o.plane_stride = plane_stride;
+  }
 
   void depend_on(const int* d, int n) {
     ndeps = 0;

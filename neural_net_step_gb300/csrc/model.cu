@@ -397,6 +397,17 @@ mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out
       }
     }
     PLAN_TRY(gemm_plan(op, r_, e_, sizeof(e_)));
+    // what a traced step copies aside
+    LaunchRec& r = out.back();
+    const int planes = x3 ? 3 : 1, eb = x3 ? 2 : (int)m->es();
+    if (l == L.L - 1) {
+      r.add_out(MLP_TRACE_Z, l, op.out, L.B, L.dims[l + 1], op.ldo, eb);
+    } else if (head_fold && l == n_layers - 1) {
+      r.add_out(MLP_TRACE_DY, l, op.out, L.B, L.dims[l + 1], op.ldo, eb, planes, op.out_plane);
+    } else {
+      r.add_out(MLP_TRACE_H, l, op.out, L.B, L.dims[l + 1], op.ldo, eb, planes, op.out_plane);
+      if (op.out_u) r.add_out(MLP_TRACE_U, l, op.out_u, L.B, L.dims[l + 1], op.ldu, eb);
+    }
   }
   return MLP_OK;
 }
@@ -468,6 +479,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     char e_[512] = "";
     LaunchRec r;
     if (head_plan(hd, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    r.add_out(MLP_TRACE_DY, l - 1, hd.dY, L.B, L.dims[l], hd.ldy, x3 ? 2 : (int)m->es(), x3 ? 3 : 1, dy_plane);
     out.push_back(r);
     dY = hd.dY; ldy = hd.ldy;
     buf = 1;
@@ -504,6 +516,8 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
       ce.err = &ctl->err;
       if (ce_plan(ce, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
     }
+    if (!ce_gemm) r.add_out(MLP_TRACE_DZ, L.L - 1, m->at(L.off_dz), L.B, L.dims[L.L], L.ldz, (int)m->es());
+    r.add_out(MLP_TRACE_LOSS_ROWS, L.L - 1, loss_rows, L.B, 1, 1, 4);
     out.push_back(r);
     LossMeanOp lm;
     lm.B = L.B; lm.loss_rows = loss_rows;
@@ -579,6 +593,8 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
         dg.ce_rowstat = wg.ce_rowstat; dg.ce_labels = wg.ce_labels; dg.ce_scale = wg.ce_scale;
       }
       PLAN_TRY(gemm_plan(dg, r_, e_, sizeof(e_)));
+      out.back().add_out(MLP_TRACE_DY, l - 1, dg.out, L.B, L.dims[l], dg.ldo, x3 ? 2 : (int)m->es(), x3 ? 3 : 1,
+                         dy_plane);
       const int d[2] = {main_tail, side_prev};
       out.back().depend_on(d, 2);
       main_tail = (int)out.size() - 1;
@@ -1039,6 +1055,55 @@ mlp_status mlp_profile_step(mlp_t* m, const void* x, const void* y, float lr, fl
     if (v) cudaEventDestroy(v);
   if (e != cudaSuccess) return fail(MLP_ERR_CUDA, "profile: %s", cudaGetErrorString(e));
   *n_out = n;
+  return ok();
+}
+
+mlp_status mlp_trace_step(mlp_t* m, const void* x, const void* y, float lr, float b1, float b2, float eps, float wd,
+                          float* loss, void* trace_dev, size_t trace_bytes, mlp_trace_entry* entries,
+                          int max_entries, int* n_entries, size_t* bytes_needed, void* stream) {
+  if (!m || !x || !y) return fail(MLP_ERR_ARG, "bad arguments");
+  if (!(lr >= 0) || !(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1) || !(eps >= 0) || !(wd >= 0))
+    return fail(MLP_ERR_ARG, "bad hyper-parameters");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_step(m, x, y, Hyper{lr, b1, b2, eps, wd}, loss, recs);
+  if (st != MLP_OK) return st;
+  // the trace layout: every traced tensor as stored, 256-byte aligned
+  std::vector<mlp_trace_entry> ents;
+  size_t off = 0;
+  for (size_t i = 0; i < recs.size(); ++i) {
+    for (int k = 0; k < recs[i].nouts; ++k) {
+      const LaunchRec::Out& o = recs[i].outs[k];
+      mlp_trace_entry e;
+      memset(&e, 0, sizeof(e));
+      e.kind = o.kind; e.layer = o.layer; e.launch = (int32_t)i; e.planes = o.planes;
+      e.rows = o.rows; e.cols = o.cols; e.ld = o.ld; e.plane_stride = o.plane_stride;
+      e.elem_bytes = o.elem_bytes;
+      e.bytes = (uint64_t)(((int64_t)(o.planes - 1) * o.plane_stride + o.rows * o.ld) * o.elem_bytes);
+      e.offset = off;
+      off = align_up(off + e.bytes);
+      ents.push_back(e);
+    }
+  }
+  const int n = (int)ents.size();
+  if (n_entries) *n_entries = n;
+  if (bytes_needed) *bytes_needed = off;
+  if (entries && max_entries >= n)
+    for (int i = 0; i < n; ++i) entries[i] = ents[i];
+  if (!trace_dev) return ok();
+  if (trace_bytes < off) return fail(MLP_ERR_ARG, "trace buffer holds %zu bytes, the step writes %zu", trace_bytes, off);
+  if (!entries || max_entries < n) return fail(MLP_ERR_ARG, "%d trace entries needed", n);
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* dst = (uint8_t*)trace_dev;
+  int j = 0;
+  for (size_t i = 0; i < recs.size(); ++i) {
+    cudaError_t e = launch_rec(recs[i], s);
+    if (e != cudaSuccess) return fail(MLP_ERR_CUDA, "launch of %s failed: %s", recs[i].name, cudaGetErrorString(e));
+    for (int k = 0; k < recs[i].nouts; ++k, ++j)
+      CUDA_TRY(cudaMemcpyAsync(dst + ents[j].offset, recs[i].outs[k].ptr, ents[j].bytes, cudaMemcpyDeviceToDevice, s));
+  }
+  CUDA_TRY(cudaStreamSynchronize(s));
   return ok();
 }
 

@@ -196,12 +196,6 @@ def test_mnist_mlp_b64_three_steps(f32_tc):
     trajectory_ensemble(W["mnist_mlp_b64"], 3, f32_tc=f32_tc)
 
 
-@pytest.mark.slow
-def test_mnist_mlp_b4096_100_steps():
-    w = W["mnist_mlp_b4096"]
-    trajectory_ensemble(w, w.steps)
-
-
 def test_cifar_mlp_reduced_batch_one_step():
     trajectory_ensemble(W["cifar_mlp_b8192"], 1, batch=320)
 

@@ -379,6 +379,48 @@ def test_whole_step_matches_torch_modules_and_optimizers(optim, max_norm, loss_k
         assert np.allclose(a, b.detach().numpy(), rtol=0, atol=1e-13)
 
 
+@pytest.mark.parametrize("optim", ["adamw", "adam", "sgd"])
+def test_run_steps_matches_torch_training_loop(optim):
+    """The oracle's multi-step driver (run_steps: the step counter advancing
+    from 1, moments carried from step to step, a fresh batch each step)
+    against a torch training loop in float64 over six whole-network steps:
+    nn.Linear + GELU / ReLU layers, F.cross_entropy, backward, the optimizer
+    (noeira "A complete example": a loop of forward, loss, backward and an
+    optimizer step over batches)."""
+    dims = [9, 8, 7, 5]
+    acts = (GELU, RELU)
+    B, steps = 13, 6
+    ps = _tiny_net(dims, 120)
+    rng = np.random.default_rng(121)
+    batches = [(rng.standard_normal((B, dims[0])), rng.integers(0, dims[-1], B)) for _ in range(steps)]
+    lr, b1, b2, eps, wd = 3e-2, 0.8, 0.95, 1e-8, 0.05
+    losses, p, m, v, _ = om.run_steps(ps, acts, batches, (lr, b1, b2, eps, wd), optim=optim)
+    tps = [torch.tensor(q, requires_grad=True) for q in ps]
+    opt = {"adamw": lambda: torch.optim.AdamW(tps, lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd),
+           "adam": lambda: torch.optim.Adam(tps, lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd),
+           "sgd": lambda: torch.optim.SGD(tps, lr=lr, momentum=b1, weight_decay=wd)}[optim]()
+    t_losses = []
+    for x, y in batches:
+        opt.zero_grad()
+        h = torch.tensor(x)
+        for l in range(3):
+            h = h @ tps[2 * l].T + tps[2 * l + 1]
+            if l == 0:
+                h = F.gelu(h, approximate="tanh")
+            elif l == 1:
+                h = torch.relu(h)
+        tl = F.cross_entropy(h, torch.tensor(y))
+        tl.backward()
+        opt.step()
+        t_losses.append(tl.item())
+    assert np.allclose(losses, t_losses, rtol=0, atol=1e-12)
+    for a, b in zip(p, tps):
+        assert np.allclose(a, b.detach().numpy(), rtol=0, atol=1e-12)
+    if optim != "sgd":   # the first moment against torch's optimizer state
+        for a, b in zip(m, tps):
+            assert np.allclose(a, opt.state[b]["exp_avg"].numpy(), rtol=0, atol=1e-12)
+
+
 # --------------------------------------------------------------------------
 # MSE: brute force, torch mse_loss and its autograd (float64), closed forms
 # --------------------------------------------------------------------------
@@ -535,6 +577,18 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_clip_matches_torch_clip_grad_norm()
     monkeypatch.setattr(om, "clip_coef", orig_clip)
+
+    # (9) a multi-step driver whose step counter does not advance, or whose
+    #     moments restart every step -> the torch training-loop pin fails
+    orig_step = om.train_step
+    monkeypatch.setattr(om, "train_step", lambda p, m, v, t, *a, **k: orig_step(p, m, v, 1, *a, **k))
+    with pytest.raises(AssertionError):
+        test_run_steps_matches_torch_training_loop("adamw")
+    monkeypatch.setattr(om, "train_step",
+                        lambda p, m, v, t, *a, **k: orig_step(p, [0 * q for q in m], [0 * q for q in v], t, *a, **k))
+    with pytest.raises(AssertionError):
+        test_run_steps_matches_torch_training_loop("adamw")
+    monkeypatch.setattr(om, "train_step", orig_step)
 
     # (8) MSE gradient scaled by 1/B instead of 1/(B C), or missing the 2
     orig_mse = om.mse
