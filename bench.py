@@ -396,6 +396,8 @@ def main():
                     help="update rule (default AdamW)")
     ap.add_argument("--max-grad-norm", type=float, default=0.0, help="> 0: global gradient-norm clipping")
     ap.add_argument("--loss", default="ce", choices=["ce", "mse"], help="softmax CE (default) or MSE")
+    ap.add_argument("--gemm-2sm", type=int, default=-1, choices=[-1, 0, 1],
+                    help="bf16 forward / dgrad GEMMs on CTA pairs with 2-SM MMAs: -1 library policy, 0 off, 1 on")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (small cases for profiling; not a bench line)")
     args = ap.parse_args()
@@ -431,6 +433,7 @@ def main():
         model.set_option(nn.OPT_F32_TENSOR_CORES, 0 if args.f32_ffma else 1)
     model.set_optimizer({"adamw": nn.OPTIM_ADAMW, "adam": nn.OPTIM_ADAM, "sgd": nn.OPTIM_SGD}[args.optim],
                         args.max_grad_norm)
+    model.set_option(nn.OPT_GEMM_2SM, args.gemm_2sm)
     mse = args.loss == "mse"
     if mse:
         model.set_loss(nn.LOSS_MSE)

@@ -152,6 +152,7 @@ def mlp_set_graph_mode(h, enable: bool) -> None:
 
 
 OPT_GRAPH, OPT_FUSE_HEAD, OPT_F32_TENSOR_CORES, OPT_PDL, OPT_CE_GEMM, OPT_RELU_BITS, OPT_HEAD_IN_GEMM = 0, 1, 2, 3, 4, 5, 6
+OPT_GEMM_2SM = 7
 
 
 def mlp_set_option(h, option: int, value: int) -> None:

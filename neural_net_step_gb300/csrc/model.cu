@@ -281,6 +281,7 @@ struct mlp {
   bool ce_gemm = false;      // softmax-CE inside the GEMMs of a wide bf16 output layer (slower on this part)
   bool relu_bits = true;     // bf16 ReLU masks as bits between the forward and the dgrad
   bool head_in_gemm = true;  // fp32 planes: the fused output layer inside the forward GEMM below it
+  int gemm_2sm = -1;         // bf16 forward / dgrad on CTA pairs with 2-SM MMAs (GemmOp::cg2)
   float max_grad_norm = 0.f; // > 0: global-norm clipping of the gradient before the update
   std::mutex mu;
   std::vector<GraphCache> graphs;
@@ -374,6 +375,7 @@ mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out
     op.b_plane = L.plane_n;
     op.bias = m->plane(MLP_PLANE_P) + L.boff[l];
     op.err = &m->ctl()->err;
+    op.cg2 = m->gemm_2sm;
     if (l < L.L - 1) {
       op.act = L.acts[l];
       op.out = m->at(L.off_h[l]); op.ldo = L.ld_h[l]; op.out_plane = L.B * L.ld_h[l];
@@ -519,6 +521,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     if (!ce_gemm) r.add_out(MLP_TRACE_DZ, L.L - 1, m->at(L.off_dz), L.B, L.dims[L.L], L.ldz, (int)m->es());
     r.add_out(MLP_TRACE_LOSS_ROWS, L.L - 1, loss_rows, L.B, 1, 1, 4);
     out.push_back(r);
+    r.nouts = 0;   // the record is reused for the loss mean, which writes no traced tensor
     LossMeanOp lm;
     lm.B = L.B; lm.loss_rows = loss_rows;
     lm.count = mse ? (double)L.B * (double)L.dims[L.L] : (double)L.B;
@@ -589,6 +592,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
       }
       dg.out = m->at(L.off_dy[buf]); dg.ldo = L.ld_h[l - 1];
       dg.err = &ctl->err;
+      dg.cg2 = m->gemm_2sm;
       if (ce_top) {
         dg.ce_rowstat = wg.ce_rowstat; dg.ce_labels = wg.ce_labels; dg.ce_scale = wg.ce_scale;
       }
@@ -885,6 +889,7 @@ mlp_status mlp_set_option(mlp_t* m, int option, int64_t value) {
     case MLP_OPT_CE_GEMM: m->ce_gemm = value != 0; break;
     case MLP_OPT_RELU_BITS: m->relu_bits = value != 0; break;
     case MLP_OPT_HEAD_IN_GEMM: m->head_in_gemm = value != 0; break;
+    case MLP_OPT_GEMM_2SM: m->gemm_2sm = value < 0 ? -1 : value > 0 ? 1 : 0; break;
     default: return fail(MLP_ERR_ARG, "unknown option %d", option);
   }
   if (option == MLP_OPT_FUSE_HEAD || option == MLP_OPT_F32_TENSOR_CORES) {   // planes kept current only while used

@@ -65,6 +65,10 @@ struct GemmOp {
   // warp's rows are contiguous: bit n % 64 of word (n / 64) * ld_bits + m is
   // "stored h[m, n] > 0".
   uint64_t* relu_bits = nullptr; int64_t ld_bits = 0;
+  // bf16 forward / dgrad on CTA pairs with 2-SM MMAs (256 x 256 tiles):
+  // -1 where there is at least one full wave of pair tiles, 0 never, 1
+  // wherever the form allows (N and M of at least 256, no softmax-CE)
+  int cg2 = -1;
   float2* ce_stats = nullptr; float* ce_zy = nullptr;
   const float2* ce_rowstat = nullptr;
   const int32_t* ce_labels = nullptr;

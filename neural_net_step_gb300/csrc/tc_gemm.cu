@@ -20,6 +20,7 @@
 #include <cuda.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -477,6 +478,11 @@ struct PParams {
   CUtensorMap tmOut;     // bf16 [M rows, N cols] (2-D, or 3-D with 3 planes), box {64, 32}, 128B swizzle
   int M, N, K;
   int num_kb, tiles_n, num_tiles;
+  // tile order: m_fast = 1 walks the row tiles of a column tile first (CTAs
+  // running at the same time share B's columns; chosen when A is the smaller
+  // operand, so B is read from DRAM once and A stays in L2), else the column
+  // tiles of a row tile first
+  int tiles_m, m_fast;
   int b_mn;
   int kind, act;
   uint32_t idesc;
@@ -503,6 +509,17 @@ struct PParams {
   float* head_ws; int64_t head_loss_off; float head_scale;
   int64_t* step_counter; float* bias_corr; float beta1, beta2;
 };
+
+// Output tile t of a persistent walk: its first row and column.
+__device__ __forceinline__ void tile_origin(const PParams& p, int t, int bm, int bn, int& m0, int& n0) {
+  if (p.m_fast) {
+    m0 = (t % p.tiles_m) * bm;
+    n0 = (t / p.tiles_m) * bn;
+  } else {
+    m0 = (t / p.tiles_n) * bm;
+    n0 = (t % p.tiles_n) * bn;
+  }
+}
 
 constexpr int kFhC = 10, kFhK = 128;   // classes, inputs of the folded output layer
 constexpr int kFhPart = kFhC * kFhK + kFhC;   // dW_out + db_out partial length
@@ -725,7 +742,8 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
       int it = 0;
       bool ok = true;
       for (int t = t0; t < p.num_tiles && ok; t += tstep) {
-        const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
+        int m0, n0;
+        tile_origin(p, t, BM, BN, m0, n0);
         for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
@@ -819,7 +837,8 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
     int tc = 0, chunk = 0, it = 0;
     bool ok = true;
     for (int t = t0; t < p.num_tiles && ok; t += tstep, ++tc) {
-      const int m0 = (t / p.tiles_n) * BM, n0 = (t % p.tiles_n) * BN;
+      int m0, n0;
+        tile_origin(p, t, BM, BN, m0, n0);
       const int buf = tc & 1;
       const bool last_tile = t + tstep >= p.num_tiles;
       if (ce_a) {
@@ -883,7 +902,9 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
           if (gn0 + 32 + lane < p.N) bias1 = __ldg(p.bias + gn0 + 32 + lane);
         } else if (p.act == ACT_RELU && row_ok && !X3 && !PAIR && p.relu_bits) {
           // the forward's bits of these 64 columns: 8 bytes instead of 128
-          const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.relu_bits + (int64_t)(gn0 / 64) * p.ld_bits + gm));
+          // (a chunk wholly beyond N has no bit group: its mask stays 0)
+          const uint2 w = gn0 < p.N ? __ldg(reinterpret_cast<const uint2*>(p.relu_bits + (int64_t)(gn0 / 64) * p.ld_bits + gm))
+                                    : make_uint2(0u, 0u);
           mask0 = w.x;
           mask1 = w.y;
         } else if (p.act == ACT_RELU && row_ok) {
@@ -955,7 +976,7 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
             }
           }
           act_chunk(v, p.act);
-          if (!X3 && !PAIR && p.relu_bits && row_ok) {
+          if (!X3 && !PAIR && p.relu_bits && row_ok && gn0 < p.N) {
             // bit j: the stored (bf16) activation is positive
             uint32_t b0 = 0u, b1 = 0u;
 #pragma unroll
@@ -1365,6 +1386,342 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_gemm_persistent_kernel(const 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 tc_gemm_pair_kernel(const __grid_constant__ PParams p) {
   persistent_body<128, true, true>(p);
+}
+
+// ---------------------------------------------------------------------------
+// 2-SM variant of the bf16 forward / dgrad (tcgen05.mma.cta_group::2).
+//
+// A cluster of two CTAs on two SMs computes 256 x 256 output tiles.  CTA r
+// keeps rows 128 r .. 128 r + 127 of the tile's A rows and columns
+// 128 r .. 128 r + 127 of its B columns in its own shared memory; one thread
+// of CTA 0 issues the MMAs (M = 256, N = 256), which read both CTAs' halves
+// and accumulate rows 128 r .. 128 r + 127 of the tile into CTA r's TMEM.
+// Per SM a 64-deep stage is then 32 KB for a 128 x 256 x 64 share of the
+// work, against 48 KB for the same work in a one-SM 128 x 256 tile: a third
+// fewer operand bytes from L2 per FLOP.
+//   Both CTAs' loads complete on CTA 0's "full" barriers (a TMA load with
+// .cta_group::2 may signal the peer's barrier); the MMA commits signal the
+// "empty" and "accumulator full" barriers of both CTAs at once (multicast),
+// and both CTAs' epilogue warps arrive on CTA 0's "accumulator empty"
+// barrier.  The epilogue is the one-SM kernel's for bf16 (bias + activation,
+// GELU pre-activation, ReLU bits; dgrad masks) on this CTA's 128 rows.
+// ---------------------------------------------------------------------------
+struct G2Cfg {
+  static constexpr int TBM = 2 * BM, TBN = 256;          // the pair's output tile
+  static constexpr int A_BYTES = BM * BK * 2;            // this CTA's 128 rows of A
+  static constexpr int B_BYTES = (TBN / 2) * BK * 2;     // this CTA's 128 columns of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+  static constexpr int STAGES = 6;
+  static constexpr int EPI_BYTES = P_EPI_WARPS * 4096;   // one 32 x 64 staging buffer per epilogue warp
+  static constexpr int ACC_COLS = TBN;
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;         // double-buffered accumulator
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
+};
+
+__device__ __forceinline__ void tmem_alloc_cg2(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_cg2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16_cg2(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
+}
+// Arrive on the barrier at shared offset `bar` of both CTAs of the pair once
+// the MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_cg2(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+// TMA load into this CTA's shared memory, its bytes counted on a barrier of
+// either CTA of the pair (a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                                uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"((uint64_t)tm), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      if (err) atomicOr(err, ERRBIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
+tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
+  using C = G2Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t a_base = base;
+  const uint32_t b_base = base + C::STAGES * C::A_BYTES;
+  const uint32_t epi_base = b_base + C::STAGES * C::B_BYTES;
+  const uint32_t bar_base = epi_base + C::EPI_BYTES;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * C::STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * C::STAGES + 2 + b); };
+  const uint32_t tmem_slot = bar_base + 8u * (2 * C::STAGES + 4);
+  volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: the CTA whose thread issues the MMAs
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * P_EPI_WARPS);   // the epilogue warps of both CTAs
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc_cg2(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync_all();   // both CTAs' barriers exist before either signals the other's
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_ptr;
+  pdl_enter();   // shared memory and TMEM are set up: now wait for the inputs
+  const uint32_t lead_full0 = mapa_cluster(full_bar(0), 0);
+  const uint32_t lead_tempty0 = mapa_cluster(tempty_bar(0), 0);
+  const int t0 = (int)(blockIdx.x >> 1), tstep = (int)(gridDim.x >> 1);
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      prefetch_tmap(&p.tmA);
+      prefetch_tmap(&p.tmB);
+      prefetch_tmap(&p.tmOut);
+      int it = 0;
+      bool ok = true;
+      for (int t = t0; t < p.num_tiles && ok; t += tstep) {
+        int m0, n0;
+        tile_origin(p, t, C::TBM, C::TBN, m0, n0);
+        m0 += (int)rank * BM;                             // this CTA's rows of A
+        const int nb = n0 + (int)rank * (C::TBN / 2);     // this CTA's columns of B
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
+          if (rank == 0) mbar_expect_tx(full_bar(s), 2u * C::STAGE_BYTES);   // both CTAs' bytes
+          const uint32_t fb = lead_full0 + 8u * (uint32_t)s;
+          const int k0 = kb * BK;
+          const uint32_t sa = a_base + s * C::A_BYTES;
+          const uint32_t sb = b_base + s * C::B_BYTES;
+          tma_load_2d_cg2(sa, &p.tmA, k0, m0, fb);
+          if (!p.b_mn) {
+            tma_load_2d_cg2(sb, &p.tmB, k0, nb, fb);
+          } else {
+            tma_load_2d_cg2(sb, &p.tmB, nb, k0, fb);
+            tma_load_2d_cg2(sb + 8192u, &p.tmB, nb + 64, k0, fb);
+          }
+        }
+      }
+      // every stage this CTA filled has been read by the MMAs (its empty
+      // barrier completed), so no copy into this CTA's memory is in flight
+      for (int i = max(0, it - C::STAGES); i < it; ++i)
+        mbar_wait(empty_bar(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u, p.err);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (CTA 0) ----------------
+    if (rank == 0 && lane == 0) {
+      const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
+      const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int t = t0; t < p.num_tiles && ok; t += tstep, ++tc) {
+        const int buf = tc & 1;
+        if (!mbar_wait_cluster(tempty_bar(buf), (((uint32_t)tc >> 1) & 1u) ^ 1u, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          if (!mbar_wait(full_bar(s), (uint32_t)(it / C::STAGES) & 1u, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = a_base + s * C::A_BYTES;
+          const uint32_t sb = b_base + s * C::B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16_cg2(d, sdesc(sa + kk * 32u, 16u, 1024u), sdesc(sb + kk * b_kstep, b_lbo, 1024u), p.idesc,
+                         (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_cg2(empty_bar(s));
+        }
+        mma_commit_cg2(tfull_bar(buf));
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..9: this CTA's 128 rows ----------------
+    // warp w reads TMEM lanes 32 (w % 4) .. +31 and the 128 columns of its
+    // half of the tile, 64 at a time
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * 4096);
+    uint8_t* srow = base_ptr + (stage0 - base) + lane * 128;
+    int tc = 0;
+    bool ok = true;
+    for (int t = t0; t < p.num_tiles && ok; t += tstep, ++tc) {
+      int m0, n0;
+      tile_origin(p, t, C::TBM, C::TBN, m0, n0);
+      m0 += (int)rank * BM;
+      const int buf = tc & 1;
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::ACC_COLS);
+      const int gm = m0 + q * 32 + lane;
+      const bool row_ok = gm < p.M;
+      bool acc_ready = false;
+#pragma unroll 1
+      for (int c0 = half * (C::TBN / 2); c0 < (half + 1) * (C::TBN / 2); c0 += 64) {
+        const int gn0 = n0 + c0;
+        // the chunk's bias (lane j: columns j and 32 + j) or ReLU mask, loaded
+        // before the accumulator wait
+        float bias0 = 0.f, bias1 = 0.f;
+        uint32_t mask0 = 0u, mask1 = 0u;
+        if (p.kind == GEMM_FWD) {
+          if (gn0 + lane < p.N) bias0 = __ldg(p.bias + gn0 + lane);
+          if (gn0 + 32 + lane < p.N) bias1 = __ldg(p.bias + gn0 + 32 + lane);
+        } else if (p.act == ACT_RELU && row_ok && p.relu_bits && gn0 < p.N) {
+          // (a chunk wholly beyond N has no bit group: its mask stays 0)
+          const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.relu_bits + (int64_t)(gn0 / 64) * p.ld_bits + gm));
+          mask0 = w.x;
+          mask1 = w.y;
+        } else if (p.act == ACT_RELU && row_ok) {
+          const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
+          for (int j = 0; j < 32; ++j) {
+            if (gn0 + j < p.N && __bfloat162float(ar[j]) > 0.f) mask0 |= 1u << j;
+            if (gn0 + 32 + j < p.N && __bfloat162float(ar[32 + j]) > 0.f) mask1 |= 1u << j;
+          }
+        }
+        if (!acc_ready) {
+          ok = __all_sync(0xffffffffu, mbar_wait_cluster(tfull_bar(buf), ((uint32_t)tc >> 1) & 1u, p.err));
+          if (!ok) break;
+          tc_fence_after();
+          acc_ready = true;
+        }
+        float v[64];
+        tmem_ld64(trow + (uint32_t)c0, v);
+        if (c0 + 64 >= (half + 1) * (C::TBN / 2)) {
+          // this warp's part of the accumulator is drained: hand it back to CTA 0
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lead_tempty0 + 8u * (uint32_t)buf);
+        }
+        if (p.kind == GEMM_FWD) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] += __shfl_sync(0xffffffffu, bias0, j);
+            v[32 + j] += __shfl_sync(0xffffffffu, bias1, j);
+          }
+          if (p.out_u && row_ok) {
+            __nv_bfloat16* du = p.out_u + (int64_t)gm * p.ldu + gn0;
+            if (gn0 + 64 <= p.N) {
+#pragma unroll
+              for (int j = 0; j < 64; j += 8) {
+                uint4 w;
+                __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+                for (int h = 0; h < 4; ++h) w2[h] = __floats2bfloat162_rn(v[j + 2 * h], v[j + 2 * h + 1]);
+                *reinterpret_cast<uint4*>(du + j) = w;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 64; ++j)
+                if (gn0 + j < p.N) du[j] = __float2bfloat16_rn(v[j]);
+            }
+          }
+          act_chunk(v, p.act);
+          if (p.relu_bits && row_ok && gn0 < p.N) {
+            // bit j: the stored (bf16) activation is positive
+            uint32_t b0 = 0u, b1 = 0u;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              b0 |= (gn0 + j < p.N && __bfloat162float(__float2bfloat16_rn(v[j])) > 0.f ? 1u : 0u) << j;
+              b1 |= (gn0 + 32 + j < p.N && __bfloat162float(__float2bfloat16_rn(v[32 + j])) > 0.f ? 1u : 0u) << j;
+            }
+            *reinterpret_cast<uint2*>(p.relu_bits + (int64_t)(gn0 / 64) * p.ld_bits + gm) = make_uint2(b0, b1);
+          }
+        } else if (p.act == ACT_RELU) {   // dgrad: dX * 1[h > 0]
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] *= (float)((mask0 >> j) & 1u);
+            v[32 + j] *= (float)((mask1 >> j) & 1u);
+          }
+        } else if (p.act == ACT_GELU_TANH) {   // dgrad: dX * gelu'(u)
+          const __nv_bfloat16* ar = p.aux + (int64_t)gm * p.ld_aux + gn0;
+          if (row_ok && gn0 + 64 <= p.N) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint4 a = __ldg(reinterpret_cast<const uint4*>(ar) + u);
+              const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&a);
+#pragma unroll
+              for (int h = 0; h < 8; ++h) v[8 * u + h] *= gelu_tanh_grad(__bfloat162float(e[h]));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              v[j] *= (row_ok && gn0 + j < p.N) ? gelu_tanh_grad(__bfloat162float(ar[j])) : 0.f;
+          }
+        }
+        // stage the chunk (128B-swizzled) once the previous store has read
+        // the buffer, then one TMA store (it clips the ragged edges); a chunk
+        // wholly beyond N stores nothing
+        if (gn0 >= p.N) continue;
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        stage_plane(srow, lane, v, false);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tmOut, stage0, gn0, m0 + q * 32);
+          bulk_commit();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  // neither CTA leaves while the other may still signal its barriers, or the
+  // MMAs may still read this CTA's shared memory or write its TMEM
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_cg2(tmem, C::TMEM_COLS);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1968,6 +2325,86 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   return 1;
 }
 
+const void* tcg2_kernel_ptr() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute((const void*)tc::tc_gemm_cg2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         tc::G2Cfg::SMEM_BYTES);
+  });
+  return (const void*)tc::tc_gemm_cg2_kernel;
+}
+
+// CTA pairs of the 2-SM kernel that fit on the device at once (a GPC may
+// leave an SM unpaired), so that a persistent grid is one wave.
+int cg2_max_clusters() {
+  static int n = [] {
+    const int sms = device_sms();
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)(sms & ~1));
+    cfg.blockDim = dim3(tc::P_THREADS);
+    cfg.dynamicSmemBytes = tc::G2Cfg::SMEM_BYTES;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, tcg2_kernel_ptr(), &cfg) != cudaSuccess || c < 1) {
+      cudaGetLastError();
+      c = sms / 2;
+    }
+    return c;
+  }();
+  return n;
+}
+
+// Forward / dgrad on the 2-SM kernel: CTA pairs walk 256 x 256 tiles.
+int tc_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
+  using G = tc::G2Cfg;
+  tc::PParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_tmap(&p.tmA, op.A, op.K, op.M, op.lda, 64, tc::BM, err, errlen)) return -1;
+  if (op.b_kmajor) {
+    if (!make_tmap(&p.tmB, op.B, op.K, op.N, op.ldb, 64, G::TBN / 2, err, errlen)) return -1;
+  } else {
+    if (!make_tmap(&p.tmB, op.B, op.N, op.K, op.ldb, 64, 64, err, errlen)) return -1;
+  }
+  if (!make_tmap(&p.tmOut, op.out, op.N, op.M, op.ldo, 64, 32, err, errlen)) return -1;
+  p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
+  p.num_kb = (int)ceil_div(op.K, tc::BK);
+  p.tiles_n = (int)ceil_div(op.N, G::TBN);
+  p.tiles_m = (int)ceil_div(op.M, G::TBM);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.m_fast = op.M < op.N ? 1 : 0;
+  p.b_mn = op.b_kmajor ? 0 : 1;
+  p.kind = op.kind; p.act = op.act;
+  // D f32, A and B bf16, B MN-major for the dgrad, N = 256, M = 256 (two CTAs)
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)p.b_mn << 16) | ((uint32_t)(G::TBN >> 3) << 17) |
+            ((uint32_t)(G::TBM >> 4) << 24);
+  p.bias = op.bias;
+  p.out_u = (__nv_bfloat16*)op.out_u; p.ldu = op.ldu;
+  p.aux = (const __nv_bfloat16*)op.aux; p.ld_aux = op.ld_aux;
+  p.err = op.err;
+  if (op.relu_bits && op.act == ACT_RELU) {
+    if (op.ld_bits < op.M || ((uintptr_t)op.relu_bits & 7)) {
+      snprintf(err, errlen, "ReLU bits: ld_bits >= M, 8-byte aligned");
+      return -1;
+    }
+    p.relu_bits = op.relu_bits; p.ld_bits = op.ld_bits;
+  }
+  const int clusters = std::min(p.num_tiles, cg2_max_clusters());
+  LaunchRec& r = recs[0];
+  r.func = tcg2_kernel_ptr();
+  r.smem = G::SMEM_BYTES;
+  r.grid = dim3((unsigned)(2 * clusters));
+  r.block = dim3(tc::P_THREADS);
+  r.early = true;
+  r.name = op.kind == GEMM_FWD ? "tc2_gemm_fwd" : "tc2_gemm_dgrad";
+  r.set_args(p);
+  return 1;
+}
+
 // Forward / dgrad on the persistent kernel (bf16 output through TMA stores).
 int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   // 256-wide tiles where they still give every SM a tile
@@ -1980,6 +2417,11 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
     snprintf(err, errlen, "softmax-CE GEMM: bf16, labels, and (forward) more than 128 columns");
     return -1;
   }
+  // bf16 with at least 256 rows and columns: CTA pairs with 2-SM MMAs,
+  // by default where the pair tiles fill the device at least once
+  if (!x3 && !ce_f && !ce_a && op.dtype == DT_BF16 && op.cg2 != 0 && op.M >= 256 && op.N >= 256 &&
+      (op.cg2 > 0 || ceil_div(op.M, 256) * ceil_div(op.N, 256) >= cg2_max_clusters()))
+    return tc_cg2_plan(op, recs, err, errlen);
   const int BN = !x3 && op.N > 128 && (ce_f || ceil_div(op.M, tc::BM) * ceil_div(op.N, 256) >= sms) ? 256 : 128;
   tc::PParams p;
   memset(&p, 0, sizeof(p));
@@ -1993,7 +2435,8 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
   p.num_kb = (int)ceil_div(op.K, tc::BK);
   p.tiles_n = (int)ceil_div(op.N, BN);
-  p.num_tiles = (int)(ceil_div(op.M, tc::BM) * p.tiles_n);
+  p.tiles_m = (int)ceil_div(op.M, tc::BM);
+  p.num_tiles = p.tiles_m * p.tiles_n;
   p.b_mn = op.b_kmajor ? 0 : 1;
   p.kind = op.kind; p.act = op.act;
   p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)p.b_mn << 16) | ((uint32_t)(BN >> 3) << 17) |
@@ -2011,6 +2454,9 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   // fp32 planes with few tiles: a CTA pair per tile, each half of K (with
   // fewer than three K stages the exchange costs more than the halved loop)
   const bool pair = x3 && 2 * p.num_tiles <= sms && p.num_kb >= 3;
+  // B is the larger operand (more columns than rows): walk the row tiles of
+  // a column tile first, so B is read from DRAM about once
+  p.m_fast = !pair && op.M < op.N ? 1 : 0;
   if (op.relu_bits && op.act == ACT_RELU) {
     if (x3 || pair || op.ld_bits < op.M || ((uintptr_t)op.relu_bits & 7)) {
       snprintf(err, errlen, "ReLU bits: bf16 only, ld_bits >= M, 8-byte aligned");

@@ -414,6 +414,46 @@ def test_train_step_host_matches_device_inputs(name, batch):
 
 
 # --------------------------------------------------------------------------
+# 2-SM GEMMs (CTA pairs, 256 x 256 tiles): the same sums as the one-SM kernels
+# --------------------------------------------------------------------------
+RAGGED_2SM = synth.Workload("ragged_2sm", (320, 264, 520, 100), (om.ACT_GELU_TANH, om.ACT_RELU), synth.BF16, 300, 2,
+                            1e-3, 0.9, 0.999, 1e-8, 0.01, "normal", 12)
+
+
+@pytest.mark.parametrize("w,batch", [(W["cifar_mlp_b8192"], None), (W["lm_block_t16384"], 2048),
+                                     (W["deep_narrow_b65536"], 3000), (RAGGED_2SM, None)],
+                         ids=["cifar_full", "lm_block_2048", "deep_narrow_3000", "ragged"])
+def test_gemm_2sm_equals_one_sm(w, batch):
+    """The step with the bf16 forward / dgrad GEMMs on CTA pairs with 2-SM
+    MMAs (MLP_OPT_GEMM_2SM 1) and with every GEMM on one SM (0): each output
+    element is the same sequence of 16-deep MMA accumulations, so losses,
+    parameters and gradients agree bit for bit.  Ragged case: 300 rows (one
+    full and one partial 256-row pair tile), 264 and 520 columns, GELU and
+    ReLU layers (the ReLU bits and the GELU pre-activation on pair tiles)."""
+    B = w.batch if batch is None else batch
+    params0 = synth.make_params(w)
+    bl = P.batches(w, 2, B)
+    res, names = [], []
+    for on in (1, 0):
+        m = make_model(w, B, params0)
+        m.set_option(nn.OPT_GEMM_2SM, on)
+        x, y = bl[0]
+        prof = nn.mlp_profile_step(m.h, x.to(DEV).data_ptr(), y.to(DEV).data_ptr(), w.lr, w.beta1, w.beta2, w.eps,
+                                   w.wd, None, m.stream())
+        names.append([n for n, _ in prof])
+        m.close()
+        m = make_model(w, B, params0)
+        m.set_option(nn.OPT_GEMM_2SM, on)
+        losses, p, g = gpu_run(m, w, bl)
+        m.close()
+        res.append((losses, P.flat(p), P.flat(g)))
+    assert "tc2_gemm_fwd" in names[0] and "tc2_gemm_dgrad" in names[0]
+    assert not any(n.startswith("tc2_") for n in names[1])
+    for a, b in zip(res[0], res[1]):
+        assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------------------------
 # ReLU masks as bits (bf16): identical to reading the stored activation
 # --------------------------------------------------------------------------
 RAGGED_BF16 = synth.Workload("bits_ragged", (64, 200, 72, 10), (om.ACT_RELU, om.ACT_RELU), synth.BF16, 300, 2,
