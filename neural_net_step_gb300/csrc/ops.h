@@ -193,6 +193,9 @@ struct AdamWOp {
 enum { OPTIM_ADAMW = 0, OPTIM_ADAM = 1, OPTIM_SGD = 2 };
 // One or two records (clipping: norm, then update) into rec[0..1].
 int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen);
+// The gradient finished without an update: the segments added and written
+// to g, and the loss formed from loss_parts (both as the update would).
+int grad_finish_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen);
 
 // Row argmax, lowest index among equal maxima.
 struct ArgmaxOp {

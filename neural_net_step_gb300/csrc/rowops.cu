@@ -730,7 +730,19 @@ __global__ void __launch_bounds__(256) grad_norm_kernel(const __grid_constant__ 
     a += g * g;
   }
   a = block_sum256(a, red);
-  if (threadIdx.x == 0) q.norm_ws[blockIdx.x] = a;
+  if (threadIdx.x == 0 && q.norm_ws) q.norm_ws[blockIdx.x] = a;
+  if (q.loss_parts && blockIdx.x == 0 && threadIdx.x < 32) {
+    // the batch loss from the output layer's partials (a gradient step that
+    // leaves the update to a later launch): as in the update kernel
+    float l = 0.f;
+    for (int c = threadIdx.x; c < q.loss_n; c += 32) l += __ldcg(q.loss_parts + c);
+    l = warp_sum(l);
+    const float L = l * q.loss_scale;
+    if (threadIdx.x == 0) {
+      if (q.loss) *q.loss = L;
+      if (q.err && !isfinite(L)) atomicOr(q.err, ERRBIT_NONFINITE);
+    }
+  }
 }
 
 template <int KIND, bool CLIP>
@@ -816,6 +828,29 @@ const void* update_kernel(int kind) {
   return kind == OPTIM_ADAM ? (const void*)adamw_kernel<OPTIM_ADAM, CLIP>
          : kind == OPTIM_SGD ? (const void*)adamw_kernel<OPTIM_SGD, CLIP>
                              : (const void*)adamw_kernel<OPTIM_ADAMW, CLIP>;
+}
+
+int grad_finish_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {
+  if (op.n < 0 || op.nseg < 0 || op.nseg > AdamWOp::kMaxSegs || ((uintptr_t)op.g % 16)) {
+    snprintf(err, errlen, "gradient finish: bad plane or segments");
+    return -1;
+  }
+  AdamWParams q{};
+  q.g = op.g; q.n = op.n;
+  for (int k = 0; k < op.nseg; ++k) q.seg[k] = op.seg[k];
+  q.nseg = op.nseg;
+  q.loss_parts = op.loss_parts; q.loss_n = op.loss_n; q.loss_scale = op.loss_scale; q.loss = op.loss; q.err = op.err;
+  q.norm_ws = op.norm_ws;
+  int64_t blocks = ceil_div(op.n / 4 + 1, 256);
+  if (blocks > AdamWOp::kNormParts) blocks = AdamWOp::kNormParts;
+  if (blocks < 1) blocks = 1;
+  rec->func = (const void*)grad_norm_kernel;
+  rec->grid = dim3((unsigned)blocks);
+  rec->block = dim3(256);
+  rec->smem = 0;
+  rec->name = "grad_finish";
+  rec->set_args(q);
+  return 1;
 }
 
 int adamw_plan(const AdamWOp& op, LaunchRec* rec, char* err, size_t errlen) {

@@ -2417,10 +2417,14 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
     snprintf(err, errlen, "softmax-CE GEMM: bf16, labels, and (forward) more than 128 columns");
     return -1;
   }
-  // bf16 with at least 256 rows and columns: CTA pairs with 2-SM MMAs,
-  // by default where the pair tiles fill the device at least once
+  // bf16 with at least 256 rows and columns: CTA pairs with 2-SM MMAs, by
+  // default where the pair tiles fill the device at least once and the
+  // reduction is at least 16 stages long (with fewer, the per-tile costs
+  // that a pair pays together outweigh the halved operand traffic: the
+  // 512-wide layers of the deep narrow net, K = 512, measured 12 % slower)
   if (!x3 && !ce_f && !ce_a && op.dtype == DT_BF16 && op.cg2 != 0 && op.M >= 256 && op.N >= 256 &&
-      (op.cg2 > 0 || ceil_div(op.M, 256) * ceil_div(op.N, 256) >= cg2_max_clusters()))
+      (op.cg2 > 0 || (ceil_div(op.M, 256) * ceil_div(op.N, 256) >= cg2_max_clusters() &&
+                      ceil_div(op.K, tc::BK) >= 16)))
     return tc_cg2_plan(op, recs, err, errlen);
   const int BN = !x3 && op.N > 128 && (ce_f || ceil_div(op.M, tc::BM) * ceil_div(op.N, 256) >= sms) ? 256 : 128;
   tc::PParams p;
