@@ -280,6 +280,35 @@ mlp_status mlp_profile_step(mlp_t* model, const void* x_dev, const void* y_dev, 
                             float beta2, float eps, float wd, float* loss_dev, void* stream, float* ms_out,
                             const char** names_out, int max_kernels, int* n_out);
 
+/* Data-parallel training (MuNet, pypi "munet-nn", "Reliability,
+ * observability and scaling": mu.DataParallel splits each batch on dim 0 and
+ * averages the gradients; netcl.online "Architecture: Distributed &
+ * Multi-Device Execution", data_parallel_step: shard the batch, synchronise
+ * the gradients, update; noeira.ai "Neural networks", "Distributed
+ * training": DDP).  A step is split at its one exchange point:
+ *   1. mlp_grad_step on this rank's rows of a global batch of global_batch
+ *      rows (the model's batch is the shard's row count; shards may differ
+ *      by rank): forward and backward; G receives the shard's gradient of
+ *      the GLOBAL mean loss (dz scaled by 1 / global_batch), so the sum of G
+ *      over ranks is the gradient of the whole batch; *loss_dev (nullable)
+ *      receives the shard's share, sum of its row losses / global_batch
+ *      (MSE: / (global_batch C)), so those sum to the batch loss.  Advances
+ *      the step counter.  global_batch < the model's batch: MLP_ERR_ARG.
+ *   2. the caller sums G over the ranks in place (an NCCL all-reduce on the
+ *      buffer mlp_grad_buffer names, on this stream or ordered after it).
+ *   3. mlp_apply_update: the update rule of mlp_set_optimizer (clipping
+ *      included) over G, at the step counter of step 1.  Exactly one update
+ *      per gradient step; every rank then holds the same parameters.
+ * With one rank (global_batch = the model's batch) 1 + 3 is mlp_train_step,
+ * bit for bit.  Both are CUDA-graph replays like mlp_train_step. */
+mlp_status mlp_grad_step(mlp_t* model, const void* x_dev, const void* y_dev, int64_t global_batch, float* loss_dev,
+                         void* stream);
+mlp_status mlp_apply_update(mlp_t* model, float lr, float beta1, float beta2, float eps, float wd, void* stream);
+/* The gradient plane G: device address and length in floats (the flat
+ * parameter layout with its padding, every tensor 64-element aligned; the
+ * padding holds zeros and sums to zero).  Valid for the model's lifetime. */
+mlp_status mlp_grad_buffer(mlp_t* model, float** g_dev, int64_t* n_floats);
+
 /* Traced step: one training step (same arguments and effect as
  * mlp_train_step) whose kernels run one after another on `stream`, each
  * followed by device-to-device copies of the tensors it wrote into the

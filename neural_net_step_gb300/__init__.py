@@ -58,6 +58,9 @@ _SIGS = {
     "mlp_kernels_per_step": (_I32, [_P]),
     "mlp_profile_step": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P, _c.POINTER(_F), _c.POINTER(_c.c_char_p),
                                 _I32, _c.POINTER(_I32)]),
+    "mlp_grad_step": (_I32, [_P, _P, _P, _I64, _P, _P]),
+    "mlp_apply_update": (_I32, [_P, _F, _F, _F, _F, _F, _P]),
+    "mlp_grad_buffer": (_I32, [_P, _c.POINTER(_P), _c.POINTER(_I64)]),
     "mlp_trace_step": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P, _SZ, _P, _I32, _c.POINTER(_I32),
                               _c.POINTER(_SZ), _P]),
     "mlp_last_error": (_c.c_char_p, []),
@@ -138,6 +141,21 @@ def mlp_train_step(h, x_ptr, labels_ptr, lr, beta1, beta2, eps, wd, loss_ptr, st
 
 def mlp_train_step_host(h, x_host_ptr, labels_host_ptr, lr, beta1, beta2, eps, wd, loss_host_ptr, stream) -> None:
     _check(lib().mlp_train_step_host(h, x_host_ptr, labels_host_ptr, lr, beta1, beta2, eps, wd, loss_host_ptr, stream))
+
+
+def mlp_grad_step(h, x_ptr, y_ptr, global_batch, loss_ptr, stream) -> None:
+    _check(lib().mlp_grad_step(h, x_ptr, y_ptr, global_batch, loss_ptr, stream))
+
+
+def mlp_apply_update(h, lr, beta1, beta2, eps, wd, stream) -> None:
+    _check(lib().mlp_apply_update(h, lr, beta1, beta2, eps, wd, stream))
+
+
+def mlp_grad_buffer(h):
+    """(device address, length in floats) of the gradient plane G."""
+    ptr, n = _P(), _I64(0)
+    _check(lib().mlp_grad_buffer(h, ctypes.byref(ptr), ctypes.byref(n)))
+    return ptr.value, n.value
 
 
 def mlp_train_steps(h, x_ptrs, label_ptrs, lr, beta1, beta2, eps, wd, losses_ptr, stream) -> None:
@@ -391,6 +409,25 @@ class Model:
         mlp_forward(self.h, x.data_ptr(), logits.data_ptr() if logits is not None else None,
                     am.data_ptr() if am is not None else None, self.stream())
         return logits, am
+
+    def grad_step(self, x, labels, global_batch, loss=None):
+        """Forward + backward of this shard of a global batch (mlp_grad_step);
+        G then holds the shard's gradient of the global mean loss."""
+        self._check_x(x, labels)
+        if loss is None:
+            loss = self.torch.empty((), dtype=self.torch.float32, device=x.device)
+        mlp_grad_step(self.h, x.data_ptr(), labels.data_ptr(), global_batch, loss.data_ptr(), self.stream())
+        return loss
+
+    def apply_update(self, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0):
+        mlp_apply_update(self.h, lr, beta1, beta2, eps, wd, self.stream())
+
+    def grad_tensor(self):
+        """G as a float32 CUDA tensor viewing the arena (the all-reduce buffer)."""
+        ptr, n = mlp_grad_buffer(self.h)
+        off = ptr - self.arena.data_ptr()
+        assert 0 <= off and off + 4 * n <= self.arena.numel() and off % 4 == 0
+        return self.arena[off:off + 4 * n].view(self.torch.float32)
 
     def trace_step(self, x, labels, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0, loss=None):
         """One traced training step (mlp_trace_step).  Returns (loss, [(entry,

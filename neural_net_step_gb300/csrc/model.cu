@@ -416,10 +416,16 @@ mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out
 
 struct Hyper { float lr, b1, b2, eps, wd; };
 
+// A step's plan.  grad_only: forward and backward only, the gradient left
+// finished in G (no update; the update is planned by plan_update).
+// scale_batch > 0: the loss and its gradient are those of a mean over
+// scale_batch rows of which this batch is a part (a data-parallel shard);
+// 0: over this batch.
 mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp, float* loss,
-                     std::vector<LaunchRec>& out) {
+                     std::vector<LaunchRec>& out, bool grad_only = false, int64_t scale_batch = 0) {
   const Layout& L = m->lay;
   const bool mse = m->loss == MLP_LOSS_MSE;
+  const double Bs = (double)(scale_batch > 0 ? scale_batch : L.B);   // the batch the loss is a mean over
   const bool fuse = m->fuse_head && L.L >= 2 && head_supported(L.dims[L.L], L.dims[L.L - 1]);
   const bool x3 = m->x3();   // implies fuse
   // a wide bf16 output layer: softmax-CE inside its GEMMs (statistics from the
@@ -438,7 +444,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     hf.head_bias = m->plane(MLP_PLANE_P) + L.boff[l];
     hf.head_labels = (const int32_t*)y;
     hf.head_ws = (float*)m->at(L.off_hws);
-    hf.head_scale = (float)(1.0 / (double)L.B);
+    hf.head_scale = (float)(1.0 / Bs);
     hf.step_counter = &ctl->step;
     hf.bias_corr = ctl->bias_corr; hf.beta1 = hp.b1; hf.beta2 = hp.b2;
     hf.out = m->at(L.off_dy[0]); hf.ldo = L.ld_h[l - 1]; hf.out_plane = dy_plane;
@@ -476,7 +482,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     hd.step_counter = &ctl->step;
     hd.err = &ctl->err;
     hd.ws = (float*)m->at(L.off_hws); hd.ws_bytes = L.hws_bytes;
-    hd.grad_scale = (float)((mse ? 2.0 / (double)L.dims[L.L] : 1.0) / (double)L.B);
+    hd.grad_scale = (float)((mse ? 2.0 / (double)L.dims[L.L] : 1.0) / Bs);
     hd.bias_corr = ctl->bias_corr; hd.beta1 = hp.b1; hd.beta2 = hp.b2;
     char e_[512] = "";
     LaunchRec r;
@@ -505,7 +511,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
       op.t = (const float*)y; op.ldt = L.dims[L.L];
       op.dz = m->at(L.off_dz); op.lddz = L.ldz;
       op.loss_rows = loss_rows;
-      op.grad_scale = (float)(2.0 / ((double)L.B * (double)L.dims[L.L]));
+      op.grad_scale = (float)(2.0 / (Bs * (double)L.dims[L.L]));
       if (mse_plan(op, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
     } else {
       CeOp ce;
@@ -514,7 +520,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
       ce.labels = (const int32_t*)y;
       ce.dz = m->at(L.off_dz); ce.lddz = L.ldz;
       ce.loss_rows = loss_rows;
-      ce.grad_scale = (float)(1.0 / (double)L.B);
+      ce.grad_scale = (float)(1.0 / Bs);
       ce.err = &ctl->err;
       if (ce_plan(ce, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
     }
@@ -524,7 +530,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     r.nouts = 0;   // the record is reused for the loss mean, which writes no traced tensor
     LossMeanOp lm;
     lm.B = L.B; lm.loss_rows = loss_rows;
-    lm.count = mse ? (double)L.B * (double)L.dims[L.L] : (double)L.B;
+    lm.count = mse ? Bs * (double)L.dims[L.L] : Bs;
     lm.loss = loss ? loss : &ctl->loss_slot;
     lm.step_counter = &ctl->step;
     lm.err = &ctl->err;
@@ -556,7 +562,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     const bool ce_top = ce_gemm && l == L.L - 1;
     if (ce_top) {
       wg.ce_rowstat = (const float2*)m->at(L.off_cerow); wg.ce_labels = (const int32_t*)y;
-      wg.ce_scale = (float)(1.0 / (double)L.B);
+      wg.ce_scale = (float)(1.0 / Bs);
     }
     // split-K partials go to the optimizer (it reads them 4 at a time)
     const int64_t MN = wg.M * wg.N;
@@ -628,12 +634,22 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     ad.seg[ad.nseg++] = AdamWOp::Seg{L.woff[l], nw, hws, hpart.n, hpart.stride};
     ad.seg[ad.nseg++] = AdamWOp::Seg{L.boff[l], L.dims[L.L], hws + nw, hpart.n, hpart.stride};
     ad.loss_parts = hws + hpart.loss_off; ad.loss_n = hpart.n;
-    ad.loss_scale = (float)(1.0 / ((double)L.B * (mse ? (double)L.dims[L.L] : 1.0)));
+    ad.loss_scale = (float)(1.0 / (Bs * (mse ? (double)L.dims[L.L] : 1.0)));
     ad.loss = loss ? loss : &ctl->loss_slot;
     ad.err = &ctl->err;
   }
   char e_[512] = "";
   LaunchRec r[2];
+  if (grad_only) {
+    // the gradient finished where parts of it are still partial sums (and
+    // the loss formed from the output layer's partials); else nothing to do
+    if (ad.nseg == 0 && !ad.loss_parts) return MLP_OK;
+    if (grad_finish_plan(ad, r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_ARG, "%s", e_);
+    const int d[1] = {side_tail >= 0 ? side_tail : main_tail};
+    r[0].depend_on(d, 1);
+    add(out, 1, r);
+    return MLP_OK;
+  }
   const int nr = adamw_plan(ad, r, e_, sizeof(e_));
   if (nr < 0) return fail(MLP_ERR_ARG, "%s", e_);
   // the last weight gradient already follows the last dgrad (a single edge
@@ -643,6 +659,37 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
   add(out, nr, r);
   return MLP_OK;
 }
+
+// The update half of a split step: the model's update rule over the
+// finished gradient in G, at the step counter the gradient step advanced
+// (bias corrections from that t and the betas given here).
+mlp_status plan_update(const mlp* m, const Hyper& hp, std::vector<LaunchRec>& out) {
+  const Layout& L = m->lay;
+  Ctl* ctl = m->ctl();
+  const bool x3 = m->x3();
+  AdamWOp ad;
+  ad.n = L.plane_n;
+  ad.p = m->plane(MLP_PLANE_P); ad.g = m->plane(MLP_PLANE_G);
+  ad.m = m->plane(MLP_PLANE_M); ad.v = m->plane(MLP_PLANE_V);
+  ad.w16 = L.dtype == MLP_BF16 || x3 ? m->w16() : nullptr;
+  ad.w16_plane = x3 ? L.plane_n : 0;
+  ad.step_counter = &ctl->step;
+  ad.bias_corr = nullptr;
+  ad.lr = hp.lr; ad.beta1 = hp.b1; ad.beta2 = hp.b2; ad.eps = hp.eps; ad.wd = hp.wd;
+  ad.kind = m->optim;
+  ad.max_norm = m->max_grad_norm;
+  ad.norm_ws = (float*)m->at(L.off_norm);
+  ad.norm_out = &ctl->grad_norm;
+  char e_[512] = "";
+  LaunchRec r[2];
+  const int nr = adamw_plan(ad, r, e_, sizeof(e_));
+  if (nr < 0) return fail(MLP_ERR_ARG, "%s", e_);
+  add(out, nr, r);
+  return MLP_OK;
+}
+
+// Graph-cache keys of the two halves of a split step (whole steps use n >= 1).
+constexpr int kGradStepKey = -1, kUpdateKey = -2;
 
 mlp_status launch_eager(const std::vector<LaunchRec>& recs, cudaStream_t s) {
   for (const auto& r : recs) {
@@ -1011,6 +1058,38 @@ mlp_status mlp_train_step_host(mlp_t* m, const void* x_host, const void* y_host,
   CUDA_TRY(cudaEventRecord(m->consumed[k], s));
   if (copy_loss) CUDA_TRY(cudaMemcpyAsync(loss_host, &m->ctl()->loss_slot, 4, cudaMemcpyDeviceToHost, s));
   ++m->host_calls;
+  return ok();
+}
+
+mlp_status mlp_grad_step(mlp_t* m, const void* x, const void* y, int64_t global_batch, float* loss, void* stream) {
+  if (!m || !x || !y) return fail(MLP_ERR_ARG, "bad arguments");
+  if (global_batch < m->lay.B) return fail(MLP_ERR_ARG, "global_batch (%lld) is smaller than the model's batch (%lld)",
+                                           (long long)global_batch, (long long)m->lay.B);
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  std::vector<LaunchRec> recs;
+  // (the betas only feed bias corrections that mlp_apply_update recomputes)
+  mlp_status st = plan_step(m, x, y, Hyper{0.f, 0.9f, 0.999f, 0.f, 0.f}, loss, recs, true, global_batch);
+  if (st != MLP_OK) return st;
+  return run(m, kGradStepKey, recs, (cudaStream_t)stream);
+}
+
+mlp_status mlp_apply_update(mlp_t* m, float lr, float b1, float b2, float eps, float wd, void* stream) {
+  if (!m) return fail(MLP_ERR_ARG, "model is NULL");
+  if (!(lr >= 0) || !(b1 >= 0 && b1 < 1) || !(b2 >= 0 && b2 < 1) || !(eps >= 0) || !(wd >= 0))
+    return fail(MLP_ERR_ARG, "bad hyper-parameters");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_update(m, Hyper{lr, b1, b2, eps, wd}, recs);
+  if (st != MLP_OK) return st;
+  return run(m, kUpdateKey, recs, (cudaStream_t)stream);
+}
+
+mlp_status mlp_grad_buffer(mlp_t* m, float** g_dev, int64_t* n) {
+  if (!m || !g_dev || !n) return fail(MLP_ERR_ARG, "bad arguments");
+  *g_dev = m->plane(MLP_PLANE_G);
+  *n = m->lay.plane_n;
   return ok();
 }
 
