@@ -14,9 +14,13 @@ steps as one CUDA graph (the deep narrow net's configuration captures 50).
 Timing: W untimed warm-up steps, then K steps between CUDA events on the
 launching stream, bracketed by a barrier and a device synchronize; the step
 reads a fresh batch each time from a device-resident pool larger than L2
-(129 MB), so no step finds its input in L2.  Under torchrun every rank runs
-an independent replica of the step on its own GPU (the path is replicated,
-not sharded, here) and the slowest rank's time counts.
+(129 MB), so no step finds its input in L2.  Under torchrun (N ranks, one
+GPU each) the default is data parallelism at the workload's fixed global
+batch (strong scaling): each rank steps on its rows, the flat fp32 gradient
+plane is summed over the ranks with an NCCL all-reduce between the gradient
+step and the update (neural_net_step_gb300.dp), and `value` is the global
+batch per step time; `--parallel replicas` runs N independent replicas
+instead (weak scaling).  The slowest rank's time counts.
 
 Also reported: `e2e` (the same metric through the C ABI with pinned host
 buffers: every step copies its batch host->device and reads the loss back),
@@ -396,6 +400,8 @@ def main():
                     help="update rule (default AdamW)")
     ap.add_argument("--max-grad-norm", type=float, default=0.0, help="> 0: global gradient-norm clipping")
     ap.add_argument("--loss", default="ce", choices=["ce", "mse"], help="softmax CE (default) or MSE")
+    ap.add_argument("--parallel", default="dp", choices=["dp", "replicas"],
+                    help="N > 1: data parallelism at the fixed global batch (default) or independent replicas")
     ap.add_argument("--gemm-2sm", type=int, default=-1, choices=[-1, 0, 1],
                     help="bf16 forward / dgrad GEMMs on CTA pairs with 2-SM MMAs: -1 library policy, 0 off, 1 on")
     ap.add_argument("--batch", type=int, default=0,
@@ -428,7 +434,14 @@ def main():
         pg = dist
 
     peaks = load_peaks()
-    model = nn.Model(w.dims, w.acts, nn.ACT_RELU, w.dtype, seed=w.seed + rank, batch=w.batch, device=local)
+    dp_mode = world > 1 and args.parallel == "dp"
+    from neural_net_step_gb300.dp import DataParallel, shard_rows
+    lo, hi = shard_rows(w.batch, world, rank) if dp_mode else (0, w.batch)
+    B_local = hi - lo
+    # data parallel: every rank starts from the same parameters (same seed,
+    # then rank 0's broadcast); replicas: one seed per rank
+    model = nn.Model(w.dims, w.acts, nn.ACT_RELU, w.dtype, seed=w.seed + (0 if dp_mode else rank), batch=B_local,
+                     device=local)
     if w.dtype == 0:
         model.set_option(nn.OPT_F32_TENSOR_CORES, 0 if args.f32_ffma else 1)
     model.set_optimizer({"adamw": nn.OPTIM_ADAMW, "adam": nn.OPTIM_ADAM, "sgd": nn.OPTIM_SGD}[args.optim],
@@ -441,15 +454,23 @@ def main():
         "FFMA" if args.f32_ffma or mse else
         "tensor cores, fp32 operands as three bf16 planes (6 products, fp32 accumulate)")
     hyper = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, wd=w.wd)
+    dp = None
+    if dp_mode:
+        dp = DataParallel(model, w.batch)
+        dp.broadcast_params(0)
 
-    # device-resident batch pool larger than L2
+    # device-resident batch pool larger than L2 (data parallel: every rank
+    # draws the same global batches and keeps its own rows)
     x0, y0 = synth.make_batch(w, 0)
     per = x0.numel() * x0.element_size() + (w.batch * w.n_classes if args.loss == "mse" else y0.numel()) * 4
     n_pool = max(4, min(64, math.ceil(1.5 * L2_BYTES / per)))
     n_gen = min(n_pool, 8)
-    gen = [synth.make_batch(w, s + 1000 * rank) for s in range(n_gen)]
+    seed_off = 0 if dp_mode else 1000 * rank
+    gen = [synth.make_batch(w, s + seed_off) for s in range(n_gen)]
     if mse:   # regression targets in place of the labels
-        gen = [(x, synth.make_targets(w, s + 1000 * rank)) for s, (x, _) in enumerate(gen)]
+        gen = [(x, synth.make_targets(w, s + seed_off)) for s, (x, _) in enumerate(gen)]
+    if dp_mode:
+        gen = [(x[lo:hi].contiguous(), y[lo:hi].contiguous()) for x, y in gen]
     xs, ys = [], []
     for i in range(n_pool):
         x, y = gen[i % n_gen]
@@ -460,10 +481,14 @@ def main():
     stream = torch.cuda.current_stream()
     losses = torch.empty(args.steps + args.warmup, dtype=torch.float32, device=dev)
 
-    G = args.graph_steps if args.graph_steps > 0 else w.graph_steps
+    # (data parallel: one exchange per step, so one step per launch)
+    G = 1 if dp_mode else (args.graph_steps if args.graph_steps > 0 else w.graph_steps)
 
     def step(i, loss_slot):
-        model.train_step(xs[i % n_pool], ys[i % n_pool], loss=loss_slot, **hyper)
+        if dp_mode:
+            dp.step(xs[i % n_pool], ys[i % n_pool], loss=loss_slot, **hyper)
+        else:
+            model.train_step(xs[i % n_pool], ys[i % n_pool], loss=loss_slot, **hyper)
 
     def steps(i0, n, loss_slots):
         """Steps i0 .. i0+n-1: one graph launch of n steps (G > 1), else n
@@ -520,7 +545,8 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
     ms_per_step = ms / args.steps
-    value = w.batch * world * args.steps / (ms / 1e3)
+    samples_per_step = w.batch if dp_mode else w.batch * world   # the whole job's rows a step
+    value = samples_per_step * args.steps / (ms / 1e3)
     kernels_per_step = model.kernels_per_step()
     clocks = clk.summary()
 
@@ -531,15 +557,24 @@ def main():
     hx = [gen[i % n_gen][0].pin_memory() for i in range(n_gen)]
     hy = [gen[i % n_gen][1].pin_memory() for i in range(n_gen)]
     hl = torch.empty(args.steps + 3, dtype=torch.float32).pin_memory()
+
+    def host_step(i, slot):
+        if dp_mode:   # this rank's rows up, the data-parallel step, the global loss down
+            xd = hx[i % n_gen].to(dev, non_blocking=True)
+            yd = hy[i % n_gen].to(dev, non_blocking=True)
+            hl[slot].copy_(dp.step(xd, yd, **hyper), non_blocking=True)
+        else:
+            model.train_step_host(hx[i % n_gen], hy[i % n_gen], loss=hl[slot:slot + 1], **hyper)
+
     for i in range(3):
-        model.train_step_host(hx[i % n_gen], hy[i % n_gen], loss=hl[i:i + 1], **hyper)
+        host_step(i, i)
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        model.train_step_host(hx[i % n_gen], hy[i % n_gen], loss=hl[3 + i:4 + i], **hyper)
+        host_step(i, 3 + i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -548,7 +583,7 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e_ms = float(t.item())
     x_bytes = hx[0].numel() * hx[0].element_size()
-    e2e = {"value": w.batch * world * args.steps / (e2e_ms / 1e3), "unit": "samples/s",
+    e2e = {"value": samples_per_step * args.steps / (e2e_ms / 1e3), "unit": "samples/s",
            "h2d_bytes_per_step": int(x_bytes + hy[0].numel() * hy[0].element_size()), "d2h_bytes_per_step": 4}
 
     # ---- per-kernel times (serialised profiling pass, same stream) ----
@@ -573,13 +608,17 @@ def main():
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "samples/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if w.dtype == 0 else "bf16",
+            "scaling": "strong" if dp_mode else "weak", "vs_baseline": None,
+            "dtype": "f32" if w.dtype == 0 else "bf16",
             "data": "synthetic",
             "config": config_of(w, {"l2": f"fresh batch per step from a {n_pool}-batch device pool "
                                           f"({n_pool * per / 2**20:.0f} MiB > 129 MB L2)",
                                     "graph": (f"{G} steps per CUDA-graph launch" if G > 1 else
                                               "one CUDA-graph replay per step"),
-                                    **({"f32_gemm": gemm_mode} if gemm_mode else {})}, args),
+                                    **({"f32_gemm": gemm_mode} if gemm_mode else {}),
+                                    **({"parallelism": f"dp{world}: {B_local} of {w.batch} rows a rank, NCCL sum "
+                                                       f"all-reduce of the fp32 gradient plane each step"}
+                                       if dp_mode else {})}, args),
             "roofline": rf,
             "step_roofline": {"t_roof_ms": round(t_roof_ms, 5), "measured_ms": round(ms_per_step, 5),
                               "frac": round(t_roof_ms / ms_per_step, 4),

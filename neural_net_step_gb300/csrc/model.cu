@@ -185,7 +185,7 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
   std::vector<size_t> need(L.L);
   for (int l = 0; l < L.L; ++l) {
     int s = wgrad_splits(dtype, dims[l + 1], dims[l], batch);
-    size_t b = wgrad_workspace_bytes(dtype, dims[l + 1], dims[l], batch, s);
+    size_t b = wgrad_workspace_bytes_any(dtype, dims[l + 1], dims[l], batch);
     if (L.x3_ok) {
       s = wgrad_splits(DT_F32X3, dims[l + 1], dims[l], batch);
       const size_t b3 = wgrad_workspace_bytes(DT_F32X3, dims[l + 1], dims[l], batch, s);
@@ -559,6 +559,7 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     wg.db = G + L.boff[l];
     wg.ws = L.wws_bytes[l] ? (float*)m->at(L.off_wws[l]) : nullptr; wg.ws_bytes = L.wws_bytes[l];
     wg.err = &ctl->err;
+    wg.cg2 = m->gemm_2sm;
     const bool ce_top = ce_gemm && l == L.L - 1;
     if (ce_top) {
       wg.ce_rowstat = (const float2*)m->at(L.off_cerow); wg.ce_labels = (const int32_t*)y;

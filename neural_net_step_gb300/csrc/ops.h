@@ -94,6 +94,9 @@ struct GemmOp {
 // Number of K splits the wgrad of this shape uses, and the workspace bytes.
 int wgrad_splits(int dtype, int64_t M, int64_t N, int64_t K);
 size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int splits);
+// The largest workspace any kernel choice for this shape uses (one-SM or CTA
+// pairs, whatever GemmOp::cg2 says): a layout sized by it fits either.
+size_t wgrad_workspace_bytes_any(int dtype, int64_t M, int64_t N, int64_t K);
 
 // Plans: fill recs[0..n) and return n (<= 2), or -1 with a message in err.
 int simt_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen);

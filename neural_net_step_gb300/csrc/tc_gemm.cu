@@ -2030,6 +2030,215 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// 2-SM variant of the bf16 weight gradient: dW = dY^T X on CTA pairs with
+// tcgen05.mma.cta_group::2, 256 x 256 tiles (each CTA holds 128 rows of dY^T
+// and 128 columns of X per stage, 32 KB, both MN-major), split over K like
+// the one-SM kernel.  The bias gradient is a second 2-SM MMA of the same A
+// against a ones tile (N = 32, of which one column is read).  One
+// accumulator buffer: the next unit's MMAs wait until both CTAs' epilogues
+// have read it (units are long; their epilogue is a small part of them).
+// ---------------------------------------------------------------------------
+struct W2Cfg {
+  static constexpr int TBM = 2 * BM, TBN = 256;                 // the pair's output tile
+  static constexpr int CHUNK_BYTES = 64 * BK * 2;               // 64 (m or n) x 64 (k) bf16, 8 KB
+  static constexpr int A_BYTES = 2 * CHUNK_BYTES;               // this CTA's 128 rows of dY^T
+  static constexpr int B_BYTES = 2 * CHUNK_BYTES;               // this CTA's 128 columns of X
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;         // 32 KB
+  static constexpr int STAGES = 5;
+  static constexpr int EPI_BYTES = P_EPI_WARPS * 4096;          // one 32 x 32 fp32 box per epilogue warp
+  static constexpr int ONES_BYTES = 16 * 128;                   // 16 rows of 64 bf16 ones (N = 32 over the pair)
+  static constexpr int DB_N = 32;
+  static constexpr int TMEM_COLS = 512;                         // 256 (dW) + 32 (db), one buffer
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + ONES_BYTES + 1024 + 256;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
+tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
+  using C = W2Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t a_base = base;
+  const uint32_t b_base = base + C::STAGES * C::A_BYTES;
+  const uint32_t epi_base = b_base + C::STAGES * C::B_BYTES;
+  const uint32_t ones_base = epi_base + C::EPI_BYTES;
+  const uint32_t bar_base = ones_base + C::ONES_BYTES;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
+  const uint32_t tfull = bar_base + 8u * (2 * C::STAGES);
+  const uint32_t tempty = bar_base + 8u * (2 * C::STAGES + 1);
+  const uint32_t tmem_slot = bar_base + 8u * (2 * C::STAGES + 2);
+  volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: the CTA whose thread issues the MMAs
+  {   // the constant ones tile (bf16 1.0 = 0x3F80)
+    uint32_t* ones = reinterpret_cast<uint32_t*>(base_ptr + (ones_base - base));
+    for (int i = threadIdx.x; i < C::ONES_BYTES / 4; i += blockDim.x) ones[i] = 0x3F803F80u;
+    fence_async_smem();   // visible to the tensor cores (async proxy)
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * P_EPI_WARPS);   // the epilogue warps of both CTAs
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc_cg2(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync_all();   // both CTAs' barriers and ones tiles exist before either's use
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_ptr;
+  pdl_enter();
+  const uint32_t lead_full0 = mapa_cluster(full_bar(0), 0);
+  const uint32_t lead_tempty = mapa_cluster(tempty, 0);
+  const int u0 = (int)(blockIdx.x >> 1), ustep = (int)(gridDim.x >> 1);
+  // work unit u: pair tile u % num_tiles (row tiles of a column tile in
+  // turn), K split u / num_tiles
+  auto unit_coords = [&](int u, int& m0, int& n0, int& split, int& kb0, int& kb1) {
+    const int tile = u % p.num_tiles;
+    split = u / p.num_tiles;
+    m0 = (tile / p.tiles_n) * C::TBM;
+    n0 = (tile % p.tiles_n) * C::TBN;
+    kb0 = split * p.kb_per_split;
+    kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      prefetch_tmap(&p.tmA);
+      prefetch_tmap(&p.tmB);
+      prefetch_tmap(&p.tmOut);
+      int it = 0;
+      bool ok = true;
+      for (int u = u0; u < p.num_units && ok; u += ustep) {
+        int m0, n0, split, kb0, kb1;
+        unit_coords(u, m0, n0, split, kb0, kb1);
+        const int ma = m0 + (int)rank * BM, nb = n0 + (int)rank * (C::TBN / 2);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
+          if (rank == 0) mbar_expect_tx(full_bar(s), 2u * C::STAGE_BYTES);   // both CTAs' bytes
+          const uint32_t fb = lead_full0 + 8u * (uint32_t)s;
+          const int k0 = kb * BK;
+          const uint32_t sa = a_base + s * C::A_BYTES;
+          const uint32_t sb = b_base + s * C::B_BYTES;
+          tma_load_2d_cg2(sa, &p.tmA, ma, k0, fb);
+          tma_load_2d_cg2(sa + C::CHUNK_BYTES, &p.tmA, ma + 64, k0, fb);
+          tma_load_2d_cg2(sb, &p.tmB, nb, k0, fb);
+          tma_load_2d_cg2(sb + C::CHUNK_BYTES, &p.tmB, nb + 64, k0, fb);
+        }
+      }
+      // every stage this CTA filled has been read by the MMAs
+      for (int i = max(0, it - C::STAGES); i < it; ++i)
+        mbar_wait(empty_bar(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u, p.err);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (CTA 0) ----------------
+    if (rank == 0 && lane == 0) {
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int u = u0; u < p.num_units && ok; u += ustep, ++tc) {
+        int m0, n0, split, kb0, kb1;
+        unit_coords(u, m0, n0, split, kb0, kb1);
+        const bool do_db = p.db_out != nullptr && n0 == 0;
+        if (!mbar_wait_cluster(tempty, ((uint32_t)tc & 1u) ^ 1u, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          if (!mbar_wait(full_bar(s), (uint32_t)(it / C::STAGES) & 1u, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = a_base + s * C::A_BYTES;
+          const uint32_t sb = b_base + s * C::B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sdesc(sa + kk * 2048u, (uint32_t)C::CHUNK_BYTES, 1024u);
+            const uint64_t bd = sdesc(sb + kk * 2048u, (uint32_t)C::CHUNK_BYTES, 1024u);
+            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+            mma_bf16_cg2(d, ad, bd, p.idesc, acc);
+            if (do_db) mma_bf16_cg2(d + (uint32_t)C::TBN, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db, acc);
+          }
+          mma_commit_cg2(empty_bar(s));
+        }
+        mma_commit_cg2(tfull);
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..9: this CTA's 128 rows ----------------
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * 4096);
+    uint8_t* srow = base_ptr + (stage0 - base) + lane * 128;
+    int tc = 0;
+    bool ok = true;
+    for (int u = u0; u < p.num_units && ok; u += ustep, ++tc) {
+      int m0, n0, split, kb0, kb1;
+      unit_coords(u, m0, n0, split, kb0, kb1);
+      const int mr = m0 + (int)rank * BM;   // this CTA's rows
+      const bool do_db = p.db_out != nullptr && n0 == 0;
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(tfull, (uint32_t)tc & 1u, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+      const int gm = mr + q * 32 + lane;
+      float dbv = 0.f;
+      if (do_db && half == 0 && kb1 > kb0) dbv = tmem_ld1(trow + (uint32_t)C::TBN);
+      if (do_db && half == 0 && gm < p.M) p.db_out[(int64_t)split * p.M + gm] = dbv;
+      // this warp's 128 columns, 64 at a time, each as two 32 x 32 fp32 stores
+#pragma unroll 1
+      for (int c0 = half * (C::TBN / 2); c0 < (half + 1) * (C::TBN / 2); c0 += 64) {
+        float v[64];
+        tmem_ld32(trow, v, c0);
+        tmem_ld32(trow, v + 32, c0 + 32);
+        if (c0 + 64 >= (half + 1) * (C::TBN / 2)) {
+          // this warp's part of the accumulator is read: hand it back to CTA 0
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lead_tempty);
+        }
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const int gn = n0 + c0 + sub * 32;
+          if (gn >= p.N) continue;   // wholly beyond N: nothing to store
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+#pragma unroll
+          for (int w4 = 0; w4 < 8; ++w4) {
+            const float4 f = make_float4(v[sub * 32 + 4 * w4], v[sub * 32 + 4 * w4 + 1], v[sub * 32 + 4 * w4 + 2],
+                                         v[sub * 32 + 4 * w4 + 3]);
+            *reinterpret_cast<float4*>(srow + ((w4 ^ (lane & 7)) << 4)) = f;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&p.tmOut, stage0, gn, mr + q * 32, split);
+            bulk_commit();
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  // neither CTA leaves while the other may still signal its barriers, or the
+  // MMAs may still read this CTA's shared memory or write its TMEM
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_cg2(tmem, C::TMEM_COLS);
+  }
+}
+
 }  // namespace tc
 
 // ---------------------------------------------------------------------------
@@ -2189,11 +2398,50 @@ static void tc_wgrad_choice(int dtype, int64_t M, int64_t N, int64_t K, int* bn,
   *splits = (int)best_s;
 }
 
+namespace {
+int cg2_max_clusters();   // (defined with the 2-SM plans below)
+}
+
+// K splits of a 2-SM weight gradient: the count that minimises waves x
+// (stages per unit + 6) over the 256 x 256 pair tiles on the pairs that fit
+// at once (the 6 stands for the epilogue a single accumulator buffer does
+// not overlap), with at least 8 stages per unit.
+static int cg2_wgrad_splits(int64_t M, int64_t N, int64_t K) {
+  const int64_t tiles = ceil_div(M, 256) * ceil_div(N, 256);
+  const int64_t kbs = ceil_div(K, tc::BK);
+  const int64_t cl = cg2_max_clusters();
+  int64_t best_s = 1, best_cost = INT64_MAX;
+  for (int64_t s = 1; s <= 256 && (s == 1 || kbs / s >= 8); s *= 2) {
+    const int64_t cost = ceil_div(tiles * s, cl) * (ceil_div(kbs, s) + 6);
+    if (cost < best_cost) { best_cost = cost; best_s = s; }
+  }
+  return (int)best_s;
+}
+
+// The default policy for a bf16 weight gradient on CTA pairs: both output
+// dimensions at least 256 and work units of at least 16 stages.
+static bool cg2_wgrad_default(int dtype, int64_t M, int64_t N, int64_t K) {
+  if (dtype != DT_BF16 || M < 256 || N < 256) return false;
+  return ceil_div(ceil_div(K, tc::BK), cg2_wgrad_splits(M, N, K)) >= 16;
+}
+
 int wgrad_splits(int dtype, int64_t M, int64_t N, int64_t K) {
   if (dtype == DT_F32) return simt_gemm_splits(M, N, K);
+  if (cg2_wgrad_default(dtype, M, N, K)) return cg2_wgrad_splits(M, N, K);
   int bn, s;
   tc_wgrad_choice(dtype, M, N, K, &bn, &s);
   return s;
+}
+
+size_t wgrad_workspace_bytes_any(int dtype, int64_t M, int64_t N, int64_t K) {
+  size_t b = wgrad_workspace_bytes(dtype, M, N, K, wgrad_splits(dtype, M, N, K));
+  if (dtype == DT_BF16) {
+    int bn, s;
+    tc_wgrad_choice(dtype, M, N, K, &bn, &s);
+    b = std::max(b, wgrad_workspace_bytes(dtype, M, N, K, s));
+    if (M >= 256 && N >= 256) b = std::max(b, wgrad_workspace_bytes(dtype, M, N, K, cg2_wgrad_splits(M, N, K)));
+  }
+  return b;
 }
 
 size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int splits) {
@@ -2266,8 +2514,73 @@ const void* tcw_kernel_ptr() {
   return (const void*)tc::tc_wgrad_persistent_kernel<X3, WBN>;
 }
 
+const void* tcw2_kernel_ptr() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute((const void*)tc::tc_wgrad_cg2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         tc::W2Cfg::SMEM_BYTES);
+  });
+  return (const void*)tc::tc_wgrad_cg2_kernel;
+}
+
+// Weight gradient on CTA pairs (2-SM MMAs, 256 x 256 tiles, split K).
+int tc_wgrad_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
+  using G = tc::W2Cfg;
+  tc::WParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_tmap(&p.tmA, op.A, op.M, op.K, op.lda, 64, tc::BK, err, errlen)) return -1;
+  if (!make_tmap(&p.tmB, op.B, op.N, op.K, op.ldb, 64, tc::BK, err, errlen)) return -1;
+  p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
+  p.num_kb = (int)ceil_div(op.K, tc::BK);
+  int splits = op.splits > 0 ? op.splits : cg2_wgrad_splits(op.M, op.N, op.K);
+  if (splits > p.num_kb) splits = p.num_kb;
+  p.kb_per_split = (int)ceil_div(p.num_kb, splits);
+  splits = (int)ceil_div(p.num_kb, p.kb_per_split);
+  p.splits = splits;
+  p.tiles_n = (int)ceil_div(op.N, G::TBN);
+  p.num_tiles = (int)(ceil_div(op.M, G::TBM) * p.tiles_n);
+  p.num_units = p.num_tiles * splits;
+  // D f32, A and B bf16, both MN-major; M = 256 (two CTAs); N = 256, and 32
+  // for the bias gradient against the ones tile (K-major)
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(G::TBN >> 3) << 17) |
+            ((uint32_t)(G::TBM >> 4) << 24);
+  p.idesc_db = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(G::DB_N >> 3) << 17) |
+               ((uint32_t)(G::TBM >> 4) << 24);
+  p.err = op.err;
+  if (splits > 1) {
+    const size_t need = wgrad_workspace_bytes(op.dtype, op.M, op.N, op.K, splits);
+    if (!op.ws || op.ws_bytes < need) {
+      snprintf(err, errlen, "wgrad workspace too small (%zu < %zu)", op.ws_bytes, need);
+      return -1;
+    }
+    if (!make_tmap_f32_3d(&p.tmOut, op.ws, op.N, op.M, splits, op.N, op.M * op.N, err, errlen)) return -1;
+    p.db_out = op.db ? op.ws + (int64_t)splits * op.M * op.N : nullptr;
+  } else {
+    if (!make_tmap_f32_3d(&p.tmOut, op.dW, op.N, op.M, 1, op.ld_dw, op.M * op.ld_dw, err, errlen)) return -1;
+    p.db_out = op.db;
+  }
+  const int clusters = std::min(p.num_units, cg2_max_clusters());
+  LaunchRec& r = recs[0];
+  r.func = tcw2_kernel_ptr();
+  r.smem = G::SMEM_BYTES;
+  r.grid = dim3((unsigned)(2 * clusters));
+  r.block = dim3(tc::P_THREADS);
+  r.early = true;
+  r.name = "tc2_gemm_wgrad";
+  r.set_args(p);
+  if (op.splits_out) *op.splits_out = splits;
+  if (splits > 1 && !op.defer_reduce) {
+    split_reduce_plan(op.ws, splits, op.M, op.N, op.dW, op.ld_dw, op.db, &recs[1]);
+    return 2;
+  }
+  return 1;
+}
+
 // Weight gradient on the persistent split-K kernel (+ the fixed-order reduce).
 int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
+  if (op.dtype == DT_BF16 && !op.ce_rowstat && op.cg2 != 0 && op.M >= 256 && op.N >= 256 &&
+      (op.cg2 > 0 || cg2_wgrad_default(op.dtype, op.M, op.N, op.K)))
+    return tc_wgrad_cg2_plan(op, recs, err, errlen);
   tc::WParams p;
   memset(&p, 0, sizeof(p));
   const bool x3 = op.dtype == DT_F32X3;
