@@ -68,19 +68,37 @@ _GELU_C = 0.044715
 # ---------------------------------------------------------------------------
 # bfloat16 round-to-nearest-even (definition: keep 8 significant bits; the
 # smallest quantum is 2^-133, bf16's subnormal spacing; ties go to the even
-# neighbour).  Mixed precision per MuNet "Configuration" (precision="mixed":
-# inputs rounded to nearest), with bfloat16 in place of fp16.
+# neighbour; beyond the largest bf16 value, infinity).  Mixed precision per
+# MuNet "Configuration" (precision="mixed": inputs rounded to nearest), with
+# bfloat16 in place of fp16.
 # ---------------------------------------------------------------------------
+_BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+
 def rne_bf16(a: np.ndarray) -> np.ndarray:
+    """Round every value to the nearest bfloat16, ties to even.
+
+    From 2^-126 up (bf16's normal range) the quantum is 2^(e-8) for a value
+    in [2^(e-1), 2^e): of the fp64 significand's 52 stored bits the top 7
+    stay, and the 45 below are rounded away on the bit pattern -- add
+    2^44 - 1 plus the lowest kept bit, then clear them (half rounds up only
+    when the kept part is odd; a carry moves to the next binade, as it
+    should).  Below 2^-126 the quantum is the fixed 2^-133: rint(a / q) q.
+    Zeros, infinities and NaNs pass through."""
     a = np.asarray(a, dtype=np.float64)
-    out = np.zeros_like(a)
-    nz = (a != 0) & np.isfinite(a)
-    _, e = np.frexp(a[nz])                      # a = m 2^e, 0.5 <= |m| < 1
-    q = np.ldexp(1.0, np.maximum(e - 8, -133))  # value of one unit in the 8th bit
-    out[nz] = np.rint(a[nz] / q) * q            # rint: round half to even
-    out[~nz] = a[~nz]
-    bf16_max = (2.0 - 2.0 ** -7) * 2.0 ** 127
-    out[np.abs(out) > bf16_max] = np.copysign(np.inf, out[np.abs(out) > bf16_max])
+    out = a.copy()
+    fin = np.isfinite(a)
+    mag = np.abs(a)
+    normal = fin & (mag >= 2.0 ** -126)
+    bits = a[normal].view(np.int64)
+    lsb = (bits >> 45) & 1
+    bits = (bits + ((1 << 44) - 1) + lsb) & ~np.int64((1 << 45) - 1)
+    out[normal] = bits.view(np.float64)
+    tiny = fin & (mag < 2.0 ** -126) & (a != 0)
+    q = 2.0 ** -133
+    out[tiny] = np.rint(a[tiny] / q) * q
+    over = np.abs(out) > _BF16_MAX
+    out[over] = np.copysign(np.inf, out[over])
     return out
 
 

@@ -47,6 +47,27 @@ def test_rne_bf16_matches_torch_cast_on_fp32_values():
 # --------------------------------------------------------------------------
 # Linear layer: brute-force triple loop on a tiny shape
 # --------------------------------------------------------------------------
+def test_rne_bf16_equals_its_definition_on_fp64_values():
+    """The rounding on fp64 inputs (which torch's cast from fp32 cannot
+    give) against the definition written out: quantum q = 2^max(e - 8, -133)
+    for |a| in [2^(e-1), 2^e), a rounded to a multiple of q, half to even;
+    ties at 8 significant bits of both parities, bf16 subnormals, overflow."""
+    rng = np.random.default_rng(21)
+    a = np.concatenate([rng.standard_normal(200000) * np.exp(rng.uniform(-200, 200, 200000)),
+                        rng.standard_normal(50000) * 2.0 ** rng.integers(-140, -120, 50000),
+                        (rng.integers(128, 256, 50000) * 2 + 1) / 2 * 2.0 ** rng.integers(-100, 100, 50000),
+                        (rng.integers(0, 1024, 20000) + 0.5) * 2.0 ** -133,
+                        [(2 - 2.0 ** -8) * 2.0 ** 127, (2 - 2.0 ** -9) * 2.0 ** 127, 2.0 ** -126, 2.0 ** -134]])
+    a = np.concatenate([a, -a])
+    _, e = np.frexp(a)
+    q = np.ldexp(1.0, np.maximum(e - 8, -133))
+    want = np.rint(a / q) * q
+    want[np.abs(want) > (2 - 2.0 ** -7) * 2.0 ** 127] = np.inf * np.sign(want[np.abs(want) > (2 - 2.0 ** -7) * 2.0 ** 127])
+    got = om.rne_bf16(a)
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+
+
 def test_linear_bruteforce():
     X, W, b = _rand((3, 5), 1), _rand((4, 5), 2), _rand(4, 3)
     want = np.zeros((3, 4))
