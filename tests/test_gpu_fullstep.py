@@ -289,6 +289,25 @@ def test_full_size_first_step_layer_by_layer(name):
     assert abs(rep["loss"] - exact) <= 2e-2 * abs(exact), (rep["loss"], exact)
 
 
+def test_ragged_pair_tiles_layer_by_layer():
+    """A ragged bf16 net whose forwards run on CTA pairs by default (so they
+    also store their activations transposed and the weight gradients read
+    them K-major): 2000 rows, widths 2600 and 2520, GELU and ReLU; every
+    kernel of a step checked element by element."""
+    from tests.test_gpu_step import RAGGED_PAIRS as w
+    m = make_model(w, synth.make_params(w))
+    x, y = synth.make_batch(w, 0)
+    xd, yd = x.to(DEV), y.to(DEV)
+    names = [n for n, _ in nn.mlp_profile_step(m.h, xd.data_ptr(), yd.data_ptr(), w.lr, w.beta1, w.beta2, w.eps,
+                                                 w.wd, None, m.stream())]
+    assert names.count("tc2_gemm_fwd") == 2 and names.count("tc2_gemm_wgrad") == 2, names
+    m.close()
+    m = make_model(w, synth.make_params(w))
+    rep, _, _, _ = traced_step_check(w, m, 0)
+    m.close()
+    assert rep["backward"] == "ok"
+
+
 def test_trace_entries_describe_the_step():
     """The trace lists each stored tensor once, written by the launch that the
     profiling pass names for it."""

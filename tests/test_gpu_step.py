@@ -418,11 +418,16 @@ def test_train_step_host_matches_device_inputs(name, batch):
 # --------------------------------------------------------------------------
 RAGGED_2SM = synth.Workload("ragged_2sm", (320, 264, 520, 100), (om.ACT_GELU_TANH, om.ACT_RELU), synth.BF16, 300, 2,
                             1e-3, 0.9, 0.999, 1e-8, 0.01, "normal", 12)
+# enough pair tiles for the 2-SM forwards by default (8 x 11), so they also
+# store their activations transposed and the weight gradients read them
+# K-major: 2000 rows (a 208-row pair tile, a 16-row K tail), 2600 / 2520 columns
+RAGGED_PAIRS = synth.Workload("ragged_pairs", (1024, 2600, 2520, 100), (om.ACT_GELU_TANH, om.ACT_RELU), synth.BF16,
+                              2000, 2, 1e-3, 0.9, 0.999, 1e-8, 0.01, "normal", 13)
 
 
 @pytest.mark.parametrize("w,batch", [(W["cifar_mlp_b8192"], None), (W["lm_block_t16384"], 2048),
-                                     (W["deep_narrow_b65536"], 3000), (RAGGED_2SM, None)],
-                         ids=["cifar_full", "lm_block_2048", "deep_narrow_3000", "ragged"])
+                                     (W["deep_narrow_b65536"], 3000), (RAGGED_2SM, None), (RAGGED_PAIRS, None)],
+                         ids=["cifar_full", "lm_block_2048", "deep_narrow_3000", "ragged", "ragged_pairs"])
 def test_gemm_2sm_equals_one_sm(w, batch):
     """The step with the bf16 forward / dgrad GEMMs on CTA pairs with 2-SM
     MMAs (MLP_OPT_GEMM_2SM 1) and with every GEMM on one SM (0): each output
