@@ -163,7 +163,9 @@ mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
  *     Used where the model allows it: ReLU / no activation, the fused output
  *     layer (MLP_OPT_FUSE_HEAD on and supported), and input / hidden widths
  *     below the output layer that are multiples of 8.  Otherwise, or with 0,
- *     the GEMMs run on the FFMA pipes.  mlp_forward always uses FFMA. */
+ *     the GEMMs run on the FFMA pipes.  mlp_forward follows the same
+ *     choice for the hidden layers (the small output layer takes the joined
+ *     fp32 activation on the FFMA pipes). */
 /*   MLP_OPT_PDL (default 1): in the step's CUDA graph, let each kernel be
  *     scheduled as soon as every block of the kernel before it has started
  *     (programmatic dependent launch); it runs its prologue (barriers, tensor
@@ -308,6 +310,14 @@ mlp_status mlp_apply_update(mlp_t* model, float lr, float beta1, float beta2, fl
  * parameter layout with its padding, every tensor 64-element aligned; the
  * padding holds zeros and sums to zero).  Valid for the model's lifetime. */
 mlp_status mlp_grad_buffer(mlp_t* model, float** g_dev, int64_t* n_floats);
+
+/* mlp_forward with every kernel launched on its own and bracketed by CUDA
+ * events, as mlp_profile_step does for a training step (MuNet
+ * "Configuration": profile=True): device ms and name of kernel i to
+ * ms_out[i] / names_out[i] (nullable) for i < min(*n_out, max_kernels).
+ * Same arguments and results as mlp_forward.  Synchronises the stream. */
+mlp_status mlp_profile_forward(mlp_t* model, const void* x_dev, void* logits_dev, int32_t* argmax_dev, void* stream,
+                               float* ms_out, const char** names_out, int max_kernels, int* n_out);
 
 /* Traced step: one training step (same arguments and effect as
  * mlp_train_step) whose kernels run one after another on `stream`, each

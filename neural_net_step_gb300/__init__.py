@@ -58,6 +58,8 @@ _SIGS = {
     "mlp_kernels_per_step": (_I32, [_P]),
     "mlp_profile_step": (_I32, [_P, _P, _P, _F, _F, _F, _F, _F, _P, _P, _c.POINTER(_F), _c.POINTER(_c.c_char_p),
                                 _I32, _c.POINTER(_I32)]),
+    "mlp_profile_forward": (_I32, [_P, _P, _P, _P, _P, _c.POINTER(_F), _c.POINTER(_c.c_char_p), _I32,
+                                   _c.POINTER(_I32)]),
     "mlp_grad_step": (_I32, [_P, _P, _P, _I64, _P, _P]),
     "mlp_apply_update": (_I32, [_P, _F, _F, _F, _F, _F, _P]),
     "mlp_grad_buffer": (_I32, [_P, _c.POINTER(_P), _c.POINTER(_I64)]),
@@ -233,6 +235,16 @@ def mlp_trace_step(h, x_ptr, y_ptr, lr, beta1, beta2, eps, wd, loss_ptr, trace_p
     _check(lib().mlp_trace_step(h, x_ptr, y_ptr, lr, beta1, beta2, eps, wd, loss_ptr, trace_ptr, trace_bytes, ents,
                                 max_entries, ctypes.byref(n), ctypes.byref(need), stream))
     return [ents[i] for i in range(n.value)], need.value
+
+
+def mlp_profile_forward(h, x_ptr, logits_ptr, argmax_ptr, stream, max_kernels=256):
+    """Returns [(kernel name, device ms), ...] of one serialised mlp_forward."""
+    ms = (_F * max_kernels)()
+    names = (_c.c_char_p * max_kernels)()
+    n = _I32(0)
+    _check(lib().mlp_profile_forward(h, x_ptr, logits_ptr, argmax_ptr, stream, ms, names, max_kernels,
+                                     ctypes.byref(n)))
+    return [(names[i].decode(), ms[i]) for i in range(min(n.value, max_kernels))]
 
 
 def mlp_read_params(h, plane, host_ptr, n) -> int:

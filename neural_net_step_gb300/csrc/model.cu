@@ -967,16 +967,41 @@ mlp_status mlp_set_option(mlp_t* m, int option, int64_t value) {
   return ok();
 }
 
-mlp_status mlp_forward(mlp_t* m, const void* x, void* logits, int32_t* argmax_out, void* stream) {
-  if (!m || !x) return fail(MLP_ERR_ARG, "model or x is NULL");
-  std::lock_guard<std::mutex> lk(m->mu);
-  DevGuard g(m->device);
-  std::vector<LaunchRec> recs;
-  mlp_status st = plan_forward(m, x, recs);
-  if (st != MLP_OK) return st;
+// The launches of mlp_forward.
+static mlp_status plan_inference(mlp_t* m, const void* x, void* logits, int32_t* argmax_out,
+                                 std::vector<LaunchRec>& recs) {
   const Layout& L = m->lay;
   char e_[512] = "";
   LaunchRec r;
+  mlp_status st;
+  if (m->x3()) {
+    // fp32 model on the tensor cores, as in the training step: the hidden
+    // layers on the plane GEMMs, then the last hidden activation joined back
+    // into fp32 (exactly) and the small output layer on the FFMA pipes
+    st = plan_forward(m, x, recs, L.L - 1, true);
+    if (st != MLP_OK) return st;
+    const int l = L.L - 1;
+    float* hf = (float*)m->at(L.off_dy[0]);   // free outside a step; room for fp32 rows of ld_h
+    if (join3_plan(L.B, L.dims[l], m->at(L.off_h[l - 1]), L.ld_h[l - 1], L.B * L.ld_h[l - 1], hf, L.ld_h[l - 1], &r,
+                   e_, sizeof(e_)) < 0)
+      return fail(MLP_ERR_SHAPE, "%s", e_);
+    recs.push_back(r);
+    GemmOp op;
+    op.dtype = MLP_F32; op.kind = GEMM_FWD; op.act = MLP_ACT_NONE;
+    op.M = L.B; op.N = L.dims[L.L]; op.K = L.dims[l];
+    op.A = hf; op.lda = L.ld_h[l - 1]; op.a_kmajor = true;
+    op.B = m->weight(l); op.ldb = L.dims[l]; op.b_kmajor = true;
+    op.bias = m->plane(MLP_PLANE_P) + L.boff[l];
+    op.out = m->at(L.off_z); op.ldo = L.ldz;
+    op.err = &m->ctl()->err;
+    LaunchRec r2[2];
+    const int n = gemm_plan(op, r2, e_, sizeof(e_));
+    if (n < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
+    for (int i = 0; i < n; ++i) recs.push_back(r2[i]);
+  } else {
+    st = plan_forward(m, x, recs);
+    if (st != MLP_OK) return st;
+  }
   if (logits) {
     CopyRowsOp c;
     c.dtype = L.dtype; c.B = L.B; c.C = L.dims[L.L];
@@ -992,8 +1017,48 @@ mlp_status mlp_forward(mlp_t* m, const void* x, void* logits, int32_t* argmax_ou
     if (argmax_plan(a, &r, e_, sizeof(e_)) < 0) return fail(MLP_ERR_SHAPE, "%s", e_);
     recs.push_back(r);
   }
+  return MLP_OK;
+}
+
+mlp_status mlp_forward(mlp_t* m, const void* x, void* logits, int32_t* argmax_out, void* stream) {
+  if (!m || !x) return fail(MLP_ERR_ARG, "model or x is NULL");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_inference(m, x, logits, argmax_out, recs);
+  if (st != MLP_OK) return st;
   st = launch_eager(recs, (cudaStream_t)stream);
   if (st != MLP_OK) return st;
+  return ok();
+}
+
+mlp_status mlp_profile_forward(mlp_t* m, const void* x, void* logits, int32_t* argmax_out, void* stream,
+                               float* ms_out, const char** names_out, int max_kernels, int* n_out) {
+  if (!m || !x || !n_out || (max_kernels > 0 && !ms_out)) return fail(MLP_ERR_ARG, "bad arguments");
+  std::lock_guard<std::mutex> lk(m->mu);
+  DevGuard g(m->device);
+  std::vector<LaunchRec> recs;
+  mlp_status st = plan_inference(m, x, logits, argmax_out, recs);
+  if (st != MLP_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int n = (int)recs.size();
+  std::vector<cudaEvent_t> ev(n + 1, nullptr);
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i <= n && e == cudaSuccess; ++i) e = cudaEventCreate(&ev[i]);
+  for (int i = 0; i < n && e == cudaSuccess; ++i) {
+    if (i == 0) e = cudaEventRecord(ev[0], s);
+    if (e == cudaSuccess) e = launch_rec(recs[i], s);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[i + 1], s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  for (int i = 0; i < n && i < max_kernels && e == cudaSuccess; ++i) {
+    e = cudaEventElapsedTime(&ms_out[i], ev[i], ev[i + 1]);
+    if (names_out) names_out[i] = recs[i].name;
+  }
+  for (auto& v : ev)
+    if (v) cudaEventDestroy(v);
+  if (e != cudaSuccess) return fail(MLP_ERR_CUDA, "profile: %s", cudaGetErrorString(e));
+  *n_out = n;
   return ok();
 }
 

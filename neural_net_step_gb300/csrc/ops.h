@@ -234,6 +234,9 @@ int cast_bf16_plan(int64_t n, const float* p, void* w16, LaunchRec* rec, char* e
 // The three bf16 planes of an fp32 [rows, cols] matrix (row pitch lds):
 // dst[pl * plane + r * ldd + c] for pl = 0 (hi), 1 (mid), 2 (lo), with
 // hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid).
+// fp32 [rows, cols] (ldd) from its three bf16 planes (lds, `plane` apart).
+int join3_plan(int64_t rows, int64_t cols, const void* src, int64_t lds, int64_t plane, float* dst, int64_t ldd,
+               LaunchRec* rec, char* err, size_t errlen);
 int split3_plan(int64_t rows, int64_t cols, const float* src, int64_t lds, void* dst, int64_t ldd, int64_t plane,
                 LaunchRec* rec, char* err, size_t errlen);
 

@@ -1069,6 +1069,44 @@ __global__ void __launch_bounds__(256) split3_kernel(const __grid_constant__ Spl
   }
 }
 
+// The inverse: an fp32 matrix from its three bf16 planes, (hi + mid) + lo in
+// fp32 -- exact, since the three planes hold the value's 24 significant bits
+// in three 8-bit pieces.
+struct Join3Params {
+  const __nv_bfloat16* src; int64_t lds, plane;
+  float* dst; int64_t ldd;
+  int64_t rows, cols;
+};
+
+__global__ void __launch_bounds__(256) join3_kernel(const __grid_constant__ Join3Params q) {
+  pdl_enter();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t n = q.rows * q.cols;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t r = i / q.cols, c = i - r * q.cols;
+    const __nv_bfloat16* s = q.src + r * q.lds + c;
+    q.dst[r * q.ldd + c] = (__bfloat162float(s[0]) + __bfloat162float(s[q.plane])) + __bfloat162float(s[2 * q.plane]);
+  }
+}
+
+int join3_plan(int64_t rows, int64_t cols, const void* src, int64_t lds, int64_t plane, float* dst, int64_t ldd,
+               LaunchRec* rec, char* err, size_t errlen) {
+  if (rows <= 0 || cols <= 0 || lds < cols || ldd < cols || plane < rows * lds || !src || !dst) {
+    snprintf(err, errlen, "join3: bad shape");
+    return -1;
+  }
+  Join3Params q{(const __nv_bfloat16*)src, lds, plane, dst, ldd, rows, cols};
+  int64_t blocks = ceil_div(rows * cols, 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  rec->func = (const void*)join3_kernel;
+  rec->grid = dim3((unsigned)blocks);
+  rec->block = dim3(256);
+  rec->smem = 0;
+  rec->name = "join3";
+  rec->set_args(q);
+  return 1;
+}
+
 int split3_plan(int64_t rows, int64_t cols, const float* src, int64_t lds, void* dst, int64_t ldd, int64_t plane,
                 LaunchRec* rec, char* err, size_t errlen) {
   if (rows <= 0 || cols <= 0 || lds < cols || ldd < cols || plane < rows * ldd || !src || !dst) {

@@ -291,6 +291,37 @@ def test_forward_sampled_rows_full_size(name):
     m.close()
 
 
+def test_fp32_forward_runs_on_the_plane_gemms():
+    """mlp_forward of an fp32 model runs its hidden layers on the tensor
+    cores as three bf16 planes (as the training step does; the small output
+    layer on the FFMA pipes from the exactly joined fp32 activation), and on
+    the FFMA pipes throughout with the option off; logits agree with the
+    oracle within the fp32 bound either way and argmax is the same."""
+    w = W["mnist_mlp_b4096"]
+    params0 = synth.make_params(w)
+    x, _ = synth.make_batch(w, 0)
+    xd = x.to(DEV)
+    out = {}
+    for tc in (1, 0):
+        m = make_model(w, params=params0, f32_tc=tc)
+        logits = torch.empty((w.batch, w.n_classes), dtype=torch.float32, device=DEV)
+        am = torch.empty(w.batch, dtype=torch.int32, device=DEV)
+        prof = nn.mlp_profile_forward(m.h, xd.data_ptr(), logits.data_ptr(), am.data_ptr(), m.stream())
+        out[tc] = ([n for n, _ in prof], P.to64(logits), am.cpu().numpy())
+        m.close()
+    names1, names0 = out[1][0], out[0][0]
+    assert names1[:3] == ["split3", "tc_gemm_fwd", "tc_gemm_fwd"] and "join3" in names1, names1
+    assert not any(n.startswith("tc") for n in names0) and "split3" not in names0, names0
+    p64 = [P.to64(p) for p in params0]
+    z_ref = om.forward(p64, P.to64(x), w.acts, "fp64")["z"]
+    scale = np.max(np.abs(z_ref), axis=1, keepdims=True)
+    for tc in (1, 0):
+        assert np.all(np.abs(out[tc][1] - z_ref) <= 1e-4 * scale)
+        s = np.sort(z_ref, axis=1)
+        clear = (s[:, -1] - s[:, -2]) > 2e-4 * scale[:, 0]
+        assert np.array_equal(out[tc][2][clear], om.argmax_rows(z_ref)[clear])
+
+
 # --------------------------------------------------------------------------
 # Determinism, graph vs eager, error reporting
 # --------------------------------------------------------------------------
