@@ -78,10 +78,6 @@ struct Layout {
   int64_t max_ld = 8;             // row pitch bound of the dY ping-pong buffers
   std::vector<size_t> off_h, off_u;
   std::vector<size_t> off_bits;   // bf16 ReLU layers: the activation's mask as bits, [N / 64][B] words
-  // bf16 hidden layers whose forward runs on CTA pairs: the activation also
-  // stored transposed, [N rows, ld_t], for the next layer's weight gradient
-  std::vector<size_t> off_ht;
-  int64_t ld_t = 0;
   std::vector<int64_t> ld_bits;
   std::vector<int64_t> ld_h;
   size_t off_z = 0, off_dz = 0;
@@ -177,9 +173,6 @@ mlp_status plan_layout(const int64_t* dims, int n_dims, const int* acts, int act
     const bool bits = dtype == MLP_BF16 && L.acts[l] == MLP_ACT_RELU;
     L.ld_bits.push_back(bits ? batch : 0);
     L.off_bits.push_back(bits ? take((dims[l + 1] + 63) / 64 * batch * 8) : 0);
-    L.ld_t = (batch + 7) / 8 * 8;
-    const bool ht = dtype == MLP_BF16 && tc_fwd_uses_cg2(batch, dims[l + 1], dims[l]);
-    L.off_ht.push_back(ht ? take(dims[l + 1] * L.ld_t * 2) : 0);
   }
   L.ldz = (dims[L.L] + 7) / 8 * 8;
   L.off_z = take(batch * L.ldz * es);
@@ -358,8 +351,7 @@ mlp_status add(std::vector<LaunchRec>& out, int n, const LaunchRec* recs) {
 // z buffer).  x3: fp32 model with operands as bf16 planes (the input is
 // split into the arena's xs planes first; hidden outputs are planes).
 mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out, int n_layers = -1,
-                        bool x3 = false, const int32_t* ce_labels = nullptr, const GemmOp* head_fold = nullptr,
-                        std::vector<int>* ht_written = nullptr) {
+                        bool x3 = false, const int32_t* ce_labels = nullptr, const GemmOp* head_fold = nullptr) {
   const Layout& L = m->lay;
   const void* X = x;
   int64_t ldx = L.dims[0], xplane = 0;
@@ -390,10 +382,6 @@ mlp_status plan_forward(const mlp* m, const void* x, std::vector<LaunchRec>& out
       if (op.act == MLP_ACT_GELU_TANH) { op.out_u = m->at(L.off_u[l]); op.ldu = L.ld_h[l]; }
       if (m->relu_bits && L.ld_bits[l] && !x3) {
         op.relu_bits = (uint64_t*)m->at(L.off_bits[l]); op.ld_bits = L.ld_bits[l];
-      }
-      if (ht_written && L.off_ht[l] && !x3) {   // the training step's weight gradient reads h transposed
-        op.out_t = m->at(L.off_ht[l]); op.ld_t = L.ld_t;
-        op.out_t_done = &(*ht_written)[l];
       }
       X = op.out; ldx = L.ld_h[l]; xplane = op.out_plane;
       if (head_fold && l == n_layers - 1) {   // the output layer in this epilogue: it writes dY, not h
@@ -461,9 +449,8 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     hf.bias_corr = ctl->bias_corr; hf.beta1 = hp.b1; hf.beta2 = hp.b2;
     hf.out = m->at(L.off_dy[0]); hf.ldo = L.ld_h[l - 1]; hf.out_plane = dy_plane;
   }
-  std::vector<int> ht_written(L.L, 0);   // forwards that also stored their activation transposed
   mlp_status st = plan_forward(m, x, out, fuse ? L.L - 1 : L.L, x3, ce_gemm ? (const int32_t*)y : nullptr,
-                               head_gemm ? &hf : nullptr, &ht_written);
+                               head_gemm ? &hf : nullptr);
   if (st != MLP_OK) return st;
   const void* dY = m->at(L.off_dz);
   int64_t ldy = L.ldz;
@@ -573,7 +560,6 @@ mlp_status plan_step(const mlp* m, const void* x, const void* y, const Hyper& hp
     wg.ws = L.wws_bytes[l] ? (float*)m->at(L.off_wws[l]) : nullptr; wg.ws_bytes = L.wws_bytes[l];
     wg.err = &ctl->err;
     wg.cg2 = m->gemm_2sm;
-    if (l > 0 && ht_written[l - 1]) { wg.B_t = m->at(L.off_ht[l - 1]); wg.ld_bt = L.ld_t; }
     const bool ce_top = ce_gemm && l == L.L - 1;
     if (ce_top) {
       wg.ce_rowstat = (const float2*)m->at(L.off_cerow); wg.ce_labels = (const int32_t*)y;

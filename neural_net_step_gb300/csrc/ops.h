@@ -69,14 +69,6 @@ struct GemmOp {
   // -1 where there is at least one full wave of pair tiles, 0 never, 1
   // wherever the form allows (N and M of at least 256, no softmax-CE)
   int cg2 = -1;
-  // The activation also stored transposed (GEMM_FWD, bf16, CTA pairs):
-  // out_t [N rows, ld_t >= M] (the batch contiguous), the K-major form in
-  // which the next layer's weight gradient reads it.  The weight gradient
-  // on CTA pairs takes B_t (X transposed, [N rows, ld_bt >= K]) in place of
-  // the MN-major B when given.
-  void* out_t = nullptr; int64_t ld_t = 0;
-  int* out_t_done = nullptr;   // set to 1 when the planned kernel writes out_t
-  const void* B_t = nullptr; int64_t ld_bt = 0;
   float2* ce_stats = nullptr; float* ce_zy = nullptr;
   const float2* ce_rowstat = nullptr;
   const int32_t* ce_labels = nullptr;
@@ -105,8 +97,6 @@ size_t wgrad_workspace_bytes(int dtype, int64_t M, int64_t N, int64_t K, int spl
 // The largest workspace any kernel choice for this shape uses (one-SM or CTA
 // pairs, whatever GemmOp::cg2 says): a layout sized by it fits either.
 size_t wgrad_workspace_bytes_any(int dtype, int64_t M, int64_t N, int64_t K);
-// Whether a bf16 forward / dgrad of this shape runs on CTA pairs by default.
-bool tc_fwd_uses_cg2(int64_t M, int64_t N, int64_t K);
 
 // Plans: fill recs[0..n) and return n (<= 2), or -1 with a message in err.
 int simt_gemm_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen);

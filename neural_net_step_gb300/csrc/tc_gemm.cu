@@ -508,9 +508,6 @@ struct PParams {
   const float* head_W; const float* head_bias; const int32_t* head_labels;
   float* head_ws; int64_t head_loss_off; float head_scale;
   int64_t* step_counter; float* bias_corr; float beta1, beta2;
-  // (2-SM forward) the activation also stored transposed: bf16 [N, ld_t],
-  // box {32 (rows of the batch), 64 (columns)}, no swizzle
-  CUtensorMap tmOutT; int has_out_t;
 };
 
 // Output tile t of a persistent walk: its first row and column.
@@ -1711,22 +1708,6 @@ tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
           tma_store_2d(&p.tmOut, stage0, gn0, m0 + q * 32);
           bulk_commit();
         }
-        if (p.has_out_t) {
-          // the same 32 x 64 chunk transposed (64 rows of 32 batch rows, the
-          // batch contiguous) for the next layer's weight gradient, through
-          // the staging buffer once the store above has read it
-          if (lane == 0) bulk_wait_read0();
-          __syncwarp();
-          uint16_t* st = reinterpret_cast<uint16_t*>(base_ptr + (stage0 - base));
-#pragma unroll
-          for (int j = 0; j < 64; ++j) st[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&p.tmOutT, stage0, m0 + q * 32, gn0);
-            bulk_commit();
-          }
-        }
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -1797,9 +1778,6 @@ struct WParams {
   // (batch), M (classes)]; each stage is formed into dz in shared memory
   // (dz = (exp(z - M_k) invS_k - [m == y_k]) ce_scale) before the MMA
   const float2* ce_rowstat; const int32_t* ce_labels; float ce_scale;
-  // (2-SM kernel) B read K-major from X transposed: box {64 (k), 128 (n)},
-  // 128B swizzle
-  int b_kmajor;
 };
 
 __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
@@ -2154,12 +2132,8 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
           const uint32_t sb = b_base + s * C::B_BYTES;
           tma_load_2d_cg2(sa, &p.tmA, ma, k0, fb);
           tma_load_2d_cg2(sa + C::CHUNK_BYTES, &p.tmA, ma + 64, k0, fb);
-          if (p.b_kmajor) {   // X transposed: one 64 (k) x 128 (n) box
-            tma_load_2d_cg2(sb, &p.tmB, k0, nb, fb);
-          } else {
-            tma_load_2d_cg2(sb, &p.tmB, nb, k0, fb);
-            tma_load_2d_cg2(sb + C::CHUNK_BYTES, &p.tmB, nb + 64, k0, fb);
-          }
+          tma_load_2d_cg2(sb, &p.tmB, nb, k0, fb);
+          tma_load_2d_cg2(sb + C::CHUNK_BYTES, &p.tmB, nb + 64, k0, fb);
         }
       }
       // every stage this CTA filled has been read by the MMAs
@@ -2187,8 +2161,7 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = sdesc(sa + kk * 2048u, (uint32_t)C::CHUNK_BYTES, 1024u);
-            const uint64_t bd = p.b_kmajor ? sdesc(sb + kk * 32u, 16u, 1024u)
-                                           : sdesc(sb + kk * 2048u, (uint32_t)C::CHUNK_BYTES, 1024u);
+            const uint64_t bd = sdesc(sb + kk * 2048u, (uint32_t)C::CHUNK_BYTES, 1024u);
             const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
             mma_bf16_cg2(d, ad, bd, p.idesc, acc);
             if (do_db) mma_bf16_cg2(d + (uint32_t)C::TBN, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db, acc);
@@ -2311,32 +2284,6 @@ bool make_tmap(CUtensorMap* tm, const void* ptr, int64_t inner, int64_t outer, i
   if (r != CUDA_SUCCESS) {
     snprintf(err, errlen, "cuTensorMapEncodeTiled failed (%d) inner=%lld outer=%lld ld=%lld box=%dx%d", (int)r,
              (long long)inner, (long long)outer, (long long)ld, box_inner, box_outer);
-    return false;
-  }
-  return true;
-}
-
-// make_tmap without swizzle (row pitch `ld` elements), for the transposed
-// activation store: box {box_inner, box_outer}, box_inner * 2 bytes a
-// multiple of 16.
-bool make_tmap_plain(CUtensorMap* tm, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int box_inner,
-                     int box_outer, char* err, size_t errlen) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) { snprintf(err, errlen, "cuTensorMapEncodeTiled unavailable"); return false; }
-  if (((uintptr_t)ptr & 15) || ((ld * 2) & 15) || ((box_inner * 2) & 15)) {
-    snprintf(err, errlen, "TMA operand needs a 16-byte aligned base, row pitch and box row (ld=%lld)", (long long)ld);
-    return false;
-  }
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(err, errlen, "cuTensorMapEncodeTiled (plain) failed (%d) inner=%lld outer=%lld ld=%lld", (int)r,
-             (long long)inner, (long long)outer, (long long)ld);
     return false;
   }
   return true;
@@ -2582,13 +2529,7 @@ int tc_wgrad_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errle
   tc::WParams p;
   memset(&p, 0, sizeof(p));
   if (!make_tmap(&p.tmA, op.A, op.M, op.K, op.lda, 64, tc::BK, err, errlen)) return -1;
-  if (op.B_t) {   // X transposed ([N, ld_bt], the batch contiguous): B K-major
-    if (op.ld_bt < op.K) { snprintf(err, errlen, "transposed B: ld_bt >= K"); return -1; }
-    if (!make_tmap(&p.tmB, op.B_t, op.K, op.N, op.ld_bt, tc::BK, G::TBN / 2, err, errlen)) return -1;
-    p.b_kmajor = 1;
-  } else {
-    if (!make_tmap(&p.tmB, op.B, op.N, op.K, op.ldb, 64, tc::BK, err, errlen)) return -1;
-  }
+  if (!make_tmap(&p.tmB, op.B, op.N, op.K, op.ldb, 64, tc::BK, err, errlen)) return -1;
   p.M = (int)op.M; p.N = (int)op.N; p.K = (int)op.K;
   p.num_kb = (int)ceil_div(op.K, tc::BK);
   int splits = op.splits > 0 ? op.splits : cg2_wgrad_splits(op.M, op.N, op.K);
@@ -2601,8 +2542,8 @@ int tc_wgrad_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errle
   p.num_units = p.num_tiles * splits;
   // D f32, A and B bf16, both MN-major; M = 256 (two CTAs); N = 256, and 32
   // for the bias gradient against the ones tile (K-major)
-  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(p.b_kmajor ? 0 : 1) << 16) |
-            ((uint32_t)(G::TBN >> 3) << 17) | ((uint32_t)(G::TBM >> 4) << 24);
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(G::TBN >> 3) << 17) |
+            ((uint32_t)(G::TBM >> 4) << 24);
   p.idesc_db = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(G::DB_N >> 3) << 17) |
                ((uint32_t)(G::TBM >> 4) << 24);
   p.err = op.err;
@@ -2765,12 +2706,6 @@ int tc_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
     }
     p.relu_bits = op.relu_bits; p.ld_bits = op.ld_bits;
   }
-  if (op.out_t && op.kind == GEMM_FWD) {   // the activation also stored transposed, [N, ld_t]
-    if (op.ld_t < op.M) { snprintf(err, errlen, "transposed output: ld_t >= M"); return -1; }
-    if (!make_tmap_plain(&p.tmOutT, op.out_t, op.M, op.N, op.ld_t, 32, 64, err, errlen)) return -1;
-    p.has_out_t = 1;
-    if (op.out_t_done) *op.out_t_done = 1;
-  }
   const int clusters = std::min(p.num_tiles, cg2_max_clusters());
   LaunchRec& r = recs[0];
   r.func = tcg2_kernel_ptr();
@@ -2782,17 +2717,6 @@ int tc_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   r.set_args(p);
   return 1;
 }
-
-}  // namespace
-
-// The 2-SM kernel's default choice for a bf16 forward / dgrad (see
-// tc_persistent_plan).
-bool tc_fwd_uses_cg2(int64_t M, int64_t N, int64_t K) {
-  return M >= 256 && N >= 256 && ceil_div(M, 256) * ceil_div(N, 256) >= cg2_max_clusters() &&
-         ceil_div(K, tc::BK) >= 16;
-}
-
-namespace {
 
 // Forward / dgrad on the persistent kernel (bf16 output through TMA stores).
 int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
@@ -2812,7 +2736,8 @@ int tc_persistent_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errl
   // that a pair pays together outweigh the halved operand traffic: the
   // 512-wide layers of the deep narrow net, K = 512, measured 12 % slower)
   if (!x3 && !ce_f && !ce_a && op.dtype == DT_BF16 && op.cg2 != 0 && op.M >= 256 && op.N >= 256 &&
-      (op.cg2 > 0 || tc_fwd_uses_cg2(op.M, op.N, op.K)))
+      (op.cg2 > 0 || (ceil_div(op.M, 256) * ceil_div(op.N, 256) >= cg2_max_clusters() &&
+                      ceil_div(op.K, tc::BK) >= 16)))
     return tc_cg2_plan(op, recs, err, errlen);
   const int BN = !x3 && op.N > 128 && (ce_f || ceil_div(op.M, tc::BM) * ceil_div(op.N, 256) >= sms) ? 256 : 128;
   tc::PParams p;
