@@ -38,28 +38,40 @@ __host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return ceil_
 // 1 + tanh(a) = 2 s and 1 - tanh(a)^2 = 4 s (1 - s), s = 1 / (1 + e^{-2a}),
 // 1 - s = 1 / (1 + e^{2a}), which keep fp32 relative accuracy in both tails
 // (1 + tanh(a) computed directly cancels to 0 for very negative u).
-// The GEMM epilogues evaluate this for every output, so it uses CUDA's fast
-// intrinsics (__expf, __fdividef: a few ulp in fp32, far below the bf16
-// rounding of the stored result).
-__device__ __forceinline__ void gelu_parts(float u, float& s, float& sm, float& dinner) {
-  const float k0 = 0.7978845608028654f;   // sqrt(2/pi)
-  const float k1 = 0.044715f;
-  const float a = k0 * (u + k1 * u * u * u);
-  // clamp keeps e finite (the results saturate long before |2a| = 80)
-  const float e = __expf(fminf(fmaxf(-2.0f * a, -80.f), 80.f));   // e^{-2a}
-  s = __fdividef(1.0f, 1.0f + e);
-  sm = __fdividef(e, 1.0f + e);
-  dinner = k0 * (1.0f + 3.0f * k1 * u * u);
+// The GEMM epilogues evaluate this for every output, so it is written for
+// few instructions: with c0 = -2 log2(e) sqrt(2/pi) and c1 = 0.044715 c0,
+// e^{-2a} = 2^{u (c0 + c1 u^2)} (a multiply, an FMA, a multiply and the
+// ex2.approx instruction), and 1 / (1 + e) by rcp.approx -- each about 2 ulp
+// in fp32, far below the bf16 rounding of the stored result.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
+__device__ __forceinline__ float rcp_fast(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kGeluC0 = -2.302208198144325f;    // -2 log2(e) sqrt(2/pi)
+constexpr float kGeluC1 = -0.1029432395800235f;   // 0.044715 kGeluC0
+constexpr float kGeluK0 = 0.7978845608028654f;    // sqrt(2/pi)
+constexpr float kGeluK3 = 0.10703222440890038f;   // 3 * 0.044715 sqrt(2/pi)
+// u s with s = 1 / (1 + e^{-2a}).  For very negative u, e^{-2a} overflows
+// to +inf and s to 0: the result is -0, the value bf16 storage gives anyway.
 __device__ __forceinline__ float gelu_tanh(float u) {
-  float s, sm, d;
-  gelu_parts(u, s, sm, d);
-  return u * s;
+  const float e = ex2_fast(u * fmaf(kGeluC1, u * u, kGeluC0));
+  return u * rcp_fast(1.0f + e);
 }
+// s + 2 u s (1 - s) a', a' = sqrt(2/pi) (1 + 3 * 0.044715 u^2), with
+// 1 - s = e s; the exponent is clamped so that e stays finite.
 __device__ __forceinline__ float gelu_tanh_grad(float u) {
-  float s, sm, d;
-  gelu_parts(u, s, sm, d);
-  return s + 2.0f * u * s * sm * d;
+  const float u2 = u * u;
+  const float x = fminf(fmaxf(u * fmaf(kGeluC1, u2, kGeluC0), -126.f), 126.f);
+  const float e = ex2_fast(x);
+  const float s = rcp_fast(1.0f + e);
+  const float d = fmaf(kGeluK3, u2, kGeluK0);
+  return fmaf(2.0f * u * s * (e * s), d, s);
 }
 __device__ __forceinline__ float apply_act(float v, int act) {
   if (act == ACT_RELU) return fmaxf(v, 0.0f);
