@@ -2361,6 +2361,14 @@ int tc_wgrad_splits(int64_t M, int64_t N, int64_t K, int bk = tc::BK, int bn = t
 // least 256 columns: 256-wide tiles, with the split count that minimises
 // waves x (stages per unit + 6), the 6 standing for the epilogue that a
 // single-buffered accumulator does not overlap; else 128-wide tiles.
+// The fixed-order reduce of s split-K partial sums of an M x N fp32 gradient
+// (read s planes, write one: (s + 1) M N 4 bytes at about 6.7 TB/s), in the
+// split cost models' unit: one 64-deep stage of a 128 x 256 tile on one SM
+// (2 128 256 64 flops at about 12.5 TFLOP/s, 0.34 us).
+static int64_t split_reduce_cost(int64_t s, int64_t M, int64_t N) {
+  return s > 1 ? (s + 1) * M * N / 563000 : 0;
+}
+
 static void tc_wgrad_choice(int dtype, int64_t M, int64_t N, int64_t K, int* bn, int* splits) {
   if (dtype == DT_F32X3) {
     // double-buffered accumulators hide most of the epilogue (cost 2); at
@@ -2391,7 +2399,7 @@ static void tc_wgrad_choice(int dtype, int64_t M, int64_t N, int64_t K, int* bn,
   const int64_t kbs = ceil_div(K, tc::BK);
   int64_t best_s = 1, best_cost = INT64_MAX;
   for (int64_t s = 1; s <= 256 && (s == 1 || kbs / s >= 8); s *= 2) {
-    const int64_t cost = ceil_div(tiles * s, kSMs) * (ceil_div(kbs, s) + 6);
+    const int64_t cost = ceil_div(tiles * s, kSMs) * (ceil_div(kbs, s) + 6) + split_reduce_cost(s, M, N);
     if (cost < best_cost) { best_cost = cost; best_s = s; }
   }
   *bn = 256;
@@ -2405,14 +2413,15 @@ int cg2_max_clusters();   // (defined with the 2-SM plans below)
 // K splits of a 2-SM weight gradient: the count that minimises waves x
 // (stages per unit + 6) over the 256 x 256 pair tiles on the pairs that fit
 // at once (the 6 stands for the epilogue a single accumulator buffer does
-// not overlap), with at least 8 stages per unit.
+// not overlap), plus the reduce of the partial sums, with at least 8 stages
+// per unit.
 static int cg2_wgrad_splits(int64_t M, int64_t N, int64_t K) {
   const int64_t tiles = ceil_div(M, 256) * ceil_div(N, 256);
   const int64_t kbs = ceil_div(K, tc::BK);
   const int64_t cl = cg2_max_clusters();
   int64_t best_s = 1, best_cost = INT64_MAX;
   for (int64_t s = 1; s <= 256 && (s == 1 || kbs / s >= 8); s *= 2) {
-    const int64_t cost = ceil_div(tiles * s, cl) * (ceil_div(kbs, s) + 6);
+    const int64_t cost = ceil_div(tiles * s, cl) * (ceil_div(kbs, s) + 6) + split_reduce_cost(s, M, N);
     if (cost < best_cost) { best_cost = cost; best_s = s; }
   }
   return (int)best_s;
