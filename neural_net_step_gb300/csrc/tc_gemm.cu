@@ -1727,9 +1727,12 @@ tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
 // ---------------------------------------------------------------------------
 // Persistent split-K weight gradient: dW[m, n] = sum_k A(m, k) B(k, n), with
 // A = dY^T and B = X both MN-major in memory, fp32 out.  The bias gradient
-// db[m] = sum_k A(m, k) comes from the tensor cores too: for units of the
-// first column tile a second MMA multiplies the same A tile by a constant
-// 16 x 64 tile of ones (N = 16) into spare TMEM columns.
+// db[m] = sum_k A(m, k) is formed in units of the first column tile: for
+// bf16 by the epilogue warps on the CUDA cores from the landed A stages
+// (db_stage_add: they are idle while a long unit's MMAs run, and a second
+// narrow MMA per K step would lengthen those units by about a third); for
+// fp32 planes and the softmax-CE forming by a second MMA of the same A tile
+// against a constant 16 x 64 tile of ones (N = 16) into spare TMEM columns.
 //
 // Work units are (tile, K split) pairs, tile index fastest, so CTAs running
 // at the same time share K ranges in L2.  Each unit's fp32 result goes out
@@ -1791,6 +1794,47 @@ __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
   return __uint_as_float(r);
 }
 
+// Bias gradient of a bf16 weight-gradient unit on the CUDA cores: the column
+// sums of dY over the unit's K rows, taken from the landed A stages (dY^T,
+// MN-major: two 64-column chunks of 64 K rows, 128B-swizzled) by the
+// epilogue warps, which the long units otherwise leave idle.  Epilogue warp
+// w (0..7) owns columns 16 w .. 16 w + 15 as 8 bf16 pairs; lane l takes
+// pair l % 8 and the 16 rows 16 g + ((i + 2 g) mod 16), i = 0..15, g = l / 8,
+// in that order (the row offset puts a warp's four row groups on distinct
+// banks).  A stage's 16 rows are summed first and then added to the running
+// pair; rows beyond K are zero-filled by the copy.
+__device__ __forceinline__ void db_stage_add(const uint8_t* stage_a, int w, int lane, float& acc0, float& acc1) {
+  const int mp = 8 * w + (lane & 7);   // columns 2 mp and 2 mp + 1 of the CTA's 128
+  const int g = lane >> 3;
+  const uint8_t* chunk = stage_a + (mp >> 5) * 8192;
+  const int unit = (mp & 31) >> 2, byte = (mp & 3) * 4;
+  float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int r = 16 * g + ((i + 2 * g) & 15);
+    const uint32_t x = *reinterpret_cast<const uint32_t*>(chunk + r * 128 + ((unit ^ (r & 7)) << 4) + byte);
+    t0 += __uint_as_float(x << 16);
+    t1 += __uint_as_float(x & 0xFFFF0000u);
+  }
+  acc0 += t0;
+  acc1 += t1;
+}
+// The unit's bias gradient for columns m0 + 16 w + 2 (lane % 8) + {0, 1}:
+// the four row groups added as (g0 + g1) + (g2 + g3) and stored by lanes
+// 0..7 (row m0 + c of the [splits][M] output).
+__device__ __forceinline__ void db_finish_store(float acc0, float acc1, int w, int lane, int m0, int M, int split,
+                                                float* db_out) {
+  acc0 += __shfl_xor_sync(0xffffffffu, acc0, 8);
+  acc1 += __shfl_xor_sync(0xffffffffu, acc1, 8);
+  acc0 += __shfl_xor_sync(0xffffffffu, acc0, 16);
+  acc1 += __shfl_xor_sync(0xffffffffu, acc1, 16);
+  const int m = m0 + 16 * w + 2 * lane;
+  if (lane < 8) {
+    if (m < M) db_out[(int64_t)split * M + m] = acc0;
+    if (m + 1 < M) db_out[(int64_t)split * M + m + 1] = acc1;
+  }
+}
+
 template <bool X3, int WBN>
 __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const __grid_constant__ WParams p) {
   using C = WCfg<X3, WBN>;
@@ -1809,9 +1853,14 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
   auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * W_STAGES + b); };
   auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * W_STAGES + 2 + b); };
   auto formed_bar = [&](int s) { return bar_base + 8u * (2 * W_STAGES + 4 + s); };
-  const uint32_t tmem_slot = bar_base + 8u * (3 * W_STAGES + 4);
+  auto dbdone_bar = [&](int s) { return bar_base + 8u * (3 * W_STAGES + 4 + s); };
+  const uint32_t tmem_slot = bar_base + 8u * (4 * W_STAGES + 4);
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
   const bool ce_a = !X3 && p.ce_rowstat != nullptr;
+  // bf16 without the softmax-CE forming: the bias gradient is summed by the
+  // epilogue warps from the landed stages (db_stage_add), and the producer
+  // refills such a stage only after they arrive on its dbdone barrier
+  const bool db_cc = !X3 && !ce_a && p.db_out != nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   {   // the constant ones tile (bf16 1.0 = 0x3F80)
@@ -1824,6 +1873,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(formed_bar(s), P_EPI_WARPS);
+      mbar_init(dbdone_bar(s), P_EPI_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -1854,13 +1904,22 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       prefetch_tmap(&p.tmOut);   // the epilogue's first TMA store need not fetch it
       int it = 0;
       bool ok = true;
+      // bit s: the last fill of stage s feeds a bias-gradient sum / the
+      // parity of that stage's next dbdone completion
+      uint32_t db_prev = 0u, db_ph = 0u;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
+        const bool sum_db = db_cc && n0 == 0;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % W_STAGES;
           const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
+          if ((db_prev >> s) & 1u) {
+            if (!mbar_wait(dbdone_bar(s), (db_ph >> s) & 1u, p.err)) { ok = false; break; }
+            db_ph ^= 1u << s;
+          }
+          db_prev = sum_db ? (db_prev | (1u << s)) : (db_prev & ~(1u << s));
           mbar_expect_tx(full_bar(s), C::STAGE_BYTES);
           const int k0 = kb * C::BKW;
           const uint32_t sa = a_base + s * C::A_BYTES;
@@ -1893,7 +1952,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++tc) {
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
-        const bool do_db = p.db_out != nullptr && n0 == 0;
+        const bool do_db = p.db_out != nullptr && n0 == 0 && !db_cc;   // on the tensor cores
         const int buf = C::NBUF == 2 ? (tc & 1) : 0;
         const uint32_t tph = C::NBUF == 2 ? (((uint32_t)tc >> 1) & 1u) : ((uint32_t)tc & 1u);
         if (!mbar_wait(tempty_bar(buf), tph ^ 1u, p.err)) break;
@@ -1975,8 +2034,22 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
           if (lane == 0) mbar_arrive(formed_bar(s));
         }
         if (!ok) break;
+      } else if (db_cc && n0 == 0) {
+        float a0 = 0.f, a1 = 0.f;
+        for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
+          const int s = it % W_STAGES;
+          ok = __all_sync(0xffffffffu, mbar_wait(full_bar(s), (uint32_t)(it / W_STAGES) & 1u, p.err));
+          if (!ok) break;
+          db_stage_add(base_ptr + (a_base - base) + s * C::A_BYTES, warp - 2, lane, a0, a1);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dbdone_bar(s));
+        }
+        if (!ok) break;
+        db_finish_store(a0, a1, warp - 2, lane, m0, p.M, split, p.db_out);
+      } else {
+        it += kb1 - kb0;
       }
-      const bool do_db = p.db_out != nullptr && n0 == 0;
+      const bool do_db = p.db_out != nullptr && n0 == 0 && !db_cc;   // read from TMEM
       const int buf = C::NBUF == 2 ? (tc & 1) : 0;
       const uint32_t tph = C::NBUF == 2 ? (((uint32_t)tc >> 1) & 1u) : ((uint32_t)tc & 1u);
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), tph, p.err));
@@ -2035,10 +2108,14 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
 // 2-SM variant of the bf16 weight gradient: dW = dY^T X on CTA pairs with
 // tcgen05.mma.cta_group::2, 256 x 256 tiles (each CTA holds 128 rows of dY^T
 // and 128 columns of X per stage, 32 KB, both MN-major), split over K like
-// the one-SM kernel.  The bias gradient is a second 2-SM MMA of the same A
-// against a ones tile (N = 32, of which one column is read).  One
-// accumulator buffer: the next unit's MMAs wait until both CTAs' epilogues
-// have read it (units are long; their epilogue is a small part of them).
+// the one-SM kernel.  The bias gradient is summed on the CUDA cores by each
+// CTA's epilogue warps from its own landed A stages (db_stage_add, the same
+// order as the one-SM kernel).  They learn that a stage has landed from the
+// MMA's completion on the local "empty" barrier (the "full" barriers live in
+// CTA 0), and the producer refills such a stage only after their arrival on
+// its dbdone barrier.  One accumulator buffer: the next unit's MMAs wait
+// until both CTAs' epilogues have read it into registers (units are long;
+// that read is a small part of them).
 // ---------------------------------------------------------------------------
 struct W2Cfg {
   static constexpr int TBM = 2 * BM, TBN = 256;                 // the pair's output tile
@@ -2046,13 +2123,12 @@ struct W2Cfg {
   static constexpr int A_BYTES = 2 * CHUNK_BYTES;               // this CTA's 128 rows of dY^T
   static constexpr int B_BYTES = 2 * CHUNK_BYTES;               // this CTA's 128 columns of X
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;         // 32 KB
-  static constexpr int STAGES = 5;
+  static constexpr int STAGES = 6;
   static constexpr int EPI_BYTES = P_EPI_WARPS * 4096;          // one 32 x 32 fp32 box per epilogue warp
-  static constexpr int ONES_BYTES = 16 * 128;                   // 16 rows of 64 bf16 ones (N = 32 over the pair)
-  static constexpr int DB_N = 32;
-  static constexpr int TMEM_COLS = 512;                         // 256 (dW) + 32 (db), one buffer
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + ONES_BYTES + 1024 + 256;
+  static constexpr int TMEM_COLS = 256;                         // the dW accumulator, one buffer
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(8 * (3 * STAGES + 3) <= 256, "barrier slots");
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
@@ -2065,25 +2141,21 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
   const uint32_t a_base = base;
   const uint32_t b_base = base + C::STAGES * C::A_BYTES;
   const uint32_t epi_base = b_base + C::STAGES * C::B_BYTES;
-  const uint32_t ones_base = epi_base + C::EPI_BYTES;
-  const uint32_t bar_base = ones_base + C::ONES_BYTES;
+  const uint32_t bar_base = epi_base + C::EPI_BYTES;
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
-  const uint32_t tfull = bar_base + 8u * (2 * C::STAGES);
-  const uint32_t tempty = bar_base + 8u * (2 * C::STAGES + 1);
-  const uint32_t tmem_slot = bar_base + 8u * (2 * C::STAGES + 2);
+  auto dbdone_bar = [&](int s) { return bar_base + 8u * (2 * C::STAGES + s); };
+  const uint32_t tfull = bar_base + 8u * (3 * C::STAGES);
+  const uint32_t tempty = bar_base + 8u * (3 * C::STAGES + 1);
+  const uint32_t tmem_slot = bar_base + 8u * (3 * C::STAGES + 2);
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();   // 0: the CTA whose thread issues the MMAs
-  {   // the constant ones tile (bf16 1.0 = 0x3F80)
-    uint32_t* ones = reinterpret_cast<uint32_t*>(base_ptr + (ones_base - base));
-    for (int i = threadIdx.x; i < C::ONES_BYTES / 4; i += blockDim.x) ones[i] = 0x3F803F80u;
-    fence_async_smem();   // visible to the tensor cores (async proxy)
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(dbdone_bar(s), P_EPI_WARPS);
     }
     mbar_init(tfull, 1);
     mbar_init(tempty, 2 * P_EPI_WARPS);   // the epilogue warps of both CTAs
@@ -2091,7 +2163,7 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
   }
   if (warp == 1) tmem_alloc_cg2(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
-  cluster_sync_all();   // both CTAs' barriers and ones tiles exist before either's use
+  cluster_sync_all();   // both CTAs' barriers exist before either's use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
   pdl_enter();
@@ -2117,14 +2189,23 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
       prefetch_tmap(&p.tmOut);
       int it = 0;
       bool ok = true;
+      // bit s: the last fill of stage s feeds a bias-gradient sum / the
+      // parity of that stage's next dbdone completion
+      uint32_t db_prev = 0u, db_ph = 0u;
       for (int u = u0; u < p.num_units && ok; u += ustep) {
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
+        const bool sum_db = p.db_out != nullptr && n0 == 0;
         const int ma = m0 + (int)rank * BM, nb = n0 + (int)rank * (C::TBN / 2);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err)) { ok = false; break; }
+          if ((db_prev >> s) & 1u) {
+            if (!mbar_wait(dbdone_bar(s), (db_ph >> s) & 1u, p.err)) { ok = false; break; }
+            db_ph ^= 1u << s;
+          }
+          db_prev = sum_db ? (db_prev | (1u << s)) : (db_prev & ~(1u << s));
           if (rank == 0) mbar_expect_tx(full_bar(s), 2u * C::STAGE_BYTES);   // both CTAs' bytes
           const uint32_t fb = lead_full0 + 8u * (uint32_t)s;
           const int k0 = kb * BK;
@@ -2148,7 +2229,6 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
       for (int u = u0; u < p.num_units && ok; u += ustep, ++tc) {
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
-        const bool do_db = p.db_out != nullptr && n0 == 0;
         if (!mbar_wait_cluster(tempty, ((uint32_t)tc & 1u) ^ 1u, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem;
@@ -2162,9 +2242,7 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = sdesc(sa + kk * 2048u, (uint32_t)C::CHUNK_BYTES, 1024u);
             const uint64_t bd = sdesc(sb + kk * 2048u, (uint32_t)C::CHUNK_BYTES, 1024u);
-            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-            mma_bf16_cg2(d, ad, bd, p.idesc, acc);
-            if (do_db) mma_bf16_cg2(d + (uint32_t)C::TBN, ad, sdesc(ones_base + kk * 32u, 16u, 1024u), p.idesc_db, acc);
+            mma_bf16_cg2(d, ad, bd, p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_cg2(empty_bar(s));
         }
@@ -2177,51 +2255,59 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
     const int half = (warp - 2) >> 2;
     const uint32_t stage0 = epi_base + (uint32_t)((warp - 2) * 4096);
     uint8_t* srow = base_ptr + (stage0 - base) + lane * 128;
-    int tc = 0;
+    int tc = 0, it = 0;
     bool ok = true;
     for (int u = u0; u < p.num_units && ok; u += ustep, ++tc) {
       int m0, n0, split, kb0, kb1;
       unit_coords(u, m0, n0, split, kb0, kb1);
       const int mr = m0 + (int)rank * BM;   // this CTA's rows
-      const bool do_db = p.db_out != nullptr && n0 == 0;
+      if (p.db_out != nullptr && n0 == 0) {
+        // the bias gradient of this CTA's rows, stage by stage as the MMAs
+        // finish with them (the stage's bytes have landed by then)
+        float a0 = 0.f, a1 = 0.f;
+        for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(s), (uint32_t)(it / C::STAGES) & 1u, p.err));
+          if (!ok) break;
+          db_stage_add(base_ptr + (a_base - base) + s * C::A_BYTES, warp - 2, lane, a0, a1);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dbdone_bar(s));
+        }
+        if (!ok) break;
+        db_finish_store(a0, a1, warp - 2, lane, mr, p.M, split, p.db_out);
+      } else {
+        it += kb1 - kb0;
+      }
       ok = __all_sync(0xffffffffu, mbar_wait_cluster(tfull, (uint32_t)tc & 1u, p.err));
       if (!ok) break;
       tc_fence_after();
+      // this warp's 128 columns into registers, the accumulator handed back
+      // to CTA 0, then four 32 x 32 fp32 stores
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-      const int gm = mr + q * 32 + lane;
-      float dbv = 0.f;
-      if (do_db && half == 0 && kb1 > kb0) dbv = tmem_ld1(trow + (uint32_t)C::TBN);
-      if (do_db && half == 0 && gm < p.M) p.db_out[(int64_t)split * p.M + gm] = dbv;
-      // this warp's 128 columns, 64 at a time, each as two 32 x 32 fp32 stores
-#pragma unroll 1
-      for (int c0 = half * (C::TBN / 2); c0 < (half + 1) * (C::TBN / 2); c0 += 64) {
-        float v[64];
-        tmem_ld32(trow, v, c0);
-        tmem_ld32(trow, v + 32, c0 + 32);
-        if (c0 + 64 >= (half + 1) * (C::TBN / 2)) {
-          // this warp's part of the accumulator is read: hand it back to CTA 0
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(lead_tempty);
+      const int c0 = half * (C::TBN / 2);
+      float v[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(trow, v + 32 * c, c0 + 32 * c);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lead_tempty);
+#pragma unroll
+      for (int sub = 0; sub < 4; ++sub) {
+        const int gn = n0 + c0 + sub * 32;
+        if (gn >= p.N) continue;   // wholly beyond N: nothing to store
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+#pragma unroll
+        for (int w4 = 0; w4 < 8; ++w4) {
+          const float4 f = make_float4(v[sub * 32 + 4 * w4], v[sub * 32 + 4 * w4 + 1], v[sub * 32 + 4 * w4 + 2],
+                                       v[sub * 32 + 4 * w4 + 3]);
+          *reinterpret_cast<float4*>(srow + ((w4 ^ (lane & 7)) << 4)) = f;
         }
-#pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-          const int gn = n0 + c0 + sub * 32;
-          if (gn >= p.N) continue;   // wholly beyond N: nothing to store
-          if (lane == 0) bulk_wait_read0();
-          __syncwarp();
-#pragma unroll
-          for (int w4 = 0; w4 < 8; ++w4) {
-            const float4 f = make_float4(v[sub * 32 + 4 * w4], v[sub * 32 + 4 * w4 + 1], v[sub * 32 + 4 * w4 + 2],
-                                         v[sub * 32 + 4 * w4 + 3]);
-            *reinterpret_cast<float4*>(srow + ((w4 ^ (lane & 7)) << 4)) = f;
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&p.tmOut, stage0, gn, mr + q * 32, split);
-            bulk_commit();
-          }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&p.tmOut, stage0, gn, mr + q * 32, split);
+          bulk_commit();
         }
       }
     }
@@ -2549,12 +2635,11 @@ int tc_wgrad_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errle
   p.tiles_n = (int)ceil_div(op.N, G::TBN);
   p.num_tiles = (int)(ceil_div(op.M, G::TBM) * p.tiles_n);
   p.num_units = p.num_tiles * splits;
-  // D f32, A and B bf16, both MN-major; M = 256 (two CTAs); N = 256, and 32
-  // for the bias gradient against the ones tile (K-major)
+  // D f32, A and B bf16, both MN-major; M = 256 (two CTAs), N = 256 (the
+  // bias gradient is summed on the CUDA cores)
   p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(G::TBN >> 3) << 17) |
             ((uint32_t)(G::TBM >> 4) << 24);
-  p.idesc_db = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(G::DB_N >> 3) << 17) |
-               ((uint32_t)(G::TBM >> 4) << 24);
+  p.idesc_db = 0u;
   p.err = op.err;
   if (splits > 1) {
     const size_t need = wgrad_workspace_bytes(op.dtype, op.M, op.N, op.K, splits);
