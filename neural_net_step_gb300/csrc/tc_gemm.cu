@@ -476,6 +476,8 @@ struct PParams {
   CUtensorMap tmA;
   CUtensorMap tmB;
   CUtensorMap tmOut;     // bf16 [M rows, N cols] (2-D, or 3-D with 3 planes), box {64, 32}, 128B swizzle
+  CUtensorMap tmU;       // the GELU pre-activation out_u like tmOut (CTA pairs, when u_tma)
+  int u_tma;
   int M, N, K;
   int num_kb, tiles_n, num_tiles;
   // tile order: m_fast = 1 walks the row tiles of a column tile first (CTAs
@@ -1481,6 +1483,10 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
+// FWD: the forward epilogue (bias, activation, pre-activation or ReLU bits),
+// else the dgrad's (activation derivative); separate instances so that each
+// epilogue has the registers to itself.
+template <bool FWD>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
   using C = G2Cfg;
@@ -1610,7 +1616,7 @@ tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
         // before the accumulator wait
         float bias0 = 0.f, bias1 = 0.f;
         uint32_t mask0 = 0u, mask1 = 0u;
-        if (p.kind == GEMM_FWD) {
+        if (FWD) {
           if (gn0 + lane < p.N) bias0 = __ldg(p.bias + gn0 + lane);
           if (gn0 + 32 + lane < p.N) bias1 = __ldg(p.bias + gn0 + 32 + lane);
         } else if (p.act == ACT_RELU && row_ok && p.relu_bits && gn0 < p.N) {
@@ -1633,19 +1639,34 @@ tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
         }
         float v[64];
         tmem_ld64(trow + (uint32_t)c0, v);
-        if (c0 + 64 >= (half + 1) * (C::TBN / 2)) {
+        const bool last = c0 + 64 >= (half + 1) * (C::TBN / 2);
+        if (last) {
           // this warp's part of the accumulator is drained: hand it back to CTA 0
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(lead_tempty0 + 8u * (uint32_t)buf);
         }
-        if (p.kind == GEMM_FWD) {
+        if (FWD) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             v[j] += __shfl_sync(0xffffffffu, bias0, j);
             v[32 + j] += __shfl_sync(0xffffffffu, bias1, j);
           }
-          if (p.out_u && row_ok) {
+          if (p.out_u && p.u_tma) {
+            // the pre-activation through the staging buffer and a TMA store
+            // (it clips the ragged edges), like the activation below
+            if (gn0 < p.N) {
+              if (lane == 0) bulk_wait_read0();
+              __syncwarp();
+              stage_plane(srow, lane, v, false);
+              fence_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&p.tmU, stage0, gn0, m0 + q * 32);
+                bulk_commit();
+              }
+            }
+          } else if (p.out_u && row_ok) {
             __nv_bfloat16* du = p.out_u + (int64_t)gm * p.ldu + gn0;
             if (gn0 + 64 <= p.N) {
 #pragma unroll
@@ -1727,7 +1748,7 @@ tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
 // ---------------------------------------------------------------------------
 // Persistent split-K weight gradient: dW[m, n] = sum_k A(m, k) B(k, n), with
 // A = dY^T and B = X both MN-major in memory, fp32 out.  The bias gradient
-// db[m] = sum_k A(m, k) is formed in units of the first column tile: for
+// db[m] = sum_k A(m, k) is formed in one unit per row tile: for
 // bf16 by the epilogue warps on the CUDA cores from the landed A stages
 // (db_stage_add: they are idle while a long unit's MMAs run, and a second
 // narrow MMA per K step would lengthen those units by about a third); for
@@ -1895,6 +1916,9 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
     kb0 = split * p.kb_per_split;
     kb1 = min(p.num_kb, kb0 + p.kb_per_split);
   };
+  // the units that form the bias gradient: row tile i in column tile
+  // i mod tiles_n (spread over the CTAs rather than all in column tile 0)
+  auto db_unit = [&](int m0, int n0) { return p.db_out != nullptr && n0 / WBN == (m0 / BM) % p.tiles_n; };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -1910,7 +1934,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
-        const bool sum_db = db_cc && n0 == 0;
+        const bool sum_db = db_cc && db_unit(m0, n0);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % W_STAGES;
           const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
@@ -1952,7 +1976,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++tc) {
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
-        const bool do_db = p.db_out != nullptr && n0 == 0 && !db_cc;   // on the tensor cores
+        const bool do_db = db_unit(m0, n0) && !db_cc;   // on the tensor cores
         const int buf = C::NBUF == 2 ? (tc & 1) : 0;
         const uint32_t tph = C::NBUF == 2 ? (((uint32_t)tc >> 1) & 1u) : ((uint32_t)tc & 1u);
         if (!mbar_wait(tempty_bar(buf), tph ^ 1u, p.err)) break;
@@ -2034,7 +2058,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
           if (lane == 0) mbar_arrive(formed_bar(s));
         }
         if (!ok) break;
-      } else if (db_cc && n0 == 0) {
+      } else if (db_cc && db_unit(m0, n0)) {
         float a0 = 0.f, a1 = 0.f;
         for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
           const int s = it % W_STAGES;
@@ -2049,7 +2073,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       } else {
         it += kb1 - kb0;
       }
-      const bool do_db = p.db_out != nullptr && n0 == 0 && !db_cc;   // read from TMEM
+      const bool do_db = db_unit(m0, n0) && !db_cc;   // read from TMEM
       const int buf = C::NBUF == 2 ? (tc & 1) : 0;
       const uint32_t tph = C::NBUF == 2 ? (((uint32_t)tc >> 1) & 1u) : ((uint32_t)tc & 1u);
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), tph, p.err));
@@ -2110,12 +2134,17 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
 // and 128 columns of X per stage, 32 KB, both MN-major), split over K like
 // the one-SM kernel.  The bias gradient is summed on the CUDA cores by each
 // CTA's epilogue warps from its own landed A stages (db_stage_add, the same
-// order as the one-SM kernel).  They learn that a stage has landed from the
-// MMA's completion on the local "empty" barrier (the "full" barriers live in
-// CTA 0), and the producer refills such a stage only after their arrival on
-// its dbdone barrier.  One accumulator buffer: the next unit's MMAs wait
-// until both CTAs' epilogues have read it into registers (units are long;
-// that read is a small part of them).
+// order as the one-SM kernel), in the units that db_unit() picks (one per
+// row tile, spread over the column tiles so that every pair carries its
+// share).  The "full" barriers live in CTA 0, so the summing warps take a
+// stage once the MMAs are done with it (the local "empty" barrier), and the
+// producer refills it only after they arrive on its dbdone barrier.  (A
+// landed-stage signal passed on from CTA 0 measured no faster: the second
+// read of the A stage from shared memory, not the wait, is what the bias
+// gradient costs, about a third of a unit; hence the spread.)  One
+// accumulator buffer:
+// the next unit's MMAs wait until both CTAs' epilogues have read it into
+// registers (units are long; that read is a small part of them).
 // ---------------------------------------------------------------------------
 struct W2Cfg {
   static constexpr int TBM = 2 * BM, TBN = 256;                 // the pair's output tile
@@ -2180,6 +2209,10 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
     kb0 = split * p.kb_per_split;
     kb1 = min(p.num_kb, kb0 + p.kb_per_split);
   };
+  // the units that sum the bias gradient: row tile i in column tile i mod tiles_n
+  auto db_unit = [&](int m0, int n0) {
+    return p.db_out != nullptr && n0 / C::TBN == (m0 / C::TBM) % p.tiles_n;
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
@@ -2195,7 +2228,7 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
       for (int u = u0; u < p.num_units && ok; u += ustep) {
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
-        const bool sum_db = p.db_out != nullptr && n0 == 0;
+        const bool sum_db = db_unit(m0, n0);
         const int ma = m0 + (int)rank * BM, nb = n0 + (int)rank * (C::TBN / 2);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES;
@@ -2261,7 +2294,7 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
       int m0, n0, split, kb0, kb1;
       unit_coords(u, m0, n0, split, kb0, kb1);
       const int mr = m0 + (int)rank * BM;   // this CTA's rows
-      if (p.db_out != nullptr && n0 == 0) {
+      if (db_unit(m0, n0)) {
         // the bias gradient of this CTA's rows, stage by stage as the MMAs
         // finish with them (the stage's bytes have landed by then)
         float a0 = 0.f, a1 = 0.f;
@@ -2732,13 +2765,14 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   return 1;
 }
 
+template <bool FWD>
 const void* tcg2_kernel_ptr() {
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute((const void*)tc::tc_gemm_cg2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute((const void*)tc::tc_gemm_cg2_kernel<FWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          tc::G2Cfg::SMEM_BYTES);
   });
-  return (const void*)tc::tc_gemm_cg2_kernel;
+  return (const void*)tc::tc_gemm_cg2_kernel<FWD>;
 }
 
 // CTA pairs of the 2-SM kernel that fit on the device at once (a GPC may
@@ -2757,7 +2791,7 @@ int cg2_max_clusters() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, tcg2_kernel_ptr(), &cfg) != cudaSuccess || c < 1) {
+    if (cudaOccupancyMaxActiveClusters(&c, tcg2_kernel_ptr<true>(), &cfg) != cudaSuccess || c < 1) {
       cudaGetLastError();
       c = sms / 2;
     }
@@ -2791,6 +2825,12 @@ int tc_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
             ((uint32_t)(G::TBM >> 4) << 24);
   p.bias = op.bias;
   p.out_u = (__nv_bfloat16*)op.out_u; p.ldu = op.ldu;
+  // the pre-activation through TMA stores where its layout allows a tensor
+  // map (16-byte aligned base and pitch), else plain stores
+  if (op.out_u && ((uintptr_t)op.out_u & 15) == 0 && ((op.ldu * 2) & 15) == 0) {
+    char e2[256];
+    p.u_tma = make_tmap(&p.tmU, op.out_u, op.N, op.M, op.ldu, 64, 32, e2, sizeof(e2)) ? 1 : 0;
+  }
   p.aux = (const __nv_bfloat16*)op.aux; p.ld_aux = op.ld_aux;
   p.err = op.err;
   if (op.relu_bits && op.act == ACT_RELU) {
@@ -2802,7 +2842,7 @@ int tc_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   }
   const int clusters = std::min(p.num_tiles, cg2_max_clusters());
   LaunchRec& r = recs[0];
-  r.func = tcg2_kernel_ptr();
+  r.func = op.kind == GEMM_FWD ? tcg2_kernel_ptr<true>() : tcg2_kernel_ptr<false>();
   r.smem = G::SMEM_BYTES;
   r.grid = dim3((unsigned)(2 * clusters));
   r.block = dim3(tc::P_THREADS);
