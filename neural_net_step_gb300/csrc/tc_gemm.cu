@@ -1748,12 +1748,12 @@ tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
 // ---------------------------------------------------------------------------
 // Persistent split-K weight gradient: dW[m, n] = sum_k A(m, k) B(k, n), with
 // A = dY^T and B = X both MN-major in memory, fp32 out.  The bias gradient
-// db[m] = sum_k A(m, k) is formed in one unit per row tile: for
-// bf16 by the epilogue warps on the CUDA cores from the landed A stages
-// (db_stage_add: they are idle while a long unit's MMAs run, and a second
-// narrow MMA per K step would lengthen those units by about a third); for
-// fp32 planes and the softmax-CE forming by a second MMA of the same A tile
-// against a constant 16 x 64 tile of ones (N = 16) into spare TMEM columns.
+// db[m] = sum_k A(m, k): for bf16 by the epilogue warps on the CUDA cores
+// from the landed A stages (db_stage_add: they are idle while a long unit's
+// MMAs run, and a second narrow MMA per K step would lengthen those units by
+// about a third), in the units db_part picks; for fp32 planes and the softmax-CE forming by a second MMA of
+// the same A tile against a constant 16 x 64 tile of ones (N = 16) into
+// spare TMEM columns, in one unit per row tile.
 //
 // Work units are (tile, K split) pairs, tile index fastest, so CTAs running
 // at the same time share K ranges in L2.  Each unit's fp32 result goes out
@@ -1795,6 +1795,7 @@ struct WParams {
   int M, N, K;
   int num_kb, kb_per_split, splits;   // K stages (32 or 64 rows each), split into units
   int tiles_n, num_tiles, num_units;
+  int db_share;          // bf16 bias gradient: see db_part
   uint32_t idesc, idesc_db;
   float* db_out;         // [splits][M] (nullable: no bias gradient)
   uint32_t* err;
@@ -1854,6 +1855,24 @@ __device__ __forceinline__ void db_finish_store(float acc0, float acc1, int w, i
     if (m < M) db_out[(int64_t)split * M + m] = acc0;
     if (m + 1 < M) db_out[(int64_t)split * M + m + 1] = acc1;
   }
+}
+// Which units sum the bias gradient of a row tile (each epilogue warp's
+// sums are the same whichever unit forms them, so this changes no result).
+// share = 0 (several waves of units): the unit of column tile
+// ti_m mod tiles_n, all eight warps (part 0), spreading such units over
+// the CTAs.  share = 1 (one wave: the slowest unit sets the time): the
+// rows are shared among the row tile's column tiles, P = min(tiles_n, 8)
+// parts; the unit of column tile ti_n takes part (ti_n + ti_m) mod tiles_n
+// (none if that is >= P), part j being the rows of the warps w with
+// w P / 8 == j.  Returns the part, or -1.
+__device__ __forceinline__ int db_part(const float* db_out, int ti_m, int ti_n, int tiles_n, int share) {
+  if (db_out == nullptr) return -1;
+  if (!share) return ti_n == ti_m % tiles_n ? 0 : -1;
+  const int j = (ti_n + ti_m) % tiles_n;
+  return j < min(tiles_n, 8) ? j : -1;
+}
+__device__ __forceinline__ bool db_warp_in_part(int w, int part, int tiles_n, int share) {
+  return !share || w * min(tiles_n, 8) / 8 == part;
 }
 
 template <bool X3, int WBN>
@@ -1916,8 +1935,8 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
     kb0 = split * p.kb_per_split;
     kb1 = min(p.num_kb, kb0 + p.kb_per_split);
   };
-  // the units that form the bias gradient: row tile i in column tile
-  // i mod tiles_n (spread over the CTAs rather than all in column tile 0)
+  // the units that form the bias gradient on the tensor cores (fp32 planes,
+  // softmax-CE forming): row tile i in column tile i mod tiles_n
   auto db_unit = [&](int m0, int n0) { return p.db_out != nullptr && n0 / WBN == (m0 / BM) % p.tiles_n; };
 
   if (warp == 0) {
@@ -1934,7 +1953,7 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
-        const bool sum_db = db_cc && db_unit(m0, n0);
+        const bool sum_db = db_cc && db_part(p.db_out, m0 / BM, n0 / WBN, p.tiles_n, p.db_share) >= 0;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % W_STAGES;
           const uint32_t ph = (uint32_t)(it / W_STAGES) & 1u;
@@ -2058,18 +2077,22 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
           if (lane == 0) mbar_arrive(formed_bar(s));
         }
         if (!ok) break;
-      } else if (db_cc && db_unit(m0, n0)) {
+      } else if (db_cc && db_part(p.db_out, m0 / BM, n0 / WBN, p.tiles_n, p.db_share) >= 0) {
+        // this warp's rows if they are in the unit's part; every warp waits
+        // for each stage and arrives on its dbdone barrier
+        const bool mine = db_warp_in_part(warp - 2, db_part(p.db_out, m0 / BM, n0 / WBN, p.tiles_n, p.db_share),
+                                          p.tiles_n, p.db_share);
         float a0 = 0.f, a1 = 0.f;
         for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
           const int s = it % W_STAGES;
           ok = __all_sync(0xffffffffu, mbar_wait(full_bar(s), (uint32_t)(it / W_STAGES) & 1u, p.err));
           if (!ok) break;
-          db_stage_add(base_ptr + (a_base - base) + s * C::A_BYTES, warp - 2, lane, a0, a1);
+          if (mine) db_stage_add(base_ptr + (a_base - base) + s * C::A_BYTES, warp - 2, lane, a0, a1);
           __syncwarp();
           if (lane == 0) mbar_arrive(dbdone_bar(s));
         }
         if (!ok) break;
-        db_finish_store(a0, a1, warp - 2, lane, m0, p.M, split, p.db_out);
+        if (mine) db_finish_store(a0, a1, warp - 2, lane, m0, p.M, split, p.db_out);
       } else {
         it += kb1 - kb0;
       }
@@ -2134,16 +2157,13 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
 // and 128 columns of X per stage, 32 KB, both MN-major), split over K like
 // the one-SM kernel.  The bias gradient is summed on the CUDA cores by each
 // CTA's epilogue warps from its own landed A stages (db_stage_add, the same
-// order as the one-SM kernel), in the units that db_unit() picks (one per
-// row tile, spread over the column tiles so that every pair carries its
-// share).  The "full" barriers live in CTA 0, so the summing warps take a
+// order as the one-SM kernel), in the units db_part picks.  The "full" barriers live in CTA 0, so the summing warps take a
 // stage once the MMAs are done with it (the local "empty" barrier), and the
 // producer refills it only after they arrive on its dbdone barrier.  (A
 // landed-stage signal passed on from CTA 0 measured no faster: the second
 // read of the A stage from shared memory, not the wait, is what the bias
-// gradient costs, about a third of a unit; hence the spread.)  One
-// accumulator buffer:
-// the next unit's MMAs wait until both CTAs' epilogues have read it into
+// gradient costs, about a third of a unit; hence db_part.)  One
+// accumulator buffer: the next unit's MMAs wait until both CTAs' epilogues have read it into
 // registers (units are long; that read is a small part of them).
 // ---------------------------------------------------------------------------
 struct W2Cfg {
@@ -2209,9 +2229,9 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
     kb0 = split * p.kb_per_split;
     kb1 = min(p.num_kb, kb0 + p.kb_per_split);
   };
-  // the units that sum the bias gradient: row tile i in column tile i mod tiles_n
-  auto db_unit = [&](int m0, int n0) {
-    return p.db_out != nullptr && n0 / C::TBN == (m0 / C::TBM) % p.tiles_n;
+  // this unit's part of its row tile's bias-gradient sums (db_part), or -1
+  auto unit_part = [&](int m0, int n0) {
+    return db_part(p.db_out, m0 / C::TBM, n0 / C::TBN, p.tiles_n, p.db_share);
   };
 
   if (warp == 0) {
@@ -2228,7 +2248,7 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
       for (int u = u0; u < p.num_units && ok; u += ustep) {
         int m0, n0, split, kb0, kb1;
         unit_coords(u, m0, n0, split, kb0, kb1);
-        const bool sum_db = db_unit(m0, n0);
+        const bool sum_db = unit_part(m0, n0) >= 0;
         const int ma = m0 + (int)rank * BM, nb = n0 + (int)rank * (C::TBN / 2);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES;
@@ -2294,20 +2314,23 @@ tc_wgrad_cg2_kernel(const __grid_constant__ WParams p) {
       int m0, n0, split, kb0, kb1;
       unit_coords(u, m0, n0, split, kb0, kb1);
       const int mr = m0 + (int)rank * BM;   // this CTA's rows
-      if (db_unit(m0, n0)) {
-        // the bias gradient of this CTA's rows, stage by stage as the MMAs
-        // finish with them (the stage's bytes have landed by then)
+      const int part = unit_part(m0, n0);
+      if (part >= 0) {
+        // this unit's part of the bias gradient of this CTA's rows, stage by
+        // stage as the MMAs finish with them (the stage's bytes have landed
+        // by then); every warp waits and arrives, the part's warps sum
+        const bool mine = db_warp_in_part(warp - 2, part, p.tiles_n, p.db_share);
         float a0 = 0.f, a1 = 0.f;
         for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
           const int s = it % C::STAGES;
           ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(s), (uint32_t)(it / C::STAGES) & 1u, p.err));
           if (!ok) break;
-          db_stage_add(base_ptr + (a_base - base) + s * C::A_BYTES, warp - 2, lane, a0, a1);
+          if (mine) db_stage_add(base_ptr + (a_base - base) + s * C::A_BYTES, warp - 2, lane, a0, a1);
           __syncwarp();
           if (lane == 0) mbar_arrive(dbdone_bar(s));
         }
         if (!ok) break;
-        db_finish_store(a0, a1, warp - 2, lane, mr, p.M, split, p.db_out);
+        if (mine) db_finish_store(a0, a1, warp - 2, lane, mr, p.M, split, p.db_out);
       } else {
         it += kb1 - kb0;
       }
@@ -2687,6 +2710,7 @@ int tc_wgrad_cg2_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errle
     p.db_out = op.db;
   }
   const int clusters = std::min(p.num_units, cg2_max_clusters());
+  p.db_share = p.num_units <= clusters ? 1 : 0;   // one wave
   LaunchRec& r = recs[0];
   r.func = tcw2_kernel_ptr();
   r.smem = G::SMEM_BYTES;
@@ -2752,6 +2776,7 @@ int tc_wgrad_plan(const GemmOp& op, LaunchRec* recs, char* err, size_t errlen) {
   r.smem = x3 ? tc::WCfg<true>::SMEM_BYTES
               : wbn == 256 ? tc::WCfg<false, 256>::SMEM_BYTES : tc::WCfg<false, 128>::SMEM_BYTES;
   const int sms = device_sms();
+  p.db_share = p.num_units <= sms ? 1 : 0;   // one wave
   r.grid = dim3((unsigned)(p.num_units < sms ? p.num_units : sms));
   r.block = dim3(tc::P_THREADS);
   r.early = true;
