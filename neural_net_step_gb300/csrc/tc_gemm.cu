@@ -1144,7 +1144,7 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(0), 0u, p.err));
       tc_fence_after();
     }
-    // one verdict for the whole CTA: the finishing warps below meet at named
+    // one decision for the whole CTA: the finishing warps below meet at named
     // barriers, so either all of them run or none
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
     cluster_sync_all();   // both CTAs' MMAs are done: their pipeline memory is free
