@@ -606,6 +606,28 @@ __device__ __forceinline__ void act_chunk(float (&v)[64], int act) {
     for (int j = 0; j < 64; ++j) v[j] = gelu_tanh(v[j]);
   }
 }
+// The ReLU mask of a 64-column chunk as two 32-bit words: bit j set where
+// the bf16 rounding of v[j] is positive.  v is the ReLU output (>= 0, or
+// -0), and bf16's smallest positive value is 2^-133, so the rounding is
+// positive exactly when v > 2^-134 (2^-134 itself ties to the even zero):
+// one compare per element where the chunk lies inside N; columns at or
+// beyond N get no bit.
+__device__ __forceinline__ void relu_mask_bits(const float (&v)[64], int gn0, int N, uint32_t& b0, uint32_t& b1) {
+  constexpr float kMinPos = 0x1p-134f;
+  if (gn0 + 64 <= N) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      b0 |= (v[j] > kMinPos ? 1u : 0u) << j;
+      b1 |= (v[32 + j] > kMinPos ? 1u : 0u) << j;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      b0 |= (gn0 + j < N && v[j] > kMinPos ? 1u : 0u) << j;
+      b1 |= (gn0 + 32 + j < N && v[32 + j] > kMinPos ? 1u : 0u) << j;
+    }
+  }
+}
 // One output plane of a warp's 32 rows x 64 columns into 128B-swizzled
 // shared memory (16-byte unit u of row r at r*128 + ((u ^ (r & 7)) * 16)):
 // the bf16 rounding of v; with `rest`, v then keeps the remainder v - plane,
@@ -981,11 +1003,7 @@ __device__ __forceinline__ void persistent_body(const PParams& p) {
           if (!X3 && !PAIR && p.relu_bits && row_ok && gn0 < p.N) {
             // bit j: the stored (bf16) activation is positive
             uint32_t b0 = 0u, b1 = 0u;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              b0 |= (gn0 + j < p.N && __bfloat162float(__float2bfloat16_rn(v[j])) > 0.f ? 1u : 0u) << j;
-              b1 |= (gn0 + 32 + j < p.N && __bfloat162float(__float2bfloat16_rn(v[32 + j])) > 0.f ? 1u : 0u) << j;
-            }
+            relu_mask_bits(v, gn0, p.N, b0, b1);
             // a warp's 32 rows are 32 consecutive words: one coalesced store
             *reinterpret_cast<uint2*>(p.relu_bits + (int64_t)(gn0 / 64) * p.ld_bits + gm) = make_uint2(b0, b1);
           }
@@ -1687,11 +1705,7 @@ tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
           if (p.relu_bits && row_ok && gn0 < p.N) {
             // bit j: the stored (bf16) activation is positive
             uint32_t b0 = 0u, b1 = 0u;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              b0 |= (gn0 + j < p.N && __bfloat162float(__float2bfloat16_rn(v[j])) > 0.f ? 1u : 0u) << j;
-              b1 |= (gn0 + 32 + j < p.N && __bfloat162float(__float2bfloat16_rn(v[32 + j])) > 0.f ? 1u : 0u) << j;
-            }
+            relu_mask_bits(v, gn0, p.N, b0, b1);
             *reinterpret_cast<uint2*>(p.relu_bits + (int64_t)(gn0 / 64) * p.ld_bits + gm) = make_uint2(b0, b1);
           }
         } else if (p.act == ACT_RELU) {   // dgrad: dX * 1[h > 0]
