@@ -206,9 +206,10 @@ mlp_status mlp_set_graph_mode(mlp_t* model, int enable);
  *     weight-gradient GEMMs with at least 256 rows and columns on CTA pairs
  *     that share 256 x 256 output tiles through 2-SM tensor-core MMAs (each
  *     SM loads half of A's and half of B's tile; a third fewer operand bytes
- *     per FLOP than one SM on a 128 x 256 tile).  -1: where the pair tiles
- *     fill the device at least once and the reduction has at least 16 K
- *     stages of 64; 1: wherever the shape allows; 0: never.  The same MMA
+ *     per FLOP than one SM on a 128 x 256 tile).  -1: forward and dgrad
+ *     where the pair tiles fill the device at least once and K is at least
+ *     16 stages of 64 rows, weight gradients where each K split is at least
+ *     16 stages; 1: wherever the shape allows; 0: never.  The same MMA
  *     arithmetic and the same bias-gradient sums either way (results are
  *     bit for bit those of the one-SM kernels). */
 enum { MLP_OPT_GRAPH = 0, MLP_OPT_FUSE_HEAD = 1, MLP_OPT_F32_TENSOR_CORES = 2, MLP_OPT_PDL = 3, MLP_OPT_CE_GEMM = 4,
