@@ -308,6 +308,39 @@ def test_ragged_pair_tiles_layer_by_layer():
     assert rep["backward"] == "ok"
 
 
+# Ragged nets (widths that are multiples of 8, as the bf16 row pitches need)
+# whose bf16 weight gradients run in one wave with 16, 5, 3 and 2 column
+# tiles of 256, so that the bias-gradient sums of a row tile are
+# shared among its column tiles in every arrangement the kernels use (parts
+# over eight epilogue warps: 8 of 16 tiles, 5, 3, 2), on CTA pairs and on one
+# SM.  Both kernels give the same sums, so only a check against the oracle
+# shows that every row of db is summed once.
+BIAS_PARTS = [
+    synth.Workload("bias_parts_16_2", (4000, 512, 1096, 100), (om.ACT_GELU_TANH, om.ACT_RELU), synth.BF16, 1000, 2,
+                   1e-3, 0.9, 0.999, 1e-8, 0.01, "normal", 21),
+    synth.Workload("bias_parts_5_3", (1096, 704, 2200, 100), (om.ACT_RELU, om.ACT_GELU_TANH), synth.BF16, 1200, 2,
+                   1e-3, 0.9, 0.999, 1e-8, 0.01, "normal", 22),
+]
+
+
+@pytest.mark.parametrize("two_sm", [1, 0])
+@pytest.mark.parametrize("w", BIAS_PARTS, ids=[w.name for w in BIAS_PARTS])
+def test_bias_gradient_parts_layer_by_layer(w, two_sm):
+    m = make_model(w, synth.make_params(w))
+    m.set_option(nn.OPT_GEMM_2SM, two_sm)
+    x, y = synth.make_batch(w, 0)
+    xd, yd = x.to(DEV), y.to(DEV)
+    names = [n for n, _ in nn.mlp_profile_step(m.h, xd.data_ptr(), yd.data_ptr(), w.lr, w.beta1, w.beta2, w.eps,
+                                                 w.wd, None, m.stream())]
+    assert (names.count("tc2_gemm_wgrad") == 2) == (two_sm == 1), names
+    m.close()
+    m = make_model(w, synth.make_params(w))
+    m.set_option(nn.OPT_GEMM_2SM, two_sm)
+    rep, _, _, _ = traced_step_check(w, m, 0)
+    m.close()
+    assert rep["backward"] == "ok"
+
+
 def test_trace_entries_describe_the_step():
     """The trace lists each stored tensor once, written by the launch that the
     profiling pass names for it."""
