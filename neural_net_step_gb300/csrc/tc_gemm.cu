@@ -1761,13 +1761,14 @@ tc_gemm_cg2_kernel(const __grid_constant__ PParams p) {
 
 // ---------------------------------------------------------------------------
 // Persistent split-K weight gradient: dW[m, n] = sum_k A(m, k) B(k, n), with
-// A = dY^T and B = X both MN-major in memory, fp32 out.  The bias gradient
+// A = dY^T and B = X both MN-major in memory, fp32 out. The bias gradient
 // db[m] = sum_k A(m, k): for bf16 by the epilogue warps on the CUDA cores
 // from the landed A stages (db_stage_add: they are idle while a long unit's
 // MMAs run, and a second narrow MMA per K step would lengthen those units by
-// about a third), in the units db_part picks; for fp32 planes and the softmax-CE forming by a second MMA of
-// the same A tile against a constant 16 x 64 tile of ones (N = 16) into
-// spare TMEM columns, in one unit per row tile.
+// about a third), in the units db_part picks; for fp32 planes and the
+// softmax-CE forming by a second MMA of the same A tile against a constant
+// 16 x 64 tile of ones (N = 16) into spare TMEM columns, in one unit per row
+// tile.
 //
 // Work units are (tile, K split) pairs, tile index fastest, so CTAs running
 // at the same time share K ranges in L2.  Each unit's fp32 result goes out
@@ -2169,16 +2170,17 @@ __global__ void __launch_bounds__(P_THREADS, 1) tc_wgrad_persistent_kernel(const
 // 2-SM variant of the bf16 weight gradient: dW = dY^T X on CTA pairs with
 // tcgen05.mma.cta_group::2, 256 x 256 tiles (each CTA holds 128 rows of dY^T
 // and 128 columns of X per stage, 32 KB, both MN-major), split over K like
-// the one-SM kernel.  The bias gradient is summed on the CUDA cores by each
+// the one-SM kernel. The bias gradient is summed on the CUDA cores by each
 // CTA's epilogue warps from its own landed A stages (db_stage_add, the same
-// order as the one-SM kernel), in the units db_part picks.  The "full" barriers live in CTA 0, so the summing warps take a
-// stage once the MMAs are done with it (the local "empty" barrier), and the
-// producer refills it only after they arrive on its dbdone barrier.  (A
-// landed-stage signal passed on from CTA 0 measured no faster: the second
-// read of the A stage from shared memory, not the wait, is what the bias
-// gradient costs, about a third of a unit; hence db_part.)  One
-// accumulator buffer: the next unit's MMAs wait until both CTAs' epilogues have read it into
-// registers (units are long; that read is a small part of them).
+// order as the one-SM kernel), in the units db_part picks. The "full"
+// barriers live in CTA 0, so the summing warps take a stage once the MMAs
+// are done with it (the local "empty" barrier), and the producer refills it
+// only after they arrive on its dbdone barrier. (A landed-stage signal
+// passed on from CTA 0 measured no faster: the second read of the A stage
+// from shared memory, not the wait, is what the bias gradient costs, about a
+// third of a unit; hence db_part.) One accumulator buffer: the next unit's
+// MMAs wait until both CTAs' epilogues have read it into registers (units
+// are long; that read is a small part of them).
 // ---------------------------------------------------------------------------
 struct W2Cfg {
   static constexpr int TBM = 2 * BM, TBN = 256;                 // the pair's output tile
