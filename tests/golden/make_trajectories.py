@@ -48,7 +48,9 @@ from tests import parity as P  # noqa: E402
 
 WORKLOADS = ["mnist_mlp_b4096", "cifar_mlp_b8192", "deep_narrow_b65536", "lm_block_t16384"]
 SAMPLES = 4096
-ENSEMBLE = 3
+# perturbed oracle runs per workload (MLP_TRAJ_ENSEMBLE overrides; the test
+# takes the spread over however many the file holds)
+ENSEMBLE = int(os.environ.get("MLP_TRAJ_ENSEMBLE", "3"))
 
 
 def source_hash() -> str:
