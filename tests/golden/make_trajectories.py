@@ -27,8 +27,10 @@ mirror-rounding mode for the others):
 The GPU tests compare the library's trajectory with these values; nothing
 here comes from the CUDA path.
 
-Run:  python tests/golden/make_trajectories.py [workload ...]   (about two
-hours on 8 cores for all four; the LM block needs ~30 GB of host memory)
+Run:  python tests/golden/make_trajectories.py [--jobs N] [workload ...]
+(one after another: hours for the deep narrow net and the LM block on 8
+cores, and the LM block holds about 40 GB; --jobs runs the reference, exact
+and perturbed runs as N processes at a time where memory allows)
 """
 import hashlib
 import inspect
@@ -75,24 +77,31 @@ def scale_of(w, ref, p0, U):
     return np.full(ref.shape, max(U, 1e-30))
 
 
-def run(name: str) -> str:
+def _piece(name: str, kind: str, j: int = 0):
+    """One oracle run of workload `name`: kind "ref" (the reference mode),
+    "exact" (bf16 workloads: the exact-rounding mode) or "ens" (perturbed
+    run j + 1).  Returns (losses, final parameters or None)."""
     w = synth.WORKLOADS[name]
-    t0 = time.time()
     params0 = synth.make_params(w)
     bl = P.batches(w, w.steps)
     mode = P.oracle_mode(w)
-    ref = P.oracle_run(w, params0, bl, mode)
-    print(f"{name}: reference run {time.time() - t0:.0f} s", flush=True)
-    out = {"workload": name, "steps": w.steps, "mode": mode, "source_hash": source_hash(),
-           "losses_ref": np.array(ref[0])}
-    if w.dtype != synth.F32:
-        ex = P.oracle_run(w, params0, bl, "bf16")
-        out["losses_exact"] = np.array(ex[0])
-        del ex
-        print(f"{name}: exact-mode run {time.time() - t0:.0f} s", flush=True)
-    p0 = [P.to64(p) for p in params0]
-    pref = [np.asarray(a, np.float64) for a in ref[1]]
-    del ref
+    if kind == "exact":
+        e = P.oracle_run(w, params0, bl, "bf16")
+        return np.array(e[0]), None
+    r = P.oracle_run(w, params0, bl, mode, perturb_seed=(j + 1) if kind == "ens" else 0)
+    return np.array(r[0]), [np.asarray(a, np.float64) for a in r[1]]
+
+
+def _assemble(name: str, ref, exact, ens, t0: float) -> str:
+    """The stored file from the pieces: ref = (losses, params), exact =
+    losses or None, ens = [(losses, params)] in member order."""
+    w = synth.WORKLOADS[name]
+    out = {"workload": name, "steps": w.steps, "mode": P.oracle_mode(w), "source_hash": source_hash(),
+           "losses_ref": ref[0]}
+    if exact is not None:
+        out["losses_exact"] = exact
+    p0 = [P.to64(p) for p in synth.make_params(w)]
+    pref = ref[1]
     n_t = len(pref)
     U = np.array([float(np.max(np.abs(r - q))) for r, q in zip(pref, p0)])
     out["U"] = U
@@ -104,24 +113,19 @@ def run(name: str) -> str:
         idx.append(ii)
         out[f"idx_{i}"] = ii.astype(np.int64)
         out[f"ref_{i}"] = r.ravel()[ii]
-    ens_l, ens_s = [], [[] for _ in range(n_t)]
-    rms = np.zeros((ENSEMBLE, n_t))
-    frac = np.zeros((ENSEMBLE, n_t))
-    mx = np.zeros((ENSEMBLE, n_t))
-    for j in range(ENSEMBLE):
-        e = P.oracle_run(w, params0, bl, mode, perturb_seed=j + 1)
-        ens_l.append(np.array(e[0]))
+    m = len(ens)
+    rms, frac, mx = np.zeros((m, n_t)), np.zeros((m, n_t)), np.zeros((m, n_t))
+    ens_s = [[] for _ in range(n_t)]
+    for jj, (_, pe_all) in enumerate(ens):
         for i in range(n_t):
-            pe = np.asarray(e[1][i], np.float64)
+            pe = pe_all[i]
             sc = scale_of(w, pref[i], p0[i], U[i])
             d = np.abs(pe - pref[i]) / sc
-            rms[j, i] = float(np.sqrt(np.mean(d ** 2)))
-            frac[j, i] = float(np.mean(d > stated(w)))
-            mx[j, i] = float(d.max())
+            rms[jj, i] = float(np.sqrt(np.mean(d ** 2)))
+            frac[jj, i] = float(np.mean(d > stated(w)))
+            mx[jj, i] = float(d.max())
             ens_s[i].append(pe.ravel()[idx[i]])
-        del e
-        print(f"{name}: ensemble member {j} {time.time() - t0:.0f} s", flush=True)
-    out["losses_ens"] = np.stack(ens_l)
+    out["losses_ens"] = np.stack([e[0] for e in ens])
     for i in range(n_t):
         out[f"ens_{i}"] = np.stack(ens_s[i])
     out["ens_rms"], out["ens_frac"], out["ens_max"] = rms, frac, mx
@@ -131,6 +135,90 @@ def run(name: str) -> str:
     return path
 
 
+def run(name: str) -> str:
+    """The oracle runs one after another in this process."""
+    w = synth.WORKLOADS[name]
+    t0 = time.time()
+    ref = _piece(name, "ref")
+    print(f"{name}: reference run {time.time() - t0:.0f} s", flush=True)
+    exact = None
+    if w.dtype != synth.F32:
+        exact = _piece(name, "exact")[0]
+        print(f"{name}: exact-mode run {time.time() - t0:.0f} s", flush=True)
+    ens = []
+    for j in range(ENSEMBLE):
+        ens.append(_piece(name, "ens", j))
+        print(f"{name}: ensemble member {j} {time.time() - t0:.0f} s", flush=True)
+    return _assemble(name, ref, exact, ens, t0)
+
+
+def _mem_available() -> float:
+    """Bytes of host memory available (Linux)."""
+    with open("/proc/meminfo") as f:
+        for line in f:
+            if line.startswith("MemAvailable:"):
+                return float(line.split()[1]) * 1024.0
+    return 0.0
+
+
+def _piece_to_file(name, kind, j, path):
+    losses, params = _piece(name, kind, j)
+    arrs = {"losses": losses}
+    if params is not None:
+        for i, a in enumerate(params):
+            arrs[f"p_{i}"] = a
+    np.savez(path, **arrs)
+
+
+def run_parallel(name: str, jobs: int, min_free_gb: float) -> str:
+    """The same oracle runs as separate processes, at most `jobs` at a time
+    and a new one only while more than `min_free_gb` of host memory is
+    free (each full-batch run of the LM block holds about 40 GB)."""
+    import multiprocessing as mp
+    import tempfile
+    w = synth.WORKLOADS[name]
+    t0 = time.time()
+    kinds = [("ref", 0)] + ([("exact", 0)] if w.dtype != synth.F32 else []) + [("ens", j) for j in range(ENSEMBLE)]
+    ctx = mp.get_context("spawn")
+    tmp = tempfile.mkdtemp(prefix="traj_")
+    files = {k: os.path.join(tmp, f"{k[0]}_{k[1]}.npz") for k in kinds}
+    todo, running = list(kinds), {}
+    while todo or running:
+        for k, pr in list(running.items()):
+            if not pr.is_alive():
+                pr.join()
+                if pr.exitcode != 0:
+                    raise RuntimeError(f"{name}: oracle run {k} failed ({pr.exitcode})")
+                print(f"{name}: {k[0]} {k[1]} done at {time.time() - t0:.0f} s", flush=True)
+                del running[k]
+        if todo and len(running) < jobs and (not running or _mem_available() > min_free_gb * 2 ** 30):
+            k = todo.pop(0)
+            pr = ctx.Process(target=_piece_to_file, args=(name, k[0], k[1], files[k]))
+            pr.start()
+            running[k] = pr
+            time.sleep(60)   # let its memory grow before the next check
+        else:
+            time.sleep(5)
+
+    def load(k):
+        d = np.load(files[k])
+        n = len([f for f in d.files if f.startswith("p_")])
+        return d["losses"], ([d[f"p_{i}"] for i in range(n)] if n else None)
+    ref = load(("ref", 0))
+    exact = load(("exact", 0))[0] if ("exact", 0) in files else None
+    ens = [load(("ens", j)) for j in range(ENSEMBLE)]
+    return _assemble(name, ref, exact, ens, t0)
+
+
 if __name__ == "__main__":
-    for name in (sys.argv[1:] or WORKLOADS):
-        run(name)
+    import argparse
+    ap = argparse.ArgumentParser()
+    ap.add_argument("workloads", nargs="*", default=WORKLOADS)
+    ap.add_argument("--jobs", type=int, default=1, help="oracle runs at a time, each in its own process")
+    ap.add_argument("--min-free-gb", type=float, default=60.0)
+    a = ap.parse_args()
+    for name in a.workloads:
+        if a.jobs > 1:
+            run_parallel(name, a.jobs, a.min_free_gb)
+        else:
+            run(name)
