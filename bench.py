@@ -319,7 +319,25 @@ class OracleRunner:
 
     def sample(self) -> str:
         return (f"oracle steps (numpy fp64, {self.mode} mode) on {self.rows} of {self.w.batch} rows of the "
-                f"{self.w.name} workload; OpenBLAS threads = host cores")
+                f"{self.w.name} workload; {blas_threads()} BLAS threads on {os.cpu_count()} host cores")
+
+
+def blas_threads() -> int:
+    """Threads the oracle's BLAS actually uses: threadpoolctl where installed,
+    else the thread-count variables OpenBLAS reads (torchrun sets
+    OMP_NUM_THREADS=1 for its ranks), else every host core."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit() and int(v) > 0:
+            return int(v)
+    return os.cpu_count() or 1
 
 
 def time_oracle(w, target_s=10.0, optim="adamw", max_norm=0.0, loss="ce"):
@@ -328,7 +346,7 @@ def time_oracle(w, target_s=10.0, optim="adamw", max_norm=0.0, loss="ce"):
     while el < target_s:
         el += r.step()
         steps += 1
-    return {"value": r.rows * steps / el, "unit": "samples/s", "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": r.rows * steps / el, "unit": "samples/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"{steps} " + r.sample()}
 
 
@@ -354,7 +372,7 @@ def run_reference(args, w, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * t_all / args.steps, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(w, None, args),
-            "cpu_baseline": {"value": round(value, 2), "unit": "samples/s", "cores": os.cpu_count(),
+            "cpu_baseline": {"value": round(value, 2), "unit": "samples/s", "cores": blas_threads(),
                              "kind": "oracle", "sample": f"each step: one of {args.steps} " + r.sample()},
             "e2e": {"value": round(value, 2), "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
